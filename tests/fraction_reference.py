@@ -1,0 +1,86 @@
+"""Exact-rational brute force for tiny inputs: an independent third check of
+the C oracle.  Written separately from it (bit-level field extraction over the
+whole 96-bit scale word, Python integers and fractions.Fraction throughout) so
+that a slip in either implementation shows up as a disagreement.
+
+Follows SKaiNET PR #562 "SIMD-fused Q4_K matmul kernel + Q4KMatmulKernel SPI",
+section "Pipeline", and SKaiNET issue #1138 "[ternary-f32] Phase 2 …",
+section "Tasks".
+"""
+from fractions import Fraction
+
+
+def fp16(bits: int) -> Fraction:
+    sign = -1 if bits >> 15 else 1
+    e = (bits >> 10) & 31
+    mant = bits & 1023
+    assert e != 31, "Inf/NaN are outside the generator's range"
+    if e == 0:
+        return sign * Fraction(mant, 1 << 24)
+    return sign * Fraction(1024 + mant, 1 << 10) * Fraction(2) ** (e - 15)
+
+
+def _bits(word: int, lo: int, n: int) -> int:
+    return (word >> lo) & ((1 << n) - 1)
+
+
+def scales_mins(packed: bytes):
+    """Eight (sc, m) pairs from the 12 packed bytes, read as one 96-bit
+    little-endian word.  Byte i occupies bits 8i..8i+7."""
+    word = int.from_bytes(bytes(packed), "little")
+    out = []
+    for s in range(8):
+        if s < 4:
+            sc = _bits(word, 8 * s, 6)
+            m = _bits(word, 8 * (s + 4), 6)
+        else:
+            sc = _bits(word, 8 * (s + 4), 4) + (_bits(word, 8 * (s - 4) + 6, 2) << 4)
+            m = _bits(word, 8 * (s + 4) + 4, 4) + (_bits(word, 8 * s + 6, 2) << 4)
+        out.append((sc, m))
+    return out
+
+
+def block_values(blk: bytes):
+    """The 256 exact values of one block."""
+    blk = bytes(blk)
+    d = fp16(blk[0] | blk[1] << 8)
+    dmin = fp16(blk[2] | blk[3] << 8)
+    sm = scales_mins(blk[4:16])
+    qs = blk[16:144]
+    vals = [None] * 256
+    for j in range(4):
+        for l in range(32):
+            byte = qs[32 * j + l]
+            for e, q in ((64 * j + l, byte % 16), (64 * j + 32 + l, byte // 16)):
+                sc, m = sm[e // 32]
+                vals[e] = d * sc * q - dmin * m
+    return vals
+
+
+def q4k_matmul(x_rows, W_rows, K: int):
+    """y[t][o] exactly, with each weight rounded once to fp32 first (the
+    oracle's dequantize-to-FP32 step).  x_rows: list of lists of floats,
+    W_rows: list of byte strings."""
+    import numpy as np
+    nb = K // 256
+    y = []
+    for xt in x_rows:
+        row_out = []
+        for wrow in W_rows:
+            acc = Fraction(0)
+            for b in range(nb):
+                vals = block_values(wrow[144 * b:144 * (b + 1)])
+                for e, v in enumerate(vals):
+                    w32 = Fraction(float(np.float32(float(v))))  # v is exact in double
+                    acc += Fraction(float(xt[256 * b + e])) * w32
+            row_out.append(acc)
+        y.append(row_out)
+    return y
+
+
+def ternary_codes(row: bytes, K: int):
+    codes = []
+    for i in range(K):
+        field = (row[i // 4] >> (2 * (i % 4))) & 3
+        codes.append(field - 1)
+    return codes

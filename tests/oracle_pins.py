@@ -1,0 +1,251 @@
+"""Pins for the CPU oracle: checks against facts other than the oracle itself.
+
+Each pin takes a loaded oracle library (so the planted-mistake tests can run
+the same pins against a deliberately broken copy) and raises AssertionError
+when the oracle disagrees with the fact it pins.
+
+Sources of the facts:
+  * hand-worked fixtures in tests/golden/ (worked out by hand, cited there);
+  * IEEE 754 binary16 and bfloat16 definitions, checked against numpy / torch;
+  * closed forms and special cases of w = d·sc·q − dmin·m (SKaiNET PR #562,
+    section "Pipeline");
+  * the lazy-dmin identity of the same section, as an invariant between two
+    differently ordered computations;
+  * integer counts for the ternary code-dot (SKaiNET issue #1138, section
+    "Tests": exact equality on the code-dot for integer activations);
+  * an exact-rational brute force (tests/fraction_reference.py).
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+import synth
+import fraction_reference as fr
+from golden import fixtures
+
+
+def _hand_block(lib):
+    fx = fixtures.read("q4k_handworked_block.txt")
+    sc = fixtures.ints(fx["sc"])
+    m = fixtures.ints(fx["m"])
+    q = [(e // 32 + e % 32) % 16 for e in range(256)]
+    blk = oracle.q4k_pack_block(int(fx["d_bits"], 16), int(fx["dmin_bits"], 16), sc, m, q, lib=lib)
+    return fx, blk
+
+
+def pin_fp16_decode(lib):
+    # IEEE 754 binary16 closed forms.
+    cases = {0x3C00: 1.0, 0x3800: 0.5, 0x3400: 0.25, 0xC000: -2.0, 0x7BFF: 65504.0,
+             0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24, 0x0400: 2.0 ** -14, 0x0000: 0.0}
+    for bits, v in cases.items():
+        got = oracle.fp16_to_double(bits, lib=lib)
+        assert got == v, (hex(bits), got, v)
+    # Every finite pattern against numpy's binary16 conversion.
+    allbits = np.arange(65536, dtype=np.uint16)
+    ref = allbits.view("<f2").astype(np.float64)
+    finite = np.isfinite(ref)
+    got = np.array([oracle.fp16_to_double(int(b), lib=lib) for b in allbits[finite][::37]])
+    assert np.array_equal(got, ref[finite][::37])
+
+
+def pin_bf16_round(lib):
+    import torch
+    g = np.random.default_rng(7)
+    vals = np.concatenate([g.standard_normal(2000).astype(np.float32),
+                           (g.standard_normal(500) * 1e-30).astype(np.float32),
+                           np.array([1.0, 1.00390625, 1.005859375, 255.5, -3.0e38], np.float32)])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).to(torch.float32).numpy()
+    got = np.array([oracle.round_bf16(float(v), lib=lib) for v in vals], np.float32)
+    assert np.array_equal(got, ref)
+
+
+def pin_handworked_pack(lib):
+    fx, blk = _hand_block(lib)
+    assert list(blk[4:16]) == fixtures.hexbytes(fx["packed_scales"])
+    assert list(blk[16:20]) == fixtures.hexbytes(fx["qs_0_3"])
+    assert list(blk[48:52]) == fixtures.hexbytes(fx["qs_32_35"])
+
+
+def pin_handworked_values(lib):
+    fx, blk = _hand_block(lib)
+    w = oracle.q4k_dequant(blk, 256, 1, lib=lib)[0]
+    for e in (0, 31, 32, 255):
+        assert w[e] == float(fx[f"w_{e}"]), (e, w[e])
+    ones = np.ones((1, 256), np.float32)
+    assert oracle.q4k_matmul(ones, blk, 256, 1, lib=lib)[0, 0] == float(fx["sum_w"])
+    x = np.array([[(e % 7) - 3 for e in range(256)]], np.float32)
+    want = float(fx["y_x_mod7"])
+    assert oracle.q4k_matmul(x, blk, 256, 1, lib=lib)[0, 0] == want
+    assert oracle.q4k_matmul_lazy(x, blk, 256, 1, lib=lib)[0, 0] == want
+
+
+def pin_nibble_positions(lib):
+    # One nonzero qs byte at a time: byte 32j+l = 0xAB puts code 11 at element
+    # 64j+l (low nibble) and code 10 at element 64j+32+l (high nibble); with
+    # d = 1, every sc = 1 and dmin = 0 those are the only nonzero values.
+    sc = [1] * 8
+    m = [0] * 8
+    for j in range(4):
+        for l in (0, 7, 16, 31):
+            q = [0] * 256
+            q[64 * j + l] = 0xB
+            q[64 * j + 32 + l] = 0xA
+            blk = oracle.q4k_pack_block(0x3C00, 0x0000, sc, m, q, lib=lib)
+            assert blk[16 + 32 * j + l] == 0xAB
+            blk2 = np.zeros(144, np.uint8)
+            blk2[:16] = blk[:16]
+            blk2[16 + 32 * j + l] = 0xAB
+            w = oracle.q4k_dequant(blk2, 256, 1, lib=lib)[0]
+            want = np.zeros(256, np.float32)
+            want[64 * j + l] = 11
+            want[64 * j + 32 + l] = 10
+            assert np.array_equal(w, want), (j, l)
+
+
+def pin_scale_positions(lib):
+    # Distinct scales per sub-block, all codes 1, dmin = 0: each
+    # sub-block's 32 values equal its own scale.  Then mins alone (codes 0,
+    # d = 0, dmin = 1): each sub-block's values equal minus its own min.
+    sc = [1, 2, 4, 8, 16, 32, 3, 63]
+    m = [5, 7, 9, 11, 17, 33, 48, 63]
+    q = [1] * 256
+    blk = oracle.q4k_pack_block(0x3C00, 0x0000, sc, m, q, lib=lib)
+    w = oracle.q4k_dequant(blk, 256, 1, lib=lib)[0]
+    assert np.array_equal(w, np.repeat(np.array(sc, np.float32), 32))
+    blk = oracle.q4k_pack_block(0x0000, 0x3C00, sc, m, [0] * 256, lib=lib)
+    w = oracle.q4k_dequant(blk, 256, 1, lib=lib)[0]
+    assert np.array_equal(w, -np.repeat(np.array(m, np.float32), 32))
+
+
+def pin_special_cases(lib):
+    g = np.random.default_rng(3)
+    K, N, T = 512, 3, 2
+    x = g.standard_normal((T, K)).astype(np.float32)
+    # All codes 0 and all mins 0: y = 0.
+    W = synth.q4k_weights(g, N, K)
+    W3 = W.reshape(N, K // 256, 144).copy()
+    W3[:, :, 16:] = 0
+    W3[:, :, 4:16] = 0
+    assert np.all(oracle.q4k_matmul(x, W3, K, N, lib=lib) == 0.0)
+    # d = 0, dmin = 1, every m = 1: y = −Σx.
+    W3 = W.reshape(N, K // 256, 144).copy()
+    W3[:, :, 0:2] = [0x00, 0x00]
+    W3[:, :, 2:4] = [0x00, 0x3C]
+    W3[:, :, 4:16] = [0, 0, 0, 0, 1, 1, 1, 1, 0x10, 0x10, 0x10, 0x10]
+    y = oracle.q4k_matmul(x, W3, K, N, lib=lib)
+    want = -x.astype(np.float64).sum(axis=1)
+    assert np.allclose(y, want[:, None], rtol=0, atol=1e-9)
+
+
+def pin_one_hot_rows(lib):
+    # x = e_k picks out w[o][k]; rows of x go to rows of y (no transposition).
+    K, N = 512, 5
+    g = np.random.default_rng(11)
+    W = synth.q4k_weights(g, N, K)
+    w = oracle.q4k_dequant(W, K, N, lib=lib)
+    ks = [0, 1, 31, 32, 63, 64, 255, 256, 300, 511]
+    x = np.zeros((len(ks), K), np.float32)
+    for t, k in enumerate(ks):
+        x[t, k] = 1.0
+    y = oracle.q4k_matmul(x, W, K, N, lib=lib)
+    for t, k in enumerate(ks):
+        assert np.array_equal(y[t], w[:, k].astype(np.float64)), k
+
+
+def pin_lazy_equals_direct(lib):
+    x, W, K, N, T = synth.q4k_case((1024, 64, 3), seed=5)
+    yd = oracle.q4k_matmul(x, W, K, N, lib=lib)
+    yl = oracle.q4k_matmul_lazy(x, W, K, N, lib=lib)
+    # The direct form rounds each dequantized weight to fp32 once (relative
+    # error ≤ 2^-24); the lazy form keeps every value exact in double.  So the
+    # two may differ by at most 2^-24·Σ_k |x_k·w_k| plus double round-off.
+    w = oracle.q4k_dequant(W, K, N, lib=lib).astype(np.float64)
+    bound = 2.0 ** -24 * (np.abs(x.astype(np.float64)) @ np.abs(w).T) * (1 + 1e-6)
+    bound += 1e-12 * np.abs(yd).max()
+    assert np.all(np.abs(yd - yl) <= bound)
+
+
+def pin_fraction_bruteforce(lib):
+    for (K, N, T), seed in (((256, 2, 2), 1), ((512, 3, 1), 2), ((256, 4, 3), 4)):
+        x, W, K, N, T = synth.q4k_case((K, N, T), seed=seed)
+        y = oracle.q4k_matmul(x, W, K, N, lib=lib)
+        exact = fr.q4k_matmul(x.tolist(), [bytes(r) for r in W], K)
+        for t in range(T):
+            for o in range(N):
+                e = exact[t][o]
+                assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
+
+
+def pin_ternary_handworked(lib):
+    fx = fixtures.read("ternary_handworked.txt")
+    codes = fixtures.ints(fx["codes"])
+    packed = oracle.ternary_pack(codes, lib=lib)
+    assert list(packed) == fixtures.hexbytes(fx["bytes"])
+    x = np.array([fixtures.ints(fx["x"])], np.float32)
+    dot, y = oracle.ternary_gemv(x, packed, float(fx["scale"]), 8, 1, lib=lib)
+    assert dot[0, 0] == float(fx["dot"])
+    assert y[0, 0] == np.float32(fx["y"])
+
+
+def pin_ternary_integer_count(lib):
+    # On integer activations the code-dot is an integer: the sum of x over the
+    # +1 codes minus the sum over the −1 codes, counted in Python integers.
+    g = np.random.default_rng(9)
+    K, N, T = 2560, 7, 3
+    codes = g.integers(-1, 2, size=(N, K))
+    W = np.stack([oracle.ternary_pack(c, lib=lib) for c in codes])
+    x = g.integers(-8, 9, size=(T, K))
+    dot, _ = oracle.ternary_gemv(x.astype(np.float32), W, 1.0, K, N, lib=lib)
+    for t in range(T):
+        for o in range(N):
+            plus = int(x[t][codes[o] == 1].sum())
+            minus = int(x[t][codes[o] == -1].sum())
+            assert dot[t, o] == plus - minus, (t, o)
+    # All-ones activation: count of +1 codes minus count of −1 codes.
+    dot1, _ = oracle.ternary_gemv(np.ones((1, K), np.float32), W, 1.0, K, N, lib=lib)
+    assert np.array_equal(dot1[0], (codes == 1).sum(1) - (codes == -1).sum(1))
+    # Bytes read back through the brute-force decoder give the same codes.
+    for o in range(N):
+        assert fr.ternary_codes(bytes(W[o]), K) == codes[o].tolist()
+
+
+def pin_ternary_scale(lib):
+    # The scale multiplies the fp32 code-dot once, after the dot product.
+    x, W, scale, K, N, T = synth.ternary_case((256, 9, 2), seed=13, xkind="int")
+    dot, y = oracle.ternary_gemv(x, W, scale, K, N, lib=lib)
+    dot1, y1 = oracle.ternary_gemv(x, W, 1.0, K, N, lib=lib)
+    assert np.array_equal(dot, dot1)
+    assert np.array_equal(y1, dot.astype(np.float32))
+    assert np.array_equal(y, (dot.astype(np.float32).astype(np.float64) * np.float64(scale)).astype(np.float32))
+
+
+def pin_bf16_variant(lib):
+    # With bf16-exact operands (d = 1, dmin = 0, sc·q ≤ 225, small integer x)
+    # the bf16 variant equals the direct form; otherwise it equals the direct
+    # form applied to bf16-rounded operands (rounded by torch here).
+    import torch
+    K, N = 256, 4
+    g = np.random.default_rng(17)
+    W = np.stack([oracle.q4k_pack_block(0x3C00, 0, g.integers(0, 16, 8), [0] * 8,
+                                        g.integers(0, 16, 256), lib=lib) for _ in range(N)])
+    x = g.integers(-4, 5, size=(2, K)).astype(np.float32)
+    assert np.array_equal(oracle.q4k_matmul_bf16(x, W, K, N, lib=lib),
+                          oracle.q4k_matmul(x, W, K, N, lib=lib))
+    x, W, K, N, T = synth.q4k_case((512, 6, 2), seed=19)
+    w = oracle.q4k_dequant(W, K, N, lib=lib)
+    wb = torch.from_numpy(w).to(torch.bfloat16).double().numpy()
+    xb = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    want = xb @ wb.T
+    got = oracle.q4k_matmul_bf16(x, W, K, N, lib=lib)
+    assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max()
+
+
+ALL_PINS = [
+    pin_fp16_decode, pin_bf16_round, pin_handworked_pack, pin_handworked_values,
+    pin_nibble_positions, pin_scale_positions, pin_special_cases, pin_one_hot_rows,
+    pin_lazy_equals_direct, pin_fraction_bruteforce, pin_ternary_handworked,
+    pin_ternary_integer_count, pin_ternary_scale, pin_bf16_variant,
+]

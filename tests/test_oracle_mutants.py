@@ -1,0 +1,57 @@
+"""Planted mistakes: each test copies the oracle's C source, plants one
+plausible mistake (a swapped nibble, a wrong sign, a wrong index, a transposed
+operand, a dropped term, a wrong rounding), builds the copy on the CPU and
+checks that at least one pin rejects it.  This shows the pins are strong
+enough to catch such mistakes in the real oracle."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "low_nibble_from_high": ("return qs[32 * j + l] & 15;", "return qs[32 * j + l] >> 4;"),
+    "halves_swapped": ("int j = e / 64, l = e % 64;", "int j = e / 64, l = (e + 32) % 64;"),
+    "dmin_sign": ("w[e] = (float)(d * sc * q4k_code(qs, e) - dmin * m);",
+                  "w[e] = (float)(d * sc * q4k_code(qs, e) + dmin * m);"),
+    "sub_block_index": ("q4k_scale_min(packed, e / 32, &sc, &m);",
+                        "q4k_scale_min(packed, (e / 32) ^ 1, &sc, &m);"),
+    "scale_high_bits_byte": ("*sc = (packed[s + 4] & 15) | ((packed[s - 4] >> 6) << 4);",
+                             "*sc = (packed[s + 4] & 15) | ((packed[s] >> 6) << 4);"),
+    "min_low_bits_nibble": ("*m = (packed[s + 4] >> 4) |", "*m = (packed[s + 4] & 15) |"),
+    "d_dmin_swapped": ("double d = q4k_d(blk), dmin = q4k_dmin(blk);",
+                       "double dmin = q4k_d(blk), d = q4k_dmin(blk);"),
+    "fp16_bias": ("exponent - 25", "exponent - 24"),
+    "fp16_subnormal": ("ldexp((double)mantissa, -24)", "ldexp((double)mantissa, -25)"),
+    "output_transposed": ("y[t * N + o] = acc;", "y[o * T + t] = acc;"),
+    "activation_row": ("const float *xt = x + t * K;\n                double acc",
+                       "const float *xt = x + t;\n                double acc"),
+    "dropped_last_term": ("for (int64_t k = 0; k < K; ++k) {\n                    float xv",
+                          "for (int64_t k = 0; k < K - 1; ++k) {\n                    float xv"),
+    "lazy_offset_dropped": ("acc += (d * sc) * code_sum - (dmin * m) * input_sum;",
+                            "acc += (d * sc) * code_sum;"),
+    "ternary_field_order": ("return ((row[i / 4] >> (2 * (i % 4))) & 3) - 1;",
+                            "return ((row[i / 4] >> (2 * (3 - i % 4))) & 3) - 1;"),
+    "ternary_offset": ("return ((row[i / 4] >> (2 * (i % 4))) & 3) - 1;",
+                       "return ((row[i / 4] >> (2 * (i % 4))) & 3);"),
+    "bf16_truncates": ("u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;", "u = u & 0xFFFF0000u;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert old in src, f"mutation target for {name} no longer in the oracle source"
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(src.replace(old, new, 1))
+    lib_path = oracle.build(str(mutant_src), str(tmp_path / "libmutant.so"), force=True)
+    lib = oracle.load(lib_path)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, RuntimeError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
