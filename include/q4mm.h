@@ -1,0 +1,139 @@
+/*
+ * q4mm — GB300 (sm_103a) kernels for the Linear-layer product y = x·Wᵀ with
+ * an FP32 activation and a block-quantized weight that is dequantized inside
+ * the kernel.  C ABI of libq4mm.so.
+ *
+ * Shapes and layouts (every entry point):
+ *   K = inputDim, N = outputDim, T = tokens.
+ *   x  : T rows of K fp32 values, row-major ([T][K]); token r starts at x + r·K.
+ *   W  : N output rows stored one after another ([out, in] order, used in
+ *        place, never transposed; SKaiNET docs "Eager execution: backends and
+ *        kernels", paragraph on the dense x·Wᵀ row).  Each row is a run of
+ *        contiguous blocks (the BLOCKED_ROW_MAJOR order of SKaiNET issue
+ *        #1138, section "Tasks").
+ *   y  : T rows of N fp32 values, row-major ([T][N]); token r writes y + r·N
+ *        (the prefill loop "advance offsets by r·k / r·n", same section).
+ *        y is overwritten, never accumulated into.
+ *
+ * Ownership and memory: x, W and y are DEVICE pointers owned by the caller.
+ * The library allocates nothing: no workspace, no per-call scratch.  x, W and
+ * y must not overlap.
+ *
+ * Streams: every compute call is asynchronous on `stream` (NULL means the
+ * legacy default stream).  Validation is synchronous: an invalid call returns
+ * its error before anything is launched and leaves y untouched.  Calls on one
+ * stream may overlap their prologue with the previous kernel on that stream
+ * (programmatic dependent launch): weight bytes, which no earlier kernel
+ * writes, may be fetched before the previous kernel has finished; x is read
+ * and y written only after it has.
+ *
+ * Errors: every entry point returns Q4MM_OK (0) or a negative q4mm_status;
+ * q4mm_last_error() then returns a message for the calling thread.  No C++
+ * exception crosses this boundary.  Asynchronous faults surface through the
+ * CUDA runtime as usual (the next synchronising call on the stream).
+ */
+#ifndef Q4MM_H
+#define Q4MM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *q4mm_stream_t;
+
+typedef enum {
+    Q4MM_OK = 0,
+    Q4MM_ERR_DIM = -1,     /* a dimension is <= 0, above its limit, or inputDim breaks its multiple */
+    Q4MM_ERR_NULL = -2,    /* a required pointer is NULL */
+    Q4MM_ERR_ALIGN = -3,   /* a pointer is not aligned as its entry point requires */
+    Q4MM_ERR_CUDA = -4,    /* the CUDA runtime reported an error (launch, device query) */
+    Q4MM_ERR_TIMEOUT = -5, /* a bounded in-kernel wait ran out (see q4mm_device_status) */
+    Q4MM_ERR_ALIAS = -6    /* x, W and y overlap */
+} q4mm_status;
+
+/* Largest inputDim accepted by every entry point. */
+#define Q4MM_MAX_INPUT_DIM 65536
+
+/*
+ * q4k_matmul — y = x·Wᵀ with W in Q4_K, FP32 arithmetic.
+ *
+ * Defined by SKaiNET PR #562 "feat(kernel): SIMD-fused Q4_K matmul kernel +
+ * Q4KMatmulKernel SPI": section "Pipeline" (the 256-value super-block, the
+ * strided nibble layout with sub-block 2j in the low nibbles and 2j+1 in the
+ * high nibbles of the same 32 bytes, value = d·sc·q − dmin·m, and the lazy
+ * correction acc += scale·codeSum − offset·inputSum) and section "Test plan"
+ * (inputDim must be a multiple of 256; results within 1e-4 relative of the
+ * dequantize-then-matmul reference).
+ *
+ * w_q4k : N·(K/256) blocks of 144 bytes: fp16 d (little-endian), fp16 dmin,
+ *         12 bytes packing eight 6-bit scales and eight 6-bit mins (ggml
+ *         canonical packing), 128 bytes of 4-bit codes.  16-byte aligned.
+ * x     : 16-byte aligned.  y: 4-byte aligned.
+ * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
+ *         outputDim >= 1; tokens >= 1.
+ * Precision: FP32 fused multiply-add throughout; per token row t,
+ *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
+ * Every weight byte is read from HBM once per call, whatever `tokens` is.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
+               int tokens, q4mm_stream_t stream);
+
+/*
+ * q4k_matmul_tc — the same product on the tensor cores (tcgen05), for
+ * prefill-sized token counts.  The dequantized weight and the activation are
+ * rounded to bfloat16 before the multiply; products are accumulated in FP32
+ * (tensor memory).  Same layouts, alignment and limits as q4k_matmul.
+ * Precision: per token row, max_o |y − y_bf16| <= 1e-4 · max_o |y_bf16| where
+ * y_bf16 is the exact product of the bf16-rounded operands, and
+ * max_o |y − y_exact| <= 1e-2 · max_o |y_exact|.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.  A bounded wait
+ * that runs out sets the device status word (see q4mm_device_status).
+ */
+int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
+                  int tokens, q4mm_stream_t stream);
+
+/*
+ * ternary_gemv — y = scale · (x·codesᵀ) with W in the BitNet b1.58 payload.
+ *
+ * Defined by SKaiNET issue #1138 "[ternary-f32] Phase 2: TernaryF32GemvNative
+ * SPI + reference ViewKernel + TernaryF32KernelPack", section "Tasks": four
+ * codes per byte, code(o, i) = ((byte >> 2·(i%4)) & 3) − 1 for byte
+ * o·K/4 + i/4; out[o] = Σ_k in[k]·code(o,k) accumulated in FP32; the scale
+ * multiplies the finished dot product once (pass 1.0f for the seam's raw,
+ * unscaled code-dot); rows for prefill advance by r·k and r·n.
+ *
+ * w_packed : N rows of K/4 bytes, no alignment required.  x: 16-byte
+ *            aligned.  y: 4-byte aligned.
+ * Limits: inputDim a positive multiple of 4 and <= Q4MM_MAX_INPUT_DIM;
+ *         outputDim >= 1; tokens >= 1.
+ * Precision: FP32.  The field value 3 decodes to +2 by the literal formula.
+ *            With integer activations the code-dot is exact, so y equals
+ *            the single fp32 rounding of scale × dot bit for bit.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,
+                 int outputDim, int tokens, q4mm_stream_t stream);
+
+/* Message for the last error returned on the calling thread ("" if none).
+ * The pointer stays valid until the thread's next failing call. */
+const char *q4mm_last_error(void);
+
+/*
+ * q4mm_device_status — waits for `stream`, then returns Q4MM_OK, or
+ * Q4MM_ERR_TIMEOUT if a bounded in-kernel wait of an earlier call on the
+ * current device ran out.  clear != 0 resets the status word afterwards.
+ * Returns Q4MM_ERR_CUDA if the stream reports an error.
+ */
+int q4mm_device_status(q4mm_stream_t stream, int clear);
+
+/* Library version, major·10000 + minor·100 + patch. */
+int q4mm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4MM_H */

@@ -1,0 +1,139 @@
+"""ctypes binding of libq4mm.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+Q4K_VALUES = 256
+Q4K_BYTES = 144
+
+_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "ternary_gemv", "q4mm_last_error",
+            "q4mm_device_status", "q4mm_version")
+
+
+class Q4mmError(RuntimeError):
+    """A q4mm entry point returned a negative status."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"q4mm status {code}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return os.environ.get("Q4MM_LIB", os.path.join(PKG, "libq4mm.so"))
+
+
+def _load() -> ctypes.CDLL:
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libq4mm.so not found at {path}: build it with `python quantized_matmul_q4_gb300/_build.py` "
+            "(needs nvcc); there is no fallback implementation")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    for name in ("q4k_matmul", "q4k_matmul_tc"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        fn.restype = i32
+    lib.ternary_gemv.argtypes = [vp, vp, f32, vp, i32, i32, i32, vp]
+    lib.ternary_gemv.restype = i32
+    lib.q4mm_last_error.argtypes = []
+    lib.q4mm_last_error.restype = ctypes.c_char_p
+    lib.q4mm_device_status.argtypes = [vp, i32]
+    lib.q4mm_device_status.restype = i32
+    lib.q4mm_version.argtypes = []
+    lib.q4mm_version.restype = i32
+    return lib
+
+
+_LIB = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _LIB
+
+
+def last_error() -> str:
+    return _LIB.q4mm_last_error().decode()
+
+
+def version() -> int:
+    return _LIB.q4mm_version()
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise Q4mmError(rc, last_error())
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# Raw-pointer entry points (device pointers, sizes, stream handle).
+
+def q4k_matmul_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
+    _check(_LIB.q4k_matmul(x, w, y, K, N, T, stream))
+
+
+def q4k_matmul_tc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
+    _check(_LIB.q4k_matmul_tc(x, w, y, K, N, T, stream))
+
+
+def ternary_gemv_ptr(x: int, w: int, scale: float, y: int, K: int, N: int, T: int,
+                     stream: int = 0) -> None:
+    _check(_LIB.ternary_gemv(x, w, ctypes.c_float(scale), y, K, N, T, stream))
+
+
+def device_status(stream=None, clear: bool = True) -> None:
+    """Raise Q4mmError if a bounded in-kernel wait ran out on this device."""
+    _check(_LIB.q4mm_device_status(_stream_ptr(stream), int(clear)))
+
+
+# Tensor entry points (torch CUDA tensors; y allocated unless `out` is given).
+
+def _prep(x, w, K, bytes_per_row, out, N):
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    if w.dtype != torch.uint8 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("the packed weight must be a contiguous uint8 CUDA tensor")
+    x2 = x.reshape(-1, x.shape[-1])
+    T, K_ = x2.shape
+    if K is not None and K != K_:
+        raise ValueError("x's last dimension must equal inputDim")
+    if N is None:
+        if bytes_per_row(K_) <= 0 or w.numel() % bytes_per_row(K_):
+            raise ValueError("weight size is not a whole number of rows")
+        N = w.numel() // bytes_per_row(K_)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=x.device)
+    elif out.dtype != torch.float32 or not out.is_cuda or not out.is_contiguous() or out.numel() != T * N:
+        raise ValueError("out must be a contiguous float32 CUDA tensor with tokens·outputDim elements")
+    return x2, T, K_, N, out
+
+
+def q4k_matmul(x, w, N: int | None = None, out=None, stream=None):
+    """y[T, N] = x[T, K] · dequant(W)ᵀ in FP32 (decode GEMV up to 8 tokens)."""
+    x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q4K_BYTES, out, N)
+    q4k_matmul_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+def q4k_matmul_tc(x, w, N: int | None = None, out=None, stream=None):
+    """As q4k_matmul on the tensor cores with bf16-rounded operands."""
+    x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q4K_BYTES, out, N)
+    q4k_matmul_tc_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+def ternary_gemv(x, w, scale: float = 1.0, N: int | None = None, out=None, stream=None):
+    """y[T, N] = scale · x[T, K] · codes(W)ᵀ, BitNet b1.58 payload, FP32."""
+    x2, T, K, N, out = _prep(x, w, None, lambda k: k // 4, out, N)
+    ternary_gemv_ptr(x2.data_ptr(), w.data_ptr(), float(scale), out.data_ptr(), K, N, T,
+                     _stream_ptr(stream))
+    return out.view(T, N)

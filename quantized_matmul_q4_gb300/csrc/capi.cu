@@ -1,0 +1,208 @@
+// C ABI of libq4mm.so: argument validation, dispatch to the kernels, error
+// reporting.  Declarations and the contract of every entry point are in
+// include/q4mm.h.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/q4mm.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int fail_cuda(cudaError_t e, const char *what) {
+    return fail(Q4MM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Set by a kernel whose bounded wait gave up.
+__device__ int g_device_status;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    int *status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("Q4MM_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
+int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(Q4MM_ERR_CUDA, "device ordinal %d out of range", dev);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!d.ready) {
+            e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+            e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(shared memory)");
+            e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
+            d.ready = true;
+        }
+    }
+    ctx->stream = reinterpret_cast<cudaStream_t>(stream);
+    ctx->num_sms = d.num_sms;
+    ctx->max_smem_optin = d.max_smem_optin;
+    ctx->status = d.status;
+    ctx->pdl = pdl_enabled();
+    return Q4MM_OK;
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_common(const float *x, const void *w, const float *y, int K, int N, int T, int k_multiple,
+                 size_t w_bytes_per_row, size_t w_align) {
+    if (!x || !w || !y) return fail(Q4MM_ERR_NULL, "x, weight and y must be non-NULL");
+    if (K <= 0 || N <= 0 || T <= 0)
+        return fail(Q4MM_ERR_DIM, "inputDim (%d), outputDim (%d) and tokens (%d) must be positive", K, N, T);
+    if (K % k_multiple)
+        return fail(Q4MM_ERR_DIM, "inputDim %d is not a multiple of %d", K, k_multiple);
+    if (K > Q4MM_MAX_INPUT_DIM)
+        return fail(Q4MM_ERR_DIM, "inputDim %d exceeds the limit %d", K, Q4MM_MAX_INPUT_DIM);
+    if (reinterpret_cast<uintptr_t>(x) % 16) return fail(Q4MM_ERR_ALIGN, "x must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(y) % 4) return fail(Q4MM_ERR_ALIGN, "y must be 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(w) % w_align)
+        return fail(Q4MM_ERR_ALIGN, "weight must be %zu-byte aligned", w_align);
+    const size_t xb = (size_t)T * K * sizeof(float), yb = (size_t)T * N * sizeof(float);
+    const size_t wb = (size_t)N * w_bytes_per_row;
+    if (overlap(x, xb, y, yb) || overlap(x, xb, w, wb) || overlap(w, wb, y, yb))
+        return fail(Q4MM_ERR_ALIAS, "x, weight and y must not overlap");
+    return Q4MM_OK;
+}
+
+}  // namespace
+
+namespace q4mm {
+
+cudaError_t ensure_smem_limit(const void *kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    struct Entry {
+        int dev;
+        const void *fn;
+        size_t bytes;
+    };
+    static Entry table[256];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (table[i].dev == dev && table[i].fn == kernel && table[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < used; ++i)
+        if (table[i].dev == dev && table[i].fn == kernel) {
+            table[i].bytes = bytes;
+            return cudaSuccess;
+        }
+    if (used < 256) table[used++] = Entry{dev, kernel, bytes};
+    return cudaSuccess;
+}
+
+}  // namespace q4mm
+
+extern "C" {
+
+int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim, int tokens,
+               q4mm_stream_t stream) {
+    int rc = check_common(x, w_q4k, y, inputDim, outputDim, tokens, 256,
+                          (size_t)(inputDim / 256) * 144, 16);
+    if (rc) return rc;
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    const uint8_t *W = static_cast<const uint8_t *>(w_q4k);
+    cudaError_t e;
+    if (tokens == 1) {
+        e = q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim);
+        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, 1);
+    } else if (tokens <= 8) {
+        e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
+        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
+    } else {
+        e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul launch");
+    return Q4MM_OK;
+}
+
+int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
+                  int tokens, q4mm_stream_t stream) {
+    int rc = check_common(x, w_q4k, y, inputDim, outputDim, tokens, 256,
+                          (size_t)(inputDim / 256) * 144, 16);
+    if (rc) return rc;
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    cudaError_t e = q4mm::launch_q4k_mm_tc(ctx, x, static_cast<const uint8_t *>(w_q4k), y, inputDim,
+                                           outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul_tc launch");
+    return Q4MM_OK;
+}
+
+int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,
+                 int outputDim, int tokens, q4mm_stream_t stream) {
+    int rc = check_common(x, w_packed, y, inputDim, outputDim, tokens, 4, (size_t)inputDim / 4, 1);
+    if (rc) return rc;
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    cudaError_t e = q4mm::launch_ternary_gemv(ctx, x, static_cast<const uint8_t *>(w_packed), scale, y,
+                                              inputDim, outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "ternary_gemv launch");
+    return Q4MM_OK;
+}
+
+const char *q4mm_last_error(void) { return g_err; }
+
+int q4mm_device_status(q4mm_stream_t stream, int clear) {
+    q4mm::LaunchCtx ctx;
+    int rc = device_ctx(stream, &ctx);
+    if (rc) return rc;
+    int host = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&host, ctx.status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the device status word");
+    if (clear && host) {
+        const int zero = 0;
+        e = cudaMemcpyAsync(ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return fail_cuda(e, "clearing the device status word");
+    }
+    if (host) return fail(Q4MM_ERR_TIMEOUT, "a bounded in-kernel wait ran out (status word %d)", host);
+    return Q4MM_OK;
+}
+
+int q4mm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal launchers behind the C ABI.  Each returns cudaSuccess or the
+// launch error; arguments are already validated by capi.cu.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <utility>
+
+namespace q4mm {
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    int num_sms;
+    int max_smem_optin;  // bytes of shared memory a CTA may opt into
+    int *status;         // device status word (bounded-wait time-outs)
+    bool pdl;            // launch with programmatic stream serialization
+};
+
+// Q4_K decode GEMV, one token (TMA-staged weight rows, x slab in registers).
+// Returns cudaErrorNotSupported when the shape is outside its geometry.
+cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                               int K, int N);
+
+// Q4_K decode GEMV for 1..8 tokens with x staged in shared memory.
+cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                  int K, int N, int T);
+
+// Q4_K prefill, FP32 FMA (any token count, tiles of 64 tokens).
+cudaError_t launch_q4k_mm_fp32(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                               int K, int N, int T);
+
+// Q4_K prefill on tcgen05 tensor cores (bf16 operands, fp32 accumulate).
+cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
+                             int N, int T);
+
+// BitNet b1.58 ternary GEMV, any token count.
+cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_t *W, float scale,
+                                float *y, int K, int N, int T);
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the attribute call is made only when the limit grows, so a
+// warmed-up launch (for instance one being captured into a CUDA graph) issues
+// nothing but the launch itself.
+cudaError_t ensure_smem_limit(const void *kernel, size_t bytes);
+
+template <typename... KArgs>
+cudaError_t ensure_smem(void (*kernel)(KArgs...), size_t bytes) {
+    return ensure_smem_limit(reinterpret_cast<const void *>(kernel), bytes);
+}
+
+// Launch helper: cudaLaunchKernelEx with optional programmatic serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(const LaunchCtx &c, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                          size_t smem, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    int nattr = 0;
+    if (c.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        nattr = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace q4mm

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol that include/q4mm.h declares, and rejects invalid arguments
+before any CUDA call (SKaiNET PR #562, section "Test plan": inputDim not a
+multiple of 256 is rejected; SKaiNET issue #1138, section "Tasks":
+inputDim % 4 == 0 for the ternary payload)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4mm.h")
+
+
+@pytest.fixture(scope="module")
+def q4mm():
+    import quantized_matmul_q4_gb300 as m
+    return m
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("q4k_matmul", "q4k_matmul_tc", "ternary_gemv", "q4mm_last_error",
+              "q4mm_device_status", "q4mm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(q4mm):
+    lib = ctypes.CDLL(q4mm.library_path())
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert q4mm.version() >= 100
+
+
+# Fake, suitably aligned device addresses: validation must reject before any
+# pointer is used, so nothing is dereferenced.
+X, W, Y = 0x10000000, 0x20000000, 0x30000000
+DIM, NULL, ALIGN, ALIAS = -1, -2, -3, -6
+
+
+@pytest.mark.parametrize("K", [0, -256, 100, 255, 257, 384, 65536 + 256])
+def test_q4k_rejects_bad_input_dim(q4mm, K):
+    for fn in (q4mm.q4k_matmul_ptr, q4mm.q4k_matmul_tc_ptr):
+        with pytest.raises(q4mm.Q4mmError) as e:
+            fn(X, W, Y, K, 16, 1, 0)
+        assert e.value.code == DIM
+        assert "inputDim" in q4mm.last_error()
+
+
+@pytest.mark.parametrize("K", [0, 2, 6, 2561, 65540])
+def test_ternary_rejects_bad_input_dim(q4mm, K):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.ternary_gemv_ptr(X, W, 1.0, Y, K, 16, 1, 0)
+    assert e.value.code == DIM
+
+
+@pytest.mark.parametrize("N,T", [(0, 1), (-1, 1), (16, 0), (16, -3)])
+def test_rejects_nonpositive_sizes(q4mm, N, T):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_ptr(X, W, Y, 256, N, T, 0)
+    assert e.value.code == DIM
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.ternary_gemv_ptr(X, W, 1.0, Y, 256, N, T, 0)
+    assert e.value.code == DIM
+
+
+def test_rejects_null(q4mm):
+    for args in ((0, W, Y), (X, 0, Y), (X, W, 0)):
+        with pytest.raises(q4mm.Q4mmError) as e:
+            q4mm.q4k_matmul_ptr(*args, 256, 4, 1, 0)
+        assert e.value.code == NULL
+        with pytest.raises(q4mm.Q4mmError) as e:
+            q4mm.ternary_gemv_ptr(args[0], args[1], 1.0, args[2], 256, 4, 1, 0)
+        assert e.value.code == NULL
+
+
+def test_rejects_misalignment(q4mm):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_ptr(X + 4, W, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIGN
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_ptr(X, W + 8, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIGN
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_ptr(X, W, Y + 2, 256, 4, 1, 0)
+    assert e.value.code == ALIGN
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.ternary_gemv_ptr(X + 8, W, 1.0, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIGN
+
+
+def test_rejects_overlap(q4mm):
+    # y overlapping x, and weight overlapping y.
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_ptr(X, W, X + 512, 256, 4, 2, 0)
+    assert e.value.code == ALIAS
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.ternary_gemv_ptr(X, Y + 4, 1.0, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIAS

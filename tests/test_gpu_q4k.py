@@ -1,0 +1,124 @@
+"""GPU parity of the Q4_K FP32 path (q4k_matmul) against the CPU oracle.
+
+Tolerance (SKaiNET PR #562, section "Test plan": 1e-4 relative against the
+gold dequantize-then-matmul reference), read per token row t as
+max_o |gpu − oracle| <= 1e-4 · max_o |oracle|.  Cases: the hand-worked block
+(exact), one-hot activations (element order), the workloads' shapes (full
+outputs where the oracle is quick, sampled rows at the largest sizes), an
+odd-shape sweep over the three kernels (1 token, 2–8 tokens, >8 tokens),
+ragged row counts, and run-to-run bit identity.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from golden import fixtures
+from gpu_helpers import assert_rows_close, q4k
+
+pytestmark = pytest.mark.gpu
+REL = 1e-4
+
+
+def _hand_block():
+    fx = fixtures.read("q4k_handworked_block.txt")
+    q = [(e // 32 + e % 32) % 16 for e in range(256)]
+    blk = oracle.q4k_pack_block(int(fx["d_bits"], 16), int(fx["dmin_bits"], 16),
+                                fixtures.ints(fx["sc"]), fixtures.ints(fx["m"]), q)
+    return fx, blk
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 64])
+def test_handworked_block_exact(T):
+    fx, blk = _hand_block()
+    xm = np.array([(e % 7) - 3 for e in range(256)], np.float32)
+    x = np.stack([xm if t % 2 == 0 else np.ones(256, np.float32) for t in range(T)])
+    y = q4k(x, blk, 256, 1)
+    for t in range(T):
+        want = float(fx["y_x_mod7"]) if t % 2 == 0 else float(fx["sum_w"])
+        assert y[t, 0] == want, (t, y[t, 0], want)
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_one_hot_reproduces_weights(T):
+    # Pins the element order inside the kernels: x = e_k must return w[:, k].
+    K, N = 512, 37
+    g = synth.rng(21)
+    W = synth.q4k_weights(g, N, K)
+    w = oracle.q4k_dequant(W, K, N)
+    ks = [0, 5, 31, 32, 40, 63, 64, 100, 127, 128, 191, 192, 255, 256, 300, 383, 384, 511]
+    for i in range(0, len(ks), T):
+        chunk = ks[i:i + T]
+        x = np.zeros((len(chunk), K), np.float32)
+        for t, k in enumerate(chunk):
+            x[t, k] = 1.0
+        y = q4k(x, W, K, N)
+        for t, k in enumerate(chunk):
+            ref = w[:, k].astype(np.float64)
+            assert np.abs(y[t] - ref).max() <= 1e-6 * np.abs(w).max(), k
+
+
+@pytest.mark.parametrize("name", ["q4k_gemv_1024x1024_t1", "q4k_gemv_4096x1024_t1",
+                                  "q4k_gemv_4096x4096_t1"])
+def test_decode_workloads_full(name):
+    x, W, K, N, T = synth.q4k_case(name)
+    y = q4k(x, W, K, N)
+    assert_rows_close(y, oracle.q4k_matmul(x, W, K, N), REL, name)
+
+
+SWEEP = [
+    (256, 1, 1), (256, 3, 2), (256, 33, 7), (256, 1000, 9), (512, 3, 8), (512, 33, 16),
+    (512, 1000, 1), (768, 5, 3), (1280, 33, 1), (2048, 17, 4), (4096, 33, 63), (4096, 65, 64),
+    (4096, 7, 65), (11008, 33, 1), (11008, 3, 8), (11008, 9, 9), (8192, 31, 1), (16384, 5, 1),
+    (24576, 3, 1), (24576, 3, 2), (65536, 2, 1), (3072, 1001, 1), (3072, 1001, 2),
+]
+
+
+@pytest.mark.parametrize("K,N,T", SWEEP, ids=[f"K{k}_N{n}_T{t}" for k, n, t in SWEEP])
+def test_shape_sweep(K, N, T):
+    x, W, K, N, T = synth.q4k_case((K, N, T), seed=K + N + T)
+    y = q4k(x, W, K, N)
+    assert_rows_close(y, oracle.q4k_matmul(x, W, K, N), REL, f"K{K} N{N} T{T}")
+
+
+def _sampled(K, N, T, seed, nsample=192):
+    x, W, K, N, T = synth.q4k_case((K, N, T), seed=seed)
+    y = q4k(x, W, K, N)
+    g = np.random.default_rng(seed + 1)
+    rows = np.unique(np.concatenate([[0, N - 1], g.choice(N, nsample, replace=False)]))
+    ref = oracle.q4k_matmul(x, W[rows], K, len(rows))
+    assert_rows_close(y[:, rows], ref, REL, f"K{K} N{N} T{T} sampled")
+    assert np.all(np.isfinite(y))
+
+
+def test_prefill_workload_sampled():
+    # 64 tokens × 4096 → 11008, FP32 variant, sampled output rows.
+    _sampled(4096, 11008, 64, seed=0)
+
+
+@pytest.mark.parametrize("K,N", synth.LLAMA7B_LAYER[3:7])
+@pytest.mark.parametrize("T", [1, 8])
+def test_llama7b_layer_shapes_sampled(K, N, T):
+    _sampled(K, N, T, seed=7 * K + N + T)
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_run_to_run_bit_identity(T):
+    x, W, K, N, T = synth.q4k_case((4096, 4096, T), seed=3)
+    a = q4k(x, W, K, N)
+    b = q4k(x, W, K, N)
+    assert a.tobytes() == b.tobytes()
+
+
+def test_special_case_min_only():
+    # d = 0, dmin = 1, every m = 1: y = −Σx on every row.
+    K, N, T = 1024, 9, 3
+    g = synth.rng(5)
+    W = synth.q4k_weights(g, N, K).reshape(N, K // 256, 144)
+    W[:, :, 0:4] = [0x00, 0x00, 0x00, 0x3C]
+    W[:, :, 4:16] = [0, 0, 0, 0, 1, 1, 1, 1, 0x10, 0x10, 0x10, 0x10]
+    x = synth.activations(g, T, K)
+    for TT in (1, T):
+        y = q4k(x[:TT], W, K, N)
+        want = -x[:TT].astype(np.float64).sum(1)
+        assert np.abs(y - want[:, None]).max() <= 1e-5 * np.abs(x).sum()
