@@ -21,6 +21,7 @@
 // removed together with the lazy min term: per sub-block s the contribution
 // is (256·d·sc_s)·acc_s − (128·d·sc_s + dmin·m_s)·Σx_s where
 // acc_s = Σ x·(0.5 + q/256).
+#include <cstdlib>
 #include <utility>
 
 #include "common.cuh"
@@ -60,26 +61,30 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 // Σ x·(0.5 + q/256) over the 32 low-nibble and the 32 high-nibble weights of a
 // 32-byte slab (q0 = bytes 0..15, q1 = bytes 16..31), x from registers:
 // xs[l] pairs with the low nibble of slab byte l, xs[32 + l] with its high
-// nibble.
+// nibble.  Two accumulator pairs per half keep the dependent chains short.
 __device__ __forceinline__ void slab_dot(const float (&xs)[64], uint4 q0, uint4 q1, float &lo,
                                          float &hi) {
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float2 alo = make_float2(0.f, 0.f), ahi = make_float2(0.f, 0.f);
+    float2 alo[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 ahi[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
-        const uint32_t h4 = (qw[w] >> 4) & 0x0F0F0F0Fu;
-        alo = ffma2(make_float2(xs[4 * w], xs[4 * w + 1]),
-                    make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), alo);
-        alo = ffma2(make_float2(xs[4 * w + 2], xs[4 * w + 3]),
-                    make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), alo);
-        ahi = ffma2(make_float2(xs[32 + 4 * w], xs[32 + 4 * w + 1]),
-                    make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), ahi);
-        ahi = ffma2(make_float2(xs[32 + 4 * w + 2], xs[32 + 4 * w + 3]),
-                    make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), ahi);
+        // (q >> 4) via a multiply-high, which issues on the FMA pipe and so
+        // leaves the integer pipe to the byte permutes.
+        const uint32_t h4 = __umulhi(qw[w], 1u << 28) & 0x0F0F0F0Fu;
+        float2 &al = alo[w & 1], &ah = ahi[w & 1];
+        al = ffma2(make_float2(xs[4 * w], xs[4 * w + 1]),
+                   make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), al);
+        al = ffma2(make_float2(xs[4 * w + 2], xs[4 * w + 3]),
+                   make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), al);
+        ah = ffma2(make_float2(xs[32 + 4 * w], xs[32 + 4 * w + 1]),
+                   make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), ah);
+        ah = ffma2(make_float2(xs[32 + 4 * w + 2], xs[32 + 4 * w + 3]),
+                   make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), ah);
     }
-    lo = alo.x + alo.y;
-    hi = ahi.x + ahi.y;
+    lo = (alo[0].x + alo[1].x) + (alo[0].y + alo[1].y);
+    hi = (ahi[0].x + ahi[1].x) + (ahi[0].y + ahi[1].y);
 }
 
 // x in shared memory: 16-byte unit u (elements 4u..4u+3) is stored at unit
@@ -89,8 +94,22 @@ __device__ __forceinline__ void slab_dot(const float (&xs)[64], uint4 q0, uint4 
 __device__ __forceinline__ int x_swz(int u) { return u ^ ((u >> 4) & 7); }
 
 // ----------------------------------------------------------------------------
-// One token: TMA-staged rows, x slab in registers
+// One token: bulk-copied rows, slab lanes, compile-time row geometry
 // ----------------------------------------------------------------------------
+//
+// Roles in a CTA (a contiguous range of output rows):
+//  * warp 0, lane 0 streams the rows into a shared-memory ring with 1-D bulk
+//    copies of whole stages (weights are never written by an earlier kernel,
+//    so this starts before the wait on the previous kernel), then copies x;
+//  * the other warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j
+//    of block b of every row it visits (32 low nibbles of sub-block 2j, 32
+//    high nibbles of 2j+1) with its 64 activations in registers, and decodes
+//    the two 6-bit scale/min pairs it needs from the block header.  Passes of
+//    two rows are numbered across the whole CTA, so different warps work on
+//    different stages at once.
+// kNB (blocks per row) is a template constant for common widths so that all
+// row and stage address arithmetic folds at compile time; 0 reads it at run
+// time.
 
 struct T1Params {
     const float *x;
@@ -99,32 +118,51 @@ struct T1Params {
     int *status;
     int N;
     int nb;            // blocks per row (K/256)
-    int wc;            // warps per row
-    int lpr;           // lanes per row (power of two) when wc == 1
-    int rpp;           // rows per warp pass (32/lpr when wc == 1, else 1)
     int rg;            // row groups: compute warps = wc·rg
     int rows_per_cta;  // contiguous rows per CTA
-    int stage_rows;    // rows per ring slot (multiple of rpp·rg)
+    int stage_rows;    // rows per ring slot (multiple of the pass size)
     int nslots;        // ring depth
-    uint32_t row_bytes;
 };
 
-__global__ void __launch_bounds__(32 * 9, 2) q4k_gemv_t1_kernel(T1Params p) {
+constexpr int kT1RoleWarps = 1;  // the copy warp
+
+template <int kNB>
+__global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
+    __shared__ __align__(8) uint64_t x_bar;
+
+    // Row geometry: compile-time when kNB > 0.
+    const int nb = kNB > 0 ? kNB : p.nb;
+    const int K = nb * kQ4kValues;
+    const uint32_t row_bytes = (uint32_t)nb * kQ4kBytes;
+    const int L = 4 * nb;                          // slab lanes per row
+    const bool wide = L > 32;                      // a row spans several warps
+    const int wc = wide ? (L + 31) / 32 : 1;       // warps per row
+    int lpr = 32;                                  // lanes per row slot when !wide
+    if (!wide) {
+        lpr = 4;
+        while (lpr < L) lpr <<= 1;
+    }
+    const int rpp = wide ? 1 : 32 / lpr;           // row slots per warp pass
+    const int pass_rows = 2 * rpp;
+    const int half = wide ? 16 : lpr / 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ncw = p.wc * p.rg;
-    const uint32_t slot_bytes = p.stage_rows * p.row_bytes;
-    uint8_t *ring = smem;
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + (size_t)p.nslots * slot_bytes);
+    const int ncw = wc * p.rg;
+    const uint32_t slot_bytes = p.stage_rows * row_bytes;
+    float *xlin = reinterpret_cast<float *>(smem);  // K floats as copied
+    float *xsm = xlin + K;                          // K floats, swizzled units
+    float *sx = xsm + K;                            // K/32 sub-block sums
+    uint8_t *ring = reinterpret_cast<uint8_t *>(sx + K / 32);
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
-    float *xsm = reinterpret_cast<float *>(empty_bar + p.nslots);  // K floats, swizzled
-    float *part = xsm + p.nb * kQ4kValues;                         // [rows_per_cta][wc]
+    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [rows_per_cta][wc]
 
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
     const int nstages = (nrows + p.stage_rows - 1) / p.stage_rows;
+    const int passes_per_stage = p.stage_rows / pass_rows;
 
     // Bulk copies need a 16-byte aligned destination; never issue one otherwise.
     if (smem_addr(smem) & 15) {
@@ -132,10 +170,15 @@ __global__ void __launch_bounds__(32 * 9, 2) q4k_gemv_t1_kernel(T1Params p) {
         return;
     }
     if (threadIdx.x == 0) {
+        // Warm L2 with x: a hint that returns no data, so it may run before
+        // the wait on the kernel that produces x.
+        bulk_prefetch_l2(p.x, (uint32_t)K * sizeof(float));
         for (int s = 0; s < p.nslots; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], ncw);
+            // Every pass of a stage is worked by the wc warps of a row.
+            mbar_init(&empty_bar[s], passes_per_stage * wc);
         }
+        mbar_init(&x_bar, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -143,110 +186,139 @@ __global__ void __launch_bounds__(32 * 9, 2) q4k_gemv_t1_kernel(T1Params p) {
     pdl_launch_dependents();
 
     if (warp == 0) {
-        // Producer: stream this CTA's contiguous rows, stage by stage.
         if (lane == 0) {
-            const uint8_t *src = p.W + (size_t)row0 * p.row_bytes;
-            for (int st = 0; st < nstages; ++st) {
+            const uint8_t *src = p.W + (size_t)row0 * row_bytes;
+            int st = 0;
+            for (; st < min(nstages, p.nslots); ++st) {
+                const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
+                mbar_arrive_expect_tx(&full_bar[st], rows * row_bytes);
+                bulk_g2s(ring + (size_t)st * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
+                         rows * row_bytes, &full_bar[st]);
+            }
+            // x may be produced by the previous kernel on the stream.
+            pdl_wait();
+            mbar_arrive_expect_tx(&x_bar, (uint32_t)K * sizeof(float));
+            bulk_g2s(xlin, p.x, (uint32_t)K * sizeof(float), &x_bar);
+            for (; st < nstages; ++st) {
                 const int slot = st % p.nslots;
-                if (st >= p.nslots &&
-                    !mbar_wait_bounded(&empty_bar[slot], ((st / p.nslots) - 1) & 1,
+                if (abort_flag) break;
+                if (!mbar_wait_bounded(&empty_bar[slot], ((st / p.nslots) - 1) & 1,
                                        kWaitLimitCycles)) {
                     abort_flag = 1;
                     flag_timeout(p.status);
                     break;
                 }
-                if (abort_flag) break;
                 const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-                const uint32_t bytes = rows * p.row_bytes;
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_g2s(ring + (size_t)slot * slot_bytes,
-                         src + (size_t)st * p.stage_rows * p.row_bytes, bytes, &full_bar[slot]);
+                mbar_arrive_expect_tx(&full_bar[slot], rows * row_bytes);
+                bulk_g2s(ring + (size_t)slot * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
+                         rows * row_bytes, &full_bar[slot]);
             }
         }
+        __syncwarp();
     } else {
-        const int cw = warp - 1;
-        const int wcol = cw % p.wc, rgi = cw / p.wc;
-        int s, ro;
-        if (p.wc == 1) {
-            ro = lane / p.lpr;
-            s = lane % p.lpr;
-        } else {
-            ro = 0;
-            s = wcol * 32 + lane;
-        }
-        const bool active = s < 4 * p.nb;
+        const int cw = warp - kT1RoleWarps;
+        const int wcol = cw % wc, rgi = cw / wc;
+        const int ro = wide ? 0 : lane / lpr;
+        const int s = wide ? wcol * 32 + lane : lane % lpr;
+        const bool active = s < L;
         const int b = active ? (s >> 2) : 0, j = s & 3;
 
-        // x may be produced by the previous kernel on the stream.
-        pdl_wait();
-        const int K = p.nb * kQ4kValues;
-        for (int u = threadIdx.x - 32; u < K / 4; u += ncw * 32) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.x) + u);
-            reinterpret_cast<float4 *>(xsm)[x_swz(u)] = v;
+        float xs[64];
+        float sum_lo, sum_hi;
+        if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
+            abort_flag = 1;
+            flag_timeout(p.status);
+        }
+        // Linear → swizzled copy with the sub-block sums: thread ct takes
+        // half sub-blocks (4 units); a sub-block's two halves sit in
+        // neighbouring lanes and are joined by one shuffle.
+        {
+            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, nh = K / 16;
+            for (int h0 = 0; h0 < nh; h0 += nth) {
+                const int h = h0 + ct;
+                float sum = 0.f;
+                if (h < nh) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = reinterpret_cast<const float4 *>(xlin)[4 * h + k];
+                        reinterpret_cast<float4 *>(xsm)[x_swz(4 * h + k)] = v;
+                        sum += (v.x + v.y) + (v.z + v.w);
+                    }
+                }
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                if (h < nh && (h & 1) == 0) sx[h / 2] = sum;
+            }
         }
         named_bar_sync(1, ncw * 32);
-
-        float xs[64];
-        float sum_lo = 0.f, sum_hi = 0.f;
         {
-            const int u0 = (b * kQ4kValues + j * 64) / 4;
+            const float4 *xv = reinterpret_cast<const float4 *>(xsm);
+            const int u0 = 16 * (4 * b + j);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (active) v = reinterpret_cast<const float4 *>(xsm)[x_swz(u0 + i)];
+                const float4 v = active ? xv[x_swz(u0 + i)] : make_float4(0.f, 0.f, 0.f, 0.f);
                 xs[4 * i] = v.x;
                 xs[4 * i + 1] = v.y;
                 xs[4 * i + 2] = v.z;
                 xs[4 * i + 3] = v.w;
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sum_lo += xs[i];
-                sum_hi += xs[32 + i];
-            }
+            sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
+            sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
 
-        for (int st = 0; st < nstages; ++st) {
+        const int npasses = (nrows + pass_rows - 1) / pass_rows;
+        const uint8_t *lane_ring = ring + b * kQ4kBytes;
+        int waited_stage = -1;
+        for (int pass = rgi; pass < npasses; pass += p.rg) {
+            const int st = pass / passes_per_stage;
             const int slot = st % p.nslots;
-            if (abort_flag) break;
-            if (!mbar_wait_bounded(&full_bar[slot], (st / p.nslots) & 1, kWaitLimitCycles)) {
-                abort_flag = 1;
-                flag_timeout(p.status);
-                break;
+            if (st != waited_stage) {
+                if (abort_flag) break;
+                if (!mbar_wait_bounded(&full_bar[slot], (st / p.nslots) & 1, kWaitLimitCycles)) {
+                    abort_flag = 1;
+                    flag_timeout(p.status);
+                    break;
+                }
+                waited_stage = st;
             }
-            const uint8_t *stage = ring + (size_t)slot * slot_bytes;
             const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-            for (int pass = rgi; pass * p.rpp < rows; pass += p.rg) {
-                const int rl = pass * p.rpp + ro;
-                float partial = 0.f;
-                if (active && rl < rows) {
-                    const uint8_t *blk = stage + (size_t)rl * p.row_bytes + b * kQ4kBytes;
-                    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
-                    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
-                    const SlabScales sc = slab_scales(hdr, j);
-                    float lo, hi;
-                    slab_dot(xs, q0, q1, lo, hi);
-                    partial = fmaf(sc.s0, lo, sc.s1 * hi) - fmaf(sc.o0, sum_lo, sc.o1 * sum_hi);
-                }
-                if (p.wc == 1) {
-                    partial = group_sum(partial, p.lpr);
-                    if (s == 0 && rl < rows) p.y[row0 + st * p.stage_rows + rl] = partial;
-                } else {
-                    partial = warp_sum(partial);
-                    if (lane == 0 && rl < rows)
-                        part[(st * p.stage_rows + rl) * p.wc + wcol] = partial;
-                }
+            const int ra = (pass - st * passes_per_stage) * pass_rows + 2 * ro, rb = ra + 1;
+            const uint8_t *ba = lane_ring + (size_t)slot * slot_bytes + min(ra, rows - 1) * row_bytes;
+            const uint8_t *bb = lane_ring + (size_t)slot * slot_bytes + min(rb, rows - 1) * row_bytes;
+            const uint4 ha = *reinterpret_cast<const uint4 *>(ba);
+            const uint4 hb = *reinterpret_cast<const uint4 *>(bb);
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(ba + 16 + 32 * j);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(ba + 32 + 32 * j);
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(bb + 16 + 32 * j);
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(bb + 32 + 32 * j);
+            const SlabScales sa = slab_scales(ha, j), sb = slab_scales(hb, j);
+            float alo, ahi, blo, bhi;
+            slab_dot(xs, a0, a1, alo, ahi);
+            slab_dot(xs, b0, b1, blo, bhi);
+            float pa = fmaf(sa.s0, alo, sa.s1 * ahi) - fmaf(sa.o0, sum_lo, sa.o1 * sum_hi);
+            float pb = fmaf(sb.s0, blo, sb.s1 * bhi) - fmaf(sb.o0, sum_lo, sb.o1 * sum_hi);
+            if (!active || ra >= rows) pa = 0.f;
+            if (!active || rb >= rows) pb = 0.f;
+            // Two-row butterfly: lanes with (lane & half) == 0 finish with
+            // row a, the others with row b.
+            const bool up = (lane & half) != 0;
+            float v = (up ? pb : pa) + __shfl_xor_sync(0xFFFFFFFFu, up ? pa : pb, half);
+            for (int o = half >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            const int r = up ? rb : ra;
+            const int rl = st * p.stage_rows + r;
+            if (wide) {
+                if ((lane & (half - 1)) == 0 && r < rows) part[rl * wc + wcol] = v;
+            } else {
+                if (s == (up ? half : 0) && r < rows) p.y[row0 + rl] = v;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
         }
 
-        if (p.wc > 1) {
+        if (wide) {
             named_bar_sync(1, ncw * 32);
-            for (int i = threadIdx.x - 32; i < nrows; i += ncw * 32) {
+            for (int i = threadIdx.x - 32 * kT1RoleWarps; i < nrows; i += ncw * 32) {
                 float acc = 0.f;
-                for (int w = 0; w < p.wc; ++w) acc += part[i * p.wc + w];
+                for (int w = 0; w < wc; ++w) acc += part[i * wc + w];
                 p.y[row0 + i] = acc;
             }
         }
@@ -254,7 +326,8 @@ __global__ void __launch_bounds__(32 * 9, 2) q4k_gemv_t1_kernel(T1Params p) {
 
     // Never leave a bulk copy writing into shared memory of an exiting CTA.
     __syncthreads();
-    if (abort_flag && threadIdx.x == 0) {
+    if (threadIdx.x == 0 && abort_flag) {
+        (void)mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles);
         for (int st = max(0, nstages - p.nslots); st < nstages; ++st)
             (void)mbar_wait_bounded(&full_bar[st % p.nslots], (st / p.nslots) & 1,
                                     kWaitLimitCycles);
@@ -300,11 +373,24 @@ __global__ void __launch_bounds__(32 * kMultiWarps) q4k_gemv_multi_kernel(MultiP
     for (int c0 = 0; c0 < p.nb; c0 += p.chunk_blocks) {
         const int cb = min(p.chunk_blocks, p.nb - c0);
         __syncthreads();  // previous chunk's x no longer in use; acc zeroed
-        for (int i = threadIdx.x; i < T * cb * 64; i += blockDim.x) {
-            const int t = i / (cb * 64), u = i % (cb * 64);
-            const float4 v =
-                __ldg(reinterpret_cast<const float4 *>(p.x + (size_t)t * p.K + c0 * kQ4kValues) + u);
-            reinterpret_cast<float4 *>(xsm + t * chunk_elems)[x_swz(u)] = v;
+        // Four loads in flight per thread before their stores.
+        const int total = T * cb * 64;
+        for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * blockDim.x;
+                const int t = i / (cb * 64), u = i % (cb * 64);
+                v[k] = i < total ? __ldg(reinterpret_cast<const float4 *>(
+                                             p.x + (size_t)t * p.K + c0 * kQ4kValues) + u)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * blockDim.x;
+                const int t = i / (cb * 64), u = i % (cb * 64);
+                if (i < total) reinterpret_cast<float4 *>(xsm + t * chunk_elems)[x_swz(u)] = v[k];
+            }
         }
         __syncthreads();
 
@@ -361,6 +447,34 @@ __global__ void __launch_bounds__(32 * kMultiWarps) q4k_gemv_multi_kernel(MultiP
     }
 }
 
+// Geometry knobs of the one-token kernel (environment, read once): compute
+// warps per CTA, resident CTAs per SM, bytes per ring slot, ring budget.
+struct T1Tuning {
+    int warps = 14;
+    int ctas_per_sm = 1;
+    int stage_bytes = 16384;
+    int ring_bytes = 200 * 1024;
+};
+
+int env_int(const char *name, int dflt, int lo, int hi) {
+    const char *v = getenv(name);
+    if (!v || !*v) return dflt;
+    const int x = atoi(v);
+    return x < lo ? lo : (x > hi ? hi : x);
+}
+
+const T1Tuning &t1_tuning() {
+    static const T1Tuning t = [] {
+        T1Tuning r;
+        r.warps = env_int("Q4MM_T1_WARPS", r.warps, 1, 15);
+        r.ctas_per_sm = env_int("Q4MM_T1_CTAS_PER_SM", r.ctas_per_sm, 1, 8);
+        r.stage_bytes = env_int("Q4MM_T1_STAGE_BYTES", r.stage_bytes, 1024, 65536);
+        r.ring_bytes = env_int("Q4MM_T1_RING_BYTES", r.ring_bytes, 8192, 200 * 1024);
+        return r;
+    }();
+    return t;
+}
+
 int next_pow2(int v) {
     int p = 1;
     while (p < v) p <<= 1;
@@ -378,52 +492,54 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     p.status = c.status;
     p.N = N;
     p.nb = K / kQ4kValues;
-    p.row_bytes = (uint32_t)p.nb * kQ4kBytes;
-    const int L = 4 * p.nb;
-    if (L <= 32) {
-        p.wc = 1;
-        p.lpr = next_pow2(L);
-        p.rpp = 32 / p.lpr;
-    } else {
-        p.wc = (L + 31) / 32;
-        p.lpr = 32;
-        p.rpp = 1;
-    }
-    // At most 8 compute warps (+1 producer): wider rows go to the generic kernel.
-    if (p.wc > 8) return cudaErrorNotSupported;
-    const int target_warps = 8;
-    p.rg = max(1, target_warps / p.wc);
-    const int ncw = p.wc * p.rg;
-    const int group_rows = p.rpp * p.rg;
-    const int m = max(1, 16384 / (int)(group_rows * p.row_bytes));
-    p.stage_rows = m * group_rows;
-    const size_t slot_bytes = (size_t)p.stage_rows * p.row_bytes;
+    const int row_bytes = p.nb * kQ4kBytes;
+    const int L = 4 * p.nb;  // slab lanes per row
+    const bool wide = L > 32;
+    const int wc = wide ? (L + 31) / 32 : 1;
+    const int pass_rows = wide ? 2 : 2 * (32 / next_pow2(max(L, 4)));
+    // At most 15 compute warps (+1 copy warp): wider rows go to the generic kernel.
+    if (wc > 15) return cudaErrorNotSupported;
+    const T1Tuning &tun = t1_tuning();
+    p.rg = max(1, tun.warps / wc);
+    const int ncw = wc * p.rg;
+    // Stage: whole passes, at least stage_bytes of weights (bulk copies of
+    // 16 KB and more run at full HBM bandwidth).
+    p.stage_rows = pass_rows * max(1, (tun.stage_bytes + pass_rows * row_bytes - 1) /
+                                          (pass_rows * row_bytes));
 
-    // Two CTAs per SM so that the next kernel's CTAs can start streaming while
-    // this one drains; rows split evenly and contiguously.
-    int grid = 2 * c.num_sms;
+    int grid = tun.ctas_per_sm * c.num_sms;
     p.rows_per_cta = (N + grid - 1) / grid;
-    if (p.rows_per_cta < p.rpp) p.rows_per_cta = p.rpp;
+    if (p.rows_per_cta < pass_rows) p.rows_per_cta = pass_rows;
+    if (p.stage_rows > p.rows_per_cta)
+        p.stage_rows = pass_rows * ((p.rows_per_cta + pass_rows - 1) / pass_rows);
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
+    const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
-    const size_t xs_bytes = (size_t)K * sizeof(float);
-    const size_t part_bytes = p.wc > 1 ? (size_t)p.rows_per_cta * p.wc * sizeof(float) : 0;
-    const size_t budget = 100 * 1024;
-    size_t fixed = xs_bytes + part_bytes + 2 * 8 * 8;
+    const size_t xs_bytes = 2 * (size_t)K * sizeof(float) + (size_t)(K / 32) * sizeof(float);
+    const size_t part_bytes = wide ? (size_t)p.rows_per_cta * wc * sizeof(float) : 0;
+    const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
+    const size_t budget = tun.ring_bytes;
     int nslots = (int)((budget > fixed ? budget - fixed : 0) / slot_bytes);
     const int stages_needed = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
-    nslots = min(nslots, max(2, stages_needed));
-    nslots = min(nslots, 8);
-    if (nslots < 2) {
-        nslots = 2;
-    }
+    nslots = max(2, min(nslots, min(stages_needed, 8)));
     p.nslots = nslots;
-    const size_t smem = (size_t)nslots * slot_bytes + 2 * nslots * sizeof(uint64_t) + xs_bytes + part_bytes;
+    const size_t smem = xs_bytes + (size_t)nslots * slot_bytes + 2 * nslots * sizeof(uint64_t) + part_bytes;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
 
-    cudaError_t e = ensure_smem(q4k_gemv_t1_kernel, smem);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(c, q4k_gemv_t1_kernel, dim3(grid), dim3(32 * (1 + ncw)), smem, p);
+    const dim3 block(32 * (kT1RoleWarps + ncw));
+    auto go = [&](auto kernel) -> cudaError_t {
+        cudaError_t e = ensure_smem(kernel, smem);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(c, kernel, dim3(grid), block, smem, p);
+    };
+    switch (p.nb) {
+        case 4: return go(q4k_gemv_t1_kernel<4>);
+        case 8: return go(q4k_gemv_t1_kernel<8>);
+        case 16: return go(q4k_gemv_t1_kernel<16>);
+        case 32: return go(q4k_gemv_t1_kernel<32>);
+        case 43: return go(q4k_gemv_t1_kernel<43>);
+        default: return go(q4k_gemv_t1_kernel<0>);
+    }
 }
 
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
