@@ -94,22 +94,80 @@ __device__ __forceinline__ void slab_dot(const float (&xs)[64], uint4 q0, uint4 
 __device__ __forceinline__ int x_swz(int u) { return u ^ ((u >> 4) & 7); }
 
 // ----------------------------------------------------------------------------
-// One token: bulk-copied rows, slab lanes, compile-time row geometry
+// One token: bulk-copied rows, slab lanes, exact int8 activation planes
 // ----------------------------------------------------------------------------
 //
 // Roles in a CTA (a contiguous range of output rows):
 //  * warp 0, lane 0 streams the rows into a shared-memory ring with 1-D bulk
 //    copies of whole stages (weights are never written by an earlier kernel,
-//    so this starts before the wait on the previous kernel), then copies x;
+//    so this starts before the wait on the previous kernel);
 //  * the other warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j
 //    of block b of every row it visits (32 low nibbles of sub-block 2j, 32
-//    high nibbles of 2j+1) with its 64 activations in registers, and decodes
-//    the two 6-bit scale/min pairs it needs from the block header.  Passes of
-//    two rows are numbered across the whole CTA, so different warps work on
-//    different stages at once.
-// kNB (blocks per row) is a template constant for common widths so that all
-// row and stage address arithmetic folds at compile time; 0 reads it at run
-// time.
+//    high nibbles of 2j+1) and decodes the two 6-bit scale/min pairs it needs
+//    from the block header.  Passes of two rows are numbered across the whole
+//    CTA, so different warps work on different stages at once.
+//
+// The code-dot Σ x·q of a sub-block runs on integer dot-product instructions
+// (four byte products per instruction).  Each 256-value block of x is split,
+// once per CTA, into three int8 planes under a power-of-two block scale s_b:
+//   x = s_b·(p1 + p2/128 + p3/16384) + e,  |e| ≤ 2^-15·s_b ≤ 2^-21·max|x_b|,
+// with |p1| ≤ 127 and |p2|, |p3| ≤ 64; every step of the split is exact
+// (power-of-two scalings and exact fp32 subtractions), so activations with at
+// most 21 significant bits below their block maximum (integers included) are
+// represented exactly.  The 4-bit codes are used as they are (no bias), the
+// integer sums are exact, and scales, mins and the final combination are fp32.
+// kNB (blocks per row) is a template constant for common widths so that row
+// and stage address arithmetic folds at compile time; 0 reads it at run time.
+
+// Scale d·sc and offset dmin·m of the two sub-blocks 2j and 2j+1 of a block
+// (lane-constant j), from the 16-byte block header.
+struct SlabScalesRaw {
+    float s0, s1, o0, o1;
+};
+
+__device__ __forceinline__ SlabScalesRaw slab_scales_raw(uint4 hdr, int j) {
+    const float2 dm = q4k_d_dmin(hdr.x);
+    const Q4kScales u = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+    const bool upper = j >= 2;
+    const uint32_t scw = upper ? u.sc_hi : u.sc_lo;
+    const uint32_t mw = upper ? u.m_hi : u.m_lo;
+    const int k0 = 2 * (j & 1);
+    SlabScalesRaw r;
+    r.s0 = dm.x * byte_to_float(scw, k0);  // exact: 11-bit × 6-bit
+    r.s1 = dm.x * byte_to_float(scw, k0 + 1);
+    r.o0 = dm.y * byte_to_float(mw, k0);
+    r.o1 = dm.y * byte_to_float(mw, k0 + 1);
+    return r;
+}
+
+// Integer code-dots of one slab against the three activation planes:
+// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] likewise for the high nibbles.
+// Slab byte l pairs with plane byte l of the low 32 positions (words 0..7)
+// and with plane byte l of the high 32 positions (words 8..15).
+__device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0, uint4 q1,
+                                                int (&d_lo)[3], int (&d_hi)[3]) {
+    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const int l4 = (int)(qw[w] & 0x0F0F0F0Fu);
+        const int h4 = (int)((qw[w] >> 4) & 0x0F0F0F0Fu);
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp) {
+            d_lo[pp] = __dp4a(l4, pl[pp][w], d_lo[pp]);
+            d_hi[pp] = __dp4a(h4, pl[pp][8 + w], d_hi[pp]);
+        }
+    }
+}
+
+// Σ q·x in units of the block scale from the three plane sums.
+__device__ __forceinline__ float plane_combine(const int (&d)[3]) {
+    const int d01 = d[0] * 128 + d[1];  // |d01| < 2^23: exact in fp32
+    return fmaf(static_cast<float>(d[2]), 1.0f / 16384.0f, static_cast<float>(d01) * (1.0f / 128.0f));
+}
+
+// Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter;
+// the low byte of the shifted value's bits is the result as an int8.
+__device__ __forceinline__ float shifted(float v) { return v + 12582912.0f; }
 
 struct T1Params {
     const float *x;
@@ -130,11 +188,11 @@ template <int kNB>
 __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
-    __shared__ __align__(8) uint64_t x_bar;
 
     // Row geometry: compile-time when kNB > 0.
     const int nb = kNB > 0 ? kNB : p.nb;
     const int K = nb * kQ4kValues;
+    const int nslabs = 4 * nb;                     // 64-value slabs per row
     const uint32_t row_bytes = (uint32_t)nb * kQ4kBytes;
     const int L = 4 * nb;                          // slab lanes per row
     const bool wide = L > 32;                      // a row spans several warps
@@ -151,10 +209,10 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ncw = wc * p.rg;
     const uint32_t slot_bytes = p.stage_rows * row_bytes;
-    float *xlin = reinterpret_cast<float *>(smem);  // K floats as copied
-    float *xsm = xlin + K;                          // K floats, swizzled units
-    float *sx = xsm + K;                            // K/32 sub-block sums
-    uint8_t *ring = reinterpret_cast<uint8_t *>(sx + K / 32);
+    int8_t *planes = reinterpret_cast<int8_t *>(smem);                // 3 planes of K bytes
+    float *sx = reinterpret_cast<float *>(planes + 3 * K);            // K/32 sub-block sums
+    float *sb = sx + K / 32;                                          // K/256 block scales
+    uint8_t *ring = reinterpret_cast<uint8_t *>(sb) + ((nb * 4 + 15) & ~15);
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
     float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [rows_per_cta][wc]
@@ -178,7 +236,6 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
             // Every pass of a stage is worked by the wc warps of a row.
             mbar_init(&empty_bar[s], passes_per_stage * wc);
         }
-        mbar_init(&x_bar, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -195,10 +252,6 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
                 bulk_g2s(ring + (size_t)st * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
                          rows * row_bytes, &full_bar[st]);
             }
-            // x may be produced by the previous kernel on the stream.
-            pdl_wait();
-            mbar_arrive_expect_tx(&x_bar, (uint32_t)K * sizeof(float));
-            bulk_g2s(xlin, p.x, (uint32_t)K * sizeof(float), &x_bar);
             for (; st < nstages; ++st) {
                 const int slot = st % p.nslots;
                 if (abort_flag) break;
@@ -223,79 +276,142 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
         const bool active = s < L;
         const int b = active ? (s >> 2) : 0, j = s & 3;
 
-        float xs[64];
-        float sum_lo, sum_hi;
-        if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
-            abort_flag = 1;
-            flag_timeout(p.status);
-        }
-        // Linear → swizzled copy with the sub-block sums: thread ct takes
-        // half sub-blocks (4 units); a sub-block's two halves sit in
-        // neighbouring lanes and are joined by one shuffle.
+        // x may be produced by the previous kernel on the stream.
+        pdl_wait();
+        // x → three int8 planes under power-of-two block scales, plus the
+        // fp32 sub-block sums.  Thread ct takes half sub-blocks (16 values);
+        // the 16 threads of a block (an aligned 16-lane group) share its
+        // maximum through shuffles, and the two halves of a sub-block sit in
+        // neighbouring lanes.
         {
             const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, nh = K / 16;
             for (int h0 = 0; h0 < nh; h0 += nth) {
                 const int h = h0 + ct;
-                float sum = 0.f;
-                if (h < nh) {
+                const bool on = h < nh;
+                float v[16];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 v = reinterpret_cast<const float4 *>(xlin)[4 * h + k];
-                        reinterpret_cast<float4 *>(xsm)[x_swz(4 * h + k)] = v;
-                        sum += (v.x + v.y) + (v.z + v.w);
-                    }
+                for (int k = 0; k < 4; ++k) {
+                    const float4 t = on ? __ldg(reinterpret_cast<const float4 *>(p.x) + 4 * h + k)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[4 * k] = t.x;
+                    v[4 * k + 1] = t.y;
+                    v[4 * k + 2] = t.z;
+                    v[4 * k + 3] = t.w;
                 }
+                float amax = 0.f, sum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    amax = fmaxf(amax, fabsf(v[i]));
+                    sum += v[i];
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
                 sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                if (h < nh && (h & 1) == 0) sx[h / 2] = sum;
+                // s_b = 2^e with amax / 2^e < 127 (1 when the block is zero).
+                int e = 0;
+                if (amax > 0.f) (void)frexpf(amax * (1.0f / 127.0f), &e);
+                e = max(e, -120);  // keeps 2^-e finite; such blocks still scale below 127
+                const float inv = ldexpf(1.0f, -e);
+                uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t b1[4], b2[4], b3[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float a = v[4 * k + i] * inv;  // exact
+                        const float s1 = shifted(a);
+                        const float r1 = (a - (s1 - 12582912.0f)) * 128.0f;  // exact
+                        const float s2 = shifted(r1);
+                        const float r2 = (r1 - (s2 - 12582912.0f)) * 128.0f;  // exact
+                        const float s3 = shifted(r2);
+                        b1[i] = __float_as_uint(s1);
+                        b2[i] = __float_as_uint(s2);
+                        b3[i] = __float_as_uint(s3);
+                    }
+                    // Low byte of each shifted value, four to a word.
+                    w1[k] = __byte_perm(__byte_perm(b1[0], b1[1], 0x0040), __byte_perm(b1[2], b1[3], 0x0040), 0x5410);
+                    w2[k] = __byte_perm(__byte_perm(b2[0], b2[1], 0x0040), __byte_perm(b2[2], b2[3], 0x0040), 0x5410);
+                    w3[k] = __byte_perm(__byte_perm(b3[0], b3[1], 0x0040), __byte_perm(b3[2], b3[3], 0x0040), 0x5410);
+                }
+                if (on) {
+                    // Unit-major layout: 16-byte unit u (0..11) of slab S at
+                    // index u·nslabs + S, with u = 4·plane + (h & 3) and
+                    // S = h / 4, so the eight lanes of a quarter warp read
+                    // eight consecutive units.
+                    uint4 *pu = reinterpret_cast<uint4 *>(planes) + (h & 3) * nslabs + (h >> 2);
+                    pu[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    pu[4 * nslabs] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    pu[8 * nslabs] = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+                    if ((h & 1) == 0) sx[h / 2] = sum;
+                    if ((h & 15) == 0) sb[h / 16] = ldexpf(1.0f, e);
+                }
             }
         }
         named_bar_sync(1, ncw * 32);
+        int pl[3][16];
+        float s_blk, sum_lo, sum_hi;
         {
-            const float4 *xv = reinterpret_cast<const float4 *>(xsm);
-            const int u0 = 16 * (4 * b + j);
+            // This slab's 64 plane bytes per plane: positions 64j..64j+31
+            // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
+            const uint4 *src = reinterpret_cast<const uint4 *>(planes) + (4 * b + j);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 v = active ? xv[x_swz(u0 + i)] : make_float4(0.f, 0.f, 0.f, 0.f);
-                xs[4 * i] = v.x;
-                xs[4 * i + 1] = v.y;
-                xs[4 * i + 2] = v.z;
-                xs[4 * i + 3] = v.w;
+            for (int pp = 0; pp < 3; ++pp) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 t = active ? src[(4 * pp + i) * nslabs] : make_uint4(0u, 0u, 0u, 0u);
+                    pl[pp][4 * i] = (int)t.x;
+                    pl[pp][4 * i + 1] = (int)t.y;
+                    pl[pp][4 * i + 2] = (int)t.z;
+                    pl[pp][4 * i + 3] = (int)t.w;
+                }
             }
+            s_blk = active ? sb[b] : 0.f;
             sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
 
         const int npasses = (nrows + pass_rows - 1) / pass_rows;
-        const uint8_t *lane_ring = ring + b * kQ4kBytes;
+        // Stage, slot and phase of the current pass, advanced without
+        // divisions as the pass index steps by rg.
+        int pin = rgi, st = 0;
+        while (pin >= passes_per_stage) {
+            pin -= passes_per_stage;
+            ++st;
+        }
+        int slot = st % p.nslots;
+        uint32_t phase = (st / p.nslots) & 1;
         int waited_stage = -1;
+        const uint8_t *stage_base = ring;
+        int rows = 0;
         for (int pass = rgi; pass < npasses; pass += p.rg) {
-            const int st = pass / passes_per_stage;
-            const int slot = st % p.nslots;
             if (st != waited_stage) {
                 if (abort_flag) break;
-                if (!mbar_wait_bounded(&full_bar[slot], (st / p.nslots) & 1, kWaitLimitCycles)) {
+                if (!mbar_wait_bounded(&full_bar[slot], phase, kWaitLimitCycles)) {
                     abort_flag = 1;
                     flag_timeout(p.status);
                     break;
                 }
                 waited_stage = st;
+                stage_base = ring + (size_t)slot * slot_bytes + b * kQ4kBytes;
+                rows = min(p.stage_rows, nrows - st * p.stage_rows);
             }
-            const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-            const int ra = (pass - st * passes_per_stage) * pass_rows + 2 * ro, rb = ra + 1;
-            const uint8_t *ba = lane_ring + (size_t)slot * slot_bytes + min(ra, rows - 1) * row_bytes;
-            const uint8_t *bb = lane_ring + (size_t)slot * slot_bytes + min(rb, rows - 1) * row_bytes;
+            const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
+            const uint8_t *ba = stage_base + min(ra, rows - 1) * row_bytes;
+            const uint8_t *bb = stage_base + min(rb, rows - 1) * row_bytes;
             const uint4 ha = *reinterpret_cast<const uint4 *>(ba);
             const uint4 hb = *reinterpret_cast<const uint4 *>(bb);
             const uint4 a0 = *reinterpret_cast<const uint4 *>(ba + 16 + 32 * j);
             const uint4 a1 = *reinterpret_cast<const uint4 *>(ba + 32 + 32 * j);
             const uint4 b0 = *reinterpret_cast<const uint4 *>(bb + 16 + 32 * j);
             const uint4 b1 = *reinterpret_cast<const uint4 *>(bb + 32 + 32 * j);
-            const SlabScales sa = slab_scales(ha, j), sb = slab_scales(hb, j);
-            float alo, ahi, blo, bhi;
-            slab_dot(xs, a0, a1, alo, ahi);
-            slab_dot(xs, b0, b1, blo, bhi);
-            float pa = fmaf(sa.s0, alo, sa.s1 * ahi) - fmaf(sa.o0, sum_lo, sa.o1 * sum_hi);
-            float pb = fmaf(sb.s0, blo, sb.s1 * bhi) - fmaf(sb.o0, sum_lo, sb.o1 * sum_hi);
+            const SlabScalesRaw sa = slab_scales_raw(ha, j), sc_b = slab_scales_raw(hb, j);
+            int da_lo[3] = {0, 0, 0}, da_hi[3] = {0, 0, 0}, db_lo[3] = {0, 0, 0}, db_hi[3] = {0, 0, 0};
+            slab_dot_planes(pl, a0, a1, da_lo, da_hi);
+            slab_dot_planes(pl, b0, b1, db_lo, db_hi);
+            float pa = s_blk * fmaf(sa.s0, plane_combine(da_lo), sa.s1 * plane_combine(da_hi)) -
+                       fmaf(sa.o0, sum_lo, sa.o1 * sum_hi);
+            float pb = s_blk * fmaf(sc_b.s0, plane_combine(db_lo), sc_b.s1 * plane_combine(db_hi)) -
+                       fmaf(sc_b.o0, sum_lo, sc_b.o1 * sum_hi);
             if (!active || ra >= rows) pa = 0.f;
             if (!active || rb >= rows) pb = 0.f;
             // Two-row butterfly: lanes with (lane & half) == 0 finish with
@@ -312,6 +428,15 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
+            pin += p.rg;
+            while (pin >= passes_per_stage) {
+                pin -= passes_per_stage;
+                ++st;
+                if (++slot == p.nslots) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
         }
 
         if (wide) {
@@ -327,7 +452,6 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     // Never leave a bulk copy writing into shared memory of an exiting CTA.
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
-        (void)mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles);
         for (int st = max(0, nstages - p.nslots); st < nstages; ++st)
             (void)mbar_wait_bounded(&full_bar[st % p.nslots], (st / p.nslots) & 1,
                                     kWaitLimitCycles);
@@ -515,7 +639,7 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
     const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
-    const size_t xs_bytes = 2 * (size_t)K * sizeof(float) + (size_t)(K / 32) * sizeof(float);
+    const size_t xs_bytes = 3 * (size_t)K + (size_t)(K / 32) * sizeof(float) + (size_t)((p.nb * 4 + 15) & ~15);
     const size_t part_bytes = wide ? (size_t)p.rows_per_cta * wc * sizeof(float) : 0;
     const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
     const size_t budget = tun.ring_bytes;
