@@ -410,7 +410,10 @@ def run_ours(a) -> None:
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n_ranks,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i32+f32",
+                "arithmetic": "fp32 activations split exactly (to 2^-21 of each 256-value block's "
+                              "maximum) into three int8 planes; 4-bit codes x planes in int32 dp4a; "
+                              "scales, mins and combination in fp32",
                 "data": "synthetic", "config": workload_config(layers),
                 "pct_of_hbm_peak": 100.0 * value / n_ranks / peaks["hbm_gbs"],
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
