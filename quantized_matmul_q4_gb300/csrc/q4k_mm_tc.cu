@@ -1,11 +1,523 @@
-// Q4_K prefill on tcgen05 tensor cores: not built yet.
+// Q4_K prefill on the tcgen05 tensor cores: bf16 operands, fp32 accumulation
+// in tensor memory (sm_103a).
+//
+// y[t][o] = Σ_k x[t][k]·w[o][k] with w = d·sc_s·q − dmin·m_s (SKaiNET PR #562
+// "feat(kernel): SIMD-fused Q4_K matmul kernel + Q4KMatmulKernel SPI",
+// section "Pipeline"), evaluated as D[o][t] = A[o][k]·B[t][k] with
+//   A = the dequantized weight tile, rounded to bf16 (M = 128 rows per CTA),
+//   B = the activation tile, rounded to bf16 (N = tokens, padded to 16),
+//   D = fp32 in tensor memory, K = 16 per MMA instruction.
+// Every weight byte is read once per call for up to 64 tokens.
+//
+// Roles in a CTA:
+//  * warp 8 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
+//    (128 rows × 144 bytes) per 256 values of K, and a 64-wide fp32 tile of x
+//    per 64 values of K.  Weights go first, before the wait on the previous
+//    kernel; x only after it.
+//  * warps 0–7 (two threads per weight row) dequantize each 64-value chunk of
+//    their row into bf16 and convert the matching x tile to bf16, both written
+//    in the 128-byte-swizzled K-major layout the MMA reads, then fence the
+//    writes to the async proxy and arrive on the chunk's barrier.
+//  * warp 9 allocates two accumulators in tensor memory; its first thread
+//    issues four 128×N×16 MMAs per chunk and commits them to the chunk's
+//    "empty" barrier.  K is cut into segments of 2048: each segment starts
+//    from zero in the accumulator the previous-but-one segment used, and its
+//    completion is committed to that accumulator's barrier.
+//  * warps 0–7 fold each finished segment into fp32 registers (tcgen05.ld
+//    plus an add) a few chunks after it ends, and finally write y.  Short
+//    accumulation chains in the tensor core keep the error of its fp32
+//    accumulation independent of K.
+// All waits are bounded; a time-out sets the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+#include <mutex>
+#include <utility>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "sync.cuh"
 
 namespace q4mm {
 
-cudaError_t launch_q4k_mm_tc(const LaunchCtx &, const float *, const uint8_t *, float *, int, int,
-                             int) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kTcRows = 128;                       // MMA M: weight rows per CTA
+constexpr int kTcKc = 64;                          // K per chunk: a 128-byte row of bf16
+constexpr int kTcDqWarps = 8;                      // dequant + epilogue warps
+constexpr int kTcWarpTma = kTcDqWarps;             // TMA producer warp
+constexpr int kTcWarpMma = kTcDqWarps + 1;         // MMA issuer warp
+constexpr int kTcThreads = 32 * (kTcDqWarps + 2);
+constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads
+constexpr int kTcWStages = 3;                      // Q4_K block-column tiles in flight
+constexpr int kTcXStages = 2;                      // fp32 activation tiles in flight
+constexpr int kTcABStages = 4;                     // bf16 operand tiles in flight
+constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 18432
+constexpr int kTcMaxTokens = 64;                   // tokens per launch tile
+constexpr int kTcSegChunks = 32;                   // chunks per accumulation segment (K = 2048)
+static_assert(kTcSegChunks > kTcABStages, "a segment is drained kTcABStages chunks after it ends");
+
+template <int TP>
+struct TcLayout {
+    static constexpr uint32_t a_bytes = kTcRows * 128;
+    static constexpr uint32_t b_bytes = TP * 128;
+    static constexpr uint32_t x_bytes = TP * kTcKc * 4;
+    static constexpr uint32_t off_a = 0;
+    static constexpr uint32_t off_b = off_a + kTcABStages * a_bytes;
+    static constexpr uint32_t off_w = off_b + kTcABStages * b_bytes;
+    static constexpr uint32_t off_x = off_w + kTcWStages * kTcWTileBytes;
+    static constexpr uint32_t off_bar = off_x + kTcXStages * x_bytes;
+    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcXStages + 2 * kTcABStages + 4 + 1;
+    static constexpr uint32_t off_misc = off_bar + 8 * n_bars;
+    static constexpr uint32_t total = off_misc + 16;
+    static_assert(off_b % 1024 == 0 && off_w % 1024 == 0, "operand tiles must be 1024-byte aligned");
+    static_assert(b_bytes % 1024 == 0, "B tile must hold whole 8-row swizzle atoms");
+};
+
+// tcgen05 shared-memory matrix descriptor for a K-major operand in the
+// 128-byte swizzle layout: rows of 128 bytes, 8-row atoms 1024 bytes apart,
+// the 16-byte chunk c of row r stored at chunk c ^ (r % 8).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1u << 16;                          // leading byte offset (unused here): 16 B
+    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows × 128 B
+    d |= (uint64_t)1u << 46;                          // descriptor version for tcgen05
+    d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major.
+template <int TP>
+__device__ __forceinline__ uint32_t mma_idesc() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TP >> 3) << 17) |
+           ((uint32_t)(kTcRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int TP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                     float *__restrict__ y, int K, int N, int T, int *status) {
+    using L = TcLayout<TP>;
+    constexpr uint32_t kAccCols = TP <= 32 ? 32 : 64;     // one accumulator
+    constexpr uint32_t kTmemCols = 2 * kAccCols;          // two, alternating by segment
+    constexpr int kGroups = TP / 16;                      // 16-column groups
+    constexpr int kLowGroups = (kGroups + 1) / 2;         // groups read by warps 0–3
+    extern __shared__ uint8_t tc_smem_raw[];
+    __shared__ volatile int abort_flag;
+    // Operand tiles need 1024-byte aligned swizzle atoms.
+    const uint32_t raw = smem_addr(tc_smem_raw);
+    uint8_t *smem = tc_smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
+    uint64_t *full_w = bars, *empty_w = full_w + kTcWStages;
+    uint64_t *full_x = empty_w + kTcWStages, *empty_x = full_x + kTcXStages;
+    uint64_t *full_ab = empty_x + kTcXStages, *empty_ab = full_ab + kTcABStages;
+    uint64_t *seg_full = empty_ab + kTcABStages, *seg_free = seg_full + 2;
+    uint64_t *done = seg_free + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * kTcRows;
+    const int nchunks = K / kTcKc;
+    const int nblocks = K / kQ4kValues;
+    const int nsegs = (nchunks + kTcSegChunks - 1) / kTcSegChunks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcWStages; ++s) {
+            mbar_init(&full_w[s], 1);
+            mbar_init(&empty_w[s], kTcDq);
+        }
+        for (int s = 0; s < kTcXStages; ++s) {
+            mbar_init(&full_x[s], 1);
+            mbar_init(&empty_x[s], kTcDq);
+        }
+        for (int s = 0; s < kTcABStages; ++s) {
+            mbar_init(&full_ab[s], kTcDq);
+            mbar_init(&empty_ab[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&seg_full[s], 1);
+            mbar_init(&seg_free[s], kTcDq);
+        }
+        mbar_init(done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kTcWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == kTcWarpTma) {
+        if (lane == 0) {
+            // Weight tiles and activation tiles are issued independently, each
+            // as soon as its ring slot is free, so the weight stream runs up to
+            // kTcWStages blocks ahead whatever the activation ring does.
+            int nw = 0, nx = 0;
+            for (; nw < min(nblocks, kTcWStages); ++nw) {
+                mbar_arrive_expect_tx(&full_w[nw], kTcWTileBytes);
+                tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, nw * kQ4kBytes, row0, &full_w[nw]);
+            }
+            // x may be produced by the previous kernel on the stream.
+            pdl_wait();
+            long long t_last = clock64();
+            while ((nw < nblocks || nx < nchunks) && !abort_flag) {
+                bool progressed = false;
+                if (nw < nblocks) {
+                    const int ws = nw % kTcWStages;
+                    if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
+                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, nw * kQ4kBytes, row0,
+                                    &full_w[ws]);
+                        ++nw;
+                        progressed = true;
+                    }
+                }
+                if (nx < nchunks) {
+                    const int xs = nx % kTcXStages;
+                    if (nx < kTcXStages || mbar_try_wait(&empty_x[xs], ((nx / kTcXStages) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&full_x[xs], L::x_bytes);
+                        tma_load_2d(sbase + L::off_x + xs * L::x_bytes, &tm_x, nx * kTcKc, 0, &full_x[xs]);
+                        ++nx;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    t_last = clock64();
+                } else if (clock64() - t_last > kWaitLimitCycles) {
+                    abort_flag = 1;
+                    flag_timeout(status);
+                }
+            }
+            // Never leave a tensor copy writing into an exiting CTA: the last
+            // use of each ring slot must have landed.
+            for (int b = max(0, nw - kTcWStages); b < nw; ++b)
+                (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
+            for (int c = max(0, nx - kTcXStages); c < nx; ++c)
+                (void)mbar_wait_bounded(&full_x[c % kTcXStages], (c / kTcXStages) & 1, kWaitLimitCycles);
+        }
+        __syncwarp();
+    } else if (warp == kTcWarpMma) {
+        if (lane == 0) {
+            // Segment sg (kTcSegChunks chunks) accumulates into buffer sg % 2,
+            // starting from zero; the dequant warps fold each finished segment
+            // into fp32 registers.  Short accumulation chains keep the tensor
+            // core's accumulation error independent of K.
+            const uint32_t idesc = mma_idesc<TP>();
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kTcABStages;
+                const int sg = c / kTcSegChunks, cs = c - sg * kTcSegChunks;
+                const int buf = sg & 1;
+                if (abort_flag) break;
+                bool ok = true;
+                if (cs == 0 && sg >= 2)
+                    ok = mbar_wait_bounded(&seg_free[buf], ((sg >> 1) - 1) & 1, kWaitLimitCycles);
+                ok = ok && mbar_wait_bounded(&full_ab[s], (c / kTcABStages) & 1, kWaitLimitCycles);
+                if (!ok) {
+                    abort_flag = 1;
+                    flag_timeout(status);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sbase + L::off_a + s * L::a_bytes;
+                const uint32_t b0 = sbase + L::off_b + s * L::b_bytes;
+                const uint32_t d = tmem_base + (uint32_t)buf * kAccCols;
+#pragma unroll
+                for (int kk = 0; kk < kTcKc / 16; ++kk)
+                    tc_mma(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (cs | kk) != 0);
+                tc_commit(&empty_ab[s]);
+                if (cs == kTcSegChunks - 1 || c == nchunks - 1) tc_commit(&seg_full[buf]);
+            }
+            // Always signal completion of whatever was issued, and wait for
+            // it, so that tensor memory is never released with MMAs in flight.
+            tc_commit(done);
+            (void)mbar_wait_bounded(done, 0, kWaitLimitCycles);
+        }
+        __syncwarp();
+    } else {
+        // Dequantize: thread (r, h) fills the 32 values of half h of row r's
+        // 64-value chunk: h = 0 the low nibbles (sub-block 2j), h = 1 the high
+        // nibbles (sub-block 2j+1) of the same 32 qs bytes.
+        const int t = threadIdx.x;
+        const int r = t >> 1, h = t & 1;
+        // Epilogue geometry: TMEM lanes 32·(warp % 4) .. +31 hold this
+        // quarter's rows; warps 0–3 read the first kLowGroups 16-column
+        // groups, warps 4–7 the rest.
+        const int quarter = warp & 3;
+        const int g_begin = warp < 4 ? 0 : kLowGroups;
+        const int n_groups = warp < 4 ? kLowGroups : kGroups - kLowGroups;
+        float acc[2][16];
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[gi][i] = 0.f;
+        // Fold segment sg into acc.  Warp-uniform: tcgen05.ld is collective.
+        auto drain = [&](int sg) -> bool {
+            const int buf = sg & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&seg_full[buf], (sg >> 1) & 1, kWaitLimitCycles)))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+                if (gi < n_groups) {
+                    float v[16];
+                    tc_ld16(tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)buf * kAccCols +
+                                (uint32_t)(16 * (g_begin + gi)),
+                            v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[gi][i] += v[i];
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&seg_free[buf]);
+            return true;
+        };
+
+        bool good = true;
+        int drained = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c >> 2, j = c & 3;
+            const int ws = b % kTcWStages, xs = c % kTcXStages, s = c % kTcABStages;
+            if (__any_sync(0xffffffffu, abort_flag != 0)) {
+                good = false;
+                break;
+            }
+            // Segment `drained` ended kTcABStages chunks ago, so the previous
+            // iteration's wait on empty_ab already covered its last MMAs.
+            if (c == (drained + 1) * kTcSegChunks + kTcABStages && !drain(drained++)) {
+                good = false;
+                break;
+            }
+            bool ok = true;
+            if (j == 0) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
+            ok = ok && mbar_wait_bounded(&full_x[xs], (c / kTcXStages) & 1, kWaitLimitCycles);
+            if (ok && c >= kTcABStages)
+                ok = mbar_wait_bounded(&empty_ab[s], ((c / kTcABStages) - 1) & 1, kWaitLimitCycles);
+            if (!__all_sync(0xffffffffu, ok)) {
+                good = false;
+                break;
+            }
+            // A: weight row r.
+            {
+                const uint8_t *blk = smem + L::off_w + ws * kTcWTileBytes + r * kQ4kBytes;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
+                const float2 dm = q4k_d_dmin(hdr.x);
+                const Q4kScales u = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+                const int sb = 2 * j + h;
+                const uint32_t scw = sb < 4 ? u.sc_lo : u.sc_hi;
+                const uint32_t mw = sb < 4 ? u.m_lo : u.m_hi;
+                const float scale = dm.x * byte_to_float(scw, sb & 3);   // exact
+                const float offset = dm.y * byte_to_float(mw, sb & 3);   // exact
+                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint8_t *arow = smem + L::off_a + s * L::a_bytes + r * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // Logical 16-byte chunk 4h + i holds k = 32h + 8i .. 32h + 8i + 7,
+                    // i.e. qs bytes 8i .. 8i + 7 (words 2i, 2i + 1).
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int wv = 0; wv < 2; ++wv) {
+                        const uint32_t v = h ? (qw[2 * i + wv] >> 4) : qw[2 * i + wv];
+                        const float e0 = fmaf(scale, (float)(v & 15u), -offset);
+                        const float e1 = fmaf(scale, (float)((v >> 8) & 15u), -offset);
+                        const float e2 = fmaf(scale, (float)((v >> 16) & 15u), -offset);
+                        const float e3 = fmaf(scale, (float)((v >> 24) & 15u), -offset);
+                        pk[2 * wv] = pack_bf16x2(e0, e1);
+                        pk[2 * wv + 1] = pack_bf16x2(e2, e3);
+                    }
+                    const int lc = 4 * h + i;
+                    *reinterpret_cast<uint4 *>(arow + ((lc ^ (r & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+            // B: the activation tile, TP tokens × 64 values, fp32 → bf16.
+            {
+                const float *xt = reinterpret_cast<const float *>(smem + L::off_x + xs * L::x_bytes);
+                uint8_t *bt = smem + L::off_b + s * L::b_bytes;
+                for (int task = t; task < TP * 8; task += kTcDq) {
+                    const int tok = task >> 3, qc = task & 7;
+                    const float4 v0 = *reinterpret_cast<const float4 *>(xt + tok * kTcKc + 8 * qc);
+                    const float4 v1 = *reinterpret_cast<const float4 *>(xt + tok * kTcKc + 8 * qc + 4);
+                    *reinterpret_cast<uint4 *>(bt + tok * 128 + ((qc ^ (tok & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w),
+                                   pack_bf16x2(v1.x, v1.y), pack_bf16x2(v1.z, v1.w));
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(&full_ab[s]);
+            mbar_arrive(&empty_x[xs]);
+            if (j == 3) mbar_arrive(&empty_w[ws]);
+        }
+        while (good && drained < nsegs) good = drain(drained++);
+
+        if (good) {
+            pdl_wait();
+            const int row = row0 + 32 * quarter + lane;
+            if (row < N) {
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi)
+                    if (gi < n_groups) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int col = 16 * (g_begin + gi) + i;
+                            if (col < T) y[(size_t)col * N + row] = acc[gi][i];
+                        }
+                    }
+            }
+        } else {
+            abort_flag = 1;
+            flag_timeout(status);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcWarpMma) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+template <int TP>
+cudaError_t launch_tile(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                        int T) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    alignas(64) CUtensorMap tm_w, tm_x;
+    const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
+    {
+        const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)kQ4kBytes, (cuuint32_t)kTcRows};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(W), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(float)};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcKc, (cuuint32_t)TP};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = TcLayout<TP>::total + 1024;
+    if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
+    cudaError_t e = ensure_smem(q4k_mm_tc_kernel<TP>, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((N + kTcRows - 1) / kTcRows);
+    return launch_kernel(c, q4k_mm_tc_kernel<TP>, grid, dim3(kTcThreads), smem, tm_w, tm_x, y, K, N, T,
+                         c.status);
+}
+
+}  // namespace
+
+cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
+                             int N, int T) {
+    // Token tiles of up to 64 (the weights are re-read once per tile).
+    cudaError_t e = cudaSuccess;
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += kTcMaxTokens) {
+        const int tt = min(kTcMaxTokens, T - t0);
+        const float *xt = x + (size_t)t0 * K;
+        float *yt = y + (size_t)t0 * N;
+        const int tp = (tt + 15) / 16 * 16;
+        switch (tp) {
+            case 16: e = launch_tile<16>(c, xt, W, yt, K, N, tt); break;
+            case 32: e = launch_tile<32>(c, xt, W, yt, K, N, tt); break;
+            case 48: e = launch_tile<48>(c, xt, W, yt, K, N, tt); break;
+            default: e = launch_tile<64>(c, xt, W, yt, K, N, tt); break;
+        }
+    }
+    return e;
 }
 
 }  // namespace q4mm
