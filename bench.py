@@ -1,29 +1,37 @@
 #!/usr/bin/env python3
-"""Benchmark: Q4_K decode GEMV weight-stream GB/s at 4096×4096, one token.
+"""Benchmark of the library's kernels through its C ABI, one JSON line.
 
-One step is one decode pass over `--layers` (default 64) distinct
-4096×4096 Q4_K weights, each a one-token GEMV through the C ABI
-(q4k_matmul): 64 × 9.44 MB = 604 MB of weights per step, 4.7× the 129 MB L2,
-so no step finds its weights in L2 and no flush is needed.  The timed region
-replays the step as a CUDA graph (the launches are the library's own kernels,
-captured once).  `value` is whole-job weight bytes per second.
+Default workload (`q4k_gemv_4096x4096_t1`): Q4_K decode GEMV weight-stream
+GB/s at 4096×4096, one token.  One step is one decode pass over 64 distinct
+4096×4096 Q4_K weights, each a one-token GEMV (q4k_matmul): 64 × 9.44 MB =
+604 MB of weights per step, 4.7× the 129 MB L2, so no step finds its weights
+in L2 and no flush is needed.  `--workload` selects another of the table
+below (prefill on the tensor cores or in FP32, ternary GEMV, a Llama-2-7B
+decode sweep, smaller GEMVs); each is sized above L2 the same way.
 
-Also reported: `roofline` (the GEMV kernel against the measured HBM copy
-bandwidth), `e2e` (the same step through the raw-pointer C ABI with the
-activations copied in from pinned host memory and the outputs copied back,
-every step, no graph), `cpu_baseline` (the CPU oracle on a bounded sample of
-the same workload), `clocks` (nvidia-smi sampled during the timed region).
+The timed region replays the step as a CUDA graph (the launches are the
+library's own kernels, captured once).  `value` is whole-job weight bytes
+per second (GB/s workloads) or 2·K·N·T flops per second (TFLOP/s workloads).
 
-`--impl reference` times the CPU oracle itself on the same workload, metric
-and unit (the reference arm for this build).
+Also reported: `roofline` (the dominant kernel against the measured HBM copy
+bandwidth, the measured sustained bf16 tensor rate, or the FP32 FMA rate of
+152 SMs at 2.07 GHz), `e2e` (the same step through the raw-pointer C ABI
+with the activations copied in from pinned host memory and the outputs
+copied back, every step, no graph), `cpu_baseline` (the CPU oracle on a
+bounded sample of the same workload), `clocks` (nvidia-smi sampled during
+the timed region).
+
+`--impl reference` times the CPU oracle itself on a bounded sample of the
+same workload, in the same metric and unit.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs its own copy of
 the workload (weak scaling, no data-path collective); elapsed time is the
-maximum over ranks, value = bytes of all ranks ÷ that time.
+maximum over ranks, value = work of all ranks ÷ that time.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -38,14 +46,77 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "Q4_K GEMV weight-stream GB/s and % of GB300 HBM peak at 4096×4096, batch 1"
-K_DIM, N_DIM, TOKENS = 4096, 4096, 1
-Q4K_ROW_BYTES = K_DIM // 256 * 144
-WEIGHT_BYTES = N_DIM * Q4K_ROW_BYTES                      # 9,437,184 per GEMV
-ALG_BYTES = WEIGHT_BYTES + 4 * K_DIM * TOKENS + 4 * N_DIM * TOKENS  # weights + x + y
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "q4k_gemv_t1_4096x4096.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "quantized_matmul_q4_gb300", "csrc", f)
-                  for f in ("q4k_gemv.cu", "common.cuh", "sync.cuh")]
+FALLBACK_BF16_TFLOPS = 1700.0
+# FP32 FMA peak: 152 SMs × 128 FP32 lanes × 2 flop per FMA × 2.07 GHz (maximum SM clock).
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+CSRC = os.path.join(ROOT, "quantized_matmul_q4_gb300", "csrc")
+COMMON_SOURCES = ["common.cuh", "sync.cuh"]
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    kind: str                 # "q4k" or "ternary"
+    entry: str                # C-ABI symbol called once per matrix
+    mats: list                # (K, N) of each launch in one layer
+    tokens: int
+    layers: int               # layers per step (distinct device buffers)
+    unit: str                 # "GB/s" (weight bytes) or "TFLOP/s" (2·K·N·T)
+    bound: str                # roofline of the dominant kernel: "hbm", "tensor" or "alu"
+    kernel: str               # dominant kernel
+    metric: str
+    sources: list             # kernel sources (under csrc/) hashed for the traffic record
+    profile: str | None = None  # ncu summary with dram_bytes_per_launch, under profiles/
+    distinct: int = 4         # distinct host-generated weights per matrix (the rest are copies)
+    arithmetic: str = ""
+
+
+def _q4k_bytes(K, N):
+    return N * (K // 256) * 144
+
+
+def weight_bytes(kind, K, N):
+    return _q4k_bytes(K, N) if kind == "q4k" else N * (K // 4)
+
+
+T1_ARITH = ("fp32 activations split exactly (to 2^-21 of each 256-value block's maximum) into three "
+            "int8 planes; 4-bit codes x planes in int32 dp4a; scales, mins and combination in fp32")
+LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
+WORKLOADS = {w.name: w for w in [
+    Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",
+             "q4k_gemv_t1_kernel", METRIC, ["q4k_gemv.cu"], "q4k_gemv_t1_4096x4096.md",
+             distinct=64, arithmetic=T1_ARITH),
+    Workload("q4k_gemv_4096x1024_t1", "q4k", "q4k_matmul", [(4096, 1024)], 1, 128, "GB/s", "hbm",
+             "q4k_gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 4096->1024, batch 1",
+             ["q4k_gemv.cu"], arithmetic=T1_ARITH),
+    Workload("q4k_gemv_1024x1024_t1", "q4k", "q4k_matmul", [(1024, 1024)], 1, 512, "GB/s", "hbm",
+             "q4k_gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 1024x1024, batch 1",
+             ["q4k_gemv.cu"], arithmetic=T1_ARITH),
+    Workload("q4k_prefill_tc_4096x11008_t64", "q4k", "q4k_matmul_tc", [(4096, 11008)], 64, 16,
+             "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
+             "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands",
+             ["q4k_mm_tc.cu"], arithmetic="bf16 operands (dequantized in fp32, rounded once), "
+                                          "fp32 accumulation in tensor memory"),
+    Workload("q4k_prefill_fp32_4096x11008_t64", "q4k", "q4k_matmul", [(4096, 11008)], 64, 16,
+             "TFLOP/s", "alu", "q4k_mm_fp32_kernel",
+             "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu"],
+             arithmetic="fp32 dequantization and fp32 FMA"),
+    Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
+             "hbm", "ternary_gemv_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "batch 1", ["ternary_gemv.cu"], arithmetic="fp32"),
+    Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",
+             "hbm", "ternary_gemv_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "16 tokens", ["ternary_gemv.cu"], arithmetic="fp32"),
+    Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
+             "q4k_gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
+             "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
+    Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "hbm",
+             "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
+             "layers x q,k,v,o,gate,up,down), 8 tokens", ["q4k_gemv.cu"], distinct=1,
+             arithmetic="fp32 dequantization and fp32 FMA"),
+]}
+DEFAULT_WORKLOAD = "q4k_gemv_4096x4096_t1"
 
 
 def parse_args(argv=None):
@@ -54,7 +125,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--layers", type=int, default=64, help="distinct weights per step")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--layers", type=int, default=None, help="layers per step (default: the workload's)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -180,25 +252,33 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json hbm_gbs)"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback 6.8 TB/s"}
+        return {"hbm_gbs": float(d["hbm_gbs"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained") or d["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS,
+            "source": "fallback (6.8 TB/s, 1.7 PFLOP/s bf16 sustained)"}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(w: Workload) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
+    for name in w.sources + COMMON_SOURCES:
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic():
+def profile_path(w: Workload):
+    return os.path.join(ROOT, "profiles", w.profile) if w.profile else None
+
+
+def profiled_traffic(w: Workload, path: str | None = None):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
     sources have not changed since it was captured."""
-    if not os.path.exists(PROFILE_SUMMARY):
-        return None, "no ncu summary committed"
+    path = path or profile_path(w)
+    if not path or not os.path.exists(path):
+        return None, "no ncu traffic record committed for this kernel"
     fields = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and not line.lstrip().startswith("#"):
                 k, v = line.split(":", 1)
@@ -207,44 +287,101 @@ def profiled_traffic():
         traffic = int(float(fields["dram_bytes_per_launch"]))
     except (KeyError, ValueError):
         return None, "ncu summary has no dram_bytes_per_launch"
-    if fields.get("kernel_source_sha256") != kernel_source_hash():
+    if fields.get("kernel_source_sha256") != kernel_source_hash(w):
         return None, "kernel changed since the ncu capture"
     return traffic, "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"
 
 
-def make_workload(layers: int, seed: int = 0):
+class Plan:
+    """The launches of one step: per layer, one C-ABI call per matrix, each
+    with its own weight, activation and output buffers."""
+
+    def __init__(self, w: Workload, layers: int):
+        self.w, self.layers, self.T = w, layers, w.tokens
+        self.launches = []  # (K, N, w_off, x_off, y_off, mat index)
+        wo = xo = yo = 0
+        for _ in range(layers):
+            for m, (K, N) in enumerate(w.mats):
+                self.launches.append((K, N, wo, xo, yo, m))
+                wo += -(-weight_bytes(w.kind, K, N) // 256) * 256
+                xo += self.T * K
+                yo += self.T * N
+        self.w_total, self.x_total, self.y_total = wo, xo, yo
+        self.weight_bytes = sum(weight_bytes(w.kind, K, N) for K, N, *_ in self.launches)
+        self.alg_bytes = sum(weight_bytes(w.kind, K, N) + 4 * self.T * (K + N)
+                             for K, N, *_ in self.launches)
+        self.flops = sum(2.0 * K * N * self.T for K, N, *_ in self.launches)
+
+    def per_step(self) -> float:
+        """The metric's numerator for one step."""
+        return self.weight_bytes / 1e9 if self.w.unit == "GB/s" else self.flops / 1e12
+
+
+def host_inputs(w: Workload, seed: int = 0):
+    """Per matrix: `distinct` host weights, one activation [T, K] and (ternary) a scale."""
     import synth
     g = synth.rng(seed)
-    W = synth.q4k_weights(g, N_DIM * layers, K_DIM)       # layer l = rows [l·N, (l+1)·N)
-    x = synth.activations(g, layers, K_DIM)               # layer l reads row l
-    return W, x
+    mats = []
+    for K, N in w.mats:
+        n = max(1, w.distinct)
+        if w.kind == "q4k":
+            Ws = [synth.q4k_weights(g, N, K) for _ in range(n)]
+        else:
+            Ws = [synth.ternary_weights(g, N, K) for _ in range(n)]
+        scale = float(synth.ternary_scale(g)) if w.kind == "ternary" else 1.0
+        x = synth.activations(g, w.tokens, K)
+        mats.append((Ws, x, scale))
+    return mats
 
 
-def workload_config(layers: int) -> dict:
-    return {"workload": f"Q4_K decode GEMV K=4096 N=4096 T=1, {layers} distinct weights per step",
-            "inputDim": K_DIM, "outputDim": N_DIM, "tokens": TOKENS, "layers_per_step": layers,
-            "weight_bytes_per_gemv": WEIGHT_BYTES,
-            "l2": f"inputs larger than L2: {layers * WEIGHT_BYTES / 1e6:.0f} MB of weights per step",
-            "weights": "random Q4_K blocks, seed 0 (synth.q4k_weights)",
+def workload_config(w: Workload, plan: Plan) -> dict:
+    return {"workload": w.name, "entry": w.entry, "format": w.kind,
+            "matrices_per_layer": [{"inputDim": K, "outputDim": N} for K, N in w.mats],
+            "tokens": w.tokens, "layers_per_step": plan.layers, "launches_per_step": len(plan.launches),
+            "weight_bytes_per_step": plan.weight_bytes,
+            "l2": f"inputs larger than L2: {plan.weight_bytes / 1e6:.0f} MB of weights per step "
+                  f"(L2 129 MB), no flush",
+            "weights": f"random {'Q4_K blocks' if w.kind == 'q4k' else 'ternary codes'}, seed 0 "
+                       f"(synth), {w.distinct} distinct host copies per matrix",
             "activations": "fp32 N(0,1), seed 0"}
 
 
-def cpu_baseline(W, x, layers: int, budget_s: float, rows_per_sample: int | None = None) -> dict:
+def oracle_call(w: Workload, K, N, W, x, scale, rows, r0=0):
+    import oracle
+    if w.kind == "q4k":
+        oracle.q4k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
+    else:
+        oracle.ternary_gemv(x, W.reshape(N, -1)[r0:r0 + rows], scale, K, rows)
+
+
+def oracle_rows(w: Workload) -> int:
+    """Output rows per oracle call: about 0.1–0.5 s of CPU work each."""
+    K, N = w.mats[0]
+    return max(8, min(N, int(4e8 // (K * w.tokens))))
+
+
+def oracle_unit_value(w: Workload, K, rows, calls, elapsed) -> float:
+    if w.unit == "GB/s":
+        return calls * weight_bytes(w.kind, K, rows) / elapsed / 1e9
+    return calls * 2.0 * K * rows * w.tokens / elapsed / 1e12
+
+
+def cpu_baseline(w: Workload, mats, budget_s: float) -> dict:
     import oracle
     threads = oracle.max_threads()
-    n_done, elapsed, l = 0, 0.0, 0
-    rows = rows_per_sample or N_DIM
+    K, N = w.mats[0]
+    Ws, x, scale = mats[0]
+    rows = oracle_rows(w)
+    n_done, elapsed = 0, 0.0
     t0 = time.perf_counter()
     while elapsed < budget_s or n_done == 0:
-        Wl = W[l * N_DIM:l * N_DIM + rows]
-        oracle.q4k_matmul(x[l:l + 1], Wl, K_DIM, rows)
+        oracle_call(w, K, N, Ws[n_done % len(Ws)], x, scale, rows, (n_done * rows) % (N - rows + 1))
         n_done += 1
-        l = (l + 1) % layers
         elapsed = time.perf_counter() - t0
-    gbs = n_done * rows * Q4K_ROW_BYTES / elapsed / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_done} one-token GEMVs of {rows}x4096 rows of the step's weights "
-                      f"({elapsed:.1f} s), C oracle: fp64 dequantize-then-matmul, OpenMP over rows"}
+    return {"value": oracle_unit_value(w, K, rows, n_done, elapsed), "unit": w.unit, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n_done} calls of {w.tokens} token(s) x {K} -> {rows} rows of the workload's "
+                      f"first matrix ({elapsed:.1f} s); C oracle, fp64, OpenMP over rows"}
 
 
 # ----------------------------------------------------------------------------
@@ -256,16 +393,18 @@ def run_reference(a) -> None:
     if rank != 0:
         return
     import oracle
-    rows = 512  # each step: 512 output rows of one 4096×4096 layer (1.18 MB of weights)
-    layers = min(a.layers, 4)
-    W, x = make_workload(layers)
+    w = WORKLOADS[a.workload]
+    w = dataclasses.replace(w, distinct=min(w.distinct, 2))
+    plan = Plan(w, a.layers or w.layers)
+    mats = host_inputs(w)
     oracle.build()
     threads = oracle.max_threads()
+    K, N = w.mats[0]
+    rows = oracle_rows(w)
 
     def step(i):
-        l = i % layers
-        r0 = (i // layers * rows) % N_DIM
-        oracle.q4k_matmul(x[l:l + 1], W[l * N_DIM + r0:l * N_DIM + r0 + rows], K_DIM, rows)
+        Ws, x, scale = mats[0]
+        oracle_call(w, K, N, Ws[i % len(Ws)], x, scale, rows, (i * rows) % (N - rows + 1))
 
     for i in range(a.warmup):
         step(i)
@@ -273,18 +412,17 @@ def run_reference(a) -> None:
     for i in range(a.steps):
         step(a.warmup + i)
     elapsed = time.perf_counter() - t0
-    gbs = a.steps * rows * Q4K_ROW_BYTES / elapsed / 1e9
-    sample = (f"each step: one-token GEMV over {rows} of the 4096 rows of a 4096x4096 Q4_K weight "
-              f"(C oracle, fp64, OpenMP over rows)")
-    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
+    value = oracle_unit_value(w, K, rows, a.steps, elapsed)
+    sample = (f"each step: {w.tokens} token(s) x {K} -> {rows} of the {N} output rows of the "
+              f"workload's first matrix (C oracle, fp64, OpenMP over rows)")
+    line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": elapsed / a.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(a.layers) | {"reference_sample": f"{rows} output rows of one "
-                                                   f"of {layers} host weights per step"},
+            "config": workload_config(w, plan) | {"reference_sample": sample},
             "impl": "reference",
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": w.unit, "cores": threads, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": w.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -304,20 +442,37 @@ def run_ours(a) -> None:
 
     import quantized_matmul_q4_gb300 as q
     lib = q.library()
-
-    layers = a.layers
-    W_host, x_host = make_workload(layers, seed=0)
-    W = torch.from_numpy(W_host.reshape(-1)).to(device)
-    x = torch.from_numpy(x_host).to(device)
-    y = torch.empty((layers, N_DIM), dtype=torch.float32, device=device)
+    w = WORKLOADS[a.workload]
+    fn = getattr(lib, w.entry)
+    plan = Plan(w, a.layers or w.layers)
+    mats = host_inputs(w, seed=0)
+    W = torch.empty(plan.w_total, dtype=torch.uint8, device=device)
+    x = torch.empty(plan.x_total, dtype=torch.float32, device=device)
+    y = torch.empty(plan.y_total, dtype=torch.float32, device=device)
+    x_host = torch.empty(plan.x_total, dtype=torch.float32)
+    seen = {}
+    for li, (K, N, wo, xo, yo, m) in enumerate(plan.launches):
+        Ws, xm, _ = mats[m]
+        nb = weight_bytes(w.kind, K, N)
+        k = seen.get(m, 0)
+        seen[m] = k + 1
+        W[wo:wo + nb].copy_(torch.from_numpy(Ws[k % len(Ws)].reshape(-1)))
+        x_host[xo:xo + w.tokens * K] = torch.from_numpy(xm.reshape(-1))
+    x.copy_(x_host)
+    torch.cuda.synchronize(device)
     stream = torch.cuda.Stream(device)
     sp = stream.cuda_stream
     wp, xp, yp = W.data_ptr(), x.data_ptr(), y.data_ptr()
+    calls = []
+    for K, N, wo, xo, yo, m in plan.launches:
+        if w.kind == "q4k":
+            calls.append((xp + 4 * xo, wp + wo, yp + 4 * yo, K, N, w.tokens, sp))
+        else:
+            calls.append((xp + 4 * xo, wp + wo, mats[m][2], yp + 4 * yo, K, N, w.tokens, sp))
 
     def step_direct():
-        for l in range(layers):
-            rc = lib.q4k_matmul(xp + 4 * K_DIM * l, wp + WEIGHT_BYTES * l, yp + 4 * N_DIM * l,
-                                K_DIM, N_DIM, TOKENS, sp)
+        for c in calls:
+            rc = fn(*c)
             if rc != 0:
                 raise q.Q4mmError(rc, q.last_error())
 
@@ -362,22 +517,35 @@ def run_ours(a) -> None:
     elapsed_ms = max_over_ranks(local_ms, dist, device)
     ms_per_step = elapsed_ms / a.steps
     n_ranks = max(world, 1)
-    value = n_ranks * layers * WEIGHT_BYTES / (ms_per_step * 1e-3) / 1e9
+    value = n_ranks * plan.per_step() / (ms_per_step * 1e-3)
 
+    # Roofline of the dominant kernel, from this rank's own device time.
     peaks = measured_peaks()
-    launch_s = local_ms * 1e-3 / (a.steps * layers)
-    achieved = ALG_BYTES / launch_s / 1e9
-    traffic, traffic_note = profiled_traffic()
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "q4k_gemv_t1_kernel", "alg_bytes_per_launch": ALG_BYTES,
-                "avg_launch_us": launch_s * 1e6, "peak_source": peaks["source"],
-                "traffic_source": traffic_note}
+    step_s = local_ms * 1e-3 / a.steps
+    launch_s = step_s / len(plan.launches)
+    hbm_achieved = plan.alg_bytes / step_s / 1e9
+    traffic, traffic_note = profiled_traffic(w) if (a.layers is None or a.layers == w.layers) \
+        else (None, "non-default layer count")
+    if w.bound == "hbm":
+        roofline = {"bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": hbm_achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm_gbs"}
+    else:
+        tflops = plan.flops / step_s / 1e12
+        peak = peaks["bf16_tflops_sustained"] if w.bound == "tensor" else FP32_FMA_TFLOPS
+        src = (peaks["source"] + " bf16_tflops_sustained" if w.bound == "tensor" else
+               "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz")
+        roofline = {"bound": w.bound, "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tflops / peak, "peak_source": src,
+                    "hbm": {"achieved": hbm_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": hbm_achieved / peaks["hbm_gbs"]}}
+    roofline.update({"traffic": traffic, "kernel": w.kernel,
+                     "alg_bytes_per_launch": plan.alg_bytes / len(plan.launches),
+                     "avg_launch_us": launch_s * 1e6, "traffic_source": traffic_note})
 
     e2e = None
     if not a.no_e2e:
-        x_pin = torch.from_numpy(x_host).pin_memory()
-        y_pin = torch.empty((layers, N_DIM), dtype=torch.float32).pin_memory()
+        x_pin = x_host.pin_memory()
+        y_pin = torch.empty(plan.y_total, dtype=torch.float32).pin_memory()
         e2e_steps = max(1, min(a.steps, 300))
 
         def e2e_step():
@@ -398,27 +566,27 @@ def run_ours(a) -> None:
             f1.record(stream)
         f1.synchronize()
         e2e_ms = max_over_ranks(f0.elapsed_time(f1), dist, device) / e2e_steps
-        e2e = {"value": n_ranks * layers * WEIGHT_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": layers * K_DIM * 4, "d2h_bytes_per_step": layers * N_DIM * 4,
+        e2e = {"value": n_ranks * plan.per_step() / (e2e_ms * 1e-3), "unit": w.unit,
+               "h2d_bytes_per_step": plan.x_total * 4, "d2h_bytes_per_step": plan.y_total * 4,
                "steps": e2e_steps, "ms_per_step": e2e_ms,
-               "path": "q4k_matmul C ABI per layer, activations from pinned host memory, outputs back"}
+               "path": f"{w.entry} C ABI per matrix, activations from pinned host memory, outputs back"}
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu = cpu_baseline(W_host, x_host, layers, a.cpu_seconds)
+        cpu = cpu_baseline(w, mats, a.cpu_seconds)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n_ranks,
+        dtype = {"hbm": "i32+f32" if w.arithmetic == T1_ARITH else "f32", "tensor": "bf16",
+                 "alu": "f32"}[w.bound]
+        line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": n_ranks,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i32+f32",
-                "arithmetic": "fp32 activations split exactly (to 2^-21 of each 256-value block's "
-                              "maximum) into three int8 planes; 4-bit codes x planes in int32 dp4a; "
-                              "scales, mins and combination in fp32",
-                "data": "synthetic", "config": workload_config(layers),
-                "pct_of_hbm_peak": 100.0 * value / n_ranks / peaks["hbm_gbs"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+                "arithmetic": w.arithmetic, "data": "synthetic", "config": workload_config(w, plan),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": a.steps * layers, "clocks": clocks,
+                "gpu_launches": a.steps * len(plan.launches), "clocks": clocks,
                 "gpu": props.name}
+        if w.unit == "GB/s":
+            line["pct_of_hbm_peak"] = 100.0 * value / n_ranks / peaks["hbm_gbs"]
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -59,13 +59,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
+// Suspend-time hint of the bounded wait, in nanoseconds (0: no hint, the
+// hardware's own try_wait time limit).
+#ifndef Q4MM_WAIT_HINT_NS
+#define Q4MM_WAIT_HINT_NS 20000
+#endif
+
 // Wait for phase `parity` of `bar` to complete, giving up after about
 // `limit_cycles` SM cycles.  Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   long long limit_cycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+#if Q4MM_WAIT_HINT_NS > 0
+    while (!mbar_try_wait_sleep(bar, parity, Q4MM_WAIT_HINT_NS)) {
+#else
+    while (!mbar_try_wait(bar, parity)) {
+#endif
         if (clock64() - t0 > limit_cycles) return false;
     }
     return true;

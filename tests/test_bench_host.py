@@ -75,13 +75,51 @@ def test_warmup_minimum():
         bench.parse_args(["--warmup", "2"])
 
 
-def test_traffic_record_tracks_kernel_sources(tmp_path, monkeypatch):
+def test_traffic_record_tracks_kernel_sources(tmp_path):
     sys.path.insert(0, ROOT)
     import bench
+    w = bench.WORKLOADS[bench.DEFAULT_WORKLOAD]
     rec = tmp_path / "summary.md"
-    rec.write_text(f"kernel_source_sha256: {bench.kernel_source_hash()}\n"
+    rec.write_text(f"kernel_source_sha256: {bench.kernel_source_hash(w)}\n"
                    "dram_bytes_per_launch: 9500000\n")
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(rec))
-    assert bench.profiled_traffic()[0] == 9500000
+    assert bench.profiled_traffic(w, str(rec))[0] == 9500000
     rec.write_text("kernel_source_sha256: 0000\ndram_bytes_per_launch: 9500000\n")
-    assert bench.profiled_traffic()[0] is None
+    assert bench.profiled_traffic(w, str(rec))[0] is None
+
+
+def test_workload_plans():
+    # Every workload's step is larger than the 129 MB L2, and its byte and
+    # flop counts follow the formats' sizes.
+    sys.path.insert(0, ROOT)
+    import bench
+    for name, w in bench.WORKLOADS.items():
+        plan = bench.Plan(w, w.layers)
+        assert plan.weight_bytes > 2 * 129e6, name
+        assert len(plan.launches) == w.layers * len(w.mats)
+        for K, N, wo, xo, yo, m in plan.launches:
+            assert wo % 256 == 0 and (K, N) == w.mats[m]
+    w = bench.WORKLOADS["q4k_gemv_4096x4096_t1"]
+    plan = bench.Plan(w, 64)
+    assert plan.weight_bytes == 64 * 9437184
+    assert plan.alg_bytes == 64 * (9437184 + 4 * 4096 + 4 * 4096)
+    t = bench.Plan(bench.WORKLOADS["ternary_gemv_2560x6912_t16"], 1)
+    assert t.weight_bytes == 6912 * 640 and t.flops == 2.0 * 2560 * 6912 * 16
+    llama = bench.Plan(bench.WORKLOADS["llama7b_decode_t1"], 32)
+    assert llama.weight_bytes == 32 * 113836032
+
+
+@pytest.mark.parametrize("workload", ["ternary_gemv_2560x6912_t16", "q4k_prefill_tc_4096x11008_t64"])
+def test_reference_arm_other_workloads(workload):
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", workload, "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["config"]["workload"] == workload and line["value"] > 0
+    assert line["unit"] == bench_unit(workload)
+
+
+def bench_unit(workload):
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench.WORKLOADS[workload].unit

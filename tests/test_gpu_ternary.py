@@ -46,6 +46,13 @@ def test_workload_normal(T):
 
 ODD = [(4, 1, 1), (8, 3, 2), (12, 5, 1), (100, 33, 3), (2564, 7, 1), (4100, 9, 9), (64, 1000, 1),
        (8192, 65, 17), (6000, 13, 8), (16, 2, 4)]
+# Shapes for the streamed kernels (K % 64 == 0, 16-byte aligned weights):
+# one token with 1..15 word columns and ragged row counts, the tile kernel
+# with 2..8-token tiles, ragged token groups, several K chunks, and K beyond
+# the one-token kernel's 15 columns.
+STREAMED = [(64, 1, 1), (128, 48, 2), (2560, 100, 3), (6400, 37, 5), (7680, 20, 1), (7744, 3, 1),
+            (2560, 6913, 1), (1024, 4097, 16), (256, 1, 8), (65536, 2, 1), (65536, 3, 9),
+            (4096, 300, 12), (512, 152 * 8 + 5, 1), (2560, 49, 7)]
 
 
 @pytest.mark.parametrize("K,N,T", ODD, ids=[f"K{k}_N{n}_T{t}" for k, n, t in ODD])
@@ -57,21 +64,38 @@ def test_odd_shapes_and_unaligned_weights(K, N, T, offset):
     assert y.tobytes() == y_ref.tobytes()
 
 
+@pytest.mark.parametrize("K,N,T", STREAMED, ids=[f"K{k}_N{n}_T{t}" for k, n, t in STREAMED])
+def test_streamed_shapes_integer_bit_exact(K, N, T):
+    x, W, scale, K, N, T = synth.ternary_case((K, N, T), seed=3 * K + N + T, xkind="int")
+    dot, y_ref = oracle.ternary_gemv(x, W, scale, K, N)
+    assert np.array_equal(ternary(x, W, 1.0, K, N).astype(np.float64), dot)
+    assert ternary(x, W, scale, K, N).tobytes() == y_ref.tobytes()
+
+
+@pytest.mark.parametrize("K,N,T", STREAMED[:8], ids=[f"K{k}_N{n}_T{t}" for k, n, t in STREAMED[:8]])
+def test_streamed_shapes_normal(K, N, T):
+    x, W, scale, K, N, T = synth.ternary_case((K, N, T), seed=5 * K + N + T)
+    dot, _ = oracle.ternary_gemv(x, W, scale, K, N)
+    assert_rows_close(ternary(x, W, scale, K, N), dot * np.float64(scale), REL, f"K{K} N{N} T{T}")
+
+
 def test_field_value_three_decodes_to_plus_two():
     # The literal formula maps bits 11 to +2; both sides decode it that way.
     K, N = 64, 3
     W = np.full((N, K // 4), 0xFF, np.uint8)
     W[1] = 0xAA  # all fields 2 → +1
     W[2] = 0x00  # all fields 0 → −1
-    x = synth.activations(synth.rng(1), 2, K, "int")
-    dot, y_ref = oracle.ternary_gemv(x, W, 1.0, K, N)
-    y = ternary(x, W, 1.0, K, N)
-    assert y.tobytes() == y_ref.tobytes()
-    assert np.array_equal(dot[:, 0], 2 * x.astype(np.float64).sum(1))
+    for T in (1, 2, 9):  # the one-token, tile and fallback kernels
+        x = synth.activations(synth.rng(1), T, K, "int")
+        dot, y_ref = oracle.ternary_gemv(x, W, 1.0, K, N)
+        y = ternary(x, W, 1.0, K, N)
+        assert y.tobytes() == y_ref.tobytes()
+        assert np.array_equal(dot[:, 0], 2 * x.astype(np.float64).sum(1))
 
 
-def test_run_to_run_bit_identity():
-    x, W, scale, K, N, T = synth.ternary_case((2560, 6912, 16))
+@pytest.mark.parametrize("T", [1, 16])
+def test_run_to_run_bit_identity(T):
+    x, W, scale, K, N, T = synth.ternary_case((2560, 6912, T))
     a = ternary(x, W, scale, K, N)
     b = ternary(x, W, scale, K, N)
     assert a.tobytes() == b.tobytes()
