@@ -58,41 +58,6 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
     return r;
 }
 
-// Σ x·(0.5 + q/256) over the 32 low-nibble and the 32 high-nibble weights of a
-// 32-byte slab (q0 = bytes 0..15, q1 = bytes 16..31), x from registers:
-// xs[l] pairs with the low nibble of slab byte l, xs[32 + l] with its high
-// nibble.  Two accumulator pairs per half keep the dependent chains short.
-__device__ __forceinline__ void slab_dot(const float (&xs)[64], uint4 q0, uint4 q1, float &lo,
-                                         float &hi) {
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float2 alo[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float2 ahi[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
-        // (q >> 4) via a multiply-high, which issues on the FMA pipe and so
-        // leaves the integer pipe to the byte permutes.
-        const uint32_t h4 = __umulhi(qw[w], 1u << 28) & 0x0F0F0F0Fu;
-        float2 &al = alo[w & 1], &ah = ahi[w & 1];
-        al = ffma2(make_float2(xs[4 * w], xs[4 * w + 1]),
-                   make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), al);
-        al = ffma2(make_float2(xs[4 * w + 2], xs[4 * w + 3]),
-                   make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), al);
-        ah = ffma2(make_float2(xs[32 + 4 * w], xs[32 + 4 * w + 1]),
-                   make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), ah);
-        ah = ffma2(make_float2(xs[32 + 4 * w + 2], xs[32 + 4 * w + 3]),
-                   make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), ah);
-    }
-    lo = (alo[0].x + alo[1].x) + (alo[0].y + alo[1].y);
-    hi = (ahi[0].x + ahi[1].x) + (ahi[0].y + ahi[1].y);
-}
-
-// x in shared memory: 16-byte unit u (elements 4u..4u+3) is stored at unit
-// u ^ ((u >> 4) & 7), so the eight slab lanes of a quarter warp, which read
-// the same unit offset of eight consecutive 64-element slabs, hit eight
-// different bank groups.
-__device__ __forceinline__ int x_swz(int u) { return u ^ ((u >> 4) & 7); }
-
 // ----------------------------------------------------------------------------
 // One token: bulk-copied rows, slab lanes, exact int8 activation planes
 // ----------------------------------------------------------------------------
@@ -459,115 +424,179 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
 }
 
 // ----------------------------------------------------------------------------
-// 1..8 tokens: x staged in shared memory by K-chunks, weights by plain loads
+// 2..8 tokens: bulk-copied row groups, word lanes, register tiles
 // ----------------------------------------------------------------------------
+//
+// A CTA owns a contiguous range of rows in groups of four; one producer
+// thread streams each group (four whole rows) into its own ring slot with a
+// bulk copy, before the wait on the previous kernel.  Compute warp c takes
+// groups c, c + kMultiCw, …, and for each group walks all blocks of the rows:
+// lane l owns qs word l of every block — 4 low-nibble weights of sub-block
+// 2j and 4 high-nibble weights of 2j+1 (j = l/8) — with the 8 matching
+// activations of all TT tokens loaded once per block and reused by the four
+// rows.  Each weight is dequantized once (scale'·(0.5 + q/256) − offset') and
+// multiplied into TT token accumulators, two positions per paired FMA.  A
+// butterfly over the 4·TT sums at the end of the group finishes the rows.
 
-constexpr int kMultiWarps = 8;
-constexpr int kMultiChunkBlocks = 8;  // blocks per K-chunk: one warp spans a row-chunk
+constexpr int kMultiWarps = 8;                    // copy warp + 7 compute warps
+constexpr int kMultiCw = kMultiWarps - 1;
+constexpr int kMultiRows = 4;                     // rows per group (one ring slot)
 
 struct MultiParams {
     const float *x;
     const uint8_t *W;
     float *y;
-    int K, N;
+    int *status;
+    int K, N, T;       // T: tokens of this launch (<= TT)
     int nb;            // blocks per row
-    int chunk_blocks;  // blocks per K-chunk (<= 8)
-    int lpr;           // lanes per row-chunk (power of two, >= 4·chunk_blocks)
-    int rows_per_cta;
+    int rows_per_cta;  // multiple of kMultiRows
+    int nslots;        // ring depth (groups in flight)
 };
 
-template <int T>
-__global__ void __launch_bounds__(32 * kMultiWarps) q4k_gemv_multi_kernel(MultiParams p) {
-    extern __shared__ __align__(16) float msm[];
-    float *xsm = msm;                                         // [T][chunk·256] swizzled
-    float *acc = msm + T * p.chunk_blocks * kQ4kValues;       // [rows_per_cta][T]
-
+template <int TT>
+__global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(MultiParams p) {
+    extern __shared__ __align__(128) uint8_t msmem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rpp = 32 / p.lpr;
-    const int ro = lane / p.lpr, s = lane % p.lpr;
+    const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
+    const uint32_t slot_bytes = kMultiRows * row_bytes;
+    uint8_t *ring = msmem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
+    uint64_t *empty = full + p.nslots;
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
-    const size_t row_bytes = (size_t)p.nb * kQ4kBytes;
-    const int chunk_elems = p.chunk_blocks * kQ4kValues;
+    const int ngroups = (nrows + kMultiRows - 1) / kMultiRows;
 
-    pdl_launch_dependents();
-    pdl_wait();
-    for (int i = threadIdx.x; i < nrows * T; i += blockDim.x) acc[i] = 0.f;
-
-    for (int c0 = 0; c0 < p.nb; c0 += p.chunk_blocks) {
-        const int cb = min(p.chunk_blocks, p.nb - c0);
-        __syncthreads();  // previous chunk's x no longer in use; acc zeroed
-        // Four loads in flight per thread before their stores.
-        const int total = T * cb * 64;
-        for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
-            float4 v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = i0 + k * blockDim.x;
-                const int t = i / (cb * 64), u = i % (cb * 64);
-                v[k] = i < total ? __ldg(reinterpret_cast<const float4 *>(
-                                             p.x + (size_t)t * p.K + c0 * kQ4kValues) + u)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = i0 + k * blockDim.x;
-                const int t = i / (cb * 64), u = i % (cb * 64);
-                if (i < total) reinterpret_cast<float4 *>(xsm + t * chunk_elems)[x_swz(u)] = v[k];
-            }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.nslots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
-        __syncthreads();
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
 
-        const bool active = s < 4 * cb;
-        const int b = active ? (s >> 2) : 0, j = s & 3;
-        const int u0 = (b * kQ4kValues + j * 64) / 4;
-        for (int pass = warp; pass * rpp < nrows; pass += kMultiWarps) {
-            const int rl = pass * rpp + ro;
-            float2 a[T];
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int g = 0; g < ngroups; ++g, ++issued) {
+                const int slot = g % p.nslots;
+                if (g >= p.nslots &&
+                    !mbar_wait_bounded(&empty[slot], ((g / p.nslots) - 1) & 1, kWaitLimitCycles)) {
+                    flag_timeout(p.status);
+                    break;
+                }
+                const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+                bulk_g2s(ring + (size_t)slot * slot_bytes,
+                         p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes, &full[slot]);
+            }
+            // Never leave a copy writing into an exiting CTA.
+            for (int g = max(0, issued - p.nslots); g < issued; ++g)
+                (void)mbar_wait_bounded(&full[g % p.nslots], (g / p.nslots) & 1, kWaitLimitCycles);
+        }
+        __syncwarp();
+        return;
+    }
+
+    const int cw = warp - 1;
+    const int j = lane >> 3, wq = lane & 7;   // slab and word within it
+    // x may be produced by the previous kernel on the stream.
+    pdl_wait();
+    for (int g = cw; g < ngroups; g += kMultiCw) {
+        const int slot = g % p.nslots;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (g / p.nslots) & 1, kWaitLimitCycles))) {
+            flag_timeout(p.status);
+            break;
+        }
+        const uint8_t *grp = ring + (size_t)slot * slot_bytes;
+        const int rows = min(kMultiRows, nrows - g * kMultiRows);
+        float2 acc[kMultiRows][TT];
 #pragma unroll
-            for (int t = 0; t < T; ++t) a[t] = make_float2(0.f, 0.f);
-            if (active && rl < nrows) {
-                const uint8_t *blk =
-                    p.W + (size_t)(row0 + rl) * row_bytes + (size_t)(c0 + b) * kQ4kBytes;
-                const uint4 hdr = ld_stream_u4(blk);
-                const uint4 q0 = ld_stream_u4(blk + 16 + 32 * j);
-                const uint4 q1 = ld_stream_u4(blk + 32 + 32 * j);
-                const SlabScales sc = slab_scales(hdr, j);
-                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        for (int r = 0; r < kMultiRows; ++r)
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
-                    const uint32_t h4 = (qw[w] >> 4) & 0x0F0F0F0Fu;
-                    // Dequantized weights: scale'·(0.5 + q/256) − offset' = d·sc·q − dmin·m.
-                    const float2 s0 = make_float2(sc.s0, sc.s0), n0 = make_float2(-sc.o0, -sc.o0);
-                    const float2 s1 = make_float2(sc.s1, sc.s1), n1 = make_float2(-sc.o1, -sc.o1);
-                    const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
-                    const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
-                    const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
-                    const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+            for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+
+        for (int b = 0; b < p.nb; ++b) {
+            // Activations of this lane's 8 positions for every token.
+            float4 xl[TT], xh[TT];
+            const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
 #pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        const float4 *xt = reinterpret_cast<const float4 *>(xsm + t * chunk_elems);
-                        const float4 xl = xt[x_swz(u0 + w)];
-                        const float4 xh = xt[x_swz(u0 + 8 + w)];
-                        a[t] = ffma2(make_float2(xl.x, xl.y), wl01, a[t]);
-                        a[t] = ffma2(make_float2(xl.z, xl.w), wl23, a[t]);
-                        a[t] = ffma2(make_float2(xh.x, xh.y), wh01, a[t]);
-                        a[t] = ffma2(make_float2(xh.z, xh.w), wh23, a[t]);
-                    }
+            for (int t = 0; t < TT; ++t) {
+                if (t < p.T) {
+                    const float *xt = p.x + (size_t)t * p.K + k0;
+                    xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
+                    xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                } else {
+                    xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    xh[t] = xl[t];
                 }
             }
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
-                const float v = group_sum(a[t].x + a[t].y, p.lpr);
-                if (s == 0 && rl < nrows) acc[rl * T + t] += v;
+            for (int r = 0; r < kMultiRows; ++r) {
+                // Absent rows of a short last group read row 0 of the slot;
+                // their sums are never stored.
+                const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+                const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
+                const SlabScales sc = slab_scales(hdr, j);
+                const uint32_t l4 = q & 0x0F0F0F0Fu;
+                const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
+                const float2 s0 = make_float2(sc.s0, sc.s0), n0 = make_float2(-sc.o0, -sc.o0);
+                const float2 s1 = make_float2(sc.s1, sc.s1), n1 = make_float2(-sc.o1, -sc.o1);
+                const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
+                const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
+                const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
+                const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                }
             }
         }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nrows * T; i += blockDim.x) {
-        const int rl = i / T, t = i % T;
-        p.y[(size_t)t * p.N + row0 + rl] = acc[i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+
+        // Butterfly over the 4·TT sums: afterwards lane l holds value index
+        // idx .. idx + n − 1 (see the halving below), summed over the warp.
+        constexpr int V = kMultiRows * TT;
+        float v[V];
+#pragma unroll
+        for (int r = 0; r < kMultiRows; ++r)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t].x + acc[r][t].y;
+        int idx = 0, n = V;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            if (n > 1) {
+                const int half = n >> 1;
+                const bool up = lane & o;
+#pragma unroll
+                for (int i = 0; i < V / 2; ++i) {
+                    if (i < half) {
+                        const float send = up ? v[i] : v[i + half];
+                        const float keep = up ? v[i + half] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                if (up) idx += half;
+                n = half;
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+            }
+        }
+        const bool writer = V >= 32 || (lane & (32 / V - 1)) == 0;
+        if (writer) {
+#pragma unroll
+            for (int i = 0; i < (V >= 32 ? V / 32 : 1); ++i) {
+                const int id = idx + i;
+                const int r = id / TT, t = id % TT;
+                if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = v[i];
+            }
+        }
     }
 }
 
@@ -672,38 +701,36 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.x = x;
     p.W = W;
     p.y = y;
+    p.status = c.status;
     p.K = K;
     p.N = N;
+    p.T = T;
     p.nb = K / kQ4kValues;
-    p.chunk_blocks = min(kMultiChunkBlocks, p.nb);
-    p.lpr = next_pow2(4 * p.chunk_blocks);
-    int grid = 2 * c.num_sms;
-    p.rows_per_cta = (N + grid - 1) / grid;
+    const size_t row_bytes = (size_t)p.nb * kQ4kBytes;
+    const size_t slot_bytes = kMultiRows * row_bytes;
+    const int groups = (N + kMultiRows - 1) / kMultiRows;
+    int grid = min(c.num_sms, groups);
+    p.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
-    const size_t smem =
-        (size_t)T * p.chunk_blocks * kQ4kValues * sizeof(float) + (size_t)p.rows_per_cta * T * sizeof(float);
+    const int cta_groups = p.rows_per_cta / kMultiRows;
+    // Ring: up to 200 KB, at least two slots, never more slots than groups.
+    p.nslots = (int)min((size_t)min(cta_groups, 16), max((size_t)2, (size_t)(200 * 1024) / slot_bytes));
+    p.nslots = max(p.nslots, min(cta_groups, 2));
+    const size_t smem = (size_t)p.nslots * slot_bytes + 2 * (size_t)p.nslots * sizeof(uint64_t);
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
 
 #define Q4MM_MULTI_CASE(TT)                                                                    \
-    case TT: {                                                                                 \
-        cudaError_t e = ensure_smem(q4k_gemv_multi_kernel<TT>, smem);                                       \
+    {                                                                                          \
+        cudaError_t e = ensure_smem(q4k_gemv_multi_kernel<TT>, smem);                          \
         if (e != cudaSuccess) return e;                                                        \
         return launch_kernel(c, q4k_gemv_multi_kernel<TT>, dim3(grid), dim3(32 * kMultiWarps), \
                              smem, p);                                                         \
     }
-    switch (T) {
-        Q4MM_MULTI_CASE(1)
-        Q4MM_MULTI_CASE(2)
-        Q4MM_MULTI_CASE(3)
-        Q4MM_MULTI_CASE(4)
-        Q4MM_MULTI_CASE(5)
-        Q4MM_MULTI_CASE(6)
-        Q4MM_MULTI_CASE(7)
-        Q4MM_MULTI_CASE(8)
-        default:
-            return cudaErrorInvalidValue;
-    }
+    if (T <= 2) Q4MM_MULTI_CASE(2)
+    if (T <= 4) Q4MM_MULTI_CASE(4)
+    if (T <= 8) Q4MM_MULTI_CASE(8)
 #undef Q4MM_MULTI_CASE
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace q4mm
