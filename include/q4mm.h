@@ -83,14 +83,21 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
 
 /*
  * q4k_matmul_tc — the same product on the tensor cores (tcgen05), for
- * prefill-sized token counts.  The dequantized weight and the activation are
- * rounded to bfloat16 before the multiply; products are accumulated in FP32
- * (tensor memory).  Same layouts, alignment and limits as q4k_matmul.
+ * prefill-sized token counts.  The dequantized weight (computed in fp32 and
+ * rounded once) and the activation are rounded to bfloat16 before the
+ * multiply; products are accumulated in FP32 (tensor memory).  Same layouts,
+ * alignment and limits as q4k_matmul.
  * Precision: per token row, max_o |y − y_bf16| <= 1e-4 · max_o |y_bf16| where
- * y_bf16 is the exact product of the bf16-rounded operands, and
- * max_o |y − y_exact| <= 1e-2 · max_o |y_exact|.
- * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.  A bounded wait
- * that runs out sets the device status word (see q4mm_device_status).
+ * y_bf16 is the exact product of the bf16-rounded operands; the deviation
+ * from the exact product is that of bf16 operand rounding (about 5e-3 of
+ * max_o |y_exact| on random data).
+ * Memory: each call takes 2·tokens·inputDim bytes of stream-ordered scratch
+ * (cudaMallocAsync on `stream`, freed on `stream` before the call returns
+ * control to the stream) for the bf16 copy of x; the weights are read once
+ * per 64 tokens.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA} (CUDA also when the
+ * scratch allocation fails).  A bounded wait that runs out sets the device
+ * status word (see q4mm_device_status).
  */
 int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
                   int tokens, q4mm_stream_t stream);

@@ -9,20 +9,30 @@
 //   D = fp32 in tensor memory, K = 16 per MMA instruction.
 // Every weight byte is read once per call for up to 64 tokens.
 //
-// Roles in a CTA:
+// Before the main kernel, a small kernel rounds x to bf16 once into a
+// stream-ordered scratch buffer (2·T·K bytes, allocated and freed on the
+// call's stream); the main kernel then loads activation tiles by TMA with the
+// hardware 128-byte swizzle, already in the layout the MMA reads.
+//
+// Roles in a CTA of the main kernel:
 //  * warp 8 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
-//    (128 rows × 144 bytes) per 256 values of K, and a 64-wide fp32 tile of x
-//    per 64 values of K.  Weights go first, before the wait on the previous
-//    kernel; x only after it.
-//  * warps 0–7 (two threads per weight row) dequantize each 64-value chunk of
-//    their row into bf16 and convert the matching x tile to bf16, both written
-//    in the 128-byte-swizzled K-major layout the MMA reads, then fence the
-//    writes to the async proxy and arrive on the chunk's barrier.
+//    (128 rows × 144 bytes) per 256 values of K, before the wait on the
+//    previous kernel, and a bf16 activation tile (TP tokens × 64 values) per
+//    chunk of 64 values, after it, each as soon as its ring slot is free.
+//  * warps 0–7 dequantize: thread (r, h), r = t mod 128 and h = t / 128, turns
+//    qs bytes 16h..16h+15 of row r's slab into 16 low-nibble values of
+//    sub-block 2j and 16 high-nibble values of 2j+1.  Each nibble becomes a
+//    float with one logic op (2^23 + q·2^p), one paired FMA with the scale at
+//    2^-p and −scale·2^(23−p) gives scale·q exactly, one paired add removes
+//    the min term (the single rounding of the fp32 dequantization), and one
+//    conversion packs two bf16.  Results go in the 128-byte-swizzled K-major
+//    layout; the writes are fenced to the async proxy before the chunk's
+//    barrier arrive.
 //  * warp 9 allocates two accumulators in tensor memory; its first thread
-//    issues four 128×N×16 MMAs per chunk and commits them to the chunk's
-//    "empty" barrier.  K is cut into segments of 2048: each segment starts
-//    from zero in the accumulator the previous-but-one segment used, and its
-//    completion is committed to that accumulator's barrier.
+//    issues four 128×TP×16 MMAs per chunk and commits them to the chunk's
+//    weight and activation slots.  K is cut into segments of 2048: each
+//    segment starts from zero in the accumulator the previous-but-one segment
+//    used, and its completion is committed to that accumulator's barrier.
 //  * warps 0–7 fold each finished segment into fp32 registers (tcgen05.ld
 //    plus an add) a few chunks after it ends, and finally write y.  Short
 //    accumulation chains in the tensor core keep the error of its fp32
@@ -52,24 +62,22 @@ constexpr int kTcWarpMma = kTcDqWarps + 1;         // MMA issuer warp
 constexpr int kTcThreads = 32 * (kTcDqWarps + 2);
 constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads
 constexpr int kTcWStages = 3;                      // Q4_K block-column tiles in flight
-constexpr int kTcXStages = 2;                      // fp32 activation tiles in flight
-constexpr int kTcABStages = 4;                     // bf16 operand tiles in flight
+constexpr int kTcAStages = 4;                      // bf16 weight operand tiles in flight
+constexpr int kTcBStages = 12;                     // bf16 activation tiles in flight
 constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 18432
 constexpr int kTcMaxTokens = 64;                   // tokens per launch tile
 constexpr int kTcSegChunks = 32;                   // chunks per accumulation segment (K = 2048)
-static_assert(kTcSegChunks > kTcABStages, "a segment is drained kTcABStages chunks after it ends");
+static_assert(kTcSegChunks > kTcAStages, "a segment is drained kTcAStages chunks after it ends");
 
 template <int TP>
 struct TcLayout {
     static constexpr uint32_t a_bytes = kTcRows * 128;
     static constexpr uint32_t b_bytes = TP * 128;
-    static constexpr uint32_t x_bytes = TP * kTcKc * 4;
     static constexpr uint32_t off_a = 0;
-    static constexpr uint32_t off_b = off_a + kTcABStages * a_bytes;
-    static constexpr uint32_t off_w = off_b + kTcABStages * b_bytes;
-    static constexpr uint32_t off_x = off_w + kTcWStages * kTcWTileBytes;
-    static constexpr uint32_t off_bar = off_x + kTcXStages * x_bytes;
-    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcXStages + 2 * kTcABStages + 4 + 1;
+    static constexpr uint32_t off_b = off_a + kTcAStages * a_bytes;
+    static constexpr uint32_t off_w = off_b + kTcBStages * b_bytes;
+    static constexpr uint32_t off_bar = off_w + kTcWStages * kTcWTileBytes;
+    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcAStages + 2 * kTcBStages + 4 + 1;
     static constexpr uint32_t off_misc = off_bar + 8 * n_bars;
     static constexpr uint32_t total = off_misc + 16;
     static_assert(off_b % 1024 == 0 && off_w % 1024 == 0, "operand tiles must be 1024-byte aligned");
@@ -147,14 +155,96 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 2^23 + (w & mask) as a float: the masked nibble sits in the mantissa.
+__device__ __forceinline__ float magic(uint32_t w, uint32_t mask) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, 0x4B000000, 0xEA;" : "=r"(r) : "r"(w), "r"(mask));  // (a & b) | c
+    return __uint_as_float(r);
+}
+
+// Per sub-block constants: for a nibble at bit p of its word, built as
+// f = 2^23 + q·2^p, fma(s·2^-p, f, −s·2^(23−p)) = s·q exactly, then − o.
+struct NibScale {
+    float2 s01, c01, s23, c23, no;
+};
+
+// Low nibbles: bytes 0,1 at bits 0 and 8; bytes 2,3 at bit 16 (byte 3 after
+// a shift by 8).  High nibbles: bytes 0,1 at bits 4 and 12; bytes 2,3 at bit
+// 12 (after shifts by 8 and 16).
+__device__ __forceinline__ NibScale nib_scale_lo(float s, float o) {
+    NibScale r;
+    r.s01 = make_float2(s, s * 0x1p-8f);
+    r.c01 = make_float2(s * -0x1p23f, s * -0x1p15f);
+    r.s23 = make_float2(s * 0x1p-16f, s * 0x1p-16f);
+    r.c23 = make_float2(s * -0x1p7f, s * -0x1p7f);
+    r.no = make_float2(-o, -o);
+    return r;
+}
+__device__ __forceinline__ NibScale nib_scale_hi(float s, float o) {
+    NibScale r;
+    r.s01 = make_float2(s * 0x1p-4f, s * 0x1p-12f);
+    r.c01 = make_float2(s * -0x1p19f, s * -0x1p11f);
+    r.s23 = make_float2(s * 0x1p-12f, s * 0x1p-12f);
+    r.c23 = make_float2(s * -0x1p11f, s * -0x1p11f);
+    r.no = make_float2(-o, -o);
+    return r;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    return __fadd2_rn(a, b);
+}
+
+// One qs word → two bf16x2 words of low-nibble values (bytes 0,1 and 2,3)
+// and two of high-nibble values.
+__device__ __forceinline__ void dequant_word(uint32_t v, const NibScale &lo, const NibScale &hi,
+                                             uint32_t &l01, uint32_t &l23, uint32_t &h01,
+                                             uint32_t &h23) {
+    const uint32_t v8 = __umulhi(v, 1u << 24);   // v >> 8, on the FMA pipe
+    const uint32_t v16 = __umulhi(v, 1u << 16);  // v >> 16
+    const float2 tl01 = __ffma2_rn(make_float2(magic(v, 0xFu), magic(v, 0xF00u)), lo.s01, lo.c01);
+    const float2 tl23 = __ffma2_rn(make_float2(magic(v, 0xF0000u), magic(v8, 0xF0000u)), lo.s23, lo.c23);
+    const float2 th01 = __ffma2_rn(make_float2(magic(v, 0xF0u), magic(v, 0xF000u)), hi.s01, hi.c01);
+    const float2 th23 = __ffma2_rn(make_float2(magic(v8, 0xF000u), magic(v16, 0xF000u)), hi.s23, hi.c23);
+    l01 = pack_bf16x2(fadd2(tl01, lo.no));
+    l23 = pack_bf16x2(fadd2(tl23, lo.no));
+    h01 = pack_bf16x2(fadd2(th01, hi.no));
+    h23 = pack_bf16x2(fadd2(th23, hi.no));
+}
+
+// Scale d·sc and offset dmin·m of sub-block `sb` of a block header (ggml
+// canonical 6-bit packing), both exact in fp32.  Called with sb constant
+// after unrolling, so the byte selection folds.
+__device__ __forceinline__ float2 sub_scale(int sb, uint4 hdr, float2 dm) {
+    uint32_t sc, m;
+    if (sb < 4) {
+        sc = (hdr.y >> (8 * sb)) & 63u;
+        m = (hdr.z >> (8 * sb)) & 63u;
+    } else {
+        const uint32_t hi = (hdr.w >> (8 * (sb - 4))) & 0xFFu;
+        sc = (hi & 15u) | (((hdr.y >> (8 * (sb - 4) + 6)) & 3u) << 4);
+        m = (hi >> 4) | (((hdr.z >> (8 * (sb - 4) + 6)) & 3u) << 4);
+    }
+    return make_float2(dm.x * static_cast<float>(sc), dm.y * static_cast<float>(m));
+}
+
+// fp32 → bf16 activations, round to nearest even, four values per thread step.
+__global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, size_t n4) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = x[i];
+        xb[i] = make_uint2(pack_bf16x2(make_float2(v.x, v.y)), pack_bf16x2(make_float2(v.z, v.w)));
+    }
 }
 
 template <int TP>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                      float *__restrict__ y, int K, int N, int T, int *status) {
     using L = TcLayout<TP>;
     constexpr uint32_t kAccCols = TP <= 32 ? 32 : 64;     // one accumulator
@@ -169,9 +259,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full_w = bars, *empty_w = full_w + kTcWStages;
-    uint64_t *full_x = empty_w + kTcWStages, *empty_x = full_x + kTcXStages;
-    uint64_t *full_ab = empty_x + kTcXStages, *empty_ab = full_ab + kTcABStages;
-    uint64_t *seg_full = empty_ab + kTcABStages, *seg_free = seg_full + 2;
+    uint64_t *full_a = empty_w + kTcWStages, *empty_a = full_a + kTcAStages;
+    uint64_t *full_b = empty_a + kTcAStages, *empty_b = full_b + kTcBStages;
+    uint64_t *seg_full = empty_b + kTcBStages, *seg_free = seg_full + 2;
     uint64_t *done = seg_free + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
 
@@ -186,13 +276,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full_w[s], 1);
             mbar_init(&empty_w[s], kTcDq);
         }
-        for (int s = 0; s < kTcXStages; ++s) {
-            mbar_init(&full_x[s], 1);
-            mbar_init(&empty_x[s], kTcDq);
+        for (int s = 0; s < kTcAStages; ++s) {
+            mbar_init(&full_a[s], kTcDq);
+            mbar_init(&empty_a[s], 1);
         }
-        for (int s = 0; s < kTcABStages; ++s) {
-            mbar_init(&full_ab[s], kTcDq);
-            mbar_init(&empty_ab[s], 1);
+        for (int s = 0; s < kTcBStages; ++s) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&empty_b[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&seg_full[s], 1);
@@ -218,15 +308,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcWarpTma) {
         if (lane == 0) {
             // Weight tiles and activation tiles are issued independently, each
-            // as soon as its ring slot is free, so the weight stream runs up to
-            // kTcWStages blocks ahead whatever the activation ring does.
+            // as soon as its ring slot is free.
             int nw = 0, nx = 0;
             for (; nw < min(nblocks, kTcWStages); ++nw) {
                 mbar_arrive_expect_tx(&full_w[nw], kTcWTileBytes);
                 tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, nw * kQ4kBytes, row0, &full_w[nw]);
             }
-            // x may be produced by the previous kernel on the stream.
+            // The bf16 activations come from the previous kernel on the stream.
             pdl_wait();
+            for (; nx < min(nchunks, kTcBStages); ++nx) {
+                mbar_arrive_expect_tx(&full_b[nx], L::b_bytes);
+                tma_load_2d(sbase + L::off_b + nx * L::b_bytes, &tm_b, nx * kTcKc, 0, &full_b[nx]);
+            }
             long long t_last = clock64();
             while ((nw < nblocks || nx < nchunks) && !abort_flag) {
                 bool progressed = false;
@@ -241,10 +334,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 if (nx < nchunks) {
-                    const int xs = nx % kTcXStages;
-                    if (nx < kTcXStages || mbar_try_wait(&empty_x[xs], ((nx / kTcXStages) - 1) & 1)) {
-                        mbar_arrive_expect_tx(&full_x[xs], L::x_bytes);
-                        tma_load_2d(sbase + L::off_x + xs * L::x_bytes, &tm_x, nx * kTcKc, 0, &full_x[xs]);
+                    const int bs = nx % kTcBStages;
+                    if (mbar_try_wait(&empty_b[bs], ((nx / kTcBStages) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&full_b[bs], L::b_bytes);
+                        tma_load_2d(sbase + L::off_b + bs * L::b_bytes, &tm_b, nx * kTcKc, 0, &full_b[bs]);
                         ++nx;
                         progressed = true;
                     }
@@ -260,39 +353,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // use of each ring slot must have landed.
             for (int b = max(0, nw - kTcWStages); b < nw; ++b)
                 (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
-            for (int c = max(0, nx - kTcXStages); c < nx; ++c)
-                (void)mbar_wait_bounded(&full_x[c % kTcXStages], (c / kTcXStages) & 1, kWaitLimitCycles);
+            for (int c = max(0, nx - kTcBStages); c < nx; ++c)
+                (void)mbar_wait_bounded(&full_b[c % kTcBStages], (c / kTcBStages) & 1, kWaitLimitCycles);
         }
         __syncwarp();
     } else if (warp == kTcWarpMma) {
         if (lane == 0) {
             // Segment sg (kTcSegChunks chunks) accumulates into buffer sg % 2,
             // starting from zero; the dequant warps fold each finished segment
-            // into fp32 registers.  Short accumulation chains keep the tensor
-            // core's accumulation error independent of K.
+            // into fp32 registers.
             const uint32_t idesc = mma_idesc<TP>();
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kTcABStages;
+                const int sa = c % kTcAStages, sbx = c % kTcBStages;
                 const int sg = c / kTcSegChunks, cs = c - sg * kTcSegChunks;
                 const int buf = sg & 1;
                 if (abort_flag) break;
                 bool ok = true;
                 if (cs == 0 && sg >= 2)
                     ok = mbar_wait_bounded(&seg_free[buf], ((sg >> 1) - 1) & 1, kWaitLimitCycles);
-                ok = ok && mbar_wait_bounded(&full_ab[s], (c / kTcABStages) & 1, kWaitLimitCycles);
+                ok = ok && mbar_wait_bounded(&full_b[sbx], (c / kTcBStages) & 1, kWaitLimitCycles);
+                ok = ok && mbar_wait_bounded(&full_a[sa], (c / kTcAStages) & 1, kWaitLimitCycles);
                 if (!ok) {
                     abort_flag = 1;
                     flag_timeout(status);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + L::off_a + s * L::a_bytes;
-                const uint32_t b0 = sbase + L::off_b + s * L::b_bytes;
+                const uint32_t a0 = sbase + L::off_a + sa * L::a_bytes;
+                const uint32_t b0 = sbase + L::off_b + sbx * L::b_bytes;
                 const uint32_t d = tmem_base + (uint32_t)buf * kAccCols;
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
                     tc_mma(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (cs | kk) != 0);
-                tc_commit(&empty_ab[s]);
+                tc_commit(&empty_a[sa]);
+                tc_commit(&empty_b[sbx]);
                 if (cs == kTcSegChunks - 1 || c == nchunks - 1) tc_commit(&seg_full[buf]);
             }
             // Always signal completion of whatever was issued, and wait for
@@ -302,11 +396,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // Dequantize: thread (r, h) fills the 32 values of half h of row r's
-        // 64-value chunk: h = 0 the low nibbles (sub-block 2j), h = 1 the high
-        // nibbles (sub-block 2j+1) of the same 32 qs bytes.
         const int t = threadIdx.x;
-        const int r = t >> 1, h = t & 1;
+        const int r = t & (kTcRows - 1), h = t >> 7;
         // Epilogue geometry: TMEM lanes 32·(warp % 4) .. +31 hold this
         // quarter's rows; warps 0–3 read the first kLowGroups 16-column
         // groups, warps 4–7 the rest.
@@ -342,80 +433,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         bool good = true;
         int drained = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            const int b = c >> 2, j = c & 3;
-            const int ws = b % kTcWStages, xs = c % kTcXStages, s = c % kTcABStages;
-            if (__any_sync(0xffffffffu, abort_flag != 0)) {
-                good = false;
-                break;
-            }
-            // Segment `drained` ended kTcABStages chunks ago, so the previous
-            // iteration's wait on empty_ab already covered its last MMAs.
-            if (c == (drained + 1) * kTcSegChunks + kTcABStages && !drain(drained++)) {
-                good = false;
-                break;
-            }
-            bool ok = true;
-            if (j == 0) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
-            ok = ok && mbar_wait_bounded(&full_x[xs], (c / kTcXStages) & 1, kWaitLimitCycles);
-            if (ok && c >= kTcABStages)
-                ok = mbar_wait_bounded(&empty_ab[s], ((c / kTcABStages) - 1) & 1, kWaitLimitCycles);
-            if (!__all_sync(0xffffffffu, ok)) {
-                good = false;
-                break;
-            }
-            // A: weight row r.
-            {
-                const uint8_t *blk = smem + L::off_w + ws * kTcWTileBytes + r * kQ4kBytes;
+        for (int b = 0; b < nblocks && good; ++b) {
+            const int ws = b % kTcWStages;
+            const uint8_t *blk = smem + L::off_w + ws * kTcWTileBytes + r * kQ4kBytes;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * b + j, sa = c % kTcAStages;
+                if (__any_sync(0xffffffffu, abort_flag != 0)) {
+                    good = false;
+                    break;
+                }
+                // Segment `drained` ended kTcAStages chunks ago, so the previous
+                // iterations' waits on empty_a already covered its last MMAs.
+                if (c == (drained + 1) * kTcSegChunks + kTcAStages && !drain(drained++)) {
+                    good = false;
+                    break;
+                }
+                bool ok = true;
+                if (j == 0) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
+                if (ok && c >= kTcAStages)
+                    ok = mbar_wait_bounded(&empty_a[sa], ((c / kTcAStages) - 1) & 1, kWaitLimitCycles);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    good = false;
+                    break;
+                }
                 const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
+                const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * h);
                 const float2 dm = q4k_d_dmin(hdr.x);
-                const Q4kScales u = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
-                const int sb = 2 * j + h;
-                const uint32_t scw = sb < 4 ? u.sc_lo : u.sc_hi;
-                const uint32_t mw = sb < 4 ? u.m_lo : u.m_hi;
-                const float scale = dm.x * byte_to_float(scw, sb & 3);   // exact
-                const float offset = dm.y * byte_to_float(mw, sb & 3);   // exact
-                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint8_t *arow = smem + L::off_a + s * L::a_bytes + r * 128;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // Logical 16-byte chunk 4h + i holds k = 32h + 8i .. 32h + 8i + 7,
-                    // i.e. qs bytes 8i .. 8i + 7 (words 2i, 2i + 1).
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int wv = 0; wv < 2; ++wv) {
-                        const uint32_t v = h ? (qw[2 * i + wv] >> 4) : qw[2 * i + wv];
-                        const float e0 = fmaf(scale, (float)(v & 15u), -offset);
-                        const float e1 = fmaf(scale, (float)((v >> 8) & 15u), -offset);
-                        const float e2 = fmaf(scale, (float)((v >> 16) & 15u), -offset);
-                        const float e3 = fmaf(scale, (float)((v >> 24) & 15u), -offset);
-                        pk[2 * wv] = pack_bf16x2(e0, e1);
-                        pk[2 * wv + 1] = pack_bf16x2(e2, e3);
-                    }
-                    const int lc = 4 * h + i;
-                    *reinterpret_cast<uint4 *>(arow + ((lc ^ (r & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+                const float2 slo = sub_scale(2 * j, hdr, dm);
+                const float2 shi = sub_scale(2 * j + 1, hdr, dm);
+                const NibScale lo = nib_scale_lo(slo.x, slo.y), hi = nib_scale_hi(shi.x, shi.y);
+                uint32_t lw[8], hw[8];
+                dequant_word(q.x, lo, hi, lw[0], lw[1], hw[0], hw[1]);
+                dequant_word(q.y, lo, hi, lw[2], lw[3], hw[2], hw[3]);
+                dequant_word(q.z, lo, hi, lw[4], lw[5], hw[4], hw[5]);
+                dequant_word(q.w, lo, hi, lw[6], lw[7], hw[6], hw[7]);
+                // Low values k = 16h..16h+15 are logical chunks 2h, 2h+1; high
+                // values k = 32+16h.. are chunks 4+2h, 5+2h.
+                uint8_t *arow = smem + L::off_a + sa * L::a_bytes + r * 128;
+                const int sw = r & 7;
+                *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                *reinterpret_cast<uint4 *>(arow + (((4 + 2 * h) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(arow + (((5 + 2 * h) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                fence_async_smem();
+                mbar_arrive(&full_a[sa]);
+                if (j == 3) mbar_arrive(&empty_w[ws]);
             }
-            // B: the activation tile, TP tokens × 64 values, fp32 → bf16.
-            {
-                const float *xt = reinterpret_cast<const float *>(smem + L::off_x + xs * L::x_bytes);
-                uint8_t *bt = smem + L::off_b + s * L::b_bytes;
-                for (int task = t; task < TP * 8; task += kTcDq) {
-                    const int tok = task >> 3, qc = task & 7;
-                    const float4 v0 = *reinterpret_cast<const float4 *>(xt + tok * kTcKc + 8 * qc);
-                    const float4 v1 = *reinterpret_cast<const float4 *>(xt + tok * kTcKc + 8 * qc + 4);
-                    *reinterpret_cast<uint4 *>(bt + tok * 128 + ((qc ^ (tok & 7)) << 4)) =
-                        make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w),
-                                   pack_bf16x2(v1.x, v1.y), pack_bf16x2(v1.z, v1.w));
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(&full_ab[s]);
-            mbar_arrive(&empty_x[xs]);
-            if (j == 3) mbar_arrive(&empty_w[ws]);
         }
         while (good && drained < nsegs) good = drain(drained++);
 
@@ -464,11 +528,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int TP>
-cudaError_t launch_tile(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
-                        int T) {
+cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, int K,
+                        int N, int T) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap tm_w, tm_x;
+    alignas(64) CUtensorMap tm_w, tm_b;
     const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
     {
         const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
@@ -481,12 +545,15 @@ cudaError_t launch_tile(const LaunchCtx &c, const float *x, const uint8_t *W, fl
             return cudaErrorInvalidValue;
     }
     {
+        // bf16 activations [T][K]: a 64-value (128-byte) by TP-token box with
+        // the 128-byte swizzle is exactly one K-major MMA operand tile; token
+        // rows past T read as zero.
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(float)};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(__nv_bfloat16)};
         const cuuint32_t box[2] = {(cuuint32_t)kTcKc, (cuuint32_t)TP};
         const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+        if (encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(xb), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
@@ -495,7 +562,7 @@ cudaError_t launch_tile(const LaunchCtx &c, const float *x, const uint8_t *W, fl
     cudaError_t e = ensure_smem(q4k_mm_tc_kernel<TP>, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((N + kTcRows - 1) / kTcRows);
-    return launch_kernel(c, q4k_mm_tc_kernel<TP>, grid, dim3(kTcThreads), smem, tm_w, tm_x, y, K, N, T,
+    return launch_kernel(c, q4k_mm_tc_kernel<TP>, grid, dim3(kTcThreads), smem, tm_w, tm_b, y, K, N, T,
                          c.status);
 }
 
@@ -503,11 +570,23 @@ cudaError_t launch_tile(const LaunchCtx &c, const float *x, const uint8_t *W, fl
 
 cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
                              int N, int T) {
-    // Token tiles of up to 64 (the weights are re-read once per tile).
-    cudaError_t e = cudaSuccess;
+    // x rounded to bf16 once into stream-ordered scratch, freed on the same
+    // stream after the last tile (token tiles of up to 64; the weights are
+    // re-read once per tile).
+    const size_t n = (size_t)T * K;
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(&scratch, n * sizeof(__nv_bfloat16), c.stream);
+    if (e != cudaSuccess) return e;
+    __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(scratch);
+    {
+        const size_t n4 = n / 4;
+        const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
+        e = launch_kernel(c, x_to_bf16_kernel, dim3(grid), dim3(256), 0,
+                          reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb), n4);
+    }
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += kTcMaxTokens) {
         const int tt = min(kTcMaxTokens, T - t0);
-        const float *xt = x + (size_t)t0 * K;
+        const __nv_bfloat16 *xt = xb + (size_t)t0 * K;
         float *yt = y + (size_t)t0 * N;
         const int tp = (tt + 15) / 16 * 16;
         switch (tp) {
@@ -517,7 +596,8 @@ cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *
             default: e = launch_tile<64>(c, xt, W, yt, K, N, tt); break;
         }
     }
-    return e;
+    const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
+    return e != cudaSuccess ? e : ef;
 }
 
 }  // namespace q4mm
