@@ -73,9 +73,14 @@ typedef enum {
  * x     : 16-byte aligned.  y: 4-byte aligned.
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
  *         outputDim >= 1; tokens >= 1.
- * Precision: FP32 fused multiply-add throughout; per token row t,
- *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
- * Every weight byte is read from HBM once per call, whatever `tokens` is.
+ * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
+ *         One token: x is split exactly (to 2^-21 of each 256-value block's
+ *         largest magnitude, exactly for integers) into three int8 planes
+ *         under a power-of-two block scale; the code-dots are exact integer
+ *         sums, scales, mins and the combination are fp32.  Two or more
+ *         tokens: fp32 dequantization and fp32 fused multiply-add.
+ * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
+ * 64 tokens above that).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
  */
 int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
