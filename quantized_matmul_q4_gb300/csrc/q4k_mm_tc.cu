@@ -3,41 +3,50 @@
 //
 // y[t][o] = Σ_k x[t][k]·w[o][k] with w = d·sc_s·q − dmin·m_s (SKaiNET PR #562
 // "feat(kernel): SIMD-fused Q4_K matmul kernel + Q4KMatmulKernel SPI",
-// section "Pipeline"), evaluated as D[o][t] = A[o][k]·B[t][k] with
-//   A = the dequantized weight tile, rounded to bf16 (M = 128 rows per CTA),
-//   B = the activation tile, rounded to bf16 (N = tokens, padded to 16),
+// section "Pipeline"), evaluated as D[t][o] = A[t][k]·B[o][k] with
+//   A = the activations rounded to bf16 (M = 128 token rows; tokens past the
+//       tile's count read as zero),
+//   B = the dequantized weights rounded to bf16 (N = 256 output rows),
 //   D = fp32 in tensor memory, K = 16 per MMA instruction.
-// Every weight byte is read once per call for up to 64 tokens.
+// A tcgen05.mma instruction occupies the tensor unit for the same time at
+// any M and N (measured on GB300), so each instruction is made as large as
+// the tile allows: 128 × 256 × 16.
 //
 // Before the main kernel, a small kernel rounds x to bf16 once into a
 // stream-ordered scratch buffer (2·T·K bytes, allocated and freed on the
-// call's stream); the main kernel then loads activation tiles by TMA with the
+// call's stream); the main kernel loads activation tiles by TMA with the
 // hardware 128-byte swizzle, already in the layout the MMA reads.
 //
-// Roles in a CTA of the main kernel:
-//  * warp 8 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
-//    (128 rows × 144 bytes) per 256 values of K, before the wait on the
-//    previous kernel, and a bf16 activation tile (TP tokens × 64 values) per
+// Grid: clusters of S CTAs (3, or 4 above K = 49152) per 256-row tile, CTA
+// rank r of a cluster taking 64-value chunks [r·nc/S, (r+1)·nc/S) of K, so
+// that the 43 row tiles of an 11008-row weight spread over 129 SMs.  Each
+// CTA accumulates its K range in one tensor-memory accumulator (at most
+// 16384 values of K, within which the tensor core's fp32 accumulation stays
+// far inside the stated tolerance); ranks 1..S−1 store their partial sums in
+// slices of the scratch buffer, and after a cluster barrier rank 0 adds them
+// in rank order to its own, read from tensor memory, and writes y, so the
+// result does not depend on scheduling.
+//
+// Roles in a CTA:
+//  * warp 16 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
+//    (256 rows × 144 bytes) per 256 values of K, before the wait on the
+//    previous kernel, and a bf16 activation tile (128 tokens × 64 values) per
 //    chunk of 64 values, after it, each as soon as its ring slot is free.
-//  * warps 0–7 dequantize: thread (r, h), r = t mod 128 and h = t / 128, turns
-//    qs bytes 16h..16h+15 of row r's slab into 16 low-nibble values of
-//    sub-block 2j and 16 high-nibble values of 2j+1.  Each nibble becomes a
-//    float with one logic op (2^23 + q·2^p), one paired FMA with the scale at
-//    2^-p and −scale·2^(23−p) gives scale·q exactly, one paired add removes
-//    the min term (the single rounding of the fp32 dequantization), and one
-//    conversion packs two bf16.  Results go in the 128-byte-swizzled K-major
-//    layout; the writes are fenced to the async proxy before the chunk's
-//    barrier arrive.
-//  * warp 9 allocates two accumulators in tensor memory; its first thread
-//    issues four 128×TP×16 MMAs per chunk and commits them to the chunk's
-//    weight and activation slots.  K is cut into segments of 2048: each
-//    segment starts from zero in the accumulator the previous-but-one segment
-//    used, and its completion is committed to that accumulator's barrier.
-//  * warps 0–7 fold each finished segment into fp32 registers (tcgen05.ld
-//    plus an add) a few chunks after it ends, and finally write y.  Short
-//    accumulation chains in the tensor core keep the error of its fp32
-//    accumulation independent of K.
-// All waits are bounded; a time-out sets the device status word.
+//  * warps 0–15 dequantize: thread (r, h), r = t mod 256 and h = t / 256,
+//    turns qs bytes 16h..16h+15 of row r's slab into 16 low-nibble values of
+//    sub-block 2j and 16 high-nibble values of 2j+1.  Each nibble becomes a float with one logic op (2^23 + q·2^p), one
+//    paired FMA with the scale at 2^-p and −scale·2^(23−p) gives scale·q
+//    exactly, one paired add removes the min term (the single rounding of the
+//    fp32 dequantization), and one conversion packs two bf16.  Results go in
+//    the 128-byte-swizzled K-major layout; the writes are fenced to the async
+//    proxy before the chunk's barrier arrive.
+//  * warp 17 allocates the accumulator in tensor memory; its first thread
+//    issues four 128×256×16 MMAs per chunk and commits them to the chunk's
+//    activation and weight slots.
+//  * warps 0–15 then read the accumulator (tcgen05.ld) and store the partial
+//    sums; rank 0 adds the cluster's partials and writes y.
+// All mbarrier waits are bounded; a time-out sets the device status word and
+// every thread still reaches the two cluster barriers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -54,35 +63,36 @@ namespace q4mm {
 
 namespace {
 
-constexpr int kTcRows = 128;                       // MMA M: weight rows per CTA
+constexpr int kTcRows = 256;                       // MMA N: weight rows per CTA
+constexpr int kTcTok = 128;                        // MMA M: token rows per tile
 constexpr int kTcKc = 64;                          // K per chunk: a 128-byte row of bf16
-constexpr int kTcDqWarps = 8;                      // dequant + epilogue warps
+constexpr int kTcDqWarps = 16;                     // dequant + epilogue warps
 constexpr int kTcWarpTma = kTcDqWarps;             // TMA producer warp
 constexpr int kTcWarpMma = kTcDqWarps + 1;         // MMA issuer warp
 constexpr int kTcThreads = 32 * (kTcDqWarps + 2);
-constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads
-constexpr int kTcWStages = 3;                      // Q4_K block-column tiles in flight
-constexpr int kTcAStages = 4;                      // bf16 weight operand tiles in flight
-constexpr int kTcBStages = 12;                     // bf16 activation tiles in flight
-constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 18432
-constexpr int kTcMaxTokens = 64;                   // tokens per launch tile
-constexpr int kTcSegChunks = 32;                   // chunks per accumulation segment (K = 2048)
-static_assert(kTcSegChunks > kTcAStages, "a segment is drained kTcAStages chunks after it ends");
+constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads (two per weight row)
+constexpr int kTcWStages = 2;                      // Q4_K block-column tiles in flight
+constexpr int kTcAStages = 3;                      // bf16 activation tiles in flight
+constexpr int kTcBStages = 3;                      // bf16 weight operand tiles in flight
+constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 36864
+constexpr uint32_t kTcATileBytes = kTcTok * 128;         // 16384
+constexpr uint32_t kTcBTileBytes = kTcRows * 128;        // 32768
+constexpr int kTcMaxKPerCta = 16384;               // one accumulator per CTA
+constexpr uint32_t kTcTmemCols = kTcRows;          // fp32 accumulator columns
 
-template <int TP>
 struct TcLayout {
-    static constexpr uint32_t a_bytes = kTcRows * 128;
-    static constexpr uint32_t b_bytes = TP * 128;
     static constexpr uint32_t off_a = 0;
-    static constexpr uint32_t off_b = off_a + kTcAStages * a_bytes;
-    static constexpr uint32_t off_w = off_b + kTcBStages * b_bytes;
+    static constexpr uint32_t off_b = off_a + kTcAStages * kTcATileBytes;
+    static constexpr uint32_t off_w = off_b + kTcBStages * kTcBTileBytes;
     static constexpr uint32_t off_bar = off_w + kTcWStages * kTcWTileBytes;
-    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcAStages + 2 * kTcBStages + 4 + 1;
+    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcAStages + 2 * kTcBStages + 1;
     static constexpr uint32_t off_misc = off_bar + 8 * n_bars;
     static constexpr uint32_t total = off_misc + 16;
     static_assert(off_b % 1024 == 0 && off_w % 1024 == 0, "operand tiles must be 1024-byte aligned");
-    static_assert(b_bytes % 1024 == 0, "B tile must hold whole 8-row swizzle atoms");
 };
+
+// Tokens per launch tile: the token rows of one MMA.
+constexpr int kTcMaxTokens = kTcTok;
 
 // tcgen05 shared-memory matrix descriptor for a K-major operand in the
 // 128-byte swizzle layout: rows of 128 bytes, 8-row atoms 1024 bytes apart,
@@ -97,11 +107,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major.
-template <int TP>
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major,
+// M × N.
+template <int M, int N>
 __device__ __forceinline__ uint32_t mma_idesc() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TP >> 3) << 17) |
-           ((uint32_t)(kTcRows >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -242,15 +252,23 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
     }
 }
 
-template <int TP>
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __global__ void __launch_bounds__(kTcThreads, 1)
-    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
-                     float *__restrict__ y, int K, int N, int T, int *status) {
-    using L = TcLayout<TP>;
-    constexpr uint32_t kAccCols = TP <= 32 ? 32 : 64;     // one accumulator
-    constexpr uint32_t kTmemCols = 2 * kAccCols;          // two, alternating by segment
-    constexpr int kGroups = TP / 16;                      // 16-column groups
-    constexpr int kLowGroups = (kGroups + 1) / 2;         // groups read by warps 0–3
+    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                     float *__restrict__ y, float *__restrict__ part, int K, int N, int T, int *status) {
+    using L = TcLayout;
     extern __shared__ uint8_t tc_smem_raw[];
     __shared__ volatile int abort_flag;
     // Operand tiles need 1024-byte aligned swizzle atoms.
@@ -261,15 +279,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *full_w = bars, *empty_w = full_w + kTcWStages;
     uint64_t *full_a = empty_w + kTcWStages, *empty_a = full_a + kTcAStages;
     uint64_t *full_b = empty_a + kTcAStages, *empty_b = full_b + kTcBStages;
-    uint64_t *seg_full = empty_b + kTcBStages, *seg_free = seg_full + 2;
-    uint64_t *done = seg_free + 2;
+    uint64_t *done = empty_b + kTcBStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * kTcRows;
-    const int nchunks = K / kTcKc;
-    const int nblocks = K / kQ4kValues;
-    const int nsegs = (nchunks + kTcSegChunks - 1) / kTcSegChunks;
+    const int S = (int)cluster_size(), rank = (int)cluster_rank();
+    const int row0 = (blockIdx.x / S) * kTcRows;
+    const int nc_all = K / kTcKc;
+    const int c_base = rank * nc_all / S;                 // first chunk of K (absolute)
+    const int nchunks = (rank + 1) * nc_all / S - c_base; // may be 0 when K is short
+    // Q4_K blocks touched: the first may be entered at chunk j0 > 0.
+    const int b_begin = c_base / 4;
+    const int j0 = c_base % 4;
+    const int nblocks = nchunks > 0 ? (c_base + nchunks + 3) / 4 - b_begin : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcWStages; ++s) {
@@ -277,16 +299,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&empty_w[s], kTcDq);
         }
         for (int s = 0; s < kTcAStages; ++s) {
-            mbar_init(&full_a[s], kTcDq);
+            mbar_init(&full_a[s], 1);
             mbar_init(&empty_a[s], 1);
         }
         for (int s = 0; s < kTcBStages; ++s) {
-            mbar_init(&full_b[s], 1);
+            mbar_init(&full_b[s], kTcDq);
             mbar_init(&empty_b[s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&seg_full[s], 1);
-            mbar_init(&seg_free[s], kTcDq);
         }
         mbar_init(done, 1);
         abort_flag = 0;
@@ -295,14 +313,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
-                     "r"(kTmemCols)
+                     "r"(kTcTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
 
     if (warp == kTcWarpTma) {
@@ -312,13 +330,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int nw = 0, nx = 0;
             for (; nw < min(nblocks, kTcWStages); ++nw) {
                 mbar_arrive_expect_tx(&full_w[nw], kTcWTileBytes);
-                tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, nw * kQ4kBytes, row0, &full_w[nw]);
+                tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
+                            &full_w[nw]);
             }
             // The bf16 activations come from the previous kernel on the stream.
             pdl_wait();
-            for (; nx < min(nchunks, kTcBStages); ++nx) {
-                mbar_arrive_expect_tx(&full_b[nx], L::b_bytes);
-                tma_load_2d(sbase + L::off_b + nx * L::b_bytes, &tm_b, nx * kTcKc, 0, &full_b[nx]);
+            for (; nx < min(nchunks, kTcAStages); ++nx) {
+                mbar_arrive_expect_tx(&full_a[nx], kTcATileBytes);
+                tma_load_2d(sbase + L::off_a + nx * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0, &full_a[nx]);
             }
             long long t_last = clock64();
             while ((nw < nblocks || nx < nchunks) && !abort_flag) {
@@ -327,17 +346,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int ws = nw % kTcWStages;
                     if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
                         mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
-                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, nw * kQ4kBytes, row0,
-                                    &full_w[ws]);
+                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes,
+                                    row0, &full_w[ws]);
                         ++nw;
                         progressed = true;
                     }
                 }
                 if (nx < nchunks) {
-                    const int bs = nx % kTcBStages;
-                    if (mbar_try_wait(&empty_b[bs], ((nx / kTcBStages) - 1) & 1)) {
-                        mbar_arrive_expect_tx(&full_b[bs], L::b_bytes);
-                        tma_load_2d(sbase + L::off_b + bs * L::b_bytes, &tm_b, nx * kTcKc, 0, &full_b[bs]);
+                    const int as = nx % kTcAStages;
+                    if (mbar_try_wait(&empty_a[as], ((nx / kTcAStages) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&full_a[as], kTcATileBytes);
+                        tma_load_2d(sbase + L::off_a + as * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
+                                    &full_a[as]);
                         ++nx;
                         progressed = true;
                     }
@@ -349,110 +369,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     flag_timeout(status);
                 }
             }
-            // Never leave a tensor copy writing into an exiting CTA: the last
-            // use of each ring slot must have landed.
+            // Never leave a tensor copy writing into shared memory that is
+            // about to be reused: the last use of each ring slot must land.
             for (int b = max(0, nw - kTcWStages); b < nw; ++b)
                 (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
-            for (int c = max(0, nx - kTcBStages); c < nx; ++c)
-                (void)mbar_wait_bounded(&full_b[c % kTcBStages], (c / kTcBStages) & 1, kWaitLimitCycles);
+            for (int c = max(0, nx - kTcAStages); c < nx; ++c)
+                (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, kWaitLimitCycles);
         }
         __syncwarp();
     } else if (warp == kTcWarpMma) {
         if (lane == 0) {
-            // Segment sg (kTcSegChunks chunks) accumulates into buffer sg % 2,
-            // starting from zero; the dequant warps fold each finished segment
-            // into fp32 registers.
-            const uint32_t idesc = mma_idesc<TP>();
+            const uint32_t idesc = mma_idesc<kTcTok, kTcRows>();
             for (int c = 0; c < nchunks; ++c) {
-                const int sa = c % kTcAStages, sbx = c % kTcBStages;
-                const int sg = c / kTcSegChunks, cs = c - sg * kTcSegChunks;
-                const int buf = sg & 1;
+                const int as = c % kTcAStages, bs = c % kTcBStages;
                 if (abort_flag) break;
-                bool ok = true;
-                if (cs == 0 && sg >= 2)
-                    ok = mbar_wait_bounded(&seg_free[buf], ((sg >> 1) - 1) & 1, kWaitLimitCycles);
-                ok = ok && mbar_wait_bounded(&full_b[sbx], (c / kTcBStages) & 1, kWaitLimitCycles);
-                ok = ok && mbar_wait_bounded(&full_a[sa], (c / kTcAStages) & 1, kWaitLimitCycles);
+                bool ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
+                ok = ok && mbar_wait_bounded(&full_b[bs], (c / kTcBStages) & 1, kWaitLimitCycles);
                 if (!ok) {
                     abort_flag = 1;
                     flag_timeout(status);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + L::off_a + sa * L::a_bytes;
-                const uint32_t b0 = sbase + L::off_b + sbx * L::b_bytes;
-                const uint32_t d = tmem_base + (uint32_t)buf * kAccCols;
+                const uint32_t a0 = sbase + L::off_a + as * kTcATileBytes;
+                const uint32_t b0 = sbase + L::off_b + bs * kTcBTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
-                    tc_mma(d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (cs | kk) != 0);
-                tc_commit(&empty_a[sa]);
-                tc_commit(&empty_b[sbx]);
-                if (cs == kTcSegChunks - 1 || c == nchunks - 1) tc_commit(&seg_full[buf]);
+                    tc_mma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (c | kk) != 0);
+                tc_commit(&empty_a[as]);
+                tc_commit(&empty_b[bs]);
             }
             // Always signal completion of whatever was issued, and wait for
-            // it, so that tensor memory is never released with MMAs in flight.
+            // it, so that tensor memory is never read or released with MMAs
+            // in flight.
             tc_commit(done);
             (void)mbar_wait_bounded(done, 0, kWaitLimitCycles);
         }
         __syncwarp();
     } else {
-        const int t = threadIdx.x;
-        const int r = t & (kTcRows - 1), h = t >> 7;
-        // Epilogue geometry: TMEM lanes 32·(warp % 4) .. +31 hold this
-        // quarter's rows; warps 0–3 read the first kLowGroups 16-column
-        // groups, warps 4–7 the rest.
-        const int quarter = warp & 3;
-        const int g_begin = warp < 4 ? 0 : kLowGroups;
-        const int n_groups = warp < 4 ? kLowGroups : kGroups - kLowGroups;
-        float acc[2][16];
-#pragma unroll
-        for (int gi = 0; gi < 2; ++gi)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[gi][i] = 0.f;
-        // Fold segment sg into acc.  Warp-uniform: tcgen05.ld is collective.
-        auto drain = [&](int sg) -> bool {
-            const int buf = sg & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&seg_full[buf], (sg >> 1) & 1, kWaitLimitCycles)))
-                return false;
-            tc_fence_after();
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-                if (gi < n_groups) {
-                    float v[16];
-                    tc_ld16(tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)buf * kAccCols +
-                                (uint32_t)(16 * (g_begin + gi)),
-                            v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[gi][i] += v[i];
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&seg_free[buf]);
-            return true;
-        };
-
+        const int r = threadIdx.x & (kTcRows - 1), h = threadIdx.x >> 8;  // row of the tile, byte half
         bool good = true;
-        int drained = 0;
+        int c = 0;  // chunk of this CTA
         for (int b = 0; b < nblocks && good; ++b) {
             const int ws = b % kTcWStages;
             const uint8_t *blk = smem + L::off_w + ws * kTcWTileBytes + r * kQ4kBytes;
+            // Chunks of this block within the CTA's range.
+            const int jb = b == 0 ? j0 : 0;
+            const int je = min(4, jb + (nchunks - c));
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int c = 4 * b + j, sa = c % kTcAStages;
+                if (j < jb || j >= je) continue;
+                const int bs = c % kTcBStages;
                 if (__any_sync(0xffffffffu, abort_flag != 0)) {
                     good = false;
                     break;
                 }
-                // Segment `drained` ended kTcAStages chunks ago, so the previous
-                // iterations' waits on empty_a already covered its last MMAs.
-                if (c == (drained + 1) * kTcSegChunks + kTcAStages && !drain(drained++)) {
-                    good = false;
-                    break;
-                }
                 bool ok = true;
-                if (j == 0) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
-                if (ok && c >= kTcAStages)
-                    ok = mbar_wait_bounded(&empty_a[sa], ((c / kTcAStages) - 1) & 1, kWaitLimitCycles);
+                if (j == jb) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
+                if (ok && c >= kTcBStages)
+                    ok = mbar_wait_bounded(&empty_b[bs], ((c / kTcBStages) - 1) & 1, kWaitLimitCycles);
                 if (!__all_sync(0xffffffffu, ok)) {
                     good = false;
                     break;
@@ -470,45 +445,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dequant_word(q.w, lo, hi, lw[6], lw[7], hw[6], hw[7]);
                 // Low values k = 16h..16h+15 are logical chunks 2h, 2h+1; high
                 // values k = 32+16h.. are chunks 4+2h, 5+2h.
-                uint8_t *arow = smem + L::off_a + sa * L::a_bytes + r * 128;
+                uint8_t *brow = smem + L::off_b + bs * kTcBTileBytes + r * 128;
                 const int sw = r & 7;
-                *reinterpret_cast<uint4 *>(arow + (((2 * h) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                *reinterpret_cast<uint4 *>(arow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-                *reinterpret_cast<uint4 *>(arow + (((4 + 2 * h) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(arow + (((5 + 2 * h) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                *reinterpret_cast<uint4 *>(brow + (((2 * h) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4 *>(brow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                *reinterpret_cast<uint4 *>(brow + (((4 + 2 * h) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(brow + (((5 + 2 * h) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
                 fence_async_smem();
-                mbar_arrive(&full_a[sa]);
-                if (j == 3) mbar_arrive(&empty_w[ws]);
+                mbar_arrive(&full_b[bs]);
+                ++c;
             }
+            // Every dequant thread releases the block once, after its last chunk.
+            if (good) mbar_arrive(&empty_w[ws]);
         }
-        while (good && drained < nsegs) good = drain(drained++);
-
-        if (good) {
-            pdl_wait();
-            const int row = row0 + 32 * quarter + lane;
-            if (row < N) {
-#pragma unroll
-                for (int gi = 0; gi < 2; ++gi)
-                    if (gi < n_groups) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int col = 16 * (g_begin + gi) + i;
-                            if (col < T) y[(size_t)col * N + row] = acc[gi][i];
-                        }
-                    }
-            }
-        } else {
+        if (!good) {
             abort_flag = 1;
             flag_timeout(status);
         }
     }
 
+    // The accumulator is complete once every MMA this CTA issued has finished.
+    const bool have_acc = __syncthreads_and(mbar_wait_bounded(done, 0, kWaitLimitCycles) ? 1 : 0) != 0;
+    tc_fence_after();
+
+    // Epilogue.  Warps w, w+4, w+8, w+12 share TMEM lane quarter w % 4
+    // (tokens 32·quarter..) and read 64 of the 256 columns each into a shared
+    // tile [T][257] (the padding keeps the lanes, which hold consecutive
+    // tokens, on distinct banks); the rings are idle by now.  Ranks 1..S−1
+    // copy their tile row by row into slice rank − 1 of the scratch; after a
+    // cluster barrier rank 0 adds the slices to its own tile in rank order
+    // and writes y, all with consecutive threads on consecutive columns.
+    constexpr int kPitch = kTcRows + 1;
+    float *ysm = reinterpret_cast<float *>(smem);
+    const int quarter = warp & 3, cq = warp >> 2;
+    const int tok = 32 * quarter + lane;
+    const int tile = blockIdx.x / S, ntiles = gridDim.x / S;
+    if (warp < kTcDqWarps && 32 * quarter < T) {  // warp-uniform
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+            float v[16];
+            if (have_acc && nchunks > 0) {
+                tc_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(64 * cq + 16 * g), v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            }
+            if (tok < T) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ysm[tok * kPitch + 64 * cq + 16 * g + i] = v[i];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    const int n_el = T * kTcRows;
+    auto slice = [&](int s) -> float * {  // [T][256] partial sums of rank s for this tile
+        return part + ((size_t)(s - 1) * ntiles + tile) * (size_t)n_el;
+    };
+    if (rank != 0) {
+        float *dst = slice(rank);
+        for (int i = threadIdx.x; i < n_el; i += kTcThreads) dst[i] = ysm[(i / kTcRows) * kPitch + i % kTcRows];
+    }
+    // Partials of every rank are visible to rank 0 after the cluster barrier
+    // (release / acquire at cluster scope).
+    cluster_sync_all();
+
+    if (rank == 0) {
+        // The output may be read by the previous kernel on the stream.
+        pdl_wait();
+        const int ncols = min(kTcRows, N - row0);
+        // Four elements per thread step with every partial load issued before
+        // the adds (S <= 4: at most three other ranks), so the L2 latencies
+        // overlap.  L2 reads: an earlier tile may have left these lines in L1.
+        const float *p1 = slice(1), *p2 = S > 2 ? slice(2) : p1, *p3 = S > 3 ? slice(3) : p1;
+        constexpr int kU = 4;
+        for (int i0 = threadIdx.x; i0 < n_el; i0 += kU * kTcThreads) {
+            float a1[kU], a2[kU], a3[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = min(i0 + u * kTcThreads, n_el - 1);
+                a1[u] = __ldcg(p1 + i);
+                a2[u] = S > 2 ? __ldcg(p2 + i) : 0.f;
+                a3[u] = S > 3 ? __ldcg(p3 + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = i0 + u * kTcThreads;
+                if (i < n_el) {
+                    const int t = i / kTcRows, col = i % kTcRows;
+                    float acc = ysm[t * kPitch + col] + a1[u];
+                    if (S > 2) acc += a2[u];
+                    if (S > 3) acc += a3[u];
+                    if (col < ncols) y[(size_t)t * N + row0 + col] = acc;
+                }
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == kTcWarpMma) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
                      : "memory");
     }
 }
@@ -527,12 +564,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int TP>
-cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, int K,
-                        int N, int T) {
+cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, float *part,
+                        int K, int N, int T, int S) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap tm_w, tm_b;
+    alignas(64) CUtensorMap tm_w, tm_x;
     const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
     {
         const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
@@ -545,56 +581,75 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8
             return cudaErrorInvalidValue;
     }
     {
-        // bf16 activations [T][K]: a 64-value (128-byte) by TP-token box with
+        // bf16 activations [T][K]: a 64-value (128-byte) by 128-token box with
         // the 128-byte swizzle is exactly one K-major MMA operand tile; token
         // rows past T read as zero.
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
         const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(__nv_bfloat16)};
-        const cuuint32_t box[2] = {(cuuint32_t)kTcKc, (cuuint32_t)TP};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcKc, (cuuint32_t)kTcTok};
         const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(xb), dims, strides,
+        if (encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(xb), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const size_t smem = TcLayout<TP>::total + 1024;
+    const size_t smem = TcLayout::total + 1024;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
-    cudaError_t e = ensure_smem(q4k_mm_tc_kernel<TP>, smem);
+    cudaError_t e = ensure_smem(q4k_mm_tc_kernel, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((N + kTcRows - 1) / kTcRows);
-    return launch_kernel(c, q4k_mm_tc_kernel<TP>, grid, dim3(kTcThreads), smem, tm_w, tm_b, y, K, N, T,
-                         c.status);
+    const int tiles = (N + kTcRows - 1) / kTcRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int nattr = 1;
+    if (c.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        nattr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    return cudaLaunchKernelEx(&cfg, q4k_mm_tc_kernel, tm_w, tm_x, y, part, K, N, T, c.status);
 }
 
 }  // namespace
 
 cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
                              int N, int T) {
-    // x rounded to bf16 once into stream-ordered scratch, freed on the same
-    // stream after the last tile (token tiles of up to 64; the weights are
-    // re-read once per tile).
+    // Split of K over the cluster: at least 3 CTAs per row tile, and at most
+    // kTcMaxKPerCta values of K per CTA.
+    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
+    if (S > 4) return cudaErrorNotSupported;  // the reduction adds at most three other ranks
+    // Stream-ordered scratch, freed on the same stream after the last token
+    // tile: x rounded to bf16 once (2·T·K bytes), then the partial sums of
+    // ranks 1..S−1 for one tile of tokens (whole 256-column row tiles).  The weights are re-read once
+    // per tile of 128 tokens.
     const size_t n = (size_t)T * K;
+    const int tmax = min(T, kTcMaxTokens);
+    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
+    const size_t ncols = (size_t)(N + kTcRows - 1) / kTcRows * kTcRows;
+    const size_t part_bytes = (size_t)(S - 1) * tmax * ncols * sizeof(float);
     void *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(&scratch, n * sizeof(__nv_bfloat16), c.stream);
+    cudaError_t e = cudaMallocAsync(&scratch, xb_bytes + part_bytes, c.stream);
     if (e != cudaSuccess) return e;
     __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(scratch);
+    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + xb_bytes);
     {
         const size_t n4 = n / 4;
         const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
         e = launch_kernel(c, x_to_bf16_kernel, dim3(grid), dim3(256), 0,
                           reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb), n4);
     }
-    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += kTcMaxTokens) {
-        const int tt = min(kTcMaxTokens, T - t0);
-        const __nv_bfloat16 *xt = xb + (size_t)t0 * K;
-        float *yt = y + (size_t)t0 * N;
-        const int tp = (tt + 15) / 16 * 16;
-        switch (tp) {
-            case 16: e = launch_tile<16>(c, xt, W, yt, K, N, tt); break;
-            case 32: e = launch_tile<32>(c, xt, W, yt, K, N, tt); break;
-            case 48: e = launch_tile<48>(c, xt, W, yt, K, N, tt); break;
-            default: e = launch_tile<64>(c, xt, W, yt, K, N, tt); break;
-        }
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
+        const int tt = min(tmax, T - t0);
+        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, part, K, N, tt, S);
     }
     const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
     return e != cudaSuccess ? e : ef;
