@@ -96,18 +96,18 @@ WORKLOADS = {w.name: w for w in [
     Workload("q4k_prefill_tc_4096x11008_t64", "q4k", "q4k_matmul_tc", [(4096, 11008)], 64, 16,
              "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands",
-             ["q4k_mm_tc.cu"], arithmetic="bf16 operands (dequantized in fp32, rounded once), "
+             ["q4k_mm_tc.cu"], "q4k_mm_tc_4096x11008_t64.md", arithmetic="bf16 operands (dequantized in fp32, rounded once), "
                                           "fp32 accumulation in tensor memory"),
     Workload("q4k_prefill_fp32_4096x11008_t64", "q4k", "q4k_matmul", [(4096, 11008)], 64, 16,
              "TFLOP/s", "alu", "q4k_mm_fp32_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu"],
-             arithmetic="fp32 dequantization and fp32 FMA"),
+             "q4k_mm_fp32_4096x11008_t64.md", arithmetic="fp32 dequantization and fp32 FMA"),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
-             "hbm", "ternary_gemv_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
-             "batch 1", ["ternary_gemv.cu"], arithmetic="fp32"),
+             "hbm", "ternary_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "batch 1", ["ternary_gemv.cu"], "ternary_t1_2560x6912.md", arithmetic="fp32"),
     Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",
-             "hbm", "ternary_gemv_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
-             "16 tokens", ["ternary_gemv.cu"], arithmetic="fp32"),
+             "hbm", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),
     Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
              "q4k_gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
              "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
