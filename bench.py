@@ -96,11 +96,11 @@ WORKLOADS = {w.name: w for w in [
     Workload("q4k_prefill_tc_4096x11008_t64", "q4k", "q4k_matmul_tc", [(4096, 11008)], 64, 16,
              "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands",
-             ["q4k_mm_tc.cu"], "q4k_mm_tc_4096x11008_t64.md", arithmetic="bf16 operands (dequantized in fp32, rounded once), "
+             ["q4k_mm_tc.cu", "cluster.cuh"], "q4k_mm_tc_4096x11008_t64.md", arithmetic="bf16 operands (dequantized in fp32, rounded once), "
                                           "fp32 accumulation in tensor memory"),
     Workload("q4k_prefill_fp32_4096x11008_t64", "q4k", "q4k_matmul", [(4096, 11008)], 64, 16,
              "TFLOP/s", "alu", "q4k_mm_fp32_kernel",
-             "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu"],
+             "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu", "cluster.cuh"],
              "q4k_mm_fp32_4096x11008_t64.md", arithmetic="fp32 dequantization and fp32 FMA"),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "ternary_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "

@@ -55,6 +55,7 @@
 #include <mutex>
 #include <utility>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "sync.cuh"
@@ -252,19 +253,6 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
     }
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __global__ void __launch_bounds__(kTcThreads, 1)
     q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                      float *__restrict__ y, float *__restrict__ part, int K, int N, int T, int *status) {
