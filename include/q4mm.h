@@ -15,9 +15,10 @@
  *        (the prefill loop "advance offsets by r·k / r·n", same section).
  *        y is overwritten, never accumulated into.
  *
- * Ownership and memory: x, W and y are DEVICE pointers owned by the caller.
- * The library allocates nothing: no workspace, no per-call scratch.  x, W and
- * y must not overlap.
+ * Ownership and memory: x, W and y are DEVICE pointers owned by the caller
+ * and must not overlap.  q4k_matmul and ternary_gemv allocate nothing;
+ * q4k_matmul_tc takes stream-ordered scratch for the length of each call (its
+ * entry below gives the size).
  *
  * Streams: every compute call is asynchronous on `stream` (NULL means the
  * legacy default stream).  Validation is synchronous: an invalid call returns
@@ -96,10 +97,13 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
  * y_bf16 is the exact product of the bf16-rounded operands; the deviation
  * from the exact product is that of bf16 operand rounding (about 5e-3 of
  * max_o |y_exact| on random data).
- * Memory: each call takes 2·tokens·inputDim bytes of stream-ordered scratch
- * (cudaMallocAsync on `stream`, freed on `stream` before the call returns
- * control to the stream) for the bf16 copy of x; the weights are read once
- * per 64 tokens.
+ * Memory: each call takes stream-ordered scratch (cudaMallocAsync on
+ * `stream`, released by cudaFreeAsync on `stream` after the call's last
+ * kernel): the bf16 copy of x, 2·tokens·inputDim bytes rounded up to 256,
+ * plus (S − 1)·min(tokens, 128)·ceil(outputDim/256)·256·4 bytes of partial
+ * sums, where S = max(3, ceil(inputDim/16384)) CTAs of a cluster split the
+ * input dimension of each 256-row tile.  The weights are read once per 128
+ * tokens.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA} (CUDA also when the
  * scratch allocation fails).  A bounded wait that runs out sets the device
  * status word (see q4mm_device_status).
