@@ -111,6 +111,43 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
 int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
                   int tokens, q4mm_stream_t stream);
 
+/* Size of the fixed device array that q4k_matmul_tc_noalloc uses as scratch. */
+#define Q4MM_TC_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * q4k_matmul_tc_noalloc — q4k_matmul_tc with no allocation at all.  The pages
+ * that define the product have no counterpart of this entry point.  It is for
+ * callers that cannot allocate device memory while a call runs: a host
+ * framework whose own allocator owns the whole device budget and forbids
+ * allocations behind its back, a process on a device or driver set-up
+ * without stream-ordered memory pools (where cudaMallocAsync fails), or a
+ * serving loop with a latency budget that keeps allocator calls off its hot
+ * path.
+ *
+ * Same arguments, layouts, alignment, limits, precision and results as
+ * q4k_matmul_tc: the same kernels run.  The scratch that q4k_matmul_tc takes
+ * per call lives instead in one fixed array of Q4MM_TC_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) of device memory inside the library, which every GPU that loads
+ * the library holds until the process exits.  A call whose scratch (the size
+ * formula under q4k_matmul_tc) is larger returns Q4MM_ERR_DIM before
+ * launching anything; for example 128 tokens of a 4096 → 11008 layer need
+ * 12.3 MB, 64 tokens of it 6.1 MB.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  No part of it has to start at zero: a call writes every
+ * byte of scratch before reading it.  Calls whose kernels may overlap on the
+ * GPU (different streams with no ordering between them, or several host
+ * threads) race on the array: issue them on one stream or synchronise
+ * between them.
+ *
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and keeps it for later
+ * calls; make that first call before any stream capture.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int inputDim,
+                          int outputDim, int tokens, q4mm_stream_t stream);
+
 /*
  * ternary_gemv — y = scale · (x·codesᵀ) with W in the BitNet b1.58 payload.
  *

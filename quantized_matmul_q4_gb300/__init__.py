@@ -20,6 +20,8 @@ from ._binding import (  # noqa: F401
     q4k_matmul_ptr,
     q4k_matmul_tc,
     q4k_matmul_tc_ptr,
+    q4k_matmul_tc_noalloc,
+    q4k_matmul_tc_noalloc_ptr,
     ternary_gemv,
     ternary_gemv_ptr,
     version,

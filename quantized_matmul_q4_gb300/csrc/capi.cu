@@ -170,6 +170,25 @@ int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int
     return Q4MM_OK;
 }
 
+int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
+                          int tokens, q4mm_stream_t stream) {
+    int rc = check_common(x, w_q4k, y, inputDim, outputDim, tokens, 256,
+                          (size_t)(inputDim / 256) * 144, 16);
+    if (rc) return rc;
+    const size_t need = q4mm::q4k_mm_tc_scratch_bytes(inputDim, outputDim, tokens);
+    if (need > (size_t)Q4MM_TC_NOALLOC_SCRATCH_BYTES)
+        return fail(Q4MM_ERR_DIM,
+                    "q4k_matmul_tc_noalloc: %d tokens x inputDim %d x outputDim %d need %zu bytes of scratch, "
+                    "more than the fixed %zu-byte array (use q4k_matmul_tc, or fewer tokens per call)",
+                    tokens, inputDim, outputDim, need, (size_t)Q4MM_TC_NOALLOC_SCRATCH_BYTES);
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    cudaError_t e = q4mm::launch_q4k_mm_tc_fixed_scratch(ctx, x, static_cast<const uint8_t *>(w_q4k), y,
+                                                         inputDim, outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul_tc_noalloc launch");
+    return Q4MM_OK;
+}
+
 int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,
                  int outputDim, int tokens, q4mm_stream_t stream) {
     int rc = check_common(x, w_packed, y, inputDim, outputDim, tokens, 4, (size_t)inputDim / 4, 1);

@@ -33,6 +33,13 @@ cudaError_t launch_q4k_mm_fp32(const LaunchCtx &c, const float *x, const uint8_t
 cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
                              int N, int T);
 
+// The tensor-core prefill with its scratch in a fixed array of library
+// memory (no allocation): bytes of scratch a call needs, and the launcher
+// (cudaErrorInvalidValue if the need exceeds the array).
+size_t q4k_mm_tc_scratch_bytes(int K, int N, int T);
+cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                           int K, int N, int T);
+
 // BitNet b1.58 ternary GEMV, any token count.
 cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_t *W, float scale,
                                 float *y, int K, int N, int T);

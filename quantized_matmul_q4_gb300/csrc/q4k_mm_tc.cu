@@ -55,6 +55,7 @@
 #include <mutex>
 #include <utility>
 
+#include "../../include/q4mm.h"
 #include "cluster.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -641,6 +642,87 @@ cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *
     }
     const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
     return e != cudaSuccess ? e : ef;
+}
+
+// ----------------------------------------------------------------------------
+// The same product with its scratch in a fixed array of library memory, for
+// callers that cannot allocate during a call (q4k_matmul_tc_noalloc).
+// ----------------------------------------------------------------------------
+
+namespace {
+
+// Module memory: every GPU that loads the library holds it until the process
+// exits.  In host code this name is only a stand-in for the device object;
+// kernels get the address that cudaGetSymbolAddress returns for the current
+// device.
+static __device__ __align__(256) uint8_t g_tc_fixed_scratch[Q4MM_TC_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kFixedMaxDevices = 64;
+
+struct FixedScratch {
+    bool ready = false;
+    uint8_t *ptr = nullptr;
+};
+FixedScratch g_fixed[kFixedMaxDevices];
+std::mutex g_fixed_mu;
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) and kept.
+cudaError_t fixed_scratch(uint8_t **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kFixedMaxDevices) return cudaErrorInvalidDevice;
+    FixedScratch &f = g_fixed[dev];
+    std::lock_guard<std::mutex> lock(g_fixed_mu);
+    if (!f.ready) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&f.ptr), g_tc_fixed_scratch);
+        if (e != cudaSuccess) return e;
+        f.ready = true;
+    }
+    *out = f.ptr;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t q4k_mm_tc_scratch_bytes(int K, int N, int T) {
+    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
+    const size_t n = (size_t)T * K;
+    const int tmax = min(T, kTcMaxTokens);
+    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
+    const size_t ncols = (size_t)(N + kTcRows - 1) / kTcRows * kTcRows;
+    return xb_bytes + (size_t)(S - 1) * tmax * ncols * sizeof(float);
+}
+
+cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                           int K, int N, int T) {
+    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
+    if (S > 4) return cudaErrorNotSupported;
+    if (q4k_mm_tc_scratch_bytes(K, N, T) > (size_t)Q4MM_TC_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    uint8_t *scratch = nullptr;
+    cudaError_t e = fixed_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    // Layout as in launch_q4k_mm_tc: bf16 x, then the partial sums of ranks
+    // 1..S−1 for one tile of tokens.  Nothing needs clearing: the pre-pass
+    // writes all of x's copy and every partial slice is written by its rank
+    // before rank 0 reads it.
+    const size_t n = (size_t)T * K;
+    const int tmax = min(T, kTcMaxTokens);
+    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
+    __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(scratch);
+    float *part = reinterpret_cast<float *>(scratch + xb_bytes);
+    {
+        const size_t n4 = n / 4;
+        const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
+        e = launch_kernel(c, x_to_bf16_kernel, dim3(grid), dim3(256), 0,
+                          reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb), n4);
+    }
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
+        const int tt = min(tmax, T - t0);
+        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, part, K, N, tt, S);
+    }
+    return e;
 }
 
 }  // namespace q4mm

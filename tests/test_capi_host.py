@@ -104,3 +104,15 @@ def test_rejects_overlap(q4mm):
     with pytest.raises(q4mm.Q4mmError) as e:
         q4mm.ternary_gemv_ptr(X, Y + 4, 1.0, Y, 256, 4, 1, 0)
     assert e.value.code == ALIAS
+
+
+def test_noalloc_refuses_oversize_before_any_cuda_call(q4mm):
+    # The fixed scratch array holds 16 MiB; 512 tokens x 16384 need 20 MiB.
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_noalloc_ptr(X, W, Y, 16384, 4096, 512, 0)
+    assert e.value.code == DIM
+    assert "scratch" in q4mm.last_error()
+    # Validation shared with q4k_matmul_tc comes first.
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_noalloc_ptr(X, W, Y, 300, 16, 1, 0)
+    assert e.value.code == DIM and "inputDim" in q4mm.last_error()
