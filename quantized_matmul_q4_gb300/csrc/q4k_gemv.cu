@@ -64,8 +64,14 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 //
 // Roles in a CTA (a contiguous range of output rows):
 //  * warp 0, lane 0 streams the rows into a shared-memory ring with 1-D bulk
-//    copies of whole stages (weights are never written by an earlier kernel,
-//    so this starts before the wait on the previous kernel);
+//    copies of whole stages.  It first waits for the previous kernel on the
+//    stream (which may write x), copies x into shared memory with one bulk
+//    copy, and only then issues the weight stages: an activation fetch that
+//    queues behind the CTA's weight stream arrives late, and everything after
+//    it (plane split, code-dots) waits for it, while the weights have the
+//    plane split's time to land.  (pre_stages > 0 sends that many stages
+//    ahead of the wait instead; measured slower on GB300.)  Above 64 KB of x
+//    the compute threads load x themselves and all stages go out first;
 //  * the other warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j
 //    of block b of every row it visits (32 low nibbles of sub-block 2j, 32
 //    high nibbles of 2j+1) and decodes the two 6-bit scale/min pairs it needs
@@ -79,34 +85,71 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 // with |p1| ≤ 127 and |p2|, |p3| ≤ 64; every step of the split is exact
 // (power-of-two scalings and exact fp32 subtractions), so activations with at
 // most 21 significant bits below their block maximum (integers included) are
-// represented exactly.  The 4-bit codes are used as they are (no bias), the
-// integer sums are exact, and scales, mins and the final combination are fp32.
+// represented exactly.  Low-nibble codes enter the dot products as they are;
+// high-nibble codes enter as 16·q (the byte masked in place, no shift) and
+// the factor 16 is taken out of that sub-block's scale.  The integer sums are
+// exact; scales, mins and the final combination are fp32.
 // kNB (blocks per row) is a template constant for common widths so that row
 // and stage address arithmetic folds at compile time; 0 reads it at run time.
 
-// Scale d·sc and offset dmin·m of the two sub-blocks 2j and 2j+1 of a block
-// (lane-constant j), from the 16-byte block header.
-struct SlabScalesRaw {
-    float s0, s1, o0, o1;
+// Lane-constant selectors that pick the two 6-bit scale/min pairs of
+// sub-blocks 2j and 2j+1 out of the 12 packed bytes (ggml canonical packing:
+// sub-blocks 0..3 in the low 6 bits of bytes 0..3 / 4..7; sub-blocks 4..7
+// from the nibbles of bytes 8..11 plus the top 2 bits of bytes 0..3 / 4..7).
+struct LaneScaleSel {
+    uint32_t mask_lo;   // nibble field of bytes 8..11 (upper sub-blocks only)
+    uint32_t mask_hi;   // 6-bit field (lower) or top-2-bit field (upper)
+    uint32_t sh_hi;     // shift bringing the top 2 bits to bits 4..5
+    uint32_t sh_min;    // the mins' nibbles sit in bits 4..7 of bytes 8..11
+    uint32_t sel0, sel1;  // byte permutes: byte k of a word → float 2^23 + byte
 };
 
-__device__ __forceinline__ SlabScalesRaw slab_scales_raw(uint4 hdr, int j) {
-    const float2 dm = q4k_d_dmin(hdr.x);
-    const Q4kScales u = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+__device__ __forceinline__ LaneScaleSel lane_scale_sel(int j) {
     const bool upper = j >= 2;
-    const uint32_t scw = upper ? u.sc_hi : u.sc_lo;
-    const uint32_t mw = upper ? u.m_hi : u.m_lo;
-    const int k0 = 2 * (j & 1);
-    SlabScalesRaw r;
-    r.s0 = dm.x * byte_to_float(scw, k0);  // exact: 11-bit × 6-bit
-    r.s1 = dm.x * byte_to_float(scw, k0 + 1);
-    r.o0 = dm.y * byte_to_float(mw, k0);
-    r.o1 = dm.y * byte_to_float(mw, k0 + 1);
+    const uint32_t k0 = 2 * (j & 1);
+    LaneScaleSel r;
+    r.mask_lo = upper ? 0x0F0F0F0Fu : 0u;
+    r.mask_hi = upper ? 0x30303030u : 0x3F3F3F3Fu;
+    r.sh_hi = upper ? 2u : 0u;
+    r.sh_min = upper ? 4u : 0u;
+    r.sel0 = 0x7440u | k0;
+    r.sel1 = 0x7440u | (k0 + 1);
     return r;
 }
 
+// Scales and mins of sub-blocks 2j and 2j+1 of one block: s0 = d'·sc_2j,
+// s1 = d'·sc_2j+1 / 16 (the high-nibble sums carry a factor 16), o = dmin·m,
+// with d' = d·dscale (dscale a power of two).  A 6-bit field becomes the
+// float 2^23 + v by one byte permute, and d'·v comes exactly out of one FMA
+// against −d'·2^23.
+struct RowScales {
+    float s0, s1, o0, o1;
+};
+
+__device__ __forceinline__ RowScales row_scales(uint4 h, const LaneScaleSel &L, float dscale) {
+    const float2 dm = q4k_d_dmin(h.x);
+    const float d = dm.x * dscale;
+    const float d16 = d * 0.0625f;
+    const uint32_t scw = (h.w & L.mask_lo) | ((h.y >> L.sh_hi) & L.mask_hi);
+    const uint32_t mw = ((h.w >> L.sh_min) & L.mask_lo) | ((h.z >> L.sh_hi) & L.mask_hi);
+    constexpr float kTwo23 = 8388608.0f;
+    RowScales r;
+    r.s0 = fmaf(d, __uint_as_float(__byte_perm(scw, 0x4B000000u, L.sel0)), -d * kTwo23);
+    r.s1 = fmaf(d16, __uint_as_float(__byte_perm(scw, 0x4B000000u, L.sel1)), -d16 * kTwo23);
+    r.o0 = fmaf(dm.y, __uint_as_float(__byte_perm(mw, 0x4B000000u, L.sel0)), -dm.y * kTwo23);
+    r.o1 = fmaf(dm.y, __uint_as_float(__byte_perm(mw, 0x4B000000u, L.sel1)), -dm.y * kTwo23);
+    return r;
+}
+
+// d = c + Σ a_i·b_i with a as four unsigned bytes and b as four signed bytes.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Integer code-dots of one slab against the three activation planes:
-// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] likewise for the high nibbles.
+// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] = 16·Σ_l q_hi(l)·plane_p[32 + l].
 // Slab byte l pairs with plane byte l of the low 32 positions (words 0..7)
 // and with plane byte l of the high 32 positions (words 8..15).
 __device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0, uint4 q1,
@@ -114,25 +157,38 @@ __device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        const int l4 = (int)(qw[w] & 0x0F0F0F0Fu);
-        const int h4 = (int)((qw[w] >> 4) & 0x0F0F0F0Fu);
+        const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
+        const uint32_t h4 = qw[w] & 0xF0F0F0F0u;
 #pragma unroll
         for (int pp = 0; pp < 3; ++pp) {
-            d_lo[pp] = __dp4a(l4, pl[pp][w], d_lo[pp]);
-            d_hi[pp] = __dp4a(h4, pl[pp][8 + w], d_hi[pp]);
+            d_lo[pp] = dp4a_us(l4, pl[pp][w], d_lo[pp]);
+            d_hi[pp] = dp4a_us(h4, pl[pp][8 + w], d_hi[pp]);
         }
     }
 }
 
-// Σ q·x in units of the block scale from the three plane sums.
+// 128·(d0 + d1/128 + d2/16384), i.e. Σ q·x in units of s_b/128: the first two
+// terms are an exact integer (|·| < 2^31), converted with one rounding.
 __device__ __forceinline__ float plane_combine(const int (&d)[3]) {
-    const int d01 = d[0] * 128 + d[1];  // |d01| < 2^23: exact in fp32
-    return fmaf(static_cast<float>(d[2]), 1.0f / 16384.0f, static_cast<float>(d01) * (1.0f / 128.0f));
+    const int d01 = d[0] * 128 + d[1];
+    return fmaf(static_cast<float>(d[2]), 1.0f / 128.0f, static_cast<float>(d01));
+}
+
+// One row's contribution from one slab lane: scales, code-dots, lazy mins.
+__device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneScaleSel &L, float dscale,
+                                          const int (&pl)[3][16], float sum_lo, float sum_hi) {
+    const uint4 h = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
+    const RowScales r = row_scales(h, L, dscale);
+    int dl[3] = {0, 0, 0}, dh[3] = {0, 0, 0};
+    slab_dot_planes(pl, q0, q1, dl, dh);
+    return fmaf(r.s0, plane_combine(dl), r.s1 * plane_combine(dh)) - fmaf(r.o0, sum_lo, r.o1 * sum_hi);
 }
 
 // Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter;
 // the low byte of the shifted value's bits is the result as an int8.
-__device__ __forceinline__ float shifted(float v) { return v + 12582912.0f; }
+constexpr float kShifter = 12582912.0f;
 
 struct T1Params {
     const float *x;
@@ -145,14 +201,19 @@ struct T1Params {
     int rows_per_cta;  // contiguous rows per CTA
     int stage_rows;    // rows per ring slot (multiple of the pass size)
     int nslots;        // ring depth
+    int pre_stages;    // stages issued before the wait on the previous kernel
+    int x_staged;      // 1: x arrives by one bulk copy into shared memory
 };
 
 constexpr int kT1RoleWarps = 1;  // the copy warp
+constexpr int kT1MaxCw = 16;     // compute warps at most
 
 template <int kNB>
-__global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
+__global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
+    __shared__ int issued;  // weight stages issued so far (for the abort drain)
+    __shared__ __align__(8) uint64_t x_bar;
 
     // Row geometry: compile-time when kNB > 0.
     const int nb = kNB > 0 ? kNB : p.nb;
@@ -177,7 +238,8 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     int8_t *planes = reinterpret_cast<int8_t *>(smem);                // 3 planes of K bytes
     float *sx = reinterpret_cast<float *>(planes + 3 * K);            // K/32 sub-block sums
     float *sb = sx + K / 32;                                          // K/256 block scales
-    uint8_t *ring = reinterpret_cast<uint8_t *>(sb) + ((nb * 4 + 15) & ~15);
+    float *xst = sb + ((nb + 3) & ~3);                                // x (when staged)
+    uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? K : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
     float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [rows_per_cta][wc]
@@ -193,15 +255,14 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
         return;
     }
     if (threadIdx.x == 0) {
-        // Warm L2 with x: a hint that returns no data, so it may run before
-        // the wait on the kernel that produces x.
-        bulk_prefetch_l2(p.x, (uint32_t)K * sizeof(float));
         for (int s = 0; s < p.nslots; ++s) {
             mbar_init(&full_bar[s], 1);
             // Every pass of a stage is worked by the wc warps of a row.
             mbar_init(&empty_bar[s], passes_per_stage * wc);
         }
+        mbar_init(&x_bar, 1);
         abort_flag = 0;
+        issued = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -210,13 +271,24 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     if (warp == 0) {
         if (lane == 0) {
             const uint8_t *src = p.W + (size_t)row0 * row_bytes;
-            int st = 0;
-            for (; st < min(nstages, p.nslots); ++st) {
+            auto issue = [&](int st, int slot) {
                 const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-                mbar_arrive_expect_tx(&full_bar[st], rows * row_bytes);
-                bulk_g2s(ring + (size_t)st * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
-                         rows * row_bytes, &full_bar[st]);
+                mbar_arrive_expect_tx(&full_bar[slot], rows * row_bytes);
+                bulk_g2s(ring + (size_t)slot * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
+                         rows * row_bytes, &full_bar[slot]);
+                issued = st + 1;
+            };
+            const int first = min(nstages, p.nslots);
+            const int pre = min(first, p.pre_stages);
+            int st = 0;
+            for (; st < pre; ++st) issue(st, st);
+            // x may be written by the previous kernel on the stream.
+            pdl_wait();
+            if (p.x_staged) {
+                mbar_arrive_expect_tx(&x_bar, (uint32_t)K * sizeof(float));
+                bulk_g2s(xst, p.x, (uint32_t)K * sizeof(float), &x_bar);
             }
+            for (; st < first; ++st) issue(st, st);
             for (; st < nstages; ++st) {
                 const int slot = st % p.nslots;
                 if (abort_flag) break;
@@ -226,10 +298,7 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
                     flag_timeout(p.status);
                     break;
                 }
-                const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-                mbar_arrive_expect_tx(&full_bar[slot], rows * row_bytes);
-                bulk_g2s(ring + (size_t)slot * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
-                         rows * row_bytes, &full_bar[slot]);
+                issue(st, slot);
             }
         }
         __syncwarp();
@@ -243,52 +312,66 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
 
         // x may be produced by the previous kernel on the stream.
         pdl_wait();
+        const float *xsrc = p.x;
+        if (p.x_staged) {
+            if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
+                abort_flag = 1;
+                flag_timeout(p.status);
+            }
+            xsrc = xst;
+        }
         // x → three int8 planes under power-of-two block scales, plus the
-        // fp32 sub-block sums.  Thread ct takes half sub-blocks (16 values);
-        // the 16 threads of a block (an aligned 16-lane group) share its
-        // maximum through shuffles, and the two halves of a sub-block sit in
+        // fp32 sub-block sums.  Thread ct takes eighths of sub-blocks (8
+        // values): the 32 threads of a block form one warp and share its
+        // maximum through shuffles; the four threads of a sub-block are
         // neighbouring lanes.
         {
-            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, nh = K / 16;
-            for (int h0 = 0; h0 < nh; h0 += nth) {
-                const int h = h0 + ct;
-                const bool on = h < nh;
-                float v[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 t = on ? __ldg(reinterpret_cast<const float4 *>(p.x) + 4 * h + k)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[4 * k] = t.x;
-                    v[4 * k + 1] = t.y;
-                    v[4 * k + 2] = t.z;
-                    v[4 * k + 3] = t.w;
+            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, ne = K / 8;
+            for (int e0 = 0; e0 < ne; e0 += nth) {
+                const int e = e0 + ct;
+                const bool on = e < ne && !abort_flag;
+                float v[8];
+                {
+                    const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 2 * e;
+                    const float4 t0 = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 t1 = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[0] = t0.x; v[1] = t0.y; v[2] = t0.z; v[3] = t0.w;
+                    v[4] = t1.x; v[5] = t1.y; v[6] = t1.z; v[7] = t1.w;
                 }
                 float amax = 0.f, sum = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     amax = fmaxf(amax, fabsf(v[i]));
                     sum += v[i];
                 }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                // Non-negative floats order like their bit patterns.
+                amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));
                 sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                // s_b = 2^e with amax / 2^e < 127 (1 when the block is zero).
-                int e = 0;
-                if (amax > 0.f) (void)frexpf(amax * (1.0f / 127.0f), &e);
-                e = max(e, -120);  // keeps 2^-e finite; such blocks still scale below 127
-                const float inv = ldexpf(1.0f, -e);
-                uint32_t w1[4], w2[4], w3[4];
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+                // s_b = 2^ex with amax / 2^ex <= 127 (1 when the block is
+                // zero): ex is the binary exponent of amax/127 written as
+                // m·2^ex with m in [0.5, 1), read from the float's exponent
+                // field; -120 bounds it below so that 2^-ex stays finite
+                // (such blocks still scale below 127).
+                const int ebits = (int)(__float_as_uint(amax * (1.0f / 127.0f)) >> 23);
+                const int ex = amax > 0.f ? max(ebits - 126, -120) : 0;
+                const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
+                // Per value: s1 = shifter + rint(v/s_b); r1 = v/s_b − rint(·)
+                // exactly; s2 = shifter + rint(128·r1); r2 = 128·r1 − rint(·)
+                // exactly; s3 = shifter + rint(128·r2).  Each FMA's product is
+                // exact (power-of-two factors), so each rounds only once.
+                uint32_t w1[2], w2[2], w3[2];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 2; ++k) {
                     uint32_t b1[4], b2[4], b3[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float a = v[4 * k + i] * inv;  // exact
-                        const float s1 = shifted(a);
-                        const float r1 = (a - (s1 - 12582912.0f)) * 128.0f;  // exact
-                        const float s2 = shifted(r1);
-                        const float r2 = (r1 - (s2 - 12582912.0f)) * 128.0f;  // exact
-                        const float s3 = shifted(r2);
+                        const float a = v[4 * k + i];
+                        const float s1 = fmaf(a, inv, kShifter);
+                        const float r1 = fmaf(a, inv, kShifter - s1);
+                        const float s2 = fmaf(r1, 128.0f, kShifter);
+                        const float r2 = fmaf(r1, 128.0f, kShifter - s2);
+                        const float s3 = fmaf(r2, 128.0f, kShifter);
                         b1[i] = __float_as_uint(s1);
                         b2[i] = __float_as_uint(s2);
                         b3[i] = __float_as_uint(s3);
@@ -299,16 +382,18 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
                     w3[k] = __byte_perm(__byte_perm(b3[0], b3[1], 0x0040), __byte_perm(b3[2], b3[3], 0x0040), 0x5410);
                 }
                 if (on) {
-                    // Unit-major layout: 16-byte unit u (0..11) of slab S at
-                    // index u·nslabs + S, with u = 4·plane + (h & 3) and
-                    // S = h / 4, so the eight lanes of a quarter warp read
-                    // eight consecutive units.
-                    uint4 *pu = reinterpret_cast<uint4 *>(planes) + (h & 3) * nslabs + (h >> 2);
-                    pu[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                    pu[4 * nslabs] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-                    pu[8 * nslabs] = make_uint4(w3[0], w3[1], w3[2], w3[3]);
-                    if ((h & 1) == 0) sx[h / 2] = sum;
-                    if ((h & 15) == 0) sb[h / 16] = ldexpf(1.0f, e);
+                    // Unit-major layout: the 16-byte unit of half sub-block
+                    // h = e/2 (values 16h..16h+15) of plane q sits at unit
+                    // index (4q + h % 4)·nslabs + h / 4, so the eight lanes of
+                    // a quarter warp read eight consecutive units.
+                    const int h = e >> 1;
+                    uint2 *pu = reinterpret_cast<uint2 *>(reinterpret_cast<uint4 *>(planes) +
+                                                          (h & 3) * nslabs + (h >> 2)) + (e & 1);
+                    pu[0] = make_uint2(w1[0], w1[1]);
+                    pu[8 * nslabs] = make_uint2(w2[0], w2[1]);
+                    pu[16 * nslabs] = make_uint2(w3[0], w3[1]);
+                    if ((e & 3) == 0) sx[e / 4] = sum;
+                    if ((e & 31) == 0) sb[e / 32] = __uint_as_float((uint32_t)(127 + ex) << 23);
                 }
             }
         }
@@ -334,6 +419,8 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
             sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
+        const LaneScaleSel lsel = lane_scale_sel(j);
+        const float dscale = s_blk * (1.0f / 128.0f);
 
         const int npasses = (nrows + pass_rows - 1) / pass_rows;
         // Stage, slot and phase of the current pass, advanced without
@@ -361,22 +448,8 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
                 rows = min(p.stage_rows, nrows - st * p.stage_rows);
             }
             const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
-            const uint8_t *ba = stage_base + min(ra, rows - 1) * row_bytes;
-            const uint8_t *bb = stage_base + min(rb, rows - 1) * row_bytes;
-            const uint4 ha = *reinterpret_cast<const uint4 *>(ba);
-            const uint4 hb = *reinterpret_cast<const uint4 *>(bb);
-            const uint4 a0 = *reinterpret_cast<const uint4 *>(ba + 16 + 32 * j);
-            const uint4 a1 = *reinterpret_cast<const uint4 *>(ba + 32 + 32 * j);
-            const uint4 b0 = *reinterpret_cast<const uint4 *>(bb + 16 + 32 * j);
-            const uint4 b1 = *reinterpret_cast<const uint4 *>(bb + 32 + 32 * j);
-            const SlabScalesRaw sa = slab_scales_raw(ha, j), sc_b = slab_scales_raw(hb, j);
-            int da_lo[3] = {0, 0, 0}, da_hi[3] = {0, 0, 0}, db_lo[3] = {0, 0, 0}, db_hi[3] = {0, 0, 0};
-            slab_dot_planes(pl, a0, a1, da_lo, da_hi);
-            slab_dot_planes(pl, b0, b1, db_lo, db_hi);
-            float pa = s_blk * fmaf(sa.s0, plane_combine(da_lo), sa.s1 * plane_combine(da_hi)) -
-                       fmaf(sa.o0, sum_lo, sa.o1 * sum_hi);
-            float pb = s_blk * fmaf(sc_b.s0, plane_combine(db_lo), sc_b.s1 * plane_combine(db_hi)) -
-                       fmaf(sc_b.o0, sum_lo, sc_b.o1 * sum_hi);
+            float pa = slab_row(stage_base + min(ra, rows - 1) * row_bytes, j, lsel, dscale, pl, sum_lo, sum_hi);
+            float pb = slab_row(stage_base + min(rb, rows - 1) * row_bytes, j, lsel, dscale, pl, sum_lo, sum_hi);
             if (!active || ra >= rows) pa = 0.f;
             if (!active || rb >= rows) pb = 0.f;
             // Two-row butterfly: lanes with (lane & half) == 0 finish with
@@ -417,9 +490,10 @@ __global__ void __launch_bounds__(32 * 16, 1) q4k_gemv_t1_kernel(T1Params p) {
     // Never leave a bulk copy writing into shared memory of an exiting CTA.
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
-        for (int st = max(0, nstages - p.nslots); st < nstages; ++st)
+        for (int st = max(0, issued - p.nslots); st < issued; ++st)
             (void)mbar_wait_bounded(&full_bar[st % p.nslots], (st / p.nslots) & 1,
                                     kWaitLimitCycles);
+        if (p.x_staged) (void)mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles);
     }
 }
 
@@ -603,10 +677,12 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 // Geometry knobs of the one-token kernel (environment, read once): compute
 // warps per CTA, resident CTAs per SM, bytes per ring slot, ring budget.
 struct T1Tuning {
-    int warps = 14;
+    int warps = 16;
     int ctas_per_sm = 1;
     int stage_bytes = 16384;
     int ring_bytes = 200 * 1024;
+    int pre_stages = 0;        // weight stages issued before the activation copy
+    int x_stage_max = 65536;   // bytes of x staged by a bulk copy (0: plain loads)
 };
 
 int env_int(const char *name, int dflt, int lo, int hi) {
@@ -619,10 +695,12 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 const T1Tuning &t1_tuning() {
     static const T1Tuning t = [] {
         T1Tuning r;
-        r.warps = env_int("Q4MM_T1_WARPS", r.warps, 1, 15);
+        r.warps = env_int("Q4MM_T1_WARPS", r.warps, 1, kT1MaxCw);
         r.ctas_per_sm = env_int("Q4MM_T1_CTAS_PER_SM", r.ctas_per_sm, 1, 8);
         r.stage_bytes = env_int("Q4MM_T1_STAGE_BYTES", r.stage_bytes, 1024, 65536);
         r.ring_bytes = env_int("Q4MM_T1_RING_BYTES", r.ring_bytes, 8192, 200 * 1024);
+        r.pre_stages = env_int("Q4MM_T1_PRE_STAGES", r.pre_stages, 0, 64);
+        r.x_stage_max = env_int("Q4MM_T1_X_STAGE_MAX", r.x_stage_max, 0, 65536);
         return r;
     }();
     return t;
@@ -650,8 +728,9 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     const bool wide = L > 32;
     const int wc = wide ? (L + 31) / 32 : 1;
     const int pass_rows = wide ? 2 : 2 * (32 / next_pow2(max(L, 4)));
-    // At most 15 compute warps (+1 copy warp): wider rows go to the generic kernel.
-    if (wc > 15) return cudaErrorNotSupported;
+    // At most kT1MaxCw compute warps (+1 copy warp): wider rows go to the
+    // generic kernel.
+    if (wc > kT1MaxCw) return cudaErrorNotSupported;
     const T1Tuning &tun = t1_tuning();
     p.rg = max(1, tun.warps / wc);
     const int ncw = wc * p.rg;
@@ -668,7 +747,9 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
     const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
-    const size_t xs_bytes = 3 * (size_t)K + (size_t)(K / 32) * sizeof(float) + (size_t)((p.nb * 4 + 15) & ~15);
+    p.x_staged = (size_t)K * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
+    const size_t xs_bytes = 3 * (size_t)K + (size_t)(K / 32) * sizeof(float) + (size_t)((p.nb * 4 + 15) & ~15) +
+                            (p.x_staged ? (size_t)K * sizeof(float) : 0);
     const size_t part_bytes = wide ? (size_t)p.rows_per_cta * wc * sizeof(float) : 0;
     const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
     const size_t budget = tun.ring_bytes;
@@ -676,6 +757,8 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     const int stages_needed = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
     nslots = max(2, min(nslots, min(stages_needed, 8)));
     p.nslots = nslots;
+    // With plain activation loads nothing needs to go out ahead of the rest.
+    p.pre_stages = p.x_staged ? tun.pre_stages : nslots;
     const size_t smem = xs_bytes + (size_t)nslots * slot_bytes + 2 * nslots * sizeof(uint64_t) + part_bytes;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
 
