@@ -80,8 +80,8 @@ def weight_bytes(kind, K, N):
     return _q4k_bytes(K, N) if kind == "q4k" else N * (K // 4)
 
 
-T1_ARITH = ("fp32 activations split exactly (to 2^-21 of each 256-value block's maximum) into three "
-            "int8 planes; 4-bit codes x planes in int32 dp4a; scales, mins and combination in fp32")
+T1_ARITH = ("fp32 activations rounded once to 2^-22 of each 256-value block's maximum and split into three "
+            "byte planes; 4-bit codes x planes in int32 dp4a; scales, mins and combination in fp32")
 LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
 WORKLOADS = {w.name: w for w in [
     Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",

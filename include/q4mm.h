@@ -75,10 +75,11 @@ typedef enum {
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
  *         outputDim >= 1; tokens >= 1.
  * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
- *         One token: x is split exactly (to 2^-21 of each 256-value block's
- *         largest magnitude, exactly for integers) into three int8 planes
- *         under a power-of-two block scale; the code-dots are exact integer
- *         sums, scales, mins and the combination are fp32.  Two or more
+ *         One token: x is rounded once to 2^-22 of each 256-value block's
+ *         largest magnitude (exactly for integers and any value with at
+ *         most 22 significant bits below that maximum) and split into three
+ *         byte planes under a power-of-two block scale; the code-dots are
+ *         exact integer sums, scales, mins and the combination are fp32.  Two or more
  *         tokens: fp32 dequantization and fp32 fused multiply-add.
  * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
  * 64 tokens above that).

@@ -80,11 +80,13 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 //
 // The code-dot Σ x·q of a sub-block runs on integer dot-product instructions
 // (four byte products per instruction).  Each 256-value block of x is split,
-// once per CTA, into three int8 planes under a power-of-two block scale s_b:
-//   x = s_b·(p1 + p2/128 + p3/16384) + e,  |e| ≤ 2^-15·s_b ≤ 2^-21·max|x_b|,
-// with |p1| ≤ 127 and |p2|, |p3| ≤ 64; every step of the split is exact
-// (power-of-two scalings and exact fp32 subtractions), so activations with at
-// most 21 significant bits below their block maximum (integers included) are
+// once per CTA, into three byte planes under a power-of-two block scale s_b:
+//   n = rint(x·2^15/s_b),  |n| < 127·2^15 < 2^22,
+//   n = 65536·p2 + 256·p1 + p0  (p0, p1 unsigned bytes, p2 a signed byte),
+// so x = s_b·2^-15·n + e with |e| ≤ 2^-16·s_b ≤ 2^-22·max|x_b|.  The rounding
+// is a single FMA against the 1.5·2^23 shifter (the product by a power of two
+// is exact), whose low bytes are the digits of n; activations with at most
+// 22 significant bits below their block maximum (integers included) are
 // represented exactly.  Low-nibble codes enter the dot products as they are;
 // high-nibble codes enter as 16·q (the byte masked in place, no shift) and
 // the factor 16 is taken out of that sub-block's scale.  The integer sums are
@@ -117,18 +119,17 @@ __device__ __forceinline__ LaneScaleSel lane_scale_sel(int j) {
     return r;
 }
 
-// Scales and mins of sub-blocks 2j and 2j+1 of one block: s0 = d'·sc_2j,
-// s1 = d'·sc_2j+1 / 16 (the high-nibble sums carry a factor 16), o = dmin·m,
-// with d' = d·dscale (dscale a power of two).  A 6-bit field becomes the
-// float 2^23 + v by one byte permute, and d'·v comes exactly out of one FMA
-// against −d'·2^23.
+// Scales and mins of sub-blocks 2j and 2j+1 of one block: s0 = d·sc_2j,
+// s1 = d·sc_2j+1 / 16 (the high-nibble sums carry a factor 16), o = dmin·m.
+// A 6-bit field becomes the float 2^23 + v by one byte permute, and d·v comes
+// exactly out of one FMA against −d·2^23.
 struct RowScales {
     float s0, s1, o0, o1;
 };
 
-__device__ __forceinline__ RowScales row_scales(uint4 h, const LaneScaleSel &L, float dscale) {
+__device__ __forceinline__ RowScales row_scales(uint4 h, const LaneScaleSel &L) {
     const float2 dm = q4k_d_dmin(h.x);
-    const float d = dm.x * dscale;
+    const float d = dm.x;
     const float d16 = d * 0.0625f;
     const uint32_t scw = (h.w & L.mask_lo) | ((h.y >> L.sh_hi) & L.mask_hi);
     const uint32_t mw = ((h.w >> L.sh_min) & L.mask_lo) | ((h.z >> L.sh_hi) & L.mask_hi);
@@ -148,10 +149,18 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     return d;
 }
 
+// d = c + Σ a_i·b_i with a and b as four unsigned bytes each.
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Integer code-dots of one slab against the three activation planes:
-// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] = 16·Σ_l q_hi(l)·plane_p[32 + l].
-// Slab byte l pairs with plane byte l of the low 32 positions (words 0..7)
-// and with plane byte l of the high 32 positions (words 8..15).
+// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] = 16·Σ_l q_hi(l)·plane_p[32 + l]
+// (planes 0 and 1 unsigned, plane 2 signed).  Slab byte l pairs with plane
+// byte l of the low 32 positions (words 0..7) and with plane byte l of the
+// high 32 positions (words 8..15).  |d| < 2^21.
 __device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0, uint4 q1,
                                                 int (&d_lo)[3], int (&d_hi)[3]) {
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -160,35 +169,45 @@ __device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0
         const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
         const uint32_t h4 = qw[w] & 0xF0F0F0F0u;
 #pragma unroll
-        for (int pp = 0; pp < 3; ++pp) {
-            d_lo[pp] = dp4a_us(l4, pl[pp][w], d_lo[pp]);
-            d_hi[pp] = dp4a_us(h4, pl[pp][8 + w], d_hi[pp]);
+        for (int pp = 0; pp < 2; ++pp) {
+            d_lo[pp] = dp4a_uu(l4, (uint32_t)pl[pp][w], d_lo[pp]);
+            d_hi[pp] = dp4a_uu(h4, (uint32_t)pl[pp][8 + w], d_hi[pp]);
         }
+        d_lo[2] = dp4a_us(l4, pl[2][w], d_lo[2]);
+        d_hi[2] = dp4a_us(h4, pl[2][8 + w], d_hi[2]);
     }
 }
 
-// 128·(d0 + d1/128 + d2/16384), i.e. Σ q·x in units of s_b/128: the first two
-// terms are an exact integer (|·| < 2^31), converted with one rounding.
+// 65536·d2 + 256·d1 + d0, i.e. Σ q·x in units of s_b·2^-15: the last two
+// terms are an exact integer (|·| < 2^29), the sum takes one rounding.
 __device__ __forceinline__ float plane_combine(const int (&d)[3]) {
-    const int d01 = d[0] * 128 + d[1];
-    return fmaf(static_cast<float>(d[2]), 1.0f / 128.0f, static_cast<float>(d01));
+    const int d01 = d[1] * 256 + d[0];
+    return fmaf(static_cast<float>(d[2]), 65536.0f, static_cast<float>(d01));
 }
 
-// One row's contribution from one slab lane: scales, code-dots, lazy mins.
-__device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneScaleSel &L, float dscale,
+// One row's contribution from one slab lane: scales, code-dots (times the
+// plane unit s_b·2^-15, a power of two), lazy mins.
+__device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneScaleSel &L, float unit,
                                           const int (&pl)[3][16], float sum_lo, float sum_hi) {
     const uint4 h = *reinterpret_cast<const uint4 *>(blk);
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
     const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
-    const RowScales r = row_scales(h, L, dscale);
+    const RowScales r = row_scales(h, L);
     int dl[3] = {0, 0, 0}, dh[3] = {0, 0, 0};
     slab_dot_planes(pl, q0, q1, dl, dh);
-    return fmaf(r.s0, plane_combine(dl), r.s1 * plane_combine(dh)) - fmaf(r.o0, sum_lo, r.o1 * sum_hi);
+    return fmaf(unit, fmaf(r.s0, plane_combine(dl), r.s1 * plane_combine(dh)),
+                -fmaf(r.o0, sum_lo, r.o1 * sum_hi));
 }
 
-// Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter;
-// the low byte of the shifted value's bits is the result as an int8.
+// Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter:
+// the float's bits are 0x4B400000 + rint(v).
 constexpr float kShifter = 12582912.0f;
+constexpr uint32_t kShifterBits = 0x4B400000u;
+
+// Bytes per 64-value slab in the plane area: 12 units of 16 bytes (3 planes
+// × 4 quarters) plus 16 bytes of padding, so that the eight slabs read by a
+// quarter warp start in eight different bank groups.
+constexpr int kPlaneSlabBytes = 208;
 
 struct T1Params {
     const float *x;
@@ -235,8 +254,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ncw = wc * p.rg;
     const uint32_t slot_bytes = p.stage_rows * row_bytes;
-    int8_t *planes = reinterpret_cast<int8_t *>(smem);                // 3 planes of K bytes
-    float *sx = reinterpret_cast<float *>(planes + 3 * K);            // K/32 sub-block sums
+    uint8_t *planes = smem;                                           // nslabs × 208 bytes
+    float *sx = reinterpret_cast<float *>(planes + nslabs * kPlaneSlabBytes);  // K/32 sub-block sums
     float *sb = sx + K / 32;                                          // K/256 block scales
     float *xst = sb + ((nb + 3) & ~3);                                // x (when staged)
     uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? K : 0));
@@ -320,11 +339,10 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
             }
             xsrc = xst;
         }
-        // x → three int8 planes under power-of-two block scales, plus the
+        // x → three byte planes under power-of-two block scales, plus the
         // fp32 sub-block sums.  Thread ct takes eighths of sub-blocks (8
         // values): the 32 threads of a block form one warp and share its
-        // maximum through shuffles; the four threads of a sub-block are
-        // neighbouring lanes.
+        // maximum; the four threads of a sub-block are neighbouring lanes.
         {
             const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, ne = K / 8;
             for (int e0 = 0; e0 < ne; e0 += nth) {
@@ -351,47 +369,34 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
                 // s_b = 2^ex with amax / 2^ex <= 127 (1 when the block is
                 // zero): ex is the binary exponent of amax/127 written as
                 // m·2^ex with m in [0.5, 1), read from the float's exponent
-                // field; -120 bounds it below so that 2^-ex stays finite
-                // (such blocks still scale below 127).
+                // field; -112 bounds it below so that 2^(15-ex) stays a
+                // normal float (such blocks still scale below 127).
                 const int ebits = (int)(__float_as_uint(amax * (1.0f / 127.0f)) >> 23);
-                const int ex = amax > 0.f ? max(ebits - 126, -120) : 0;
-                const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
-                // Per value: s1 = shifter + rint(v/s_b); r1 = v/s_b − rint(·)
-                // exactly; s2 = shifter + rint(128·r1); r2 = 128·r1 − rint(·)
-                // exactly; s3 = shifter + rint(128·r2).  Each FMA's product is
-                // exact (power-of-two factors), so each rounds only once.
-                uint32_t w1[2], w2[2], w3[2];
+                const int ex = amax > 0.f ? max(ebits - 126, -112) : 0;
+                const float inv = __uint_as_float((uint32_t)(127 + 15 - ex) << 23);  // 2^(15-ex)
+                // n = rint(v·2^(15-ex)) with one FMA (exact product, one
+                // rounding); its three low bytes are the planes' digits.
+                uint32_t nb_[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) nb_[i] = __float_as_uint(fmaf(v[i], inv, kShifter)) - kShifterBits;
+                uint32_t w[3][2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    uint32_t b1[4], b2[4], b3[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float a = v[4 * k + i];
-                        const float s1 = fmaf(a, inv, kShifter);
-                        const float r1 = fmaf(a, inv, kShifter - s1);
-                        const float s2 = fmaf(r1, 128.0f, kShifter);
-                        const float r2 = fmaf(r1, 128.0f, kShifter - s2);
-                        const float s3 = fmaf(r2, 128.0f, kShifter);
-                        b1[i] = __float_as_uint(s1);
-                        b2[i] = __float_as_uint(s2);
-                        b3[i] = __float_as_uint(s3);
-                    }
-                    // Low byte of each shifted value, four to a word.
-                    w1[k] = __byte_perm(__byte_perm(b1[0], b1[1], 0x0040), __byte_perm(b1[2], b1[3], 0x0040), 0x5410);
-                    w2[k] = __byte_perm(__byte_perm(b2[0], b2[1], 0x0040), __byte_perm(b2[2], b2[3], 0x0040), 0x5410);
-                    w3[k] = __byte_perm(__byte_perm(b3[0], b3[1], 0x0040), __byte_perm(b3[2], b3[3], 0x0040), 0x5410);
+                    const uint32_t *n4 = nb_ + 4 * k;
+                    w[0][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0040), __byte_perm(n4[2], n4[3], 0x0040), 0x5410);
+                    w[1][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0051), __byte_perm(n4[2], n4[3], 0x0051), 0x5410);
+                    w[2][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0062), __byte_perm(n4[2], n4[3], 0x0062), 0x5410);
                 }
                 if (on) {
-                    // Unit-major layout: the 16-byte unit of half sub-block
-                    // h = e/2 (values 16h..16h+15) of plane q sits at unit
-                    // index (4q + h % 4)·nslabs + h / 4, so the eight lanes of
-                    // a quarter warp read eight consecutive units.
-                    const int h = e >> 1;
-                    uint2 *pu = reinterpret_cast<uint2 *>(reinterpret_cast<uint4 *>(planes) +
-                                                          (h & 3) * nslabs + (h >> 2)) + (e & 1);
-                    pu[0] = make_uint2(w1[0], w1[1]);
-                    pu[8 * nslabs] = make_uint2(w2[0], w2[1]);
-                    pu[16 * nslabs] = make_uint2(w3[0], w3[1]);
+                    // Slab-major layout: slab S = e/8 holds 12 units of 16
+                    // bytes, unit 4p + i covering plane p of values
+                    // 16i..16i+15 of the slab; this thread writes the half
+                    // e % 2 of unit i = (e/2) % 4 of each plane.
+                    uint2 *pu = reinterpret_cast<uint2 *>(planes + (e >> 3) * kPlaneSlabBytes) +
+                                2 * ((e >> 1) & 3) + (e & 1);
+                    pu[0] = make_uint2(w[0][0], w[0][1]);
+                    pu[8] = make_uint2(w[1][0], w[1][1]);
+                    pu[16] = make_uint2(w[2][0], w[2][1]);
                     if ((e & 3) == 0) sx[e / 4] = sum;
                     if ((e & 31) == 0) sb[e / 32] = __uint_as_float((uint32_t)(127 + ex) << 23);
                 }
@@ -403,12 +408,12 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
         {
             // This slab's 64 plane bytes per plane: positions 64j..64j+31
             // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
-            const uint4 *src = reinterpret_cast<const uint4 *>(planes) + (4 * b + j);
+            const uint4 *src = reinterpret_cast<const uint4 *>(planes + (4 * b + j) * kPlaneSlabBytes);
 #pragma unroll
             for (int pp = 0; pp < 3; ++pp) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 t = active ? src[(4 * pp + i) * nslabs] : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 t = active ? src[4 * pp + i] : make_uint4(0u, 0u, 0u, 0u);
                     pl[pp][4 * i] = (int)t.x;
                     pl[pp][4 * i + 1] = (int)t.y;
                     pl[pp][4 * i + 2] = (int)t.z;
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
         const LaneScaleSel lsel = lane_scale_sel(j);
-        const float dscale = s_blk * (1.0f / 128.0f);
+        const float unit = s_blk * (1.0f / 32768.0f);
 
         const int npasses = (nrows + pass_rows - 1) / pass_rows;
         // Stage, slot and phase of the current pass, advanced without
@@ -448,8 +453,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
                 rows = min(p.stage_rows, nrows - st * p.stage_rows);
             }
             const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
-            float pa = slab_row(stage_base + min(ra, rows - 1) * row_bytes, j, lsel, dscale, pl, sum_lo, sum_hi);
-            float pb = slab_row(stage_base + min(rb, rows - 1) * row_bytes, j, lsel, dscale, pl, sum_lo, sum_hi);
+            float pa = slab_row(stage_base + min(ra, rows - 1) * row_bytes, j, lsel, unit, pl, sum_lo, sum_hi);
+            float pb = slab_row(stage_base + min(rb, rows - 1) * row_bytes, j, lsel, unit, pl, sum_lo, sum_hi);
             if (!active || ra >= rows) pa = 0.f;
             if (!active || rb >= rows) pb = 0.f;
             // Two-row butterfly: lanes with (lane & half) == 0 finish with
@@ -748,7 +753,8 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
     const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
     p.x_staged = (size_t)K * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
-    const size_t xs_bytes = 3 * (size_t)K + (size_t)(K / 32) * sizeof(float) + (size_t)((p.nb * 4 + 15) & ~15) +
+    const size_t xs_bytes = (size_t)(K / 64) * kPlaneSlabBytes + (size_t)(K / 32) * sizeof(float) +
+                            (size_t)((p.nb * 4 + 15) & ~15) +
                             (p.x_staged ? (size_t)K * sizeof(float) : 0);
     const size_t part_bytes = wide ? (size_t)p.rows_per_cta * wc * sizeof(float) : 0;
     const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);

@@ -122,3 +122,33 @@ def test_special_case_min_only():
         y = q4k(x[:TT], W, K, N)
         want = -x[:TT].astype(np.float64).sum(1)
         assert np.abs(y - want[:, None]).max() <= 1e-5 * np.abs(x).sum()
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 11008])
+def test_one_token_wide_dynamic_range(K):
+    # One value per 256-value block 1000 times larger than the others.  The
+    # small activations still carry about 1% of each output, so the one-token
+    # kernel's rounding of x relative to each block's maximum must stay far
+    # below 1e-4 of the output scale (a split to 2^-14 of the block maximum
+    # would already miss the bound; dropping the small values misses it 100x).
+    N = 96
+    g = synth.rng(K + 1)
+    W = synth.q4k_weights(g, N, K)
+    x = g.uniform(-1.0, 1.0, size=(1, K)).astype(np.float32)
+    spikes = g.integers(0, 256, size=K // 256) + 256 * np.arange(K // 256)
+    x[0, spikes] = np.float32(1000.0) * np.sign(g.uniform(-1, 1, size=spikes.size)).astype(np.float32)
+    y = q4k(x, W, K, N)
+    assert_rows_close(y, oracle.q4k_matmul(x, W, K, N), REL, f"K{K} spikes")
+
+
+def test_one_token_integer_activations_near_exact():
+    # Integer activations up to 2^21 in magnitude are represented exactly by
+    # the one-token split, so the only error left is fp32 rounding of the
+    # scaled sums: far below the 1e-4 bound.
+    K, N = 4096, 128
+    g = synth.rng(77)
+    W = synth.q4k_weights(g, N, K)
+    x = g.integers(-(1 << 21), 1 << 21, size=(1, K)).astype(np.float32)
+    ref = oracle.q4k_matmul(x, W, K, N)
+    y = q4k(x, W, K, N)
+    assert_rows_close(y, ref, 2e-6, "integer activations")
