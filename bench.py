@@ -57,7 +57,7 @@ COMMON_SOURCES = ["common.cuh", "sync.cuh"]
 @dataclasses.dataclass
 class Workload:
     name: str
-    kind: str                 # "q4k" or "ternary"
+    kind: str                 # "q4k", "q4_0" or "ternary"
     entry: str                # C-ABI symbol called once per matrix
     mats: list                # (K, N) of each launch in one layer
     tokens: int
@@ -77,7 +77,11 @@ def _q4k_bytes(K, N):
 
 
 def weight_bytes(kind, K, N):
-    return _q4k_bytes(K, N) if kind == "q4k" else N * (K // 4)
+    if kind == "q4k":
+        return _q4k_bytes(K, N)
+    if kind == "q4_0":
+        return N * (K // 32) * 18
+    return N * (K // 4)
 
 
 T1_ARITH = ("fp32 activations rounded once to 2^-22 of each 256-value block's maximum and split into three "
@@ -85,13 +89,13 @@ T1_ARITH = ("fp32 activations rounded once to 2^-22 of each 256-value block's ma
 LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
 WORKLOADS = {w.name: w for w in [
     Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",
-             "q4k_gemv_t1_kernel", METRIC, ["q4k_gemv.cu"], "q4k_gemv_t1_4096x4096.md",
+             "gemv_t1_kernel", METRIC, ["q4k_gemv.cu"], "q4k_gemv_t1_4096x4096.md",
              distinct=64, arithmetic=T1_ARITH),
     Workload("q4k_gemv_4096x1024_t1", "q4k", "q4k_matmul", [(4096, 1024)], 1, 128, "GB/s", "hbm",
-             "q4k_gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 4096->1024, batch 1",
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 4096->1024, batch 1",
              ["q4k_gemv.cu"], arithmetic=T1_ARITH),
     Workload("q4k_gemv_1024x1024_t1", "q4k", "q4k_matmul", [(1024, 1024)], 1, 512, "GB/s", "hbm",
-             "q4k_gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 1024x1024, batch 1",
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 1024x1024, batch 1",
              ["q4k_gemv.cu"], arithmetic=T1_ARITH),
     Workload("q4k_prefill_tc_4096x11008_t64", "q4k", "q4k_matmul_tc", [(4096, 11008)], 64, 16,
              "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
@@ -102,6 +106,9 @@ WORKLOADS = {w.name: w for w in [
              "TFLOP/s", "alu", "q4k_mm_fp32_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu", "cluster.cuh"],
              "q4k_mm_fp32_4096x11008_t64.md", arithmetic="fp32 dequantization and fp32 FMA"),
+    Workload("q4_0_gemv_4096x4096_t1", "q4_0", "q4_0_gemv", [(4096, 4096)], 1, 64, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q4_0 GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
+             "q4_0_gemv_t1_4096x4096.md", distinct=64, arithmetic=T1_ARITH),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "ternary_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "batch 1", ["ternary_gemv.cu"], "ternary_t1_2560x6912.md", arithmetic="fp32"),
@@ -109,7 +116,7 @@ WORKLOADS = {w.name: w for w in [
              "hbm", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),
     Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
-             "q4k_gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
+             "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
              "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
     Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "hbm",
              "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
@@ -326,6 +333,8 @@ def host_inputs(w: Workload, seed: int = 0):
         n = max(1, w.distinct)
         if w.kind == "q4k":
             Ws = [synth.q4k_weights(g, N, K) for _ in range(n)]
+        elif w.kind == "q4_0":
+            Ws = [synth.q4_0_weights(g, N, K) for _ in range(n)]
         else:
             Ws = [synth.ternary_weights(g, N, K) for _ in range(n)]
         scale = float(synth.ternary_scale(g)) if w.kind == "ternary" else 1.0
@@ -341,7 +350,7 @@ def workload_config(w: Workload, plan: Plan) -> dict:
             "weight_bytes_per_step": plan.weight_bytes,
             "l2": f"inputs larger than L2: {plan.weight_bytes / 1e6:.0f} MB of weights per step "
                   f"(L2 129 MB), no flush",
-            "weights": f"random {'Q4_K blocks' if w.kind == 'q4k' else 'ternary codes'}, seed 0 "
+            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks').get(w.kind, 'ternary codes')}, seed 0 "
                        f"(synth), {w.distinct} distinct host copies per matrix",
             "activations": "fp32 N(0,1), seed 0"}
 
@@ -350,6 +359,8 @@ def oracle_call(w: Workload, K, N, W, x, scale, rows, r0=0):
     import oracle
     if w.kind == "q4k":
         oracle.q4k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
+    elif w.kind == "q4_0":
+        oracle.q4_0_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
     else:
         oracle.ternary_gemv(x, W.reshape(N, -1)[r0:r0 + rows], scale, K, rows)
 
@@ -465,7 +476,7 @@ def run_ours(a) -> None:
     wp, xp, yp = W.data_ptr(), x.data_ptr(), y.data_ptr()
     calls = []
     for K, N, wo, xo, yo, m in plan.launches:
-        if w.kind == "q4k":
+        if w.kind != "ternary":
             calls.append((xp + 4 * xo, wp + wo, yp + 4 * yo, K, N, w.tokens, sp))
         else:
             calls.append((xp + 4 * xo, wp + wo, mats[m][2], yp + 4 * yo, K, N, w.tokens, sp))

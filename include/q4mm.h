@@ -112,6 +112,36 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
 int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,
                   int tokens, q4mm_stream_t stream);
 
+/* Largest inputDim accepted by q4_0_gemv. */
+#define Q4MM_Q4_0_MAX_INPUT_DIM 32768
+
+/*
+ * q4_0_gemv — y = x·Wᵀ with W in Q4_0, FP32 result.
+ *
+ * The block is the one SKaiNET PR #562 names as its follow-up (section "Out
+ * of scope": Q4_0, "same algorithm, simpler block", 32 values in 18 bytes).
+ * The page gives no byte layout; this library reads it as ggml's: fp16 d
+ * (little-endian), then 16 bytes qs; element l (l < 16) of a block is the low
+ * nibble of qs[l] and element 16 + l its high nibble (the same strided
+ * pattern as the Q4_K slabs); w = d·(q − 8), i.e. scale d and offset 8·d in
+ * the page's lazy form.
+ *
+ * w_q4_0 : N·(K/32) blocks of 18 bytes, each row contiguous.  16-byte aligned.
+ * x      : 16-byte aligned.  y: 4-byte aligned.
+ * Limits: inputDim a positive multiple of 256 and <= Q4MM_Q4_0_MAX_INPUT_DIM
+ *         (the one-token kernel's geometry: 256 values occupy 144 bytes of a
+ *         row, as in Q4_K); outputDim >= 1; tokens >= 1.
+ * Precision: as the one-token path of q4k_matmul: per token row,
+ *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|, with x rounded once
+ *         to 2^-22 of each 256-value block's largest magnitude and integer
+ *         code-dots.
+ * Tokens: each token is its own pass over the weights (a decode GEMV; no
+ *         weight reuse across tokens).
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int outputDim,
+              int tokens, q4mm_stream_t stream);
+
 /* Size of the fixed device array that q4k_matmul_tc_noalloc uses as scratch. */
 #define Q4MM_TC_NOALLOC_SCRATCH_BYTES (16u << 20)
 

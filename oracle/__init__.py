@@ -72,6 +72,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i64, i64, i64, vp, i32]
             fn.restype = i32
+        lib.oracle_q4_0_dequant_block.argtypes = [vp, vp]
+        lib.oracle_q4_0_dequant_block.restype = None
+        lib.oracle_q4_0_dequant.argtypes = [vp, i64, i64, vp]
+        lib.oracle_q4_0_dequant.restype = i32
+        lib.oracle_q4_0_matmul.argtypes = [vp, vp, i64, i64, i64, vp, i32]
+        lib.oracle_q4_0_matmul.restype = i32
+        lib.oracle_q4_0_pack_block.argtypes = [ctypes.c_uint16, vp, vp]
+        lib.oracle_q4_0_pack_block.restype = None
         lib.oracle_ternary_gemv.argtypes = [vp, vp, flt, i64, i64, i64, vp, vp, i32]
         lib.oracle_ternary_gemv.restype = i32
         lib.oracle_q4k_pack_block.argtypes = [ctypes.c_uint16, ctypes.c_uint16, vp, vp, vp, vp]
@@ -148,6 +156,48 @@ def q4k_matmul_bf16(x, W, K, N, threads=0, lib=None) -> np.ndarray:
 def q4k_matmul_lazy(x, W, K, N, threads=0, lib=None) -> np.ndarray:
     """The lazy-dmin form (scale·Σxq − offset·Σx per sub-block), double."""
     return _matmul("oracle_q4k_matmul_lazy", x, W, K, N, threads, lib)
+
+
+Q40_VALUES, Q40_BYTES = 32, 18
+
+
+def _check_q4_0(W: np.ndarray, K: int, N: int) -> np.ndarray:
+    if K <= 0 or K % Q40_VALUES:
+        raise ValueError(f"inputDim {K} is not a positive multiple of {Q40_VALUES}")
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    if W.size != N * (K // Q40_VALUES) * Q40_BYTES:
+        raise ValueError("weight bytes do not match N·K/32·18")
+    return W
+
+
+def q4_0_dequant(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
+    """Dequantized fp32 Q4_0 weight [N, K]."""
+    W = _check_q4_0(W, K, N)
+    out = np.empty((N, K), np.float32)
+    if (lib or load()).oracle_q4_0_dequant(_ptr(W), K, N, _ptr(out)) != 0:
+        raise ValueError("oracle_q4_0_dequant rejected its arguments")
+    return out
+
+
+def q4_0_matmul(x, W, K, N, threads=0, lib=None) -> np.ndarray:
+    """y = x · dequant_q4_0(W)ᵀ, double accumulation; returns float64 [T, N]."""
+    W = _check_q4_0(W, K, N)
+    x = _check_x(x, K)
+    T = x.shape[0]
+    y = np.empty((T, N), np.float64)
+    rc = (lib or load()).oracle_q4_0_matmul(_ptr(x), _ptr(W), K, N, T, _ptr(y), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_q4_0_matmul failed with {rc}")
+    return y
+
+
+def q4_0_pack_block(d_bits: int, q, lib=None) -> np.ndarray:
+    """Encode one 18-byte Q4_0 block from d (fp16 bits) and 32 codes (0..15)."""
+    q = np.ascontiguousarray(q, dtype=np.int32)
+    assert q.size == Q40_VALUES
+    out = np.zeros(Q40_BYTES, np.uint8)
+    (lib or load()).oracle_q4_0_pack_block(d_bits, _ptr(q), _ptr(out))
+    return out
 
 
 def ternary_gemv(x, W, scale, K, N, threads=0, lib=None):

@@ -26,6 +26,8 @@
  *    out[o] = Σ_k in[k]·code(o,k) with the scale NOT applied, inputDim % 4 == 0,
  *    code = ((byte >> 2·(i%4)) & 3) − 1, fp32 accumulate, then one multiply by
  *    the BitNet scale; prefill loops rows advancing by r·k and r·n).
+ *  - Q4_0, the 32-value / 18-byte block named as the follow-up in the same
+ *    PR (section "Out of scope"); layout read as ggml's (see its section).
  *  - x·Wᵀ with W stored [out, in] and used in place (SKaiNET docs "Eager
  *    execution: backends and kernels", the paragraph on the dense x·Wᵀ row).
  *
@@ -275,7 +277,90 @@ int oracle_ternary_gemv(const float *x, const uint8_t *W, float scale, int64_t K
     return 0;
 }
 
+/* ------------------------------------------------------------------------
+ * Q4_0 (SKaiNET PR #562, section "Out of scope": the simpler 32-value,
+ * 18-byte block that runs the same algorithm).  The page gives only the block
+ * size; the byte layout is the ggml canonical one the PR builds on: fp16 d
+ * (little-endian), then 16 bytes qs; element l (l < 16) is the low nibble of
+ * qs[l] and element 16 + l its high nibble (the same strided pattern as the
+ * Q4_K slabs), and w = d·(q − 8).  In the page's lazy form this is scale d
+ * and offset 8·d per block.
+ * ------------------------------------------------------------------------ */
+#define Q40_VALUES 32
+#define Q40_BYTES 18
+
+static int q40_code(const uint8_t *qs, int e)
+{
+    return e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);
+}
+
+/* Dequantize one 18-byte block: w[e] = d·(q_e − 8), exact in double (11-bit
+ * d times a 4-bit integer) and rounded once to float. */
+void oracle_q4_0_dequant_block(const uint8_t *blk, float w[Q40_VALUES])
+{
+    double d = oracle_fp16_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    for (int e = 0; e < Q40_VALUES; ++e)
+        w[e] = (float)(d * (q40_code(blk + 2, e) - 8));
+}
+
+/* W [N][K/32 blocks] → out [N][K] fp32. Returns 0, or -1 on bad sizes. */
+int oracle_q4_0_dequant(const uint8_t *W, int64_t K, int64_t N, float *out)
+{
+    if (K <= 0 || N <= 0 || K % Q40_VALUES)
+        return -1;
+    int64_t nb = K / Q40_VALUES;
+    for (int64_t o = 0; o < N; ++o)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_q4_0_dequant_block(W + (o * nb + b) * Q40_BYTES, out + o * K + b * Q40_VALUES);
+    return 0;
+}
+
+/* y[t][o] = Σ_k x[t][k]·w[o][k], w the fp32 dequantized Q4_0 weight, summed
+ * sequentially in k with a double accumulator (dequantize-then-matmul). */
+int oracle_q4_0_matmul(const float *x, const uint8_t *W, int64_t K, int64_t N, int64_t T,
+                       double *y, int nthreads)
+{
+    if (K <= 0 || N <= 0 || T <= 0 || K % Q40_VALUES)
+        return -1;
+    int64_t nb = K / Q40_VALUES;
+    int nt = set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel num_threads(nt)
+    {
+        float *w = (float *)malloc((size_t)K * sizeof(float));
+        if (!w) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t o = 0; o < N; ++o) {
+            if (!w)
+                continue;
+            for (int64_t b = 0; b < nb; ++b)
+                oracle_q4_0_dequant_block(W + (o * nb + b) * Q40_BYTES, w + b * Q40_VALUES);
+            for (int64_t t = 0; t < T; ++t) {
+                const float *xt = x + t * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (double)xt[k] * (double)w[k];
+                y[t * N + o] = acc;
+            }
+        }
+        free(w);
+    }
+    return failed ? -2 : 0;
+}
+
 /* Encoders, used only to build hand-worked fixtures in the tests. */
+
+/* Pack one Q4_0 block from d's fp16 bits and 32 codes (0..15). */
+void oracle_q4_0_pack_block(uint16_t d_bits, const int q[Q40_VALUES], uint8_t out[Q40_BYTES])
+{
+    out[0] = d_bits & 255;
+    out[1] = d_bits >> 8;
+    for (int l = 0; l < 16; ++l)
+        out[2 + l] = (uint8_t)((q[l] & 15) | ((q[16 + l] & 15) << 4));
+}
 
 /* Pack one Q4_K block from its parts (inverse of the unpacking above). */
 void oracle_q4k_pack_block(uint16_t d_bits, uint16_t dmin_bits, const int sc[8], const int m[8],

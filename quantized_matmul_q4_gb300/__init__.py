@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     q4k_matmul_tc_ptr,
     q4k_matmul_tc_noalloc,
     q4k_matmul_tc_noalloc_ptr,
+    q4_0_gemv,
+    q4_0_gemv_ptr,
     ternary_gemv,
     ternary_gemv_ptr,
     version,

@@ -8,7 +8,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 Q4K_VALUES = 256
 Q4K_BYTES = 144
 
-_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "ternary_gemv",
+_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "ternary_gemv",
             "q4mm_last_error", "q4mm_device_status", "q4mm_version")
 
 
@@ -32,7 +32,7 @@ def _load() -> ctypes.CDLL:
             "(needs nvcc); there is no fallback implementation")
     lib = ctypes.CDLL(path)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc"):
+    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         fn.restype = i32
@@ -88,6 +88,10 @@ def q4k_matmul_tc_noalloc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, st
     _check(_LIB.q4k_matmul_tc_noalloc(x, w, y, K, N, T, stream))
 
 
+def q4_0_gemv_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
+    _check(_LIB.q4_0_gemv(x, w, y, K, N, T, stream))
+
+
 def ternary_gemv_ptr(x: int, w: int, scale: float, y: int, K: int, N: int, T: int,
                      stream: int = 0) -> None:
     _check(_LIB.ternary_gemv(x, w, ctypes.c_float(scale), y, K, N, T, stream))
@@ -140,6 +144,16 @@ def q4k_matmul_tc_noalloc(x, w, N: int | None = None, out=None, stream=None):
     (no allocation; calls that overlap on the GPU race on that array)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q4K_BYTES, out, N)
     q4k_matmul_tc_noalloc_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+Q40_VALUES, Q40_BYTES = 32, 18
+
+
+def q4_0_gemv(x, w, N: int | None = None, out=None, stream=None):
+    """y[T, N] = x[T, K] · dequant_q4_0(W)ᵀ in FP32 (one weight pass per token)."""
+    x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q40_VALUES) * Q40_BYTES, out, N)
+    q4_0_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
     return out.view(T, N)
 
 

@@ -189,6 +189,24 @@ int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int input
     return Q4MM_OK;
 }
 
+int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int outputDim, int tokens,
+              q4mm_stream_t stream) {
+    int rc = check_common(x, w_q4_0, y, inputDim, outputDim, tokens, 256,
+                          (size_t)(inputDim / 32) * 18, 16);
+    if (rc) return rc;
+    if (inputDim > Q4MM_Q4_0_MAX_INPUT_DIM)
+        return fail(Q4MM_ERR_DIM, "inputDim %d exceeds the Q4_0 limit %d", inputDim, Q4MM_Q4_0_MAX_INPUT_DIM);
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    const uint8_t *W = static_cast<const uint8_t *>(w_q4_0);
+    for (int t = 0; t < tokens; ++t) {
+        const cudaError_t e = q4mm::launch_q4_0_gemv_t1(ctx, x + (size_t)t * inputDim, W,
+                                                        y + (size_t)t * outputDim, inputDim, outputDim);
+        if (e != cudaSuccess) return fail_cuda(e, "q4_0_gemv launch");
+    }
+    return Q4MM_OK;
+}
+
 int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,
                  int outputDim, int tokens, q4mm_stream_t stream) {
     int rc = check_common(x, w_packed, y, inputDim, outputDim, tokens, 4, (size_t)inputDim / 4, 1);

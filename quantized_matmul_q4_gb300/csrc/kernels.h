@@ -21,6 +21,11 @@ struct LaunchCtx {
 cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                int K, int N);
 
+// Q4_0 decode GEMV, one token (same kernel as the Q4_K one with the Q4_0
+// row format).  cudaErrorNotSupported when the shape is outside its geometry.
+cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                int K, int N);
+
 // Q4_K decode GEMV for 1..8 tokens with x staged in shared memory.
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                   int K, int N, int T);

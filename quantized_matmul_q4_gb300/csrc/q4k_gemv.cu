@@ -22,6 +22,7 @@
 // is (256·d·sc_s)·acc_s − (128·d·sc_s + dmin·m_s)·Σx_s where
 // acc_s = Σ x·(0.5 + q/256).
 #include <cstdlib>
+#include <type_traits>
 #include <utility>
 
 #include "common.cuh"
@@ -199,6 +200,71 @@ __device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneS
                 -fmaf(r.o0, sum_lo, r.o1 * sum_hi));
 }
 
+// Row formats of the one-token kernel.  Both spend 144 bytes on every 256
+// values of a row, so rows, stages and slab lanes have the same geometry;
+// lane (b, j) covers values 64j..64j+63 of the 256-value group b, and
+// row() returns that lane's share of one row, given the group's first byte.
+
+// Q4_K: the group is one super-block; the lane reads the header and qs slab j.
+struct FmtQ4K {
+    struct Lane {
+        LaneScaleSel sel;
+        int j;
+    };
+    __device__ static Lane lane(int j) { return Lane{lane_scale_sel(j), j}; }
+    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
+                                float sum_lo, float sum_hi) {
+        return slab_row(grp, L.j, L.sel, unit, pl, sum_lo, sum_hi);
+    }
+};
+
+// Q4_0: the group is eight 18-byte blocks; the lane's 64 values are blocks
+// 2j and 2j+1 (bytes 36j..36j+35, 4-byte aligned): block A = values 0..31
+// (its 16 qs bytes start 2 bytes in, so its words come out of funnel shifts),
+// block B = values 32..63 (qs 4-byte aligned at byte 20).  Per block,
+// Σ w·x = d·(Σ q·x − 8·Σ x).
+struct FmtQ40 {
+    struct Lane {
+        int j;
+    };
+    __device__ static Lane lane(int j) { return Lane{j}; }
+    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
+                                float sum_lo, float sum_hi) {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(grp + 36 * L.j);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = p[i];
+        const float2 dd = __half22float2(__halves2half2(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)),
+                                                        __ushort_as_half((unsigned short)(w[4] >> 16))));
+        uint32_t qa[4], qb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            qa[k] = __funnelshift_r(w[k], w[k + 1], 16);
+            qb[k] = w[5 + k];
+        }
+        int da_lo[3] = {0, 0, 0}, da_hi[3] = {0, 0, 0}, db_lo[3] = {0, 0, 0}, db_hi[3] = {0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t al = qa[k] & 0x0F0F0F0Fu, ah = qa[k] & 0xF0F0F0F0u;
+            const uint32_t bl = qb[k] & 0x0F0F0F0Fu, bh = qb[k] & 0xF0F0F0F0u;
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                da_lo[pp] = dp4a_uu(al, (uint32_t)pl[pp][k], da_lo[pp]);
+                da_hi[pp] = dp4a_uu(ah, (uint32_t)pl[pp][4 + k], da_hi[pp]);
+                db_lo[pp] = dp4a_uu(bl, (uint32_t)pl[pp][8 + k], db_lo[pp]);
+                db_hi[pp] = dp4a_uu(bh, (uint32_t)pl[pp][12 + k], db_hi[pp]);
+            }
+            da_lo[2] = dp4a_us(al, pl[2][k], da_lo[2]);
+            da_hi[2] = dp4a_us(ah, pl[2][4 + k], da_hi[2]);
+            db_lo[2] = dp4a_us(bl, pl[2][8 + k], db_lo[2]);
+            db_hi[2] = dp4a_us(bh, pl[2][12 + k], db_hi[2]);
+        }
+        const float qa_x = fmaf(plane_combine(da_hi), 0.0625f, plane_combine(da_lo));
+        const float qb_x = fmaf(plane_combine(db_hi), 0.0625f, plane_combine(db_lo));
+        return fmaf(dd.x, fmaf(unit, qa_x, -8.0f * sum_lo), dd.y * fmaf(unit, qb_x, -8.0f * sum_hi));
+    }
+};
+
 // Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter:
 // the float's bits are 0x4B400000 + rint(v).
 constexpr float kShifter = 12582912.0f;
@@ -227,8 +293,8 @@ struct T1Params {
 constexpr int kT1RoleWarps = 1;  // the copy warp
 constexpr int kT1MaxCw = 16;     // compute warps at most
 
-template <int kNB>
-__global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1_kernel(T1Params p) {
+template <class Fmt, int kNB>
+__global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
     __shared__ int issued;  // weight stages issued so far (for the abort drain)
@@ -424,7 +490,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
             sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
-        const LaneScaleSel lsel = lane_scale_sel(j);
+        const typename Fmt::Lane lfmt = Fmt::lane(j);
         const float unit = s_blk * (1.0f / 32768.0f);
 
         const int npasses = (nrows + pass_rows - 1) / pass_rows;
@@ -453,8 +519,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) q4k_gemv_t1
                 rows = min(p.stage_rows, nrows - st * p.stage_rows);
             }
             const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
-            float pa = slab_row(stage_base + min(ra, rows - 1) * row_bytes, j, lsel, unit, pl, sum_lo, sum_hi);
-            float pb = slab_row(stage_base + min(rb, rows - 1) * row_bytes, j, lsel, unit, pl, sum_lo, sum_hi);
+            float pa = Fmt::row(stage_base + min(ra, rows - 1) * row_bytes, lfmt, unit, pl, sum_lo, sum_hi);
+            float pb = Fmt::row(stage_base + min(rb, rows - 1) * row_bytes, lfmt, unit, pl, sum_lo, sum_hi);
             if (!active || ra >= rows) pa = 0.f;
             if (!active || rb >= rows) pb = 0.f;
             // Two-row butterfly: lanes with (lane & half) == 0 finish with
@@ -719,8 +785,8 @@ int next_pow2(int v) {
 
 }  // namespace
 
-cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
-                               int K, int N) {
+template <class Fmt>
+cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
     T1Params p;
     p.x = x;
     p.W = W;
@@ -774,14 +840,30 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
         if (e != cudaSuccess) return e;
         return launch_kernel(c, kernel, dim3(grid), block, smem, p);
     };
-    switch (p.nb) {
-        case 4: return go(q4k_gemv_t1_kernel<4>);
-        case 8: return go(q4k_gemv_t1_kernel<8>);
-        case 16: return go(q4k_gemv_t1_kernel<16>);
-        case 32: return go(q4k_gemv_t1_kernel<32>);
-        case 43: return go(q4k_gemv_t1_kernel<43>);
-        default: return go(q4k_gemv_t1_kernel<0>);
+    if constexpr (std::is_same<Fmt, FmtQ4K>::value) {
+        switch (p.nb) {
+            case 4: return go(gemv_t1_kernel<Fmt, 4>);
+            case 8: return go(gemv_t1_kernel<Fmt, 8>);
+            case 16: return go(gemv_t1_kernel<Fmt, 16>);
+            case 32: return go(gemv_t1_kernel<Fmt, 32>);
+            case 43: return go(gemv_t1_kernel<Fmt, 43>);
+            default: return go(gemv_t1_kernel<Fmt, 0>);
+        }
+    } else {
+        switch (p.nb) {
+            case 16: return go(gemv_t1_kernel<Fmt, 16>);
+            case 43: return go(gemv_t1_kernel<Fmt, 43>);
+            default: return go(gemv_t1_kernel<Fmt, 0>);
+        }
     }
+}
+
+cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
+    return launch_gemv_t1<FmtQ4K>(c, x, W, y, K, N);
+}
+
+cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
+    return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N);
 }
 
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,

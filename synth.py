@@ -13,6 +13,9 @@ qs bytes give exactly the distribution the workloads call for: the 12-byte
 independent, and uniform qs bytes mean every 4-bit code is uniform on 0..15.
 d ~ U[1e-3, 1e-2] and dmin ~ U[0, 1e-2] are rounded to fp16 by numpy.
 
+Q4_0 weights are 18-byte blocks: fp16 d ~ U[1e-3, 1e-2] and 16 uniform qs
+bytes (every 4-bit code uniform on 0..15).
+
 Ternary weights are drawn uniformly from the 81 byte values whose four 2-bit
 fields are all 0, 1 or 2 — the same as drawing each code uniformly from
 {-1, 0, +1} independently.
@@ -44,6 +47,23 @@ def q4k_weights(g: np.random.Generator, N: int, K: int,
     blocks[:, :, 4:16] = scales
     blocks[:, :, 16:144] = qs
     return blocks.reshape(N, nb * Q4K_BYTES)
+
+
+Q40_VALUES = 32
+Q40_BYTES = 18
+
+
+def q4_0_weights(g: np.random.Generator, N: int, K: int, d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Random Q4_0 weight: uint8 [N, K/32·18], rows of contiguous 18-byte
+    blocks (fp16 d ~ U[1e-3, 1e-2], then 16 uniform qs bytes)."""
+    assert K % Q40_VALUES == 0 and K > 0 and N > 0
+    nb = K // Q40_VALUES
+    d = g.uniform(d_range[0], d_range[1], size=(N, nb)).astype("<f2")
+    qs = g.integers(0, 256, size=(N, nb, 16), dtype=np.uint8)
+    blocks = np.empty((N, nb, Q40_BYTES), np.uint8)
+    blocks[:, :, 0:2] = d.view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:18] = qs
+    return blocks.reshape(N, nb * Q40_BYTES)
 
 
 def _valid_ternary_bytes() -> np.ndarray:
@@ -82,6 +102,7 @@ WORKLOADS = {
     "q4k_gemv_4096x1024_t1": dict(kind="q4k", K=4096, N=1024, T=1),
     "q4k_gemv_4096x4096_t1": dict(kind="q4k", K=4096, N=4096, T=1),
     "q4k_prefill_4096x11008_t64": dict(kind="q4k", K=4096, N=11008, T=64),
+    "q4_0_gemv_4096x4096_t1": dict(kind="q4_0", K=4096, N=4096, T=1),
     "ternary_gemv_2560x6912_t1": dict(kind="ternary", K=2560, N=6912, T=1),
     "ternary_gemv_2560x6912_t16": dict(kind="ternary", K=2560, N=6912, T=16),
 }
@@ -117,3 +138,16 @@ def ternary_case(name_or_dims, seed: int = 0, xkind: str = "normal"):
     scale = ternary_scale(g)
     x = activations(g, T, K, xkind)
     return x, W, scale, K, N, T
+
+
+def q4_0_case(name_or_dims, seed: int = 0, xkind: str = "normal"):
+    """(x, W, K, N, T) with a Q4_0 weight, for a named workload or (K, N, T)."""
+    if isinstance(name_or_dims, str):
+        w = WORKLOADS[name_or_dims]
+        K, N, T = w["K"], w["N"], w["T"]
+    else:
+        K, N, T = name_or_dims
+    g = rng(seed)
+    W = q4_0_weights(g, N, K)
+    x = activations(g, T, K, xkind)
+    return x, W, K, N, T

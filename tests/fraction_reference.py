@@ -84,3 +84,30 @@ def ternary_codes(row: bytes, K: int):
         field = (row[i // 4] >> (2 * (i % 4))) & 3
         codes.append(field - 1)
     return codes
+
+
+def q4_0_block_values(blk: bytes):
+    """The 32 exact values of one Q4_0 block: fp16 d, then 16 bytes whose low
+    nibbles are elements 0..15 and high nibbles elements 16..31; w = d·(q − 8)."""
+    blk = bytes(blk)
+    d = fp16(blk[0] | blk[1] << 8)
+    vals = [None] * 32
+    for l, byte in enumerate(blk[2:18]):
+        vals[l] = d * (byte % 16 - 8)
+        vals[16 + l] = d * (byte // 16 - 8)
+    return vals
+
+
+def q4_0_matmul(x_rows, W_rows, K: int):
+    """y[t][o] exactly from Q4_0 rows (each weight exact in fp32 already)."""
+    y = []
+    for xt in x_rows:
+        row_out = []
+        for wrow in W_rows:
+            acc = Fraction(0)
+            for b in range(K // 32):
+                for e, v in enumerate(q4_0_block_values(wrow[18 * b:18 * (b + 1)])):
+                    acc += Fraction(float(xt[32 * b + e])) * v
+            row_out.append(acc)
+        y.append(row_out)
+    return y

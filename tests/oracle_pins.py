@@ -13,7 +13,10 @@ Sources of the facts:
     differently ordered computations;
   * integer counts for the ternary code-dot (SKaiNET issue #1138, section
     "Tests": exact equality on the code-dot for integer activations);
-  * an exact-rational brute force (tests/fraction_reference.py).
+  * an exact-rational brute force (tests/fraction_reference.py);
+  * for Q4_0 (SKaiNET PR #562, section "Out of scope"): a hand-worked block,
+    nibble positions, and equality with the Q4_K oracle on blocks that both
+    formats can express.
 """
 from __future__ import annotations
 
@@ -243,9 +246,77 @@ def pin_bf16_variant(lib):
     assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max()
 
 
+def pin_q4_0_handworked(lib):
+    fx = fixtures.read("q4_0_handworked_block.txt")
+    q = list(range(16)) + [(7 + l) % 16 for l in range(16)]
+    blk = oracle.q4_0_pack_block(int(fx["d_bits"], 16), q, lib=lib)
+    assert list(blk[2:6]) == fixtures.hexbytes(fx["qs_0_3"])
+    assert blk[17] == fixtures.hexbytes(fx["qs_15"])[0]
+    w = oracle.q4_0_dequant(blk, 32, 1, lib=lib)[0]
+    for e in (0, 15, 16, 31):
+        assert w[e] == float(fx[f"w_{e}"]), (e, w[e])
+    ones = np.ones((1, 32), np.float32)
+    assert oracle.q4_0_matmul(ones, blk, 32, 1, lib=lib)[0, 0] == float(fx["sum_w"])
+    x = np.array([[(e % 3) - 1 for e in range(32)]], np.float32)
+    assert oracle.q4_0_matmul(x, blk, 32, 1, lib=lib)[0, 0] == float(fx["y_x_mod3"])
+
+
+def pin_q4_0_nibble_positions(lib):
+    # Byte l = 0xAB with every other byte 0x88 (code 8, value 0) and d = 1:
+    # element l is 11 − 8 = 3 and element 16 + l is 10 − 8 = 2, the rest 0.
+    for l in (0, 5, 15):
+        blk = np.full(18, 0x88, np.uint8)
+        blk[0:2] = [0x00, 0x3C]
+        blk[2 + l] = 0xAB
+        w = oracle.q4_0_dequant(blk, 32, 1, lib=lib)[0]
+        want = np.zeros(32, np.float32)
+        want[l], want[16 + l] = 3.0, 2.0
+        assert np.array_equal(w, want), l
+
+
+def pin_q4_0_as_q4k(lib):
+    # Eight Q4_0 blocks sharing one d are the Q4_K block with that d, every
+    # scale 1, dmin = d and every min 8 (w = d·q − d·8), the codes in the
+    # same element order: an independent check against the Q4_K oracle,
+    # itself pinned by the hand-worked Q4_K block above.
+    g = np.random.default_rng(23)
+    N, K = 3, 512
+    rows40, rowsk = [], []
+    for _ in range(N):
+        r40, rk = [], []
+        for b in range(K // 256):
+            d_bits = int(g.integers(0x1C00, 0x2C00))
+            codes = g.integers(0, 16, 256)
+            for i in range(8):
+                r40.append(oracle.q4_0_pack_block(d_bits, codes[32 * i:32 * i + 32], lib=lib))
+            rk.append(oracle.q4k_pack_block(d_bits, d_bits, [1] * 8, [8] * 8, codes, lib=lib))
+        rows40.append(np.concatenate(r40))
+        rowsk.append(np.concatenate(rk))
+    W40, Wk = np.stack(rows40), np.stack(rowsk)
+    assert np.array_equal(oracle.q4_0_dequant(W40, K, N, lib=lib), oracle.q4k_dequant(Wk, K, N, lib=lib))
+    x = g.standard_normal((2, K)).astype(np.float32)
+    assert np.array_equal(oracle.q4_0_matmul(x, W40, K, N, lib=lib), oracle.q4k_matmul(x, Wk, K, N, lib=lib))
+
+
+def pin_q4_0_fraction_bruteforce(lib):
+    g = np.random.default_rng(29)
+    for K, N, T in ((32, 2, 2), (96, 3, 1)):
+        W = np.stack([np.concatenate([oracle.q4_0_pack_block(int(g.integers(0x1800, 0x3000)),
+                                                             g.integers(0, 16, 32), lib=lib)
+                                      for _ in range(K // 32)]) for _ in range(N)])
+        x = g.standard_normal((T, K)).astype(np.float32)
+        y = oracle.q4_0_matmul(x, W, K, N, lib=lib)
+        exact = fr.q4_0_matmul(x.tolist(), [bytes(r) for r in W], K)
+        for t in range(T):
+            for o in range(N):
+                e = exact[t][o]
+                assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
+
+
 ALL_PINS = [
     pin_fp16_decode, pin_bf16_round, pin_handworked_pack, pin_handworked_values,
     pin_nibble_positions, pin_scale_positions, pin_special_cases, pin_one_hot_rows,
     pin_lazy_equals_direct, pin_fraction_bruteforce, pin_ternary_handworked,
     pin_ternary_integer_count, pin_ternary_scale, pin_bf16_variant,
+    pin_q4_0_handworked, pin_q4_0_nibble_positions, pin_q4_0_as_q4k, pin_q4_0_fraction_bruteforce,
 ]

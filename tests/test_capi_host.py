@@ -116,3 +116,10 @@ def test_noalloc_refuses_oversize_before_any_cuda_call(q4mm):
     with pytest.raises(q4mm.Q4mmError) as e:
         q4mm.q4k_matmul_tc_noalloc_ptr(X, W, Y, 300, 16, 1, 0)
     assert e.value.code == DIM and "inputDim" in q4mm.last_error()
+
+
+@pytest.mark.parametrize("K", [0, 32, 128, 300, 32768 + 256])
+def test_q4_0_rejects_bad_input_dim(q4mm, K):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4_0_gemv_ptr(X, W, Y, K, 16, 1, 0)
+    assert e.value.code == DIM and "inputDim" in q4mm.last_error()

@@ -36,6 +36,14 @@ MUTANTS = {
     "ternary_offset": ("return ((row[i / 4] >> (2 * (i % 4))) & 3) - 1;",
                        "return ((row[i / 4] >> (2 * (i % 4))) & 3);"),
     "bf16_truncates": ("u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;", "u = u & 0xFFFF0000u;"),
+    "q4_0_nibble_halves": ("return e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);",
+                           "return e < 16 ? (qs[e] >> 4) : (qs[e - 16] & 15);"),
+    "q4_0_offset": ("w[e] = (float)(d * (q40_code(blk + 2, e) - 8));",
+                    "w[e] = (float)(d * (q40_code(blk + 2, e) - 7));"),
+    "q4_0_d_bytes": ("double d = oracle_fp16_to_double((uint16_t)(blk[0] | (blk[1] << 8)));\n    for (int e = 0; e < Q40_VALUES",
+                     "double d = oracle_fp16_to_double((uint16_t)(blk[1] | (blk[0] << 8)));\n    for (int e = 0; e < Q40_VALUES"),
+    "q4_0_block_stride": ("oracle_q4_0_dequant_block(W + (o * nb + b) * Q40_BYTES, w + b * Q40_VALUES);",
+                          "oracle_q4_0_dequant_block(W + (o * nb + b) * 16, w + b * Q40_VALUES);"),
 }
 
 
