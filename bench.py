@@ -57,7 +57,7 @@ COMMON_SOURCES = ["common.cuh", "sync.cuh"]
 @dataclasses.dataclass
 class Workload:
     name: str
-    kind: str                 # "q4k", "q4_0" or "ternary"
+    kind: str                 # "q4k", "q4_0", "q4k_ffn" (gate + up, fused SwiGLU) or "ternary"
     entry: str                # C-ABI symbol called once per matrix
     mats: list                # (K, N) of each launch in one layer
     tokens: int
@@ -81,6 +81,8 @@ def weight_bytes(kind, K, N):
         return _q4k_bytes(K, N)
     if kind == "q4_0":
         return N * (K // 32) * 18
+    if kind == "q4k_ffn":
+        return 2 * _q4k_bytes(K, N)
     return N * (K // 4)
 
 
@@ -109,6 +111,13 @@ WORKLOADS = {w.name: w for w in [
     Workload("q4_0_gemv_4096x4096_t1", "q4_0", "q4_0_gemv", [(4096, 4096)], 1, 64, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_0 GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
              "q4_0_gemv_t1_4096x4096.md", distinct=64, arithmetic=T1_ARITH),
+    Workload("llama7b_ffn_swiglu_t1", "q4k_ffn", "q4k_ffn_swiglu", [(4096, 11008)], 1, 32, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q4_K fused gate+up SwiGLU weight-stream GB/s, Llama-2-7B FFN (32 layers x "
+             "4096 -> 2 x 11008), batch 1", ["q4k_gemv.cu"], "q4k_ffn_swiglu_llama7b_t1.md", distinct=1,
+             arithmetic=T1_ARITH + "; h = silu(g)*u in fp32"),
+    Workload("llama7b_gate_up_t1", "q4k", "q4k_matmul", [(4096, 11008)] * 2, 1, 32, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q4_K gate and up projections as two GEMVs, weight-stream GB/s, Llama-2-7B "
+             "FFN (32 layers x 2 x 4096 -> 11008), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "ternary_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "batch 1", ["ternary_gemv.cu"], "ternary_t1_2560x6912.md", arithmetic="fp32"),
@@ -335,6 +344,10 @@ def host_inputs(w: Workload, seed: int = 0):
             Ws = [synth.q4k_weights(g, N, K) for _ in range(n)]
         elif w.kind == "q4_0":
             Ws = [synth.q4_0_weights(g, N, K) for _ in range(n)]
+        elif w.kind == "q4k_ffn":
+            import numpy as np
+            Ws = [np.concatenate([synth.q4k_weights(g, N, K).reshape(-1), synth.q4k_weights(g, N, K).reshape(-1)])
+                  for _ in range(n)]
         else:
             Ws = [synth.ternary_weights(g, N, K) for _ in range(n)]
         scale = float(synth.ternary_scale(g)) if w.kind == "ternary" else 1.0
@@ -350,7 +363,7 @@ def workload_config(w: Workload, plan: Plan) -> dict:
             "weight_bytes_per_step": plan.weight_bytes,
             "l2": f"inputs larger than L2: {plan.weight_bytes / 1e6:.0f} MB of weights per step "
                   f"(L2 129 MB), no flush",
-            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks').get(w.kind, 'ternary codes')}, seed 0 "
+            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks', q4k_ffn='Q4_K blocks (gate, up)').get(w.kind, 'ternary codes')}, seed 0 "
                        f"(synth), {w.distinct} distinct host copies per matrix",
             "activations": "fp32 N(0,1), seed 0"}
 
@@ -361,6 +374,9 @@ def oracle_call(w: Workload, K, N, W, x, scale, rows, r0=0):
         oracle.q4k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
     elif w.kind == "q4_0":
         oracle.q4_0_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
+    elif w.kind == "q4k_ffn":
+        Wg, Wu = W.reshape(2, N, -1)
+        oracle.q4k_ffn_swiglu(x, Wg[r0:r0 + rows], Wu[r0:r0 + rows], K, rows)
     else:
         oracle.ternary_gemv(x, W.reshape(N, -1)[r0:r0 + rows], scale, K, rows)
 
@@ -476,7 +492,9 @@ def run_ours(a) -> None:
     wp, xp, yp = W.data_ptr(), x.data_ptr(), y.data_ptr()
     calls = []
     for K, N, wo, xo, yo, m in plan.launches:
-        if w.kind != "ternary":
+        if w.kind == "q4k_ffn":
+            calls.append((xp + 4 * xo, wp + wo, wp + wo + _q4k_bytes(K, N), yp + 4 * yo, K, N, w.tokens, sp))
+        elif w.kind != "ternary":
             calls.append((xp + 4 * xo, wp + wo, yp + 4 * yo, K, N, w.tokens, sp))
         else:
             calls.append((xp + 4 * xo, wp + wo, mats[m][2], yp + 4 * yo, K, N, w.tokens, sp))

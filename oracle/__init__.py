@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i64, i64, i64, vp, i32]
             fn.restype = i32
+        lib.oracle_q4k_ffn_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, i32]
+        lib.oracle_q4k_ffn_swiglu.restype = i32
         lib.oracle_q4_0_dequant_block.argtypes = [vp, vp]
         lib.oracle_q4_0_dequant_block.restype = None
         lib.oracle_q4_0_dequant.argtypes = [vp, i64, i64, vp]
@@ -156,6 +158,22 @@ def q4k_matmul_bf16(x, W, K, N, threads=0, lib=None) -> np.ndarray:
 def q4k_matmul_lazy(x, W, K, N, threads=0, lib=None) -> np.ndarray:
     """The lazy-dmin form (scale·Σxq − offset·Σx per sub-block), double."""
     return _matmul("oracle_q4k_matmul_lazy", x, W, K, N, threads, lib)
+
+
+def q4k_ffn_swiglu(x, Wg, Wu, K, N, threads=0, lib=None):
+    """(g, u, h) float64 [T, N]: g = x·dequant(Wg)ᵀ, u = x·dequant(Wu)ᵀ, h = silu(g)·u."""
+    Wg = _check_q4k(Wg, K, N)
+    Wu = _check_q4k(Wu, K, N)
+    x = _check_x(x, K)
+    T = x.shape[0]
+    g = np.empty((T, N), np.float64)
+    u = np.empty((T, N), np.float64)
+    h = np.empty((T, N), np.float64)
+    rc = (lib or load()).oracle_q4k_ffn_swiglu(_ptr(x), _ptr(Wg), _ptr(Wu), K, N, T, _ptr(g), _ptr(u),
+                                                _ptr(h), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_q4k_ffn_swiglu failed with {rc}")
+    return g, u, h
 
 
 Q40_VALUES, Q40_BYTES = 32, 18

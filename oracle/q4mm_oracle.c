@@ -205,6 +205,40 @@ int oracle_q4k_matmul_bf16(const float *x, const uint8_t *W, int64_t K, int64_t 
     return q4k_matmul_impl(x, W, K, N, T, y, nthreads, 1);
 }
 
+/* Llama feed-forward input side with SwiGLU: g = x·W_gateᵀ and u = x·W_upᵀ
+ * (both Q4_K, each exactly as oracle_q4k_matmul computes it), then
+ * h = silu(g)·u with silu(z) = z / (1 + e^(−z)), in double.  The pages name
+ * this fused operation only as the llama.cpp benchmark "ffn_swiglu" (PR #37
+ * "ggml-cpu: cache-aware tiling in ggml_compute_forward_mul_mat", section
+ * "Measured impact"); the formula is the standard Llama FFN.  g and u are
+ * returned too when their pointers are non-NULL. */
+int oracle_q4k_ffn_swiglu(const float *x, const uint8_t *Wg, const uint8_t *Wu, int64_t K, int64_t N,
+                          int64_t T, double *g, double *u, double *h, int nthreads)
+{
+    if (K <= 0 || N <= 0 || T <= 0 || K % Q4K_VALUES)
+        return -1;
+    double *gg = (double *)malloc((size_t)(T * N) * sizeof(double));
+    double *uu = (double *)malloc((size_t)(T * N) * sizeof(double));
+    int rc = (gg && uu) ? 0 : -2;
+    if (!rc)
+        rc = q4k_matmul_impl(x, Wg, K, N, T, gg, nthreads, 0);
+    if (!rc)
+        rc = q4k_matmul_impl(x, Wu, K, N, T, uu, nthreads, 0);
+    if (!rc) {
+        for (int64_t i = 0; i < T * N; ++i) {
+            double z = gg[i];
+            h[i] = z / (1.0 + exp(-z)) * uu[i];
+            if (g)
+                g[i] = z;
+            if (u)
+                u[i] = uu[i];
+        }
+    }
+    free(gg);
+    free(uu);
+    return rc;
+}
+
 /* The pages' lazy-dmin form, in double: per sub-block s of each block,
  *   acc += (d·sc_s)·Σ_e x_e·q_e − (dmin·m_s)·Σ_e x_e
  * with the "scale" d·sc_s and "offset" dmin·m_s applied once per

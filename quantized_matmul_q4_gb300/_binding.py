@@ -8,7 +8,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 Q4K_VALUES = 256
 Q4K_BYTES = 144
 
-_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "ternary_gemv",
+_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q4k_ffn_swiglu",
+            "ternary_gemv",
             "q4mm_last_error", "q4mm_device_status", "q4mm_version")
 
 
@@ -36,6 +37,8 @@ def _load() -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         fn.restype = i32
+    lib.q4k_ffn_swiglu.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+    lib.q4k_ffn_swiglu.restype = i32
     lib.ternary_gemv.argtypes = [vp, vp, f32, vp, i32, i32, i32, vp]
     lib.ternary_gemv.restype = i32
     lib.q4mm_last_error.argtypes = []
@@ -90,6 +93,11 @@ def q4k_matmul_tc_noalloc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, st
 
 def q4_0_gemv_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
     _check(_LIB.q4_0_gemv(x, w, y, K, N, T, stream))
+
+
+def q4k_ffn_swiglu_ptr(x: int, w_gate: int, w_up: int, h: int, K: int, N: int, T: int,
+                       stream: int = 0) -> None:
+    _check(_LIB.q4k_ffn_swiglu(x, w_gate, w_up, h, K, N, T, stream))
 
 
 def ternary_gemv_ptr(x: int, w: int, scale: float, y: int, K: int, N: int, T: int,
@@ -154,6 +162,17 @@ def q4_0_gemv(x, w, N: int | None = None, out=None, stream=None):
     """y[T, N] = x[T, K] · dequant_q4_0(W)ᵀ in FP32 (one weight pass per token)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q40_VALUES) * Q40_BYTES, out, N)
     q4_0_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+def q4k_ffn_swiglu(x, w_gate, w_up, N: int | None = None, out=None, stream=None):
+    """h[T, N] = silu(x · dequant(W_gate)ᵀ) · (x · dequant(W_up)ᵀ), both Q4_K."""
+    x2, T, K, N, out = _prep(x, w_gate, None, lambda k: (k // Q4K_VALUES) * Q4K_BYTES, out, N)
+    if (w_up.dtype != w_gate.dtype or w_up.numel() != w_gate.numel() or not w_up.is_cuda
+            or not w_up.is_contiguous()):
+        raise ValueError("w_up must be a contiguous CUDA uint8 tensor of the gate weight's size")
+    q4k_ffn_swiglu_ptr(x2.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(),
+                       K, N, T, _stream_ptr(stream))
     return out.view(T, N)
 
 

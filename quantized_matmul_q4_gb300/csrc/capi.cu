@@ -207,6 +207,25 @@ int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int ou
     return Q4MM_OK;
 }
 
+int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *h, int inputDim,
+                   int hiddenDim, int tokens, q4mm_stream_t stream) {
+    const size_t row_bytes = (size_t)(inputDim / 256) * 144;
+    int rc = check_common(x, w_gate, h, inputDim, hiddenDim, tokens, 256, row_bytes, 16);
+    if (rc) return rc;
+    if ((rc = check_common(x, w_up, h, inputDim, hiddenDim, tokens, 256, row_bytes, 16))) return rc;
+    if (inputDim > Q4MM_FFN_MAX_INPUT_DIM)
+        return fail(Q4MM_ERR_DIM, "inputDim %d exceeds the fused FFN limit %d", inputDim, Q4MM_FFN_MAX_INPUT_DIM);
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    const uint8_t *Wg = static_cast<const uint8_t *>(w_gate), *Wu = static_cast<const uint8_t *>(w_up);
+    for (int t = 0; t < tokens; ++t) {
+        const cudaError_t e = q4mm::launch_q4k_ffn_swiglu_t1(ctx, x + (size_t)t * inputDim, Wg, Wu,
+                                                             h + (size_t)t * hiddenDim, inputDim, hiddenDim);
+        if (e != cudaSuccess) return fail_cuda(e, "q4k_ffn_swiglu launch");
+    }
+    return Q4MM_OK;
+}
+
 int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,
                  int outputDim, int tokens, q4mm_stream_t stream) {
     int rc = check_common(x, w_packed, y, inputDim, outputDim, tokens, 4, (size_t)inputDim / 4, 1);

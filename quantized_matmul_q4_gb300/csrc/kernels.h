@@ -26,6 +26,11 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                 int K, int N);
 
+// Llama FFN input side, one token: h = silu(x·Wgᵀ)·(x·Wuᵀ), both Q4_K, in one
+// launch of the one-token kernel (x split once for both weights).
+cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,
+                                     float *h, int K, int N);
+
 // Q4_K decode GEMV for 1..8 tokens with x staged in shared memory.
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                   int K, int N, int T);

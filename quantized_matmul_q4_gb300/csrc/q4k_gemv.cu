@@ -278,6 +278,7 @@ constexpr int kPlaneSlabBytes = 208;
 struct T1Params {
     const float *x;
     const uint8_t *W;
+    const uint8_t *W2;  // SwiGLU: the up projection (W is the gate projection)
     float *y;
     int *status;
     int N;
@@ -293,7 +294,10 @@ struct T1Params {
 constexpr int kT1RoleWarps = 1;  // the copy warp
 constexpr int kT1MaxCw = 16;     // compute warps at most
 
-template <class Fmt, int kNB>
+// kSwiGLU: the CTA's rows of W (gate) and then the same rows of W2 (up) form
+// one list of 2·nrows virtual rows through the same ring and passes; every
+// row result goes to shared memory and y[o] = silu(g[o])·u[o] at the end.
+template <class Fmt, int kNB, bool kSwiGLU>
 __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
@@ -327,11 +331,13 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? K : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
-    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [rows_per_cta][wc]
+    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [virtual rows][wc]
 
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
-    const int nstages = (nrows + p.stage_rows - 1) / p.stage_rows;
+    const int nv = kSwiGLU ? 2 * nrows : nrows;  // rows streamed through the ring
+    const bool to_smem = wide || kSwiGLU;        // row results go to part[]
+    const int nstages = (nv + p.stage_rows - 1) / p.stage_rows;
     const int passes_per_stage = p.stage_rows / pass_rows;
 
     // Bulk copies need a 16-byte aligned destination; never issue one otherwise.
@@ -355,12 +361,20 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint8_t *src = p.W + (size_t)row0 * row_bytes;
             auto issue = [&](int st, int slot) {
-                const int rows = min(p.stage_rows, nrows - st * p.stage_rows);
-                mbar_arrive_expect_tx(&full_bar[slot], rows * row_bytes);
-                bulk_g2s(ring + (size_t)slot * slot_bytes, src + (size_t)st * p.stage_rows * row_bytes,
-                         rows * row_bytes, &full_bar[slot]);
+                const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
+                uint8_t *dst = ring + (size_t)slot * slot_bytes;
+                mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
+                // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
+                const int g1 = kSwiGLU ? min(v1, nrows) : v1;
+                if (g1 > v0)
+                    bulk_g2s(dst, p.W + (size_t)(row0 + v0) * row_bytes, (uint32_t)(g1 - v0) * row_bytes,
+                             &full_bar[slot]);
+                if (kSwiGLU && v1 > nrows) {
+                    const int u0 = max(v0, nrows);
+                    bulk_g2s(dst + (size_t)(u0 - v0) * row_bytes, p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes,
+                             (uint32_t)(v1 - u0) * row_bytes, &full_bar[slot]);
+                }
                 issued = st + 1;
             };
             const int first = min(nstages, p.nslots);
@@ -493,7 +507,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
         const typename Fmt::Lane lfmt = Fmt::lane(j);
         const float unit = s_blk * (1.0f / 32768.0f);
 
-        const int npasses = (nrows + pass_rows - 1) / pass_rows;
+        const int npasses = (nv + pass_rows - 1) / pass_rows;
         // Stage, slot and phase of the current pass, advanced without
         // divisions as the pass index steps by rg.
         int pin = rgi, st = 0;
@@ -516,7 +530,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                 }
                 waited_stage = st;
                 stage_base = ring + (size_t)slot * slot_bytes + b * kQ4kBytes;
-                rows = min(p.stage_rows, nrows - st * p.stage_rows);
+                rows = min(p.stage_rows, nv - st * p.stage_rows);
             }
             const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
             float pa = Fmt::row(stage_base + min(ra, rows - 1) * row_bytes, lfmt, unit, pl, sum_lo, sum_hi);
@@ -532,6 +546,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             const int rl = st * p.stage_rows + r;
             if (wide) {
                 if ((lane & (half - 1)) == 0 && r < rows) part[rl * wc + wcol] = v;
+            } else if (kSwiGLU) {
+                if (s == (up ? half : 0) && r < rows) part[rl] = v;
             } else {
                 if (s == (up ? half : 0) && r < rows) p.y[row0 + rl] = v;
             }
@@ -548,11 +564,16 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             }
         }
 
-        if (wide) {
+        if (to_smem) {
             named_bar_sync(1, ncw * 32);
             for (int i = threadIdx.x - 32 * kT1RoleWarps; i < nrows; i += ncw * 32) {
                 float acc = 0.f;
                 for (int w = 0; w < wc; ++w) acc += part[i * wc + w];
+                if (kSwiGLU) {
+                    float up = 0.f;
+                    for (int w = 0; w < wc; ++w) up += part[(nrows + i) * wc + w];
+                    acc = acc / (1.0f + expf(-acc)) * up;  // silu(g)·u
+                }
                 p.y[row0 + i] = acc;
             }
         }
@@ -785,11 +806,13 @@ int next_pow2(int v) {
 
 }  // namespace
 
-template <class Fmt>
-cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
+template <class Fmt, bool kSwiGLU = false>
+cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                           const uint8_t *W2 = nullptr) {
     T1Params p;
     p.x = x;
     p.W = W;
+    p.W2 = W2;
     p.y = y;
     p.status = c.status;
     p.N = N;
@@ -822,11 +845,12 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     const size_t xs_bytes = (size_t)(K / 64) * kPlaneSlabBytes + (size_t)(K / 32) * sizeof(float) +
                             (size_t)((p.nb * 4 + 15) & ~15) +
                             (p.x_staged ? (size_t)K * sizeof(float) : 0);
-    const size_t part_bytes = wide ? (size_t)p.rows_per_cta * wc * sizeof(float) : 0;
+    const int vrows_per_cta = (kSwiGLU ? 2 : 1) * p.rows_per_cta;
+    const size_t part_bytes = (wide || kSwiGLU) ? (size_t)vrows_per_cta * wc * sizeof(float) : 0;
     const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
     const size_t budget = tun.ring_bytes;
     int nslots = (int)((budget > fixed ? budget - fixed : 0) / slot_bytes);
-    const int stages_needed = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
+    const int stages_needed = (vrows_per_cta + p.stage_rows - 1) / p.stage_rows;
     nslots = max(2, min(nslots, min(stages_needed, 8)));
     p.nslots = nslots;
     // With plain activation loads nothing needs to go out ahead of the rest.
@@ -840,20 +864,25 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
         if (e != cudaSuccess) return e;
         return launch_kernel(c, kernel, dim3(grid), block, smem, p);
     };
-    if constexpr (std::is_same<Fmt, FmtQ4K>::value) {
+    if constexpr (kSwiGLU) {
         switch (p.nb) {
-            case 4: return go(gemv_t1_kernel<Fmt, 4>);
-            case 8: return go(gemv_t1_kernel<Fmt, 8>);
-            case 16: return go(gemv_t1_kernel<Fmt, 16>);
-            case 32: return go(gemv_t1_kernel<Fmt, 32>);
-            case 43: return go(gemv_t1_kernel<Fmt, 43>);
-            default: return go(gemv_t1_kernel<Fmt, 0>);
+            case 16: return go(gemv_t1_kernel<Fmt, 16, true>);
+            default: return go(gemv_t1_kernel<Fmt, 0, true>);
+        }
+    } else if constexpr (std::is_same<Fmt, FmtQ4K>::value) {
+        switch (p.nb) {
+            case 4: return go(gemv_t1_kernel<Fmt, 4, false>);
+            case 8: return go(gemv_t1_kernel<Fmt, 8, false>);
+            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
+            case 32: return go(gemv_t1_kernel<Fmt, 32, false>);
+            case 43: return go(gemv_t1_kernel<Fmt, 43, false>);
+            default: return go(gemv_t1_kernel<Fmt, 0, false>);
         }
     } else {
         switch (p.nb) {
-            case 16: return go(gemv_t1_kernel<Fmt, 16>);
-            case 43: return go(gemv_t1_kernel<Fmt, 43>);
-            default: return go(gemv_t1_kernel<Fmt, 0>);
+            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
+            case 43: return go(gemv_t1_kernel<Fmt, 43, false>);
+            default: return go(gemv_t1_kernel<Fmt, 0, false>);
         }
     }
 }
@@ -864,6 +893,11 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
     return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N);
+}
+
+cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,
+                                     float *h, int K, int N) {
+    return launch_gemv_t1<FmtQ4K, true>(c, x, Wg, h, K, N, Wu);
 }
 
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,

@@ -313,10 +313,46 @@ def pin_q4_0_fraction_bruteforce(lib):
                 assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
 
 
+def pin_swiglu(lib):
+    # silu(z) = z / (1 + e^-z): closed values, then h = silu(g)·u where g and
+    # u come from one-hot activations (x = e_k gives the weights' column k),
+    # so every g and u is a known dequantized weight.
+    K, N = 256, 6
+    g_ = np.random.default_rng(37)
+    Wg = synth.q4k_weights(g_, N, K)
+    Wu = synth.q4k_weights(g_, N, K)
+    wg = oracle.q4k_dequant(Wg, K, N, lib=lib).astype(np.float64)
+    wu = oracle.q4k_dequant(Wu, K, N, lib=lib).astype(np.float64)
+    ks = [0, 77, 255]
+    x = np.zeros((len(ks), K), np.float32)
+    for t, k in enumerate(ks):
+        x[t, k] = 1.0
+    g, u, h = oracle.q4k_ffn_swiglu(x, Wg, Wu, K, N, lib=lib)
+    for t, k in enumerate(ks):
+        assert np.array_equal(g[t], wg[:, k]) and np.array_equal(u[t], wu[:, k])
+        sig = 1.0 / (1.0 + np.exp(-wg[:, k]))
+        assert np.allclose(h[t], wg[:, k] * sig * wu[:, k], rtol=1e-15, atol=0)
+    # Closed values of silu through a one-row weight: w = d·q with d = 1,
+    # dmin = 0, sc = 1 gives g = q exactly; u = 1 via the same construction.
+    q = [0] * 256
+    q[0], q[1], q[2] = 0, 1, 15
+    Wg1 = oracle.q4k_pack_block(0x3C00, 0, [1] * 8, [0] * 8, q, lib=lib)
+    qu = [1] * 256
+    Wu1 = oracle.q4k_pack_block(0x3C00, 0, [1] * 8, [0] * 8, qu, lib=lib)
+    x = np.zeros((3, K), np.float32)
+    for t in range(3):
+        x[t, t] = 1.0
+    _, _, h = oracle.q4k_ffn_swiglu(x, Wg1, Wu1, K, 1, lib=lib)
+    assert h[0, 0] == 0.0
+    assert abs(h[1, 0] - 0.7310585786300049) < 1e-15      # 1 / (1 + e^-1)
+    assert abs(h[2, 0] - 14.999995411466594) < 1e-13      # 15 / (1 + e^-15)
+
+
 ALL_PINS = [
     pin_fp16_decode, pin_bf16_round, pin_handworked_pack, pin_handworked_values,
     pin_nibble_positions, pin_scale_positions, pin_special_cases, pin_one_hot_rows,
     pin_lazy_equals_direct, pin_fraction_bruteforce, pin_ternary_handworked,
     pin_ternary_integer_count, pin_ternary_scale, pin_bf16_variant,
     pin_q4_0_handworked, pin_q4_0_nibble_positions, pin_q4_0_as_q4k, pin_q4_0_fraction_bruteforce,
+    pin_swiglu,
 ]

@@ -123,3 +123,19 @@ def test_q4_0_rejects_bad_input_dim(q4mm, K):
     with pytest.raises(q4mm.Q4mmError) as e:
         q4mm.q4_0_gemv_ptr(X, W, Y, K, 16, 1, 0)
     assert e.value.code == DIM and "inputDim" in q4mm.last_error()
+
+
+def test_ffn_swiglu_validation(q4mm):
+    W2 = 0x28000000
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_ffn_swiglu_ptr(X, W, W2, Y, 300, 16, 1, 0)
+    assert e.value.code == DIM
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_ffn_swiglu_ptr(X, W, W2, Y, 32768 + 256, 16, 1, 0)
+    assert e.value.code == DIM and "inputDim" in q4mm.last_error()
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_ffn_swiglu_ptr(X, W, 0, Y, 256, 16, 1, 0)
+    assert e.value.code == NULL
+    with pytest.raises(q4mm.Q4mmError) as e:   # h inside the up weight
+        q4mm.q4k_ffn_swiglu_ptr(X, W, Y, Y + 64, 256, 16, 1, 0)
+    assert e.value.code == ALIAS

@@ -36,6 +36,9 @@ MUTANTS = {
     "ternary_offset": ("return ((row[i / 4] >> (2 * (i % 4))) & 3) - 1;",
                        "return ((row[i / 4] >> (2 * (i % 4))) & 3);"),
     "bf16_truncates": ("u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;", "u = u & 0xFFFF0000u;"),
+    "swiglu_sigmoid_sign": ("h[i] = z / (1.0 + exp(-z)) * uu[i];", "h[i] = z / (1.0 + exp(z)) * uu[i];"),
+    "swiglu_gate_up_swapped": ("rc = q4k_matmul_impl(x, Wg, K, N, T, gg, nthreads, 0);",
+                               "rc = q4k_matmul_impl(x, Wu, K, N, T, gg, nthreads, 0);"),
     "q4_0_nibble_halves": ("return e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);",
                            "return e < 16 ? (qs[e] >> 4) : (qs[e - 16] & 15);"),
     "q4_0_offset": ("w[e] = (float)(d * (q40_code(blk + 2, e) - 8));",
