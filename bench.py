@@ -119,8 +119,11 @@ WORKLOADS = {w.name: w for w in [
              "gemv_t1_kernel", "Q4_K gate and up projections as two GEMVs, weight-stream GB/s, Llama-2-7B "
              "FFN (32 layers x 2 x 4096 -> 11008), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
-             "hbm", "ternary_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
-             "batch 1", ["ternary_gemv.cu"], "ternary_t1_2560x6912.md", arithmetic="fp32"),
+             "hbm", "gemv_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "batch 1", ["ternary_gemv.cu", "q4k_gemv.cu"], "ternary_t1_2560x6912.md",
+             arithmetic="fp32 activations rounded once to 2^-22 of each 256-value block's maximum and split "
+                        "into three byte planes; 2-bit fields x planes in int32 dp4a; fp32 combination, scale "
+                        "applied once"),
     Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",
              "hbm", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),

@@ -26,6 +26,12 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                 int K, int N);
 
+// BitNet b1.58 ternary GEMV, one token, on the same one-token kernel with the
+// byte-plane integer code-dot (K % 256 == 0, W 16-byte aligned; otherwise
+// cudaErrorNotSupported).
+cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,
+                                   int K, int N);
+
 // Llama FFN input side, one token: h = silu(x·Wgᵀ)·(x·Wuᵀ), both Q4_K, in one
 // launch of the one-token kernel (x split once for both weights).
 cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,

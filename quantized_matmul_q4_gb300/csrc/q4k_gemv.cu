@@ -207,6 +207,8 @@ __device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneS
 
 // Q4_K: the group is one super-block; the lane reads the header and qs slab j.
 struct FmtQ4K {
+    static constexpr int kGroupBytes = 144;  // bytes per 256 values of a row
+    __device__ static void prep_planes(int (&)[3][16]) {}
     struct Lane {
         LaneScaleSel sel;
         int j;
@@ -224,6 +226,8 @@ struct FmtQ4K {
 // block B = values 32..63 (qs 4-byte aligned at byte 20).  Per block,
 // Σ w·x = d·(Σ q·x − 8·Σ x).
 struct FmtQ40 {
+    static constexpr int kGroupBytes = 144;
+    __device__ static void prep_planes(int (&)[3][16]) {}
     struct Lane {
         int j;
     };
@@ -265,6 +269,55 @@ struct FmtQ40 {
     }
 };
 
+// BitNet b1.58 ternary (SKaiNET issue #1138 "[ternary-f32] Phase 2:
+// TernaryF32GemvNative SPI + reference ViewKernel + TernaryF32KernelPack",
+// section "Tasks"): 256 values in 64 bytes, four 2-bit fields per byte,
+// code = field − 1.  The lane's 64 values are bytes 16j..16j+15 of the group
+// (one 16-byte load); byte k of word w holds values 16w + 4k + i in field i.
+// prep_planes transposes each 16-value run of the plane words so that plane
+// word 4w + i holds values 16w + i, 16w + 4 + i, 16w + 8 + i, 16w + 12 + i,
+// the order in which field i of word w meets them.  Σ x·code = Σ x·field − Σ x,
+// the scale is applied after the dot (T1Params::out_scale).
+struct FmtTern {
+    static constexpr int kGroupBytes = 64;
+    __device__ static void prep_planes(int (&pl)[3][16]) {
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t i0 = (uint32_t)pl[pp][4 * w], i1 = (uint32_t)pl[pp][4 * w + 1];
+                const uint32_t i2 = (uint32_t)pl[pp][4 * w + 2], i3 = (uint32_t)pl[pp][4 * w + 3];
+                const uint32_t t0 = __byte_perm(i0, i1, 0x5140), t1 = __byte_perm(i0, i1, 0x7362);
+                const uint32_t t2 = __byte_perm(i2, i3, 0x5140), t3 = __byte_perm(i2, i3, 0x7362);
+                pl[pp][4 * w] = (int)__byte_perm(t0, t2, 0x5410);
+                pl[pp][4 * w + 1] = (int)__byte_perm(t0, t2, 0x7632);
+                pl[pp][4 * w + 2] = (int)__byte_perm(t1, t3, 0x5410);
+                pl[pp][4 * w + 3] = (int)__byte_perm(t1, t3, 0x7632);
+            }
+    }
+    struct Lane {
+        int j;
+    };
+    __device__ static Lane lane(int j) { return Lane{j}; }
+    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
+                                float sum_lo, float sum_hi) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(grp + 16 * L.j);
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        int d[3] = {0, 0, 0};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t f = (qw[w] >> (2 * i)) & 0x03030303u;
+                d[0] = dp4a_uu(f, (uint32_t)pl[0][4 * w + i], d[0]);
+                d[1] = dp4a_uu(f, (uint32_t)pl[1][4 * w + i], d[1]);
+                d[2] = dp4a_us(f, pl[2][4 * w + i], d[2]);
+            }
+        }
+        return fmaf(unit, plane_combine(d), -(sum_lo + sum_hi));
+    }
+};
+
 // Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter:
 // the float's bits are 0x4B400000 + rint(v).
 constexpr float kShifter = 12582912.0f;
@@ -289,6 +342,7 @@ struct T1Params {
     int nslots;        // ring depth
     int pre_stages;    // stages issued before the wait on the previous kernel
     int x_staged;      // 1: x arrives by one bulk copy into shared memory
+    float out_scale;   // y = out_scale · (row result); 1 except for the ternary scale
 };
 
 constexpr int kT1RoleWarps = 1;  // the copy warp
@@ -308,7 +362,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     const int nb = kNB > 0 ? kNB : p.nb;
     const int K = nb * kQ4kValues;
     const int nslabs = 4 * nb;                     // 64-value slabs per row
-    const uint32_t row_bytes = (uint32_t)nb * kQ4kBytes;
+    const uint32_t row_bytes = (uint32_t)nb * Fmt::kGroupBytes;
     const int L = 4 * nb;                          // slab lanes per row
     const bool wide = L > 32;                      // a row spans several warps
     const int wc = wide ? (L + 31) / 32 : 1;       // warps per row
@@ -504,6 +558,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
+        Fmt::prep_planes(pl);
         const typename Fmt::Lane lfmt = Fmt::lane(j);
         const float unit = s_blk * (1.0f / 32768.0f);
 
@@ -529,7 +584,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                     break;
                 }
                 waited_stage = st;
-                stage_base = ring + (size_t)slot * slot_bytes + b * kQ4kBytes;
+                stage_base = ring + (size_t)slot * slot_bytes + b * Fmt::kGroupBytes;
                 rows = min(p.stage_rows, nv - st * p.stage_rows);
             }
             const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
@@ -549,7 +604,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             } else if (kSwiGLU) {
                 if (s == (up ? half : 0) && r < rows) part[rl] = v;
             } else {
-                if (s == (up ? half : 0) && r < rows) p.y[row0 + rl] = v;
+                if (s == (up ? half : 0) && r < rows) p.y[row0 + rl] = p.out_scale * v;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -574,7 +629,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                     for (int w = 0; w < wc; ++w) up += part[(nrows + i) * wc + w];
                     acc = acc / (1.0f + expf(-acc)) * up;  // silu(g)·u
                 }
-                p.y[row0 + i] = acc;
+                p.y[row0 + i] = p.out_scale * acc;
             }
         }
     }
@@ -808,16 +863,17 @@ int next_pow2(int v) {
 
 template <class Fmt, bool kSwiGLU = false>
 cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
-                           const uint8_t *W2 = nullptr) {
+                           const uint8_t *W2 = nullptr, float out_scale = 1.0f) {
     T1Params p;
     p.x = x;
     p.W = W;
     p.W2 = W2;
+    p.out_scale = out_scale;
     p.y = y;
     p.status = c.status;
     p.N = N;
     p.nb = K / kQ4kValues;
-    const int row_bytes = p.nb * kQ4kBytes;
+    const int row_bytes = p.nb * Fmt::kGroupBytes;
     const int L = 4 * p.nb;  // slab lanes per row
     const bool wide = L > 32;
     const int wc = wide ? (L + 31) / 32 : 1;
@@ -869,6 +925,11 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
             case 16: return go(gemv_t1_kernel<Fmt, 16, true>);
             default: return go(gemv_t1_kernel<Fmt, 0, true>);
         }
+    } else if constexpr (std::is_same<Fmt, FmtTern>::value) {
+        switch (p.nb) {
+            case 10: return go(gemv_t1_kernel<Fmt, 10, false>);
+            default: return go(gemv_t1_kernel<Fmt, 0, false>);
+        }
     } else if constexpr (std::is_same<Fmt, FmtQ4K>::value) {
         switch (p.nb) {
             case 4: return go(gemv_t1_kernel<Fmt, 4, false>);
@@ -893,6 +954,11 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
     return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N);
+}
+
+cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,
+                                   int K, int N) {
+    return launch_gemv_t1<FmtTern>(c, x, W, y, K, N, nullptr, scale);
 }
 
 cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,

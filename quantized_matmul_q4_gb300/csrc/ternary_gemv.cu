@@ -15,6 +15,7 @@
 // exact for integer activations (every partial sum is a multiple of 1/8 far
 // below 2^21), so the code-dot is bit-exact there and the scale multiply is a
 // single fp32 rounding.
+#include <cstdlib>
 #include <utility>
 
 #include "common.cuh"
@@ -574,6 +575,16 @@ cudaError_t launch_t(const LaunchCtx &c, const float *x, const uint8_t *W, float
 
 }  // namespace
 
+// Q4MM_TERNARY_T1=float selects the float one-token kernel for every K
+// (for comparisons); read once.
+bool ternary_float_t1() {
+    static const bool on = [] {
+        const char *v = getenv("Q4MM_TERNARY_T1");
+        return v && v[0] == 'f';
+    }();
+    return on;
+}
+
 cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_t *W, float scale,
                                 float *y, int K, int N, int T) {
     // The streamed kernels copy whole 16-byte runs of code bytes: rows of
@@ -581,7 +592,10 @@ cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_
     const bool bulk = (K % 64 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
     if (bulk) {
         cudaError_t e = cudaErrorNotSupported;
-        if (T == 1) e = launch_ternary_t1(c, x, W, scale, y, K, N);
+        // One token with K % 256 == 0: the shared one-token kernel (byte-plane
+        // integer code-dot); otherwise the float one-token kernel below.
+        if (T == 1 && K % 256 == 0 && !ternary_float_t1()) e = launch_ternary_gemv_t1(c, x, W, scale, y, K, N);
+        if (T == 1 && e == cudaErrorNotSupported) e = launch_ternary_t1(c, x, W, scale, y, K, N);
         if (e == cudaErrorNotSupported) e = launch_ternary_tile(c, x, W, scale, y, K, N, T);
         if (e != cudaErrorNotSupported) return e;
     }
