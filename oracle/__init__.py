@@ -74,6 +74,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
             fn.restype = i32
         lib.oracle_q4k_ffn_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, i32]
         lib.oracle_q4k_ffn_swiglu.restype = i32
+        lib.oracle_q6k_dequant_block.argtypes = [vp, vp]
+        lib.oracle_q6k_dequant_block.restype = None
+        lib.oracle_q6k_dequant.argtypes = [vp, i64, i64, vp]
+        lib.oracle_q6k_dequant.restype = i32
+        lib.oracle_q6k_matmul.argtypes = [vp, vp, i64, i64, i64, vp, i32]
+        lib.oracle_q6k_matmul.restype = i32
+        lib.oracle_q6k_pack_block.argtypes = [ctypes.c_uint16, vp, vp, vp]
+        lib.oracle_q6k_pack_block.restype = None
         lib.oracle_q4_0_dequant_block.argtypes = [vp, vp]
         lib.oracle_q4_0_dequant_block.restype = None
         lib.oracle_q4_0_dequant.argtypes = [vp, i64, i64, vp]
@@ -257,3 +265,46 @@ def ternary_pack(codes, lib=None) -> np.ndarray:
 
 def max_threads(lib=None) -> int:
     return (lib or load()).oracle_max_threads()
+
+
+Q6K_VALUES, Q6K_BYTES = 256, 210
+
+
+def _check_q6k(W: np.ndarray, K: int, N: int) -> np.ndarray:
+    if K <= 0 or K % Q6K_VALUES:
+        raise ValueError(f"inputDim {K} is not a positive multiple of {Q6K_VALUES}")
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    if W.size != N * (K // Q6K_VALUES) * Q6K_BYTES:
+        raise ValueError("weight bytes do not match N·K/256·210")
+    return W
+
+
+def q6k_dequant(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
+    """Dequantized fp32 Q6_K weight [N, K]."""
+    W = _check_q6k(W, K, N)
+    out = np.empty((N, K), np.float32)
+    if (lib or load()).oracle_q6k_dequant(_ptr(W), K, N, _ptr(out)) != 0:
+        raise ValueError("oracle_q6k_dequant rejected its arguments")
+    return out
+
+
+def q6k_matmul(x, W, K, N, threads=0, lib=None) -> np.ndarray:
+    """y = x · dequant_q6k(W)ᵀ, double accumulation; returns float64 [T, N]."""
+    W = _check_q6k(W, K, N)
+    x = _check_x(x, K)
+    T = x.shape[0]
+    y = np.empty((T, N), np.float64)
+    rc = (lib or load()).oracle_q6k_matmul(_ptr(x), _ptr(W), K, N, T, _ptr(y), threads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_q6k_matmul failed with {rc}")
+    return y
+
+
+def q6k_pack_block(d_bits: int, sc, q, lib=None) -> np.ndarray:
+    """Encode one 210-byte Q6_K block from d (fp16 bits), 16 scales and 256 codes (0..63)."""
+    sc = np.ascontiguousarray(sc, dtype=np.int32)
+    q = np.ascontiguousarray(q, dtype=np.int32)
+    assert sc.size == 16 and q.size == Q6K_VALUES
+    out = np.zeros(Q6K_BYTES, np.uint8)
+    (lib or load()).oracle_q6k_pack_block(d_bits, _ptr(sc), _ptr(q), _ptr(out))
+    return out

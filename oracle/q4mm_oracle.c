@@ -28,6 +28,7 @@
  *    the BitNet scale; prefill loops rows advancing by r·k and r·n).
  *  - Q4_0, the 32-value / 18-byte block named as the follow-up in the same
  *    PR (section "Out of scope"); layout read as ggml's (see its section).
+ *  - Q6_K, the other follow-up of that section; layout read as ggml's.
  *  - x·Wᵀ with W stored [out, in] and used in place (SKaiNET docs "Eager
  *    execution: backends and kernels", the paragraph on the dense x·Wᵀ row).
  *
@@ -385,7 +386,111 @@ int oracle_q4_0_matmul(const float *x, const uint8_t *W, int64_t K, int64_t N, i
     return failed ? -2 : 0;
 }
 
+/* ------------------------------------------------------------------------
+ * Q6_K (SKaiNET PR #562, section "Out of scope": "ql + qh with the
+ * 4-codes-per-qh-byte half-interleaved layout").  The page names the parts;
+ * the byte layout is ggml's: 256 values in 210 bytes, ql[128] (low 4 bits),
+ * qh[64] (high 2 bits), 16 signed 8-bit sub-block scales, fp16 d (little-
+ * endian) last.  Half n (values 128n..128n+127) uses ql[64n..64n+63],
+ * qh[32n..32n+31] and scales[8n..8n+7]; for l < 32 and group g (0..3), value
+ * 128n + 32g + l takes the low nibble of ql[64n + l] (g = 0), of
+ * ql[64n + 32 + l] (g = 1), the high nibble of ql[64n + l] (g = 2), of
+ * ql[64n + 32 + l] (g = 3), plus bits 2g..2g+1 of qh[32n + l] as bits 4..5;
+ * its sub-block is 8n + 2g + l/16 and w = d·scale·(q − 32).
+ * ------------------------------------------------------------------------ */
+#define Q6K_VALUES 256
+#define Q6K_BYTES 210
+
+static int q6k_code(const uint8_t *blk, int v)
+{
+    int n = v / 128, g = (v % 128) / 32, l = v % 32;
+    const uint8_t *ql = blk + 64 * n, *qh = blk + 128 + 32 * n;
+    int lo = (g & 1) ? ql[32 + l] : ql[l];
+    lo = (g & 2) ? (lo >> 4) : (lo & 15);
+    int hi = (qh[l] >> (2 * g)) & 3;
+    return lo | (hi << 4);
+}
+
+/* Dequantize one 210-byte block: w[v] = d·scale_s·(q_v − 32), exact in double
+ * (11-bit d × 8-bit scale × 6-bit code) and rounded once to float. */
+void oracle_q6k_dequant_block(const uint8_t *blk, float w[Q6K_VALUES])
+{
+    double d = oracle_fp16_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+    const int8_t *sc = (const int8_t *)(blk + 192);
+    for (int v = 0; v < Q6K_VALUES; ++v) {
+        int n = v / 128, g = (v % 128) / 32, l = v % 32;
+        int s = 8 * n + 2 * g + l / 16;
+        w[v] = (float)(d * sc[s] * (q6k_code(blk, v) - 32));
+    }
+}
+
+int oracle_q6k_dequant(const uint8_t *W, int64_t K, int64_t N, float *out)
+{
+    if (K <= 0 || N <= 0 || K % Q6K_VALUES)
+        return -1;
+    int64_t nb = K / Q6K_VALUES;
+    for (int64_t o = 0; o < N; ++o)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_q6k_dequant_block(W + (o * nb + b) * Q6K_BYTES, out + o * K + b * Q6K_VALUES);
+    return 0;
+}
+
+/* y[t][o] = Σ_k x[t][k]·w[o][k], w the fp32 dequantized Q6_K weight, summed
+ * sequentially in k with a double accumulator. */
+int oracle_q6k_matmul(const float *x, const uint8_t *W, int64_t K, int64_t N, int64_t T, double *y,
+                      int nthreads)
+{
+    if (K <= 0 || N <= 0 || T <= 0 || K % Q6K_VALUES)
+        return -1;
+    int64_t nb = K / Q6K_VALUES;
+    int nt = set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel num_threads(nt)
+    {
+        float *w = (float *)malloc((size_t)K * sizeof(float));
+        if (!w) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t o = 0; o < N; ++o) {
+            if (!w)
+                continue;
+            for (int64_t b = 0; b < nb; ++b)
+                oracle_q6k_dequant_block(W + (o * nb + b) * Q6K_BYTES, w + b * Q6K_VALUES);
+            for (int64_t t = 0; t < T; ++t) {
+                const float *xt = x + t * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (double)xt[k] * (double)w[k];
+                y[t * N + o] = acc;
+            }
+        }
+        free(w);
+    }
+    return failed ? -2 : 0;
+}
+
 /* Encoders, used only to build hand-worked fixtures in the tests. */
+
+/* Pack one Q6_K block from d's fp16 bits, 16 scales (−128..127) and 256 codes
+ * (0..63), inverse of the unpacking above. */
+void oracle_q6k_pack_block(uint16_t d_bits, const int sc[16], const int q[Q6K_VALUES],
+                           uint8_t out[Q6K_BYTES])
+{
+    memset(out, 0, Q6K_BYTES);
+    for (int v = 0; v < Q6K_VALUES; ++v) {
+        int n = v / 128, g = (v % 128) / 32, l = v % 32;
+        int lo = q[v] & 15, hi = (q[v] >> 4) & 3;
+        uint8_t *ql = out + 64 * n + ((g & 1) ? 32 : 0) + l;
+        *ql |= (uint8_t)((g & 2) ? (lo << 4) : lo);
+        out[128 + 32 * n + l] |= (uint8_t)(hi << (2 * g));
+    }
+    for (int s = 0; s < 16; ++s)
+        out[192 + s] = (uint8_t)(int8_t)sc[s];
+    out[208] = d_bits & 255;
+    out[209] = d_bits >> 8;
+}
 
 /* Pack one Q4_0 block from d's fp16 bits and 32 codes (0..15). */
 void oracle_q4_0_pack_block(uint16_t d_bits, const int q[Q40_VALUES], uint8_t out[Q40_BYTES])

@@ -111,3 +111,37 @@ def q4_0_matmul(x_rows, W_rows, K: int):
             row_out.append(acc)
         y.append(row_out)
     return y
+
+
+def q6k_block_values(blk: bytes):
+    """The 256 exact values of one Q6_K block, read bit by bit: the whole ql
+    area and qh area as little-endian integers, nibble and 2-bit fields taken
+    at computed bit offsets."""
+    blk = bytes(blk)
+    ql = int.from_bytes(blk[0:128], "little")
+    qh = int.from_bytes(blk[128:192], "little")
+    scales = [b - 256 if b > 127 else b for b in blk[192:208]]
+    d = fp16(blk[208] | blk[209] << 8)
+    vals = []
+    for v in range(256):
+        n, g, l = v // 128, (v % 128) // 32, v % 32
+        byte = 64 * n + (32 if g % 2 else 0) + l
+        lo = _bits(ql, 8 * byte + (4 if g >= 2 else 0), 4)
+        hi = _bits(qh, 8 * (32 * n + l) + 2 * g, 2)
+        vals.append(d * scales[8 * n + 2 * g + l // 16] * (lo + 16 * hi - 32))
+    return vals
+
+
+def q6k_matmul(x_rows, W_rows, K: int):
+    """y[t][o] exactly from Q6_K rows (each weight exact in fp32 already)."""
+    y = []
+    for xt in x_rows:
+        row_out = []
+        for wrow in W_rows:
+            acc = Fraction(0)
+            for b in range(K // 256):
+                for e, v in enumerate(q6k_block_values(wrow[210 * b:210 * (b + 1)])):
+                    acc += Fraction(float(xt[256 * b + e])) * v
+            row_out.append(acc)
+        y.append(row_out)
+    return y

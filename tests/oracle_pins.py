@@ -348,11 +348,79 @@ def pin_swiglu(lib):
     assert abs(h[2, 0] - 14.999995411466594) < 1e-13      # 15 / (1 + e^-15)
 
 
+def _q6k_sub(v):
+    return 8 * (v // 128) + 2 * ((v % 128) // 32) + (v % 32) // 16
+
+
+def pin_q6k_handworked(lib):
+    fx = fixtures.read("q6k_handworked_block.txt")
+    sc = [s - 8 for s in range(16)]
+    q = [(5 * v + 3) % 64 for v in range(256)]
+    blk = oracle.q6k_pack_block(int(fx["d_bits"], 16), sc, q, lib=lib)
+    assert list(blk[0:4]) == fixtures.hexbytes(fx["ql_0_3"])
+    assert blk[128] == fixtures.hexbytes(fx["qh_0"])[0]
+    assert list(blk[192:196]) == fixtures.hexbytes(fx["scales_0_3"])
+    w = oracle.q6k_dequant(blk, 256, 1, lib=lib)[0]
+    for v in (0, 17, 100, 255):
+        assert w[v] == float(fx[f"w_{v}"]), (v, w[v])
+    assert oracle.q6k_matmul(np.ones((1, 256), np.float32), blk, 256, 1, lib=lib)[0, 0] == float(fx["sum_w"])
+    x = np.array([[(v % 5) - 2 for v in range(256)]], np.float32)
+    assert oracle.q6k_matmul(x, blk, 256, 1, lib=lib)[0, 0] == float(fx["y_x_mod5"])
+
+
+def pin_q6k_code_positions(lib):
+    # d = 1, every scale 1, every code 32 (value 0) except code 63 at one
+    # value: exactly that value is 31.  Each group, both halves, both
+    # sub-blocks of a group.
+    for v in (0, 15, 16, 31, 32, 47, 63, 64, 95, 96, 127, 128, 160, 200, 255):
+        q = [32] * 256
+        q[v] = 63
+        blk = oracle.q6k_pack_block(0x3C00, [1] * 16, q, lib=lib)
+        w = oracle.q6k_dequant(blk, 256, 1, lib=lib)[0]
+        want = np.zeros(256, np.float32)
+        want[v] = 31.0
+        assert np.array_equal(w, want), v
+        # The same code written straight into the bytes (independent of the
+        # packer): ql nibble 15 and qh bits 3 at the computed places.
+        raw = oracle.q6k_pack_block(0x3C00, [1] * 16, [32] * 256, lib=lib)
+        n, g, l = v // 128, (v % 128) // 32, v % 32
+        ql = 64 * n + (32 if g % 2 else 0) + l
+        raw[ql] |= 0xF0 if g >= 2 else 0x0F
+        raw[128 + 32 * n + l] |= 3 << (2 * g)
+        assert np.array_equal(oracle.q6k_dequant(raw, 256, 1, lib=lib)[0], want), v
+
+
+def pin_q6k_scale_positions(lib):
+    # Every code 33 (value +1 before scaling), distinct signed scales: each
+    # value is its sub-block's scale.
+    sc = [-128, -3, 1, 2, 5, 7, 11, 13, 17, 19, 23, 29, 31, 64, 100, 127]
+    blk = oracle.q6k_pack_block(0x3C00, sc, [33] * 256, lib=lib)
+    w = oracle.q6k_dequant(blk, 256, 1, lib=lib)[0]
+    assert np.array_equal(w, np.array([sc[_q6k_sub(v)] for v in range(256)], np.float32))
+
+
+def pin_q6k_fraction_bruteforce(lib):
+    g = np.random.default_rng(41)
+    for K, N, T in ((256, 2, 2), (512, 2, 1)):
+        W = np.stack([np.concatenate([oracle.q6k_pack_block(int(g.integers(0x1400, 0x2400)),
+                                                            g.integers(-128, 128, 16), g.integers(0, 64, 256),
+                                                            lib=lib)
+                                      for _ in range(K // 256)]) for _ in range(N)])
+        x = g.standard_normal((T, K)).astype(np.float32)
+        y = oracle.q6k_matmul(x, W, K, N, lib=lib)
+        exact = fr.q6k_matmul(x.tolist(), [bytes(r) for r in W], K)
+        for t in range(T):
+            for o in range(N):
+                e = exact[t][o]
+                assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
+
+
 ALL_PINS = [
     pin_fp16_decode, pin_bf16_round, pin_handworked_pack, pin_handworked_values,
     pin_nibble_positions, pin_scale_positions, pin_special_cases, pin_one_hot_rows,
     pin_lazy_equals_direct, pin_fraction_bruteforce, pin_ternary_handworked,
     pin_ternary_integer_count, pin_ternary_scale, pin_bf16_variant,
     pin_q4_0_handworked, pin_q4_0_nibble_positions, pin_q4_0_as_q4k, pin_q4_0_fraction_bruteforce,
-    pin_swiglu,
+    pin_swiglu, pin_q6k_handworked, pin_q6k_code_positions, pin_q6k_scale_positions,
+    pin_q6k_fraction_bruteforce,
 ]

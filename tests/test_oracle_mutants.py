@@ -39,6 +39,13 @@ MUTANTS = {
     "swiglu_sigmoid_sign": ("h[i] = z / (1.0 + exp(-z)) * uu[i];", "h[i] = z / (1.0 + exp(z)) * uu[i];"),
     "swiglu_gate_up_swapped": ("rc = q4k_matmul_impl(x, Wg, K, N, T, gg, nthreads, 0);",
                                "rc = q4k_matmul_impl(x, Wu, K, N, T, gg, nthreads, 0);"),
+    "q6k_qh_shift": ("int hi = (qh[l] >> (2 * g)) & 3;", "int hi = (qh[l] >> g) & 3;"),
+    "q6k_ql_halves": ("int lo = (g & 1) ? ql[32 + l] : ql[l];", "int lo = (g & 2) ? ql[32 + l] : ql[l];"),
+    "q6k_sub_block": ("int s = 8 * n + 2 * g + l / 16;", "int s = 8 * n + g + l / 16;"),
+    "q6k_offset": ("w[v] = (float)(d * sc[s] * (q6k_code(blk, v) - 32));",
+                   "w[v] = (float)(d * sc[s] * (q6k_code(blk, v) - 31));"),
+    "q6k_scales_unsigned": ("const int8_t *sc = (const int8_t *)(blk + 192);",
+                            "const uint8_t *sc = (const uint8_t *)(blk + 192);"),
     "q4_0_nibble_halves": ("return e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);",
                            "return e < 16 ? (qs[e] >> 4) : (qs[e - 16] & 15);"),
     "q4_0_offset": ("w[e] = (float)(d * (q40_code(blk + 2, e) - 8));",
