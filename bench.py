@@ -83,6 +83,8 @@ def weight_bytes(kind, K, N):
         return N * (K // 32) * 18
     if kind == "q4k_ffn":
         return 2 * _q4k_bytes(K, N)
+    if kind == "q6k":
+        return N * (K // 256) * 210
     return N * (K // 4)
 
 
@@ -111,6 +113,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("q4_0_gemv_4096x4096_t1", "q4_0", "q4_0_gemv", [(4096, 4096)], 1, 64, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_0 GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
              "q4_0_gemv_t1_4096x4096.md", distinct=64, arithmetic=T1_ARITH),
+    Workload("q6k_gemv_4096x4096_t1", "q6k", "q6k_gemv", [(4096, 4096)], 1, 48, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q6_K GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
+             "q6k_gemv_t1_4096x4096.md", distinct=48, arithmetic=T1_ARITH.replace("4-bit", "6-bit")),
     Workload("llama7b_ffn_swiglu_t1", "q4k_ffn", "q4k_ffn_swiglu", [(4096, 11008)], 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K fused gate+up SwiGLU weight-stream GB/s, Llama-2-7B FFN (32 layers x "
              "4096 -> 2 x 11008), batch 1", ["q4k_gemv.cu"], "q4k_ffn_swiglu_llama7b_t1.md", distinct=1,
@@ -347,6 +352,8 @@ def host_inputs(w: Workload, seed: int = 0):
             Ws = [synth.q4k_weights(g, N, K) for _ in range(n)]
         elif w.kind == "q4_0":
             Ws = [synth.q4_0_weights(g, N, K) for _ in range(n)]
+        elif w.kind == "q6k":
+            Ws = [synth.q6k_weights(g, N, K) for _ in range(n)]
         elif w.kind == "q4k_ffn":
             import numpy as np
             Ws = [np.concatenate([synth.q4k_weights(g, N, K).reshape(-1), synth.q4k_weights(g, N, K).reshape(-1)])
@@ -366,7 +373,7 @@ def workload_config(w: Workload, plan: Plan) -> dict:
             "weight_bytes_per_step": plan.weight_bytes,
             "l2": f"inputs larger than L2: {plan.weight_bytes / 1e6:.0f} MB of weights per step "
                   f"(L2 129 MB), no flush",
-            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks', q4k_ffn='Q4_K blocks (gate, up)').get(w.kind, 'ternary codes')}, seed 0 "
+            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks', q4k_ffn='Q4_K blocks (gate, up)', q6k='Q6_K blocks').get(w.kind, 'ternary codes')}, seed 0 "
                        f"(synth), {w.distinct} distinct host copies per matrix",
             "activations": "fp32 N(0,1), seed 0"}
 
@@ -377,6 +384,8 @@ def oracle_call(w: Workload, K, N, W, x, scale, rows, r0=0):
         oracle.q4k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
     elif w.kind == "q4_0":
         oracle.q4_0_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
+    elif w.kind == "q6k":
+        oracle.q6k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
     elif w.kind == "q4k_ffn":
         Wg, Wu = W.reshape(2, N, -1)
         oracle.q4k_ffn_swiglu(x, Wg[r0:r0 + rows], Wu[r0:r0 + rows], K, rows)

@@ -142,6 +142,35 @@ int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int
 int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int outputDim,
               int tokens, q4mm_stream_t stream);
 
+/* Largest inputDim accepted by q6k_gemv. */
+#define Q4MM_Q6K_MAX_INPUT_DIM 32768
+
+/*
+ * q6k_gemv — y = x·Wᵀ with W in Q6_K, FP32 result.
+ *
+ * The block is the second follow-up SKaiNET PR #562 names (section "Out of
+ * scope": Q6_K, "ql + qh with the 4-codes-per-qh-byte half-interleaved
+ * layout").  The page gives no byte layout; this library reads it as ggml's:
+ * 256 values in 210 bytes — ql[128] (low 4 bits of each 6-bit code), qh[64]
+ * (high 2 bits, four codes per byte), 16 signed 8-bit sub-block scales, fp16
+ * d (little-endian) last.  In half n (values 128n..128n+127), value
+ * 128n + 32g + l (g = 0..3, l < 32) takes the low nibble of ql[64n + l]
+ * (g = 0) or of ql[64n + 32 + l] (g = 1), the high nibble of ql[64n + l]
+ * (g = 2) or of ql[64n + 32 + l] (g = 3), and bits 2g..2g+1 of qh[32n + l];
+ * its sub-block is 8n + 2g + l/16 and w = d·scale·(q − 32).
+ *
+ * w_q6k : N·(K/256) blocks of 210 bytes, each row contiguous (rows need not
+ *         start on a 16-byte boundary).  The buffer is 16-byte aligned.
+ * x     : 16-byte aligned.  y: 4-byte aligned.
+ * Limits: inputDim a positive multiple of 256 and <= Q4MM_Q6K_MAX_INPUT_DIM;
+ *         outputDim >= 1; tokens >= 1 (each token one pass over the weights).
+ * Precision: as the one-token path of q4k_matmul: per token row,
+ *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q6k_gemv(const float *x, const void *w_q6k, float *y, int inputDim, int outputDim, int tokens,
+             q4mm_stream_t stream);
+
 /* Largest inputDim accepted by q4k_ffn_swiglu. */
 #define Q4MM_FFN_MAX_INPUT_DIM 32768
 

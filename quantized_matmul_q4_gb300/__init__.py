@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     q4k_matmul_tc_noalloc_ptr,
     q4_0_gemv,
     q4_0_gemv_ptr,
+    q6k_gemv,
+    q6k_gemv_ptr,
     q4k_ffn_swiglu,
     q4k_ffn_swiglu_ptr,
     ternary_gemv,

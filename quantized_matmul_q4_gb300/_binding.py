@@ -8,7 +8,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 Q4K_VALUES = 256
 Q4K_BYTES = 144
 
-_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q4k_ffn_swiglu",
+_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q6k_gemv", "q4k_ffn_swiglu",
             "ternary_gemv",
             "q4mm_last_error", "q4mm_device_status", "q4mm_version")
 
@@ -33,7 +33,7 @@ def _load() -> ctypes.CDLL:
             "(needs nvcc); there is no fallback implementation")
     lib = ctypes.CDLL(path)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv"):
+    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q6k_gemv"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         fn.restype = i32
@@ -93,6 +93,10 @@ def q4k_matmul_tc_noalloc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, st
 
 def q4_0_gemv_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
     _check(_LIB.q4_0_gemv(x, w, y, K, N, T, stream))
+
+
+def q6k_gemv_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
+    _check(_LIB.q6k_gemv(x, w, y, K, N, T, stream))
 
 
 def q4k_ffn_swiglu_ptr(x: int, w_gate: int, w_up: int, h: int, K: int, N: int, T: int,
@@ -162,6 +166,16 @@ def q4_0_gemv(x, w, N: int | None = None, out=None, stream=None):
     """y[T, N] = x[T, K] · dequant_q4_0(W)ᵀ in FP32 (one weight pass per token)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q40_VALUES) * Q40_BYTES, out, N)
     q4_0_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+Q6K_BYTES = 210
+
+
+def q6k_gemv(x, w, N: int | None = None, out=None, stream=None):
+    """y[T, N] = x[T, K] · dequant_q6k(W)ᵀ in FP32 (one weight pass per token)."""
+    x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q6K_BYTES, out, N)
+    q6k_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
     return out.view(T, N)
 
 

@@ -207,6 +207,23 @@ int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int ou
     return Q4MM_OK;
 }
 
+int q6k_gemv(const float *x, const void *w_q6k, float *y, int inputDim, int outputDim, int tokens,
+             q4mm_stream_t stream) {
+    int rc = check_common(x, w_q6k, y, inputDim, outputDim, tokens, 256, (size_t)(inputDim / 256) * 210, 16);
+    if (rc) return rc;
+    if (inputDim > Q4MM_Q6K_MAX_INPUT_DIM)
+        return fail(Q4MM_ERR_DIM, "inputDim %d exceeds the Q6_K limit %d", inputDim, Q4MM_Q6K_MAX_INPUT_DIM);
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    const uint8_t *W = static_cast<const uint8_t *>(w_q6k);
+    for (int t = 0; t < tokens; ++t) {
+        const cudaError_t e = q4mm::launch_q6k_gemv_t1(ctx, x + (size_t)t * inputDim, W,
+                                                       y + (size_t)t * outputDim, inputDim, outputDim);
+        if (e != cudaSuccess) return fail_cuda(e, "q6k_gemv launch");
+    }
+    return Q4MM_OK;
+}
+
 int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *h, int inputDim,
                    int hiddenDim, int tokens, q4mm_stream_t stream) {
     const size_t row_bytes = (size_t)(inputDim / 256) * 144;

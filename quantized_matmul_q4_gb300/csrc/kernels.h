@@ -26,6 +26,9 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                 int K, int N);
 
+// Q6_K decode GEMV, one token (the one-token kernel with the Q6_K row format).
+cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N);
+
 // BitNet b1.58 ternary GEMV, one token, on the same one-token kernel with the
 // byte-plane integer code-dot (K % 256 == 0, W 16-byte aligned; otherwise
 // cudaErrorNotSupported).

@@ -213,7 +213,8 @@ struct FmtQ4K {
         LaneScaleSel sel;
         int j;
     };
-    __device__ static Lane lane(int j) { return Lane{lane_scale_sel(j), j}; }
+    __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
+    __device__ static Lane lane(int j, const float *) { return Lane{lane_scale_sel(j), j}; }
     __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
                                 float sum_lo, float sum_hi) {
         return slab_row(grp, L.j, L.sel, unit, pl, sum_lo, sum_hi);
@@ -231,7 +232,8 @@ struct FmtQ40 {
     struct Lane {
         int j;
     };
-    __device__ static Lane lane(int j) { return Lane{j}; }
+    __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
+    __device__ static Lane lane(int j, const float *) { return Lane{j}; }
     __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
                                 float sum_lo, float sum_hi) {
         const uint32_t *p = reinterpret_cast<const uint32_t *>(grp + 36 * L.j);
@@ -298,7 +300,8 @@ struct FmtTern {
     struct Lane {
         int j;
     };
-    __device__ static Lane lane(int j) { return Lane{j}; }
+    __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
+    __device__ static Lane lane(int j, const float *) { return Lane{j}; }
     __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
                                 float sum_lo, float sum_hi) {
         const uint4 q = *reinterpret_cast<const uint4 *>(grp + 16 * L.j);
@@ -315,6 +318,87 @@ struct FmtTern {
             }
         }
         return fmaf(unit, plane_combine(d), -(sum_lo + sum_hi));
+    }
+};
+
+// Q6_K (the other follow-up named by SKaiNET PR #562, section "Out of
+// scope"; byte layout read as ggml's): 256 values in 210 bytes — ql[128]
+// (low 4 bits), qh[64] (high 2 bits, four codes per byte), 16 signed 8-bit
+// sub-block scales, fp16 d last; w = d·scale·(q − 32).  Lane j = 2n + h takes,
+// in half n, the values 128n + 32g + 16h + l for g = 0..3 and l < 16: bytes
+// 16h..16h+15 of the runs ql[64n..], ql[64n + 32..] and qh[32n..], one
+// sub-block (and scale) per g.  Blocks start at any even byte, so every
+// 16-byte run is read as five aligned words and funnel-shifted.
+struct FmtQ6K {
+    static constexpr int kGroupBytes = 210;
+    __device__ static void prep_planes(int (&)[3][16]) {}
+    __device__ static void unit_of(int j, int i, int &slab, int &pos) {
+        slab = 2 * (j >> 1) + (i >> 1);
+        pos = 2 * (i & 1) + (j & 1);
+    }
+    struct Lane {
+        int n, h;
+        float s16[4];  // Σ x over each of the lane's four 16-value sub-blocks
+    };
+    __device__ static Lane lane(int j, const float *bsx16) {
+        Lane L;
+        L.n = j >> 1;
+        L.h = j & 1;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) L.s16[g] = bsx16[8 * L.n + 2 * g + L.h];
+        return L;
+    }
+    // Four words starting `off` bytes after the 4-byte aligned `base`, shifted
+    // right by `sh` bits across word boundaries.
+    __device__ static void run16(const uint32_t *base, int off, uint32_t sh, uint32_t (&o)[4]) {
+        const uint32_t *p = base + off / 4;
+        uint32_t w[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) w[i] = p[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
+    }
+    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16], float,
+                                float) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(grp);
+        const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
+        const uint32_t sh = (uint32_t)(a & 3) * 8;
+        uint32_t qa[4], qb[4], qh[4], sw[4];
+        run16(base, 64 * L.n + 16 * L.h, sh, qa);
+        run16(base, 64 * L.n + 32 + 16 * L.h, sh, qb);
+        run16(base, 128 + 32 * L.n + 16 * L.h, sh, qh);
+        run16(base, 192, sh, sw);  // the 16 scales
+        const uint32_t dbits = (base[52] >> sh) & 0xFFFFu;  // bytes 208..209
+        const float d = __half2float(__ushort_as_half((unsigned short)dbits));
+        // Scale g of this lane is scale byte 8n + h + 2g: word 2n (g < 2) or
+        // 2n + 1, byte h + 2(g & 1).  Signed byte v → the float 2^23 + 128 + v
+        // by one XOR and one byte permute, minus 2^23 + 128 (exact: both are
+        // integers below 2^24), times d (exact: 11 × 8 significant bits).
+        const uint32_t s0 = (L.n ? sw[2] : sw[0]) ^ 0x80808080u, s1 = (L.n ? sw[3] : sw[1]) ^ 0x80808080u;
+        float sc[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t word = g < 2 ? s0 : s1;
+            const uint32_t sel = 0x7440u | (uint32_t)(L.h + 2 * (g & 1));
+            sc[g] = d * (__uint_as_float(__byte_perm(word, 0x4B000000u, sel)) - 8388736.0f);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            int dd[3] = {0, 0, 0};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t src = (g & 1) ? qb[k] : qa[k];
+                const uint32_t lo = (g & 2) ? ((src >> 4) & 0x0F0F0F0Fu) : (src & 0x0F0F0F0Fu);
+                const uint32_t hs = g == 0 ? (qh[k] << 4) : g == 1 ? (qh[k] << 2) : g == 2 ? qh[k] : (qh[k] >> 2);
+                const uint32_t code = (hs & 0x30303030u) | lo;  // 6-bit codes, four bytes
+                dd[0] = dp4a_uu(code, (uint32_t)pl[0][4 * g + k], dd[0]);
+                dd[1] = dp4a_uu(code, (uint32_t)pl[1][4 * g + k], dd[1]);
+                dd[2] = dp4a_us(code, pl[2][4 * g + k], dd[2]);
+            }
+            acc = fmaf(sc[g], fmaf(unit, plane_combine(dd), -32.0f * L.s16[g]), acc);
+        }
+        return acc;
     }
 };
 
@@ -380,7 +464,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     const uint32_t slot_bytes = p.stage_rows * row_bytes;
     uint8_t *planes = smem;                                           // nslabs × 208 bytes
     float *sx = reinterpret_cast<float *>(planes + nslabs * kPlaneSlabBytes);  // K/32 sub-block sums
-    float *sb = sx + K / 32;                                          // K/256 block scales
+    float *sx16 = sx + K / 32;                                        // K/16 half-sub-block sums
+    float *sb = sx16 + K / 16;                                        // K/256 block scales
     float *xst = sb + ((nb + 3) & ~3);                                // x (when staged)
     uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? K : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
@@ -418,12 +503,27 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             auto issue = [&](int st, int slot) {
                 const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
                 uint8_t *dst = ring + (size_t)slot * slot_bytes;
-                mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
                 // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
                 const int g1 = kSwiGLU ? min(v1, nrows) : v1;
-                if (g1 > v0)
-                    bulk_g2s(dst, p.W + (size_t)(row0 + v0) * row_bytes, (uint32_t)(g1 - v0) * row_bytes,
-                             &full_bar[slot]);
+                if (g1 > v0) {
+                    const uint8_t *src = p.W + (size_t)(row0 + v0) * row_bytes;
+                    const uint32_t bytes = (uint32_t)(g1 - v0) * row_bytes;
+                    // Rows of a format whose row size is not a multiple of 16
+                    // start stages on 8-row boundaries (16-byte aligned); only
+                    // the last stage of the matrix can end off the 16-byte
+                    // grid: its last bytes go by plain loads, ahead of the
+                    // arrive that publishes the stage.
+                    const uint32_t bulk = bytes & ~15u;
+                    if (bulk != bytes) {
+                        for (uint32_t i = bulk; i < bytes; ++i) dst[i] = __ldg(src + i);
+                        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes - (bytes - bulk));
+                    } else {
+                        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
+                    }
+                    bulk_g2s(dst, src, bulk, &full_bar[slot]);
+                } else {
+                    mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
+                }
                 if (kSwiGLU && v1 > nrows) {
                     const int u0 = max(v0, nrows);
                     bulk_g2s(dst + (size_t)(u0 - v0) * row_bytes, p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes,
@@ -499,6 +599,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                 // Non-negative floats order like their bit patterns.
                 amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));
                 sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                const float sum16 = sum;
                 sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
                 // s_b = 2^ex with amax / 2^ex <= 127 (1 when the block is
                 // zero): ex is the binary exponent of amax/127 written as
@@ -531,6 +632,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                     pu[0] = make_uint2(w[0][0], w[0][1]);
                     pu[8] = make_uint2(w[1][0], w[1][1]);
                     pu[16] = make_uint2(w[2][0], w[2][1]);
+                    if ((e & 1) == 0) sx16[e / 2] = sum16;
                     if ((e & 3) == 0) sx[e / 4] = sum;
                     if ((e & 31) == 0) sb[e / 32] = __uint_as_float((uint32_t)(127 + ex) << 23);
                 }
@@ -542,12 +644,16 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
         {
             // This slab's 64 plane bytes per plane: positions 64j..64j+31
             // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
-            const uint4 *src = reinterpret_cast<const uint4 *>(planes + (4 * b + j) * kPlaneSlabBytes);
+            // (Fmt::unit_of names the slab and 16-value unit of each of the
+            // lane's four runs; the Q4 and ternary lanes take slab j in order.)
 #pragma unroll
             for (int pp = 0; pp < 3; ++pp) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 t = active ? src[4 * pp + i] : make_uint4(0u, 0u, 0u, 0u);
+                    int us, up;
+                    Fmt::unit_of(j, i, us, up);
+                    const uint4 *src = reinterpret_cast<const uint4 *>(planes + (4 * b + us) * kPlaneSlabBytes);
+                    const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
                     pl[pp][4 * i] = (int)t.x;
                     pl[pp][4 * i + 1] = (int)t.y;
                     pl[pp][4 * i + 2] = (int)t.z;
@@ -559,7 +665,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
         }
         Fmt::prep_planes(pl);
-        const typename Fmt::Lane lfmt = Fmt::lane(j);
+        const typename Fmt::Lane lfmt = Fmt::lane(j, sx16 + 16 * b);
         const float unit = s_blk * (1.0f / 32768.0f);
 
         const int npasses = (nv + pass_rows - 1) / pass_rows;
@@ -885,20 +991,33 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     p.rg = max(1, tun.warps / wc);
     const int ncw = wc * p.rg;
     // Stage: whole passes, at least stage_bytes of weights (bulk copies of
-    // 16 KB and more run at full HBM bandwidth).
-    p.stage_rows = pass_rows * max(1, (tun.stage_bytes + pass_rows * row_bytes - 1) /
-                                          (pass_rows * row_bytes));
+    // 16 KB and more run at full HBM bandwidth).  A row size off the 16-byte
+    // grid (Q6_K) keeps CTA and stage boundaries on multiples of rq rows,
+    // the fewest whose bytes are a multiple of 16 (row_bytes = 2·odd·nb, so
+    // rq = 8 / gcd(nb, 8)).
+    int rq = 1;
+    if (row_bytes % 16) {
+        rq = 8;
+        while (rq > 1 && (rq / 2) * row_bytes % 16 == 0) rq /= 2;
+    }
+    const int sq = max(pass_rows, rq);  // both powers of two
+    p.stage_rows = sq * max(1, (tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
 
     int grid = tun.ctas_per_sm * c.num_sms;
     p.rows_per_cta = (N + grid - 1) / grid;
+    p.rows_per_cta = (p.rows_per_cta + rq - 1) / rq * rq;
     if (p.rows_per_cta < pass_rows) p.rows_per_cta = pass_rows;
-    if (p.stage_rows > p.rows_per_cta)
-        p.stage_rows = pass_rows * ((p.rows_per_cta + pass_rows - 1) / pass_rows);
+    if (p.stage_rows > p.rows_per_cta) p.stage_rows = sq * ((p.rows_per_cta + sq - 1) / sq);
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
     const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
     p.x_staged = (size_t)K * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
-    const size_t xs_bytes = (size_t)(K / 64) * kPlaneSlabBytes + (size_t)(K / 32) * sizeof(float) +
+    // Large rows at an 8-row stage quantum can leave no room for x: then
+    // the compute threads load x themselves.
+    if (p.x_staged && (size_t)K * sizeof(float) + 2 * slot_bytes + (size_t)(K / 64) * kPlaneSlabBytes >
+                          (size_t)c.max_smem_optin - 8192)
+        p.x_staged = 0;
+    const size_t xs_bytes = (size_t)(K / 64) * kPlaneSlabBytes + (size_t)(K / 32 + K / 16) * sizeof(float) +
                             (size_t)((p.nb * 4 + 15) & ~15) +
                             (p.x_staged ? (size_t)K * sizeof(float) : 0);
     const int vrows_per_cta = (kSwiGLU ? 2 : 1) * p.rows_per_cta;
@@ -924,6 +1043,11 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
         switch (p.nb) {
             case 16: return go(gemv_t1_kernel<Fmt, 16, true>);
             default: return go(gemv_t1_kernel<Fmt, 0, true>);
+        }
+    } else if constexpr (std::is_same<Fmt, FmtQ6K>::value) {
+        switch (p.nb) {
+            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
+            default: return go(gemv_t1_kernel<Fmt, 0, false>);
         }
     } else if constexpr (std::is_same<Fmt, FmtTern>::value) {
         switch (p.nb) {
@@ -954,6 +1078,10 @@ cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
     return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N);
+}
+
+cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
+    return launch_gemv_t1<FmtQ6K>(c, x, W, y, K, N);
 }
 
 cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,

@@ -16,6 +16,9 @@ d ~ U[1e-3, 1e-2] and dmin ~ U[0, 1e-2] are rounded to fp16 by numpy.
 Q4_0 weights are 18-byte blocks: fp16 d ~ U[1e-3, 1e-2] and 16 uniform qs
 bytes (every 4-bit code uniform on 0..15).
 
+Q6_K blocks are uniform bytes (uniform 6-bit codes and signed 8-bit scales)
+with fp16 d ~ U[1e-3, 1e-2] in their last two bytes.
+
 Ternary weights are drawn uniformly from the 81 byte values whose four 2-bit
 fields are all 0, 1 or 2 — the same as drawing each code uniformly from
 {-1, 0, +1} independently.
@@ -66,6 +69,21 @@ def q4_0_weights(g: np.random.Generator, N: int, K: int, d_range=(1e-3, 1e-2)) -
     return blocks.reshape(N, nb * Q40_BYTES)
 
 
+Q6K_BYTES = 210
+
+
+def q6k_weights(g: np.random.Generator, N: int, K: int, d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Random Q6_K weight: uint8 [N, K/256·210]: uniform ql and qh bytes
+    (every 6-bit code uniform on 0..63), uniform signed scale bytes, fp16
+    d ~ U[1e-3, 1e-2] in the last two bytes of each block."""
+    assert K % Q4K_VALUES == 0 and K > 0 and N > 0
+    nb = K // Q4K_VALUES
+    blocks = g.integers(0, 256, size=(N, nb, Q6K_BYTES), dtype=np.uint8)
+    d = g.uniform(d_range[0], d_range[1], size=(N, nb)).astype("<f2")
+    blocks[:, :, 208:210] = d.view(np.uint8).reshape(N, nb, 2)
+    return blocks.reshape(N, nb * Q6K_BYTES)
+
+
 def _valid_ternary_bytes() -> np.ndarray:
     """Byte values whose four 2-bit fields each hold 0, 1 or 2 (81 of them)."""
     vals = [b for b in range(256) if all(((b >> (2 * i)) & 3) != 3 for i in range(4))]
@@ -103,6 +121,7 @@ WORKLOADS = {
     "q4k_gemv_4096x4096_t1": dict(kind="q4k", K=4096, N=4096, T=1),
     "q4k_prefill_4096x11008_t64": dict(kind="q4k", K=4096, N=11008, T=64),
     "q4_0_gemv_4096x4096_t1": dict(kind="q4_0", K=4096, N=4096, T=1),
+    "q6k_gemv_4096x4096_t1": dict(kind="q6k", K=4096, N=4096, T=1),
     "ternary_gemv_2560x6912_t1": dict(kind="ternary", K=2560, N=6912, T=1),
     "ternary_gemv_2560x6912_t16": dict(kind="ternary", K=2560, N=6912, T=16),
 }
@@ -149,5 +168,18 @@ def q4_0_case(name_or_dims, seed: int = 0, xkind: str = "normal"):
         K, N, T = name_or_dims
     g = rng(seed)
     W = q4_0_weights(g, N, K)
+    x = activations(g, T, K, xkind)
+    return x, W, K, N, T
+
+
+def q6k_case(name_or_dims, seed: int = 0, xkind: str = "normal"):
+    """(x, W, K, N, T) with a Q6_K weight, for a named workload or (K, N, T)."""
+    if isinstance(name_or_dims, str):
+        w = WORKLOADS[name_or_dims]
+        K, N, T = w["K"], w["N"], w["T"]
+    else:
+        K, N, T = name_or_dims
+    g = rng(seed)
+    W = q6k_weights(g, N, K)
     x = activations(g, T, K, xkind)
     return x, W, K, N, T

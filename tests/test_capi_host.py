@@ -139,3 +139,10 @@ def test_ffn_swiglu_validation(q4mm):
     with pytest.raises(q4mm.Q4mmError) as e:   # h inside the up weight
         q4mm.q4k_ffn_swiglu_ptr(X, W, Y, Y + 64, 256, 16, 1, 0)
     assert e.value.code == ALIAS
+
+
+@pytest.mark.parametrize("K", [0, 128, 300, 32768 + 256])
+def test_q6k_rejects_bad_input_dim(q4mm, K):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q6k_gemv_ptr(X, W, Y, K, 16, 1, 0)
+    assert e.value.code == DIM and "inputDim" in q4mm.last_error()
