@@ -75,12 +75,14 @@ typedef enum {
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
  *         outputDim >= 1; tokens >= 1.
  * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
- *         One token: x is rounded once to 2^-22 of each 256-value block's
- *         largest magnitude (exactly for integers and any value with at
- *         most 22 significant bits below that maximum) and split into three
- *         byte planes under a power-of-two block scale; the code-dots are
- *         exact integer sums, scales, mins and the combination are fp32.  Two or more
- *         tokens: fp32 dequantization and fp32 fused multiply-add.
+ *         Up to 4 tokens: x is rounded once to 2^-22 of each 256-value
+ *         block's largest magnitude (exactly for integers and any value with
+ *         at most 22 significant bits below that maximum) and split into
+ *         three byte planes under a power-of-two block scale; the code-dots
+ *         are exact integer sums, scales, mins and the combination are fp32.
+ *         Where that kernel's geometry does not fit (2-4 tokens with a large
+ *         inputDim), and above 4 tokens: fp32 dequantization and fp32 fused
+ *         multiply-add.
  * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
  * 64 tokens above that).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
@@ -135,8 +137,8 @@ int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int
  *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|, with x rounded once
  *         to 2^-22 of each 256-value block's largest magnitude and integer
  *         code-dots.
- * Tokens: each token is its own pass over the weights (a decode GEMV; no
- *         weight reuse across tokens).
+ * Tokens: up to 8 tokens share one pass over the weights (more tokens
+ *         take one pass per 8).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
  */
 int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int outputDim,
@@ -163,7 +165,8 @@ int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int ou
  *         start on a 16-byte boundary).  The buffer is 16-byte aligned.
  * x     : 16-byte aligned.  y: 4-byte aligned.
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_Q6K_MAX_INPUT_DIM;
- *         outputDim >= 1; tokens >= 1 (each token one pass over the weights).
+ *         outputDim >= 1; tokens >= 1 (up to 8 tokens per pass over the
+ *         weights).
  * Precision: as the one-token path of q4k_matmul: per token row,
  *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.

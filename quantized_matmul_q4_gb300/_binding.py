@@ -163,7 +163,7 @@ Q40_VALUES, Q40_BYTES = 32, 18
 
 
 def q4_0_gemv(x, w, N: int | None = None, out=None, stream=None):
-    """y[T, N] = x[T, K] · dequant_q4_0(W)ᵀ in FP32 (one weight pass per token)."""
+    """y[T, N] = x[T, K] · dequant_q4_0(W)ᵀ in FP32 (up to 8 tokens per weight pass)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q40_VALUES) * Q40_BYTES, out, N)
     q4_0_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
     return out.view(T, N)
@@ -173,7 +173,7 @@ Q6K_BYTES = 210
 
 
 def q6k_gemv(x, w, N: int | None = None, out=None, stream=None):
-    """y[T, N] = x[T, K] · dequant_q6k(W)ᵀ in FP32 (one weight pass per token)."""
+    """y[T, N] = x[T, K] · dequant_q6k(W)ᵀ in FP32 (up to 8 tokens per weight pass)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q6K_BYTES, out, N)
     q6k_gemv_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
     return out.view(T, N)

@@ -75,6 +75,31 @@ int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx) {
     return Q4MM_OK;
 }
 
+bool multi_fp32_forced() {
+    static const bool on = [] {
+        const char *v = getenv("Q4MM_MULTI");
+        return v && v[0] == 'f';
+    }();
+    return on;
+}
+
+// Runs a one-token-kernel launcher over the tokens in chunks of up to 8,
+// halving a chunk whose geometry the kernel cannot hold.
+template <class F>
+cudaError_t token_chunks(F launch, const float *x, float *y, int K, int N, int tokens) {
+    cudaError_t e = cudaSuccess;
+    for (int t0 = 0; t0 < tokens && e == cudaSuccess;) {
+        int tt = tokens - t0 < 8 ? tokens - t0 : 8;
+        for (;;) {
+            e = launch(x + (size_t)t0 * K, y + (size_t)t0 * N, tt);
+            if (e != cudaErrorNotSupported || tt == 1) break;
+            tt /= 2;
+        }
+        t0 += tt;
+    }
+    return e;
+}
+
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + nb && b0 < a0 + na;
@@ -148,7 +173,15 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
         e = q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, 1);
     } else if (tokens <= 8) {
-        e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
+        // Up to 4 tokens: the byte-plane kernel with one token per compute
+        // warp where its geometry allows (measured 1.4-1.9x faster at 2 and
+        // 4 tokens; at 8 tokens the FP32 kernel is faster on 4096x4096);
+        // Q4MM_MULTI=fp32 forces the FP32 kernel.  Then the FP32
+        // register-tile kernel, then the prefill kernel.
+        e = (multi_fp32_forced() || tokens > 4)
+                ? cudaErrorNotSupported
+                : q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim, tokens);
+        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
     } else {
         e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
@@ -199,11 +232,12 @@ int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int ou
     q4mm::LaunchCtx ctx;
     if ((rc = device_ctx(stream, &ctx))) return rc;
     const uint8_t *W = static_cast<const uint8_t *>(w_q4_0);
-    for (int t = 0; t < tokens; ++t) {
-        const cudaError_t e = q4mm::launch_q4_0_gemv_t1(ctx, x + (size_t)t * inputDim, W,
-                                                        y + (size_t)t * outputDim, inputDim, outputDim);
-        if (e != cudaSuccess) return fail_cuda(e, "q4_0_gemv launch");
-    }
+    const cudaError_t e = token_chunks(
+        [&](const float *xt, float *yt, int tt) {
+            return q4mm::launch_q4_0_gemv_t1(ctx, xt, W, yt, inputDim, outputDim, tt);
+        },
+        x, y, inputDim, outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "q4_0_gemv launch");
     return Q4MM_OK;
 }
 
@@ -216,11 +250,12 @@ int q6k_gemv(const float *x, const void *w_q6k, float *y, int inputDim, int outp
     q4mm::LaunchCtx ctx;
     if ((rc = device_ctx(stream, &ctx))) return rc;
     const uint8_t *W = static_cast<const uint8_t *>(w_q6k);
-    for (int t = 0; t < tokens; ++t) {
-        const cudaError_t e = q4mm::launch_q6k_gemv_t1(ctx, x + (size_t)t * inputDim, W,
-                                                       y + (size_t)t * outputDim, inputDim, outputDim);
-        if (e != cudaSuccess) return fail_cuda(e, "q6k_gemv launch");
-    }
+    const cudaError_t e = token_chunks(
+        [&](const float *xt, float *yt, int tt) {
+            return q4mm::launch_q6k_gemv_t1(ctx, xt, W, yt, inputDim, outputDim, tt);
+        },
+        x, y, inputDim, outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "q6k_gemv launch");
     return Q4MM_OK;
 }
 

@@ -16,18 +16,20 @@ struct LaunchCtx {
     bool pdl;            // launch with programmatic stream serialization
 };
 
-// Q4_K decode GEMV, one token (TMA-staged weight rows, x slab in registers).
+// Q4_K decode GEMV, 1..8 tokens on the one-token kernel (bulk-copied weight
+// rows, byte planes of x in registers; each compute warp serves one token).
 // Returns cudaErrorNotSupported when the shape is outside its geometry.
 cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
-                               int K, int N);
+                               int K, int N, int T = 1);
 
 // Q4_0 decode GEMV, one token (same kernel as the Q4_K one with the Q4_0
 // row format).  cudaErrorNotSupported when the shape is outside its geometry.
 cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
-                                int K, int N);
+                                int K, int N, int T = 1);
 
 // Q6_K decode GEMV, one token (the one-token kernel with the Q6_K row format).
-cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N);
+cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                              int T = 1);
 
 // BitNet b1.58 ternary GEMV, one token, on the same one-token kernel with the
 // byte-plane integer code-dot (K % 256 == 0, W 16-byte aligned; otherwise

@@ -427,6 +427,7 @@ struct T1Params {
     int pre_stages;    // stages issued before the wait on the previous kernel
     int x_staged;      // 1: x arrives by one bulk copy into shared memory
     float out_scale;   // y = out_scale · (row result); 1 except for the ternary scale
+    int T;             // tokens (x [T][K], y [T][N]); each compute warp serves one token
 };
 
 constexpr int kT1RoleWarps = 1;  // the copy warp
@@ -460,17 +461,21 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     const int half = wide ? 16 : lpr / 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ncw = wc * p.rg;
+    // Tokens: the planes, sums and block scales of token t follow those of
+    // token t − 1, so the split indexes them by its flat position in x [T][K].
+    const int T = kSwiGLU ? 1 : p.T;
+    const int TK = T * K;
+    const int ncw = T * wc * p.rg;
     const uint32_t slot_bytes = p.stage_rows * row_bytes;
-    uint8_t *planes = smem;                                           // nslabs × 208 bytes
-    float *sx = reinterpret_cast<float *>(planes + nslabs * kPlaneSlabBytes);  // K/32 sub-block sums
-    float *sx16 = sx + K / 32;                                        // K/16 half-sub-block sums
-    float *sb = sx16 + K / 16;                                        // K/256 block scales
-    float *xst = sb + ((nb + 3) & ~3);                                // x (when staged)
-    uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? K : 0));
+    uint8_t *planes = smem;                                           // T·nslabs × 208 bytes
+    float *sx = reinterpret_cast<float *>(planes + T * nslabs * kPlaneSlabBytes);  // T·K/32 sub-block sums
+    float *sx16 = sx + TK / 32;                                       // T·K/16 half-sub-block sums
+    float *sb = sx16 + TK / 16;                                       // T·K/256 block scales
+    float *xst = sb + ((T * nb + 3) & ~3);                            // x (when staged)
+    uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? TK : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
-    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [virtual rows][wc]
+    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [T][virtual rows][wc]
 
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
@@ -487,8 +492,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nslots; ++s) {
             mbar_init(&full_bar[s], 1);
-            // Every pass of a stage is worked by the wc warps of a row.
-            mbar_init(&empty_bar[s], passes_per_stage * wc);
+            // Every pass of a stage is worked by the wc warps of a row, per token.
+            mbar_init(&empty_bar[s], passes_per_stage * wc * T);
         }
         mbar_init(&x_bar, 1);
         abort_flag = 0;
@@ -538,8 +543,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             // x may be written by the previous kernel on the stream.
             pdl_wait();
             if (p.x_staged) {
-                mbar_arrive_expect_tx(&x_bar, (uint32_t)K * sizeof(float));
-                bulk_g2s(xst, p.x, (uint32_t)K * sizeof(float), &x_bar);
+                mbar_arrive_expect_tx(&x_bar, (uint32_t)TK * sizeof(float));
+                bulk_g2s(xst, p.x, (uint32_t)TK * sizeof(float), &x_bar);
             }
             for (; st < first; ++st) issue(st, st);
             for (; st < nstages; ++st) {
@@ -557,7 +562,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
         __syncwarp();
     } else {
         const int cw = warp - kT1RoleWarps;
-        const int wcol = cw % wc, rgi = cw / wc;
+        const int tok = cw / (wc * p.rg), cwt = cw % (wc * p.rg);
+        const int wcol = cwt % wc, rgi = cwt / wc;
         const int ro = wide ? 0 : lane / lpr;
         const int s = wide ? wcol * 32 + lane : lane % lpr;
         const bool active = s < L;
@@ -578,7 +584,7 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
         // values): the 32 threads of a block form one warp and share its
         // maximum; the four threads of a sub-block are neighbouring lanes.
         {
-            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, ne = K / 8;
+            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, ne = TK / 8;
             for (int e0 = 0; e0 < ne; e0 += nth) {
                 const int e = e0 + ct;
                 const bool on = e < ne && !abort_flag;
@@ -652,7 +658,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                 for (int i = 0; i < 4; ++i) {
                     int us, up;
                     Fmt::unit_of(j, i, us, up);
-                    const uint4 *src = reinterpret_cast<const uint4 *>(planes + (4 * b + us) * kPlaneSlabBytes);
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(planes + (tok * nslabs + 4 * b + us) * kPlaneSlabBytes);
                     const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
                     pl[pp][4 * i] = (int)t.x;
                     pl[pp][4 * i + 1] = (int)t.y;
@@ -660,12 +667,12 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                     pl[pp][4 * i + 3] = (int)t.w;
                 }
             }
-            s_blk = active ? sb[b] : 0.f;
-            sum_lo = active ? sx[8 * b + 2 * j] : 0.f;
-            sum_hi = active ? sx[8 * b + 2 * j + 1] : 0.f;
+            s_blk = active ? sb[tok * nb + b] : 0.f;
+            sum_lo = active ? sx[tok * K / 32 + 8 * b + 2 * j] : 0.f;
+            sum_hi = active ? sx[tok * K / 32 + 8 * b + 2 * j + 1] : 0.f;
         }
         Fmt::prep_planes(pl);
-        const typename Fmt::Lane lfmt = Fmt::lane(j, sx16 + 16 * b);
+        const typename Fmt::Lane lfmt = Fmt::lane(j, sx16 + tok * K / 16 + 16 * b);
         const float unit = s_blk * (1.0f / 32768.0f);
 
         const int npasses = (nv + pass_rows - 1) / pass_rows;
@@ -706,11 +713,11 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             const int r = up ? rb : ra;
             const int rl = st * p.stage_rows + r;
             if (wide) {
-                if ((lane & (half - 1)) == 0 && r < rows) part[rl * wc + wcol] = v;
+                if ((lane & (half - 1)) == 0 && r < rows) part[(tok * nv + rl) * wc + wcol] = v;
             } else if (kSwiGLU) {
                 if (s == (up ? half : 0) && r < rows) part[rl] = v;
             } else {
-                if (s == (up ? half : 0) && r < rows) p.y[row0 + rl] = p.out_scale * v;
+                if (s == (up ? half : 0) && r < rows) p.y[(size_t)tok * p.N + row0 + rl] = p.out_scale * v;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -727,15 +734,17 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
 
         if (to_smem) {
             named_bar_sync(1, ncw * 32);
-            for (int i = threadIdx.x - 32 * kT1RoleWarps; i < nrows; i += ncw * 32) {
+            for (int it = threadIdx.x - 32 * kT1RoleWarps; it < T * nrows; it += ncw * 32) {
+                const int t = it / nrows, i = it % nrows;
+                const float *pt = part + (size_t)t * nv * wc;
                 float acc = 0.f;
-                for (int w = 0; w < wc; ++w) acc += part[i * wc + w];
+                for (int w = 0; w < wc; ++w) acc += pt[i * wc + w];
                 if (kSwiGLU) {
                     float up = 0.f;
-                    for (int w = 0; w < wc; ++w) up += part[(nrows + i) * wc + w];
+                    for (int w = 0; w < wc; ++w) up += pt[(nrows + i) * wc + w];
                     acc = acc / (1.0f + expf(-acc)) * up;  // silu(g)·u
                 }
-                p.y[row0 + i] = p.out_scale * acc;
+                p.y[(size_t)t * p.N + row0 + i] = p.out_scale * acc;
             }
         }
     }
@@ -969,8 +978,9 @@ int next_pow2(int v) {
 
 template <class Fmt, bool kSwiGLU = false>
 cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
-                           const uint8_t *W2 = nullptr, float out_scale = 1.0f) {
+                           const uint8_t *W2 = nullptr, float out_scale = 1.0f, int T = 1) {
     T1Params p;
+    p.T = T;
     p.x = x;
     p.W = W;
     p.W2 = W2;
@@ -988,8 +998,10 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     // generic kernel.
     if (wc > kT1MaxCw) return cudaErrorNotSupported;
     const T1Tuning &tun = t1_tuning();
-    p.rg = max(1, tun.warps / wc);
-    const int ncw = wc * p.rg;
+    // Each token gets warps / T compute warps: whole rows (wc warps each).
+    if (tun.warps / T < wc) return cudaErrorNotSupported;
+    p.rg = (tun.warps / T) / wc;
+    const int ncw = T * wc * p.rg;
     // Stage: whole passes, at least stage_bytes of weights (bulk copies of
     // 16 KB and more run at full HBM bandwidth).  A row size off the 16-byte
     // grid (Q6_K) keeps CTA and stage boundaries on multiples of rq rows,
@@ -1011,17 +1023,17 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
     const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
 
-    p.x_staged = (size_t)K * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
+    const size_t TK = (size_t)T * K;
+    p.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
     // Large rows at an 8-row stage quantum can leave no room for x: then
     // the compute threads load x themselves.
-    if (p.x_staged && (size_t)K * sizeof(float) + 2 * slot_bytes + (size_t)(K / 64) * kPlaneSlabBytes >
+    if (p.x_staged && TK * sizeof(float) + 2 * slot_bytes + (TK / 64) * kPlaneSlabBytes >
                           (size_t)c.max_smem_optin - 8192)
         p.x_staged = 0;
-    const size_t xs_bytes = (size_t)(K / 64) * kPlaneSlabBytes + (size_t)(K / 32 + K / 16) * sizeof(float) +
-                            (size_t)((p.nb * 4 + 15) & ~15) +
-                            (p.x_staged ? (size_t)K * sizeof(float) : 0);
+    const size_t xs_bytes = (TK / 64) * kPlaneSlabBytes + (TK / 32 + TK / 16) * sizeof(float) +
+                            (size_t)((T * p.nb * 4 + 15) & ~15) + (p.x_staged ? TK * sizeof(float) : 0);
     const int vrows_per_cta = (kSwiGLU ? 2 : 1) * p.rows_per_cta;
-    const size_t part_bytes = (wide || kSwiGLU) ? (size_t)vrows_per_cta * wc * sizeof(float) : 0;
+    const size_t part_bytes = (wide || kSwiGLU) ? (size_t)T * vrows_per_cta * wc * sizeof(float) : 0;
     const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
     const size_t budget = tun.ring_bytes;
     int nslots = (int)((budget > fixed ? budget - fixed : 0) / slot_bytes);
@@ -1072,16 +1084,19 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     }
 }
 
-cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
-    return launch_gemv_t1<FmtQ4K>(c, x, W, y, K, N);
+cudaError_t launch_q4k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                               int T) {
+    return launch_gemv_t1<FmtQ4K>(c, x, W, y, K, N, nullptr, 1.0f, T);
 }
 
-cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
-    return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N);
+cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                                int T) {
+    return launch_gemv_t1<FmtQ40>(c, x, W, y, K, N, nullptr, 1.0f, T);
 }
 
-cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N) {
-    return launch_gemv_t1<FmtQ6K>(c, x, W, y, K, N);
+cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
+                              int T) {
+    return launch_gemv_t1<FmtQ6K>(c, x, W, y, K, N, nullptr, 1.0f, T);
 }
 
 cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,
