@@ -31,11 +31,11 @@ cudaError_t launch_q4_0_gemv_t1(const LaunchCtx &c, const float *x, const uint8_
 cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
                               int T = 1);
 
-// BitNet b1.58 ternary GEMV, one token, on the same one-token kernel with the
-// byte-plane integer code-dot (K % 256 == 0, W 16-byte aligned; otherwise
+// BitNet b1.58 ternary GEMV, 1..8 tokens, on the same one-token kernel with
+// the byte-plane integer code-dot (K % 256 == 0, W 16-byte aligned; otherwise
 // cudaErrorNotSupported).
 cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,
-                                   int K, int N);
+                                   int K, int N, int T = 1);
 
 // Llama FFN input side, one token: h = silu(x·Wgᵀ)·(x·Wuᵀ), both Q4_K, in one
 // launch of the one-token kernel (x split once for both weights).

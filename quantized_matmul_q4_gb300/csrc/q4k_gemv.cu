@@ -1100,8 +1100,8 @@ cudaError_t launch_q6k_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t
 }
 
 cudaError_t launch_ternary_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float scale, float *y,
-                                   int K, int N) {
-    return launch_gemv_t1<FmtTern>(c, x, W, y, K, N, nullptr, scale);
+                                   int K, int N, int T) {
+    return launch_gemv_t1<FmtTern>(c, x, W, y, K, N, nullptr, scale, T);
 }
 
 cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,

@@ -575,8 +575,8 @@ cudaError_t launch_t(const LaunchCtx &c, const float *x, const uint8_t *W, float
 
 }  // namespace
 
-// Q4MM_TERNARY_T1=float selects the float one-token kernel for every K
-// (for comparisons); read once.
+// Q4MM_TERNARY_T1=float selects the float kernels (one-token and register
+// tiles) for every K, for comparisons; read once.
 bool ternary_float_t1() {
     static const bool on = [] {
         const char *v = getenv("Q4MM_TERNARY_T1");
@@ -592,9 +592,21 @@ cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_
     const bool bulk = (K % 64 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
     if (bulk) {
         cudaError_t e = cudaErrorNotSupported;
-        // One token with K % 256 == 0: the shared one-token kernel (byte-plane
-        // integer code-dot); otherwise the float one-token kernel below.
-        if (T == 1 && K % 256 == 0 && !ternary_float_t1()) e = launch_ternary_gemv_t1(c, x, W, scale, y, K, N);
+        // K % 256 == 0 and up to 3 tokens: the shared one-token kernel
+        // (byte-plane integer code-dot, one token per compute warp).  From 4
+        // tokens on the FP32 register-tile kernel is as fast or faster
+        // (2560 -> 6912, GB300: 1 token 5.1 vs 5.6 us, 2: 7.4 vs 8.9,
+        // 3: 10.0 vs 11.8, 4: 11.7 vs 11.8, 8: 19.1 vs 13.3).  Otherwise the
+        // float one-token kernel (one token) or the register-tile kernel.
+        if (K % 256 == 0 && T <= 3 && !ternary_float_t1()) {
+            e = launch_ternary_gemv_t1(c, x, W, scale, y, K, N, T);
+            if (e == cudaErrorNotSupported && T > 1) {
+                // Too wide for T tokens at once: one token at a time if that fits.
+                e = cudaSuccess;
+                for (int t = 0; t < T && e == cudaSuccess; ++t)
+                    e = launch_ternary_gemv_t1(c, x + (size_t)t * K, W, scale, y + (size_t)t * N, K, N, 1);
+            }
+        }
         if (T == 1 && e == cudaErrorNotSupported) e = launch_ternary_t1(c, x, W, scale, y, K, N);
         if (e == cudaErrorNotSupported) e = launch_ternary_tile(c, x, W, scale, y, K, N, T);
         if (e != cudaErrorNotSupported) return e;

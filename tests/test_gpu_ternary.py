@@ -47,9 +47,10 @@ def test_workload_normal(T):
 ODD = [(4, 1, 1), (8, 3, 2), (12, 5, 1), (100, 33, 3), (2564, 7, 1), (4100, 9, 9), (64, 1000, 1),
        (8192, 65, 17), (6000, 13, 8), (16, 2, 4)]
 # Shapes for the streamed kernels (K % 64 == 0, 16-byte aligned weights):
-# one token with 1..15 word columns and ragged row counts, the tile kernel
-# with 2..8-token tiles, ragged token groups, several K chunks, and K beyond
-# the one-token kernel's 15 columns.
+# K % 256 == 0 with up to 3 tokens runs on the shared byte-plane kernel,
+# everything else on the float one-token kernel (one token) and the
+# register-tile kernel (2..8-token tiles, several K chunks); K = 65536 is
+# beyond the shared kernel's geometry.
 STREAMED = [(64, 1, 1), (128, 48, 2), (2560, 100, 3), (6400, 37, 5), (7680, 20, 1), (7744, 3, 1),
             (2560, 6913, 1), (1024, 4097, 16), (256, 1, 8), (65536, 2, 1), (65536, 3, 9),
             (4096, 300, 12), (512, 152 * 8 + 5, 1), (2560, 49, 7)]
@@ -99,3 +100,10 @@ def test_run_to_run_bit_identity(T):
     a = ternary(x, W, scale, K, N)
     b = ternary(x, W, scale, K, N)
     assert a.tobytes() == b.tobytes()
+
+
+def test_bench_shape_sixteen_tokens_normal():
+    # The 16-token bench workload's shape with N(0,1) activations.
+    x, W, scale, K, N, T = synth.ternary_case("ternary_gemv_2560x6912_t16")
+    dot, _ = oracle.ternary_gemv(x, W, scale, K, N)
+    assert_rows_close(ternary(x, W, scale, K, N), dot * np.float64(scale), REL, "2560x6912 T16")
