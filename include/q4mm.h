@@ -102,11 +102,10 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
  * max_o |y_exact| on random data).
  * Memory: each call takes stream-ordered scratch (cudaMallocAsync on
  * `stream`, released by cudaFreeAsync on `stream` after the call's last
- * kernel): the bf16 copy of x, 2·tokens·inputDim bytes rounded up to 256,
- * plus (S − 1)·min(tokens, 128)·ceil(outputDim/256)·256·4 bytes of partial
- * sums, where S = max(3, ceil(inputDim/16384)) CTAs of a cluster split the
- * input dimension of each 256-row tile.  The weights are read once per 128
- * tokens.
+ * kernel): the bf16 copy of x, 2·tokens·inputDim bytes rounded up to 256.
+ * The S = max(3, ceil(inputDim/16384)) CTAs of a cluster that split the
+ * input dimension of each 256-row tile add their partial sums in shared
+ * memory.  The weights are read once per 128 tokens.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA} (CUDA also when the
  * scratch allocation fails).  A bounded wait that runs out sets the device
  * status word (see q4mm_device_status).
@@ -220,8 +219,8 @@ int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *
  * (16 MiB) of device memory inside the library, which every GPU that loads
  * the library holds until the process exits.  A call whose scratch (the size
  * formula under q4k_matmul_tc) is larger returns Q4MM_ERR_DIM before
- * launching anything; for example 128 tokens of a 4096 → 11008 layer need
- * 12.3 MB, 64 tokens of it 6.1 MB.
+ * launching anything; for example 64 tokens of a 4096 → 11008 layer need
+ * 0.5 MiB, and the array holds up to 2048 tokens at inputDim 4096.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents.  No part of it has to start at zero: a call writes every

@@ -1,6 +1,6 @@
 // Thread-block cluster helpers (sm_103a): rank, size, a full cluster
-// barrier with release/acquire ordering, and stores into another CTA's
-// shared memory (distributed shared memory).
+// barrier with release/acquire ordering, and loads from and stores into
+// another CTA's shared memory (distributed shared memory).
 #pragma once
 
 #include <cstdint>
@@ -37,6 +37,15 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                  "f"(v.w)
                  : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 }  // namespace q4mm

@@ -22,10 +22,11 @@
 // that the 43 row tiles of an 11008-row weight spread over 129 SMs.  Each
 // CTA accumulates its K range in one tensor-memory accumulator (at most
 // 16384 values of K, within which the tensor core's fp32 accumulation stays
-// far inside the stated tolerance); ranks 1..S−1 store their partial sums in
-// slices of the scratch buffer, and after a cluster barrier rank 0 adds them
-// in rank order to its own, read from tensor memory, and writes y, so the
-// result does not depend on scheduling.
+// far inside the stated tolerance).  Every rank copies its accumulator into
+// its own shared memory; after a cluster barrier each rank takes one S-th of
+// the tile's outputs, adds the S ranks' values in rank order through
+// distributed shared memory and writes them to y, so the result does not
+// depend on scheduling and no partial sum goes through global memory.
 //
 // Roles in a CTA:
 //  * warp 16 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
@@ -43,8 +44,8 @@
 //  * warp 17 allocates the accumulator in tensor memory; its first thread
 //    issues four 128×256×16 MMAs per chunk and commits them to the chunk's
 //    activation and weight slots.
-//  * warps 0–15 then read the accumulator (tcgen05.ld) and store the partial
-//    sums; rank 0 adds the cluster's partials and writes y.
+//  * warps 0–15 then read the accumulator (tcgen05.ld) into shared memory,
+//    and every thread takes part in the cluster-wide reduction.
 // All mbarrier waits are bounded; a time-out sets the device status word and
 // every thread still reaches the two cluster barriers.
 #include <cuda.h>
@@ -256,7 +257,7 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                     float *__restrict__ y, float *__restrict__ part, int K, int N, int T, int *status) {
+                     float *__restrict__ y, int K, int N, int T, int *status) {
     using L = TcLayout;
     extern __shared__ uint8_t tc_smem_raw[];
     __shared__ volatile int abort_flag;
@@ -459,16 +460,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // Epilogue.  Warps w, w+4, w+8, w+12 share TMEM lane quarter w % 4
     // (tokens 32·quarter..) and read 64 of the 256 columns each into a shared
-    // tile [T][257] (the padding keeps the lanes, which hold consecutive
-    // tokens, on distinct banks); the rings are idle by now.  Ranks 1..S−1
-    // copy their tile row by row into slice rank − 1 of the scratch; after a
-    // cluster barrier rank 0 adds the slices to its own tile in rank order
-    // and writes y, all with consecutive threads on consecutive columns.
-    constexpr int kPitch = kTcRows + 1;
+    // tile [T][260]; the rings are idle by now.  After a cluster barrier every
+    // rank takes one S-th of the tile's outputs, adds the S ranks' values in
+    // rank order, read straight from their shared memory (distributed shared
+    // memory, 16 bytes per load), and writes them to y with consecutive
+    // threads on consecutive columns.  A second barrier keeps each tile in
+    // place until every rank has read it.
+    // Row pitch of the shared tile: 260 floats keeps every row on a 16-byte
+    // boundary, and eight lanes of consecutive tokens storing 16 bytes at
+    // the same column land on eight distinct bank groups.
+    constexpr int kPitch = kTcRows + 4;
     float *ysm = reinterpret_cast<float *>(smem);
     const int quarter = warp & 3, cq = warp >> 2;
     const int tok = 32 * quarter + lane;
-    const int tile = blockIdx.x / S, ntiles = gridDim.x / S;
     if (warp < kTcDqWarps && 32 * quarter < T) {  // warp-uniform
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) {
@@ -480,58 +484,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
             }
             if (tok < T) {
+                float4 *dst = reinterpret_cast<float4 *>(ysm + tok * kPitch + 64 * cq + 16 * g);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) ysm[tok * kPitch + 64 * cq + 16 * g + i] = v[i];
+                for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
-    const int n_el = T * kTcRows;
-    auto slice = [&](int s) -> float * {  // [T][256] partial sums of rank s for this tile
-        return part + ((size_t)(s - 1) * ntiles + tile) * (size_t)n_el;
-    };
-    if (rank != 0) {
-        float *dst = slice(rank);
-        for (int i = threadIdx.x; i < n_el; i += kTcThreads) dst[i] = ysm[(i / kTcRows) * kPitch + i % kTcRows];
-    }
-    // Partials of every rank are visible to rank 0 after the cluster barrier
-    // (release / acquire at cluster scope).
     cluster_sync_all();
-
-    if (rank == 0) {
+    {
+        // Outputs in groups of four columns; rank r takes groups
+        // [r·G/S, (r+1)·G/S) of the tile's G = T·64.
+        constexpr int kGroupsPerRow = kTcRows / 4;
+        const int n_g = T * kGroupsPerRow;
+        const int g0 = rank * n_g / S, g1 = (rank + 1) * n_g / S;
+        const int ncols = min(kTcRows, N - row0);
+        const bool vec_y = (reinterpret_cast<uintptr_t>(y) & 15) == 0 && (N & 3) == 0;
+        const uint32_t local = smem_addr(ysm);
+        uint32_t tile_of[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) tile_of[s] = map_to_rank(local, (uint32_t)min(s, S - 1));
         // The output may be read by the previous kernel on the stream.
         pdl_wait();
-        const int ncols = min(kTcRows, N - row0);
-        // Four elements per thread step with every partial load issued before
-        // the adds (S <= 4: at most three other ranks), so the L2 latencies
-        // overlap.  L2 reads: an earlier tile may have left these lines in L1.
-        const float *p1 = slice(1), *p2 = S > 2 ? slice(2) : p1, *p3 = S > 3 ? slice(3) : p1;
+        // kU groups per thread step, every remote load issued before the
+        // adds so that their latencies overlap.
         constexpr int kU = 4;
-        for (int i0 = threadIdx.x; i0 < n_el; i0 += kU * kTcThreads) {
-            float a1[kU], a2[kU], a3[kU];
+        for (int i0 = g0 + (int)threadIdx.x; i0 < g1; i0 += kU * kTcThreads) {
+            float4 v[4][kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = min(i0 + u * kTcThreads, n_el - 1);
-                a1[u] = __ldcg(p1 + i);
-                a2[u] = S > 2 ? __ldcg(p2 + i) : 0.f;
-                a3[u] = S > 3 ? __ldcg(p3 + i) : 0.f;
+            for (int s = 0; s < 4; ++s) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = min(i0 + u * kTcThreads, g1 - 1);
+                    const uint32_t off = 4u * (uint32_t)((i / kGroupsPerRow) * kPitch + 4 * (i % kGroupsPerRow));
+                    v[s][u] = s < S ? ld_cluster_v4(tile_of[s] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = i0 + u * kTcThreads;
-                if (i < n_el) {
-                    const int t = i / kTcRows, col = i % kTcRows;
-                    float acc = ysm[t * kPitch + col] + a1[u];
-                    if (S > 2) acc += a2[u];
-                    if (S > 3) acc += a3[u];
-                    if (col < ncols) y[(size_t)t * N + row0 + col] = acc;
+                if (i < g1) {
+                    const int t = i / kGroupsPerRow, col = 4 * (i % kGroupsPerRow);
+                    float4 acc = v[0][u];
+#pragma unroll
+                    for (int s = 1; s < 4; ++s) {
+                        if (s < S) {
+                            acc.x += v[s][u].x;
+                            acc.y += v[s][u].y;
+                            acc.z += v[s][u].z;
+                            acc.w += v[s][u].w;
+                        }
+                    }
+                    float *dst = y + (size_t)t * N + row0 + col;
+                    if (vec_y && col + 3 < ncols) {
+                        *reinterpret_cast<float4 *>(dst) = acc;
+                    } else {
+                        if (col < ncols) dst[0] = acc.x;
+                        if (col + 1 < ncols) dst[1] = acc.y;
+                        if (col + 2 < ncols) dst[2] = acc.z;
+                        if (col + 3 < ncols) dst[3] = acc.w;
+                    }
                 }
             }
         }
     }
-    tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     if (warp == kTcWarpMma) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
@@ -553,8 +570,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, float *part,
-                        int K, int N, int T, int S) {
+cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, int K, int N,
+                        int T, int S) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
     alignas(64) CUtensorMap tm_w, tm_x;
@@ -605,7 +622,7 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, q4k_mm_tc_kernel, tm_w, tm_x, y, part, K, N, T, c.status);
+    return cudaLaunchKernelEx(&cfg, q4k_mm_tc_kernel, tm_w, tm_x, y, K, N, T, c.status);
 }
 
 }  // namespace
@@ -617,19 +634,15 @@ cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *
     const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
     if (S > 4) return cudaErrorNotSupported;  // the reduction adds at most three other ranks
     // Stream-ordered scratch, freed on the same stream after the last token
-    // tile: x rounded to bf16 once (2·T·K bytes), then the partial sums of
-    // ranks 1..S−1 for one tile of tokens (whole 256-column row tiles).  The weights are re-read once
-    // per tile of 128 tokens.
+    // tile: x rounded to bf16 once (2·T·K bytes).  The weights are re-read
+    // once per tile of 128 tokens.
     const size_t n = (size_t)T * K;
     const int tmax = min(T, kTcMaxTokens);
     const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
-    const size_t ncols = (size_t)(N + kTcRows - 1) / kTcRows * kTcRows;
-    const size_t part_bytes = (size_t)(S - 1) * tmax * ncols * sizeof(float);
     void *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(&scratch, xb_bytes + part_bytes, c.stream);
+    cudaError_t e = cudaMallocAsync(&scratch, xb_bytes, c.stream);
     if (e != cudaSuccess) return e;
     __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(scratch);
-    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + xb_bytes);
     {
         const size_t n4 = n / 4;
         const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
@@ -638,7 +651,7 @@ cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *
     }
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
         const int tt = min(tmax, T - t0);
-        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, part, K, N, tt, S);
+        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, K, N, tt, S);
     }
     const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
     return e != cudaSuccess ? e : ef;
@@ -687,12 +700,8 @@ cudaError_t fixed_scratch(uint8_t **out) {
 }  // namespace
 
 size_t q4k_mm_tc_scratch_bytes(int K, int N, int T) {
-    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
-    const size_t n = (size_t)T * K;
-    const int tmax = min(T, kTcMaxTokens);
-    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
-    const size_t ncols = (size_t)(N + kTcRows - 1) / kTcRows * kTcRows;
-    return xb_bytes + (size_t)(S - 1) * tmax * ncols * sizeof(float);
+    (void)N;
+    return ((size_t)T * K * sizeof(__nv_bfloat16) + 255) / 256 * 256;
 }
 
 cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
@@ -703,15 +712,11 @@ cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, c
     uint8_t *scratch = nullptr;
     cudaError_t e = fixed_scratch(&scratch);
     if (e != cudaSuccess) return e;
-    // Layout as in launch_q4k_mm_tc: bf16 x, then the partial sums of ranks
-    // 1..S−1 for one tile of tokens.  Nothing needs clearing: the pre-pass
-    // writes all of x's copy and every partial slice is written by its rank
-    // before rank 0 reads it.
+    // As in launch_q4k_mm_tc, the scratch holds x rounded to bf16.  Nothing
+    // needs clearing: the pre-pass writes all of it.
     const size_t n = (size_t)T * K;
     const int tmax = min(T, kTcMaxTokens);
-    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
     __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(scratch);
-    float *part = reinterpret_cast<float *>(scratch + xb_bytes);
     {
         const size_t n4 = n / 4;
         const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
@@ -720,7 +725,7 @@ cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, c
     }
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
         const int tt = min(tmax, T - t0);
-        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, part, K, N, tt, S);
+        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, K, N, tt, S);
     }
     return e;
 }

@@ -107,9 +107,9 @@ def test_rejects_overlap(q4mm):
 
 
 def test_noalloc_refuses_oversize_before_any_cuda_call(q4mm):
-    # The fixed scratch array holds 16 MiB; 512 tokens x 16384 need 20 MiB.
+    # The fixed scratch array holds 16 MiB; 1040 tokens x 8192 need 16.25 MiB.
     with pytest.raises(q4mm.Q4mmError) as e:
-        q4mm.q4k_matmul_tc_noalloc_ptr(X, W, Y, 16384, 4096, 512, 0)
+        q4mm.q4k_matmul_tc_noalloc_ptr(X, W, Y, 8192, 256, 1040, 0)
     assert e.value.code == DIM
     assert "scratch" in q4mm.last_error()
     # Validation shared with q4k_matmul_tc comes first.

@@ -62,10 +62,9 @@ def test_two_calls_in_a_row_match_the_allocating_entry_point():
 def test_oversize_call_is_refused_before_launch():
     import torch
     import quantized_matmul_q4_gb300 as q
-    # 512 tokens of a 16384 -> 4096 layer: 16 MiB of bf16 activations plus
-    # 2 x 128 x 4096 x 4 B = 4 MiB of partial sums.
-    T, K, N = 512, 16384, 4096
-    need = (T * K * 2 + 255) // 256 * 256 + 2 * 128 * N * 4
+    # 1040 tokens of an 8192 -> 256 layer: 16.25 MiB of bf16 activations.
+    T, K, N = 1040, 8192, 256
+    need = (T * K * 2 + 255) // 256 * 256
     assert need > FIXED_BYTES
     x = torch.zeros(T * K, dtype=torch.float32, device="cuda")
     w = torch.zeros(N * (K // 256) * 144, dtype=torch.uint8, device="cuda")
