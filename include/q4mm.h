@@ -17,8 +17,8 @@
  *
  * Ownership and memory: x, W and y are DEVICE pointers owned by the caller
  * and must not overlap.  q4k_matmul and ternary_gemv allocate nothing;
- * q4k_matmul_tc takes stream-ordered scratch for the length of each call (its
- * entry below gives the size).
+ * q4k_matmul_tc takes stream-ordered scratch for the length of each call
+ * above 128 tokens (its entry below gives the size).
  *
  * Streams: every compute call is asynchronous on `stream` (NULL means the
  * legacy default stream).  Validation is synchronous: an invalid call returns
@@ -100,12 +100,14 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
  * y_bf16 is the exact product of the bf16-rounded operands; the deviation
  * from the exact product is that of bf16 operand rounding (about 5e-3 of
  * max_o |y_exact| on random data).
- * Memory: each call takes stream-ordered scratch (cudaMallocAsync on
- * `stream`, released by cudaFreeAsync on `stream` after the call's last
- * kernel): the bf16 copy of x, 2·tokens·inputDim bytes rounded up to 256.
- * The S = max(3, ceil(inputDim/16384)) CTAs of a cluster that split the
- * input dimension of each 256-row tile add their partial sums in shared
- * memory.  The weights are read once per 128 tokens.
+ * Memory: up to 128 tokens a call allocates nothing (the kernel rounds x to
+ * bf16 as it loads it).  Above 128 tokens each call takes stream-ordered
+ * scratch (cudaMallocAsync on `stream`, released by cudaFreeAsync on
+ * `stream` after the call's last kernel): the bf16 copy of x,
+ * 2·tokens·inputDim bytes rounded up to 256, and the weights are read once
+ * per 128 tokens.  The S = max(3, ceil(inputDim/16384)) CTAs of a cluster
+ * that split the input dimension of each 256-row tile add their partial
+ * sums in shared memory.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA} (CUDA also when the
  * scratch allocation fails).  A bounded wait that runs out sets the device
  * status word (see q4mm_device_status).
@@ -219,8 +221,9 @@ int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *
  * (16 MiB) of device memory inside the library, which every GPU that loads
  * the library holds until the process exits.  A call whose scratch (the size
  * formula under q4k_matmul_tc) is larger returns Q4MM_ERR_DIM before
- * launching anything; for example 64 tokens of a 4096 → 11008 layer need
- * 0.5 MiB, and the array holds up to 2048 tokens at inputDim 4096.
+ * launching anything; calls of up to 128 tokens need none, 256 tokens of a
+ * 4096 → 11008 layer need 2 MiB, and the array holds up to 2048 tokens at
+ * inputDim 4096.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents.  No part of it has to start at zero: a call writes every

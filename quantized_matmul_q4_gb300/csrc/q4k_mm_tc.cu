@@ -12,10 +12,13 @@
 // any M and N (measured on GB300), so each instruction is made as large as
 // the tile allows: 128 × 256 × 16.
 //
-// Before the main kernel, a small kernel rounds x to bf16 once into a
-// stream-ordered scratch buffer (2·T·K bytes, allocated and freed on the
-// call's stream); the main kernel loads activation tiles by TMA with the
-// hardware 128-byte swizzle, already in the layout the MMA reads.
+// Up to 128 tokens (one tile) the dequant warps also read fp32 x, round it
+// to bf16 and write each chunk's activation tile in the swizzled layout the
+// MMA reads, one chunk ahead of use; nothing is allocated.  Above 128 tokens
+// a small kernel first rounds x to bf16 once into a stream-ordered scratch
+// buffer (2·T·K bytes, allocated and freed on the call's stream), and each
+// 128-token tile loads its activation tiles from it by TMA with the hardware
+// 128-byte swizzle.
 //
 // Grid: clusters of S CTAs (3, or 4 above K = 49152) per 256-row tile, CTA
 // rank r of a cluster taking 64-value chunks [r·nc/S, (r+1)·nc/S) of K, so
@@ -31,16 +34,18 @@
 // Roles in a CTA:
 //  * warp 16 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
 //    (256 rows × 144 bytes) per 256 values of K, before the wait on the
-//    previous kernel, and a bf16 activation tile (128 tokens × 64 values) per
-//    chunk of 64 values, after it, each as soon as its ring slot is free.
+//    previous kernel, and (tiles of the bf16 copy) a bf16 activation tile
+//    (128 tokens × 64 values) per chunk of 64 values, after it, each as soon
+//    as its ring slot is free.
 //  * warps 0–15 dequantize: thread (r, h), r = t mod 256 and h = t / 256,
 //    turns qs bytes 16h..16h+15 of row r's slab into 16 low-nibble values of
 //    sub-block 2j and 16 high-nibble values of 2j+1.  Each nibble becomes a float with one logic op (2^23 + q·2^p), one
 //    paired FMA with the scale at 2^-p and −scale·2^(23−p) gives scale·q
 //    exactly, one paired add removes the min term (the single rounding of the
 //    fp32 dequantization), and one conversion packs two bf16.  Results go in
-//    the 128-byte-swizzled K-major layout; the writes are fenced to the async
-//    proxy before the chunk's barrier arrive.
+//    the 128-byte-swizzled K-major layout; with fused activations the same
+//    threads also write the chunk's activation tile.  The writes are fenced
+//    to the async proxy before the chunk's barrier arrive.
 //  * warp 17 allocates the accumulator in tensor memory; its first thread
 //    issues four 128×256×16 MMAs per chunk and commits them to the chunk's
 //    activation and weight slots.
@@ -77,6 +82,7 @@ constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads (two per w
 constexpr int kTcWStages = 2;                      // Q4_K block-column tiles in flight
 constexpr int kTcAStages = 3;                      // bf16 activation tiles in flight
 constexpr int kTcBStages = 3;                      // bf16 weight operand tiles in flight
+static_assert(kTcAStages == kTcBStages, "fused activation tiles share the weight ring's slots");
 constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 36864
 constexpr uint32_t kTcATileBytes = kTcTok * 128;         // 16384
 constexpr uint32_t kTcBTileBytes = kTcRows * 128;        // 32768
@@ -255,9 +261,14 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
     }
 }
 
+// kXTma: activation tiles come by TMA from a bf16 copy of x (tm_x).
+// Otherwise the dequant warps read fp32 x themselves, round it and write the
+// activation tile of each chunk next to its weight tile, and one barrier
+// (full_b) publishes both.
+template <bool kXTma>
 __global__ void __launch_bounds__(kTcThreads, 1)
     q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                     float *__restrict__ y, int K, int N, int T, int *status) {
+                     const float *__restrict__ x, float *__restrict__ y, int K, int N, int T, int *status) {
     using L = TcLayout;
     extern __shared__ uint8_t tc_smem_raw[];
     __shared__ volatile int abort_flag;
@@ -300,6 +311,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
+    if constexpr (!kXTma) {
+        // Token rows T..127 of every activation stage stay zero.
+        const int pad16 = (kTcTok - T) * 128 / 16;
+        for (int s = 0; s < kTcAStages; ++s) {
+            uint4 *p = reinterpret_cast<uint4 *>(smem + L::off_a + s * kTcATileBytes + T * 128);
+            for (int i = threadIdx.x; i < pad16; i += kTcThreads) p[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+    }
     if (warp == kTcWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
@@ -323,11 +343,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
                             &full_w[nw]);
             }
-            // The bf16 activations come from the previous kernel on the stream.
-            pdl_wait();
-            for (; nx < min(nchunks, kTcAStages); ++nx) {
-                mbar_arrive_expect_tx(&full_a[nx], kTcATileBytes);
-                tma_load_2d(sbase + L::off_a + nx * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0, &full_a[nx]);
+            if constexpr (kXTma) {
+                // The bf16 activations come from the previous kernel on the stream.
+                pdl_wait();
+                for (; nx < min(nchunks, kTcAStages); ++nx) {
+                    mbar_arrive_expect_tx(&full_a[nx], kTcATileBytes);
+                    tma_load_2d(sbase + L::off_a + nx * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
+                                &full_a[nx]);
+                }
+            } else {
+                nx = nchunks;  // the dequant warps write the activation tiles
             }
             long long t_last = clock64();
             while ((nw < nblocks || nx < nchunks) && !abort_flag) {
@@ -363,8 +388,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // about to be reused: the last use of each ring slot must land.
             for (int b = max(0, nw - kTcWStages); b < nw; ++b)
                 (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
-            for (int c = max(0, nx - kTcAStages); c < nx; ++c)
-                (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, kWaitLimitCycles);
+            if constexpr (kXTma) {
+                for (int c = max(0, nx - kTcAStages); c < nx; ++c)
+                    (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, kWaitLimitCycles);
+            }
         }
         __syncwarp();
     } else if (warp == kTcWarpMma) {
@@ -373,7 +400,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < nchunks; ++c) {
                 const int as = c % kTcAStages, bs = c % kTcBStages;
                 if (abort_flag) break;
-                bool ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
+                bool ok = true;
+                if constexpr (kXTma) ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
                 ok = ok && mbar_wait_bounded(&full_b[bs], (c / kTcBStages) & 1, kWaitLimitCycles);
                 if (!ok) {
                     abort_flag = 1;
@@ -386,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
                     tc_mma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (c | kk) != 0);
-                tc_commit(&empty_a[as]);
+                if constexpr (kXTma) tc_commit(&empty_a[as]);
                 tc_commit(&empty_b[bs]);
             }
             // Always signal completion of whatever was issued, and wait for
@@ -398,6 +426,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         const int r = threadIdx.x & (kTcRows - 1), h = threadIdx.x >> 8;  // row of the tile, byte half
+        // Fused activations: thread t rounds 8 values (16 bytes of the bf16
+        // tile) of token rows t/8 and 64 + t/8 per chunk, loaded one chunk
+        // ahead so that the L2 latency hides behind a chunk of dequantization.
+        const int arow = threadIdx.x >> 3, aseg = threadIdx.x & 7;
+        const bool a0on = !kXTma && arow < T, a1on = !kXTma && arow + 64 < T;
+        const float *xrow = x + (size_t)arow * K + (size_t)c_base * kTcKc + 8 * aseg;
+        float4 xr[4];
+        auto load_x = [&](int cc) {
+            const float4 *src = reinterpret_cast<const float4 *>(xrow + (size_t)cc * kTcKc);
+            if (a0on) {
+                xr[0] = __ldg(src);
+                xr[1] = __ldg(src + 1);
+            }
+            if (a1on) {
+                xr[2] = __ldg(src + 16 * (size_t)K);
+                xr[3] = __ldg(src + 16 * (size_t)K + 1);
+            }
+        };
+        if constexpr (!kXTma) {
+            // x may be written by the previous kernel on the stream.
+            pdl_wait();
+            if (nchunks > 0) load_x(0);
+        }
         bool good = true;
         int c = 0;  // chunk of this CTA
         for (int b = 0; b < nblocks && good; ++b) {
@@ -421,6 +472,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!__all_sync(0xffffffffu, ok)) {
                     good = false;
                     break;
+                }
+                if constexpr (!kXTma) {
+                    uint8_t *arow_p = smem + L::off_a + bs * kTcATileBytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
+                    if (a0on)
+                        *reinterpret_cast<uint4 *>(arow_p) =
+                            make_uint4(pack_bf16x2(make_float2(xr[0].x, xr[0].y)), pack_bf16x2(make_float2(xr[0].z, xr[0].w)),
+                                       pack_bf16x2(make_float2(xr[1].x, xr[1].y)), pack_bf16x2(make_float2(xr[1].z, xr[1].w)));
+                    if (a1on)
+                        *reinterpret_cast<uint4 *>(arow_p + 64 * 128) =
+                            make_uint4(pack_bf16x2(make_float2(xr[2].x, xr[2].y)), pack_bf16x2(make_float2(xr[2].z, xr[2].w)),
+                                       pack_bf16x2(make_float2(xr[3].x, xr[3].y)), pack_bf16x2(make_float2(xr[3].z, xr[3].w)));
+                    if (c + 1 < nchunks) load_x(c + 1);
                 }
                 const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
                 const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * h);
@@ -570,11 +633,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8_t *W, float *y, int K, int N,
-                        int T, int S) {
+// One launch over a tile of at most 128 tokens: activations either from the
+// bf16 copy xb by TMA (xb != nullptr) or from fp32 x, rounded in the kernel.
+cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float *x, const uint8_t *W, float *y,
+                        int K, int N, int T, int S) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
     alignas(64) CUtensorMap tm_w, tm_x;
+    std::memset(&tm_x, 0, sizeof(tm_x));
     const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
     {
         const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
@@ -586,7 +652,7 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {
+    if (xb) {
         // bf16 activations [T][K]: a 64-value (128-byte) by 128-token box with
         // the 128-byte swizzle is exactly one K-major MMA operand tile; token
         // rows past T read as zero.
@@ -601,7 +667,8 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8
     }
     const size_t smem = TcLayout::total + 1024;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
-    cudaError_t e = ensure_smem(q4k_mm_tc_kernel, smem);
+    auto kernel = xb ? q4k_mm_tc_kernel<true> : q4k_mm_tc_kernel<false>;
+    cudaError_t e = ensure_smem(kernel, smem);
     if (e != cudaSuccess) return e;
     const int tiles = (N + kTcRows - 1) / kTcRows;
     cudaLaunchConfig_t cfg = {};
@@ -622,37 +689,59 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const uint8
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, q4k_mm_tc_kernel, tm_w, tm_x, y, K, N, T, c.status);
+    return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_x, x, y, K, N, T, c.status);
 }
 
-}  // namespace
-
-cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
-                             int N, int T) {
-    // Split of K over the cluster: at least 3 CTAs per row tile, and at most
-    // kTcMaxKPerCta values of K per CTA.
-    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
-    if (S > 4) return cudaErrorNotSupported;  // the reduction adds at most three other ranks
-    // Stream-ordered scratch, freed on the same stream after the last token
-    // tile: x rounded to bf16 once (2·T·K bytes).  The weights are re-read
-    // once per tile of 128 tokens.
+// Tiles of 128 tokens over the bf16 copy xb of x (several tiles), or one
+// tile that rounds x itself (xb == nullptr, at most 128 tokens).
+cudaError_t launch_tiles(const LaunchCtx &c, const float *x, __nv_bfloat16 *xb, const uint8_t *W, float *y, int K,
+                         int N, int T, int S) {
+    if (!xb) return launch_tile(c, nullptr, x, W, y, K, N, T, S);
     const size_t n = (size_t)T * K;
-    const int tmax = min(T, kTcMaxTokens);
-    const size_t xb_bytes = (n * sizeof(__nv_bfloat16) + 255) / 256 * 256;
-    void *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(&scratch, xb_bytes, c.stream);
-    if (e != cudaSuccess) return e;
-    __nv_bfloat16 *xb = static_cast<__nv_bfloat16 *>(scratch);
+    cudaError_t e;
     {
         const size_t n4 = n / 4;
         const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
         e = launch_kernel(c, x_to_bf16_kernel, dim3(grid), dim3(256), 0,
                           reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb), n4);
     }
-    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
-        const int tt = min(tmax, T - t0);
-        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, K, N, tt, S);
+    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += kTcMaxTokens) {
+        const int tt = min(kTcMaxTokens, T - t0);
+        e = launch_tile(c, xb + (size_t)t0 * K, nullptr, W, y + (size_t)t0 * N, K, N, tt, S);
     }
+    return e;
+}
+
+// Split of K over the cluster: at least 3 CTAs per row tile, and at most
+// kTcMaxKPerCta values of K per CTA; 0 when the reduction (at most four
+// ranks) cannot take it.
+int tc_split(int K) {
+    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
+    return S > 4 ? 0 : S;
+}
+
+}  // namespace
+
+size_t q4k_mm_tc_scratch_bytes(int K, int N, int T) {
+    (void)N;
+    if (T <= kTcMaxTokens) return 0;
+    return ((size_t)T * K * sizeof(__nv_bfloat16) + 255) / 256 * 256;
+}
+
+cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
+                             int N, int T) {
+    const int S = tc_split(K);
+    if (S == 0) return cudaErrorNotSupported;
+    // Up to 128 tokens: one launch that rounds x itself, nothing allocated.
+    // More: x is rounded to bf16 once into stream-ordered scratch (freed on
+    // the same stream after the last tile) and the weights are re-read once
+    // per tile of 128 tokens.
+    const size_t bytes = q4k_mm_tc_scratch_bytes(K, N, T);
+    if (bytes == 0) return launch_tiles(c, x, nullptr, W, y, K, N, T, S);
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(&scratch, bytes, c.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_tiles(c, x, static_cast<__nv_bfloat16 *>(scratch), W, y, K, N, T, S);
     const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
     return e != cudaSuccess ? e : ef;
 }
@@ -699,35 +788,20 @@ cudaError_t fixed_scratch(uint8_t **out) {
 
 }  // namespace
 
-size_t q4k_mm_tc_scratch_bytes(int K, int N, int T) {
-    (void)N;
-    return ((size_t)T * K * sizeof(__nv_bfloat16) + 255) / 256 * 256;
-}
-
 cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                            int K, int N, int T) {
-    const int S = max(3, (K + kTcMaxKPerCta - 1) / kTcMaxKPerCta);
-    if (S > 4) return cudaErrorNotSupported;
-    if (q4k_mm_tc_scratch_bytes(K, N, T) > (size_t)Q4MM_TC_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    const int S = tc_split(K);
+    if (S == 0) return cudaErrorNotSupported;
+    const size_t bytes = q4k_mm_tc_scratch_bytes(K, N, T);
+    if (bytes > (size_t)Q4MM_TC_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    // The lookup runs on every call, so the first call on a device makes it
+    // whatever its size.
     uint8_t *scratch = nullptr;
     cudaError_t e = fixed_scratch(&scratch);
     if (e != cudaSuccess) return e;
-    // As in launch_q4k_mm_tc, the scratch holds x rounded to bf16.  Nothing
-    // needs clearing: the pre-pass writes all of it.
-    const size_t n = (size_t)T * K;
-    const int tmax = min(T, kTcMaxTokens);
-    __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(scratch);
-    {
-        const size_t n4 = n / 4;
-        const int grid = (int)min((size_t)4 * c.num_sms, (n4 + 255) / 256);
-        e = launch_kernel(c, x_to_bf16_kernel, dim3(grid), dim3(256), 0,
-                          reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb), n4);
-    }
-    for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += tmax) {
-        const int tt = min(tmax, T - t0);
-        e = launch_tile(c, xb + (size_t)t0 * K, W, y + (size_t)t0 * N, K, N, tt, S);
-    }
-    return e;
+    // As in launch_q4k_mm_tc, the scratch (above 128 tokens) holds x rounded
+    // to bf16.  Nothing needs clearing: the pre-pass writes all of it.
+    return launch_tiles(c, x, bytes ? reinterpret_cast<__nv_bfloat16 *>(scratch) : nullptr, W, y, K, N, T, S);
 }
 
 }  // namespace q4mm
