@@ -261,11 +261,12 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
     }
 }
 
-// kXTma: activation tiles come by TMA from a bf16 copy of x (tm_x).
-// Otherwise the dequant warps read fp32 x themselves, round it and write the
-// activation tile of each chunk next to its weight tile, and one barrier
-// (full_b) publishes both.
-template <bool kXTma>
+// kXRows = 0: activation tiles come by TMA from a bf16 copy of x (tm_x).
+// Otherwise the dequant warps read fp32 x themselves (kXRows token rows per
+// thread and chunk: 2 for up to 64 tokens, 4 for up to 128), round it and
+// write the activation tile of each chunk next to its weight tile, and one
+// barrier (full_b) publishes both.
+template <int kXRows>
 __global__ void __launch_bounds__(kTcThreads, 1)
     q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                      const float *__restrict__ x, float *__restrict__ y, int K, int N, int T, int *status) {
@@ -304,14 +305,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&empty_a[s], 1);
         }
         for (int s = 0; s < kTcBStages; ++s) {
-            mbar_init(&full_b[s], kTcDq);
+            mbar_init(&full_b[s], kTcDq / 2);
             mbar_init(&empty_b[s], 1);
         }
         mbar_init(done, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
-    if constexpr (!kXTma) {
+    if constexpr (kXRows > 0) {
         // Token rows T..127 of every activation stage stay zero.
         const int pad16 = (kTcTok - T) * 128 / 16;
         for (int s = 0; s < kTcAStages; ++s) {
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
                             &full_w[nw]);
             }
-            if constexpr (kXTma) {
+            if constexpr (kXRows == 0) {
                 // The bf16 activations come from the previous kernel on the stream.
                 pdl_wait();
                 for (; nx < min(nchunks, kTcAStages); ++nx) {
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // about to be reused: the last use of each ring slot must land.
             for (int b = max(0, nw - kTcWStages); b < nw; ++b)
                 (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
-            if constexpr (kXTma) {
+            if constexpr (kXRows == 0) {
                 for (int c = max(0, nx - kTcAStages); c < nx; ++c)
                     (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, kWaitLimitCycles);
             }
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int as = c % kTcAStages, bs = c % kTcBStages;
                 if (abort_flag) break;
                 bool ok = true;
-                if constexpr (kXTma) ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
+                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
                 ok = ok && mbar_wait_bounded(&full_b[bs], (c / kTcBStages) & 1, kWaitLimitCycles);
                 if (!ok) {
                     abort_flag = 1;
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
                     tc_mma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (c | kk) != 0);
-                if constexpr (kXTma) tc_commit(&empty_a[as]);
+                if constexpr (kXRows == 0) tc_commit(&empty_a[as]);
                 tc_commit(&empty_b[bs]);
             }
             // Always signal completion of whatever was issued, and wait for
@@ -425,29 +426,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        const int r = threadIdx.x & (kTcRows - 1), h = threadIdx.x >> 8;  // row of the tile, byte half
-        // Fused activations: thread t rounds 8 values (16 bytes of the bf16
-        // tile) of token rows t/8 and 64 + t/8 per chunk, loaded one chunk
-        // ahead so that the L2 latency hides behind a chunk of dequantization.
-        const int arow = threadIdx.x >> 3, aseg = threadIdx.x & 7;
-        const bool a0on = !kXTma && arow < T, a1on = !kXTma && arow + 64 < T;
+        // Two groups of 256 threads take alternate chunks: thread t of group
+        // g = t / 256 dequantizes all 64 values of weight row r = t mod 256 in
+        // the chunks c ≡ g (mod 2) of the CTA.
+        const int r = threadIdx.x & (kTcRows - 1), grp = threadIdx.x >> 8;
+        // Fused activations: in each of its chunks, thread r of a group
+        // rounds 16-byte segment r mod 8 of token rows r/8 + 32i, i <
+        // kXRows, loaded when the group's previous chunk is written so that
+        // the L2 latency hides behind it.
+        const int aseg = r & 7, arow = r >> 3;
         const float *xrow = x + (size_t)arow * K + (size_t)c_base * kTcKc + 8 * aseg;
-        float4 xr[4];
+        constexpr int kXR = kXRows > 0 ? kXRows : 1;
+        float4 xr[2 * kXR];
         auto load_x = [&](int cc) {
-            const float4 *src = reinterpret_cast<const float4 *>(xrow + (size_t)cc * kTcKc);
-            if (a0on) {
-                xr[0] = __ldg(src);
-                xr[1] = __ldg(src + 1);
-            }
-            if (a1on) {
-                xr[2] = __ldg(src + 16 * (size_t)K);
-                xr[3] = __ldg(src + 16 * (size_t)K + 1);
+#pragma unroll
+            for (int i = 0; i < kXR; ++i) {
+                if (kXRows > 0 && arow + 32 * i < T) {
+                    const float4 *src = reinterpret_cast<const float4 *>(xrow + (size_t)(32 * i) * K + (size_t)cc * kTcKc);
+                    xr[2 * i] = __ldg(src);
+                    xr[2 * i + 1] = __ldg(src + 1);
+                }
             }
         };
-        if constexpr (!kXTma) {
+        if constexpr (kXRows > 0) {
             // x may be written by the previous kernel on the stream.
             pdl_wait();
-            if (nchunks > 0) load_x(0);
+            if (grp < nchunks) load_x(grp);
         }
         bool good = true;
         int c = 0;  // chunk of this CTA
@@ -457,58 +461,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Chunks of this block within the CTA's range.
             const int jb = b == 0 ? j0 : 0;
             const int je = min(4, jb + (nchunks - c));
+            // Every thread waits for the block, even one with no chunk of it,
+            // before releasing it below: no thread can then release a ring
+            // slot twice in one phase.
+            if (__any_sync(0xffffffffu, abort_flag != 0) ||
+                !__all_sync(0xffffffffu, mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles))) {
+                good = false;
+                break;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (j < jb || j >= je) continue;
-                const int bs = c % kTcBStages;
+                const int cc = c + (j - jb);
+                if ((cc & 1) != grp) continue;
+                const int bs = cc % kTcBStages;
                 if (__any_sync(0xffffffffu, abort_flag != 0)) {
                     good = false;
                     break;
                 }
                 bool ok = true;
-                if (j == jb) ok = mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles);
-                if (ok && c >= kTcBStages)
-                    ok = mbar_wait_bounded(&empty_b[bs], ((c / kTcBStages) - 1) & 1, kWaitLimitCycles);
+                if (cc >= kTcBStages)
+                    ok = mbar_wait_bounded(&empty_b[bs], ((cc / kTcBStages) - 1) & 1, kWaitLimitCycles);
                 if (!__all_sync(0xffffffffu, ok)) {
                     good = false;
                     break;
                 }
-                if constexpr (!kXTma) {
-                    uint8_t *arow_p = smem + L::off_a + bs * kTcATileBytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
-                    if (a0on)
-                        *reinterpret_cast<uint4 *>(arow_p) =
-                            make_uint4(pack_bf16x2(make_float2(xr[0].x, xr[0].y)), pack_bf16x2(make_float2(xr[0].z, xr[0].w)),
-                                       pack_bf16x2(make_float2(xr[1].x, xr[1].y)), pack_bf16x2(make_float2(xr[1].z, xr[1].w)));
-                    if (a1on)
-                        *reinterpret_cast<uint4 *>(arow_p + 64 * 128) =
-                            make_uint4(pack_bf16x2(make_float2(xr[2].x, xr[2].y)), pack_bf16x2(make_float2(xr[2].z, xr[2].w)),
-                                       pack_bf16x2(make_float2(xr[3].x, xr[3].y)), pack_bf16x2(make_float2(xr[3].z, xr[3].w)));
-                    if (c + 1 < nchunks) load_x(c + 1);
+                if constexpr (kXRows > 0) {
+                    uint8_t *ap = smem + L::off_a + bs * kTcATileBytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
+#pragma unroll
+                    for (int i = 0; i < kXRows; ++i) {
+                        if (arow + 32 * i < T)
+                            *reinterpret_cast<uint4 *>(ap + 32 * 128 * i) = make_uint4(
+                                pack_bf16x2(make_float2(xr[2 * i].x, xr[2 * i].y)),
+                                pack_bf16x2(make_float2(xr[2 * i].z, xr[2 * i].w)),
+                                pack_bf16x2(make_float2(xr[2 * i + 1].x, xr[2 * i + 1].y)),
+                                pack_bf16x2(make_float2(xr[2 * i + 1].z, xr[2 * i + 1].w)));
+                    }
+                    if (cc + 2 < nchunks) load_x(cc + 2);
                 }
                 const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * h);
                 const float2 dm = q4k_d_dmin(hdr.x);
                 const float2 slo = sub_scale(2 * j, hdr, dm);
                 const float2 shi = sub_scale(2 * j + 1, hdr, dm);
                 const NibScale lo = nib_scale_lo(slo.x, slo.y), hi = nib_scale_hi(shi.x, shi.y);
-                uint32_t lw[8], hw[8];
-                dequant_word(q.x, lo, hi, lw[0], lw[1], hw[0], hw[1]);
-                dequant_word(q.y, lo, hi, lw[2], lw[3], hw[2], hw[3]);
-                dequant_word(q.z, lo, hi, lw[4], lw[5], hw[4], hw[5]);
-                dequant_word(q.w, lo, hi, lw[6], lw[7], hw[6], hw[7]);
-                // Low values k = 16h..16h+15 are logical chunks 2h, 2h+1; high
-                // values k = 32+16h.. are chunks 4+2h, 5+2h.
                 uint8_t *brow = smem + L::off_b + bs * kTcBTileBytes + r * 128;
                 const int sw = r & 7;
-                *reinterpret_cast<uint4 *>(brow + (((2 * h) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                *reinterpret_cast<uint4 *>(brow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-                *reinterpret_cast<uint4 *>(brow + (((4 + 2 * h) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(brow + (((5 + 2 * h) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                // Half hh: qs bytes 16hh..16hh+15 give low values k = 16hh..
+                // (logical 16-byte chunks 2hh, 2hh+1) and high values k =
+                // 32+16hh.. (chunks 4+2hh, 5+2hh).
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * hh);
+                    uint32_t lw[8], hw[8];
+                    dequant_word(q.x, lo, hi, lw[0], lw[1], hw[0], hw[1]);
+                    dequant_word(q.y, lo, hi, lw[2], lw[3], hw[2], hw[3]);
+                    dequant_word(q.z, lo, hi, lw[4], lw[5], hw[4], hw[5]);
+                    dequant_word(q.w, lo, hi, lw[6], lw[7], hw[6], hw[7]);
+                    *reinterpret_cast<uint4 *>(brow + (((2 * hh) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    *reinterpret_cast<uint4 *>(brow + (((2 * hh + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                    *reinterpret_cast<uint4 *>(brow + (((4 + 2 * hh) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(brow + (((5 + 2 * hh) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                }
                 fence_async_smem();
                 mbar_arrive(&full_b[bs]);
-                ++c;
             }
-            // Every dequant thread releases the block once, after its last chunk.
+            c += je - jb;
+            // Every dequant thread releases the block once.
             if (good) mbar_arrive(&empty_w[ws]);
         }
         if (!good) {
@@ -667,7 +685,7 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float
     }
     const size_t smem = TcLayout::total + 1024;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
-    auto kernel = xb ? q4k_mm_tc_kernel<true> : q4k_mm_tc_kernel<false>;
+    auto kernel = xb ? q4k_mm_tc_kernel<0> : (T <= 64 ? q4k_mm_tc_kernel<2> : q4k_mm_tc_kernel<4>);
     cudaError_t e = ensure_smem(kernel, smem);
     if (e != cudaSuccess) return e;
     const int tiles = (N + kTcRows - 1) / kTcRows;
