@@ -130,7 +130,7 @@ WORKLOADS = {w.name: w for w in [
                         "into three byte planes; 2-bit fields x planes in int32 dp4a; fp32 combination, scale "
                         "applied once"),
     Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",
-             "hbm", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
+             "alu", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),
     Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
@@ -140,7 +140,7 @@ WORKLOADS = {w.name: w for w in [
              "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv.cu"], distinct=1,
              arithmetic=T1_ARITH + " (one token per compute warp; the 11008-wide down projection on the "
                                    "fp32 register-tile kernel)"),
-    Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "hbm",
+    Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "alu",
              "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
              "layers x q,k,v,o,gate,up,down), 8 tokens", ["q4k_gemv.cu"], distinct=1,
              arithmetic="fp32 dequantization and fp32 FMA"),
@@ -622,7 +622,7 @@ def run_ours(a) -> None:
         cpu = cpu_baseline(w, mats, a.cpu_seconds)
 
     if rank == 0:
-        dtype = {"hbm": "i32+f32" if w.arithmetic == T1_ARITH else "f32", "tensor": "bf16",
+        dtype = {"hbm": "i32+f32" if "dp4a" in w.arithmetic else "f32", "tensor": "bf16",
                  "alu": "f32"}[w.bound]
         line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": n_ranks,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
