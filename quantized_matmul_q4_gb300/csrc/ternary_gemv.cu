@@ -363,7 +363,7 @@ struct TernTileParams {
 };
 
 template <int TT>
-__global__ void __launch_bounds__(32 * kTernTileWarps) ternary_tile_kernel(const TernTileParams p) {
+__global__ void __launch_bounds__(32 * kTernTileWarps, 2) ternary_tile_kernel(const TernTileParams p) {
     extern __shared__ __align__(128) uint8_t tile_smem[];
     float *xs = reinterpret_cast<float *>(tile_smem);                     // [TT][kc]
     uint8_t *ws = tile_smem + (size_t)TT * p.kc * sizeof(float);          // [rows][kc/4]
