@@ -385,11 +385,11 @@ __global__ void __launch_bounds__(32 * kTernTileWarps, 2) ternary_tile_kernel(co
     pdl_launch_dependents();
     pdl_wait();
 
-    float acc[8][TT];
+    float2 acc2[4][TT];  // rows (2rp, 2rp+1) × token t
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int rp = 0; rp < 4; ++rp)
 #pragma unroll
-        for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
+        for (int t = 0; t < TT; ++t) acc2[rp][t] = make_float2(0.f, 0.f);
     float xsum[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) xsum[t] = 0.f;
@@ -440,12 +440,13 @@ __global__ void __launch_bounds__(32 * kTernTileWarps, 2) ternary_tile_kernel(co
                     if (warp == 0) xsum[t] += (v.x + v.y) + (v.z + v.w);
                 }
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
+                for (int rp = 0; rp < 4; ++rp) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float c = __uint_as_float(__byte_perm(fb[r][i], 0x3F000000u, sel));
+                        const float2 c = make_float2(__uint_as_float(__byte_perm(fb[2 * rp][i], 0x3F000000u, sel)),
+                                                     __uint_as_float(__byte_perm(fb[2 * rp + 1][i], 0x3F000000u, sel)));
 #pragma unroll
-                        for (int t = 0; t < TT; ++t) acc[r][t] = fmaf(xq[t][i], c, acc[r][t]);
+                        for (int t = 0; t < TT; ++t) acc2[rp][t] = ffma2(make_float2(xq[t][i], xq[t][i]), c, acc2[rp][t]);
                     }
                 }
             }
@@ -466,9 +467,12 @@ __global__ void __launch_bounds__(32 * kTernTileWarps, 2) ternary_tile_kernel(co
     constexpr int V = 8 * TT;
     float v[V];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int rp = 0; rp < 4; ++rp)
 #pragma unroll
-        for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t];
+        for (int t = 0; t < TT; ++t) {
+            v[(2 * rp) * TT + t] = acc2[rp][t].x;
+            v[(2 * rp + 1) * TT + t] = acc2[rp][t].y;
+        }
     int idx = 0;
     int n = V;
 #pragma unroll
