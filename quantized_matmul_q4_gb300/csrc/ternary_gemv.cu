@@ -344,7 +344,8 @@ __global__ void __launch_bounds__(32 * kTernT1Warps, 1) ternary_t1_kernel(const 
 // A CTA owns 8·kTernTileWarps rows and TT tokens; per K chunk it copies the
 // rows' code bytes and the tokens' activations into shared memory, then warp
 // w accumulates rows 8w..8w+7 for all TT tokens with lane l on words
-// l, l+32, … of the chunk.  Each word's 16 positions go in four quads; the
+// l, l+32, … of the chunk, rows in pairs by packed FMAs.  Each word's 16
+// positions go in four quads; the
 // lanes take the quads in a rotated order ((q + l/2) mod 4) so that the
 // activation reads of a quarter-warp fall in distinct banks.  A butterfly
 // over the 8·TT accumulators finishes the sums.
