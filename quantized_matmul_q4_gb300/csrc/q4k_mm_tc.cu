@@ -398,25 +398,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcWarpMma) {
         if (lane == 0) {
             const uint32_t idesc = mma_idesc<kTcTok, kTcRows>();
+            // One thread's dependent chain sits between the chunks' MMAs, so
+            // the loop keeps it short: stage, phase and descriptors advance by
+            // additions (a descriptor's address field counts 16-byte units;
+            // every tile lies below 256 KB, so no carry leaves the field).
+            const uint64_t a_desc0 = sw128_desc(sbase + L::off_a), b_desc0 = sw128_desc(sbase + L::off_b);
+            int st = 0;
+            uint32_t ph = 0;
             for (int c = 0; c < nchunks; ++c) {
-                const int as = c % kTcAStages, bs = c % kTcBStages;
-                if (abort_flag) break;
                 bool ok = true;
-                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[as], (c / kTcAStages) & 1, kWaitLimitCycles);
-                ok = ok && mbar_wait_bounded(&full_b[bs], (c / kTcBStages) & 1, kWaitLimitCycles);
+                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[st], ph, kWaitLimitCycles);
+                ok = ok && mbar_wait_bounded(&full_b[st], ph, kWaitLimitCycles);
                 if (!ok) {
                     abort_flag = 1;
                     flag_timeout(status);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + L::off_a + as * kTcATileBytes;
-                const uint32_t b0 = sbase + L::off_b + bs * kTcBTileBytes;
+                const uint64_t ad = a_desc0 + (uint64_t)(st * (kTcATileBytes >> 4));
+                const uint64_t bd = b_desc0 + (uint64_t)(st * (kTcBTileBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
-                    tc_mma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, (c | kk) != 0);
-                if constexpr (kXRows == 0) tc_commit(&empty_a[as]);
-                tc_commit(&empty_b[bs]);
+                    tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+                if constexpr (kXRows == 0) tc_commit(&empty_a[st]);
+                tc_commit(&empty_b[st]);
+                if (++st == kTcBStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
             // Always signal completion of whatever was issued, and wait for
             // it, so that tensor memory is never read or released with MMAs
