@@ -95,6 +95,12 @@ WORKLOADS = {w.name: w for w in [
     Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",
              "gemv_t1_kernel", METRIC, ["q4k_gemv.cu"], "q4k_gemv_t1_4096x4096.md",
              distinct=64, arithmetic=T1_ARITH),
+    Workload("q4k_gemv_8192x8192_t1", "q4k", "q4k_matmul", [(8192, 8192)], 1, 16, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 8192x8192, batch 1", ["q4k_gemv.cu"],
+             distinct=4, arithmetic=T1_ARITH),
+    Workload("q4k_gemv_16384x16384_t1", "q4k", "q4k_matmul", [(16384, 16384)], 1, 4, "GB/s", "hbm",
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 16384x16384, batch 1", ["q4k_gemv.cu"],
+             distinct=1, arithmetic=T1_ARITH),
     Workload("q4k_gemv_4096x1024_t1", "q4k", "q4k_matmul", [(4096, 1024)], 1, 128, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 4096->1024, batch 1",
              ["q4k_gemv.cu"], arithmetic=T1_ARITH),

@@ -1073,6 +1073,8 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
             case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
             case 32: return go(gemv_t1_kernel<Fmt, 32, false>);
             case 43: return go(gemv_t1_kernel<Fmt, 43, false>);
+            case 56: return go(gemv_t1_kernel<Fmt, 56, false>);
+            case 64: return go(gemv_t1_kernel<Fmt, 64, false>);
             default: return go(gemv_t1_kernel<Fmt, 0, false>);
         }
     } else {

@@ -98,6 +98,13 @@ def test_prefill_workload_sampled():
     _sampled(4096, 11008, 64, seed=0)
 
 
+@pytest.mark.parametrize("K,N", [(8192, 8192), (16384, 16384), (14336, 4096)])
+def test_large_one_token_sampled(K, N):
+    # One-token GEMVs above 4096²: the 8192² and 16384² bench matrices and a
+    # 14336-wide row (Llama-3-8B down projection), sampled output rows.
+    _sampled(K, N, 1, seed=K + N)
+
+
 @pytest.mark.parametrize("K,N", synth.LLAMA7B_LAYER[3:7])
 @pytest.mark.parametrize("T", [1, 8])
 def test_llama7b_layer_shapes_sampled(K, N, T):
