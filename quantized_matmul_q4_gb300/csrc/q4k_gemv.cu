@@ -402,6 +402,32 @@ struct FmtQ6K {
     }
 };
 
+// L2 eviction policies for the weight stream.  Weights are read once per
+// call: evict_first keeps them from displacing data that is read again
+// (activations, outputs, whatever the caller keeps hot in L2).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global → shared with an L2 cache policy, completion counted
+// on `bar` in bytes; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter:
 // the float's bits are 0x4B400000 + rint(v).
 constexpr float kShifter = 12582912.0f;
@@ -428,6 +454,7 @@ struct T1Params {
     int x_staged;      // 1: x arrives by one bulk copy into shared memory
     float out_scale;   // y = out_scale · (row result); 1 except for the ternary scale
     int T;             // tokens (x [T][K], y [T][N]); each compute warp serves one token
+    int l2_evict_first;  // 1: weight copies carry the L2 evict_first policy
 };
 
 constexpr int kT1RoleWarps = 1;  // the copy warp
@@ -505,6 +532,9 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
 
     if (warp == 0) {
         if (lane == 0) {
+            // Weights are read once: streamed with evict_first so that they
+            // do not displace activations and outputs from L2.
+            const uint64_t wpol = p.l2_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
             auto issue = [&](int st, int slot) {
                 const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
                 uint8_t *dst = ring + (size_t)slot * slot_bytes;
@@ -525,14 +555,15 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                     } else {
                         mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
                     }
-                    bulk_g2s(dst, src, bulk, &full_bar[slot]);
+                    bulk_g2s_hint(dst, src, bulk, &full_bar[slot], wpol);
                 } else {
                     mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
                 }
                 if (kSwiGLU && v1 > nrows) {
                     const int u0 = max(v0, nrows);
-                    bulk_g2s(dst + (size_t)(u0 - v0) * row_bytes, p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes,
-                             (uint32_t)(v1 - u0) * row_bytes, &full_bar[slot]);
+                    bulk_g2s_hint(dst + (size_t)(u0 - v0) * row_bytes,
+                                  p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes, (uint32_t)(v1 - u0) * row_bytes,
+                                  &full_bar[slot], wpol);
                 }
                 issued = st + 1;
             };
@@ -945,6 +976,10 @@ struct T1Tuning {
     int ring_bytes = 200 * 1024;
     int pre_stages = 0;        // weight stages issued before the activation copy
     int x_stage_max = 65536;   // bytes of x staged by a bulk copy (0: plain loads)
+    int l2_evict_first = 1;    // weight copies with the L2 evict_first policy
+    int max_grid = 0;          // CTAs per launch at most (0: no limit)
+    int spare_sms = 4;         // SMs left without a CTA of a short launch
+    int spare_max_bytes = 256 * 1024;  // "short": at most this many weight bytes per CTA
 };
 
 int env_int(const char *name, int dflt, int lo, int hi) {
@@ -963,6 +998,10 @@ const T1Tuning &t1_tuning() {
         r.ring_bytes = env_int("Q4MM_T1_RING_BYTES", r.ring_bytes, 8192, 200 * 1024);
         r.pre_stages = env_int("Q4MM_T1_PRE_STAGES", r.pre_stages, 0, 64);
         r.x_stage_max = env_int("Q4MM_T1_X_STAGE_MAX", r.x_stage_max, 0, 65536);
+        r.l2_evict_first = env_int("Q4MM_T1_L2_EVICT_FIRST", r.l2_evict_first, 0, 1);
+        r.max_grid = env_int("Q4MM_T1_MAX_GRID", r.max_grid, 0, 4096);
+        r.spare_sms = env_int("Q4MM_T1_SPARE_SMS", r.spare_sms, 0, 64);
+        r.spare_max_bytes = env_int("Q4MM_T1_SPARE_MAX_BYTES", r.spare_max_bytes, 0, 1 << 30);
         return r;
     }();
     return t;
@@ -1015,7 +1054,18 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     const int sq = max(pass_rows, rq);  // both powers of two
     p.stage_rows = sq * max(1, (tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
 
+    // Grid.  A CTA of the next launch on the stream can only start where a
+    // CTA of this one has exited, and one that starts after this launch has
+    // completed gets through its wait on it ~0.7 µs later than the CTAs
+    // already resident: with a CTA on every SM, the CTAs of each launch that
+    // start last also finish last and delay the next launch the same way.
+    // For a short launch (few weight bytes per CTA) leaving spare_sms SMs
+    // free lets every CTA of the next launch be resident before this one
+    // completes; a long launch keeps every SM for the weight stream.
     int grid = tun.ctas_per_sm * c.num_sms;
+    const double cta_bytes = (double)(kSwiGLU ? 2 : 1) * N * row_bytes / grid;
+    if (cta_bytes <= tun.spare_max_bytes) grid = max(1, grid - tun.spare_sms);
+    if (tun.max_grid > 0) grid = min(grid, tun.max_grid);
     p.rows_per_cta = (N + grid - 1) / grid;
     p.rows_per_cta = (p.rows_per_cta + rq - 1) / rq * rq;
     if (p.rows_per_cta < pass_rows) p.rows_per_cta = pass_rows;
@@ -1042,6 +1092,7 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     p.nslots = nslots;
     // With plain activation loads nothing needs to go out ahead of the rest.
     p.pre_stages = p.x_staged ? tun.pre_stages : nslots;
+    p.l2_evict_first = tun.l2_evict_first;
     const size_t smem = xs_bytes + (size_t)nslots * slot_bytes + 2 * nslots * sizeof(uint64_t) + part_bytes;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
 
