@@ -866,11 +866,20 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
         return;
     }
 
+    // Consumers: min(kMultiCw, nslots) warps taking groups in turn, with
+    // nslots a multiple of their count (the launcher rounds it), so that
+    // slot s belongs to warp s mod ncons alone.  A warp's successive groups
+    // in its slot are then one ring lap apart and it has consumed the
+    // slot's previous phase itself, so its parity wait can never match an
+    // older phase (a warp reaching group g before group g − nslots, held by
+    // another warp, has landed would read the slot's previous contents).
+    const int ncons = min(kMultiCw, p.nslots);
     const int cw = warp - 1;
+    if (cw >= ncons) return;
     const int j = lane >> 3, wq = lane & 7;   // slab and word within it
     // x may be produced by the previous kernel on the stream.
     pdl_wait();
-    for (int g = cw; g < ngroups; g += kMultiCw) {
+    for (int g = cw; g < ngroups; g += ncons) {
         const int slot = g % p.nslots;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (g / p.nslots) & 1, kWaitLimitCycles))) {
             flag_timeout(p.status);
@@ -1180,9 +1189,14 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
     grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
     const int cta_groups = p.rows_per_cta / kMultiRows;
-    // Ring: up to 200 KB, at least two slots, never more slots than groups.
-    p.nslots = (int)min((size_t)min(cta_groups, 16), max((size_t)2, (size_t)(200 * 1024) / slot_bytes));
+    // Ring: up to 200 KB (less if Q4MM_MULTI_RING_BYTES says so), at least
+    // two slots, never more slots than groups.
+    static const int ring_bytes = env_int("Q4MM_MULTI_RING_BYTES", 200 * 1024, 8192, 200 * 1024);
+    p.nslots = (int)min((size_t)min(cta_groups, 16), max((size_t)2, (size_t)ring_bytes / slot_bytes));
     p.nslots = max(p.nslots, min(cta_groups, 2));
+    // Every slot has one consumer warp (see the kernel): from kMultiCw slots
+    // on, a multiple of kMultiCw; below that, one warp per slot.
+    if (p.nslots >= kMultiCw) p.nslots = p.nslots / kMultiCw * kMultiCw;
     const size_t smem = (size_t)p.nslots * slot_bytes + 2 * (size_t)p.nslots * sizeof(uint64_t);
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
 

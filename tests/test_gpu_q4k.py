@@ -105,6 +105,16 @@ def test_large_one_token_sampled(K, N):
     _sampled(K, N, 1, seed=K + N)
 
 
+@pytest.mark.parametrize("K,N,T", [(14336, 4096, 8), (16384, 4096, 5), (13056, 4096, 3)])
+def test_multi_token_wide_rows_full(K, N, T):
+    # 2-8 token kernel with rows so wide that fewer ring slots than compute
+    # warps fit in shared memory (13056 values and up), and more row groups
+    # per CTA than slots, so every slot is reused: all outputs checked.
+    x, W, K, N, T = synth.q4k_case((K, N, T), seed=K + T)
+    y = q4k(x, W, K, N)
+    assert_rows_close(y, oracle.q4k_matmul(x, W, K, N), REL, f"K{K} N{N} T{T}")
+
+
 @pytest.mark.parametrize("K,N", synth.LLAMA7B_LAYER[3:7])
 @pytest.mark.parametrize("T", [1, 8])
 def test_llama7b_layer_shapes_sampled(K, N, T):
