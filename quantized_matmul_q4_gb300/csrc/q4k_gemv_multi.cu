@@ -1,0 +1,292 @@
+// Q4_K decode GEMV for 2..8 tokens (FP32 register tiles), sm_103a.
+//
+// Computes y[t][o] = Σ_k x[t][k]·w[o][k] with w = d·sc_s·q − dmin·m_s decoded
+// on the fly from the 144-byte Q4_K super-blocks (SKaiNET PR #562
+// "feat(kernel): SIMD-fused Q4_K matmul kernel + Q4KMatmulKernel SPI",
+// section "Pipeline"); each weight is dequantized once and used by every
+// token, so the weights stream from HBM once per call.
+//
+// Nibble decode: a masked code q in byte k of a word becomes the float
+// 0.5 + q/256 with one byte permute (see nib_biased).  The bias 0.5·Σx is
+// removed together with the lazy min term: per sub-block s the contribution
+// is (256·d·sc_s)·acc_s − (128·d·sc_s + dmin·m_s)·Σx_s where
+// acc_s = Σ x·(0.5 + q/256); here the dequantized weight
+// scale'·(0.5 + q/256) − offset' is formed once and multiplied into every
+// token's accumulator.
+#include <cstdlib>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sync.cuh"
+
+namespace q4mm {
+
+namespace {
+
+// ----------------------------------------------------------------------------
+// Block scales of one lane
+// ----------------------------------------------------------------------------
+
+// Per-lane constants for the two sub-blocks 2j and 2j+1 of a block:
+// scale' = 256·d·sc and offset' = 128·d·sc + dmin·m.
+struct SlabScales {
+    float s0, s1, o0, o1;
+};
+
+__device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
+    const float2 dm = q4k_d_dmin(hdr.x);
+    const Q4kScales u = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+    const bool upper = j >= 2;  // sub-blocks 4..7 use the split 6-bit fields
+    const uint32_t scw = upper ? u.sc_hi : u.sc_lo;
+    const uint32_t mw = upper ? u.m_hi : u.m_lo;
+    const int k0 = 2 * (j & 1);
+    const float d256 = dm.x * 256.0f;  // exact: power-of-two scaling
+    SlabScales r;
+    r.s0 = d256 * byte_to_float(scw, k0);  // exact: 11-bit × 6-bit
+    r.s1 = d256 * byte_to_float(scw, k0 + 1);
+    r.o0 = fmaf(dm.y, byte_to_float(mw, k0), 0.5f * r.s0);
+    r.o1 = fmaf(dm.y, byte_to_float(mw, k0 + 1), 0.5f * r.s1);
+    return r;
+}
+
+// ----------------------------------------------------------------------------
+// 2..8 tokens: bulk-copied row groups, word lanes, register tiles
+// ----------------------------------------------------------------------------
+//
+// A CTA owns a contiguous range of rows in groups of four; one producer
+// thread streams each group (four whole rows) into its own ring slot with a
+// bulk copy, before the wait on the previous kernel.  Compute warp c takes
+// groups c, c + n, … (n consumer warps, see the kernel), and for each group
+// walks all blocks of the rows:
+// lane l owns qs word l of every block — 4 low-nibble weights of sub-block
+// 2j and 4 high-nibble weights of 2j+1 (j = l/8) — with the 8 matching
+// activations of all TT tokens loaded once per block and reused by the four
+// rows.  Each weight is dequantized once (scale'·(0.5 + q/256) − offset') and
+// multiplied into TT token accumulators, two positions per paired FMA.  A
+// butterfly over the 4·TT sums at the end of the group finishes the rows.
+
+constexpr int kMultiWarps = 8;                    // copy warp + 7 compute warps
+constexpr int kMultiCw = kMultiWarps - 1;
+constexpr int kMultiRows = 4;                     // rows per group (one ring slot)
+
+struct MultiParams {
+    const float *x;
+    const uint8_t *W;
+    float *y;
+    int *status;
+    int K, N, T;       // T: tokens of this launch (<= TT)
+    int nb;            // blocks per row
+    int rows_per_cta;  // multiple of kMultiRows
+    int nslots;        // ring depth (groups in flight)
+};
+
+template <int TT>
+__global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(MultiParams p) {
+    extern __shared__ __align__(128) uint8_t msmem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
+    const uint32_t slot_bytes = kMultiRows * row_bytes;
+    uint8_t *ring = msmem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
+    uint64_t *empty = full + p.nslots;
+    const int row0 = blockIdx.x * p.rows_per_cta;
+    const int nrows = min(p.rows_per_cta, p.N - row0);
+    const int ngroups = (nrows + kMultiRows - 1) / kMultiRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.nslots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int g = 0; g < ngroups; ++g, ++issued) {
+                const int slot = g % p.nslots;
+                if (g >= p.nslots &&
+                    !mbar_wait_bounded(&empty[slot], ((g / p.nslots) - 1) & 1, kWaitLimitCycles)) {
+                    flag_timeout(p.status);
+                    break;
+                }
+                const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+                bulk_g2s(ring + (size_t)slot * slot_bytes,
+                         p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes, &full[slot]);
+            }
+            // Never leave a copy writing into an exiting CTA.
+            for (int g = max(0, issued - p.nslots); g < issued; ++g)
+                (void)mbar_wait_bounded(&full[g % p.nslots], (g / p.nslots) & 1, kWaitLimitCycles);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // Consumers: min(kMultiCw, nslots) warps taking groups in turn, with
+    // nslots a multiple of their count (the launcher rounds it), so that
+    // slot s belongs to warp s mod ncons alone.  A warp's successive groups
+    // in its slot are then one ring lap apart and it has consumed the
+    // slot's previous phase itself, so its parity wait can never match an
+    // older phase (a warp reaching group g before group g − nslots, held by
+    // another warp, has landed would read the slot's previous contents).
+    const int ncons = min(kMultiCw, p.nslots);
+    const int cw = warp - 1;
+    if (cw >= ncons) return;
+    const int j = lane >> 3, wq = lane & 7;   // slab and word within it
+    // x may be produced by the previous kernel on the stream.
+    pdl_wait();
+    for (int g = cw; g < ngroups; g += ncons) {
+        const int slot = g % p.nslots;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (g / p.nslots) & 1, kWaitLimitCycles))) {
+            flag_timeout(p.status);
+            break;
+        }
+        const uint8_t *grp = ring + (size_t)slot * slot_bytes;
+        const int rows = min(kMultiRows, nrows - g * kMultiRows);
+        float2 acc[kMultiRows][TT];
+#pragma unroll
+        for (int r = 0; r < kMultiRows; ++r)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+
+        for (int b = 0; b < p.nb; ++b) {
+            // Activations of this lane's 8 positions for every token.
+            float4 xl[TT], xh[TT];
+            const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                if (t < p.T) {
+                    const float *xt = p.x + (size_t)t * p.K + k0;
+                    xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
+                    xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                } else {
+                    xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    xh[t] = xl[t];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kMultiRows; ++r) {
+                // Absent rows of a short last group read row 0 of the slot;
+                // their sums are never stored.
+                const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+                const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
+                const SlabScales sc = slab_scales(hdr, j);
+                const uint32_t l4 = q & 0x0F0F0F0Fu;
+                const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
+                const float2 s0 = make_float2(sc.s0, sc.s0), n0 = make_float2(-sc.o0, -sc.o0);
+                const float2 s1 = make_float2(sc.s1, sc.s1), n1 = make_float2(-sc.o1, -sc.o1);
+                const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
+                const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
+                const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
+                const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
+                    acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+
+        // Butterfly over the 4·TT sums: afterwards lane l holds value index
+        // idx .. idx + n − 1 (see the halving below), summed over the warp.
+        constexpr int V = kMultiRows * TT;
+        float v[V];
+#pragma unroll
+        for (int r = 0; r < kMultiRows; ++r)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t].x + acc[r][t].y;
+        int idx = 0, n = V;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            if (n > 1) {
+                const int half = n >> 1;
+                const bool up = lane & o;
+#pragma unroll
+                for (int i = 0; i < V / 2; ++i) {
+                    if (i < half) {
+                        const float send = up ? v[i] : v[i + half];
+                        const float keep = up ? v[i + half] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                if (up) idx += half;
+                n = half;
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+            }
+        }
+        const bool writer = V >= 32 || (lane & (32 / V - 1)) == 0;
+        if (writer) {
+#pragma unroll
+            for (int i = 0; i < (V >= 32 ? V / 32 : 1); ++i) {
+                const int id = idx + i;
+                const int r = id / TT, t = id % TT;
+                if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = v[i];
+            }
+        }
+    }
+}
+
+// Integer from the environment (read once by the caller), clamped to [lo, hi].
+int multi_env_int(const char *name, int dflt, int lo, int hi) {
+    const char *v = getenv(name);
+    if (!v || !*v) return dflt;
+    const int x = atoi(v);
+    return x < lo ? lo : (x > hi ? hi : x);
+}
+
+}  // namespace
+
+cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                  int K, int N, int T) {
+    MultiParams p;
+    p.x = x;
+    p.W = W;
+    p.y = y;
+    p.status = c.status;
+    p.K = K;
+    p.N = N;
+    p.T = T;
+    p.nb = K / kQ4kValues;
+    const size_t row_bytes = (size_t)p.nb * kQ4kBytes;
+    const size_t slot_bytes = kMultiRows * row_bytes;
+    const int groups = (N + kMultiRows - 1) / kMultiRows;
+    int grid = min(c.num_sms, groups);
+    p.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
+    grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
+    const int cta_groups = p.rows_per_cta / kMultiRows;
+    // Ring: up to 200 KB (less if Q4MM_MULTI_RING_BYTES says so), at least
+    // two slots, never more slots than groups.
+    static const int ring_bytes = multi_env_int("Q4MM_MULTI_RING_BYTES", 200 * 1024, 8192, 200 * 1024);
+    p.nslots = (int)min((size_t)min(cta_groups, 16), max((size_t)2, (size_t)ring_bytes / slot_bytes));
+    p.nslots = max(p.nslots, min(cta_groups, 2));
+    // Every slot has one consumer warp (see the kernel): from kMultiCw slots
+    // on, a multiple of kMultiCw; below that, one warp per slot.
+    if (p.nslots >= kMultiCw) p.nslots = p.nslots / kMultiCw * kMultiCw;
+    const size_t smem = (size_t)p.nslots * slot_bytes + 2 * (size_t)p.nslots * sizeof(uint64_t);
+    if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
+
+#define Q4MM_MULTI_CASE(TT)                                                                    \
+    {                                                                                          \
+        cudaError_t e = ensure_smem(q4k_gemv_multi_kernel<TT>, smem);                          \
+        if (e != cudaSuccess) return e;                                                        \
+        return launch_kernel(c, q4k_gemv_multi_kernel<TT>, dim3(grid), dim3(32 * kMultiWarps), \
+                             smem, p);                                                         \
+    }
+    if (T <= 2) Q4MM_MULTI_CASE(2)
+    if (T <= 4) Q4MM_MULTI_CASE(4)
+    if (T <= 8) Q4MM_MULTI_CASE(8)
+#undef Q4MM_MULTI_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace q4mm
