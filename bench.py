@@ -88,7 +88,7 @@ def weight_bytes(kind, K, N):
     return N * (K // 4)
 
 
-T1_ARITH = ("fp32 activations rounded once to 2^-22 of each 256-value block's maximum and split into three "
+T1_ARITH = ("fp32 activations rounded once to about 2^-22 of each 256-value block's maximum and split into three "
             "byte planes; 4-bit codes x planes in int32 dp4a; scales, mins and combination in fp32")
 LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
 WORKLOADS = {w.name: w for w in [
@@ -132,7 +132,7 @@ WORKLOADS = {w.name: w for w in [
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "gemv_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "batch 1", ["ternary_gemv.cu", "q4k_gemv.cu"], "ternary_t1_2560x6912.md",
-             arithmetic="fp32 activations rounded once to 2^-22 of each 256-value block's maximum and split "
+             arithmetic="fp32 activations rounded once to about 2^-22 of each 256-value block's maximum and split "
                         "into three byte planes; 2-bit fields x planes in int32 dp4a; fp32 combination, scale "
                         "applied once"),
     Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",

@@ -75,9 +75,10 @@ typedef enum {
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
  *         outputDim >= 1; tokens >= 1.
  * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
- *         Up to 4 tokens: x is rounded once to 2^-22 of each 256-value
- *         block's largest magnitude (exactly for integers and any value with
- *         at most 22 significant bits below that maximum) and split into
+ *         Up to 4 tokens: x is rounded once, to within 2^-15/127 (about
+ *         2^-22) of each 256-value block's largest magnitude (exactly for
+ *         integers below 2^21 and any value with at most 21 significant bits
+ *         below the leading bit of that maximum) and split into
  *         three byte planes under a power-of-two block scale; the code-dots
  *         are exact integer sums, scales, mins and the combination are fp32.
  *         Where that kernel's geometry does not fit (2-4 tokens with a large
@@ -136,8 +137,8 @@ int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int
  *         row, as in Q4_K); outputDim >= 1; tokens >= 1.
  * Precision: as the one-token path of q4k_matmul: per token row,
  *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|, with x rounded once
- *         to 2^-22 of each 256-value block's largest magnitude and integer
- *         code-dots.
+ *         to within 2^-15/127 (about 2^-22) of each 256-value block's largest
+ *         magnitude and integer code-dots.
  * Tokens: up to 8 tokens share one pass over the weights (more tokens
  *         take one pass per 8).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.

@@ -54,11 +54,13 @@ namespace {
 // once per CTA, into three byte planes under a power-of-two block scale s_b:
 //   n = rint(x·2^15/s_b),  |n| < 127·2^15 < 2^22,
 //   n = 65536·p2 + 256·p1 + p0  (p0, p1 unsigned bytes, p2 a signed byte),
-// so x = s_b·2^-15·n + e with |e| ≤ 2^-16·s_b ≤ 2^-22·max|x_b|.  The rounding
-// is a single FMA against the 1.5·2^23 shifter (the product by a power of two
-// is exact), whose low bytes are the digits of n; activations with at most
-// 22 significant bits below their block maximum (integers included) are
-// represented exactly.  Low-nibble codes enter the dot products as they are;
+// so x = s_b·2^-15·n + e with |e| ≤ 2^-16·s_b ≤ 2^-15·max|x_b|/127 (s_b is at
+// most 2·max|x_b|/127; the bound is about 2.4e-7·max|x_b|).  The rounding is a
+// single FMA against the 1.5·2^23 shifter (the product by a power of two is
+// exact), whose low bytes are the digits of n; the grid step 2^-15·s_b is at
+// most 2^-20 of the leading power of two of max|x_b|, so activations with at
+// most 21 significant bits below that leading bit (integers below 2^21
+// included) are represented exactly.  Low-nibble codes enter the dot products as they are;
 // high-nibble codes enter as 16·q (the byte masked in place, no shift) and
 // the factor 16 is taken out of that sub-block's scale.  The integer sums are
 // exact; scales, mins and the final combination are fp32.
