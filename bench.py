@@ -93,20 +93,20 @@ T1_ARITH = ("fp32 activations rounded once to about 2^-22 of each 256-value bloc
 LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
 WORKLOADS = {w.name: w for w in [
     Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",
-             "gemv_t1_kernel", METRIC, ["q4k_gemv.cu"], "q4k_gemv_t1_4096x4096.md",
+             "gemv_t1_kernel", METRIC, ["q4k_gemv.cu", "t1_geometry.h"], "q4k_gemv_t1_4096x4096.md",
              distinct=64, arithmetic=T1_ARITH),
     Workload("q4k_gemv_8192x8192_t1", "q4k", "q4k_matmul", [(8192, 8192)], 1, 16, "GB/s", "hbm",
-             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 8192x8192, batch 1", ["q4k_gemv.cu"],
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 8192x8192, batch 1", ["q4k_gemv.cu", "t1_geometry.h"],
              distinct=4, arithmetic=T1_ARITH),
     Workload("q4k_gemv_16384x16384_t1", "q4k", "q4k_matmul", [(16384, 16384)], 1, 4, "GB/s", "hbm",
-             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 16384x16384, batch 1", ["q4k_gemv.cu"],
+             "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 16384x16384, batch 1", ["q4k_gemv.cu", "t1_geometry.h"],
              distinct=1, arithmetic=T1_ARITH),
     Workload("q4k_gemv_4096x1024_t1", "q4k", "q4k_matmul", [(4096, 1024)], 1, 128, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 4096->1024, batch 1",
-             ["q4k_gemv.cu"], arithmetic=T1_ARITH),
+             ["q4k_gemv.cu", "t1_geometry.h"], arithmetic=T1_ARITH),
     Workload("q4k_gemv_1024x1024_t1", "q4k", "q4k_matmul", [(1024, 1024)], 1, 512, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K GEMV weight-stream GB/s at 1024x1024, batch 1",
-             ["q4k_gemv.cu"], arithmetic=T1_ARITH),
+             ["q4k_gemv.cu", "t1_geometry.h"], arithmetic=T1_ARITH),
     Workload("q4k_prefill_tc_4096x11008_t64", "q4k", "q4k_matmul_tc", [(4096, 11008)], 64, 16,
              "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands",
@@ -117,21 +117,21 @@ WORKLOADS = {w.name: w for w in [
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu", "cluster.cuh"],
              "q4k_mm_fp32_4096x11008_t64.md", arithmetic="fp32 dequantization and fp32 FMA"),
     Workload("q4_0_gemv_4096x4096_t1", "q4_0", "q4_0_gemv", [(4096, 4096)], 1, 64, "GB/s", "hbm",
-             "gemv_t1_kernel", "Q4_0 GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
+             "gemv_t1_kernel", "Q4_0 GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu", "t1_geometry.h"],
              "q4_0_gemv_t1_4096x4096.md", distinct=64, arithmetic=T1_ARITH),
     Workload("q6k_gemv_4096x4096_t1", "q6k", "q6k_gemv", [(4096, 4096)], 1, 48, "GB/s", "hbm",
-             "gemv_t1_kernel", "Q6_K GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu"],
+             "gemv_t1_kernel", "Q6_K GEMV weight-stream GB/s at 4096x4096, batch 1", ["q4k_gemv.cu", "t1_geometry.h"],
              "q6k_gemv_t1_4096x4096.md", distinct=48, arithmetic=T1_ARITH.replace("4-bit", "6-bit")),
     Workload("llama7b_ffn_swiglu_t1", "q4k_ffn", "q4k_ffn_swiglu", [(4096, 11008)], 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K fused gate+up SwiGLU weight-stream GB/s, Llama-2-7B FFN (32 layers x "
-             "4096 -> 2 x 11008), batch 1", ["q4k_gemv.cu"], "q4k_ffn_swiglu_llama7b_t1.md", distinct=1,
+             "4096 -> 2 x 11008), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], "q4k_ffn_swiglu_llama7b_t1.md", distinct=1,
              arithmetic=T1_ARITH + "; h = silu(g)*u in fp32"),
     Workload("llama7b_gate_up_t1", "q4k", "q4k_matmul", [(4096, 11008)] * 2, 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K gate and up projections as two GEMVs, weight-stream GB/s, Llama-2-7B "
-             "FFN (32 layers x 2 x 4096 -> 11008), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
+             "FFN (32 layers x 2 x 4096 -> 11008), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], distinct=1, arithmetic=T1_ARITH),
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "gemv_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
-             "batch 1", ["ternary_gemv.cu", "q4k_gemv.cu"], "ternary_t1_2560x6912.md",
+             "batch 1", ["ternary_gemv.cu", "q4k_gemv.cu", "t1_geometry.h"], "ternary_t1_2560x6912.md",
              arithmetic="fp32 activations rounded once to about 2^-22 of each 256-value block's maximum and split "
                         "into three byte planes; 2-bit fields x planes in int32 dp4a; fp32 combination, scale "
                         "applied once"),
@@ -140,10 +140,10 @@ WORKLOADS = {w.name: w for w in [
              "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),
     Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
-             "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu"], distinct=1, arithmetic=T1_ARITH),
+             "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], distinct=1, arithmetic=T1_ARITH),
     Workload("llama7b_decode_t4", "q4k", "q4k_matmul", LLAMA, 4, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers x "
-             "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv.cu", "q4k_gemv_multi.cu"], distinct=1,
+             "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv.cu", "t1_geometry.h", "q4k_gemv_multi.cu"], distinct=1,
              arithmetic=T1_ARITH + " (one token per compute warp; the 11008-wide down projection on the "
                                    "fp32 register-tile kernel)"),
     Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "alu",

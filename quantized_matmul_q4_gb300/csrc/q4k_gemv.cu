@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "sync.cuh"
+#include "t1_geometry.h"
 
 namespace q4mm {
 
@@ -430,7 +431,7 @@ struct T1Params {
 };
 
 constexpr int kT1RoleWarps = 1;  // the copy warp
-constexpr int kT1MaxCw = 16;     // compute warps at most
+static_assert(kPlaneSlabBytes == kT1PlaneSlabBytes, "plane layout of the kernel and its geometry");
 
 // kSwiGLU: the CTA's rows of W (gate) and then the same rows of W2 (up) form
 // one list of 2·nrows virtual rows through the same ring and passes; every
@@ -762,21 +763,8 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     }
 }
 
-// Geometry knobs of the one-token kernel (environment, read once): compute
-// warps per CTA, resident CTAs per SM, bytes per ring slot, ring budget.
-struct T1Tuning {
-    int warps = 16;
-    int ctas_per_sm = 1;
-    int stage_bytes = 16384;
-    int ring_bytes = 200 * 1024;
-    int pre_stages = 0;        // weight stages issued before the activation copy
-    int x_stage_max = 65536;   // bytes of x staged by a bulk copy (0: plain loads)
-    int l2_evict_first = 1;    // weight copies with the L2 evict_first policy
-    int max_grid = 0;          // CTAs per launch at most (0: no limit)
-    int spare_sms = 4;         // SMs left without a CTA of a short launch
-    int spare_max_bytes = 256 * 1024;  // "short": at most this many weight bytes per CTA
-};
-
+// Geometry knobs of the one-token kernel (T1Tuning, t1_geometry.h) from the
+// environment, read once; out-of-range values are clamped.
 int env_int(const char *name, int dflt, int lo, int hi) {
     const char *v = getenv(name);
     if (!v || !*v) return dflt;
@@ -802,17 +790,15 @@ const T1Tuning &t1_tuning() {
     return t;
 }
 
-int next_pow2(int v) {
-    int p = 1;
-    while (p < v) p <<= 1;
-    return p;
-}
-
 }  // namespace
 
 template <class Fmt, bool kSwiGLU = false>
 cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
                            const uint8_t *W2 = nullptr, float out_scale = 1.0f, int T = 1) {
+    const T1Tuning &tun = t1_tuning();
+    const T1Geometry g =
+        plan_gemv_t1(Fmt::kGroupBytes, K, N, T, kSwiGLU ? 2 : 1, c.num_sms, c.max_smem_optin, tun);
+    if (!g.ok) return cudaErrorNotSupported;
     T1Params p;
     p.T = T;
     p.x = x;
@@ -823,75 +809,17 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     p.status = c.status;
     p.N = N;
     p.nb = K / kQ4kValues;
-    const int row_bytes = p.nb * Fmt::kGroupBytes;
-    const int L = 4 * p.nb;  // slab lanes per row
-    const bool wide = L > 32;
-    const int wc = wide ? (L + 31) / 32 : 1;
-    const int pass_rows = wide ? 2 : 2 * (32 / next_pow2(max(L, 4)));
-    // At most kT1MaxCw compute warps (+1 copy warp): wider rows go to the
-    // generic kernel.
-    if (wc > kT1MaxCw) return cudaErrorNotSupported;
-    const T1Tuning &tun = t1_tuning();
-    // Each token gets warps / T compute warps: whole rows (wc warps each).
-    if (tun.warps / T < wc) return cudaErrorNotSupported;
-    p.rg = (tun.warps / T) / wc;
-    const int ncw = T * wc * p.rg;
-    // Stage: whole passes, at least stage_bytes of weights (bulk copies of
-    // 16 KB and more run at full HBM bandwidth).  A row size off the 16-byte
-    // grid (Q6_K) keeps CTA and stage boundaries on multiples of rq rows,
-    // the fewest whose bytes are a multiple of 16 (row_bytes = 2·odd·nb, so
-    // rq = 8 / gcd(nb, 8)).
-    int rq = 1;
-    if (row_bytes % 16) {
-        rq = 8;
-        while (rq > 1 && (rq / 2) * row_bytes % 16 == 0) rq /= 2;
-    }
-    const int sq = max(pass_rows, rq);  // both powers of two
-    p.stage_rows = sq * max(1, (tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
-
-    // Grid.  A CTA of the next launch on the stream can only start where a
-    // CTA of this one has exited, and one that starts after this launch has
-    // completed gets through its wait on it ~0.7 µs later than the CTAs
-    // already resident: with a CTA on every SM, the CTAs of each launch that
-    // start last also finish last and delay the next launch the same way.
-    // For a short launch (few weight bytes per CTA) leaving spare_sms SMs
-    // free lets every CTA of the next launch be resident before this one
-    // completes; a long launch keeps every SM for the weight stream.
-    int grid = tun.ctas_per_sm * c.num_sms;
-    const double cta_bytes = (double)(kSwiGLU ? 2 : 1) * N * row_bytes / grid;
-    if (cta_bytes <= tun.spare_max_bytes) grid = max(1, grid - tun.spare_sms);
-    if (tun.max_grid > 0) grid = min(grid, tun.max_grid);
-    p.rows_per_cta = (N + grid - 1) / grid;
-    p.rows_per_cta = (p.rows_per_cta + rq - 1) / rq * rq;
-    if (p.rows_per_cta < pass_rows) p.rows_per_cta = pass_rows;
-    if (p.stage_rows > p.rows_per_cta) p.stage_rows = sq * ((p.rows_per_cta + sq - 1) / sq);
-    grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
-    const size_t slot_bytes = (size_t)p.stage_rows * row_bytes;
-
-    const size_t TK = (size_t)T * K;
-    p.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
-    // Large rows at an 8-row stage quantum can leave no room for x: then
-    // the compute threads load x themselves.
-    if (p.x_staged && TK * sizeof(float) + 2 * slot_bytes + (TK / 64) * kPlaneSlabBytes >
-                          (size_t)c.max_smem_optin - 8192)
-        p.x_staged = 0;
-    const size_t xs_bytes = (TK / 64) * kPlaneSlabBytes + (TK / 32 + TK / 16) * sizeof(float) +
-                            (size_t)((T * p.nb * 4 + 15) & ~15) + (p.x_staged ? TK * sizeof(float) : 0);
-    const int vrows_per_cta = (kSwiGLU ? 2 : 1) * p.rows_per_cta;
-    const size_t part_bytes = (wide || kSwiGLU) ? (size_t)T * vrows_per_cta * wc * sizeof(float) : 0;
-    const size_t fixed = xs_bytes + part_bytes + 2 * 8 * sizeof(uint64_t);
-    const size_t budget = tun.ring_bytes;
-    int nslots = (int)((budget > fixed ? budget - fixed : 0) / slot_bytes);
-    const int stages_needed = (vrows_per_cta + p.stage_rows - 1) / p.stage_rows;
-    nslots = max(2, min(nslots, min(stages_needed, 8)));
-    p.nslots = nslots;
-    // With plain activation loads nothing needs to go out ahead of the rest.
-    p.pre_stages = p.x_staged ? tun.pre_stages : nslots;
+    p.rg = g.rg;
+    p.rows_per_cta = g.rows_per_cta;
+    p.stage_rows = g.stage_rows;
+    p.nslots = g.nslots;
+    p.pre_stages = g.pre_stages;
+    p.x_staged = g.x_staged;
     p.l2_evict_first = tun.l2_evict_first;
-    const size_t smem = xs_bytes + (size_t)nslots * slot_bytes + 2 * nslots * sizeof(uint64_t) + part_bytes;
-    if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
+    const int grid = g.grid;
+    const size_t smem = g.smem;
 
-    const dim3 block(32 * (kT1RoleWarps + ncw));
+    const dim3 block(32 * (kT1RoleWarps + g.ncw));
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e = ensure_smem(kernel, smem);
         if (e != cudaSuccess) return e;

@@ -1,0 +1,106 @@
+"""Launch geometry of the one-token GEMV kernel, checked on the CPU.
+
+The library's own host header (csrc/t1_geometry.h) is compiled into a small
+shim and called over many shapes; the invariants are re-derived here:
+every row belongs to one CTA, the ring fits shared memory, and every wait of
+a row group on a reused ring slot follows its own consumption of the slot's
+previous stage (the kernel waits on slot barriers by phase parity, which
+names the awaited stage only if the previous phase is known complete).
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+FIELDS = ["ok", "wide", "wc", "pass_rows", "rg", "ncw", "rq", "stage_rows", "rows_per_cta", "grid",
+          "x_staged", "nslots", "pre_stages", "xs_bytes", "part_bytes", "slot_bytes", "smem"]
+SMS, SMEM = 152, 232448  # GB300: SMs and opt-in shared memory per block
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    out = str(tmp_path_factory.mktemp("t1geo") / "libt1geo.so")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-o", out,
+                    os.path.join(HERE, "t1_geometry_shim.cpp")], check=True)
+    lib = ctypes.CDLL(out)
+    lib.t1_plan.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong)]
+
+    def call(group_bytes, K, N, T, vrow_mult=1):
+        buf = (ctypes.c_longlong * len(FIELDS))()
+        lib.t1_plan(group_bytes, K, N, T, vrow_mult, SMS, SMEM, buf)
+        return dict(zip(FIELDS, buf))
+    return call
+
+
+def _reuse_covered(g, vrow_mult):
+    """Every stage a row group waits on whose slot was used before holds a
+    stage that group consumed itself (simulated pass by pass)."""
+    pps = g["stage_rows"] // g["pass_rows"]
+    npasses = -(-vrow_mult * g["rows_per_cta"] // g["pass_rows"])
+    for r in range(g["rg"]):
+        seen = set()
+        for p in range(r, npasses, g["rg"]):
+            st = p // pps
+            if st >= g["nslots"] and st - g["nslots"] not in seen:
+                return False
+            seen.add(st)
+    return True
+
+
+FORMATS = {"q4k": (144, (1, 2, 3, 4)), "q4_0": (144, (1, 2, 8)), "q6k": (210, (1, 2, 8)),
+           "ternary": (64, (1, 2, 3))}
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS))
+def test_geometry_invariants(plan, fmt):
+    gb, Ts = FORMATS[fmt]
+    checked = 0
+    for K in range(256, 32768 + 1, 256):
+        for T in Ts:
+            for N in (1, 256, 4096, 11008, 32000):
+                for vm in ((1, 2) if fmt == "q4k" and T == 1 else (1,)):
+                    g = plan(gb, K, N, T, vm)
+                    if not g["ok"]:
+                        continue
+                    checked += 1
+                    rows, grid = g["rows_per_cta"], g["grid"]
+                    assert grid * rows >= N and (grid - 1) * rows < N, (K, N, T)
+                    assert 1 <= grid <= SMS
+                    assert rows % g["rq"] == 0 and g["stage_rows"] % g["pass_rows"] == 0
+                    assert g["stage_rows"] % g["rq"] == 0
+                    assert 2 <= g["nslots"] <= 8
+                    assert g["smem"] <= SMEM
+                    assert g["smem"] == g["xs_bytes"] + g["nslots"] * g["slot_bytes"] + \
+                        16 * g["nslots"] + g["part_bytes"]
+                    assert g["ncw"] == T * g["wc"] * g["rg"] <= 16
+                    assert _reuse_covered(g, vm), (fmt, K, N, T, vm, g)
+    assert checked > 500
+
+
+def test_known_geometries(plan):
+    # 4096²: 147 CTAs (4 SMs spare) of 28 rows, four 8-row stages, no reuse.
+    g = plan(144, 4096, 4096, 1)
+    assert (g["grid"], g["rows_per_cta"], g["stage_rows"], g["nslots"]) == (147, 28, 8, 4)
+    # 8192²: row groups take every second stage, so the ring depth is even (6, not 7).
+    g = plan(144, 8192, 8192, 1)
+    assert (g["rg"], g["stage_rows"] // g["pass_rows"], g["nslots"]) == (4, 2, 6)
+    # 16384²: a long launch keeps every SM.
+    g = plan(144, 16384, 16384, 1)
+    assert g["grid"] == 152
+    # Rows too wide for 16 compute warps, or too many tokens for the row width.
+    assert not plan(144, 33024, 64, 1)["ok"]
+    assert not plan(144, 11008, 64, 3)["ok"]
+
+
+def test_irregular_pass_patterns_take_fewer_row_groups(plan):
+    # 1792-wide rows at 32000 outputs (16 row groups, 9 passes per stage) and
+    # 5376-wide Q6_K rows (5 row groups, 4 passes per 8-row stage, rows in
+    # multiples of 8): no ring depth of two or more has every reuse covered
+    # by the waiting group itself, so fewer row groups take the rows.
+    for gb, K, N in ((144, 1792, 32000), (210, 5376, 6912)):
+        full = 16 // plan(gb, K, 64, 1)["wc"]
+        g = plan(gb, K, N, 1)
+        assert g["ok"] and g["rg"] < full, (K, N, g)
+        assert _reuse_covered(g, 1)
