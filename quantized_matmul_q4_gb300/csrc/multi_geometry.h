@@ -1,0 +1,51 @@
+// Launch geometry of the 2-8 token Q4_K GEMV kernel (q4k_gemv_multi.cu):
+// CTA rows and the weight ring.  Plain host C++ (no CUDA types), so that the
+// CPU tests compile this same header and check its invariants.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace q4mm {
+
+constexpr int kMultiWarps = 8;  // copy warp + 7 compute warps
+constexpr int kMultiCw = kMultiWarps - 1;
+constexpr int kMultiRows = 4;   // rows per group (one ring slot)
+
+struct MultiGeometry {
+    int ok = 0;            // 0: the ring does not fit shared memory
+    int grid = 0;
+    int rows_per_cta = 0;  // multiple of kMultiRows
+    int nslots = 0;        // ring depth (groups in flight)
+    int consumers = 0;     // compute warps that take groups: min(kMultiCw, nslots)
+    size_t smem = 0;       // dynamic shared memory per CTA
+};
+
+// ring_bytes: byte budget of the ring (200 KB unless a smaller one is asked for).
+inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes) {
+    MultiGeometry g;
+    const size_t row_bytes = (size_t)(K / 256) * 144;
+    const size_t slot_bytes = kMultiRows * row_bytes;
+    const int groups = (N + kMultiRows - 1) / kMultiRows;
+    const int grid = num_sms < groups ? num_sms : groups;
+    g.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
+    g.grid = (N + g.rows_per_cta - 1) / g.rows_per_cta;
+    const int cta_groups = g.rows_per_cta / kMultiRows;
+    // Ring: up to ring_bytes, at least two slots, never more slots than groups.
+    size_t fit = (size_t)ring_bytes / slot_bytes;
+    if (fit < 2) fit = 2;
+    int n = cta_groups < 16 ? cta_groups : 16;
+    if ((size_t)n > fit) n = (int)fit;
+    const int least = cta_groups < 2 ? cta_groups : 2;
+    if (n < least) n = least;
+    // Every slot has one consumer warp (see the kernel): from kMultiCw slots
+    // on, a multiple of kMultiCw; below that, one warp per slot.
+    if (n >= kMultiCw) n = n / kMultiCw * kMultiCw;
+    g.nslots = n;
+    g.consumers = n < kMultiCw ? n : kMultiCw;
+    g.smem = (size_t)n * slot_bytes + 2 * (size_t)n * sizeof(uint64_t);
+    g.ok = g.smem <= (size_t)max_smem_optin ? 1 : 0;
+    return g;
+}
+
+}  // namespace q4mm

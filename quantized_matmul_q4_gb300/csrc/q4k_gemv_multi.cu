@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "multi_geometry.h"
 #include "sync.cuh"
 
 namespace q4mm {
@@ -64,10 +65,6 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 // rows.  Each weight is dequantized once (scale'·(0.5 + q/256) − offset') and
 // multiplied into TT token accumulators, two positions per paired FMA.  A
 // butterfly over the 4·TT sums at the end of the group finishes the rows.
-
-constexpr int kMultiWarps = 8;                    // copy warp + 7 compute warps
-constexpr int kMultiCw = kMultiWarps - 1;
-constexpr int kMultiRows = 4;                     // rows per group (one ring slot)
 
 struct MultiParams {
     const float *x;
@@ -257,23 +254,14 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.N = N;
     p.T = T;
     p.nb = K / kQ4kValues;
-    const size_t row_bytes = (size_t)p.nb * kQ4kBytes;
-    const size_t slot_bytes = kMultiRows * row_bytes;
-    const int groups = (N + kMultiRows - 1) / kMultiRows;
-    int grid = min(c.num_sms, groups);
-    p.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
-    grid = (N + p.rows_per_cta - 1) / p.rows_per_cta;
-    const int cta_groups = p.rows_per_cta / kMultiRows;
-    // Ring: up to 200 KB (less if Q4MM_MULTI_RING_BYTES says so), at least
-    // two slots, never more slots than groups.
+    // Ring budget: 200 KB, less if Q4MM_MULTI_RING_BYTES says so.
     static const int ring_bytes = multi_env_int("Q4MM_MULTI_RING_BYTES", 200 * 1024, 8192, 200 * 1024);
-    p.nslots = (int)min((size_t)min(cta_groups, 16), max((size_t)2, (size_t)ring_bytes / slot_bytes));
-    p.nslots = max(p.nslots, min(cta_groups, 2));
-    // Every slot has one consumer warp (see the kernel): from kMultiCw slots
-    // on, a multiple of kMultiCw; below that, one warp per slot.
-    if (p.nslots >= kMultiCw) p.nslots = p.nslots / kMultiCw * kMultiCw;
-    const size_t smem = (size_t)p.nslots * slot_bytes + 2 * (size_t)p.nslots * sizeof(uint64_t);
-    if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
+    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, ring_bytes);
+    if (!g.ok) return cudaErrorNotSupported;
+    p.rows_per_cta = g.rows_per_cta;
+    p.nslots = g.nslots;
+    const int grid = g.grid;
+    const size_t smem = g.smem;
 
 #define Q4MM_MULTI_CASE(TT)                                                                    \
     {                                                                                          \

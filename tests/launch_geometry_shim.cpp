@@ -1,5 +1,7 @@
-// Host shim for the CPU tests: exposes the one-token kernel's launch
-// geometry (the library's own header, default tuning) through a C ABI.
+// Host shim for the CPU tests: exposes the launch geometry of the one-token
+// and the 2-8 token GEMV kernels (the library's own headers, default tuning)
+// through a C ABI.
+#include "../quantized_matmul_q4_gb300/csrc/multi_geometry.h"
 #include "../quantized_matmul_q4_gb300/csrc/t1_geometry.h"
 
 extern "C" int t1_plan(int group_bytes, int K, int N, int T, int vrow_mult, int num_sms, int max_smem,
@@ -10,6 +12,13 @@ extern "C" int t1_plan(int group_bytes, int K, int N, int T, int vrow_mult, int 
                            g.ncw,        g.rq,         g.stage_rows, g.rows_per_cta, g.grid,
                            g.x_staged,   g.nslots,     g.pre_stages, (long long)g.xs_bytes,
                            (long long)g.part_bytes, (long long)g.slot_bytes, (long long)g.smem};
+    for (int i = 0; i < (int)(sizeof(v) / sizeof(v[0])); ++i) out[i] = v[i];
+    return g.ok;
+}
+
+extern "C" int multi_plan(int K, int N, int num_sms, int max_smem, int ring_bytes, long long *out) {
+    const q4mm::MultiGeometry g = q4mm::plan_gemv_multi(K, N, num_sms, max_smem, ring_bytes);
+    const long long v[] = {g.ok, g.grid, g.rows_per_cta, g.nslots, g.consumers, (long long)g.smem};
     for (int i = 0; i < (int)(sizeof(v) / sizeof(v[0])); ++i) out[i] = v[i];
     return g.ok;
 }

@@ -1,11 +1,13 @@
-"""Launch geometry of the one-token GEMV kernel, checked on the CPU.
+"""Launch geometry of the one-token and the 2-8 token GEMV kernels, checked
+on the CPU.
 
-The library's own host header (csrc/t1_geometry.h) is compiled into a small
-shim and called over many shapes; the invariants are re-derived here:
-every row belongs to one CTA, the ring fits shared memory, and every wait of
-a row group on a reused ring slot follows its own consumption of the slot's
-previous stage (the kernel waits on slot barriers by phase parity, which
-names the awaited stage only if the previous phase is known complete).
+The library's own host headers (csrc/t1_geometry.h, csrc/multi_geometry.h)
+are compiled into a small shim and called over many shapes; the invariants
+are re-derived here: every row belongs to one CTA, the ring fits shared
+memory, and every wait on a reused ring slot follows the waiting warp's own
+consumption of the slot's previous contents (the kernels wait on slot
+barriers by phase parity, which names the awaited stage only if the previous
+phase is known to be complete).
 """
 import ctypes
 import os
@@ -19,13 +21,24 @@ FIELDS = ["ok", "wide", "wc", "pass_rows", "rg", "ncw", "rq", "stage_rows", "row
 SMS, SMEM = 152, 232448  # GB300: SMs and opt-in shared memory per block
 
 
+_LIB = []
+
+
+def _shim(tmp_path_factory):
+    if not _LIB:
+        out = str(tmp_path_factory.mktemp("geo") / "libgeo.so")
+        subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-o", out,
+                        os.path.join(HERE, "launch_geometry_shim.cpp")], check=True)
+        lib = ctypes.CDLL(out)
+        lib.t1_plan.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong)]
+        lib.multi_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_longlong)]
+        _LIB.append(lib)
+    return _LIB[0]
+
+
 @pytest.fixture(scope="module")
 def plan(tmp_path_factory):
-    out = str(tmp_path_factory.mktemp("t1geo") / "libt1geo.so")
-    subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-o", out,
-                    os.path.join(HERE, "t1_geometry_shim.cpp")], check=True)
-    lib = ctypes.CDLL(out)
-    lib.t1_plan.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong)]
+    lib = _shim(tmp_path_factory)
 
     def call(group_bytes, K, N, T, vrow_mult=1):
         buf = (ctypes.c_longlong * len(FIELDS))()
@@ -104,3 +117,55 @@ def test_irregular_pass_patterns_take_fewer_row_groups(plan):
         g = plan(gb, K, N, 1)
         assert g["ok"] and g["rg"] < full, (K, N, g)
         assert _reuse_covered(g, 1)
+
+
+MULTI = ["ok", "grid", "rows_per_cta", "nslots", "consumers", "smem"]
+
+
+@pytest.fixture(scope="module")
+def multi(tmp_path_factory):
+    lib = _shim(tmp_path_factory)
+
+    def call(K, N, ring_bytes=200 * 1024):
+        buf = (ctypes.c_longlong * len(MULTI))()
+        lib.multi_plan(K, N, SMS, SMEM, ring_bytes, buf)
+        return dict(zip(MULTI, buf))
+    return call
+
+
+def test_multi_token_ring_slots_have_one_consumer(multi):
+    # Compute warp c takes groups c, c + n, … (n consumers); the group in
+    # slot s is always taken by warp s mod n, and a warp meets its slot again
+    # exactly one ring lap later, so it has consumed the slot's previous
+    # group itself before it waits on the next.
+    checked = 0
+    for ring in (200 * 1024, 128 * 1024, 64 * 1024, 8192):
+        for K in range(256, 32768 + 1, 256):
+            for N in (1, 5, 100, 4096, 11008, 32000):
+                g = multi(K, N, ring)
+                if not g["ok"]:
+                    continue
+                checked += 1
+                n, c = g["nslots"], g["consumers"]
+                rows, grid = g["rows_per_cta"], g["grid"]
+                assert rows % 4 == 0 and grid * rows >= N and (grid - 1) * rows < N
+                assert g["smem"] <= SMEM and n >= 1
+                assert c == min(7, n) and n % c == 0
+                groups = rows // 4
+                owner, last = {}, {}
+                for grp in range(groups):
+                    slot, warp = grp % n, grp % c
+                    assert owner.setdefault(slot, warp) == warp, (K, N, ring, n)
+                    if slot in last:
+                        assert grp - last[slot] == n
+                    last[slot] = grp
+    assert checked > 1000
+
+
+def test_multi_token_known_geometries(multi):
+    # 14336-wide rows: six 32 KB slots fit, so six consumer warps, one each.
+    g = multi(14336, 4096)
+    assert (g["nslots"], g["consumers"]) == (6, 6)
+    # 4096 -> 11008: 19 groups per CTA, 16 slots would fit; 14 keep two per warp.
+    g = multi(4096, 11008)
+    assert (g["nslots"], g["consumers"]) == (14, 7)
