@@ -74,16 +74,21 @@ typedef enum {
  * x     : 16-byte aligned.  y: 4-byte aligned.
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_MAX_INPUT_DIM;
  *         outputDim >= 1; tokens >= 1.
- * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
- *         Up to 4 tokens: x is rounded once, to within 2^-15/127 (about
- *         2^-22) of each 256-value block's largest magnitude (exactly for
- *         integers below 2^21 and any value with at most 21 significant bits
- *         below the leading bit of that maximum) and split into
- *         three byte planes under a power-of-two block scale; the code-dots
- *         are exact integer sums, scales, mins and the combination are fp32.
- *         Where that kernel's geometry does not fit (2-4 tokens with a large
- *         inputDim), and above 4 tokens: fp32 dequantization and fp32 fused
- *         multiply-add.
+ * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|
+ *         on the pages' test inputs and on rows with a wide dynamic range
+ *         (activations of 1e5 next to ones of order 1, including on weights
+ *         that are zero).  The bound behind it, up to 4 tokens: each 32-value
+ *         group g of x is rounded once to a multiple of s_g·2^-23, s_g the
+ *         power of two just above max_g|x|/255, i.e. to within
+ *         max(2^-23·max_g|x|/255, 2^-127) (about 4.7e-10 of the group's
+ *         largest magnitude; values within a factor 255 of it are exact),
+ *         split into four byte planes, and the code-dots are exact integer
+ *         sums; so |y_o − y_exact,o| <= Σ_g 2^-23·max_g|x|/255·Σ_{k∈g}|w_ok|
+ *         plus fp32 rounding of the scales, mins and sums (relative 2^-22 or
+ *         so of each term).  A large activation changes only its own group's
+ *         grid.  Where that kernel's geometry does not fit (2-4 tokens with a
+ *         large inputDim), and above 4 tokens: fp32 dequantization and fp32
+ *         fused multiply-add.
  * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
  * 64 tokens above that).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
@@ -137,8 +142,9 @@ int q4k_matmul_tc(const float *x, const void *w_q4k, float *y, int inputDim, int
  *         row, as in Q4_K); outputDim >= 1; tokens >= 1.
  * Precision: as the one-token path of q4k_matmul: per token row,
  *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|, with x rounded once
- *         to within 2^-15/127 (about 2^-22) of each 256-value block's largest
- *         magnitude and integer code-dots.
+ *         to within 2^-23/255 of each 32-value group's largest magnitude and
+ *         the code-dots exact integer sums of (q − 8)·x̂, so a zero weight
+ *         (q = 8) adds nothing whatever its activation.
  * Tokens: up to 8 tokens share one pass over the weights (more tokens
  *         take one pass per 8).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
@@ -170,7 +176,8 @@ int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int ou
  *         outputDim >= 1; tokens >= 1 (up to 8 tokens per pass over the
  *         weights).
  * Precision: as the one-token path of q4k_matmul: per token row,
- *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|.
+ *         max_o |y − y_exact| <= 1e-4 · max_o |y_exact|; the code-dots are
+ *         exact integer sums of (q − 32)·x̂, so a zero weight adds nothing.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
  */
 int q6k_gemv(const float *x, const void *w_q6k, float *y, int inputDim, int outputDim, int tokens,
@@ -257,7 +264,10 @@ int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int input
  *         outputDim >= 1; tokens >= 1.
  * Precision: FP32.  The field value 3 decodes to +2 by the literal formula.
  *            With integer activations the code-dot is exact, so y equals
- *            the single fp32 rounding of scale × dot bit for bit.
+ *            the single fp32 rounding of scale × dot bit for bit.  Up to 3
+ *            tokens with inputDim a multiple of 256 (and W 16-byte aligned)
+ *            x is split as in q4k_matmul's one-token path and the code-dot
+ *            is an exact integer sum of code·x̂.
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
  */
 int ternary_gemv(const float *x, const void *w_packed, float scale, float *y, int inputDim,

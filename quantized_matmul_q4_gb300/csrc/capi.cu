@@ -1,6 +1,7 @@
 // C ABI of libq4mm.so: argument validation, dispatch to the kernels, error
 // reporting.  Declarations and the contract of every entry point are in
 // include/q4mm.h.
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -8,7 +9,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/q4mm.h"
+#include "q4mm.h"
 #include "kernels.h"
 
 namespace {
@@ -31,7 +32,9 @@ int fail_cuda(cudaError_t e, const char *what) {
 __device__ int g_device_status;
 
 struct DeviceInfo {
-    bool ready = false;
+    // Set (release) after the other fields are filled; read (acquire) without
+    // the lock, so a thread that sees it set also sees those fields.
+    std::atomic<bool> ready{false};
     int num_sms = 0;
     int max_smem_optin = 0;
     int *status = nullptr;
@@ -41,46 +44,32 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-bool pdl_enabled() {
-    static const bool on = [] {
-        const char *v = getenv("Q4MM_PDL");
-        return !(v && v[0] == '0');
-    }();
-    return on;
-}
-
 int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(Q4MM_ERR_CUDA, "device ordinal %d out of range", dev);
     DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_dev_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
             e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
             if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(shared memory)");
             e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
             if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     ctx->stream = reinterpret_cast<cudaStream_t>(stream);
     ctx->num_sms = d.num_sms;
     ctx->max_smem_optin = d.max_smem_optin;
     ctx->status = d.status;
-    ctx->pdl = pdl_enabled();
+    // Programmatic dependent launch: a kernel may start its weight stream
+    // while the previous kernel on the stream finishes.
+    ctx->pdl = true;
     return Q4MM_OK;
-}
-
-bool multi_fp32_forced() {
-    static const bool on = [] {
-        const char *v = getenv("Q4MM_MULTI");
-        return v && v[0] == 'f';
-    }();
-    return on;
 }
 
 // Runs a one-token-kernel launcher over the tokens in chunks of up to 8,
@@ -147,6 +136,10 @@ cudaError_t ensure_smem_limit(const void *kernel, size_t bytes) {
         if (table[i].dev == dev && table[i].fn == kernel && table[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
+    // The largest shared-memory configuration of the SM: kernels that pair a
+    // CTA of the next launch with one of the current launch need both to fit.
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     for (int i = 0; i < used; ++i)
         if (table[i].dev == dev && table[i].fn == kernel) {
             table[i].bytes = bytes;
@@ -175,10 +168,9 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
     } else if (tokens <= 8) {
         // Up to 4 tokens: the byte-plane kernel with one token per compute
         // warp where its geometry allows (measured 1.4-1.9x faster at 2 and
-        // 4 tokens; at 8 tokens the FP32 kernel is faster on 4096x4096);
-        // Q4MM_MULTI=fp32 forces the FP32 kernel.  Then the FP32
-        // register-tile kernel, then the prefill kernel.
-        e = (multi_fp32_forced() || tokens > 4)
+        // 4 tokens; at 8 tokens the FP32 kernel is faster on 4096x4096).
+        // Then the FP32 register-tile kernel, then the prefill kernel.
+        e = tokens > 4
                 ? cudaErrorNotSupported
                 : q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim, tokens);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);

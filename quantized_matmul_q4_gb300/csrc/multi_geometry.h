@@ -11,6 +11,7 @@ namespace q4mm {
 constexpr int kMultiWarps = 8;  // copy warp + 7 compute warps
 constexpr int kMultiCw = kMultiWarps - 1;
 constexpr int kMultiRows = 4;   // rows per group (one ring slot)
+constexpr int kMultiRingBytes = 200 * 1024;  // ring budget the library launches with
 
 struct MultiGeometry {
     int ok = 0;            // 0: the ring does not fit shared memory
@@ -21,7 +22,8 @@ struct MultiGeometry {
     size_t smem = 0;       // dynamic shared memory per CTA
 };
 
-// ring_bytes: byte budget of the ring (200 KB unless a smaller one is asked for).
+// ring_bytes: byte budget of the ring (the library passes kMultiRingBytes; the
+// CPU tests also check smaller budgets).
 inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes) {
     MultiGeometry g;
     const size_t row_bytes = (size_t)(K / 256) * 144;

@@ -15,9 +15,7 @@
 // visits, so the 64 matching activations live in its registers (as exact
 // byte planes) for the whole kernel.  Weight rows are streamed once from HBM
 // into a shared-memory ring by 1-D bulk copies (cp.async.bulk) that one
-// producer thread issues right after the activation copy.  The 2..8 token
-// kernel is in q4k_gemv_multi.cu.
-#include <cstdlib>
+// producer thread issues.  The 2..8 token kernel is in q4k_gemv_multi.cu.
 #include <type_traits>
 #include <utility>
 
@@ -31,19 +29,19 @@ namespace q4mm {
 namespace {
 
 // ----------------------------------------------------------------------------
-// One token: bulk-copied rows, slab lanes, exact int8 activation planes
+// One token: bulk-copied rows, slab lanes, byte planes of the activations
 // ----------------------------------------------------------------------------
 //
 // Roles in a CTA (a contiguous range of output rows):
 //  * warp 0, lane 0 streams the rows into a shared-memory ring with 1-D bulk
-//    copies of whole stages.  It first waits for the previous kernel on the
-//    stream (which may write x), copies x into shared memory with one bulk
-//    copy, and only then issues the weight stages: an activation fetch that
-//    queues behind the CTA's weight stream arrives late, and everything after
-//    it (plane split, code-dots) waits for it, while the weights have the
-//    plane split's time to land.  (pre_stages > 0 sends that many stages
-//    ahead of the wait instead; measured slower on GB300.)  Above 64 KB of x
-//    the compute threads load x themselves and all stages go out first;
+//    copies of whole stages.  Weights are never written by an earlier kernel
+//    on the stream, so in the paired form (every stage of the CTA fits the
+//    ring) all stages go out before the wait on the previous kernel, while
+//    that kernel still computes on the same SM; then x is copied in with one
+//    bulk copy.  In the solo form x is copied first and the stages follow
+//    (an activation fetch queued behind the CTA's own weight stream arrives
+//    late, and everything after it waits for it).  Above 64 KB of x the
+//    compute threads load x themselves and the ring's stages go out first;
 //  * the other warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j
 //    of block b of every row it visits (32 low nibbles of sub-block 2j, 32
 //    high nibbles of 2j+1) and decodes the two 6-bit scale/min pairs it needs
@@ -51,20 +49,24 @@ namespace {
 //    CTA, so different warps work on different stages at once.
 //
 // The code-dot Σ x·q of a sub-block runs on integer dot-product instructions
-// (four byte products per instruction).  Each 256-value block of x is split,
-// once per CTA, into three byte planes under a power-of-two block scale s_b:
-//   n = rint(x·2^15/s_b),  |n| < 127·2^15 < 2^22,
-//   n = 65536·p2 + 256·p1 + p0  (p0, p1 unsigned bytes, p2 a signed byte),
-// so x = s_b·2^-15·n + e with |e| ≤ 2^-16·s_b ≤ 2^-15·max|x_b|/127 (s_b is at
-// most 2·max|x_b|/127; the bound is about 2.4e-7·max|x_b|).  The rounding is a
-// single FMA against the 1.5·2^23 shifter (the product by a power of two is
-// exact), whose low bytes are the digits of n; the grid step 2^-15·s_b is at
-// most 2^-20 of the leading power of two of max|x_b|, so activations with at
-// most 21 significant bits below that leading bit (integers below 2^21
-// included) are represented exactly.  Low-nibble codes enter the dot products as they are;
-// high-nibble codes enter as 16·q (the byte masked in place, no shift) and
-// the factor 16 is taken out of that sub-block's scale.  The integer sums are
-// exact; scales, mins and the final combination are fp32.
+// (four byte products per instruction).  Each 32-value group g of x is split,
+// once per CTA, into P = kT1Planes byte planes under a power-of-two scale
+// s_g = 2^e ≥ max|x_g|/255 (so s_g < 2·max|x_g|/255), with S = 8P − 9:
+//   n = rint(x·2^S/s_g),  |n| < 255·2^S < 2^(8P−1),
+//   n = Σ_p 2^(8p)·d_p  (the low digits unsigned bytes, the top one signed),
+// so x = s_g·2^-S·n + e with |e| ≤ 2^-(S+1)·s_g < 2^-S·max|x_g|/255 (s_g is
+// at least 2^(S−126), so groups below 255·2^(S−126) have |e| ≤ 2^-127
+// instead).  The product by a power of two is exact and the conversion
+// rounds once; every x_g value of magnitude at least s_g (within a factor of
+// about 255 of the group's largest) is represented exactly, and only smaller
+// ones carry the error above.  A group's scale depends on its own 32 values
+// only, so a large activation elsewhere in the row changes nothing here.
+// Q4_K codes enter the dot products unsigned (high nibbles masked in place as
+// 16·q, the factor taken out of the sub-block's scale) and the min term uses
+// the fp32 group sums; formats whose zero point is a fixed code (Q4_0, Q6_K,
+// ternary) enter as signed bytes c − zero, so their sums are exact integers.
+// The planes' sums are combined with two fp32 roundings, and scales, mins
+// and the final sum are fp32.
 // kNB (blocks per row) is a template constant for common widths so that row
 // and stage address arithmetic folds at compile time; 0 reads it at run time.
 
@@ -116,131 +118,150 @@ __device__ __forceinline__ RowScales row_scales(uint4 h, const LaneScaleSel &L) 
     return r;
 }
 
-// d = c + Σ a_i·b_i with a as four unsigned bytes and b as four signed bytes.
-__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
-    int d;
-    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// d = c + Σ a_i·b_i with a and b as four unsigned bytes each.
+// d = c + Σ a_i·b_i over four byte pairs; a (the codes) and b (a plane)
+// each unsigned (u) or signed (s).
 __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
     int d;
     asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
-// Integer code-dots of one slab against the three activation planes:
-// d_lo[p] = Σ_l q_lo(l)·plane_p[l], d_hi[p] = 16·Σ_l q_hi(l)·plane_p[32 + l]
-// (planes 0 and 1 unsigned, plane 2 signed).  Slab byte l pairs with plane
-// byte l of the low 32 positions (words 0..7) and with plane byte l of the
-// high 32 positions (words 8..15).  |d| < 2^21.
-__device__ __forceinline__ void slab_dot_planes(const int (&pl)[3][16], uint4 q0, uint4 q1,
-                                                int (&d_lo)[3], int (&d_hi)[3]) {
-    const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+// Activation planes of one lane: kT1Planes planes of 16 words (the lane's 64
+// values, four per word); the last plane holds signed bytes.
+using Planes = int[kT1Planes][16];
+using Acc = int[kT1Planes];
+
+// Four code bytes (four values) against word w of every plane.  kSigned:
+// the codes are signed bytes (formats whose zero point is a fixed code).
+template <bool kSigned = false>
+__device__ __forceinline__ void dot4(uint32_t codes, const Planes &pl, int w, Acc &d) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t l4 = qw[w] & 0x0F0F0F0Fu;
-        const uint32_t h4 = qw[w] & 0xF0F0F0F0u;
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-            d_lo[pp] = dp4a_uu(l4, (uint32_t)pl[pp][w], d_lo[pp]);
-            d_hi[pp] = dp4a_uu(h4, (uint32_t)pl[pp][8 + w], d_hi[pp]);
-        }
-        d_lo[2] = dp4a_us(l4, pl[2][w], d_lo[2]);
-        d_hi[2] = dp4a_us(h4, pl[2][8 + w], d_hi[2]);
-    }
+    for (int p = 0; p + 1 < kT1Planes; ++p)
+        d[p] = kSigned ? dp4a_su(codes, (uint32_t)pl[p][w], d[p]) : dp4a_uu(codes, (uint32_t)pl[p][w], d[p]);
+    constexpr int t = kT1Planes - 1;
+    d[t] = kSigned ? dp4a_ss(codes, (uint32_t)pl[t][w], d[t]) : dp4a_us(codes, (uint32_t)pl[t][w], d[t]);
 }
 
-// 65536·d2 + 256·d1 + d0, i.e. Σ q·x in units of s_b·2^-15: the last two
-// terms are an exact integer (|·| < 2^29), the sum takes one rounding.
-__device__ __forceinline__ float plane_combine(const int (&d)[3]) {
-    const int d01 = d[1] * 256 + d[0];
-    return fmaf(static_cast<float>(d[2]), 65536.0f, static_cast<float>(d01));
+// Σ c·n in units of the group's step: Σ_p 2^(8p)·d_p, as 2^16·hi + lo with
+// hi = 256·d3 + d2 (four planes) or d2 (three) and lo = 256·d1 + d0.  For
+// the 4-bit and 2-bit codes hi has at most 24 significant bits (times a
+// power of two when the codes carry one), so its conversion is exact; lo
+// takes one rounding, the sum another (Q6_K's 6-bit codes over 16 values can
+// take hi to 25 bits: one more rounding there).
+__device__ __forceinline__ float plane_combine(const Acc &d) {
+    const int hi = kT1Planes == 4 ? d[kT1Planes - 1] * 256 + d[2] : d[2];
+    const int lo = d[1] * 256 + d[0];
+    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
 }
 
-// One row's contribution from one slab lane: scales, code-dots (times the
-// plane unit s_b·2^-15, a power of two), lazy mins.
-__device__ __forceinline__ float slab_row(const uint8_t *blk, int j, const LaneScaleSel &L, float unit,
-                                          const int (&pl)[3][16], float sum_lo, float sum_hi) {
-    const uint4 h = *reinterpret_cast<const uint4 *>(blk);
-    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
-    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
-    const RowScales r = row_scales(h, L);
-    int dl[3] = {0, 0, 0}, dh[3] = {0, 0, 0};
-    slab_dot_planes(pl, q0, q1, dl, dh);
-    return fmaf(unit, fmaf(r.s0, plane_combine(dl), r.s1 * plane_combine(dh)),
-                -fmaf(r.o0, sum_lo, r.o1 * sum_hi));
-}
+// The plane split's scale: n = rint(x·2^kShift/s_g) fills 8·kT1Planes − 1 bits.
+constexpr int kShift = 8 * kT1Planes - 9;
 
-// Row formats of the one-token kernel.  Both spend 144 bytes on every 256
+// Row formats of the one-token kernel.  Each spends group_bytes on every 256
 // values of a row, so rows, stages and slab lanes have the same geometry;
-// lane (b, j) covers values 64j..64j+63 of the 256-value group b, and
-// row() returns that lane's share of one row, given the group's first byte.
+// lane (b, j) covers values 64j..64j+63 of the 256-value group b (Q6_K
+// interleaves, see its unit_of), and row() returns that lane's share of one
+// row, given the group's first byte.
 
 // Q4_K: the group is one super-block; the lane reads the header and qs slab j.
 struct FmtQ4K {
     static constexpr int kGroupBytes = 144;  // bytes per 256 values of a row
-    __device__ static void prep_planes(int (&)[3][16]) {}
+    static constexpr bool kSums = true;      // needs Σx per 32-value group (the min term)
+    __device__ static void prep_planes(Planes &) {}
     struct Lane {
         LaneScaleSel sel;
         int j;
+        float u_lo, u_hi, s_lo, s_hi;
     };
     __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
-    __device__ static Lane lane(int j, const float *) { return Lane{lane_scale_sel(j), j}; }
-    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
-                                float sum_lo, float sum_hi) {
-        return slab_row(grp, L.j, L.sel, unit, pl, sum_lo, sum_hi);
+    // u32 / sx32 point at block b's first entries (8 groups of 32 per block).
+    __device__ static Lane lane(int j, const float *u32, const float *sx32) {
+        Lane L;
+        L.sel = lane_scale_sel(j);
+        L.j = j;
+        L.u_lo = u32[2 * j];
+        L.u_hi = u32[2 * j + 1];
+        L.s_lo = sx32[2 * j];
+        L.s_hi = sx32[2 * j + 1];
+        return L;
+    }
+    __device__ static float row(const uint8_t *blk, const Lane &L, const Planes &pl) {
+        const uint4 h = *reinterpret_cast<const uint4 *>(blk);
+        const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * L.j);
+        const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * L.j);
+        const RowScales r = row_scales(h, L.sel);
+        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // Slab byte l pairs with plane byte l of the low 32 positions (words
+        // 0..7) and with plane byte l of the high 32 positions (words 8..15).
+        Acc dl = {}, dh = {};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            dot4(qw[w] & 0x0F0F0F0Fu, pl, w, dl);
+            dot4(qw[w] & 0xF0F0F0F0u, pl, 8 + w, dh);
+        }
+        return fmaf(r.s0 * L.u_lo, plane_combine(dl), (r.s1 * L.u_hi) * plane_combine(dh)) -
+               fmaf(r.o0, L.s_lo, r.o1 * L.s_hi);
     }
 };
 
 // Q4_0: the group is eight 18-byte blocks; the lane's 64 values are blocks
 // 2j and 2j+1 (bytes 36j..36j+35, 4-byte aligned): block A = values 0..31
 // (its 16 qs bytes start 2 bytes in, so its words come out of funnel shifts),
-// block B = values 32..63 (qs 4-byte aligned at byte 20).  Per block,
-// Σ w·x = d·(Σ q·x − 8·Σ x).
+// block B = values 32..63 (qs 4-byte aligned at byte 20).  The zero point is
+// the code 8 (w = d·(q − 8)), so the codes enter the dot products as the
+// signed bytes 16·(q − 8) — a nibble in a byte's high half XOR 0x80 — and the
+// block's sum Σ 16·(q − 8)·n is an exact integer: a zero weight adds nothing,
+// whatever its activation.
 struct FmtQ40 {
     static constexpr int kGroupBytes = 144;
-    __device__ static void prep_planes(int (&)[3][16]) {}
+    static constexpr bool kSums = false;
+    __device__ static void prep_planes(Planes &) {}
     struct Lane {
         int j;
+        float u16_a, u16_b;  // the steps of blocks A and B, over 16 (the codes carry 16)
     };
     __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
-    __device__ static Lane lane(int j, const float *) { return Lane{j}; }
-    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
-                                float sum_lo, float sum_hi) {
+    __device__ static Lane lane(int j, const float *u32, const float *) {
+        Lane L;
+        L.j = j;
+        L.u16_a = u32[2 * j] * 0.0625f;
+        L.u16_b = u32[2 * j + 1] * 0.0625f;
+        return L;
+    }
+    __device__ static float row(const uint8_t *grp, const Lane &L, const Planes &pl) {
         const uint32_t *p = reinterpret_cast<const uint32_t *>(grp + 36 * L.j);
         uint32_t w[9];
 #pragma unroll
         for (int i = 0; i < 9; ++i) w[i] = p[i];
         const float2 dd = __half22float2(__halves2half2(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)),
                                                         __ushort_as_half((unsigned short)(w[4] >> 16))));
-        uint32_t qa[4], qb[4];
+        // Low nibbles (values 0..15 of a block) shifted into the high half,
+        // high nibbles (values 16..31) masked in place.
+        Acc a = {}, b = {};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            qa[k] = __funnelshift_r(w[k], w[k + 1], 16);
-            qb[k] = w[5 + k];
+            const uint32_t qa = __funnelshift_r(w[k], w[k + 1], 16), qb = w[5 + k];
+            dot4<true>(((qa << 4) & 0xF0F0F0F0u) ^ 0x80808080u, pl, k, a);
+            dot4<true>((qa & 0xF0F0F0F0u) ^ 0x80808080u, pl, 4 + k, a);
+            dot4<true>(((qb << 4) & 0xF0F0F0F0u) ^ 0x80808080u, pl, 8 + k, b);
+            dot4<true>((qb & 0xF0F0F0F0u) ^ 0x80808080u, pl, 12 + k, b);
         }
-        int da_lo[3] = {0, 0, 0}, da_hi[3] = {0, 0, 0}, db_lo[3] = {0, 0, 0}, db_hi[3] = {0, 0, 0};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t al = qa[k] & 0x0F0F0F0Fu, ah = qa[k] & 0xF0F0F0F0u;
-            const uint32_t bl = qb[k] & 0x0F0F0F0Fu, bh = qb[k] & 0xF0F0F0F0u;
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-                da_lo[pp] = dp4a_uu(al, (uint32_t)pl[pp][k], da_lo[pp]);
-                da_hi[pp] = dp4a_uu(ah, (uint32_t)pl[pp][4 + k], da_hi[pp]);
-                db_lo[pp] = dp4a_uu(bl, (uint32_t)pl[pp][8 + k], db_lo[pp]);
-                db_hi[pp] = dp4a_uu(bh, (uint32_t)pl[pp][12 + k], db_hi[pp]);
-            }
-            da_lo[2] = dp4a_us(al, pl[2][k], da_lo[2]);
-            da_hi[2] = dp4a_us(ah, pl[2][4 + k], da_hi[2]);
-            db_lo[2] = dp4a_us(bl, pl[2][8 + k], db_lo[2]);
-            db_hi[2] = dp4a_us(bh, pl[2][12 + k], db_hi[2]);
-        }
-        const float qa_x = fmaf(plane_combine(da_hi), 0.0625f, plane_combine(da_lo));
-        const float qb_x = fmaf(plane_combine(db_hi), 0.0625f, plane_combine(db_lo));
-        return fmaf(dd.x, fmaf(unit, qa_x, -8.0f * sum_lo), dd.y * fmaf(unit, qb_x, -8.0f * sum_hi));
+        return fmaf(dd.x * L.u16_a, plane_combine(a), (dd.y * L.u16_b) * plane_combine(b));
     }
 };
 
@@ -255,9 +276,10 @@ struct FmtQ40 {
 // the scale is applied after the dot (T1Params::out_scale).
 struct FmtTern {
     static constexpr int kGroupBytes = 64;
-    __device__ static void prep_planes(int (&pl)[3][16]) {
+    static constexpr bool kSums = false;
+    __device__ static void prep_planes(Planes &pl) {
 #pragma unroll
-        for (int pp = 0; pp < 3; ++pp)
+        for (int pp = 0; pp < kT1Planes; ++pp)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const uint32_t i0 = (uint32_t)pl[pp][4 * w], i1 = (uint32_t)pl[pp][4 * w + 1];
@@ -272,25 +294,34 @@ struct FmtTern {
     }
     struct Lane {
         int j;
+        float u_lo, u_hi;
     };
     __device__ static void unit_of(int j, int i, int &slab, int &pos) { slab = j, pos = i; }
-    __device__ static Lane lane(int j, const float *) { return Lane{j}; }
-    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16],
-                                float sum_lo, float sum_hi) {
+    __device__ static Lane lane(int j, const float *u32, const float *) {
+        Lane L;
+        L.j = j;
+        L.u_lo = u32[2 * j];
+        L.u_hi = u32[2 * j + 1];
+        return L;
+    }
+    __device__ static float row(const uint8_t *grp, const Lane &L, const Planes &pl) {
         const uint4 q = *reinterpret_cast<const uint4 *>(grp + 16 * L.j);
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-        int d[3] = {0, 0, 0};
+        // Words 0, 1 hold values 0..31 (the low group), words 2, 3 values 32..63.
+        // Each field f becomes the signed byte f − 1 (a bytewise subtraction
+        // with no borrow between bytes: bit 7 set first, then cleared), so
+        // the code-dot is an exact integer and a zero code adds nothing.
+        Acc dl = {}, dh = {};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t f = (qw[w] >> (2 * i)) & 0x03030303u;
-                d[0] = dp4a_uu(f, (uint32_t)pl[0][4 * w + i], d[0]);
-                d[1] = dp4a_uu(f, (uint32_t)pl[1][4 * w + i], d[1]);
-                d[2] = dp4a_us(f, pl[2][4 * w + i], d[2]);
+                const uint32_t f = ((qw[w] >> (2 * i)) & 0x03030303u) | 0x80808080u;
+                const uint32_t c = (f - 0x01010101u) ^ 0x80808080u;
+                dot4<true>(c, pl, 4 * w + i, w < 2 ? dl : dh);
             }
         }
-        return fmaf(unit, plane_combine(d), -(sum_lo + sum_hi));
+        return fmaf(L.u_lo, plane_combine(dl), L.u_hi * plane_combine(dh));
     }
 };
 
@@ -300,25 +331,27 @@ struct FmtTern {
 // sub-block scales, fp16 d last; w = d·scale·(q − 32).  Lane j = 2n + h takes,
 // in half n, the values 128n + 32g + 16h + l for g = 0..3 and l < 16: bytes
 // 16h..16h+15 of the runs ql[64n..], ql[64n + 32..] and qh[32n..], one
-// sub-block (and scale) per g.  Blocks start at any even byte, so every
-// 16-byte run is read as five aligned words and funnel-shifted.
+// sub-block (and scale) per g, each run in 32-value group 4n + g of the
+// block.  Blocks start at any even byte, so every 16-byte run is read as
+// five aligned words and funnel-shifted.
 struct FmtQ6K {
     static constexpr int kGroupBytes = 210;
-    __device__ static void prep_planes(int (&)[3][16]) {}
+    static constexpr bool kSums = false;
+    __device__ static void prep_planes(Planes &) {}
     __device__ static void unit_of(int j, int i, int &slab, int &pos) {
         slab = 2 * (j >> 1) + (i >> 1);
         pos = 2 * (i & 1) + (j & 1);
     }
     struct Lane {
         int n, h;
-        float s16[4];  // Σ x over each of the lane's four 16-value sub-blocks
+        float u4[4];  // per run g: the step of its 32-value group, over 4 (the codes carry 4)
     };
-    __device__ static Lane lane(int j, const float *bsx16) {
+    __device__ static Lane lane(int j, const float *u32, const float *) {
         Lane L;
         L.n = j >> 1;
         L.h = j & 1;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) L.s16[g] = bsx16[8 * L.n + 2 * g + L.h];
+        for (int g = 0; g < 4; ++g) L.u4[g] = u32[4 * L.n + g] * 0.25f;
         return L;
     }
     // Four words starting `off` bytes after the 4-byte aligned `base`, shifted
@@ -331,8 +364,7 @@ struct FmtQ6K {
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], sh);
     }
-    __device__ static float row(const uint8_t *grp, const Lane &L, float unit, const int (&pl)[3][16], float,
-                                float) {
+    __device__ static float row(const uint8_t *grp, const Lane &L, const Planes &pl) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(grp);
         const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
         const uint32_t sh = (uint32_t)(a & 3) * 8;
@@ -348,28 +380,24 @@ struct FmtQ6K {
         // by one XOR and one byte permute, minus 2^23 + 128 (exact: both are
         // integers below 2^24), times d (exact: 11 × 8 significant bits).
         const uint32_t s0 = (L.n ? sw[2] : sw[0]) ^ 0x80808080u, s1 = (L.n ? sw[3] : sw[1]) ^ 0x80808080u;
-        float sc[4];
+        float acc = 0.f;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const uint32_t word = g < 2 ? s0 : s1;
             const uint32_t sel = 0x7440u | (uint32_t)(L.h + 2 * (g & 1));
-            sc[g] = d * (__uint_as_float(__byte_perm(word, 0x4B000000u, sel)) - 8388736.0f);
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            int dd[3] = {0, 0, 0};
+            const float sc = d * (__uint_as_float(__byte_perm(word, 0x4B000000u, sel)) - 8388736.0f);
+            // The zero point is the code 32: codes enter as the signed bytes
+            // 4·(q − 32), i.e. 4·q XOR 0x80, and the sum is an exact integer.
+            Acc dd = {};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint32_t src = (g & 1) ? qb[k] : qa[k];
-                const uint32_t lo = (g & 2) ? ((src >> 4) & 0x0F0F0F0Fu) : (src & 0x0F0F0F0Fu);
-                const uint32_t hs = g == 0 ? (qh[k] << 4) : g == 1 ? (qh[k] << 2) : g == 2 ? qh[k] : (qh[k] >> 2);
-                const uint32_t code = (hs & 0x30303030u) | lo;  // 6-bit codes, four bytes
-                dd[0] = dp4a_uu(code, (uint32_t)pl[0][4 * g + k], dd[0]);
-                dd[1] = dp4a_uu(code, (uint32_t)pl[1][4 * g + k], dd[1]);
-                dd[2] = dp4a_us(code, pl[2][4 * g + k], dd[2]);
+                const uint32_t lo = (g & 2) ? ((src >> 2) & 0x3C3C3C3Cu) : ((src << 2) & 0x3C3C3C3Cu);
+                const uint32_t hs = g == 0 ? (qh[k] << 6) : g == 1 ? (qh[k] << 4) : g == 2 ? (qh[k] << 2) : qh[k];
+                const uint32_t code4 = ((hs & 0xC0C0C0C0u) | lo) ^ 0x80808080u;  // 4·(q − 32), four bytes
+                dot4<true>(code4, pl, 4 * g + k, dd);
             }
-            acc = fmaf(sc[g], fmaf(unit, plane_combine(dd), -32.0f * L.s16[g]), acc);
+            acc = fmaf(sc * L.u4[g], plane_combine(dd), acc);
         }
         return acc;
     }
@@ -401,15 +429,10 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gm
         : "memory");
 }
 
-// Round to nearest (ties to even) for |v| < 2^22 with the 1.5·2^23 shifter:
-// the float's bits are 0x4B400000 + rint(v).
-constexpr float kShifter = 12582912.0f;
-constexpr uint32_t kShifterBits = 0x4B400000u;
-
-// Bytes per 64-value slab in the plane area: 12 units of 16 bytes (3 planes
-// × 4 quarters) plus 16 bytes of padding, so that the eight slabs read by a
-// quarter warp start in eight different bank groups.
-constexpr int kPlaneSlabBytes = 208;
+// Bytes per 64-value slab in the plane area: 4·kT1Planes units of 16 bytes
+// (planes × quarters) plus 16 bytes of padding, so that the eight slabs read
+// by a quarter warp start in eight different bank groups.
+constexpr int kPlaneSlabBytes = 64 * kT1Planes + 16;
 
 struct T1Params {
     const float *x;
@@ -422,6 +445,7 @@ struct T1Params {
     int rg;            // row groups: compute warps = wc·rg
     int rows_per_cta;  // contiguous rows per CTA
     int stage_rows;    // rows per ring slot (multiple of the pass size)
+    int slot_bytes;    // bytes per ring slot (16 more when rows are off the 16-byte grid)
     int nslots;        // ring depth
     int pre_stages;    // stages issued before the wait on the previous kernel
     int x_staged;      // 1: x arrives by one bulk copy into shared memory
@@ -430,14 +454,113 @@ struct T1Params {
     int l2_evict_first;  // 1: weight copies carry the L2 evict_first policy
 };
 
-constexpr int kT1RoleWarps = 1;  // the copy warp
-static_assert(kPlaneSlabBytes == kT1PlaneSlabBytes, "plane layout of the kernel and its geometry");
+// Split of x into planes, group steps and (kSums) group sums, by every
+// compute thread: thread ct takes 16 consecutive values of x [T][K] per
+// step; the two threads of a 32-value group are neighbouring lanes and share
+// its maximum.
+template <bool kSums>
+__device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int nth, volatile int &abort_flag,
+                                        uint8_t *planes, float *u32, float *sx32) {
+    const int n16 = TK / 16;
+    for (int i0 = 0; i0 < n16; i0 += nth) {
+        const int i = i0 + ct;
+        const bool on = i < n16 && !abort_flag;
+        float v[16];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 4 * i;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 t = on ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[4 * k] = t.x;
+                v[4 * k + 1] = t.y;
+                v[4 * k + 2] = t.z;
+                v[4 * k + 3] = t.w;
+            }
+        }
+        float amax = 0.f, sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            amax = fmaxf(amax, fabsf(v[k]));
+            if (kSums) sum += v[k];
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        if (kSums) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        // s_g = 2^ex with amax / 2^ex < 255 (1 when the group is zero): ex is
+        // the binary exponent of amax/255 written as m·2^ex with m in [0.5, 1),
+        // read from the float's exponent field.  The lower bound kShift − 126
+        // keeps both 2^(kShift-ex) and the step 2^(ex-kShift) normal floats
+        // (such groups still scale below 255).  A product amax·(1/255) rounded
+        // down across a power of two gives ex one too small and |n| at most
+        // 255·2^kShift·(1 + 2^-23), still inside the planes.
+        const int ebits = (int)(__float_as_uint(amax * (1.0f / 255.0f)) >> 23);
+        const int ex = amax > 0.f ? max(ebits - 126, kShift - 126) : 0;
+        const float mul = __uint_as_float((uint32_t)(127 + kShift - ex) << 23);  // 2^(kShift-ex)
+        int n[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) n[k] = __float2int_rn(v[k] * mul);
+        if (on) {
+            // Slab-major layout: slab S = i/4 holds 4·kT1Planes units of 16
+            // bytes, unit 4p + q covering plane p of values 16q..16q+15 of the
+            // slab; this thread writes quarter q = i % 4 of each plane: a 4×4
+            // byte transpose per four values (byte p of n is plane p; with
+            // three planes byte 2 is already the signed top digit).
+            uint4 *pu = reinterpret_cast<uint4 *>(planes + (i >> 2) * kPlaneSlabBytes) + (i & 3);
+            uint32_t P[4][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t n0 = (uint32_t)n[4 * q], n1 = (uint32_t)n[4 * q + 1];
+                const uint32_t n2 = (uint32_t)n[4 * q + 2], n3 = (uint32_t)n[4 * q + 3];
+                const uint32_t t0 = __byte_perm(n0, n1, 0x5140), t1 = __byte_perm(n0, n1, 0x7362);
+                const uint32_t t2 = __byte_perm(n2, n3, 0x5140), t3 = __byte_perm(n2, n3, 0x7362);
+                P[0][q] = __byte_perm(t0, t2, 0x5410);
+                P[1][q] = __byte_perm(t0, t2, 0x7632);
+                P[2][q] = __byte_perm(t1, t3, 0x5410);
+                P[3][q] = __byte_perm(t1, t3, 0x7632);
+            }
+#pragma unroll
+            for (int p = 0; p < kT1Planes; ++p) pu[4 * p] = make_uint4(P[p][0], P[p][1], P[p][2], P[p][3]);
+            if ((i & 1) == 0) {
+                if (kSums) sx32[i >> 1] = sum;
+                u32[i >> 1] = __uint_as_float((uint32_t)(127 + ex - kShift) << 23);  // 2^(ex-kShift)
+            }
+        }
+    }
+}
+
+// Sum of kRP (2 or 4) row partials v[] over a slot of G lanes (G a power of
+// two, at least kRP; slots are aligned lane groups): exchange levels leave
+// each lane with one row, the rest is a butterfly.  Lane l of the slot ends
+// with row (l % G) / (G / kRP) summed over the slot.
+template <int kRP>
+__device__ __forceinline__ float reduce_rows(const float (&v)[kRP], int lane, int G) {
+    float b;
+    int o;
+    if constexpr (kRP == 4) {
+        const bool hi = (lane & (G >> 1)) != 0, lo = (lane & (G >> 2)) != 0;
+        float a0 = hi ? v[2] : v[0], a1 = hi ? v[3] : v[1];
+        const float s0 = hi ? v[0] : v[2], s1 = hi ? v[1] : v[3];
+        a0 += __shfl_xor_sync(0xFFFFFFFFu, s0, G >> 1);
+        a1 += __shfl_xor_sync(0xFFFFFFFFu, s1, G >> 1);
+        b = lo ? a1 : a0;
+        b += __shfl_xor_sync(0xFFFFFFFFu, lo ? a0 : a1, G >> 2);
+        o = G >> 3;
+    } else {
+        const bool hi = (lane & (G >> 1)) != 0;
+        b = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xFFFFFFFFu, hi ? v[0] : v[1], G >> 1);
+        o = G >> 2;
+    }
+    for (; o > 0; o >>= 1) b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    return b;
+}
 
 // kSwiGLU: the CTA's rows of W (gate) and then the same rows of W2 (up) form
 // one list of 2·nrows virtual rows through the same ring and passes; every
 // row result goes to shared memory and y[o] = silu(g[o])·u[o] at the end.
-template <class Fmt, int kNB, bool kSwiGLU>
-__global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_kernel(T1Params p) {
+// kCw: compute warps (kT1SoloCw: 16 warps with the copy warp, 128 registers
+// a thread; kT1MaxCw: rows of 16 warps, 96 registers).  kRP: rows a row slot
+// takes per pass (4, or 2 where 4-row stages do not fit shared memory).
+template <class Fmt, int kNB, bool kSwiGLU, int kCw, int kRP>
+__global__ void __launch_bounds__(32 * (1 + kCw), 1) gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
     __shared__ int issued;  // weight stages issued so far (for the abort drain)
@@ -451,27 +574,25 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     const int L = 4 * nb;                          // slab lanes per row
     const bool wide = L > 32;                      // a row spans several warps
     const int wc = wide ? (L + 31) / 32 : 1;       // warps per row
-    int lpr = 32;                                  // lanes per row slot when !wide
+    int lpr = 32;                                  // lanes per row slot
     if (!wide) {
         lpr = 4;
         while (lpr < L) lpr <<= 1;
     }
-    const int rpp = wide ? 1 : 32 / lpr;           // row slots per warp pass
-    const int pass_rows = 2 * rpp;
-    const int half = wide ? 16 : lpr / 2;
+    const int rpp = wide ? 1 : 32 / lpr;           // row slots per warp
+    const int pass_rows = kRP * rpp;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Tokens: the planes, sums and block scales of token t follow those of
+    // Tokens: the planes, sums and group steps of token t follow those of
     // token t − 1, so the split indexes them by its flat position in x [T][K].
     const int T = kSwiGLU ? 1 : p.T;
     const int TK = T * K;
     const int ncw = T * wc * p.rg;
-    const uint32_t slot_bytes = p.stage_rows * row_bytes;
-    uint8_t *planes = smem;                                           // T·nslabs × 208 bytes
-    float *sx = reinterpret_cast<float *>(planes + T * nslabs * kPlaneSlabBytes);  // T·K/32 sub-block sums
-    float *sx16 = sx + TK / 32;                                       // T·K/16 half-sub-block sums
-    float *sb = sx16 + TK / 16;                                       // T·K/256 block scales
-    float *xst = sb + ((T * nb + 3) & ~3);                            // x (when staged)
+    const uint32_t slot_bytes = p.slot_bytes;
+    uint8_t *planes = smem;                                           // T·nslabs slabs
+    float *u32 = reinterpret_cast<float *>(planes + T * nslabs * kPlaneSlabBytes);  // T·K/32 steps
+    float *sx32 = u32 + TK / 32;                                      // T·K/32 group sums (kSums)
+    float *xst = sx32 + (Fmt::kSums ? TK / 32 : 0);                   // x (when staged)
     uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? TK : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty_bar = full_bar + p.nslots;
@@ -514,21 +635,19 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
                 // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
                 const int g1 = kSwiGLU ? min(v1, nrows) : v1;
                 if (g1 > v0) {
+                    // The stage's bytes start `mis` bytes into the slot: the
+                    // copy starts at the 16-byte boundary below them (W is
+                    // 16-byte aligned, so that is still inside W) and its
+                    // last bytes off the 16-byte grid go by plain loads,
+                    // ahead of the arrive that publishes the stage, so
+                    // nothing past the rows is read.
                     const uint8_t *src = p.W + (size_t)(row0 + v0) * row_bytes;
-                    const uint32_t bytes = (uint32_t)(g1 - v0) * row_bytes;
-                    // Rows of a format whose row size is not a multiple of 16
-                    // start stages on 8-row boundaries (16-byte aligned); only
-                    // the last stage of the matrix can end off the 16-byte
-                    // grid: its last bytes go by plain loads, ahead of the
-                    // arrive that publishes the stage.
-                    const uint32_t bulk = bytes & ~15u;
-                    if (bulk != bytes) {
-                        for (uint32_t i = bulk; i < bytes; ++i) dst[i] = __ldg(src + i);
-                        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes - (bytes - bulk));
-                    } else {
-                        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
-                    }
-                    bulk_g2s_hint(dst, src, bulk, &full_bar[slot], wpol);
+                    const uint32_t mis = (uint32_t)(((size_t)(row0 + v0) * row_bytes) & 15);
+                    const uint32_t total = mis + (uint32_t)(g1 - v0) * row_bytes;
+                    const uint32_t bulk = total & ~15u;
+                    for (uint32_t i = bulk; i < total; ++i) dst[i] = __ldg(src - mis + i);
+                    mbar_arrive_expect_tx(&full_bar[slot], bulk + (uint32_t)(v1 - g1) * row_bytes);
+                    if (bulk) bulk_g2s_hint(dst, src - mis, bulk, &full_bar[slot], wpol);
                 } else {
                     mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
                 }
@@ -565,10 +684,12 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
         }
         __syncwarp();
     } else {
-        const int cw = warp - kT1RoleWarps;
-        const int tok = cw / (wc * p.rg), cwt = cw % (wc * p.rg);
+        const int cw = warp - 1;
+        const bool worker = cw < ncw;  // warps past ncw only help with the split
+        const int cwc = worker ? cw : 0;
+        const int tok = cwc / (wc * p.rg), cwt = cwc % (wc * p.rg);
         const int wcol = cwt % wc, rgi = cwt / wc;
-        const int ro = wide ? 0 : lane / lpr;
+        const int ro = wide ? 0 : lane / lpr;      // row slot of this lane
         const int s = wide ? wcol * 32 + lane : lane % lpr;
         const bool active = s < L;
         const int b = active ? (s >> 2) : 0, j = s & 3;
@@ -583,170 +704,115 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
             }
             xsrc = xst;
         }
-        // x → three byte planes under power-of-two block scales, plus the
-        // fp32 sub-block sums.  Thread ct takes eighths of sub-blocks (8
-        // values): the 32 threads of a block form one warp and share its
-        // maximum; the four threads of a sub-block are neighbouring lanes.
-        {
-            const int ct = threadIdx.x - 32 * kT1RoleWarps, nth = ncw * 32, ne = TK / 8;
-            for (int e0 = 0; e0 < ne; e0 += nth) {
-                const int e = e0 + ct;
-                const bool on = e < ne && !abort_flag;
-                float v[8];
-                {
-                    const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 2 * e;
-                    const float4 t0 = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 t1 = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[0] = t0.x; v[1] = t0.y; v[2] = t0.z; v[3] = t0.w;
-                    v[4] = t1.x; v[5] = t1.y; v[6] = t1.z; v[7] = t1.w;
-                }
-                float amax = 0.f, sum = 0.f;
+        split_x<Fmt::kSums>(xsrc, TK, threadIdx.x - 32, kCw * 32, abort_flag, planes, u32, sx32);
+        named_bar_sync(1, kCw * 32);
+        if (worker) {
+            Planes pl;
+            {
+                // This slab's 64 plane bytes per plane: positions 64j..64j+31
+                // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
+                // (Fmt::unit_of names the slab and 16-value unit of each of the
+                // lane's four runs; the Q4 and ternary lanes take slab j in order.)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    amax = fmaxf(amax, fabsf(v[i]));
-                    sum += v[i];
-                }
-                // Non-negative floats order like their bit patterns.
-                amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));
-                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                const float sum16 = sum;
-                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                // s_b = 2^ex with amax / 2^ex <= 127 (1 when the block is
-                // zero): ex is the binary exponent of amax/127 written as
-                // m·2^ex with m in [0.5, 1), read from the float's exponent
-                // field; -112 bounds it below so that 2^(15-ex) stays a
-                // normal float (such blocks still scale below 127).
-                const int ebits = (int)(__float_as_uint(amax * (1.0f / 127.0f)) >> 23);
-                const int ex = amax > 0.f ? max(ebits - 126, -112) : 0;
-                const float inv = __uint_as_float((uint32_t)(127 + 15 - ex) << 23);  // 2^(15-ex)
-                // n = rint(v·2^(15-ex)) with one FMA (exact product, one
-                // rounding); its three low bytes are the planes' digits.
-                uint32_t nb_[8];
+                for (int pp = 0; pp < kT1Planes; ++pp) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) nb_[i] = __float_as_uint(fmaf(v[i], inv, kShifter)) - kShifterBits;
-                uint32_t w[3][2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const uint32_t *n4 = nb_ + 4 * k;
-                    w[0][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0040), __byte_perm(n4[2], n4[3], 0x0040), 0x5410);
-                    w[1][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0051), __byte_perm(n4[2], n4[3], 0x0051), 0x5410);
-                    w[2][k] = __byte_perm(__byte_perm(n4[0], n4[1], 0x0062), __byte_perm(n4[2], n4[3], 0x0062), 0x5410);
-                }
-                if (on) {
-                    // Slab-major layout: slab S = e/8 holds 12 units of 16
-                    // bytes, unit 4p + i covering plane p of values
-                    // 16i..16i+15 of the slab; this thread writes the half
-                    // e % 2 of unit i = (e/2) % 4 of each plane.
-                    uint2 *pu = reinterpret_cast<uint2 *>(planes + (e >> 3) * kPlaneSlabBytes) +
-                                2 * ((e >> 1) & 3) + (e & 1);
-                    pu[0] = make_uint2(w[0][0], w[0][1]);
-                    pu[8] = make_uint2(w[1][0], w[1][1]);
-                    pu[16] = make_uint2(w[2][0], w[2][1]);
-                    if ((e & 1) == 0) sx16[e / 2] = sum16;
-                    if ((e & 3) == 0) sx[e / 4] = sum;
-                    if ((e & 31) == 0) sb[e / 32] = __uint_as_float((uint32_t)(127 + ex) << 23);
+                    for (int i = 0; i < 4; ++i) {
+                        int us, up;
+                        Fmt::unit_of(j, i, us, up);
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(planes + (tok * nslabs + 4 * b + us) * kPlaneSlabBytes);
+                        const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
+                        pl[pp][4 * i] = (int)t.x;
+                        pl[pp][4 * i + 1] = (int)t.y;
+                        pl[pp][4 * i + 2] = (int)t.z;
+                        pl[pp][4 * i + 3] = (int)t.w;
+                    }
                 }
             }
-        }
-        named_bar_sync(1, ncw * 32);
-        int pl[3][16];
-        float s_blk, sum_lo, sum_hi;
-        {
-            // This slab's 64 plane bytes per plane: positions 64j..64j+31
-            // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
-            // (Fmt::unit_of names the slab and 16-value unit of each of the
-            // lane's four runs; the Q4 and ternary lanes take slab j in order.)
-#pragma unroll
-            for (int pp = 0; pp < 3; ++pp) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    int us, up;
-                    Fmt::unit_of(j, i, us, up);
-                    const uint4 *src =
-                        reinterpret_cast<const uint4 *>(planes + (tok * nslabs + 4 * b + us) * kPlaneSlabBytes);
-                    const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
-                    pl[pp][4 * i] = (int)t.x;
-                    pl[pp][4 * i + 1] = (int)t.y;
-                    pl[pp][4 * i + 2] = (int)t.z;
-                    pl[pp][4 * i + 3] = (int)t.w;
-                }
-            }
-            s_blk = active ? sb[tok * nb + b] : 0.f;
-            sum_lo = active ? sx[tok * K / 32 + 8 * b + 2 * j] : 0.f;
-            sum_hi = active ? sx[tok * K / 32 + 8 * b + 2 * j + 1] : 0.f;
-        }
-        Fmt::prep_planes(pl);
-        const typename Fmt::Lane lfmt = Fmt::lane(j, sx16 + tok * K / 16 + 16 * b);
-        const float unit = s_blk * (1.0f / 32768.0f);
+            Fmt::prep_planes(pl);
+            // Steps and sums of block b (8 groups of 32).
+            const int gb = tok * K / 32 + 8 * b;
+            const typename Fmt::Lane lfmt = Fmt::lane(j, u32 + gb, sx32 + gb);
 
-        const int npasses = (nv + pass_rows - 1) / pass_rows;
-        // Stage, slot and phase of the current pass, advanced without
-        // divisions as the pass index steps by rg.
-        int pin = rgi, st = 0;
-        while (pin >= passes_per_stage) {
-            pin -= passes_per_stage;
-            ++st;
-        }
-        int slot = st % p.nslots;
-        uint32_t phase = (st / p.nslots) & 1;
-        int waited_stage = -1;
-        const uint8_t *stage_base = ring;
-        int rows = 0;
-        for (int pass = rgi; pass < npasses; pass += p.rg) {
-            if (st != waited_stage) {
+            // Rows: pass q of a stage covers rows pass_rows·q ..; this lane's
+            // row slot ro takes kT1SlotRows consecutive rows of it.  Rows past
+            // the stage's last are computed from ring bytes of the slot (never
+            // outside it) and not stored.
+            const int G = wide ? 32 : lpr;
+            const int ri = (lane % G) / (G / kRP);   // row of the slot this lane finishes
+            // (A lane past the row's last slab adds zeros but may still hold a
+            // finished row.)
+            const bool writer = (lane % (G / kRP)) == 0;
+            const int npasses = (nv + pass_rows - 1) / pass_rows;
+            int pin = rgi, st = 0;
+            while (pin >= passes_per_stage) {
+                pin -= passes_per_stage;
+                ++st;
+            }
+            int slot = st % p.nslots;
+            uint32_t phase = (st / p.nslots) & 1;
+            for (int pass = rgi; pass < npasses;) {
                 if (abort_flag) break;
                 if (!mbar_wait_bounded(&full_bar[slot], phase, kWaitLimitCycles)) {
                     abort_flag = 1;
                     flag_timeout(p.status);
                     break;
                 }
-                waited_stage = st;
-                stage_base = ring + (size_t)slot * slot_bytes + b * Fmt::kGroupBytes;
-                rows = min(p.stage_rows, nv - st * p.stage_rows);
-            }
-            const int ra = pin * pass_rows + 2 * ro, rb = ra + 1;
-            float pa = Fmt::row(stage_base + min(ra, rows - 1) * row_bytes, lfmt, unit, pl, sum_lo, sum_hi);
-            float pb = Fmt::row(stage_base + min(rb, rows - 1) * row_bytes, lfmt, unit, pl, sum_lo, sum_hi);
-            if (!active || ra >= rows) pa = 0.f;
-            if (!active || rb >= rows) pb = 0.f;
-            // Two-row butterfly: lanes with (lane & half) == 0 finish with
-            // row a, the others with row b.
-            const bool up = (lane & half) != 0;
-            float v = (up ? pb : pa) + __shfl_xor_sync(0xFFFFFFFFu, up ? pa : pb, half);
-            for (int o = half >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-            const int r = up ? rb : ra;
-            const int rl = st * p.stage_rows + r;
-            if (wide) {
-                if ((lane & (half - 1)) == 0 && r < rows) part[(tok * nv + rl) * wc + wcol] = v;
-            } else if (kSwiGLU) {
-                if (s == (up ? half : 0) && r < rows) part[rl] = v;
-            } else {
-                if (s == (up ? half : 0) && r < rows) p.y[(size_t)tok * p.N + row0 + rl] = p.out_scale * v;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[slot]);
-            pin += p.rg;
-            while (pin >= passes_per_stage) {
-                pin -= passes_per_stage;
-                ++st;
-                if (++slot == p.nslots) {
-                    slot = 0;
-                    phase ^= 1u;
+                // Rows of a width off the 16-byte grid start `mis` bytes into
+                // their slot (see the copy warp).
+                const uint32_t mis = (uint32_t)(((size_t)(row0 + st * p.stage_rows) * row_bytes) & 15);
+                const uint8_t *stage_base = ring + (size_t)slot * slot_bytes + mis + b * Fmt::kGroupBytes;
+                const int rows = min(p.stage_rows, nv - st * p.stage_rows);
+                // Every pass of this group in this stage.
+                do {
+                    const int r0 = pin * pass_rows + kRP * ro;
+                    const uint8_t *rp = stage_base + r0 * row_bytes;
+                    float v[kRP];
+#pragma unroll
+                    for (int i = 0; i < kRP; ++i) v[i] = Fmt::row(rp + i * row_bytes, lfmt, pl);
+                    if (!active) {
+#pragma unroll
+                        for (int i = 0; i < kRP; ++i) v[i] = 0.f;
+                    }
+                    const float sum = reduce_rows<kRP>(v, lane, G);
+                    const int r = r0 + ri;
+                    if (writer && r < rows) {
+                        const int rl = st * p.stage_rows + r;
+                        if (wide) {
+                            part[(tok * nv + rl) * wc + wcol] = sum;
+                        } else if (kSwiGLU) {
+                            part[rl] = sum;
+                        } else {
+                            p.y[(size_t)tok * p.N + row0 + rl] = p.out_scale * sum;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+                    pass += p.rg;
+                    pin += p.rg;
+                } while (pin < passes_per_stage && pass < npasses);
+                while (pin >= passes_per_stage) {
+                    pin -= passes_per_stage;
+                    ++st;
+                    if (++slot == p.nslots) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
 
         if (to_smem) {
-            named_bar_sync(1, ncw * 32);
-            for (int it = threadIdx.x - 32 * kT1RoleWarps; it < T * nrows; it += ncw * 32) {
+            named_bar_sync(1, kCw * 32);
+            for (int it = threadIdx.x - 32; it < T * nrows; it += kCw * 32) {
                 const int t = it / nrows, i = it % nrows;
                 const float *pt = part + (size_t)t * nv * wc;
                 float acc = 0.f;
                 for (int w = 0; w < wc; ++w) acc += pt[i * wc + w];
                 if (kSwiGLU) {
-                    float up = 0.f;
-                    for (int w = 0; w < wc; ++w) up += pt[(nrows + i) * wc + w];
-                    acc = acc / (1.0f + expf(-acc)) * up;  // silu(g)·u
+                    float upv = 0.f;
+                    for (int w = 0; w < wc; ++w) upv += pt[(nrows + i) * wc + w];
+                    acc = acc / (1.0f + expf(-acc)) * upv;  // silu(g)·u
                 }
                 p.y[(size_t)t * p.N + row0 + i] = p.out_scale * acc;
             }
@@ -763,41 +829,15 @@ __global__ void __launch_bounds__(32 * (kT1RoleWarps + kT1MaxCw), 1) gemv_t1_ker
     }
 }
 
-// Geometry knobs of the one-token kernel (T1Tuning, t1_geometry.h) from the
-// environment, read once; out-of-range values are clamped.
-int env_int(const char *name, int dflt, int lo, int hi) {
-    const char *v = getenv(name);
-    if (!v || !*v) return dflt;
-    const int x = atoi(v);
-    return x < lo ? lo : (x > hi ? hi : x);
-}
-
-const T1Tuning &t1_tuning() {
-    static const T1Tuning t = [] {
-        T1Tuning r;
-        r.warps = env_int("Q4MM_T1_WARPS", r.warps, 1, kT1MaxCw);
-        r.ctas_per_sm = env_int("Q4MM_T1_CTAS_PER_SM", r.ctas_per_sm, 1, 8);
-        r.stage_bytes = env_int("Q4MM_T1_STAGE_BYTES", r.stage_bytes, 1024, 65536);
-        r.ring_bytes = env_int("Q4MM_T1_RING_BYTES", r.ring_bytes, 8192, 200 * 1024);
-        r.pre_stages = env_int("Q4MM_T1_PRE_STAGES", r.pre_stages, 0, 64);
-        r.x_stage_max = env_int("Q4MM_T1_X_STAGE_MAX", r.x_stage_max, 0, 65536);
-        r.l2_evict_first = env_int("Q4MM_T1_L2_EVICT_FIRST", r.l2_evict_first, 0, 1);
-        r.max_grid = env_int("Q4MM_T1_MAX_GRID", r.max_grid, 0, 4096);
-        r.spare_sms = env_int("Q4MM_T1_SPARE_SMS", r.spare_sms, 0, 64);
-        r.spare_max_bytes = env_int("Q4MM_T1_SPARE_MAX_BYTES", r.spare_max_bytes, 0, 1 << 30);
-        return r;
-    }();
-    return t;
-}
-
 }  // namespace
 
 template <class Fmt, bool kSwiGLU = false>
 cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N,
                            const uint8_t *W2 = nullptr, float out_scale = 1.0f, int T = 1) {
-    const T1Tuning &tun = t1_tuning();
+    const T1Tuning tun;
     const T1Geometry g =
-        plan_gemv_t1(Fmt::kGroupBytes, K, N, T, kSwiGLU ? 2 : 1, c.num_sms, c.max_smem_optin, tun);
+        plan_gemv_t1(Fmt::kGroupBytes, Fmt::kSums ? 1 : 0, K, N, T, kSwiGLU ? 2 : 1, c.num_sms, c.max_smem_optin,
+                     tun);
     if (!g.ok) return cudaErrorNotSupported;
     T1Params p;
     p.T = T;
@@ -812,6 +852,7 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     p.rg = g.rg;
     p.rows_per_cta = g.rows_per_cta;
     p.stage_rows = g.stage_rows;
+    p.slot_bytes = (int)g.slot_bytes;
     p.nslots = g.nslots;
     p.pre_stages = g.pre_stages;
     p.x_staged = g.x_staged;
@@ -819,44 +860,43 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     const int grid = g.grid;
     const size_t smem = g.smem;
 
-    const dim3 block(32 * (kT1RoleWarps + g.ncw));
-    auto go = [&](auto kernel) -> cudaError_t {
+    auto go = [&](auto kernel, int cw) -> cudaError_t {
         cudaError_t e = ensure_smem(kernel, smem);
         if (e != cudaSuccess) return e;
-        return launch_kernel(c, kernel, dim3(grid), block, smem, p);
+        return launch_kernel(c, kernel, dim3(grid), dim3(32 * (1 + cw)), smem, p);
     };
+    // Blocks-per-row specialisations for common widths; rows of 16 warps
+    // (only widths kNB = 0) in the wide form.
+    // The general width (kNB = 0) also takes 2-row passes and the wide form.
+    auto pick = [&](auto nbc) -> cudaError_t {
+        constexpr int kNB = decltype(nbc)::value;
+        if (g.cw == kT1SoloCw && g.slot_rows == kT1SlotRows)
+            return go(gemv_t1_kernel<Fmt, kNB, kSwiGLU, kT1SoloCw, kT1SlotRows>, kT1SoloCw);
+        if constexpr (kNB == 0) {
+            if (g.cw == kT1SoloCw)
+                return go(gemv_t1_kernel<Fmt, 0, kSwiGLU, kT1SoloCw, kT1SlotRowsWide>, kT1SoloCw);
+            if constexpr (!std::is_same<Fmt, FmtQ4K>::value || kSwiGLU)
+                return go(gemv_t1_kernel<Fmt, 0, kSwiGLU, kT1MaxCw, kT1SlotRowsWide>, kT1MaxCw);
+        }
+        return cudaErrorNotSupported;  // Q4_K rows that wide go to the 2-8 token kernel
+    };
+    using I0 = std::integral_constant<int, 0>;
+    if (g.slot_rows != kT1SlotRows || g.cw != kT1SoloCw) return pick(I0{});
     if constexpr (kSwiGLU) {
-        switch (p.nb) {
-            case 16: return go(gemv_t1_kernel<Fmt, 16, true>);
-            default: return go(gemv_t1_kernel<Fmt, 0, true>);
-        }
+        return pick(I0{});
     } else if constexpr (std::is_same<Fmt, FmtQ6K>::value) {
-        switch (p.nb) {
-            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
-            default: return go(gemv_t1_kernel<Fmt, 0, false>);
-        }
+        return p.nb == 16 ? pick(std::integral_constant<int, 16>{}) : pick(I0{});
     } else if constexpr (std::is_same<Fmt, FmtTern>::value) {
-        switch (p.nb) {
-            case 10: return go(gemv_t1_kernel<Fmt, 10, false>);
-            default: return go(gemv_t1_kernel<Fmt, 0, false>);
-        }
+        return p.nb == 10 ? pick(std::integral_constant<int, 10>{}) : pick(I0{});
     } else if constexpr (std::is_same<Fmt, FmtQ4K>::value) {
         switch (p.nb) {
-            case 4: return go(gemv_t1_kernel<Fmt, 4, false>);
-            case 8: return go(gemv_t1_kernel<Fmt, 8, false>);
-            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
-            case 32: return go(gemv_t1_kernel<Fmt, 32, false>);
-            case 43: return go(gemv_t1_kernel<Fmt, 43, false>);
-            case 56: return go(gemv_t1_kernel<Fmt, 56, false>);
-            case 64: return go(gemv_t1_kernel<Fmt, 64, false>);
-            default: return go(gemv_t1_kernel<Fmt, 0, false>);
+            case 4: return pick(std::integral_constant<int, 4>{});
+            case 16: return pick(std::integral_constant<int, 16>{});
+            case 43: return pick(std::integral_constant<int, 43>{});
+            default: return pick(I0{});
         }
     } else {
-        switch (p.nb) {
-            case 16: return go(gemv_t1_kernel<Fmt, 16, false>);
-            case 43: return go(gemv_t1_kernel<Fmt, 43, false>);
-            default: return go(gemv_t1_kernel<Fmt, 0, false>);
-        }
+        return p.nb == 16 ? pick(std::integral_constant<int, 16>{}) : pick(I0{});
     }
 }
 

@@ -233,14 +233,6 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     }
 }
 
-// Integer from the environment (read once by the caller), clamped to [lo, hi].
-int multi_env_int(const char *name, int dflt, int lo, int hi) {
-    const char *v = getenv(name);
-    if (!v || !*v) return dflt;
-    const int x = atoi(v);
-    return x < lo ? lo : (x > hi ? hi : x);
-}
-
 }  // namespace
 
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
@@ -254,9 +246,7 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.N = N;
     p.T = T;
     p.nb = K / kQ4kValues;
-    // Ring budget: 200 KB, less if Q4MM_MULTI_RING_BYTES says so.
-    static const int ring_bytes = multi_env_int("Q4MM_MULTI_RING_BYTES", 200 * 1024, 8192, 200 * 1024);
-    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, ring_bytes);
+    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes);
     if (!g.ok) return cudaErrorNotSupported;
     p.rows_per_cta = g.rows_per_cta;
     p.nslots = g.nslots;

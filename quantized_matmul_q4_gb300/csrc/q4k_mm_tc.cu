@@ -61,7 +61,7 @@
 #include <mutex>
 #include <utility>
 
-#include "../../include/q4mm.h"
+#include "q4mm.h"
 #include "cluster.cuh"
 #include "common.cuh"
 #include "kernels.h"

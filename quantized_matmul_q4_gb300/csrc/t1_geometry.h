@@ -10,41 +10,46 @@
 
 namespace q4mm {
 
-// Geometry knobs (the library reads them from the environment once):
-// compute warps per CTA, resident CTAs per SM, bytes per ring slot, ring
-// budget, stages issued before the wait, largest x staged by one bulk copy,
-// L2 policy of the weight stream, grid cap, spare SMs of short launches.
+// Geometry constants of the library's launches (the CPU tests use the same
+// defaults).  A CTA has a copy warp and `warps` compute warps: 16 warps in
+// all, so that a thread may hold 128 registers (each SM sub-partition runs
+// 4 of them).  Rows that need 16 warps (inputDim above 30720) take
+// wide_warps = 16 compute warps and fewer registers.  One CTA per SM; the
+// weights stream through a ring of stages in shared memory.
 struct T1Tuning {
-    int warps = 16;
-    int ctas_per_sm = 1;
-    int stage_bytes = 16384;
-    int ring_bytes = 200 * 1024;
-    int pre_stages = 0;        // weight stages issued before the activation copy
-    int x_stage_max = 65536;   // bytes of x staged by a bulk copy (0: plain loads)
-    int l2_evict_first = 1;    // weight copies with the L2 evict_first policy
-    int max_grid = 0;          // CTAs per launch at most (0: no limit)
-    int spare_sms = 4;         // SMs left without a CTA of a short launch
+    int warps = 15;
+    int wide_warps = 16;
+    int stage_bytes = 16384;           // weight bytes per ring stage, at least
+    int ring_bytes = 200 * 1024;       // shared-memory budget of a CTA
+    int x_stage_max = 65536;           // bytes of x staged by one bulk copy (0: plain loads)
+    int l2_evict_first = 1;            // weight copies with the L2 evict_first policy
+    int spare_sms = 4;                 // SMs left without a CTA of a short launch
     int spare_max_bytes = 256 * 1024;  // "short": at most this many weight bytes per CTA
 };
 
-constexpr int kT1MaxCw = 16;           // compute warps at most
-constexpr int kT1PlaneSlabBytes = 208; // byte planes of 64 activations, padded
+constexpr int kT1MaxCw = 16;            // compute warps at most (wide rows)
+constexpr int kT1SoloCw = 15;           // compute warps of the usual form
+constexpr int kT1Planes = 4;            // byte planes of the activation split
+constexpr int kT1PlaneSlabBytes = 64 * kT1Planes + 16;  // the planes of 64 activations + 16 B padding
+constexpr int kT1SlotRows = 4;          // rows a row slot (a warp's lanes of one row) takes per pass
+constexpr int kT1SlotRowsWide = 2;      // the same where 4-row stages do not fit shared memory
 
 struct T1Geometry {
     int ok = 0;            // 0: the kernel cannot take this shape
+    int cw = 0;            // compute warps of the launched kernel (kT1SoloCw or kT1MaxCw)
     int wide = 0;          // a row spans several warps
     int wc = 1;            // warps per row
-    int pass_rows = 2;     // rows of one pass (whole CTA)
+    int slot_rows = 4;     // rows a row slot takes per pass (kT1SlotRows or kT1SlotRowsWide)
+    int pass_rows = 4;     // rows of one pass: slot_rows per row slot of a warp
     int rg = 1;            // row groups per token
-    int ncw = 0;           // compute warps
-    int rq = 1;            // rows whose bytes are a multiple of 16
-    int stage_rows = 0;    // rows per ring slot
+    int ncw = 0;           // compute warps doing passes (<= cw)
+    int stage_rows = 0;    // rows per ring slot (a multiple of pass_rows)
     int rows_per_cta = 0;
     int grid = 0;
     int x_staged = 0;      // x arrives by one bulk copy
     int nslots = 0;        // ring depth
-    int pre_stages = 0;
-    size_t xs_bytes = 0;   // planes, sums, block scales and (staged) x
+    int pre_stages = 0;    // stages issued before the wait on the previous kernel
+    size_t xs_bytes = 0;   // planes, group steps and sums, and (staged) x
     size_t part_bytes = 0; // per-row partial sums of wide rows / SwiGLU
     size_t slot_bytes = 0;
     size_t smem = 0;       // dynamic shared memory per CTA
@@ -80,36 +85,43 @@ inline bool t1_ring_covered(int npasses, int pps, int rg, int nslots) {
     return true;
 }
 
-// group_bytes: bytes per 256 values of a row in the format (144 Q4_K and
-// Q4_0, 210 Q6_K, 64 ternary).  vrow_mult: 2 for the fused gate+up (the
-// gate rows and then the same rows of the up weight through one ring).
-inline T1Geometry plan_gemv_t1(int group_bytes, int K, int N, int T, int vrow_mult, int num_sms,
-                               int max_smem_optin, const T1Tuning &tun) {
+// Shared memory of the activation side: the byte planes of every 64 values,
+// one step (and, for Q4_K's min term, one sum) per 32 values, and x itself
+// when staged.
+inline size_t t1_xs_bytes(size_t TK, int sums, bool x_staged) {
+    return (TK / 64) * kT1PlaneSlabBytes + (TK / 32) * (sums ? 2 : 1) * sizeof(float) +
+           (x_staged ? TK * sizeof(float) : 0);
+}
+
+// One form of the kernel: `warps` compute warps, slot_rows rows per slot.
+inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int T, int vrow_mult,
+                                    int num_sms, int max_smem_optin, const T1Tuning &tun, bool wide_form,
+                                    int slot_rows) {
     T1Geometry g;
+    g.cw = wide_form ? kT1MaxCw : kT1SoloCw;
+    g.slot_rows = slot_rows;
+    const int warps = wide_form ? tun.wide_warps : tun.warps;
     const int nb = K / 256;
     const int row_bytes = nb * group_bytes;
     const int L = 4 * nb;  // slab lanes per row
     g.wide = L > 32;
     g.wc = g.wide ? (L + 31) / 32 : 1;
-    g.pass_rows = g.wide ? 2 : 2 * (32 / t1_next_pow2(L > 4 ? L : 4));
-    // At most kT1MaxCw compute warps: wider rows go to another kernel.
-    if (g.wc > kT1MaxCw) return g;
+    g.pass_rows = slot_rows * (g.wide ? 1 : 32 / t1_next_pow2(L > 4 ? L : 4));
+    // At most `warps` compute warps: wider rows go to another kernel.
+    if (g.wc > warps) return g;
     // Each token gets warps / T compute warps: whole rows (wc warps each).
-    if (tun.warps / T < g.wc) return g;
-    g.rg = (tun.warps / T) / g.wc;
+    if (warps / T < g.wc) return g;
+    g.rg = (warps / T) / g.wc;
     g.ncw = T * g.wc * g.rg;
     // Stage: whole passes, at least stage_bytes of weights (bulk copies of
     // 16 KB and more run at full HBM bandwidth).  A row size off the 16-byte
-    // grid (Q6_K) keeps CTA and stage boundaries on multiples of rq rows,
-    // the fewest whose bytes are a multiple of 16 (row_bytes = 2·odd·nb, so
-    // rq = 8 / gcd(nb, 8)).
-    if (row_bytes % 16) {
-        g.rq = 8;
-        while (g.rq > 1 && (g.rq / 2) * row_bytes % 16 == 0) g.rq /= 2;
-    }
-    const int sq = g.pass_rows > g.rq ? g.pass_rows : g.rq;  // both powers of two
+    // grid (Q6_K) lets a stage start anywhere: its slot holds the bytes from
+    // the 16-byte boundary below the stage's first byte, so it is 16 bytes
+    // longer.
+    const int sq = g.pass_rows;
     int stage_rows = sq * ((tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
     if (stage_rows < sq) stage_rows = sq;
+    const size_t slot_pad = row_bytes % 16 ? 16 : 0;
 
     // Grid.  A CTA of the next launch on the stream can only start where a
     // CTA of this one has exited, and one that starts after this launch has
@@ -119,12 +131,10 @@ inline T1Geometry plan_gemv_t1(int group_bytes, int K, int N, int T, int vrow_mu
     // For a short launch (few weight bytes per CTA) leaving spare_sms SMs
     // free lets every CTA of the next launch be resident before this one
     // completes; a long launch keeps every SM for the weight stream.
-    int grid = tun.ctas_per_sm * num_sms;
+    int grid = num_sms;
     const double cta_bytes = (double)vrow_mult * N * row_bytes / grid;
     if (cta_bytes <= tun.spare_max_bytes) grid = grid - tun.spare_sms > 1 ? grid - tun.spare_sms : 1;
-    if (tun.max_grid > 0 && tun.max_grid < grid) grid = tun.max_grid;
     int rows = (N + grid - 1) / grid;
-    rows = (rows + g.rq - 1) / g.rq * g.rq;
     if (rows < g.pass_rows) rows = g.pass_rows;
     g.rows_per_cta = rows;
     g.grid = (N + rows - 1) / rows;
@@ -132,29 +142,24 @@ inline T1Geometry plan_gemv_t1(int group_bytes, int K, int N, int T, int vrow_mu
     const size_t TK = (size_t)T * K;
     const int vrows = vrow_mult * rows;
     const int npasses = (vrows + g.pass_rows - 1) / g.pass_rows;
-    // Ring for a given stage size: x staging, fixed areas, depth.
-    auto ring = [&](int srows) {
-        if (srows > rows) srows = sq * ((rows + sq - 1) / sq);
-        g.stage_rows = srows;
-        g.slot_bytes = (size_t)srows * row_bytes;
-        g.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
-        // Large rows at an 8-row stage quantum can leave no room for x: then
-        // the compute threads load x themselves.
-        if (g.x_staged && TK * sizeof(float) + 2 * g.slot_bytes + (TK / 64) * kT1PlaneSlabBytes >
-                              (size_t)max_smem_optin - 8192)
-            g.x_staged = 0;
-        g.xs_bytes = (TK / 64) * kT1PlaneSlabBytes + (TK / 32 + TK / 16) * sizeof(float) +
-                     (size_t)((T * nb * 4 + 15) & ~15) + (g.x_staged ? TK * sizeof(float) : 0);
-        g.part_bytes = (g.wide || vrow_mult > 1) ? (size_t)T * vrows * g.wc * sizeof(float) : 0;
-        const size_t fixed = g.xs_bytes + g.part_bytes + 2 * 8 * sizeof(uint64_t);
-        const size_t budget = tun.ring_bytes;
-        int n = (int)((budget > fixed ? budget - fixed : 0) / g.slot_bytes);
-        const int stages_needed = (vrows + srows - 1) / srows;
-        const int cap = stages_needed < 8 ? stages_needed : 8;
-        n = n < cap ? n : cap;
-        return n > 2 ? n : 2;
-    };
-    const int nslots_max = ring(stage_rows);
+    if (stage_rows > rows) stage_rows = sq * ((rows + sq - 1) / sq);
+    g.stage_rows = stage_rows;
+    g.slot_bytes = ((size_t)stage_rows * row_bytes + 15) / 16 * 16 + slot_pad;
+    const int nstages = (vrows + stage_rows - 1) / stage_rows;
+    g.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
+    // Large rows can leave no room for x: then the compute threads load x
+    // themselves.
+    if (g.x_staged && TK * sizeof(float) + 2 * g.slot_bytes + (TK / 64) * kT1PlaneSlabBytes >
+                          (size_t)max_smem_optin - 8192)
+        g.x_staged = 0;
+    g.xs_bytes = t1_xs_bytes(TK, sums, g.x_staged != 0);
+    g.part_bytes = (g.wide || vrow_mult > 1) ? (size_t)T * vrows * g.wc * sizeof(float) : 0;
+    const size_t fixed = g.xs_bytes + g.part_bytes + 2 * 8 * sizeof(uint64_t);
+    const size_t budget = (size_t)tun.ring_bytes;
+    int n = (int)((budget > fixed ? budget - fixed : 0) / g.slot_bytes);
+    const int cap = nstages < 8 ? nstages : 8;
+    n = n < cap ? n : cap;
+    const int nslots_max = n > 2 ? n : 2;
     // Ring depth and row groups: the deepest ring whose every reuse is
     // covered (see t1_ring_covered); where no depth of two or more is, fewer
     // row groups (one row group, or any count dividing the passes of a
@@ -168,14 +173,44 @@ inline T1Geometry plan_gemv_t1(int group_bytes, int K, int N, int T, int vrow_mu
         --g.rg;
     }
     if (nslots < 2) return g;
+    auto smem_for = [&](int ns) {
+        return g.xs_bytes + (size_t)ns * g.slot_bytes + 2 * ns * sizeof(uint64_t) + g.part_bytes;
+    };
+    // A single stage needs one slot.  Last resort for very large stages: one
+    // slot, its stages strictly in turn, with row groups that all have a
+    // pass in every stage.
+    if (nstages == 1) {
+        nslots = 1;
+    } else if (smem_for(nslots) > (size_t)max_smem_optin) {
+        while (g.rg > 1 && pps % g.rg) --g.rg;
+        nslots = 1;
+    }
     g.ncw = T * g.wc * g.rg;
     g.nslots = nslots;
     // With plain activation loads nothing needs to go out ahead of the rest.
-    g.pre_stages = g.x_staged ? tun.pre_stages : nslots;
-    g.smem = g.xs_bytes + (size_t)nslots * g.slot_bytes + 2 * nslots * sizeof(uint64_t) + g.part_bytes;
+    g.pre_stages = g.x_staged ? 0 : nslots;
+    g.smem = smem_for(nslots);
     if (g.smem > (size_t)max_smem_optin) return g;
     g.ok = 1;
     return g;
+}
+
+// group_bytes: bytes per 256 values of a row in the format (144 Q4_K and
+// Q4_0, 210 Q6_K, 64 ternary); sums: 1 for Q4_K (group sums of x for the min
+// term).  vrow_mult: 2 for the fused gate+up (the gate rows and then the
+// same rows of the up weight through one ring).  Passes of 4 rows per slot
+// where they fit, else of 2; rows of more than `warps` warps take the wide
+// form (2-row passes).
+inline T1Geometry plan_gemv_t1(int group_bytes, int sums, int K, int N, int T, int vrow_mult, int num_sms,
+                               int max_smem_optin, const T1Tuning &tun) {
+    T1Geometry g = plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, false,
+                                     kT1SlotRows);
+    if (g.ok) return g;
+    g = plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, false,
+                          kT1SlotRowsWide);
+    if (g.ok || g.wc <= tun.warps) return g;
+    return plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, true,
+                             kT1SlotRowsWide);
 }
 
 }  // namespace q4mm

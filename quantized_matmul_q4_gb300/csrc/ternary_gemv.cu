@@ -580,16 +580,6 @@ cudaError_t launch_t(const LaunchCtx &c, const float *x, const uint8_t *W, float
 
 }  // namespace
 
-// Q4MM_TERNARY_T1=float selects the float kernels (one-token and register
-// tiles) for every K, for comparisons; read once.
-bool ternary_float_t1() {
-    static const bool on = [] {
-        const char *v = getenv("Q4MM_TERNARY_T1");
-        return v && v[0] == 'f';
-    }();
-    return on;
-}
-
 cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_t *W, float scale,
                                 float *y, int K, int N, int T) {
     // The streamed kernels copy whole 16-byte runs of code bytes: rows of
@@ -603,7 +593,7 @@ cudaError_t launch_ternary_gemv(const LaunchCtx &c, const float *x, const uint8_
         // (2560 -> 6912, GB300: 1 token 5.1 vs 5.6 us, 2: 7.4 vs 8.9,
         // 3: 10.0 vs 11.8, 4: 11.7 vs 11.8, 8: 19.1 vs 13.3).  Otherwise the
         // float one-token kernel (one token) or the register-tile kernel.
-        if (K % 256 == 0 && T <= 3 && !ternary_float_t1()) {
+        if (K % 256 == 0 && T <= 3) {
             e = launch_ternary_gemv_t1(c, x, W, scale, y, K, N, T);
             if (e == cudaErrorNotSupported && T > 1) {
                 // Too wide for T tokens at once: one token at a time if that fits.

@@ -74,3 +74,32 @@ def max_rel_err(got, ref) -> float:
     ref = np.asarray(ref, np.float64)
     return max(float(np.abs(got[t] - ref[t]).max() / max(np.abs(ref[t]).max(), 1e-300))
                for t in range(ref.shape[0]))
+
+
+def gemv(fn_name: str, x: np.ndarray, W: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Call the tensor entry point `fn_name` (q4k_matmul, q4_0_gemv, q6k_gemv)
+    on device copies of x and W with a guarded output; returns y [T, N]."""
+    import torch
+    import quantized_matmul_q4_gb300 as q
+    x = np.ascontiguousarray(x, np.float32).reshape(-1, K)
+    T = x.shape[0]
+    buf, out = _guarded_out(T, N)
+    getattr(q, fn_name)(dev(x), dev(np.ascontiguousarray(W, np.uint8).reshape(-1)), N=N, out=out)
+    torch.cuda.synchronize()
+    _check_guards(buf, T, N)
+    q.device_status()
+    return out.view(T, N).cpu().numpy()
+
+
+def ffn(x: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, K: int, N: int) -> np.ndarray:
+    """q4k_ffn_swiglu on device copies, guarded output; returns h [T, N]."""
+    import torch
+    import quantized_matmul_q4_gb300 as q
+    x = np.ascontiguousarray(x, np.float32).reshape(-1, K)
+    T = x.shape[0]
+    buf, out = _guarded_out(T, N)
+    q.q4k_ffn_swiglu(dev(x), dev(Wg.reshape(-1)), dev(Wu.reshape(-1)), N=N, out=out)
+    torch.cuda.synchronize()
+    _check_guards(buf, T, N)
+    q.device_status()
+    return out.view(T, N).cpu().numpy()

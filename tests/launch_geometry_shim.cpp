@@ -4,14 +4,16 @@
 #include "../quantized_matmul_q4_gb300/csrc/multi_geometry.h"
 #include "../quantized_matmul_q4_gb300/csrc/t1_geometry.h"
 
-extern "C" int t1_plan(int group_bytes, int K, int N, int T, int vrow_mult, int num_sms, int max_smem,
+extern "C" int t1_plan(int group_bytes, int sums, int K, int N, int T, int vrow_mult, int num_sms, int max_smem,
                        long long *out) {
     const q4mm::T1Tuning tun;
-    const q4mm::T1Geometry g = q4mm::plan_gemv_t1(group_bytes, K, N, T, vrow_mult, num_sms, max_smem, tun);
+    const q4mm::T1Geometry g =
+        q4mm::plan_gemv_t1(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem, tun);
     const long long v[] = {g.ok,         g.wide,       g.wc,       g.pass_rows,  g.rg,
-                           g.ncw,        g.rq,         g.stage_rows, g.rows_per_cta, g.grid,
+                           g.ncw,        g.stage_rows, g.rows_per_cta, g.grid,
                            g.x_staged,   g.nslots,     g.pre_stages, (long long)g.xs_bytes,
-                           (long long)g.part_bytes, (long long)g.slot_bytes, (long long)g.smem};
+                           (long long)g.part_bytes, (long long)g.slot_bytes, (long long)g.smem,
+                           g.cw,         g.slot_rows};
     for (int i = 0; i < (int)(sizeof(v) / sizeof(v[0])); ++i) out[i] = v[i];
     return g.ok;
 }

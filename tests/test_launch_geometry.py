@@ -16,8 +16,9 @@ import subprocess
 import pytest
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-FIELDS = ["ok", "wide", "wc", "pass_rows", "rg", "ncw", "rq", "stage_rows", "rows_per_cta", "grid",
-          "x_staged", "nslots", "pre_stages", "xs_bytes", "part_bytes", "slot_bytes", "smem"]
+FIELDS = ["ok", "wide", "wc", "pass_rows", "rg", "ncw", "stage_rows", "rows_per_cta", "grid",
+          "x_staged", "nslots", "pre_stages", "xs_bytes", "part_bytes", "slot_bytes", "smem", "cw",
+          "slot_rows"]
 SMS, SMEM = 152, 232448  # GB300: SMs and opt-in shared memory per block
 
 
@@ -30,7 +31,7 @@ def _shim(tmp_path_factory):
         subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-o", out,
                         os.path.join(HERE, "launch_geometry_shim.cpp")], check=True)
         lib = ctypes.CDLL(out)
-        lib.t1_plan.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong)]
+        lib.t1_plan.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
         lib.multi_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_longlong)]
         _LIB.append(lib)
     return _LIB[0]
@@ -42,7 +43,8 @@ def plan(tmp_path_factory):
 
     def call(group_bytes, K, N, T, vrow_mult=1):
         buf = (ctypes.c_longlong * len(FIELDS))()
-        lib.t1_plan(group_bytes, K, N, T, vrow_mult, SMS, SMEM, buf)
+        sums = 1 if group_bytes == 144 else 0   # the Q4_K geometry (Q4_0 shares its row size, without sums)
+        lib.t1_plan(group_bytes, sums, K, N, T, vrow_mult, SMS, SMEM, buf)
         return dict(zip(FIELDS, buf))
     return call
 
@@ -81,41 +83,54 @@ def test_geometry_invariants(plan, fmt):
                     rows, grid = g["rows_per_cta"], g["grid"]
                     assert grid * rows >= N and (grid - 1) * rows < N, (K, N, T)
                     assert 1 <= grid <= SMS
-                    assert rows % g["rq"] == 0 and g["stage_rows"] % g["pass_rows"] == 0
-                    assert g["stage_rows"] % g["rq"] == 0
-                    assert 2 <= g["nslots"] <= 8
+                    # A slot holds its stage from the 16-byte boundary below it.
+                    row_bytes = (K // 256) * gb
+                    pad = 16 if row_bytes % 16 else 0
+                    assert g["slot_bytes"] % 16 == 0 and g["slot_bytes"] >= g["stage_rows"] * row_bytes + (pad and 15)
                     assert g["smem"] <= SMEM
                     assert g["smem"] == g["xs_bytes"] + g["nslots"] * g["slot_bytes"] + \
                         16 * g["nslots"] + g["part_bytes"]
-                    assert g["ncw"] == T * g["wc"] * g["rg"] <= 16
+                    assert g["ncw"] == T * g["wc"] * g["rg"] <= g["cw"]
+                    stages = -(-vm * rows // g["stage_rows"])
+                    assert g["cw"] in (15, 16) and 1 <= g["nslots"] <= 8
+                    # One slot only for a single stage, or where two do not fit
+                    # (its stages then go in turn).
+                    assert g["nslots"] > 1 or stages == 1 or \
+                        g["xs_bytes"] + 2 * g["slot_bytes"] + g["part_bytes"] + 32 > SMEM
+                    assert g["cw"] == 15 or g["wc"] == 16
+                    # A pass (4 or 2 rows per row slot) never straddles two stages.
+                    assert g["slot_rows"] in (4, 2) and g["cw"] == 15 or g["slot_rows"] == 2
+                    assert g["stage_rows"] % g["pass_rows"] == 0 and g["pass_rows"] % g["slot_rows"] == 0
                     assert _reuse_covered(g, vm), (fmt, K, N, T, vm, g)
     assert checked > 500
 
 
 def test_known_geometries(plan):
-    # 4096²: 147 CTAs (4 SMs spare) of 28 rows, four 8-row stages, no reuse.
+    # 4096²: 147 CTAs (4 SMs spare) of 28 rows, seven row groups of two
+    # warps, one 4-row pass each; four 8-row stages, no reuse.
     g = plan(144, 4096, 4096, 1)
-    assert (g["grid"], g["rows_per_cta"], g["stage_rows"], g["nslots"]) == (147, 28, 8, 4)
-    # 8192²: row groups take every second stage, so the ring depth is even (6, not 7).
-    g = plan(144, 8192, 8192, 1)
-    assert (g["rg"], g["stage_rows"] // g["pass_rows"], g["nslots"]) == (4, 2, 6)
+    assert (g["grid"], g["rows_per_cta"], g["rg"], g["stage_rows"], g["nslots"]) == (147, 28, 7, 8, 4)
     # 16384²: a long launch keeps every SM.
     g = plan(144, 16384, 16384, 1)
-    assert g["grid"] == 152
+    assert g["grid"] == 152 and g["cw"] == 15
+    # 32768-wide rows need 16 warps: the wide form, 2-row passes.
+    g = plan(144, 32768, 1024, 1)
+    assert g["ok"] and g["cw"] == 16 and g["wc"] == 16 and g["slot_rows"] == 2
     # Rows too wide for 16 compute warps, or too many tokens for the row width.
     assert not plan(144, 33024, 64, 1)["ok"]
     assert not plan(144, 11008, 64, 3)["ok"]
 
 
 def test_irregular_pass_patterns_take_fewer_row_groups(plan):
-    # 1792-wide rows at 32000 outputs (16 row groups, 9 passes per stage) and
-    # 5376-wide Q6_K rows (5 row groups, 4 passes per 8-row stage, rows in
-    # multiples of 8): no ring depth of two or more has every reuse covered
-    # by the waiting group itself, so fewer row groups take the rows.
-    for gb, K, N in ((144, 1792, 32000), (210, 5376, 6912)):
-        full = 16 // plan(gb, K, 64, 1)["wc"]
+    # 2048-wide rows at 32000 outputs (15 row groups) and 4096-wide Q6_K rows
+    # at 11008 outputs (7 row groups): no ring depth of two or more has every
+    # reuse covered by the waiting group itself, so fewer row groups take the
+    # rows.
+    for gb, K, N in ((144, 2048, 32000), (210, 4096, 11008)):
         g = plan(gb, K, N, 1)
-        assert g["ok"] and g["rg"] < full, (K, N, g)
+        assert g["ok"], (K, N, g)
+        full = 15 // g["wc"]
+        assert g["rg"] < full, (K, N, g)
         assert _reuse_covered(g, 1)
 
 
