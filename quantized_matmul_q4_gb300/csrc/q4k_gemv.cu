@@ -455,36 +455,36 @@ struct T1Params {
 };
 
 // Split of x into planes, group steps and (kSums) group sums, by every
-// compute thread: thread ct takes 16 consecutive values of x [T][K] per
-// step; the two threads of a 32-value group are neighbouring lanes and share
-// its maximum.
+// thread: thread ct takes 8 consecutive values of x [T][K] per step; the
+// four threads of a 32-value group are neighbouring lanes and share its
+// maximum.
 template <bool kSums>
 __device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int nth, volatile int &abort_flag,
                                         uint8_t *planes, float *u32, float *sx32) {
-    const int n16 = TK / 16;
-    for (int i0 = 0; i0 < n16; i0 += nth) {
+    const int n8 = TK / 8;
+    for (int i0 = 0; i0 < n8; i0 += nth) {
         const int i = i0 + ct;
-        const bool on = i < n16 && !abort_flag;
-        float v[16];
+        const bool on = i < n8 && !abort_flag;
+        float v[8];
         {
-            const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 4 * i;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 t = on ? src[k] : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[4 * k] = t.x;
-                v[4 * k + 1] = t.y;
-                v[4 * k + 2] = t.z;
-                v[4 * k + 3] = t.w;
-            }
+            const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 2 * i;
+            const float4 t0 = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 t1 = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[0] = t0.x; v[1] = t0.y; v[2] = t0.z; v[3] = t0.w;
+            v[4] = t1.x; v[5] = t1.y; v[6] = t1.z; v[7] = t1.w;
         }
         float amax = 0.f, sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 8; ++k) {
             amax = fmaxf(amax, fabsf(v[k]));
             if (kSums) sum += v[k];
         }
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        if (kSums) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        if (kSums) {
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        }
         // s_g = 2^ex with amax / 2^ex < 255 (1 when the group is zero): ex is
         // the binary exponent of amax/255 written as m·2^ex with m in [0.5, 1),
         // read from the float's exponent field.  The lower bound kShift − 126
@@ -495,19 +495,20 @@ __device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int n
         const int ebits = (int)(__float_as_uint(amax * (1.0f / 255.0f)) >> 23);
         const int ex = amax > 0.f ? max(ebits - 126, kShift - 126) : 0;
         const float mul = __uint_as_float((uint32_t)(127 + kShift - ex) << 23);  // 2^(kShift-ex)
-        int n[16];
+        int n[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) n[k] = __float2int_rn(v[k] * mul);
+        for (int k = 0; k < 8; ++k) n[k] = __float2int_rn(v[k] * mul);
         if (on) {
-            // Slab-major layout: slab S = i/4 holds 4·kT1Planes units of 16
+            // Slab-major layout: slab S = i/8 holds 4·kT1Planes units of 16
             // bytes, unit 4p + q covering plane p of values 16q..16q+15 of the
-            // slab; this thread writes quarter q = i % 4 of each plane: a 4×4
-            // byte transpose per four values (byte p of n is plane p; with
-            // three planes byte 2 is already the signed top digit).
-            uint4 *pu = reinterpret_cast<uint4 *>(planes + (i >> 2) * kPlaneSlabBytes) + (i & 3);
-            uint32_t P[4][4];
+            // slab; this thread writes half i % 2 of quarter (i % 8)/2 of each
+            // plane: a 4×4 byte transpose per four values (byte p of n is
+            // plane p; with three planes byte 2 is already the signed top
+            // digit).
+            uint2 *pu = reinterpret_cast<uint2 *>(planes + (i >> 3) * kPlaneSlabBytes) + (i & 7);
+            uint32_t P[4][2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 const uint32_t n0 = (uint32_t)n[4 * q], n1 = (uint32_t)n[4 * q + 1];
                 const uint32_t n2 = (uint32_t)n[4 * q + 2], n3 = (uint32_t)n[4 * q + 3];
                 const uint32_t t0 = __byte_perm(n0, n1, 0x5140), t1 = __byte_perm(n0, n1, 0x7362);
@@ -518,10 +519,10 @@ __device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int n
                 P[3][q] = __byte_perm(t1, t3, 0x7632);
             }
 #pragma unroll
-            for (int p = 0; p < kT1Planes; ++p) pu[4 * p] = make_uint4(P[p][0], P[p][1], P[p][2], P[p][3]);
-            if ((i & 1) == 0) {
-                if (kSums) sx32[i >> 1] = sum;
-                u32[i >> 1] = __uint_as_float((uint32_t)(127 + ex - kShift) << 23);  // 2^(ex-kShift)
+            for (int p = 0; p < kT1Planes; ++p) pu[8 * p] = make_uint2(P[p][0], P[p][1]);
+            if ((i & 3) == 0) {
+                if (kSums) sx32[i >> 2] = sum;
+                u32[i >> 2] = __uint_as_float((uint32_t)(127 + ex - kShift) << 23);  // 2^(ex-kShift)
             }
         }
     }
@@ -556,14 +557,14 @@ __device__ __forceinline__ float reduce_rows(const float (&v)[kRP], int lane, in
 // kSwiGLU: the CTA's rows of W (gate) and then the same rows of W2 (up) form
 // one list of 2·nrows virtual rows through the same ring and passes; every
 // row result goes to shared memory and y[o] = silu(g[o])·u[o] at the end.
-// kCw: compute warps (kT1SoloCw: 16 warps with the copy warp, 128 registers
-// a thread; kT1MaxCw: rows of 16 warps, 96 registers).  kRP: rows a row slot
-// takes per pass (4, or 2 where 4-row stages do not fit shared memory).
-template <class Fmt, int kNB, bool kSwiGLU, int kCw, int kRP>
-__global__ void __launch_bounds__(32 * (1 + kCw), 1) gemv_t1_kernel(T1Params p) {
+// kRP: rows a row slot takes per pass (4, or 2 where 4-row stages do not fit
+// shared memory).  All kT1Cw warps compute; thread 0 issues the first
+// stages, and each later stage is issued by the warp that finishes the last
+// pass of the stage before it in the same slot.
+template <class Fmt, int kNB, bool kSwiGLU, int kRP>
+__global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ volatile int abort_flag;
-    __shared__ int issued;  // weight stages issued so far (for the abort drain)
     __shared__ __align__(8) uint64_t x_bar;
 
     // Row geometry: compile-time when kNB > 0.
@@ -595,8 +596,9 @@ __global__ void __launch_bounds__(32 * (1 + kCw), 1) gemv_t1_kernel(T1Params p) 
     float *xst = sx32 + (Fmt::kSums ? TK / 32 : 0);                   // x (when staged)
     uint8_t *ring = reinterpret_cast<uint8_t *>(xst + (p.x_staged ? TK : 0));
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
-    uint64_t *empty_bar = full_bar + p.nslots;
-    float *part = reinterpret_cast<float *>(empty_bar + p.nslots);  // [T][virtual rows][wc]
+    int *done = reinterpret_cast<int *>(full_bar + p.nslots);        // passes finished in each slot's stage
+    int *holds = done + p.nslots;                                     // stage last issued into each slot
+    float *part = reinterpret_cast<float *>(holds + p.nslots);        // [T][virtual rows][wc]
 
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
@@ -604,6 +606,8 @@ __global__ void __launch_bounds__(32 * (1 + kCw), 1) gemv_t1_kernel(T1Params p) 
     const bool to_smem = wide || kSwiGLU;        // row results go to part[]
     const int nstages = (nv + p.stage_rows - 1) / p.stage_rows;
     const int passes_per_stage = p.stage_rows / pass_rows;
+    // Every pass of a full stage is worked by the wc warps of a row, per token.
+    const int slot_passes = passes_per_stage * wc * T;
 
     // Bulk copies need a 16-byte aligned destination; never issue one otherwise.
     if (smem_addr(smem) & 15) {
@@ -613,218 +617,224 @@ __global__ void __launch_bounds__(32 * (1 + kCw), 1) gemv_t1_kernel(T1Params p) 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nslots; ++s) {
             mbar_init(&full_bar[s], 1);
-            // Every pass of a stage is worked by the wc warps of a row, per token.
-            mbar_init(&empty_bar[s], passes_per_stage * wc * T);
+            done[s] = 0;
+            holds[s] = -1;
         }
         mbar_init(&x_bar, 1);
         abort_flag = 0;
-        issued = 0;
         fence_mbar_init();
     }
     __syncthreads();
     pdl_launch_dependents();
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // Weights are read once: streamed with evict_first so that they
-            // do not displace activations and outputs from L2.
-            const uint64_t wpol = p.l2_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-            auto issue = [&](int st, int slot) {
-                const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
-                uint8_t *dst = ring + (size_t)slot * slot_bytes;
-                // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
-                const int g1 = kSwiGLU ? min(v1, nrows) : v1;
-                if (g1 > v0) {
-                    // The stage's bytes start `mis` bytes into the slot: the
-                    // copy starts at the 16-byte boundary below them (W is
-                    // 16-byte aligned, so that is still inside W) and its
-                    // last bytes off the 16-byte grid go by plain loads,
-                    // ahead of the arrive that publishes the stage, so
-                    // nothing past the rows is read.
-                    const uint8_t *src = p.W + (size_t)(row0 + v0) * row_bytes;
-                    const uint32_t mis = (uint32_t)(((size_t)(row0 + v0) * row_bytes) & 15);
-                    const uint32_t total = mis + (uint32_t)(g1 - v0) * row_bytes;
-                    const uint32_t bulk = total & ~15u;
-                    for (uint32_t i = bulk; i < total; ++i) dst[i] = __ldg(src - mis + i);
-                    mbar_arrive_expect_tx(&full_bar[slot], bulk + (uint32_t)(v1 - g1) * row_bytes);
-                    if (bulk) bulk_g2s_hint(dst, src - mis, bulk, &full_bar[slot], wpol);
-                } else {
-                    mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
+    // Stage st into ring slot `slot` (one thread).  Weights are read once:
+    // streamed with evict_first so that they do not displace activations and
+    // outputs from L2.
+    auto issue = [&](int st, int slot) {
+        const uint64_t wpol = p.l2_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+        const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
+        uint8_t *dst = ring + (size_t)slot * slot_bytes;
+        holds[slot] = st;
+        // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
+        const int g1 = kSwiGLU ? min(v1, nrows) : v1;
+        if (g1 > v0) {
+            // The stage's bytes start `mis` bytes into the slot: the copy
+            // starts at the 16-byte boundary below them (W is 16-byte
+            // aligned, so that is still inside W) and its last bytes off the
+            // 16-byte grid go by plain loads, ahead of the arrive that
+            // publishes the stage, so nothing past the rows is read.
+            const uint8_t *src = p.W + (size_t)(row0 + v0) * row_bytes;
+            const uint32_t mis = (uint32_t)(((size_t)(row0 + v0) * row_bytes) & 15);
+            const uint32_t total = mis + (uint32_t)(g1 - v0) * row_bytes;
+            const uint32_t bulk = total & ~15u;
+            for (uint32_t i = bulk; i < total; ++i) dst[i] = __ldg(src - mis + i);
+            mbar_arrive_expect_tx(&full_bar[slot], bulk + (uint32_t)(v1 - g1) * row_bytes);
+            if (bulk) bulk_g2s_hint(dst, src - mis, bulk, &full_bar[slot], wpol);
+        } else {
+            mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(v1 - v0) * row_bytes);
+        }
+        if (kSwiGLU && v1 > nrows) {
+            const int u0 = max(v0, nrows);
+            bulk_g2s_hint(dst + (size_t)(u0 - v0) * row_bytes, p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes,
+                          (uint32_t)(v1 - u0) * row_bytes, &full_bar[slot], wpol);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        // The first stages of the ring, before or after x as the geometry
+        // says; x may be written by the previous kernel on the stream.
+        const int first = min(nstages, p.nslots);
+        const int pre = min(first, p.pre_stages);
+        int st = 0;
+        for (; st < pre; ++st) issue(st, st);
+        pdl_wait();
+        if (p.x_staged) {
+            mbar_arrive_expect_tx(&x_bar, (uint32_t)TK * sizeof(float));
+            bulk_g2s(xst, p.x, (uint32_t)TK * sizeof(float), &x_bar);
+        }
+        for (; st < first; ++st) issue(st, st);
+    }
+
+    const bool worker = warp < ncw;  // warps past ncw only help with the split
+    const int cwc = worker ? warp : 0;
+    const int tok = cwc / (wc * p.rg), cwt = cwc % (wc * p.rg);
+    const int wcol = cwt % wc, rgi = cwt / wc;
+    const int ro = wide ? 0 : lane / lpr;      // row slot of this lane
+    const int s = wide ? wcol * 32 + lane : lane % lpr;
+    const bool active = s < L;
+    const int b = active ? (s >> 2) : 0, j = s & 3;
+
+    // x may be produced by the previous kernel on the stream.
+    pdl_wait();
+    const float *xsrc = p.x;
+    if (p.x_staged) {
+        if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
+            abort_flag = 1;
+            flag_timeout(p.status);
+        }
+        xsrc = xst;
+    }
+    split_x<Fmt::kSums>(xsrc, TK, threadIdx.x, kT1Cw * 32, abort_flag, planes, u32, sx32);
+    __syncthreads();
+    if (worker) {
+        Planes pl;
+        {
+            // This slab's 64 plane bytes per plane: positions 64j..64j+31
+            // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
+            // (Fmt::unit_of names the slab and 16-value unit of each of the
+            // lane's four runs; the Q4 and ternary lanes take slab j in order.)
+#pragma unroll
+            for (int pp = 0; pp < kT1Planes; ++pp) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    int us, up;
+                    Fmt::unit_of(j, i, us, up);
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(planes + (tok * nslabs + 4 * b + us) * kPlaneSlabBytes);
+                    const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
+                    pl[pp][4 * i] = (int)t.x;
+                    pl[pp][4 * i + 1] = (int)t.y;
+                    pl[pp][4 * i + 2] = (int)t.z;
+                    pl[pp][4 * i + 3] = (int)t.w;
                 }
-                if (kSwiGLU && v1 > nrows) {
-                    const int u0 = max(v0, nrows);
-                    bulk_g2s_hint(dst + (size_t)(u0 - v0) * row_bytes,
-                                  p.W2 + (size_t)(row0 + u0 - nrows) * row_bytes, (uint32_t)(v1 - u0) * row_bytes,
-                                  &full_bar[slot], wpol);
-                }
-                issued = st + 1;
-            };
-            const int first = min(nstages, p.nslots);
-            const int pre = min(first, p.pre_stages);
-            int st = 0;
-            for (; st < pre; ++st) issue(st, st);
-            // x may be written by the previous kernel on the stream.
-            pdl_wait();
-            if (p.x_staged) {
-                mbar_arrive_expect_tx(&x_bar, (uint32_t)TK * sizeof(float));
-                bulk_g2s(xst, p.x, (uint32_t)TK * sizeof(float), &x_bar);
-            }
-            for (; st < first; ++st) issue(st, st);
-            for (; st < nstages; ++st) {
-                const int slot = st % p.nslots;
-                if (abort_flag) break;
-                if (!mbar_wait_bounded(&empty_bar[slot], ((st / p.nslots) - 1) & 1,
-                                       kWaitLimitCycles)) {
-                    abort_flag = 1;
-                    flag_timeout(p.status);
-                    break;
-                }
-                issue(st, slot);
             }
         }
-        __syncwarp();
-    } else {
-        const int cw = warp - 1;
-        const bool worker = cw < ncw;  // warps past ncw only help with the split
-        const int cwc = worker ? cw : 0;
-        const int tok = cwc / (wc * p.rg), cwt = cwc % (wc * p.rg);
-        const int wcol = cwt % wc, rgi = cwt / wc;
-        const int ro = wide ? 0 : lane / lpr;      // row slot of this lane
-        const int s = wide ? wcol * 32 + lane : lane % lpr;
-        const bool active = s < L;
-        const int b = active ? (s >> 2) : 0, j = s & 3;
+        Fmt::prep_planes(pl);
+        // Steps and sums of block b (8 groups of 32).
+        const int gb = tok * K / 32 + 8 * b;
+        const typename Fmt::Lane lfmt = Fmt::lane(j, u32 + gb, sx32 + gb);
 
-        // x may be produced by the previous kernel on the stream.
-        pdl_wait();
-        const float *xsrc = p.x;
-        if (p.x_staged) {
-            if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
+        // Rows: pass q of a stage covers rows pass_rows·q ..; this lane's row
+        // slot ro takes kRP consecutive rows of it.  Rows past the stage's
+        // last are computed from ring bytes of the slot (never outside it)
+        // and not stored.
+        const int G = wide ? 32 : lpr;
+        const int ri = (lane % G) / (G / kRP);   // row of the slot this lane finishes
+        // (A lane past the row's last slab adds zeros but may still hold a
+        // finished row.)
+        const bool writer = (lane % (G / kRP)) == 0;
+        const int npasses = (nv + pass_rows - 1) / pass_rows;
+        int pin = rgi, st = 0;
+        while (pin >= passes_per_stage) {
+            pin -= passes_per_stage;
+            ++st;
+        }
+        int slot = st % p.nslots;
+        uint32_t phase = (st / p.nslots) & 1;
+        for (int pass = rgi; pass < npasses;) {
+            if (abort_flag) break;
+            if (!mbar_wait_bounded(&full_bar[slot], phase, kWaitLimitCycles)) {
                 abort_flag = 1;
                 flag_timeout(p.status);
+                break;
             }
-            xsrc = xst;
-        }
-        split_x<Fmt::kSums>(xsrc, TK, threadIdx.x - 32, kCw * 32, abort_flag, planes, u32, sx32);
-        named_bar_sync(1, kCw * 32);
-        if (worker) {
-            Planes pl;
-            {
-                // This slab's 64 plane bytes per plane: positions 64j..64j+31
-                // (low nibbles) then 64j+32..64j+63 (high nibbles) of block b.
-                // (Fmt::unit_of names the slab and 16-value unit of each of the
-                // lane's four runs; the Q4 and ternary lanes take slab j in order.)
+            // Rows of a width off the 16-byte grid start `mis` bytes into
+            // their slot (see issue()).
+            const uint32_t mis = (uint32_t)(((size_t)(row0 + st * p.stage_rows) * row_bytes) & 15);
+            const uint8_t *stage_base = ring + (size_t)slot * slot_bytes + mis + b * Fmt::kGroupBytes;
+            const int rows = min(p.stage_rows, nv - st * p.stage_rows);
+            int finished = 0;  // passes of this warp in this stage
+            // Every pass of this group in this stage.
+            do {
+                const int r0 = pin * pass_rows + kRP * ro;
+                const uint8_t *rp = stage_base + r0 * row_bytes;
+                float v[kRP];
 #pragma unroll
-                for (int pp = 0; pp < kT1Planes; ++pp) {
+                for (int i = 0; i < kRP; ++i) v[i] = Fmt::row(rp + i * row_bytes, lfmt, pl);
+                if (!active) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        int us, up;
-                        Fmt::unit_of(j, i, us, up);
-                        const uint4 *src =
-                            reinterpret_cast<const uint4 *>(planes + (tok * nslabs + 4 * b + us) * kPlaneSlabBytes);
-                        const uint4 t = active ? src[4 * pp + up] : make_uint4(0u, 0u, 0u, 0u);
-                        pl[pp][4 * i] = (int)t.x;
-                        pl[pp][4 * i + 1] = (int)t.y;
-                        pl[pp][4 * i + 2] = (int)t.z;
-                        pl[pp][4 * i + 3] = (int)t.w;
+                    for (int i = 0; i < kRP; ++i) v[i] = 0.f;
+                }
+                const float sum = reduce_rows<kRP>(v, lane, G);
+                const int r = r0 + ri;
+                if (writer && r < rows) {
+                    const int rl = st * p.stage_rows + r;
+                    if (wide) {
+                        part[(tok * nv + rl) * wc + wcol] = sum;
+                    } else if (kSwiGLU) {
+                        part[rl] = sum;
+                    } else {
+                        p.y[(size_t)tok * p.N + row0 + rl] = p.out_scale * sum;
+                    }
+                }
+                ++finished;
+                pass += p.rg;
+                pin += p.rg;
+            } while (pin < passes_per_stage && pass < npasses);
+            // Release the slot: the warp whose passes complete the stage's
+            // count issues the stage nslots further on into it.  Every lane's
+            // reads of the slot come before lane 0's release (warp barrier,
+            // CTA-scope fence), the count's last increment reads them all
+            // (acquire fence), and the proxy fence orders them before the
+            // bulk copy's writes.
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&done[slot], finished) + finished == slot_passes) {
+                    done[slot] = 0;
+                    __threadfence_block();
+                    const int nxt = st + p.nslots;
+                    if (nxt < nstages && !abort_flag) {
+                        fence_async_proxy();
+                        issue(nxt, slot);
                     }
                 }
             }
-            Fmt::prep_planes(pl);
-            // Steps and sums of block b (8 groups of 32).
-            const int gb = tok * K / 32 + 8 * b;
-            const typename Fmt::Lane lfmt = Fmt::lane(j, u32 + gb, sx32 + gb);
-
-            // Rows: pass q of a stage covers rows pass_rows·q ..; this lane's
-            // row slot ro takes kT1SlotRows consecutive rows of it.  Rows past
-            // the stage's last are computed from ring bytes of the slot (never
-            // outside it) and not stored.
-            const int G = wide ? 32 : lpr;
-            const int ri = (lane % G) / (G / kRP);   // row of the slot this lane finishes
-            // (A lane past the row's last slab adds zeros but may still hold a
-            // finished row.)
-            const bool writer = (lane % (G / kRP)) == 0;
-            const int npasses = (nv + pass_rows - 1) / pass_rows;
-            int pin = rgi, st = 0;
             while (pin >= passes_per_stage) {
                 pin -= passes_per_stage;
                 ++st;
-            }
-            int slot = st % p.nslots;
-            uint32_t phase = (st / p.nslots) & 1;
-            for (int pass = rgi; pass < npasses;) {
-                if (abort_flag) break;
-                if (!mbar_wait_bounded(&full_bar[slot], phase, kWaitLimitCycles)) {
-                    abort_flag = 1;
-                    flag_timeout(p.status);
-                    break;
+                if (++slot == p.nslots) {
+                    slot = 0;
+                    phase ^= 1u;
                 }
-                // Rows of a width off the 16-byte grid start `mis` bytes into
-                // their slot (see the copy warp).
-                const uint32_t mis = (uint32_t)(((size_t)(row0 + st * p.stage_rows) * row_bytes) & 15);
-                const uint8_t *stage_base = ring + (size_t)slot * slot_bytes + mis + b * Fmt::kGroupBytes;
-                const int rows = min(p.stage_rows, nv - st * p.stage_rows);
-                // Every pass of this group in this stage.
-                do {
-                    const int r0 = pin * pass_rows + kRP * ro;
-                    const uint8_t *rp = stage_base + r0 * row_bytes;
-                    float v[kRP];
-#pragma unroll
-                    for (int i = 0; i < kRP; ++i) v[i] = Fmt::row(rp + i * row_bytes, lfmt, pl);
-                    if (!active) {
-#pragma unroll
-                        for (int i = 0; i < kRP; ++i) v[i] = 0.f;
-                    }
-                    const float sum = reduce_rows<kRP>(v, lane, G);
-                    const int r = r0 + ri;
-                    if (writer && r < rows) {
-                        const int rl = st * p.stage_rows + r;
-                        if (wide) {
-                            part[(tok * nv + rl) * wc + wcol] = sum;
-                        } else if (kSwiGLU) {
-                            part[rl] = sum;
-                        } else {
-                            p.y[(size_t)tok * p.N + row0 + rl] = p.out_scale * sum;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty_bar[slot]);
-                    pass += p.rg;
-                    pin += p.rg;
-                } while (pin < passes_per_stage && pass < npasses);
-                while (pin >= passes_per_stage) {
-                    pin -= passes_per_stage;
-                    ++st;
-                    if (++slot == p.nslots) {
-                        slot = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        }
-
-        if (to_smem) {
-            named_bar_sync(1, kCw * 32);
-            for (int it = threadIdx.x - 32; it < T * nrows; it += kCw * 32) {
-                const int t = it / nrows, i = it % nrows;
-                const float *pt = part + (size_t)t * nv * wc;
-                float acc = 0.f;
-                for (int w = 0; w < wc; ++w) acc += pt[i * wc + w];
-                if (kSwiGLU) {
-                    float upv = 0.f;
-                    for (int w = 0; w < wc; ++w) upv += pt[(nrows + i) * wc + w];
-                    acc = acc / (1.0f + expf(-acc)) * upv;  // silu(g)·u
-                }
-                p.y[(size_t)t * p.N + row0 + i] = p.out_scale * acc;
             }
         }
     }
 
-    // Never leave a bulk copy writing into shared memory of an exiting CTA.
+    if (to_smem) {
+        __syncthreads();
+        for (int it = threadIdx.x; it < T * nrows; it += kT1Cw * 32) {
+            const int t = it / nrows, i = it % nrows;
+            const float *pt = part + (size_t)t * nv * wc;
+            float acc = 0.f;
+            for (int w = 0; w < wc; ++w) acc += pt[i * wc + w];
+            if (kSwiGLU) {
+                float upv = 0.f;
+                for (int w = 0; w < wc; ++w) upv += pt[(nrows + i) * wc + w];
+                acc = acc / (1.0f + expf(-acc)) * upv;  // silu(g)·u
+            }
+            p.y[(size_t)t * p.N + row0 + i] = p.out_scale * acc;
+        }
+    }
+
+    // Never leave a bulk copy writing into shared memory of an exiting CTA:
+    // after a time-out, wait (bounded) for the last stage issued into each
+    // slot (the earlier ones were consumed, so they had landed) and for x.
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
-        for (int st = max(0, issued - p.nslots); st < issued; ++st)
-            (void)mbar_wait_bounded(&full_bar[st % p.nslots], (st / p.nslots) & 1,
-                                    kWaitLimitCycles);
+        for (int sl = 0; sl < p.nslots; ++sl)
+            if (holds[sl] >= 0)
+                (void)mbar_wait_bounded(&full_bar[sl], (holds[sl] / p.nslots) & 1, kWaitLimitCycles);
         if (p.x_staged) (void)mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles);
     }
 }
@@ -860,28 +870,21 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     const int grid = g.grid;
     const size_t smem = g.smem;
 
-    auto go = [&](auto kernel, int cw) -> cudaError_t {
+    auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e = ensure_smem(kernel, smem);
         if (e != cudaSuccess) return e;
-        return launch_kernel(c, kernel, dim3(grid), dim3(32 * (1 + cw)), smem, p);
+        return launch_kernel(c, kernel, dim3(grid), dim3(32 * kT1Cw), smem, p);
     };
-    // Blocks-per-row specialisations for common widths; rows of 16 warps
-    // (only widths kNB = 0) in the wide form.
-    // The general width (kNB = 0) also takes 2-row passes and the wide form.
+    // Blocks-per-row specialisations for common widths (4-row passes); the
+    // general width (kNB = 0) also takes 2-row passes.
     auto pick = [&](auto nbc) -> cudaError_t {
         constexpr int kNB = decltype(nbc)::value;
-        if (g.cw == kT1SoloCw && g.slot_rows == kT1SlotRows)
-            return go(gemv_t1_kernel<Fmt, kNB, kSwiGLU, kT1SoloCw, kT1SlotRows>, kT1SoloCw);
-        if constexpr (kNB == 0) {
-            if (g.cw == kT1SoloCw)
-                return go(gemv_t1_kernel<Fmt, 0, kSwiGLU, kT1SoloCw, kT1SlotRowsWide>, kT1SoloCw);
-            if constexpr (!std::is_same<Fmt, FmtQ4K>::value || kSwiGLU)
-                return go(gemv_t1_kernel<Fmt, 0, kSwiGLU, kT1MaxCw, kT1SlotRowsWide>, kT1MaxCw);
-        }
-        return cudaErrorNotSupported;  // Q4_K rows that wide go to the 2-8 token kernel
+        if (g.slot_rows == kT1SlotRows) return go(gemv_t1_kernel<Fmt, kNB, kSwiGLU, kT1SlotRows>);
+        if constexpr (kNB == 0) return go(gemv_t1_kernel<Fmt, 0, kSwiGLU, kT1SlotRowsWide>);
+        return cudaErrorNotSupported;
     };
     using I0 = std::integral_constant<int, 0>;
-    if (g.slot_rows != kT1SlotRows || g.cw != kT1SoloCw) return pick(I0{});
+    if (g.slot_rows != kT1SlotRows) return pick(I0{});
     if constexpr (kSwiGLU) {
         return pick(I0{});
     } else if constexpr (std::is_same<Fmt, FmtQ6K>::value) {

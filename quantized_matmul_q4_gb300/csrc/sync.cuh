@@ -99,6 +99,13 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
 }
 
+// Orders this thread's earlier shared-memory accesses (and those it has
+// acquired from other threads) before later async-proxy operations on shared
+// memory, such as a bulk copy into a buffer that was just read.
+__device__ __forceinline__ void fence_async_proxy() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -11,14 +11,12 @@
 namespace q4mm {
 
 // Geometry constants of the library's launches (the CPU tests use the same
-// defaults).  A CTA has a copy warp and `warps` compute warps: 16 warps in
-// all, so that a thread may hold 128 registers (each SM sub-partition runs
-// 4 of them).  Rows that need 16 warps (inputDim above 30720) take
-// wide_warps = 16 compute warps and fewer registers.  One CTA per SM; the
-// weights stream through a ring of stages in shared memory.
+// defaults).  A CTA has `warps` = 16 warps, all of them computing (a thread
+// may then hold 128 registers: each SM sub-partition runs 4 of them); the
+// ring's refills are issued by the warp that finishes a slot last.  One CTA
+// per SM; the weights stream through a ring of stages in shared memory.
 struct T1Tuning {
-    int warps = 15;
-    int wide_warps = 16;
+    int warps = 16;
     int stage_bytes = 16384;           // weight bytes per ring stage, at least
     int ring_bytes = 200 * 1024;       // shared-memory budget of a CTA
     int x_stage_max = 65536;           // bytes of x staged by one bulk copy (0: plain loads)
@@ -27,8 +25,7 @@ struct T1Tuning {
     int spare_max_bytes = 256 * 1024;  // "short": at most this many weight bytes per CTA
 };
 
-constexpr int kT1MaxCw = 16;            // compute warps at most (wide rows)
-constexpr int kT1SoloCw = 15;           // compute warps of the usual form
+constexpr int kT1Cw = 16;               // warps of a CTA (all compute)
 constexpr int kT1Planes = 4;            // byte planes of the activation split
 constexpr int kT1PlaneSlabBytes = 64 * kT1Planes + 16;  // the planes of 64 activations + 16 B padding
 constexpr int kT1SlotRows = 4;          // rows a row slot (a warp's lanes of one row) takes per pass
@@ -36,7 +33,7 @@ constexpr int kT1SlotRowsWide = 2;      // the same where 4-row stages do not fi
 
 struct T1Geometry {
     int ok = 0;            // 0: the kernel cannot take this shape
-    int cw = 0;            // compute warps of the launched kernel (kT1SoloCw or kT1MaxCw)
+    int cw = 0;            // warps of the launched kernel (kT1Cw)
     int wide = 0;          // a row spans several warps
     int wc = 1;            // warps per row
     int slot_rows = 4;     // rows a row slot takes per pass (kT1SlotRows or kT1SlotRowsWide)
@@ -93,14 +90,13 @@ inline size_t t1_xs_bytes(size_t TK, int sums, bool x_staged) {
            (x_staged ? TK * sizeof(float) : 0);
 }
 
-// One form of the kernel: `warps` compute warps, slot_rows rows per slot.
+// One form of the kernel: slot_rows rows per slot and pass.
 inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int T, int vrow_mult,
-                                    int num_sms, int max_smem_optin, const T1Tuning &tun, bool wide_form,
-                                    int slot_rows) {
+                                    int num_sms, int max_smem_optin, const T1Tuning &tun, int slot_rows) {
     T1Geometry g;
-    g.cw = wide_form ? kT1MaxCw : kT1SoloCw;
+    g.cw = kT1Cw;
     g.slot_rows = slot_rows;
-    const int warps = wide_form ? tun.wide_warps : tun.warps;
+    const int warps = tun.warps;
     const int nb = K / 256;
     const int row_bytes = nb * group_bytes;
     const int L = 4 * nb;  // slab lanes per row
@@ -114,13 +110,14 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
     g.rg = (warps / T) / g.wc;
     g.ncw = T * g.wc * g.rg;
     // Stage: whole passes, at least stage_bytes of weights (bulk copies of
-    // 16 KB and more run at full HBM bandwidth).  A row size off the 16-byte
-    // grid (Q6_K) lets a stage start anywhere: its slot holds the bytes from
-    // the 16-byte boundary below the stage's first byte, so it is 16 bytes
+    // 16 KB and more run at full HBM bandwidth).  When the ring must be
+    // reused, a stage holds a pass of every row group (or several): all
+    // groups then work on the same stage and the rest of the ring is
+    // prefetch, and a group that waits on a reused slot has always consumed
+    // the slot's previous stage itself.  A row size off the 16-byte grid
+    // (Q6_K) lets a stage start anywhere: its slot holds the bytes from the
+    // 16-byte boundary below the stage's first byte, so it is 16 bytes
     // longer.
-    const int sq = g.pass_rows;
-    int stage_rows = sq * ((tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
-    if (stage_rows < sq) stage_rows = sq;
     const size_t slot_pad = row_bytes % 16 ? 16 : 0;
 
     // Grid.  A CTA of the next launch on the stream can only start where a
@@ -142,49 +139,46 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
     const size_t TK = (size_t)T * K;
     const int vrows = vrow_mult * rows;
     const int npasses = (vrows + g.pass_rows - 1) / g.pass_rows;
-    if (stage_rows > rows) stage_rows = sq * ((rows + sq - 1) / sq);
-    g.stage_rows = stage_rows;
-    g.slot_bytes = ((size_t)stage_rows * row_bytes + 15) / 16 * 16 + slot_pad;
-    const int nstages = (vrows + stage_rows - 1) / stage_rows;
     g.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
-    // Large rows can leave no room for x: then the compute threads load x
-    // themselves.
-    if (g.x_staged && TK * sizeof(float) + 2 * g.slot_bytes + (TK / 64) * kT1PlaneSlabBytes >
-                          (size_t)max_smem_optin - 8192)
-        g.x_staged = 0;
-    g.xs_bytes = t1_xs_bytes(TK, sums, g.x_staged != 0);
     g.part_bytes = (g.wide || vrow_mult > 1) ? (size_t)T * vrows * g.wc * sizeof(float) : 0;
-    const size_t fixed = g.xs_bytes + g.part_bytes + 2 * 8 * sizeof(uint64_t);
-    const size_t budget = (size_t)tun.ring_bytes;
-    int n = (int)((budget > fixed ? budget - fixed : 0) / g.slot_bytes);
-    const int cap = nstages < 8 ? nstages : 8;
-    n = n < cap ? n : cap;
-    const int nslots_max = n > 2 ? n : 2;
-    // Ring depth and row groups: the deepest ring whose every reuse is
-    // covered (see t1_ring_covered); where no depth of two or more is, fewer
-    // row groups (one row group, or any count dividing the passes of a
-    // stage, has a pass in every stage and covers every depth).
-    const int pps = g.stage_rows / g.pass_rows;
-    int nslots = nslots_max;
-    for (;;) {
-        nslots = nslots_max;
-        while (nslots >= 2 && !t1_ring_covered(npasses, pps, g.rg, nslots)) --nslots;
-        if (nslots >= 2 || g.rg == 1) break;
-        --g.rg;
-    }
-    if (nslots < 2) return g;
+    int nstages = 0, nslots = 0;
+    // Per slot: the ring bytes, a full barrier, a counter of finished passes
+    // and the stage it holds.
     auto smem_for = [&](int ns) {
-        return g.xs_bytes + (size_t)ns * g.slot_bytes + 2 * ns * sizeof(uint64_t) + g.part_bytes;
+        return g.xs_bytes + (size_t)ns * (g.slot_bytes + sizeof(uint64_t) + 2 * sizeof(int)) + g.part_bytes;
     };
-    // A single stage needs one slot.  Last resort for very large stages: one
-    // slot, its stages strictly in turn, with row groups that all have a
-    // pass in every stage.
-    if (nstages == 1) {
-        nslots = 1;
-    } else if (smem_for(nslots) > (size_t)max_smem_optin) {
-        while (g.rg > 1 && pps % g.rg) --g.rg;
-        nslots = 1;
+    // Stages of sq rows (a multiple of sq, at least stage_bytes, at most the
+    // CTA's rows rounded up), slots that fit the budget.
+    auto plan_ring = [&](int sq) {
+        int stage_rows = sq * ((tun.stage_bytes + sq * row_bytes - 1) / (sq * row_bytes));
+        if (stage_rows < sq) stage_rows = sq;
+        if (stage_rows > vrows) stage_rows = sq * ((vrows + sq - 1) / sq);
+        g.stage_rows = stage_rows;
+        g.slot_bytes = ((size_t)stage_rows * row_bytes + 15) / 16 * 16 + slot_pad;
+        nstages = (vrows + stage_rows - 1) / stage_rows;
+        // Large rows can leave no room for x: then the compute threads load
+        // x themselves.
+        if (g.x_staged && TK * sizeof(float) + 2 * g.slot_bytes + (TK / 64) * kT1PlaneSlabBytes >
+                              (size_t)max_smem_optin - 8192)
+            g.x_staged = 0;
+        g.xs_bytes = t1_xs_bytes(TK, sums, g.x_staged != 0);
+        const size_t fixed = smem_for(0);
+        const size_t budget = (size_t)tun.ring_bytes;
+        nslots = (int)((budget > fixed ? budget - fixed : 0) / (g.slot_bytes + 16));
+        nslots = nslots < nstages ? nslots : nstages;
+        nslots = nslots < 8 ? nslots : 8;
+    };
+    plan_ring(g.pass_rows);
+    if (nslots < nstages) {
+        // The ring is reused: a pass of every row group per stage.
+        plan_ring(g.pass_rows * g.rg);
+        if (nslots < 2) nslots = nstages == 1 ? 1 : 2;
+        // Last resort for very large stages: one slot, its stages in turn.
+        if (smem_for(nslots) > (size_t)max_smem_optin) nslots = 1;
     }
+    // Every wait on a reused slot follows the waiting group's own pass in
+    // the slot's previous stage.
+    if (!t1_ring_covered(npasses, g.stage_rows / g.pass_rows, g.rg, nslots)) return g;
     g.ncw = T * g.wc * g.rg;
     g.nslots = nslots;
     // With plain activation loads nothing needs to go out ahead of the rest.
@@ -199,17 +193,13 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
 // Q4_0, 210 Q6_K, 64 ternary); sums: 1 for Q4_K (group sums of x for the min
 // term).  vrow_mult: 2 for the fused gate+up (the gate rows and then the
 // same rows of the up weight through one ring).  Passes of 4 rows per slot
-// where they fit, else of 2; rows of more than `warps` warps take the wide
-// form (2-row passes).
+// where they fit, else of 2.
 inline T1Geometry plan_gemv_t1(int group_bytes, int sums, int K, int N, int T, int vrow_mult, int num_sms,
                                int max_smem_optin, const T1Tuning &tun) {
-    T1Geometry g = plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, false,
-                                     kT1SlotRows);
+    const T1Geometry g =
+        plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, kT1SlotRows);
     if (g.ok) return g;
-    g = plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, false,
-                          kT1SlotRowsWide);
-    if (g.ok || g.wc <= tun.warps) return g;
-    return plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun, true,
+    return plan_gemv_t1_form(group_bytes, sums, K, N, T, vrow_mult, num_sms, max_smem_optin, tun,
                              kT1SlotRowsWide);
 }
 

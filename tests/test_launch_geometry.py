@@ -92,46 +92,53 @@ def test_geometry_invariants(plan, fmt):
                         16 * g["nslots"] + g["part_bytes"]
                     assert g["ncw"] == T * g["wc"] * g["rg"] <= g["cw"]
                     stages = -(-vm * rows // g["stage_rows"])
-                    assert g["cw"] in (15, 16) and 1 <= g["nslots"] <= 8
+                    assert g["cw"] == 16 and 1 <= g["nslots"] <= 8
                     # One slot only for a single stage, or where two do not fit
                     # (its stages then go in turn).
                     assert g["nslots"] > 1 or stages == 1 or \
                         g["xs_bytes"] + 2 * g["slot_bytes"] + g["part_bytes"] + 32 > SMEM
-                    assert g["cw"] == 15 or g["wc"] == 16
                     # A pass (4 or 2 rows per row slot) never straddles two stages.
-                    assert g["slot_rows"] in (4, 2) and g["cw"] == 15 or g["slot_rows"] == 2
+                    assert g["slot_rows"] in (4, 2)
                     assert g["stage_rows"] % g["pass_rows"] == 0 and g["pass_rows"] % g["slot_rows"] == 0
                     assert _reuse_covered(g, vm), (fmt, K, N, T, vm, g)
+                    # A reused ring holds a pass of every row group per stage.
+                    if g["nslots"] < stages:
+                        assert g["stage_rows"] % (g["pass_rows"] * g["rg"]) == 0
     assert checked > 500
 
 
 def test_known_geometries(plan):
-    # 4096²: 147 CTAs (4 SMs spare) of 28 rows, seven row groups of two
-    # warps, one 4-row pass each; four 8-row stages, no reuse.
+    # 4096²: 147 CTAs (4 SMs spare) of 28 rows, eight row groups of two
+    # warps for seven 4-row passes; four 8-row stages, no reuse.
     g = plan(144, 4096, 4096, 1)
-    assert (g["grid"], g["rows_per_cta"], g["rg"], g["stage_rows"], g["nslots"]) == (147, 28, 7, 8, 4)
-    # 16384²: a long launch keeps every SM.
+    assert (g["grid"], g["rows_per_cta"], g["rg"], g["stage_rows"], g["nslots"]) == (147, 28, 8, 8, 4)
+    # 16384²: a long launch keeps every SM; two row groups of eight warps,
+    # and stages of one pass of both groups, so that the whole CTA works on
+    # one stage while the next one streams in.
     g = plan(144, 16384, 16384, 1)
-    assert g["grid"] == 152 and g["cw"] == 15
-    # 32768-wide rows need 16 warps: the wide form, 2-row passes.
+    assert g["grid"] == 152 and g["rg"] == 2 and g["stage_rows"] % (g["pass_rows"] * g["rg"]) == 0
+    assert g["nslots"] >= 2
+    # 32768-wide rows take all 16 warps; odd-width Q6_K rows that wide fall
+    # back to 2-row passes.
     g = plan(144, 32768, 1024, 1)
-    assert g["ok"] and g["cw"] == 16 and g["wc"] == 16 and g["slot_rows"] == 2
+    assert g["ok"] and g["wc"] == 16
+    g = plan(210, 31488, 4096, 1)
+    assert g["ok"] and g["slot_rows"] == 2
     # Rows too wide for 16 compute warps, or too many tokens for the row width.
     assert not plan(144, 33024, 64, 1)["ok"]
     assert not plan(144, 11008, 64, 3)["ok"]
 
 
-def test_irregular_pass_patterns_take_fewer_row_groups(plan):
-    # 2048-wide rows at 32000 outputs (15 row groups) and 4096-wide Q6_K rows
-    # at 11008 outputs (7 row groups): no ring depth of two or more has every
-    # reuse covered by the waiting group itself, so fewer row groups take the
-    # rows.
-    for gb, K, N in ((144, 2048, 32000), (210, 4096, 11008)):
-        g = plan(gb, K, N, 1)
-        assert g["ok"], (K, N, g)
-        full = 15 // g["wc"]
-        assert g["rg"] < full, (K, N, g)
-        assert _reuse_covered(g, 1)
+def test_short_launches_use_small_stages_long_ones_group_wide(plan):
+    # A CTA whose rows all fit the ring takes pass-sized stages (the first
+    # passes start while later stages land); a streaming CTA takes stages of
+    # one pass of every row group, all groups on the same stage.
+    g = plan(144, 4096, 4096, 1)
+    assert g["nslots"] * g["stage_rows"] >= g["rows_per_cta"] and g["stage_rows"] < g["pass_rows"] * g["rg"]
+    for K, N in ((4096, 11008), (8192, 8192), (11008, 4096), (16384, 16384)):
+        g = plan(144, K, N, 1)
+        assert g["nslots"] * g["stage_rows"] < g["rows_per_cta"], (K, N, g)
+        assert g["stage_rows"] % (g["pass_rows"] * g["rg"]) == 0, (K, N, g)
 
 
 MULTI = ["ok", "grid", "rows_per_cta", "nslots", "consumers", "smem"]
