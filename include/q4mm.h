@@ -285,6 +285,23 @@ const char *q4mm_last_error(void);
  */
 int q4mm_device_status(q4mm_stream_t stream, int clear);
 
+/*
+ * q4mm_test_fail_next_wait — a test hook for the library's failure
+ * detection; the pages have no counterpart.  The calling thread's next call
+ * of q4k_matmul (one-token and 2-8 token kernels), q4_0_gemv, q6k_gemv,
+ * q4k_ffn_swiglu or q4k_matmul_tc never issues the copy of weight stage
+ * `stage` of each CTA (its ring stage, or its 256-row weight tile on the
+ * tensor cores) and bounds every in-kernel wait by `limit_cycles` SM cycles
+ * (about 2·10^6 per millisecond) instead of about 2·10^9.  The waits on the
+ * missing stage then run out: the kernel sets the device status word, lets
+ * every copy it did issue land, and exits; that call's y is undefined and
+ * q4mm_device_status reports Q4MM_ERR_TIMEOUT.  Nothing faults or waits
+ * without a bound.  Later calls, and calls on other threads, are not
+ * affected; a call rejected by validation leaves it armed.  stage = -1
+ * disarms it; otherwise stage >= 0 and limit_cycles > 0, else Q4MM_ERR_DIM.
+ */
+int q4mm_test_fail_next_wait(int stage, long long limit_cycles);
+
 /* Library version, major·10000 + minor·100 + patch. */
 int q4mm_version(void);
 

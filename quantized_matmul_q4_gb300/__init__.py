@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     Q4mmError,
     Q4K_BYTES,
     Q4K_VALUES,
+    arm_wait_failure,
     device_status,
     last_error,
     library,

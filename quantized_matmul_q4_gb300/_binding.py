@@ -10,7 +10,7 @@ Q4K_BYTES = 144
 
 _SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q6k_gemv", "q4k_ffn_swiglu",
             "ternary_gemv",
-            "q4mm_last_error", "q4mm_device_status", "q4mm_version")
+            "q4mm_last_error", "q4mm_device_status", "q4mm_version", "q4mm_test_fail_next_wait")
 
 
 class Q4mmError(RuntimeError):
@@ -47,6 +47,8 @@ def _load() -> ctypes.CDLL:
     lib.q4mm_device_status.restype = i32
     lib.q4mm_version.argtypes = []
     lib.q4mm_version.restype = i32
+    lib.q4mm_test_fail_next_wait.argtypes = [i32, ctypes.c_longlong]
+    lib.q4mm_test_fail_next_wait.restype = i32
     return lib
 
 
@@ -107,6 +109,12 @@ def q4k_ffn_swiglu_ptr(x: int, w_gate: int, w_up: int, h: int, K: int, N: int, T
 def ternary_gemv_ptr(x: int, w: int, scale: float, y: int, K: int, N: int, T: int,
                      stream: int = 0) -> None:
     _check(_LIB.ternary_gemv(x, w, ctypes.c_float(scale), y, K, N, T, stream))
+
+
+def arm_wait_failure(stage: int, limit_cycles: int) -> None:
+    """Test hook: the calling thread's next call withholds weight stage `stage`
+    and bounds its in-kernel waits by `limit_cycles` (see include/q4mm.h)."""
+    _check(_LIB.q4mm_test_fail_next_wait(int(stage), int(limit_cycles)))
 
 
 def device_status(stream=None, clear: bool = True) -> None:

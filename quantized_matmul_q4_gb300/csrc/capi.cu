@@ -11,6 +11,7 @@
 
 #include "q4mm.h"
 #include "kernels.h"
+#include "sync.cuh"
 
 namespace {
 
@@ -44,7 +45,17 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx) {
+// Armed by q4mm_test_fail_next_wait for the calling thread's next compute
+// call only.
+struct TestFault {
+    bool armed = false;
+    int stage = -1;
+    long long limit = 0;
+};
+thread_local TestFault g_test_fault;
+
+// take_test_fault: a compute call (it consumes an armed test fault).
+int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx, bool take_test_fault = true) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -69,6 +80,13 @@ int device_ctx(q4mm_stream_t stream, q4mm::LaunchCtx *ctx) {
     // Programmatic dependent launch: a kernel may start its weight stream
     // while the previous kernel on the stream finishes.
     ctx->pdl = true;
+    ctx->wait_limit = q4mm::kWaitLimitCycles;
+    ctx->withhold = -1;
+    if (take_test_fault && g_test_fault.armed) {
+        ctx->wait_limit = g_test_fault.limit;
+        ctx->withhold = g_test_fault.stage;
+        g_test_fault.armed = false;
+    }
     return Q4MM_OK;
 }
 
@@ -286,7 +304,7 @@ const char *q4mm_last_error(void) { return g_err; }
 
 int q4mm_device_status(q4mm_stream_t stream, int clear) {
     q4mm::LaunchCtx ctx;
-    int rc = device_ctx(stream, &ctx);
+    int rc = device_ctx(stream, &ctx, false);
     if (rc) return rc;
     int host = 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -303,6 +321,20 @@ int q4mm_device_status(q4mm_stream_t stream, int clear) {
     return Q4MM_OK;
 }
 
-int q4mm_version(void) { return 100; }
+int q4mm_test_fail_next_wait(int stage, long long limit_cycles) {
+    if (stage == -1) {
+        g_test_fault.armed = false;
+        return Q4MM_OK;
+    }
+    if (stage < 0 || limit_cycles <= 0)
+        return fail(Q4MM_ERR_DIM, "q4mm_test_fail_next_wait: stage (%d) must be >= 0 (or -1) and limit (%lld) > 0",
+                    stage, limit_cycles);
+    g_test_fault.armed = true;
+    g_test_fault.stage = stage;
+    g_test_fault.limit = limit_cycles;
+    return Q4MM_OK;
+}
+
+int q4mm_version(void) { return 200; }
 
 }  // extern "C"

@@ -14,6 +14,8 @@ struct LaunchCtx {
     int max_smem_optin;  // bytes of shared memory a CTA may opt into
     int *status;         // device status word (bounded-wait time-outs)
     bool pdl;            // launch with programmatic stream serialization
+    long long wait_limit;  // SM cycles a bounded in-kernel wait lasts at most
+    int withhold;          // test only: a weight stage never copied (-1: none)
 };
 
 // Q4_K decode GEMV, 1..8 tokens on the one-token kernel (bulk-copied weight

@@ -452,6 +452,8 @@ struct T1Params {
     float out_scale;   // y = out_scale · (row result); 1 except for the ternary scale
     int T;             // tokens (x [T][K], y [T][N]); each compute warp serves one token
     int l2_evict_first;  // 1: weight copies carry the L2 evict_first policy
+    long long wait_limit;  // SM cycles a bounded wait lasts at most
+    int withhold;          // test only: a stage whose copy is never issued (-1: none)
 };
 
 // Split of x into planes, group steps and (kSums) group sums, by every
@@ -462,67 +464,77 @@ template <bool kSums>
 __device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int nth, volatile int &abort_flag,
                                         uint8_t *planes, float *u32, float *sx32) {
     const int n8 = TK / 8;
-    for (int i0 = 0; i0 < n8; i0 += nth) {
-        const int i = i0 + ct;
-        const bool on = i < n8 && !abort_flag;
-        float v[8];
-        {
+    // Up to four steps' loads go out together (x may come from L2 or HBM).
+    constexpr int kBatch = 4;
+    for (int i00 = 0; i00 < n8; i00 += kBatch * nth) {
+        float4 ld[kBatch][2];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i00 + u * nth + ct;
+            const bool on = i < n8 && !abort_flag;
             const float4 *src = reinterpret_cast<const float4 *>(xsrc) + 2 * i;
-            const float4 t0 = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 t1 = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[0] = t0.x; v[1] = t0.y; v[2] = t0.z; v[3] = t0.w;
-            v[4] = t1.x; v[5] = t1.y; v[6] = t1.z; v[7] = t1.w;
+            ld[u][0] = on ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            ld[u][1] = on ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float amax = 0.f, sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            amax = fmaxf(amax, fabsf(v[k]));
-            if (kSums) sum += v[k];
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        if (kSums) {
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-        }
-        // s_g = 2^ex with amax / 2^ex < 255 (1 when the group is zero): ex is
-        // the binary exponent of amax/255 written as m·2^ex with m in [0.5, 1),
-        // read from the float's exponent field.  The lower bound kShift − 126
-        // keeps both 2^(kShift-ex) and the step 2^(ex-kShift) normal floats
-        // (such groups still scale below 255).  A product amax·(1/255) rounded
-        // down across a power of two gives ex one too small and |n| at most
-        // 255·2^kShift·(1 + 2^-23), still inside the planes.
-        const int ebits = (int)(__float_as_uint(amax * (1.0f / 255.0f)) >> 23);
-        const int ex = amax > 0.f ? max(ebits - 126, kShift - 126) : 0;
-        const float mul = __uint_as_float((uint32_t)(127 + kShift - ex) << 23);  // 2^(kShift-ex)
-        int n[8];
+        for (int u = 0; u < kBatch; ++u) {
+            if (i00 + u * nth >= n8) break;  // uniform over the CTA
+            const int i = i00 + u * nth + ct;
+            const bool on = i < n8 && !abort_flag;
+            float v[8];
+            v[0] = ld[u][0].x; v[1] = ld[u][0].y; v[2] = ld[u][0].z; v[3] = ld[u][0].w;
+            v[4] = ld[u][1].x; v[5] = ld[u][1].y; v[6] = ld[u][1].z; v[7] = ld[u][1].w;
+            float amax = 0.f, sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) n[k] = __float2int_rn(v[k] * mul);
-        if (on) {
-            // Slab-major layout: slab S = i/8 holds 4·kT1Planes units of 16
-            // bytes, unit 4p + q covering plane p of values 16q..16q+15 of the
-            // slab; this thread writes half i % 2 of quarter (i % 8)/2 of each
-            // plane: a 4×4 byte transpose per four values (byte p of n is
-            // plane p; with three planes byte 2 is already the signed top
-            // digit).
-            uint2 *pu = reinterpret_cast<uint2 *>(planes + (i >> 3) * kPlaneSlabBytes) + (i & 7);
-            uint32_t P[4][2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint32_t n0 = (uint32_t)n[4 * q], n1 = (uint32_t)n[4 * q + 1];
-                const uint32_t n2 = (uint32_t)n[4 * q + 2], n3 = (uint32_t)n[4 * q + 3];
-                const uint32_t t0 = __byte_perm(n0, n1, 0x5140), t1 = __byte_perm(n0, n1, 0x7362);
-                const uint32_t t2 = __byte_perm(n2, n3, 0x5140), t3 = __byte_perm(n2, n3, 0x7362);
-                P[0][q] = __byte_perm(t0, t2, 0x5410);
-                P[1][q] = __byte_perm(t0, t2, 0x7632);
-                P[2][q] = __byte_perm(t1, t3, 0x5410);
-                P[3][q] = __byte_perm(t1, t3, 0x7632);
+            for (int k = 0; k < 8; ++k) {
+                amax = fmaxf(amax, fabsf(v[k]));
+                if (kSums) sum += v[k];
             }
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            if (kSums) {
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+                sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+            }
+            // s_g = 2^ex with amax / 2^ex < 255 (1 when the group is zero): ex is
+            // the binary exponent of amax/255 written as m·2^ex with m in [0.5, 1),
+            // read from the float's exponent field.  The lower bound kShift − 126
+            // keeps both 2^(kShift-ex) and the step 2^(ex-kShift) normal floats
+            // (such groups still scale below 255).  A product amax·(1/255) rounded
+            // down across a power of two gives ex one too small and |n| at most
+            // 255·2^kShift·(1 + 2^-23), still inside the planes.
+            const int ebits = (int)(__float_as_uint(amax * (1.0f / 255.0f)) >> 23);
+            const int ex = amax > 0.f ? max(ebits - 126, kShift - 126) : 0;
+            const float mul = __uint_as_float((uint32_t)(127 + kShift - ex) << 23);  // 2^(kShift-ex)
+            int n[8];
 #pragma unroll
-            for (int p = 0; p < kT1Planes; ++p) pu[8 * p] = make_uint2(P[p][0], P[p][1]);
-            if ((i & 3) == 0) {
-                if (kSums) sx32[i >> 2] = sum;
-                u32[i >> 2] = __uint_as_float((uint32_t)(127 + ex - kShift) << 23);  // 2^(ex-kShift)
+            for (int k = 0; k < 8; ++k) n[k] = __float2int_rn(v[k] * mul);
+            if (on) {
+                // Slab-major layout: slab S = i/8 holds 4·kT1Planes units of 16
+                // bytes, unit 4p + q covering plane p of values 16q..16q+15 of the
+                // slab; this thread writes half i % 2 of quarter (i % 8)/2 of each
+                // plane: a 4×4 byte transpose per four values (byte p of n is
+                // plane p; with three planes byte 2 is already the signed top
+                // digit).
+                uint2 *pu = reinterpret_cast<uint2 *>(planes + (i >> 3) * kPlaneSlabBytes) + (i & 7);
+                uint32_t P[4][2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t n0 = (uint32_t)n[4 * q], n1 = (uint32_t)n[4 * q + 1];
+                    const uint32_t n2 = (uint32_t)n[4 * q + 2], n3 = (uint32_t)n[4 * q + 3];
+                    const uint32_t t0 = __byte_perm(n0, n1, 0x5140), t1 = __byte_perm(n0, n1, 0x7362);
+                    const uint32_t t2 = __byte_perm(n2, n3, 0x5140), t3 = __byte_perm(n2, n3, 0x7362);
+                    P[0][q] = __byte_perm(t0, t2, 0x5410);
+                    P[1][q] = __byte_perm(t0, t2, 0x7632);
+                    P[2][q] = __byte_perm(t1, t3, 0x5410);
+                    P[3][q] = __byte_perm(t1, t3, 0x7632);
+                }
+#pragma unroll
+                for (int p = 0; p < kT1Planes; ++p) pu[8 * p] = make_uint2(P[p][0], P[p][1]);
+                if ((i & 3) == 0) {
+                    if (kSums) sx32[i >> 2] = sum;
+                    u32[i >> 2] = __uint_as_float((uint32_t)(127 + ex - kShift) << 23);  // 2^(ex-kShift)
+                }
             }
         }
     }
@@ -634,6 +646,9 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
         const uint64_t wpol = p.l2_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
         const int v0 = st * p.stage_rows, v1 = min(v0 + p.stage_rows, nv);
         uint8_t *dst = ring + (size_t)slot * slot_bytes;
+        // (A test may ask for one stage never to arrive, to see a wait run
+        // out; nothing then writes into the slot.)
+        if (st == p.withhold) return;
         holds[slot] = st;
         // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
         const int g1 = kSwiGLU ? min(v1, nrows) : v1;
@@ -688,7 +703,7 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
     pdl_wait();
     const float *xsrc = p.x;
     if (p.x_staged) {
-        if (!mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles)) {
+        if (!mbar_wait_bounded(&x_bar, 0, p.wait_limit)) {
             abort_flag = 1;
             flag_timeout(p.status);
         }
@@ -743,7 +758,7 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
         uint32_t phase = (st / p.nslots) & 1;
         for (int pass = rgi; pass < npasses;) {
             if (abort_flag) break;
-            if (!mbar_wait_bounded(&full_bar[slot], phase, kWaitLimitCycles)) {
+            if (!mbar_wait_abortable(&full_bar[slot], phase, p.wait_limit, &abort_flag)) {
                 abort_flag = 1;
                 flag_timeout(p.status);
                 break;
@@ -834,8 +849,8 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
     if (threadIdx.x == 0 && abort_flag) {
         for (int sl = 0; sl < p.nslots; ++sl)
             if (holds[sl] >= 0)
-                (void)mbar_wait_bounded(&full_bar[sl], (holds[sl] / p.nslots) & 1, kWaitLimitCycles);
-        if (p.x_staged) (void)mbar_wait_bounded(&x_bar, 0, kWaitLimitCycles);
+                (void)mbar_wait_bounded(&full_bar[sl], (holds[sl] / p.nslots) & 1, p.wait_limit);
+        if (p.x_staged) (void)mbar_wait_bounded(&x_bar, 0, p.wait_limit);
     }
 }
 
@@ -867,6 +882,8 @@ cudaError_t launch_gemv_t1(const LaunchCtx &c, const float *x, const uint8_t *W,
     p.pre_stages = g.pre_stages;
     p.x_staged = g.x_staged;
     p.l2_evict_first = tun.l2_evict_first;
+    p.wait_limit = c.wait_limit;
+    p.withhold = c.withhold;
     const int grid = g.grid;
     const size_t smem = g.smem;
 

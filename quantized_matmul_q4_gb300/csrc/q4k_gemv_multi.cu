@@ -75,11 +75,14 @@ struct MultiParams {
     int nb;            // blocks per row
     int rows_per_cta;  // multiple of kMultiRows
     int nslots;        // ring depth (groups in flight)
+    long long wait_limit;  // SM cycles a bounded wait lasts at most
+    int withhold;          // test only: a group whose copy is never issued (-1: none)
 };
 
 template <int TT>
 __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(MultiParams p) {
     extern __shared__ __align__(128) uint8_t msmem[];
+    __shared__ volatile int abort_flag;  // set by the first warp whose wait runs out
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
     const uint32_t slot_bytes = kMultiRows * row_bytes;
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -106,18 +110,24 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
             for (int g = 0; g < ngroups; ++g, ++issued) {
                 const int slot = g % p.nslots;
                 if (g >= p.nslots &&
-                    !mbar_wait_bounded(&empty[slot], ((g / p.nslots) - 1) & 1, kWaitLimitCycles)) {
+                    !mbar_wait_abortable(&empty[slot], ((g / p.nslots) - 1) & 1, p.wait_limit, &abort_flag)) {
+                    abort_flag = 1;
                     flag_timeout(p.status);
                     break;
                 }
+                // (A test may ask for one group never to arrive, to see a
+                // wait run out.)
+                if (g == p.withhold) continue;
                 const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
                 mbar_arrive_expect_tx(&full[slot], bytes);
                 bulk_g2s(ring + (size_t)slot * slot_bytes,
                          p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes, &full[slot]);
             }
-            // Never leave a copy writing into an exiting CTA.
+            // Never leave a copy writing into an exiting CTA: the last
+            // groups issued (a withheld one has nothing in flight).
             for (int g = max(0, issued - p.nslots); g < issued; ++g)
-                (void)mbar_wait_bounded(&full[g % p.nslots], (g / p.nslots) & 1, kWaitLimitCycles);
+                if (g != p.withhold)
+                    (void)mbar_wait_bounded(&full[g % p.nslots], (g / p.nslots) & 1, p.wait_limit);
         }
         __syncwarp();
         return;
@@ -138,7 +148,8 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     pdl_wait();
     for (int g = cw; g < ngroups; g += ncons) {
         const int slot = g % p.nslots;
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (g / p.nslots) & 1, kWaitLimitCycles))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(&full[slot], (g / p.nslots) & 1, p.wait_limit, &abort_flag))) {
+            abort_flag = 1;
             flag_timeout(p.status);
             break;
         }
@@ -246,6 +257,8 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.N = N;
     p.T = T;
     p.nb = K / kQ4kValues;
+    p.wait_limit = c.wait_limit;
+    p.withhold = c.withhold;
     const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes);
     if (!g.ok) return cudaErrorNotSupported;
     p.rows_per_cta = g.rows_per_cta;

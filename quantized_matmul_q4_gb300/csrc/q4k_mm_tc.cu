@@ -269,7 +269,8 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
 template <int kXRows>
 __global__ void __launch_bounds__(kTcThreads, 1)
     q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                     const float *__restrict__ x, float *__restrict__ y, int K, int N, int T, int *status) {
+                     const float *__restrict__ x, float *__restrict__ y, int K, int N, int T, int *status,
+                     long long wait_limit, int withhold) {
     using L = TcLayout;
     extern __shared__ uint8_t tc_smem_raw[];
     __shared__ volatile int abort_flag;
@@ -339,7 +340,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Weight tiles and activation tiles are issued independently, each
             // as soon as its ring slot is free.
             int nw = 0, nx = 0;
+            // (A test may ask for one weight tile never to arrive, to see
+            // the waits on it run out; nothing then writes into its slot.)
             for (; nw < min(nblocks, kTcWStages); ++nw) {
+                if (nw == withhold) continue;
                 mbar_arrive_expect_tx(&full_w[nw], kTcWTileBytes);
                 tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
                             &full_w[nw]);
@@ -361,9 +365,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (nw < nblocks) {
                     const int ws = nw % kTcWStages;
                     if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
-                        mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
-                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes,
-                                    row0, &full_w[ws]);
+                        if (nw != withhold) {
+                            mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
+                            tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes,
+                                        row0, &full_w[ws]);
+                        }
                         ++nw;
                         progressed = true;
                     }
@@ -380,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (progressed) {
                     t_last = clock64();
-                } else if (clock64() - t_last > kWaitLimitCycles) {
+                } else if (clock64() - t_last > wait_limit) {
                     abort_flag = 1;
                     flag_timeout(status);
                 }
@@ -388,10 +394,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Never leave a tensor copy writing into shared memory that is
             // about to be reused: the last use of each ring slot must land.
             for (int b = max(0, nw - kTcWStages); b < nw; ++b)
-                (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, kWaitLimitCycles);
+                if (b != withhold)
+                    (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, wait_limit);
             if constexpr (kXRows == 0) {
                 for (int c = max(0, nx - kTcAStages); c < nx; ++c)
-                    (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, kWaitLimitCycles);
+                    (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, wait_limit);
             }
         }
         __syncwarp();
@@ -407,8 +414,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t ph = 0;
             for (int c = 0; c < nchunks; ++c) {
                 bool ok = true;
-                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[st], ph, kWaitLimitCycles);
-                ok = ok && mbar_wait_bounded(&full_b[st], ph, kWaitLimitCycles);
+                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[st], ph, wait_limit);
+                ok = ok && mbar_wait_bounded(&full_b[st], ph, wait_limit);
                 if (!ok) {
                     abort_flag = 1;
                     flag_timeout(status);
@@ -431,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // it, so that tensor memory is never read or released with MMAs
             // in flight.
             tc_commit(done);
-            (void)mbar_wait_bounded(done, 0, kWaitLimitCycles);
+            (void)mbar_wait_bounded(done, 0, wait_limit);
         }
         __syncwarp();
     } else {
@@ -474,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // before releasing it below: no thread can then release a ring
             // slot twice in one phase.
             if (__any_sync(0xffffffffu, abort_flag != 0) ||
-                !__all_sync(0xffffffffu, mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, kWaitLimitCycles))) {
+                !__all_sync(0xffffffffu, mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, wait_limit))) {
                 good = false;
                 break;
             }
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 bool ok = true;
                 if (cc >= kTcBStages)
-                    ok = mbar_wait_bounded(&empty_b[bs], ((cc / kTcBStages) - 1) & 1, kWaitLimitCycles);
+                    ok = mbar_wait_bounded(&empty_b[bs], ((cc / kTcBStages) - 1) & 1, wait_limit);
                 if (!__all_sync(0xffffffffu, ok)) {
                     good = false;
                     break;
@@ -545,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // The accumulator is complete once every MMA this CTA issued has finished.
-    const bool have_acc = __syncthreads_and(mbar_wait_bounded(done, 0, kWaitLimitCycles) ? 1 : 0) != 0;
+    const bool have_acc = __syncthreads_and(mbar_wait_bounded(done, 0, wait_limit) ? 1 : 0) != 0;
     tc_fence_after();
 
     // Epilogue.  Warps w, w+4, w+8, w+12 share TMEM lane quarter w % 4
@@ -716,7 +723,7 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_x, x, y, K, N, T, c.status);
+    return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_x, x, y, K, N, T, c.status, c.wait_limit, c.withhold);
 }
 
 // Tiles of 128 tokens over the bf16 copy xb of x (several tiles), or one

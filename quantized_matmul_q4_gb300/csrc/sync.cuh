@@ -81,6 +81,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
+// As mbar_wait_bounded, but also gives up (returns false) once *abort is set
+// by another thread of the CTA that has already given up.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, long long limit_cycles,
+                                                    const volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
+        if (*abort || clock64() - t0 > limit_cycles) return false;
+    }
+}
+
 // 1-D bulk copy global → shared, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
@@ -112,6 +124,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // About one second at GB300 clocks: far beyond any legitimate wait here.
+// (Launches take their limit as a parameter; this is its value unless a
+// test asks for a shorter one.)
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
 }  // namespace q4mm

@@ -39,6 +39,17 @@ def test_library_exports_every_declared_symbol(q4mm):
     assert q4mm.version() >= 100
 
 
+def test_wait_failure_hook_validates_arguments(q4mm):
+    # Arguments are checked on the host; arming it launches nothing, and
+    # stage -1 disarms it (the GPU tests check what an armed call does).
+    for stage, limit in ((-2, 1000), (0, 0), (3, -5)):
+        with pytest.raises(q4mm.Q4mmError) as e:
+            q4mm.arm_wait_failure(stage, limit)
+        assert e.value.code == -1
+    q4mm.arm_wait_failure(0, 2_000_000)
+    q4mm.arm_wait_failure(-1, 0)
+
+
 # Fake, suitably aligned device addresses: validation must reject before any
 # pointer is used, so nothing is dereferenced.
 X, W, Y = 0x10000000, 0x20000000, 0x30000000
