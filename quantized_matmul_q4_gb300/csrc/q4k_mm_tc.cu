@@ -359,36 +359,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
                 nx = nchunks;  // the dequant warps write the activation tiles
             }
-            long long t_last = clock64();
-            while ((nw < nblocks || nx < nchunks) && !abort_flag) {
-                bool progressed = false;
-                if (nw < nblocks) {
+            if constexpr (kXRows > 0) {
+                // Only weight tiles to issue: wait (suspended, bounded) for
+                // each slot in turn; a busy poll here would take issue slots
+                // from the dequant warps on this scheduler.
+                for (; nw < nblocks && !abort_flag; ++nw) {
                     const int ws = nw % kTcWStages;
-                    if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
-                        if (nw != withhold) {
-                            mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
-                            tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes,
-                                        row0, &full_w[ws]);
+                    if (!mbar_wait_abortable(&empty_w[ws], ((nw / kTcWStages) - 1) & 1, wait_limit, &abort_flag)) {
+                        abort_flag = 1;
+                        flag_timeout(status);
+                        break;
+                    }
+                    if (nw != withhold) {
+                        mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
+                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
+                                    &full_w[ws]);
+                    }
+                }
+            } else {
+                // Weight and activation tiles, each as soon as its slot is
+                // free: poll both, backing off while neither moves.
+                long long t_last = clock64();
+                while ((nw < nblocks || nx < nchunks) && !abort_flag) {
+                    bool progressed = false;
+                    if (nw < nblocks) {
+                        const int ws = nw % kTcWStages;
+                        if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
+                            if (nw != withhold) {
+                                mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
+                                tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w,
+                                            (b_begin + nw) * kQ4kBytes, row0, &full_w[ws]);
+                            }
+                            ++nw;
+                            progressed = true;
                         }
-                        ++nw;
-                        progressed = true;
                     }
-                }
-                if (nx < nchunks) {
-                    const int as = nx % kTcAStages;
-                    if (mbar_try_wait(&empty_a[as], ((nx / kTcAStages) - 1) & 1)) {
-                        mbar_arrive_expect_tx(&full_a[as], kTcATileBytes);
-                        tma_load_2d(sbase + L::off_a + as * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
-                                    &full_a[as]);
-                        ++nx;
-                        progressed = true;
+                    if (nx < nchunks) {
+                        const int as = nx % kTcAStages;
+                        if (mbar_try_wait(&empty_a[as], ((nx / kTcAStages) - 1) & 1)) {
+                            mbar_arrive_expect_tx(&full_a[as], kTcATileBytes);
+                            tma_load_2d(sbase + L::off_a + as * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
+                                        &full_a[as]);
+                            ++nx;
+                            progressed = true;
+                        }
                     }
-                }
-                if (progressed) {
-                    t_last = clock64();
-                } else if (clock64() - t_last > wait_limit) {
-                    abort_flag = 1;
-                    flag_timeout(status);
+                    if (progressed) {
+                        t_last = clock64();
+                    } else if (clock64() - t_last > wait_limit) {
+                        abort_flag = 1;
+                        flag_timeout(status);
+                    } else {
+                        __nanosleep(200);
+                    }
                 }
             }
             // Never leave a tensor copy writing into shared memory that is
