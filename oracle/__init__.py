@@ -68,6 +68,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_q4k_dequant_block.restype = None
         lib.oracle_q4k_dequant.argtypes = [vp, i64, i64, vp]
         lib.oracle_q4k_dequant.restype = i32
+        lib.oracle_q4k_tc_relayout.argtypes = [vp, i64, i64, vp]
+        lib.oracle_q4k_tc_relayout.restype = i32
+        lib.oracle_q4k_tc_dequant.argtypes = [vp, i64, i64, vp]
+        lib.oracle_q4k_tc_dequant.restype = i32
         for name in ("oracle_q4k_matmul", "oracle_q4k_matmul_bf16", "oracle_q4k_matmul_lazy"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i64, i64, i64, vp, i32]
@@ -139,6 +143,31 @@ def q4k_dequant(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
     out = np.empty((N, K), np.float32)
     if (lib or load()).oracle_q4k_dequant(_ptr(W), K, N, _ptr(out)) != 0:
         raise ValueError("oracle_q4k_dequant rejected its arguments")
+    return out
+
+
+Q4K_TC_CHUNK_BYTES = 48  # bytes per 64 values in the tensor-core layout
+
+
+def q4k_tc_relayout(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
+    """The one-time relayout of a Q4_K weight: [N, K/64 chunks of 48 bytes]
+    (fp32 d·sc, dmin·m of both sub-blocks of a 64-value slab, then its 32
+    code bytes)."""
+    W = _check_q4k(W, K, N)
+    R = np.empty(N * (K // 64) * Q4K_TC_CHUNK_BYTES, np.uint8)
+    if (lib or load()).oracle_q4k_tc_relayout(_ptr(W), K, N, _ptr(R)) != 0:
+        raise ValueError("oracle_q4k_tc_relayout rejected its arguments")
+    return R
+
+
+def q4k_tc_dequant(R: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
+    """Dequantized fp32 weight [N, K] of a relayouted Q4_K weight."""
+    R = np.ascontiguousarray(R, dtype=np.uint8)
+    if K <= 0 or K % 64 or R.size != N * (K // 64) * Q4K_TC_CHUNK_BYTES:
+        raise ValueError("relayouted weight bytes do not match N·K/64·48")
+    out = np.empty((N, K), np.float32)
+    if (lib or load()).oracle_q4k_tc_dequant(_ptr(R), K, N, _ptr(out)) != 0:
+        raise ValueError("oracle_q4k_tc_dequant rejected its arguments")
     return out
 
 

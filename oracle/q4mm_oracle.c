@@ -127,6 +127,95 @@ void oracle_q4k_dequant_block(const uint8_t *blk, float w[Q4K_VALUES])
     }
 }
 
+/*
+ * One-time relayout of a Q4_K weight for the tensor-core prefill (SKaiNET
+ * docs "Eager execution: backends and kernels", the paragraph on weights
+ * relayouted once when they are registered rather than on every call).  The
+ * page does not fix a target layout; this one is the library's own: every
+ * 64-value slab j of a block (the 32 bytes qs[32j..32j+31], sub-blocks 2j and
+ * 2j+1) becomes a 48-byte chunk
+ *     fp32 d·sc(2j), fp32 dmin·m(2j), fp32 d·sc(2j+1), fp32 dmin·m(2j+1),
+ *     the 32 code bytes unchanged,
+ * so a row of K values is K/64 chunks (0.75·K bytes) in the order of K.
+ * Each product has at most 17 significant bits and lies within fp32's normal
+ * range, so it is exact in fp32 and the relayouted weight dequantizes to the
+ * same fp32 matrix.  The layout keeps products, not factors: d and sc (and
+ * dmin and m) cannot be recovered separately, so the inverse is defined on
+ * the matrix (oracle_q4k_tc_dequant), not on the bytes of the scale field.
+ * Floats are stored little-endian.
+ */
+#define Q4K_TC_CHUNK_BYTES 48
+
+static void put_f32(uint8_t *dst, double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    dst[0] = (uint8_t)u;
+    dst[1] = (uint8_t)(u >> 8);
+    dst[2] = (uint8_t)(u >> 16);
+    dst[3] = (uint8_t)(u >> 24);
+}
+
+static double get_f32(const uint8_t *src)
+{
+    uint32_t u = (uint32_t)src[0] | ((uint32_t)src[1] << 8) | ((uint32_t)src[2] << 16) |
+                 ((uint32_t)src[3] << 24);
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* W [N][K/256 blocks of 144 B] → R [N][K/64 chunks of 48 B].  Returns 0, or
+ * -1 on bad sizes. */
+int oracle_q4k_tc_relayout(const uint8_t *W, int64_t K, int64_t N, uint8_t *R)
+{
+    if (K <= 0 || N <= 0 || K % Q4K_VALUES)
+        return -1;
+    int64_t nb = K / Q4K_VALUES;
+    for (int64_t o = 0; o < N; ++o) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t *blk = W + (o * nb + b) * Q4K_BYTES;
+            double d = q4k_d(blk), dmin = q4k_dmin(blk);
+            for (int j = 0; j < 4; ++j) {
+                uint8_t *ch = R + ((o * nb + b) * 4 + j) * Q4K_TC_CHUNK_BYTES;
+                for (int h = 0; h < 2; ++h) {
+                    int sc, m;
+                    q4k_scale_min(blk + 4, 2 * j + h, &sc, &m);
+                    put_f32(ch + 8 * h, d * sc);
+                    put_f32(ch + 8 * h + 4, dmin * m);
+                }
+                memcpy(ch + 16, blk + 16 + 32 * j, 32);
+            }
+        }
+    }
+    return 0;
+}
+
+/* R [N][K/64 chunks] → out [N][K] fp32: value i < 32 of chunk c is
+ * s_lo·(qs[i] & 15) − o_lo, value 32 + i is s_hi·(qs[i] >> 4) − o_hi,
+ * evaluated in double and rounded once to float.  Returns 0, or -1 on bad
+ * sizes. */
+int oracle_q4k_tc_dequant(const uint8_t *R, int64_t K, int64_t N, float *out)
+{
+    if (K <= 0 || N <= 0 || K % 64)
+        return -1;
+    int64_t nc = K / 64;
+    for (int64_t o = 0; o < N; ++o) {
+        for (int64_t c = 0; c < nc; ++c) {
+            const uint8_t *ch = R + (o * nc + c) * Q4K_TC_CHUNK_BYTES;
+            double s_lo = get_f32(ch), o_lo = get_f32(ch + 4);
+            double s_hi = get_f32(ch + 8), o_hi = get_f32(ch + 12);
+            float *w = out + o * K + c * 64;
+            for (int i = 0; i < 32; ++i) {
+                w[i] = (float)(s_lo * (ch[16 + i] & 15) - o_lo);
+                w[32 + i] = (float)(s_hi * (ch[16 + i] >> 4) - o_hi);
+            }
+        }
+    }
+    return 0;
+}
+
 /* W [N][K/256 blocks] → out [N][K] fp32. Returns 0, or -1 on bad sizes. */
 int oracle_q4k_dequant(const uint8_t *W, int64_t K, int64_t N, float *out)
 {

@@ -16,7 +16,11 @@ Sources of the facts:
   * an exact-rational brute force (tests/fraction_reference.py);
   * for Q4_0 (SKaiNET PR #562, section "Out of scope"): a hand-worked block,
     nibble positions, and equality with the Q4_K oracle on blocks that both
-    formats can express.
+    formats can express;
+  * for the one-time relayout of Q4_K for the tensor cores (SKaiNET docs
+    "Eager execution: backends and kernels", relayout-once paragraph): a
+    hand-worked relayout of the hand-worked block, the canonical
+    dequantization (itself pinned above) bit for bit, and code positions.
 """
 from __future__ import annotations
 
@@ -415,6 +419,59 @@ def pin_q6k_fraction_bruteforce(lib):
                 assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
 
 
+def pin_tc_relayout_handworked(lib):
+    # The relayout of the hand-worked block against bytes worked out by hand,
+    # and its values against the block's own hand-worked values.
+    fx, blk = _hand_block(lib)
+    tx = fixtures.read("q4k_tc_relayout_handworked.txt")
+    R = oracle.q4k_tc_relayout(blk, 256, 1, lib=lib).reshape(4, 48)
+    for j in range(4):
+        words = R[j, :16].copy().view("<u4")
+        assert [int(v) for v in words] == [int(v, 16) for v in tx[f"chunk_{j}_words"].split()], j
+    assert list(R[0, 16:20]) == fixtures.hexbytes(tx["chunk_0_qs_0_3"])
+    assert list(R[1, 16:20]) == fixtures.hexbytes(tx["chunk_1_qs_0_3"])
+    w = oracle.q4k_tc_dequant(R, 256, 1, lib=lib)[0]
+    for e in (0, 31, 32, 255):
+        assert w[e] == float(fx[f"w_{e}"]), (e, w[e])
+
+
+def pin_tc_relayout_round_trip(lib):
+    # The relayouted weight is the same matrix: its dequantization equals the
+    # canonical block's bit for bit, over random blocks and the extremes of
+    # the fp16 factors (subnormal, largest finite, zero) and of the 6-bit
+    # fields (0 and 63).
+    g = np.random.default_rng(13)
+    K, N = 768, 6
+    W = synth.q4k_weights(g, N, K).reshape(N, K // 256, 144).copy()
+    heads = [(0x0001, 0x7BFF), (0x7BFF, 0x0001), (0x0000, 0x3C00), (0x3C00, 0x0000), (0x03FF, 0x0400)]
+    for i, (d, dm) in enumerate(heads):
+        o, b = divmod(i, K // 256)
+        W[o, b, 0:4] = [d & 255, d >> 8, dm & 255, dm >> 8]
+    W[4, 0, 4:16] = 0xFF   # every sc and m = 63
+    W[4, 1, 4:16] = 0x00   # every sc and m = 0
+    W = W.reshape(-1)
+    R = oracle.q4k_tc_relayout(W, K, N, lib=lib)
+    assert R.size == N * K // 64 * 48
+    a = oracle.q4k_tc_dequant(R, K, N, lib=lib)
+    b = oracle.q4k_dequant(W, K, N, lib=lib)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def pin_tc_chunk_positions(lib):
+    # One nonzero code byte at row o, block b, slab j, byte l lands in chunk
+    # o·K/64 + 4b + j at byte 16 + l, and nowhere else.
+    K, N = 512, 3
+    base = np.zeros((N, K // 256, 144), np.uint8)
+    base[:, :, 0:2] = [0x00, 0x3C]
+    for (o, b, j, l) in ((0, 0, 0, 0), (1, 1, 3, 31), (2, 0, 2, 7), (2, 1, 1, 16)):
+        W = base.copy()
+        W[o, b, 16 + 32 * j + l] = 0xAB
+        R = oracle.q4k_tc_relayout(W.reshape(-1), K, N, lib=lib).reshape(N * K // 64, 48)
+        hit = np.argwhere(R[:, 16:] != 0)
+        assert hit.tolist() == [[o * (K // 64) + 4 * b + j, l]], (o, b, j, l, hit.tolist())
+        assert R[o * (K // 64) + 4 * b + j, 16 + l] == 0xAB
+
+
 ALL_PINS = [
     pin_fp16_decode, pin_bf16_round, pin_handworked_pack, pin_handworked_values,
     pin_nibble_positions, pin_scale_positions, pin_special_cases, pin_one_hot_rows,
@@ -422,5 +479,6 @@ ALL_PINS = [
     pin_ternary_integer_count, pin_ternary_scale, pin_bf16_variant,
     pin_q4_0_handworked, pin_q4_0_nibble_positions, pin_q4_0_as_q4k, pin_q4_0_fraction_bruteforce,
     pin_swiglu, pin_q6k_handworked, pin_q6k_code_positions, pin_q6k_scale_positions,
-    pin_q6k_fraction_bruteforce,
+    pin_q6k_fraction_bruteforce, pin_tc_relayout_handworked, pin_tc_relayout_round_trip,
+    pin_tc_chunk_positions,
 ]

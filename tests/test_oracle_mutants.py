@@ -54,6 +54,15 @@ MUTANTS = {
                      "double d = oracle_fp16_to_double((uint16_t)(blk[1] | (blk[0] << 8)));\n    for (int e = 0; e < Q40_VALUES"),
     "q4_0_block_stride": ("oracle_q4_0_dequant_block(W + (o * nb + b) * Q40_BYTES, w + b * Q40_VALUES);",
                           "oracle_q4_0_dequant_block(W + (o * nb + b) * 16, w + b * Q40_VALUES);"),
+    "tc_sub_block_swapped": ("q4k_scale_min(blk + 4, 2 * j + h, &sc, &m);",
+                             "q4k_scale_min(blk + 4, 2 * j + 1 - h, &sc, &m);"),
+    "tc_scale_min_swapped": ("put_f32(ch + 8 * h, d * sc);\n                    put_f32(ch + 8 * h + 4, dmin * m);",
+                             "put_f32(ch + 8 * h + 4, d * sc);\n                    put_f32(ch + 8 * h, dmin * m);"),
+    "tc_slab_order": ("memcpy(ch + 16, blk + 16 + 32 * j, 32);", "memcpy(ch + 16, blk + 16 + 32 * (3 - j), 32);"),
+    "tc_offset_sign": ("w[i] = (float)(s_lo * (ch[16 + i] & 15) - o_lo);",
+                       "w[i] = (float)(s_lo * (ch[16 + i] & 15) + o_lo);"),
+    "tc_high_nibble": ("w[32 + i] = (float)(s_hi * (ch[16 + i] >> 4) - o_hi);",
+                       "w[32 + i] = (float)(s_hi * (ch[16 + i] & 15) - o_hi);"),
 }
 
 
