@@ -68,6 +68,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.oracle_q4k_dequant_block.restype = None
         lib.oracle_q4k_dequant.argtypes = [vp, i64, i64, vp]
         lib.oracle_q4k_dequant.restype = i32
+        lib.oracle_q4k_tc_bytes.argtypes = [i64, i64]
+        lib.oracle_q4k_tc_bytes.restype = i64
         lib.oracle_q4k_tc_relayout.argtypes = [vp, i64, i64, vp]
         lib.oracle_q4k_tc_relayout.restype = i32
         lib.oracle_q4k_tc_dequant.argtypes = [vp, i64, i64, vp]
@@ -146,16 +148,27 @@ def q4k_dequant(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
     return out
 
 
-Q4K_TC_CHUNK_BYTES = 48  # bytes per 64 values in the tensor-core layout
+Q4K_TC_CHUNK_BYTES = 48  # bytes per row and 64 values in the tensor-core layout
+Q4K_TC_TILE_ROWS = 256   # rows per tile of that layout
+
+
+def q4k_tc_bytes(K: int, N: int, lib=None) -> int:
+    """Size of the relayouted weight (rows rounded up to whole tiles)."""
+    n = (lib or load()).oracle_q4k_tc_bytes(K, N)
+    if n < 0:
+        raise ValueError("bad relayout sizes")
+    return n
 
 
 def q4k_tc_relayout(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
-    """The one-time relayout of a Q4_K weight: [N, K/64 chunks of 48 bytes]
-    (fp32 d·sc, dmin·m of both sub-blocks of a 64-value slab, then its 32
-    code bytes)."""
+    """The one-time relayout of a Q4_K weight for the tensor cores: tiles of
+    256 rows, each 64-value chunk of a tile one contiguous run of 256 rows x
+    48 bytes (fp32 d·sc, dmin·m of both sub-blocks of the slab, then its 32
+    code bytes); zero rows pad the last tile."""
     W = _check_q4k(W, K, N)
-    R = np.empty(N * (K // 64) * Q4K_TC_CHUNK_BYTES, np.uint8)
-    if (lib or load()).oracle_q4k_tc_relayout(_ptr(W), K, N, _ptr(R)) != 0:
+    lib = lib or load()
+    R = np.empty(q4k_tc_bytes(K, N, lib), np.uint8)
+    if lib.oracle_q4k_tc_relayout(_ptr(W), K, N, _ptr(R)) != 0:
         raise ValueError("oracle_q4k_tc_relayout rejected its arguments")
     return R
 
@@ -163,10 +176,11 @@ def q4k_tc_relayout(W: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
 def q4k_tc_dequant(R: np.ndarray, K: int, N: int, lib=None) -> np.ndarray:
     """Dequantized fp32 weight [N, K] of a relayouted Q4_K weight."""
     R = np.ascontiguousarray(R, dtype=np.uint8)
-    if K <= 0 or K % 64 or R.size != N * (K // 64) * Q4K_TC_CHUNK_BYTES:
-        raise ValueError("relayouted weight bytes do not match N·K/64·48")
+    lib = lib or load()
+    if R.size != q4k_tc_bytes(K, N, lib):
+        raise ValueError("relayouted weight bytes do not match the tiled size")
     out = np.empty((N, K), np.float32)
-    if (lib or load()).oracle_q4k_tc_dequant(_ptr(R), K, N, _ptr(out)) != 0:
+    if lib.oracle_q4k_tc_dequant(_ptr(R), K, N, _ptr(out)) != 0:
         raise ValueError("oracle_q4k_tc_dequant rejected its arguments")
     return out
 

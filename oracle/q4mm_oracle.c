@@ -136,7 +136,10 @@ void oracle_q4k_dequant_block(const uint8_t *blk, float w[Q4K_VALUES])
  * 2j+1) becomes a 48-byte chunk
  *     fp32 d·sc(2j), fp32 dmin·m(2j), fp32 d·sc(2j+1), fp32 dmin·m(2j+1),
  *     the 32 code bytes unchanged,
- * so a row of K values is K/64 chunks (0.75·K bytes) in the order of K.
+ * and the chunks are stored tile-major: the rows form tiles of 256 (the last
+ * one padded with zero rows), and chunk c (values 64c..64c+63) of the 256
+ * rows of tile t is one contiguous run of 256·48 bytes at
+ *     ((t·(K/64) + c)·256 + row mod 256)·48.
  * Each product has at most 17 significant bits and lies within fp32's normal
  * range, so it is exact in fp32 and the relayouted weight dequantizes to the
  * same fp32 matrix.  The layout keeps products, not factors: d and sc (and
@@ -145,6 +148,7 @@ void oracle_q4k_dequant_block(const uint8_t *blk, float w[Q4K_VALUES])
  * Floats are stored little-endian.
  */
 #define Q4K_TC_CHUNK_BYTES 48
+#define Q4K_TC_TILE_ROWS 256
 
 static void put_f32(uint8_t *dst, double v)
 {
@@ -166,19 +170,37 @@ static double get_f32(const uint8_t *src)
     return f;
 }
 
-/* W [N][K/256 blocks of 144 B] → R [N][K/64 chunks of 48 B].  Returns 0, or
- * -1 on bad sizes. */
-int oracle_q4k_tc_relayout(const uint8_t *W, int64_t K, int64_t N, uint8_t *R)
+/* Bytes of the relayouted weight: the rows rounded up to whole tiles. */
+int64_t oracle_q4k_tc_bytes(int64_t K, int64_t N)
 {
     if (K <= 0 || N <= 0 || K % Q4K_VALUES)
         return -1;
+    int64_t tiles = (N + Q4K_TC_TILE_ROWS - 1) / Q4K_TC_TILE_ROWS;
+    return tiles * Q4K_TC_TILE_ROWS * (K / 64) * Q4K_TC_CHUNK_BYTES;
+}
+
+/* Offset of chunk c of row o. */
+static int64_t tc_chunk_offset(int64_t K, int64_t o, int64_t c)
+{
+    int64_t t = o / Q4K_TC_TILE_ROWS, r = o % Q4K_TC_TILE_ROWS;
+    return ((t * (K / 64) + c) * Q4K_TC_TILE_ROWS + r) * Q4K_TC_CHUNK_BYTES;
+}
+
+/* W [N][K/256 blocks of 144 B] → R (oracle_q4k_tc_bytes(K, N) bytes).
+ * Returns 0, or -1 on bad sizes. */
+int oracle_q4k_tc_relayout(const uint8_t *W, int64_t K, int64_t N, uint8_t *R)
+{
+    int64_t total = oracle_q4k_tc_bytes(K, N);
+    if (total < 0)
+        return -1;
+    memset(R, 0, (size_t)total);
     int64_t nb = K / Q4K_VALUES;
     for (int64_t o = 0; o < N; ++o) {
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = W + (o * nb + b) * Q4K_BYTES;
             double d = q4k_d(blk), dmin = q4k_dmin(blk);
             for (int j = 0; j < 4; ++j) {
-                uint8_t *ch = R + ((o * nb + b) * 4 + j) * Q4K_TC_CHUNK_BYTES;
+                uint8_t *ch = R + tc_chunk_offset(K, o, 4 * b + j);
                 for (int h = 0; h < 2; ++h) {
                     int sc, m;
                     q4k_scale_min(blk + 4, 2 * j + h, &sc, &m);
@@ -192,18 +214,17 @@ int oracle_q4k_tc_relayout(const uint8_t *W, int64_t K, int64_t N, uint8_t *R)
     return 0;
 }
 
-/* R [N][K/64 chunks] → out [N][K] fp32: value i < 32 of chunk c is
- * s_lo·(qs[i] & 15) − o_lo, value 32 + i is s_hi·(qs[i] >> 4) − o_hi,
- * evaluated in double and rounded once to float.  Returns 0, or -1 on bad
- * sizes. */
+/* R → out [N][K] fp32: value i < 32 of chunk c is s_lo·(qs[i] & 15) − o_lo,
+ * value 32 + i is s_hi·(qs[i] >> 4) − o_hi, evaluated in double and rounded
+ * once to float.  Returns 0, or -1 on bad sizes. */
 int oracle_q4k_tc_dequant(const uint8_t *R, int64_t K, int64_t N, float *out)
 {
-    if (K <= 0 || N <= 0 || K % 64)
+    if (oracle_q4k_tc_bytes(K, N) < 0)
         return -1;
     int64_t nc = K / 64;
     for (int64_t o = 0; o < N; ++o) {
         for (int64_t c = 0; c < nc; ++c) {
-            const uint8_t *ch = R + (o * nc + c) * Q4K_TC_CHUNK_BYTES;
+            const uint8_t *ch = R + tc_chunk_offset(K, o, c);
             double s_lo = get_f32(ch), o_lo = get_f32(ch + 4);
             double s_hi = get_f32(ch + 8), o_hi = get_f32(ch + 12);
             float *w = out + o * K + c * 64;

@@ -419,17 +419,32 @@ def pin_q6k_fraction_bruteforce(lib):
                 assert abs(Fraction(y[t, o]) - e) <= Fraction(1, 10 ** 9) * (1 + abs(e)), (t, o)
 
 
+def _tc_chunk(R, K, o, c):
+    """The 48 bytes of chunk c of row o in the tile-major relayout."""
+    t, r = divmod(o, 256)
+    off = ((t * (K // 64) + c) * 256 + r) * 48
+    return R[off:off + 48]
+
+
 def pin_tc_relayout_handworked(lib):
     # The relayout of the hand-worked block against bytes worked out by hand,
     # and its values against the block's own hand-worked values.
     fx, blk = _hand_block(lib)
     tx = fixtures.read("q4k_tc_relayout_handworked.txt")
-    R = oracle.q4k_tc_relayout(blk, 256, 1, lib=lib).reshape(4, 48)
+    R = oracle.q4k_tc_relayout(blk, 256, 1, lib=lib)
+    assert R.size == int(tx["bytes"])
     for j in range(4):
-        words = R[j, :16].copy().view("<u4")
+        ch = _tc_chunk(R, 256, 0, j)
+        assert int(tx[f"chunk_{j}_offset"]) == ch.ctypes.data - R.ctypes.data
+        words = ch[:16].copy().view("<u4")
         assert [int(v) for v in words] == [int(v, 16) for v in tx[f"chunk_{j}_words"].split()], j
-    assert list(R[0, 16:20]) == fixtures.hexbytes(tx["chunk_0_qs_0_3"])
-    assert list(R[1, 16:20]) == fixtures.hexbytes(tx["chunk_1_qs_0_3"])
+    assert list(_tc_chunk(R, 256, 0, 0)[16:20]) == fixtures.hexbytes(tx["chunk_0_qs_0_3"])
+    assert list(_tc_chunk(R, 256, 0, 1)[16:20]) == fixtures.hexbytes(tx["chunk_1_qs_0_3"])
+    # Rows 1..255 of the tile are padding.
+    mask = np.ones(R.size, bool)
+    for j in range(4):
+        mask[j * 256 * 48:j * 256 * 48 + 48] = False
+    assert not R[mask].any()
     w = oracle.q4k_tc_dequant(R, 256, 1, lib=lib)[0]
     for e in (0, 31, 32, 255):
         assert w[e] == float(fx[f"w_{e}"]), (e, w[e])
@@ -437,21 +452,21 @@ def pin_tc_relayout_handworked(lib):
 
 def pin_tc_relayout_round_trip(lib):
     # The relayouted weight is the same matrix: its dequantization equals the
-    # canonical block's bit for bit, over random blocks and the extremes of
-    # the fp16 factors (subnormal, largest finite, zero) and of the 6-bit
-    # fields (0 and 63).
+    # canonical block's bit for bit, over random blocks, rows in two tiles,
+    # and the extremes of the fp16 factors (subnormal, largest finite, zero)
+    # and of the 6-bit fields (0 and 63).
     g = np.random.default_rng(13)
-    K, N = 768, 6
+    K, N = 768, 300
     W = synth.q4k_weights(g, N, K).reshape(N, K // 256, 144).copy()
     heads = [(0x0001, 0x7BFF), (0x7BFF, 0x0001), (0x0000, 0x3C00), (0x3C00, 0x0000), (0x03FF, 0x0400)]
     for i, (d, dm) in enumerate(heads):
         o, b = divmod(i, K // 256)
-        W[o, b, 0:4] = [d & 255, d >> 8, dm & 255, dm >> 8]
+        W[o + 255, b, 0:4] = [d & 255, d >> 8, dm & 255, dm >> 8]
     W[4, 0, 4:16] = 0xFF   # every sc and m = 63
     W[4, 1, 4:16] = 0x00   # every sc and m = 0
     W = W.reshape(-1)
     R = oracle.q4k_tc_relayout(W, K, N, lib=lib)
-    assert R.size == N * K // 64 * 48
+    assert R.size == 512 * K // 64 * 48
     a = oracle.q4k_tc_dequant(R, K, N, lib=lib)
     b = oracle.q4k_dequant(W, K, N, lib=lib)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
@@ -459,17 +474,19 @@ def pin_tc_relayout_round_trip(lib):
 
 def pin_tc_chunk_positions(lib):
     # One nonzero code byte at row o, block b, slab j, byte l lands in chunk
-    # o·K/64 + 4b + j at byte 16 + l, and nowhere else.
-    K, N = 512, 3
+    # 4b + j of row o: tile o // 256, run (tile·K/64 + 4b + j), row o mod 256
+    # of the run, byte 16 + l; nowhere else.
+    K, N = 512, 300
     base = np.zeros((N, K // 256, 144), np.uint8)
     base[:, :, 0:2] = [0x00, 0x3C]
-    for (o, b, j, l) in ((0, 0, 0, 0), (1, 1, 3, 31), (2, 0, 2, 7), (2, 1, 1, 16)):
+    for (o, b, j, l) in ((0, 0, 0, 0), (1, 1, 3, 31), (255, 0, 2, 7), (256, 1, 1, 16), (299, 0, 3, 5)):
         W = base.copy()
         W[o, b, 16 + 32 * j + l] = 0xAB
-        R = oracle.q4k_tc_relayout(W.reshape(-1), K, N, lib=lib).reshape(N * K // 64, 48)
-        hit = np.argwhere(R[:, 16:] != 0)
-        assert hit.tolist() == [[o * (K // 64) + 4 * b + j, l]], (o, b, j, l, hit.tolist())
-        assert R[o * (K // 64) + 4 * b + j, 16 + l] == 0xAB
+        R = oracle.q4k_tc_relayout(W.reshape(-1), K, N, lib=lib)
+        hit = np.flatnonzero(R.reshape(-1, 48)[:, 16:])
+        t, r = divmod(o, 256)
+        want = (((t * (K // 64) + 4 * b + j) * 256 + r) * 32) + l
+        assert hit.tolist() == [want], (o, b, j, l, hit.tolist(), want)
 
 
 ALL_PINS = [

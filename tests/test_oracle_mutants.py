@@ -59,6 +59,8 @@ MUTANTS = {
     "tc_scale_min_swapped": ("put_f32(ch + 8 * h, d * sc);\n                    put_f32(ch + 8 * h + 4, dmin * m);",
                              "put_f32(ch + 8 * h + 4, d * sc);\n                    put_f32(ch + 8 * h, dmin * m);"),
     "tc_slab_order": ("memcpy(ch + 16, blk + 16 + 32 * j, 32);", "memcpy(ch + 16, blk + 16 + 32 * (3 - j), 32);"),
+    "tc_row_major": ("return ((t * (K / 64) + c) * Q4K_TC_TILE_ROWS + r) * Q4K_TC_CHUNK_BYTES;",
+                     "return (o * (K / 64) + c) * Q4K_TC_CHUNK_BYTES;"),
     "tc_offset_sign": ("w[i] = (float)(s_lo * (ch[16 + i] & 15) - o_lo);",
                        "w[i] = (float)(s_lo * (ch[16 + i] & 15) + o_lo);"),
     "tc_high_nibble": ("w[32 + i] = (float)(s_hi * (ch[16 + i] >> 4) - o_hi);",
