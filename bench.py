@@ -48,6 +48,7 @@ if ROOT not in sys.path:
 METRIC = "Q4_K GEMV weight-stream GB/s and % of GB300 HBM peak at 4096×4096, batch 1"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1700.0
+FALLBACK_BF16_TFLOPS_BURST = 1900.0
 # FP32 FMA peak: 152 SMs × 128 FP32 lanes × 2 flop per FMA × 2.07 GHz (maximum SM clock).
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 CSRC = os.path.join(ROOT, "quantized_matmul_q4_gb300", "csrc")
@@ -83,6 +84,8 @@ def weight_bytes(kind, K, N):
         return N * (K // 32) * 18
     if kind == "q4k_ffn":
         return 2 * _q4k_bytes(K, N)
+    if kind == "q4k_tc":
+        return -(-N // 256) * 256 * (K // 64) * 48
     if kind == "q6k":
         return N * (K // 256) * 210
     return N * (K // 4)
@@ -112,6 +115,12 @@ WORKLOADS = {w.name: w for w in [
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands",
              ["q4k_mm_tc.cu", "cluster.cuh"], "q4k_mm_tc_4096x11008_t64.md", arithmetic="bf16 operands (dequantized in fp32, rounded once), "
                                           "fp32 accumulation in tensor memory"),
+    Workload("q4k_prefill_tc_relayout_4096x11008_t64", "q4k_tc", "q4k_matmul_tc_relayouted", [(4096, 11008)],
+             64, 16, "TFLOP/s", "tensor", "q4k_mm_tc_kernel",
+             "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, tcgen05 with bf16 operands, weights relayouted "
+             "once for the tensor cores", ["q4k_mm_tc.cu", "cluster.cuh"], "q4k_mm_tc_relayout_4096x11008_t64.md",
+             arithmetic="bf16 operands (dequantized in fp32 from pre-decoded fp32 sub-block scales, rounded "
+                        "once), fp32 accumulation in tensor memory"),
     Workload("q4k_prefill_fp32_4096x11008_t64", "q4k", "q4k_matmul", [(4096, 11008)], 64, 16,
              "TFLOP/s", "alu", "q4k_mm_fp32_kernel",
              "Q4_K prefill TFLOP/s, 64 tokens x 4096 -> 11008, FP32 FMA", ["q4k_mm_fp32.cu", "cluster.cuh"],
@@ -287,11 +296,12 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]),
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
                 "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained") or d["bf16_tflops"]),
                 "source": "measured (MEASURED_PEAKS.json)"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS,
-            "source": "fallback (6.8 TB/s, 1.7 PFLOP/s bf16 sustained)"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS_BURST,
+            "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS,
+            "source": "fallback (6.8 TB/s, 1.9 PFLOP/s bf16 burst, 1.7 sustained)"}
 
 
 def kernel_source_hash(w: Workload) -> str:
@@ -359,7 +369,7 @@ def host_inputs(w: Workload, seed: int = 0):
     mats = []
     for K, N in w.mats:
         n = max(1, w.distinct)
-        if w.kind == "q4k":
+        if w.kind in ("q4k", "q4k_tc"):
             Ws = [synth.q4k_weights(g, N, K) for _ in range(n)]
         elif w.kind == "q4_0":
             Ws = [synth.q4_0_weights(g, N, K) for _ in range(n)]
@@ -384,14 +394,16 @@ def workload_config(w: Workload, plan: Plan) -> dict:
             "weight_bytes_per_step": plan.weight_bytes,
             "l2": f"inputs larger than L2: {plan.weight_bytes / 1e6:.0f} MB of weights per step "
                   f"(L2 129 MB), no flush",
-            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks', q4k_ffn='Q4_K blocks (gate, up)', q6k='Q6_K blocks').get(w.kind, 'ternary codes')}, seed 0 "
+            "weights": f"random {dict(q4k='Q4_K blocks', q4_0='Q4_0 blocks', q4k_ffn='Q4_K blocks (gate, up)', q6k='Q6_K blocks', q4k_tc='Q4_K blocks relayouted once on the GPU by q4k_relayout_tc (not timed)').get(w.kind, 'ternary codes')}, seed 0 "
                        f"(synth), {w.distinct} distinct host copies per matrix",
             "activations": "fp32 N(0,1), seed 0"}
 
 
 def oracle_call(w: Workload, K, N, W, x, scale, rows, r0=0):
     import oracle
-    if w.kind == "q4k":
+    if w.kind in ("q4k", "q4k_tc"):
+        # The relayouted weight is the same matrix: the oracle takes the
+        # canonical blocks it was made from.
         oracle.q4k_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
     elif w.kind == "q4_0":
         oracle.q4_0_matmul(x, W.reshape(N, -1)[r0:r0 + rows], K, rows)
@@ -506,7 +518,14 @@ def run_ours(a) -> None:
         nb = weight_bytes(w.kind, K, N)
         k = seen.get(m, 0)
         seen[m] = k + 1
-        W[wo:wo + nb].copy_(torch.from_numpy(Ws[k % len(Ws)].reshape(-1)))
+        if w.kind == "q4k_tc":
+            # The one-time relayout, on the GPU, before anything is timed.
+            canon = torch.from_numpy(Ws[k % len(Ws)].reshape(-1)).to(device)
+            q.q4k_relayout_tc_ptr(canon.data_ptr(), W.data_ptr() + wo, K, N, 0)
+            torch.cuda.synchronize(device)
+            del canon
+        else:
+            W[wo:wo + nb].copy_(torch.from_numpy(Ws[k % len(Ws)].reshape(-1)))
         x_host[xo:xo + w.tokens * K] = torch.from_numpy(xm.reshape(-1))
     x.copy_(x_host)
     torch.cuda.synchronize(device)
@@ -583,11 +602,14 @@ def run_ours(a) -> None:
                     "frac": hbm_achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " hbm_gbs"}
     else:
         tflops = plan.flops / step_s / 1e12
-        peak = peaks["bf16_tflops_sustained"] if w.bound == "tensor" else FP32_FMA_TFLOPS
-        src = (peaks["source"] + " bf16_tflops_sustained" if w.bound == "tensor" else
+        # A tensor-core kernel is held to the burst cuBLAS rate (the higher
+        # of the two measured figures); the sustained rate is reported beside it.
+        peak = peaks["bf16_tflops"] if w.bound == "tensor" else FP32_FMA_TFLOPS
+        src = (peaks["source"] + " bf16_tflops (burst)" if w.bound == "tensor" else
                "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz")
         roofline = {"bound": w.bound, "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                     "frac": tflops / peak, "peak_source": src,
+                    **({"frac_of_sustained": tflops / peaks["bf16_tflops_sustained"]} if w.bound == "tensor" else {}),
                     "hbm": {"achieved": hbm_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": hbm_achieved / peaks["hbm_gbs"]}}
     roofline.update({"traffic": traffic, "kernel": w.kernel,

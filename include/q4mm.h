@@ -248,6 +248,64 @@ int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *
 int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int inputDim,
                           int outputDim, int tokens, q4mm_stream_t stream);
 
+/* Bytes per row and 64-value chunk of the relayouted tensor-core layout, rows
+ * per tile, and the size of a relayouted inputDim → outputDim weight (rows
+ * rounded up to whole tiles). */
+#define Q4MM_TC_CHUNK_BYTES 48
+#define Q4MM_TC_TILE_ROWS 256
+#define Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim)                                                \
+    (((size_t)(outputDim) + Q4MM_TC_TILE_ROWS - 1) / Q4MM_TC_TILE_ROWS * Q4MM_TC_TILE_ROWS *        \
+     (size_t)((inputDim) / 64) * Q4MM_TC_CHUNK_BYTES)
+
+/*
+ * q4k_relayout_tc — the one-time relayout of a Q4_K weight for
+ * q4k_matmul_tc_relayouted: done once when the weight is registered, not on
+ * every call (SKaiNET docs "Eager execution: backends and kernels", the
+ * paragraph on weights relayouted once rather than per call; the page names
+ * no target layout, so this one is the library's own).
+ *
+ * Layout written to w_tc.  Each 64-value chunk c of a row (values
+ * 64c..64c+63: the slab j = c mod 4 of block b = c/4, its 32 code bytes
+ * qs[32j..32j+31], low nibbles = sub-block 2j, high nibbles = 2j+1) becomes
+ * 48 bytes:
+ *   bytes  0..3  fp32 d·sc(2j)      bytes  4..7  fp32 dmin·m(2j)
+ *   bytes  8..11 fp32 d·sc(2j+1)    bytes 12..15 fp32 dmin·m(2j+1)
+ *   bytes 16..47 the 32 code bytes, unchanged
+ * (floats little-endian).  Rows are grouped in tiles of Q4MM_TC_TILE_ROWS
+ * (256), the last tile padded with zero rows, and stored tile-major: chunk c
+ * of the 256 rows of tile t is one contiguous run of 256·48 bytes at byte
+ * (t·(inputDim/64) + c)·12288, row r of the tile at 48·r within it.  The
+ * tensor-core kernel then fetches each chunk of a tile with one plain bulk
+ * copy.  Every product is exact in fp32, so the relayouted weight
+ * dequantizes to the same fp32 matrix (w = scale·q − offset), and
+ * q4k_matmul_tc_relayouted gives bit for bit the result of q4k_matmul_tc on
+ * the canonical weight.  The layout keeps products, not factors: it cannot
+ * be turned back into the canonical bytes.  It is about 4/3 the size of the
+ * canonical weight (0.75·inputDim bytes per row, plus padding rows, against
+ * 0.5625·inputDim).
+ *
+ * Arguments: w_q4k (device, read) the canonical weight, outputDim rows of
+ * inputDim/256 blocks of 144 bytes; w_tc (device, written, padding rows
+ * included) a buffer of Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim) bytes
+ * owned by the caller.  Both 16-byte aligned, not overlapping; inputDim a
+ * positive multiple of 256 up to Q4MM_MAX_INPUT_DIM, outputDim positive.
+ * Asynchronous on `stream`; allocates nothing.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q4k_relayout_tc(const void *w_q4k, void *w_tc, int inputDim, int outputDim, q4mm_stream_t stream);
+
+/*
+ * q4k_matmul_tc_relayouted — q4k_matmul_tc on a weight made by
+ * q4k_relayout_tc: the same kernels, tiles, precision, scratch and results
+ * (bit for bit); the dequantizing warps read the two sub-block scales of a
+ * chunk as ready fp32 values instead of decoding the 6-bit scale field.
+ * w_tc: Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim) bytes as q4k_relayout_tc
+ * wrote them, 16-byte aligned.  Everything else as q4k_matmul_tc.
+ * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
+ */
+int q4k_matmul_tc_relayouted(const float *x, const void *w_tc, float *y, int inputDim, int outputDim,
+                             int tokens, q4mm_stream_t stream);
+
 /*
  * ternary_gemv — y = scale · (x·codesᵀ) with W in the BitNet b1.58 payload.
  *

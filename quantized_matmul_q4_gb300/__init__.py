@@ -23,6 +23,11 @@ from ._binding import (  # noqa: F401
     q4k_matmul_tc_ptr,
     q4k_matmul_tc_noalloc,
     q4k_matmul_tc_noalloc_ptr,
+    q4k_relayout_tc,
+    tc_relayout_bytes,
+    q4k_relayout_tc_ptr,
+    q4k_matmul_tc_relayouted,
+    q4k_matmul_tc_relayouted_ptr,
     q4_0_gemv,
     q4_0_gemv_ptr,
     q6k_gemv,

@@ -8,8 +8,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 Q4K_VALUES = 256
 Q4K_BYTES = 144
 
-_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q6k_gemv", "q4k_ffn_swiglu",
-            "ternary_gemv",
+_SYMBOLS = ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4k_relayout_tc", "q4k_matmul_tc_relayouted",
+            "q4_0_gemv", "q6k_gemv", "q4k_ffn_swiglu", "ternary_gemv",
             "q4mm_last_error", "q4mm_device_status", "q4mm_version", "q4mm_test_fail_next_wait")
 
 
@@ -33,10 +33,13 @@ def _load() -> ctypes.CDLL:
             "(needs nvcc); there is no fallback implementation")
     lib = ctypes.CDLL(path)
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4_0_gemv", "q6k_gemv"):
+    for name in ("q4k_matmul", "q4k_matmul_tc", "q4k_matmul_tc_noalloc", "q4k_matmul_tc_relayouted", "q4_0_gemv",
+                 "q6k_gemv"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         fn.restype = i32
+    lib.q4k_relayout_tc.argtypes = [vp, vp, i32, i32, vp]
+    lib.q4k_relayout_tc.restype = i32
     lib.q4k_ffn_swiglu.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
     lib.q4k_ffn_swiglu.restype = i32
     lib.ternary_gemv.argtypes = [vp, vp, f32, vp, i32, i32, i32, vp]
@@ -91,6 +94,14 @@ def q4k_matmul_tc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: in
 
 def q4k_matmul_tc_noalloc_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
     _check(_LIB.q4k_matmul_tc_noalloc(x, w, y, K, N, T, stream))
+
+
+def q4k_relayout_tc_ptr(w: int, w_tc: int, K: int, N: int, stream: int = 0) -> None:
+    _check(_LIB.q4k_relayout_tc(w, w_tc, K, N, stream))
+
+
+def q4k_matmul_tc_relayouted_ptr(x: int, w_tc: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
+    _check(_LIB.q4k_matmul_tc_relayouted(x, w_tc, y, K, N, T, stream))
 
 
 def q4_0_gemv_ptr(x: int, w: int, y: int, K: int, N: int, T: int, stream: int = 0) -> None:
@@ -164,6 +175,46 @@ def q4k_matmul_tc_noalloc(x, w, N: int | None = None, out=None, stream=None):
     (no allocation; calls that overlap on the GPU race on that array)."""
     x2, T, K, N, out = _prep(x, w, None, lambda k: (k // Q4K_VALUES) * Q4K_BYTES, out, N)
     q4k_matmul_tc_noalloc_ptr(x2.data_ptr(), w.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
+    return out.view(T, N)
+
+
+TC_CHUNK_BYTES = 48  # relayouted bytes per row and 64 values
+TC_TILE_ROWS = 256   # rows per tile of the relayouted layout
+
+
+def tc_relayout_bytes(K: int, N: int) -> int:
+    """Size of a relayouted K -> N weight (rows rounded up to whole tiles)."""
+    return -(-N // TC_TILE_ROWS) * TC_TILE_ROWS * (K // 64) * TC_CHUNK_BYTES
+
+
+def q4k_relayout_tc(w, K: int, N: int | None = None, out=None, stream=None):
+    """The one-time relayout of a canonical Q4_K weight for
+    q4k_matmul_tc_relayouted: a uint8 CUDA tensor of tc_relayout_bytes(K, N)
+    bytes (tile-major, zero rows padding the last 256-row tile)."""
+    import torch
+    if w.dtype != torch.uint8 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("the packed weight must be a contiguous uint8 CUDA tensor")
+    row = (K // Q4K_VALUES) * Q4K_BYTES
+    if N is None:
+        if row <= 0 or w.numel() % row:
+            raise ValueError("weight size is not a whole number of rows")
+        N = w.numel() // row
+    nbytes = tc_relayout_bytes(K, N)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    elif out.dtype != torch.uint8 or not out.is_cuda or not out.is_contiguous() or out.numel() != nbytes:
+        raise ValueError("out must be a contiguous uint8 CUDA tensor of tc_relayout_bytes(K, N) bytes")
+    q4k_relayout_tc_ptr(w.data_ptr(), out.data_ptr(), K, N, _stream_ptr(stream))
+    return out
+
+
+def q4k_matmul_tc_relayouted(x, w_tc, N: int, out=None, stream=None):
+    """q4k_matmul_tc on a weight relayouted by q4k_relayout_tc (N is
+    required: the padded layout does not give it)."""
+    if w_tc.numel() != tc_relayout_bytes(x.shape[-1], N):
+        raise ValueError("w_tc size does not match tc_relayout_bytes(K, N)")
+    x2, T, K, N, out = _prep(x, w_tc, None, lambda k: (k // 64) * TC_CHUNK_BYTES, out, N)
+    q4k_matmul_tc_relayouted_ptr(x2.data_ptr(), w_tc.data_ptr(), out.data_ptr(), K, N, T, _stream_ptr(stream))
     return out.view(T, N)
 
 

@@ -232,6 +232,45 @@ int q4k_matmul_tc_noalloc(const float *x, const void *w_q4k, float *y, int input
     return Q4MM_OK;
 }
 
+int q4k_relayout_tc(const void *w_q4k, void *w_tc, int inputDim, int outputDim, q4mm_stream_t stream) {
+    if (!w_q4k || !w_tc) return fail(Q4MM_ERR_NULL, "w_q4k and w_tc must be non-NULL");
+    if (inputDim <= 0 || outputDim <= 0)
+        return fail(Q4MM_ERR_DIM, "inputDim (%d) and outputDim (%d) must be positive", inputDim, outputDim);
+    if (inputDim % 256) return fail(Q4MM_ERR_DIM, "inputDim %d is not a multiple of 256", inputDim);
+    if (inputDim > Q4MM_MAX_INPUT_DIM)
+        return fail(Q4MM_ERR_DIM, "inputDim %d exceeds the limit %d", inputDim, Q4MM_MAX_INPUT_DIM);
+    if (reinterpret_cast<uintptr_t>(w_q4k) % 16 || reinterpret_cast<uintptr_t>(w_tc) % 16)
+        return fail(Q4MM_ERR_ALIGN, "w_q4k and w_tc must be 16-byte aligned");
+    const size_t wb = (size_t)outputDim * (inputDim / 256) * 144;
+    if (overlap(w_q4k, wb, w_tc, Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim)))
+        return fail(Q4MM_ERR_ALIAS, "w_q4k and w_tc must not overlap");
+    q4mm::LaunchCtx ctx;
+    int rc;
+    if ((rc = device_ctx(stream, &ctx, false))) return rc;
+    const cudaError_t e = q4mm::launch_q4k_relayout_tc(ctx, static_cast<const uint8_t *>(w_q4k),
+                                                       static_cast<uint8_t *>(w_tc), inputDim, outputDim);
+    if (e != cudaSuccess) return fail_cuda(e, "q4k_relayout_tc launch");
+    return Q4MM_OK;
+}
+
+int q4k_matmul_tc_relayouted(const float *x, const void *w_tc, float *y, int inputDim, int outputDim, int tokens,
+                             q4mm_stream_t stream) {
+    // The weight-overlap check takes the padded size: a per-row figure
+    // rounded up so that N rows cover Q4MM_TC_RELAYOUT_BYTES.
+    int rc = check_common(x, w_tc, y, inputDim, outputDim, tokens, 256,
+                          outputDim > 0 && inputDim > 0
+                              ? (Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim) + outputDim - 1) / (size_t)outputDim
+                              : 0,
+                          16);
+    if (rc) return rc;
+    q4mm::LaunchCtx ctx;
+    if ((rc = device_ctx(stream, &ctx))) return rc;
+    cudaError_t e = q4mm::launch_q4k_mm_tc_relayouted(ctx, x, static_cast<const uint8_t *>(w_tc), y, inputDim,
+                                                      outputDim, tokens);
+    if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul_tc_relayouted launch");
+    return Q4MM_OK;
+}
+
 int q4_0_gemv(const float *x, const void *w_q4_0, float *y, int inputDim, int outputDim, int tokens,
               q4mm_stream_t stream) {
     int rc = check_common(x, w_q4_0, y, inputDim, outputDim, tokens, 256,

@@ -56,6 +56,14 @@ cudaError_t launch_q4k_mm_fp32(const LaunchCtx &c, const float *x, const uint8_t
 cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
                              int N, int T);
 
+// The tensor-core prefill on a weight in the relayouted tensor-core layout
+// (48 bytes per row and 64-value chunk), and the one-time relayout that
+// makes it from a canonical Q4_K weight (q4k_relayout_tc_bytes(K, N) bytes).
+cudaError_t launch_q4k_mm_tc_relayouted(const LaunchCtx &c, const float *x, const uint8_t *R, float *y, int K,
+                                        int N, int T);
+size_t q4k_relayout_tc_bytes(int K, int N);
+cudaError_t launch_q4k_relayout_tc(const LaunchCtx &c, const uint8_t *W, uint8_t *R, int K, int N);
+
 // The tensor-core prefill with its scratch in a fixed array of library
 // memory (no allocation): bytes of scratch a call needs, and the launcher
 // (cudaErrorInvalidValue if the need exceeds the array).

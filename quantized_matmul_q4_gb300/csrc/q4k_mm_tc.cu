@@ -3,14 +3,28 @@
 //
 // y[t][o] = Σ_k x[t][k]·w[o][k] with w = d·sc_s·q − dmin·m_s (SKaiNET PR #562
 // "feat(kernel): SIMD-fused Q4_K matmul kernel + Q4KMatmulKernel SPI",
-// section "Pipeline"), evaluated as D[t][o] = A[t][k]·B[o][k] with
-//   A = the activations rounded to bf16 (M = 128 token rows; tokens past the
-//       tile's count read as zero),
-//   B = the dequantized weights rounded to bf16 (N = 256 output rows),
-//   D = fp32 in tensor memory, K = 16 per MMA instruction.
-// A tcgen05.mma instruction's time grows far less than its size (measured
-// on GB300: 108 cycles at 128 × 128 × 16, 130 at 128 × 256 × 16), so each
-// instruction is made as large as the tile allows: 128 × 256 × 16.
+// section "Pipeline"), evaluated as D[o][t] = A[o][k]·B[t][k] with
+//   A = the dequantized weights rounded to bf16, M = 128 weight rows per
+//       MMA, held in TENSOR MEMORY: the dequant warps write each chunk of A
+//       there with tcgen05.st, so the dequantized operand never passes
+//       through shared memory,
+//   B = the activations rounded to bf16 (N = the tile's tokens rounded up to
+//       16, at most 128), K-major in shared memory with the 128-byte swizzle,
+//   D = fp32 in tensor memory, one 128 × N accumulator per 128 weight rows.
+// Putting the tokens on N sizes every MMA to the tile: 64 tokens run
+// 128 × 64 × 16 instructions (measured on GB300: 46 cycles each, 70% of the
+// tensor pipe's rate; N = 128 and 256 run at the full rate), with no padded
+// token rows.
+//
+// Weights stream through a ring of chunk stages (256 rows × 64 values of K,
+// 12 KB): in the canonical 144-byte Q4_K layout a stage is two 2-D tensor
+// copies (the 16-byte header of every row's block and the 32 code bytes of
+// the chunk's slab: 256 short pieces, one per row); in the relayouted
+// tensor-core layout (48 bytes per row and chunk: fp32 d·sc and dmin·m of
+// the slab's two sub-blocks, then its 32 code bytes; tile-major, so that a
+// chunk of a 256-row tile is one 12 KB run) it is one plain bulk copy of
+// contiguous bytes, a CTA's whole weight range is one run in memory, and
+// the scales arrive already decoded.
 //
 // Up to 128 tokens (one tile) the dequant warps also read fp32 x, round it
 // to bf16 and write each chunk's activation tile in the swizzled layout the
@@ -23,33 +37,40 @@
 // Grid: clusters of S CTAs (3, or 4 above K = 49152) per 256-row tile, CTA
 // rank r of a cluster taking 64-value chunks [r·nc/S, (r+1)·nc/S) of K, so
 // that the 43 row tiles of an 11008-row weight spread over 129 SMs.  Each
-// CTA accumulates its K range in one tensor-memory accumulator (at most
-// 16384 values of K, within which the tensor core's fp32 accumulation stays
-// far inside the stated tolerance).  Every rank copies its accumulator into
-// its own shared memory; after a cluster barrier each rank takes one S-th of
-// the tile's outputs, adds the S ranks' values in rank order through
-// distributed shared memory and writes them to y, so the result does not
-// depend on scheduling and no partial sum goes through global memory.
+// CTA accumulates its K range in tensor memory (at most 16384 values of K,
+// within which the tensor core's fp32 accumulation stays far inside the
+// stated tolerance).  Every rank copies its accumulators into its own shared
+// memory; after a cluster barrier each rank takes one S-th of the tile's
+// outputs, adds the S ranks' values in rank order through distributed shared
+// memory and writes them to y, so the result does not depend on scheduling
+// and no partial sum goes through global memory.
+//
+// Tensor memory (512 columns, one CTA per SM): D of row half m at columns
+// c_D·m .. c_D·m + N, with c_D = 64 up to 64 tokens and 128 above; A of
+// operand stage s, row half m at 2·c_D + 64·s + 32·m (32 columns: 64 bf16
+// values of K per lane, two per column, lower K in the low half).  The
+// operand ring is as deep as the remaining columns allow: 6 stages up to 64
+// tokens, 4 above.  A stage is released when its MMAs complete, so the ring
+// must cover the MMAs' completion latency as well as the dequantization of
+// the next chunks: measured on GB300, 4 stages held 64-token MMAs to about
+// half of the tensor pipe's rate.
 //
 // Roles in a CTA:
-//  * warp 16 (one thread) issues 2-D TMA tensor loads: a Q4_K block column
-//    (256 rows × 144 bytes) per 256 values of K, before the wait on the
-//    previous kernel, and (tiles of the bf16 copy) a bf16 activation tile
-//    (128 tokens × 64 values) per chunk of 64 values, after it, each as soon
-//    as its ring slot is free.
-//  * warps 0–15 dequantize: thread (r, h), r = t mod 256 and h = t / 256,
-//    turns qs bytes 16h..16h+15 of row r's slab into 16 low-nibble values of
-//    sub-block 2j and 16 high-nibble values of 2j+1.  Each nibble becomes a float with one logic op (2^23 + q·2^p), one
-//    paired FMA with the scale at 2^-p and −scale·2^(23−p) gives scale·q
-//    exactly, one paired add removes the min term (the single rounding of the
-//    fp32 dequantization), and one conversion packs two bf16.  Results go in
-//    the 128-byte-swizzled K-major layout; with fused activations the same
-//    threads also write the chunk's activation tile.  The writes are fenced
-//    to the async proxy before the chunk's barrier arrive.
-//  * warp 17 allocates the accumulator in tensor memory; its first thread
-//    issues four 128×256×16 MMAs per chunk and commits them to the chunk's
-//    activation and weight slots.
-//  * warps 0–15 then read the accumulator (tcgen05.ld) into shared memory,
+//  * warp 16 (one thread) issues the weight chunk copies, before the wait on
+//    the previous kernel, and (from the bf16 copy) the activation tiles after
+//    it, each as soon as its ring slot is free.
+//  * warps 0–15 dequantize: warp w serves tensor-memory lane quarter w mod 4
+//    of row half (w / 4) mod 2, and the chunks c ≡ w / 8 (mod 2); each thread
+//    turns the 32 code bytes of its row's chunk into 64 bf16 values: each
+//    nibble becomes a float with one logic op (2^23 + q·2^p), one paired FMA
+//    with the scale at 2^-p and −scale·2^(23−p) gives scale·q exactly, one
+//    paired add removes the min term (the single rounding of the fp32
+//    dequantization), and one conversion packs two bf16.  With fused
+//    activations the same threads also write the chunk's activation tile.
+//  * warp 17 allocates tensor memory; the first threads of warps 17 and 18
+//    issue the chunk's MMAs of row half 0 and 1 (four K steps of 16 each)
+//    and commit them to the chunk's ring stage.
+//  * warps 0–15 then read the accumulators (tcgen05.ld) into shared memory,
 //    and every thread takes part in the cluster-wide reduction.
 // All mbarrier waits are bounded; a time-out sets the device status word and
 // every thread still reaches the two cluster barriers.
@@ -71,33 +92,35 @@ namespace q4mm {
 
 namespace {
 
-constexpr int kTcRows = 256;                       // MMA N: weight rows per CTA
-constexpr int kTcTok = 128;                        // MMA M: token rows per tile
+constexpr int kTcRows = 256;                       // weight rows per CTA: two MMAs of M = 128
+constexpr int kTcM = 128;                          // MMA M: weight rows of one tensor-memory accumulator
+constexpr int kTcTok = 128;                        // token rows per tile (MMA N at most)
 constexpr int kTcKc = 64;                          // K per chunk: a 128-byte row of bf16
 constexpr int kTcDqWarps = 16;                     // dequant + epilogue warps
 constexpr int kTcWarpTma = kTcDqWarps;             // TMA producer warp
-constexpr int kTcWarpMma = kTcDqWarps + 1;         // MMA issuer warp
-constexpr int kTcThreads = 32 * (kTcDqWarps + 2);
-constexpr int kTcDq = 32 * kTcDqWarps;             // dequant threads (two per weight row)
-constexpr int kTcWStages = 2;                      // Q4_K block-column tiles in flight
-constexpr int kTcAStages = 3;                      // bf16 activation tiles in flight
-constexpr int kTcBStages = 3;                      // bf16 weight operand tiles in flight
-static_assert(kTcAStages == kTcBStages, "fused activation tiles share the weight ring's slots");
-constexpr uint32_t kTcWTileBytes = kTcRows * kQ4kBytes;  // 36864
-constexpr uint32_t kTcATileBytes = kTcTok * 128;         // 16384
-constexpr uint32_t kTcBTileBytes = kTcRows * 128;        // 32768
+constexpr int kTcWarpMma = kTcDqWarps + 1;         // MMA issuer warps: kTcWarpMma + m for row half m
+constexpr int kTcThreads = 32 * (kTcDqWarps + 3);
+constexpr int kTcGroupWarps = kTcDqWarps / 2;      // warps per chunk (alternate chunks per group)
+constexpr int kTcWStages = 8;                      // weight chunk stages in flight
+constexpr int kTcStagesMax = 6;                    // operand stages (A in tensor memory, B in shared memory):
+                                                   // 6 up to 64 tokens, 4 above (tensor-memory columns)
+constexpr int kTcChunkBytes = 48;                  // relayouted bytes per row and chunk
+constexpr uint32_t kTcWStageBytes = kTcRows * kTcChunkBytes;  // 12288: both layouts
+constexpr uint32_t kTcXTileBytes = kTcTok * 128;              // 16384: the largest activation tile
+constexpr uint32_t kTcXRegion = 4 * kTcXTileBytes;            // 4 tiles of 128 tokens or 6 of 64
 constexpr int kTcMaxKPerCta = 16384;               // one accumulator per CTA
-constexpr uint32_t kTcTmemCols = kTcRows;          // fp32 accumulator columns
+constexpr uint32_t kTcTmemCols = 512;              // the whole of tensor memory
 
 struct TcLayout {
-    static constexpr uint32_t off_a = 0;
-    static constexpr uint32_t off_b = off_a + kTcAStages * kTcATileBytes;
-    static constexpr uint32_t off_w = off_b + kTcBStages * kTcBTileBytes;
-    static constexpr uint32_t off_bar = off_w + kTcWStages * kTcWTileBytes;
-    static constexpr uint32_t n_bars = 2 * kTcWStages + 2 * kTcAStages + 2 * kTcBStages + 1;
+    static constexpr uint32_t off_x = 0;
+    static constexpr uint32_t off_w = off_x + kTcXRegion;
+    static constexpr uint32_t off_bar = off_w + kTcWStages * kTcWStageBytes;
+    static constexpr uint32_t n_bars = 2 * kTcWStages + 3 * kTcStagesMax + 1;
     static constexpr uint32_t off_misc = off_bar + 8 * n_bars;
     static constexpr uint32_t total = off_misc + 16;
-    static_assert(off_b % 1024 == 0 && off_w % 1024 == 0, "operand tiles must be 1024-byte aligned");
+    static_assert(off_w % 1024 == 0, "activation tiles must be 1024-byte aligned");
+    // The epilogue's [128][260] fp32 tile reuses the rings.
+    static_assert(kTcTok * (kTcRows + 4) * 4 <= off_bar, "epilogue tile must fit the rings");
 };
 
 // Tokens per launch tile: the token rows of one MMA.
@@ -117,10 +140,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major,
-// M × N.
-template <int M, int N>
-__device__ __forceinline__ uint32_t mma_idesc() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// M = 128, N = n (a multiple of 16, 16..256).
+__device__ __forceinline__ uint32_t mma_idesc_m128(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -144,14 +166,30 @@ __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D (tensor memory) (+)= A·Bᵀ with A read from tensor memory at column
+// address a_tmem and B from shared memory through its descriptor.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Sixteen 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
@@ -218,19 +256,20 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return __fadd2_rn(a, b);
 }
 
-// One qs word → two bf16x2 words of low-nibble values (bytes 0,1 and 2,3)
-// and two of high-nibble values.
-__device__ __forceinline__ void dequant_word(uint32_t v, const NibScale &lo, const NibScale &hi,
-                                             uint32_t &l01, uint32_t &l23, uint32_t &h01,
-                                             uint32_t &h23) {
-    const uint32_t v8 = __umulhi(v, 1u << 24);   // v >> 8, on the FMA pipe
-    const uint32_t v16 = __umulhi(v, 1u << 16);  // v >> 16
+// One qs word → two bf16x2 words of its low-nibble values (bytes 0,1 and
+// 2,3), or of its high-nibble values.
+__device__ __forceinline__ void dequant_lo(uint32_t v, const NibScale &lo, uint32_t &l01, uint32_t &l23) {
+    const uint32_t v8 = __umulhi(v, 1u << 24);  // v >> 8, on the FMA pipe
     const float2 tl01 = __ffma2_rn(make_float2(magic(v, 0xFu), magic(v, 0xF00u)), lo.s01, lo.c01);
     const float2 tl23 = __ffma2_rn(make_float2(magic(v, 0xF0000u), magic(v8, 0xF0000u)), lo.s23, lo.c23);
-    const float2 th01 = __ffma2_rn(make_float2(magic(v, 0xF0u), magic(v, 0xF000u)), hi.s01, hi.c01);
-    const float2 th23 = __ffma2_rn(make_float2(magic(v8, 0xF000u), magic(v16, 0xF000u)), hi.s23, hi.c23);
     l01 = pack_bf16x2(fadd2(tl01, lo.no));
     l23 = pack_bf16x2(fadd2(tl23, lo.no));
+}
+__device__ __forceinline__ void dequant_hi(uint32_t v, const NibScale &hi, uint32_t &h01, uint32_t &h23) {
+    const uint32_t v8 = __umulhi(v, 1u << 24);   // v >> 8
+    const uint32_t v16 = __umulhi(v, 1u << 16);  // v >> 16
+    const float2 th01 = __ffma2_rn(make_float2(magic(v, 0xF0u), magic(v, 0xF000u)), hi.s01, hi.c01);
+    const float2 th23 = __ffma2_rn(make_float2(magic(v8, 0xF000u), magic(v16, 0xF000u)), hi.s23, hi.c23);
     h01 = pack_bf16x2(fadd2(th01, hi.no));
     h23 = pack_bf16x2(fadd2(th23, hi.no));
 }
@@ -264,11 +303,14 @@ __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict
 // kXRows = 0: activation tiles come by TMA from a bf16 copy of x (tm_x).
 // Otherwise the dequant warps read fp32 x themselves (kXRows token rows per
 // thread and chunk: 2 for up to 64 tokens, 4 for up to 128), round it and
-// write the activation tile of each chunk next to its weight tile, and one
-// barrier (full_b) publishes both.
-template <int kXRows>
+// write the activation tile of each chunk, published with the chunk's A.
+// kRelay: weights in the relayouted tensor-core layout (tm_w: one 48-byte
+// box per row and chunk); otherwise canonical Q4_K (tm_w: the 16-byte block
+// header of each row, tm_q: the chunk's 32 code bytes of each row).
+template <int kXRows, bool kRelay>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+    q4k_mm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_x, const uint8_t *__restrict__ w_tc,
                      const float *__restrict__ x, float *__restrict__ y, int K, int N, int T, int *status,
                      long long wait_limit, int withhold) {
     using L = TcLayout;
@@ -280,9 +322,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full_w = bars, *empty_w = full_w + kTcWStages;
-    uint64_t *full_a = empty_w + kTcWStages, *empty_a = full_a + kTcAStages;
-    uint64_t *full_b = empty_a + kTcAStages, *empty_b = full_b + kTcBStages;
-    uint64_t *done = empty_b + kTcBStages;
+    uint64_t *full_x = empty_w + kTcWStages, *full_a = full_x + kTcStagesMax, *empty_a = full_a + kTcStagesMax;
+    uint64_t *done = empty_a + kTcStagesMax;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -290,34 +331,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row0 = (blockIdx.x / S) * kTcRows;
     const int nc_all = K / kTcKc;
     const int c_base = rank * nc_all / S;                 // first chunk of K (absolute)
-    const int nchunks = (rank + 1) * nc_all / S - c_base; // may be 0 when K is short
-    // Q4_K blocks touched: the first may be entered at chunk j0 > 0.
-    const int b_begin = c_base / 4;
-    const int j0 = c_base % 4;
-    const int nblocks = nchunks > 0 ? (c_base + nchunks + 3) / 4 - b_begin : 0;
+    const int nchunks = (rank + 1) * nc_all / S - c_base;
+    const int n_mma = (T + 15) & ~15;                     // MMA N: tokens rounded up to 16
+    // Tensor-memory columns of one accumulator (64 up to 64 tokens, else
+    // 128); the rest of the 512 holds the operand stages, 64 columns each,
+    // and an activation tile has dcols token rows.  Tiles from the bf16
+    // copy are always 128 tokens high.
+    const int dcols = (kXRows > 0 && T <= 64) ? 64 : 128;
+    const int nst = (int)(kTcTmemCols - 2 * dcols) / 64;  // 6 or 4
+    const uint32_t xt_bytes = (uint32_t)dcols * 128;
+    const uint32_t tmem_a = 2 * dcols;                    // first column of the A stages
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcWStages; ++s) {
             mbar_init(&full_w[s], 1);
-            mbar_init(&empty_w[s], kTcDq);
+            mbar_init(&empty_w[s], kTcGroupWarps);
         }
-        for (int s = 0; s < kTcAStages; ++s) {
-            mbar_init(&full_a[s], 1);
-            mbar_init(&empty_a[s], 1);
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full_x[s], 1);
+            mbar_init(&full_a[s], kTcGroupWarps);
+            mbar_init(&empty_a[s], 2);  // one commit per MMA issuer
         }
-        for (int s = 0; s < kTcBStages; ++s) {
-            mbar_init(&full_b[s], kTcDq / 2);
-            mbar_init(&empty_b[s], 1);
-        }
-        mbar_init(done, 1);
+        mbar_init(done, 2);
         abort_flag = 0;
         fence_mbar_init();
     }
     if constexpr (kXRows > 0) {
-        // Token rows T..127 of every activation stage stay zero.
-        const int pad16 = (kTcTok - T) * 128 / 16;
-        for (int s = 0; s < kTcAStages; ++s) {
-            uint4 *p = reinterpret_cast<uint4 *>(smem + L::off_a + s * kTcATileBytes + T * 128);
+        // Token rows T..n_mma-1 of every activation stage read as zero.
+        const int pad16 = (n_mma - T) * 128 / 16;
+        for (int s = 0; s < nst; ++s) {
+            uint4 *p = reinterpret_cast<uint4 *>(smem + L::off_x + s * xt_bytes + T * 128);
             for (int i = threadIdx.x; i < pad16; i += kTcThreads) p[i] = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_async_smem();
@@ -336,73 +379,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_launch_dependents();
 
     if (warp == kTcWarpTma) {
-        if (lane == 0) {
-            // Weight tiles and activation tiles are issued independently, each
-            // as soon as its ring slot is free.
-            int nw = 0, nx = 0;
-            // (A test may ask for one weight tile never to arrive, to see
-            // the waits on it run out; nothing then writes into its slot.)
-            for (; nw < min(nblocks, kTcWStages); ++nw) {
-                if (nw == withhold) continue;
-                mbar_arrive_expect_tx(&full_w[nw], kTcWTileBytes);
-                tma_load_2d(sbase + L::off_w + nw * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
-                            &full_w[nw]);
+        int nw = 0, nx = 0;
+        auto issue_w = [&](int c) {
+            const int ws = c % kTcWStages;
+            const uint32_t dst = sbase + L::off_w + ws * kTcWStageBytes;
+            const int ca = c_base + c;
+            mbar_arrive_expect_tx(&full_w[ws], kTcWStageBytes);
+            if constexpr (kRelay) {
+                // Tile-major relayout: the chunk's 256 rows are one run.
+                bulk_g2s(smem + L::off_w + ws * kTcWStageBytes,
+                         w_tc + ((size_t)(row0 / kTcRows) * nc_all + ca) * kTcWStageBytes, kTcWStageBytes, &full_w[ws]);
+            } else {
+                const int b = ca >> 2, j = ca & 3;
+                tma_load_2d(dst, &tm_w, b * kQ4kBytes, row0, &full_w[ws]);
+                tma_load_2d(dst + kTcRows * 16, &tm_q, b * kQ4kBytes + 16 + 32 * j, row0, &full_w[ws]);
             }
+        };
+        auto issue_x = [&](int c) {
+            const int st = c % nst;
+            mbar_arrive_expect_tx(&full_x[st], xt_bytes);
+            tma_load_2d(sbase + L::off_x + st * xt_bytes, &tm_x, (c_base + c) * kTcKc, 0, &full_x[st]);
+        };
+        if (lane == 0) {
+            // (A test may ask for one weight chunk never to arrive, to see
+            // the waits on it run out; nothing then writes into its slot.)
+            for (; nw < min(nchunks, kTcWStages); ++nw)
+                if (nw != withhold) issue_w(nw);
             if constexpr (kXRows == 0) {
                 // The bf16 activations come from the previous kernel on the stream.
                 pdl_wait();
-                for (; nx < min(nchunks, kTcAStages); ++nx) {
-                    mbar_arrive_expect_tx(&full_a[nx], kTcATileBytes);
-                    tma_load_2d(sbase + L::off_a + nx * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
-                                &full_a[nx]);
-                }
-            } else {
-                nx = nchunks;  // the dequant warps write the activation tiles
-            }
-            if constexpr (kXRows > 0) {
-                // Only weight tiles to issue: wait (suspended, bounded) for
-                // each slot in turn; a busy poll here would take issue slots
-                // from the dequant warps on this scheduler.
-                for (; nw < nblocks && !abort_flag; ++nw) {
-                    const int ws = nw % kTcWStages;
-                    if (!mbar_wait_abortable(&empty_w[ws], ((nw / kTcWStages) - 1) & 1, wait_limit, &abort_flag)) {
-                        abort_flag = 1;
-                        flag_timeout(status);
-                        break;
-                    }
-                    if (nw != withhold) {
-                        mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
-                        tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w, (b_begin + nw) * kQ4kBytes, row0,
-                                    &full_w[ws]);
-                    }
-                }
-            } else {
-                // Weight and activation tiles, each as soon as its slot is
-                // free: poll both, backing off while neither moves.
+                for (; nx < min(nchunks, nst); ++nx) issue_x(nx);
+                // Weight chunks and activation tiles, each as soon as its
+                // slot is free: poll both, backing off while neither moves.
                 long long t_last = clock64();
-                while ((nw < nblocks || nx < nchunks) && !abort_flag) {
+                while ((nw < nchunks || nx < nchunks) && !abort_flag) {
                     bool progressed = false;
-                    if (nw < nblocks) {
-                        const int ws = nw % kTcWStages;
-                        if (mbar_try_wait(&empty_w[ws], ((nw / kTcWStages) - 1) & 1)) {
-                            if (nw != withhold) {
-                                mbar_arrive_expect_tx(&full_w[ws], kTcWTileBytes);
-                                tma_load_2d(sbase + L::off_w + ws * kTcWTileBytes, &tm_w,
-                                            (b_begin + nw) * kQ4kBytes, row0, &full_w[ws]);
-                            }
-                            ++nw;
-                            progressed = true;
-                        }
+                    if (nw < nchunks &&
+                        mbar_try_wait(&empty_w[nw % kTcWStages], ((nw / kTcWStages) - 1) & 1)) {
+                        if (nw != withhold) issue_w(nw);
+                        ++nw;
+                        progressed = true;
                     }
-                    if (nx < nchunks) {
-                        const int as = nx % kTcAStages;
-                        if (mbar_try_wait(&empty_a[as], ((nx / kTcAStages) - 1) & 1)) {
-                            mbar_arrive_expect_tx(&full_a[as], kTcATileBytes);
-                            tma_load_2d(sbase + L::off_a + as * kTcATileBytes, &tm_x, (c_base + nx) * kTcKc, 0,
-                                        &full_a[as]);
-                            ++nx;
-                            progressed = true;
-                        }
+                    if (nx < nchunks && mbar_try_wait(&empty_a[nx % nst], ((nx / nst) - 1) & 1)) {
+                        issue_x(nx);
+                        ++nx;
+                        progressed = true;
                     }
                     if (progressed) {
                         t_last = clock64();
@@ -413,46 +434,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         __nanosleep(200);
                     }
                 }
+            } else {
+                // Only weight chunks to issue: wait (suspended, bounded) for
+                // each slot in turn.
+                nx = nchunks;
+                for (; nw < nchunks && !abort_flag; ++nw) {
+                    const int ws = nw % kTcWStages;
+                    if (!mbar_wait_abortable(&empty_w[ws], ((nw / kTcWStages) - 1) & 1, wait_limit, &abort_flag)) {
+                        abort_flag = 1;
+                        flag_timeout(status);
+                        break;
+                    }
+                    if (nw != withhold) issue_w(nw);
+                }
             }
             // Never leave a tensor copy writing into shared memory that is
             // about to be reused: the last use of each ring slot must land.
-            for (int b = max(0, nw - kTcWStages); b < nw; ++b)
-                if (b != withhold)
-                    (void)mbar_wait_bounded(&full_w[b % kTcWStages], (b / kTcWStages) & 1, wait_limit);
+            for (int c = max(0, nw - kTcWStages); c < nw; ++c)
+                if (c != withhold)
+                    (void)mbar_wait_bounded(&full_w[c % kTcWStages], (c / kTcWStages) & 1, wait_limit);
             if constexpr (kXRows == 0) {
-                for (int c = max(0, nx - kTcAStages); c < nx; ++c)
-                    (void)mbar_wait_bounded(&full_a[c % kTcAStages], (c / kTcAStages) & 1, wait_limit);
+                for (int c = max(0, nx - nst); c < nx; ++c)
+                    (void)mbar_wait_bounded(&full_x[c % nst], (c / nst) & 1, wait_limit);
             }
         }
         __syncwarp();
-    } else if (warp == kTcWarpMma) {
+    } else if (warp == kTcWarpMma || warp == kTcWarpMma + 1) {
+        // One issuer per row half (accumulator), in warps on different SM
+        // sub-partitions: an MMA instruction is accepted only about as fast
+        // as the tensor pipe runs it, so the few instructions an issuer runs
+        // between chunks (its wait, descriptors, commit) leave the pipe idle
+        // unless the other issuer fills that time; and the dequantizing warps
+        // that share a sub-partition with an issuer take most of its issue
+        // slots.  Each accumulator still receives its MMAs from one thread in
+        // K order, so the sums do not depend on scheduling.
+        const int mh = warp - kTcWarpMma;
         if (lane == 0) {
-            const uint32_t idesc = mma_idesc<kTcTok, kTcRows>();
-            // One thread's dependent chain sits between the chunks' MMAs, so
-            // the loop keeps it short: stage, phase and descriptors advance by
-            // additions (a descriptor's address field counts 16-byte units;
-            // every tile lies below 256 KB, so no carry leaves the field).
-            const uint64_t a_desc0 = sw128_desc(sbase + L::off_a), b_desc0 = sw128_desc(sbase + L::off_b);
+            const uint32_t idesc = mma_idesc_m128(n_mma);
+            // A descriptor's address field counts 16-byte units; every tile
+            // lies below 256 KB, so stepping it by addition carries nowhere.
+            const uint64_t x_desc0 = sw128_desc(sbase + L::off_x);
             int st = 0;
             uint32_t ph = 0;
             for (int c = 0; c < nchunks; ++c) {
                 bool ok = true;
-                if constexpr (kXRows == 0) ok = mbar_wait_bounded(&full_a[st], ph, wait_limit);
-                ok = ok && mbar_wait_bounded(&full_b[st], ph, wait_limit);
+                if constexpr (kXRows == 0) ok = mbar_spin_abortable(&full_x[st], ph, wait_limit, &abort_flag);
+                ok = ok && mbar_spin_abortable(&full_a[st], ph, wait_limit, &abort_flag);
                 if (!ok) {
                     abort_flag = 1;
                     flag_timeout(status);
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = a_desc0 + (uint64_t)(st * (kTcATileBytes >> 4));
-                const uint64_t bd = b_desc0 + (uint64_t)(st * (kTcBTileBytes >> 4));
+                const uint64_t bd = x_desc0 + (uint64_t)(st * (xt_bytes >> 4));
+                const uint32_t ad = tmem + tmem_a + 64 * st + 32 * mh;
 #pragma unroll
                 for (int kk = 0; kk < kTcKc / 16; ++kk)
-                    tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
-                if constexpr (kXRows == 0) tc_commit(&empty_a[st]);
-                tc_commit(&empty_b[st]);
-                if (++st == kTcBStages) {
+                    tc_mma_ts(tmem + dcols * mh, ad + 8 * kk, bd + 2 * kk, idesc, (c | kk) != 0);
+                tc_commit(&empty_a[st]);
+                if (++st == nst) {
                     st = 0;
                     ph ^= 1u;
                 }
@@ -465,15 +505,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // Two groups of 256 threads take alternate chunks: thread t of group
-        // g = t / 256 dequantizes all 64 values of weight row r = t mod 256 in
-        // the chunks c ≡ g (mod 2) of the CTA.
-        const int r = threadIdx.x & (kTcRows - 1), grp = threadIdx.x >> 8;
-        // Fused activations: in each of its chunks, thread r of a group
-        // rounds 16-byte segment r mod 8 of token rows r/8 + 32i, i <
+        // Warp w: tensor-memory lane quarter q = w mod 4 of row half
+        // mh = (w / 4) mod 2, chunks c ≡ w / 8 (mod 2).  Thread (w, lane)
+        // dequantizes weight row r = 128·mh + 32·q + lane of its chunks.
+        const int q = warp & 3, mh = (warp >> 2) & 1, grp = warp >> 3;
+        const int r = kTcM * mh + 32 * q + lane;
+        const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        // Fused activations: in each of its chunks, thread i of a group
+        // rounds 16-byte segment i mod 8 of token rows i/8 + 32j, j <
         // kXRows, loaded when the group's previous chunk is written so that
         // the L2 latency hides behind it.
-        const int aseg = r & 7, arow = r >> 3;
+        const int gi = threadIdx.x & (32 * kTcGroupWarps - 1);
+        const int aseg = gi & 7, arow = gi >> 3;
         const float *xrow = x + (size_t)arow * K + (size_t)c_base * kTcKc + 8 * aseg;
         constexpr int kXR = kXRows > 0 ? kXRows : 1;
         float4 xr[2 * kXR];
@@ -493,80 +536,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (grp < nchunks) load_x(grp);
         }
         bool good = true;
-        int c = 0;  // chunk of this CTA
-        for (int b = 0; b < nblocks && good; ++b) {
-            const int ws = b % kTcWStages;
-            const uint8_t *blk = smem + L::off_w + ws * kTcWTileBytes + r * kQ4kBytes;
-            // Chunks of this block within the CTA's range.
-            const int jb = b == 0 ? j0 : 0;
-            const int je = min(4, jb + (nchunks - c));
-            // Every thread waits for the block, even one with no chunk of it,
-            // before releasing it below: no thread can then release a ring
-            // slot twice in one phase.
-            if (__any_sync(0xffffffffu, abort_flag != 0) ||
-                !__all_sync(0xffffffffu, mbar_wait_bounded(&full_w[ws], (b / kTcWStages) & 1, wait_limit))) {
+        // Operand stage st = c mod nst of round c / nst, advanced by 2 per chunk.
+        int st = grp, round = 0;
+        for (int c = grp; c < nchunks; c += 2) {
+            const int ws = c % kTcWStages;
+            if (__any_sync(0xffffffffu, abort_flag != 0)) {
                 good = false;
                 break;
             }
+            bool ok = mbar_wait_bounded(&full_w[ws], (c / kTcWStages) & 1, wait_limit);
+            // Operand stage st is free once the MMAs of chunk c - nst are done.
+            if (ok && round > 0) ok = mbar_wait_bounded(&empty_a[st], (round - 1) & 1, wait_limit);
+            if (!__all_sync(0xffffffffu, ok)) {
+                good = false;
+                break;
+            }
+            tc_fence_after();
+            if constexpr (kXRows > 0) {
+                uint8_t *ap = smem + L::off_x + st * xt_bytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j < jb || j >= je) continue;
-                const int cc = c + (j - jb);
-                if ((cc & 1) != grp) continue;
-                const int bs = cc % kTcBStages;
-                if (__any_sync(0xffffffffu, abort_flag != 0)) {
-                    good = false;
-                    break;
-                }
-                bool ok = true;
-                if (cc >= kTcBStages)
-                    ok = mbar_wait_bounded(&empty_b[bs], ((cc / kTcBStages) - 1) & 1, wait_limit);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    good = false;
-                    break;
-                }
-                if constexpr (kXRows > 0) {
-                    uint8_t *ap = smem + L::off_a + bs * kTcATileBytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
-#pragma unroll
-                    for (int i = 0; i < kXRows; ++i) {
-                        if (arow + 32 * i < T)
-                            *reinterpret_cast<uint4 *>(ap + 32 * 128 * i) = make_uint4(
-                                pack_bf16x2(make_float2(xr[2 * i].x, xr[2 * i].y)),
-                                pack_bf16x2(make_float2(xr[2 * i].z, xr[2 * i].w)),
-                                pack_bf16x2(make_float2(xr[2 * i + 1].x, xr[2 * i + 1].y)),
-                                pack_bf16x2(make_float2(xr[2 * i + 1].z, xr[2 * i + 1].w)));
-                    }
-                    if (cc + 2 < nchunks) load_x(cc + 2);
-                }
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                const float2 dm = q4k_d_dmin(hdr.x);
-                const float2 slo = sub_scale(2 * j, hdr, dm);
-                const float2 shi = sub_scale(2 * j + 1, hdr, dm);
-                const NibScale lo = nib_scale_lo(slo.x, slo.y), hi = nib_scale_hi(shi.x, shi.y);
-                uint8_t *brow = smem + L::off_b + bs * kTcBTileBytes + r * 128;
-                const int sw = r & 7;
-                // Half hh: qs bytes 16hh..16hh+15 give low values k = 16hh..
-                // (logical 16-byte chunks 2hh, 2hh+1) and high values k =
-                // 32+16hh.. (chunks 4+2hh, 5+2hh).
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * hh);
-                    uint32_t lw[8], hw[8];
-                    dequant_word(q.x, lo, hi, lw[0], lw[1], hw[0], hw[1]);
-                    dequant_word(q.y, lo, hi, lw[2], lw[3], hw[2], hw[3]);
-                    dequant_word(q.z, lo, hi, lw[4], lw[5], hw[4], hw[5]);
-                    dequant_word(q.w, lo, hi, lw[6], lw[7], hw[6], hw[7]);
-                    *reinterpret_cast<uint4 *>(brow + (((2 * hh) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    *reinterpret_cast<uint4 *>(brow + (((2 * hh + 1) ^ sw) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-                    *reinterpret_cast<uint4 *>(brow + (((4 + 2 * hh) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4 *>(brow + (((5 + 2 * hh) ^ sw) << 4)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                for (int i = 0; i < kXRows; ++i) {
+                    if (arow + 32 * i < T)
+                        *reinterpret_cast<uint4 *>(ap + 32 * 128 * i) = make_uint4(
+                            pack_bf16x2(make_float2(xr[2 * i].x, xr[2 * i].y)),
+                            pack_bf16x2(make_float2(xr[2 * i].z, xr[2 * i].w)),
+                            pack_bf16x2(make_float2(xr[2 * i + 1].x, xr[2 * i + 1].y)),
+                            pack_bf16x2(make_float2(xr[2 * i + 1].z, xr[2 * i + 1].w)));
                 }
                 fence_async_smem();
-                mbar_arrive(&full_b[bs]);
+                if (c + 2 < nchunks) load_x(c + 2);
             }
-            c += je - jb;
-            // Every dequant thread releases the block once.
-            if (good) mbar_arrive(&empty_w[ws]);
+            const uint8_t *wst = smem + L::off_w + ws * kTcWStageBytes;
+            float4 sc;  // scale and offset of the low-nibble and the high-nibble sub-block
+            uint4 q0, q1;
+            if constexpr (kRelay) {
+                const uint8_t *row = wst + r * kTcChunkBytes;
+                sc = *reinterpret_cast<const float4 *>(row);
+                q0 = *reinterpret_cast<const uint4 *>(row + 16);
+                q1 = *reinterpret_cast<const uint4 *>(row + 32);
+            } else {
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(wst + r * 16);
+                q0 = *reinterpret_cast<const uint4 *>(wst + kTcRows * 16 + r * 32);
+                q1 = *reinterpret_cast<const uint4 *>(wst + kTcRows * 16 + r * 32 + 16);
+                const float2 dm = q4k_d_dmin(hdr.x);
+                float2 sl, sh;
+                switch ((c_base + c) & 3) {  // the same for the whole warp
+                    case 0: sl = sub_scale(0, hdr, dm); sh = sub_scale(1, hdr, dm); break;
+                    case 1: sl = sub_scale(2, hdr, dm); sh = sub_scale(3, hdr, dm); break;
+                    case 2: sl = sub_scale(4, hdr, dm); sh = sub_scale(5, hdr, dm); break;
+                    default: sl = sub_scale(6, hdr, dm); sh = sub_scale(7, hdr, dm); break;
+                }
+                sc = make_float4(sl.x, sl.y, sh.x, sh.y);
+            }
+            // Columns of this lane: low-nibble values k = 0..31 of the chunk
+            // at 0..15, high-nibble values k = 32..63 at 16..31.
+            const uint32_t ta = tmem + t_lane + tmem_a + 64 * st + 32 * mh;
+            uint32_t o[16];
+            {
+                const NibScale lo = nib_scale_lo(sc.x, sc.y);
+                dequant_lo(q0.x, lo, o[0], o[1]);
+                dequant_lo(q0.y, lo, o[2], o[3]);
+                dequant_lo(q0.z, lo, o[4], o[5]);
+                dequant_lo(q0.w, lo, o[6], o[7]);
+                dequant_lo(q1.x, lo, o[8], o[9]);
+                dequant_lo(q1.y, lo, o[10], o[11]);
+                dequant_lo(q1.z, lo, o[12], o[13]);
+                dequant_lo(q1.w, lo, o[14], o[15]);
+                tc_st16(ta, o);
+            }
+            {
+                const NibScale hi = nib_scale_hi(sc.z, sc.w);
+                dequant_hi(q0.x, hi, o[0], o[1]);
+                dequant_hi(q0.y, hi, o[2], o[3]);
+                dequant_hi(q0.z, hi, o[4], o[5]);
+                dequant_hi(q0.w, hi, o[6], o[7]);
+                dequant_hi(q1.x, hi, o[8], o[9]);
+                dequant_hi(q1.y, hi, o[10], o[11]);
+                dequant_hi(q1.z, hi, o[12], o[13]);
+                dequant_hi(q1.w, hi, o[14], o[15]);
+                tc_st16(ta + 16, o);
+            }
+            // The weight stage has been read (its words are consumed above):
+            // release it to the next copy.
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_w[ws]);
+            // Publish the chunk's A (and activation tile) to the MMA thread.
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_a[st]);
+            st += 2;
+            if (st >= nst) {
+                st -= nst;
+                ++round;
+            }
         }
         if (!good) {
             abort_flag = 1;
@@ -574,40 +638,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
 
-    // The accumulator is complete once every MMA this CTA issued has finished.
+    // The accumulators are complete once every MMA this CTA issued has finished.
     const bool have_acc = __syncthreads_and(mbar_wait_bounded(done, 0, wait_limit) ? 1 : 0) != 0;
     tc_fence_after();
 
-    // Epilogue.  Warps w, w+4, w+8, w+12 share TMEM lane quarter w % 4
-    // (tokens 32·quarter..) and read 64 of the 256 columns each into a shared
-    // tile [T][260]; the rings are idle by now.  After a cluster barrier every
-    // rank takes one S-th of the tile's outputs, adds the S ranks' values in
-    // rank order, read straight from their shared memory (distributed shared
-    // memory, 16 bytes per load), and writes them to y with consecutive
-    // threads on consecutive columns.  A second barrier keeps each tile in
-    // place until every rank has read it.
+    // Epilogue.  Warp w reads lane quarter w mod 4 of row half (w / 4) mod 2:
+    // token blocks of 16 alternate between w < 8 and w >= 8.  Each value
+    // goes to a shared tile [T][260] (consecutive lanes: consecutive rows);
+    // the rings are idle by now.  After a cluster barrier every rank takes one
+    // S-th of the tile's outputs, adds the S ranks' values in rank order, read
+    // straight from their shared memory (distributed shared memory, 16 bytes
+    // per load), and writes them to y with consecutive threads on consecutive
+    // columns.  A second barrier keeps each tile in place until every rank
+    // has read it.
     // Row pitch of the shared tile: 260 floats keeps every row on a 16-byte
-    // boundary, and eight lanes of consecutive tokens storing 16 bytes at
-    // the same column land on eight distinct bank groups.
+    // boundary for the 16-byte reads of the reduction.
     constexpr int kPitch = kTcRows + 4;
     float *ysm = reinterpret_cast<float *>(smem);
-    const int quarter = warp & 3, cq = warp >> 2;
-    const int tok = 32 * quarter + lane;
-    if (warp < kTcDqWarps && 32 * quarter < T) {  // warp-uniform
+    if (warp < kTcDqWarps) {
+        const int q = warp & 3, mh = (warp >> 2) & 1;
+        const int o = kTcM * mh + 32 * q + lane;
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
+        for (int tb = warp >> 3; 16 * tb < T; tb += 2) {  // warp-uniform
             float v[16];
             if (have_acc && nchunks > 0) {
-                tc_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(64 * cq + 16 * g), v);
+                tc_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(dcols * mh + 16 * tb), v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
             }
-            if (tok < T) {
-                float4 *dst = reinterpret_cast<float4 *>(ysm + tok * kPitch + 64 * cq + 16 * g);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-            }
+            for (int i = 0; i < 16; ++i)
+                if (16 * tb + i < T) ysm[(16 * tb + i) * kPitch + o] = v[i];
         }
     }
     tc_fence_before();
@@ -692,22 +754,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // One launch over a tile of at most 128 tokens: activations either from the
 // bf16 copy xb by TMA (xb != nullptr) or from fp32 x, rounded in the kernel.
-cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float *x, const uint8_t *W, float *y,
-                        int K, int N, int T, int S) {
+// relay: W is in the relayouted tensor-core layout.
+cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float *x, const uint8_t *W, bool relay,
+                        float *y, int K, int N, int T, int S) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap tm_w, tm_x;
+    alignas(64) CUtensorMap tm_w, tm_q, tm_x;
+    std::memset(&tm_q, 0, sizeof(tm_q));
     std::memset(&tm_x, 0, sizeof(tm_x));
-    const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
-    {
+    auto map_w = [&](CUtensorMap *m, cuuint64_t row_bytes, cuuint32_t box_bytes) {
         const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)N};
         const cuuint64_t strides[1] = {row_bytes};
-        const cuuint32_t box[2] = {(cuuint32_t)kQ4kBytes, (cuuint32_t)kTcRows};
+        const cuuint32_t box[2] = {box_bytes, (cuuint32_t)kTcRows};
         const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(W), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(W), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (relay) {
+        // Tile-major: each chunk of a 256-row tile is one 12 KB run, copied
+        // by a plain bulk copy; no tensor map.
+        std::memset(&tm_w, 0, sizeof(tm_w));
+    } else {
+        // Rows of K/256 blocks of 144 bytes; boxes of the 16-byte headers and
+        // of one chunk's 32 code bytes, 256 rows each.
+        const cuuint64_t row_bytes = (cuuint64_t)(K / kQ4kValues) * kQ4kBytes;
+        if (!map_w(&tm_w, row_bytes, 16) || !map_w(&tm_q, row_bytes, 32)) return cudaErrorInvalidValue;
     }
     if (xb) {
         // bf16 activations [T][K]: a 64-value (128-byte) by 128-token box with
@@ -724,7 +796,11 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float
     }
     const size_t smem = TcLayout::total + 1024;
     if (smem > (size_t)c.max_smem_optin) return cudaErrorNotSupported;
-    auto kernel = xb ? q4k_mm_tc_kernel<0> : (T <= 64 ? q4k_mm_tc_kernel<2> : q4k_mm_tc_kernel<4>);
+    decltype(&q4k_mm_tc_kernel<0, false>) kernel;
+    if (relay)
+        kernel = xb ? q4k_mm_tc_kernel<0, true> : (T <= 64 ? q4k_mm_tc_kernel<2, true> : q4k_mm_tc_kernel<4, true>);
+    else
+        kernel = xb ? q4k_mm_tc_kernel<0, false> : (T <= 64 ? q4k_mm_tc_kernel<2, false> : q4k_mm_tc_kernel<4, false>);
     cudaError_t e = ensure_smem(kernel, smem);
     if (e != cudaSuccess) return e;
     const int tiles = (N + kTcRows - 1) / kTcRows;
@@ -746,14 +822,15 @@ cudaError_t launch_tile(const LaunchCtx &c, const __nv_bfloat16 *xb, const float
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_x, x, y, K, N, T, c.status, c.wait_limit, c.withhold);
+    return cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_q, tm_x, relay ? W : nullptr, x, y, K, N, T, c.status,
+                              c.wait_limit, c.withhold);
 }
 
 // Tiles of 128 tokens over the bf16 copy xb of x (several tiles), or one
 // tile that rounds x itself (xb == nullptr, at most 128 tokens).
-cudaError_t launch_tiles(const LaunchCtx &c, const float *x, __nv_bfloat16 *xb, const uint8_t *W, float *y, int K,
-                         int N, int T, int S) {
-    if (!xb) return launch_tile(c, nullptr, x, W, y, K, N, T, S);
+cudaError_t launch_tiles(const LaunchCtx &c, const float *x, __nv_bfloat16 *xb, const uint8_t *W, bool relay,
+                         float *y, int K, int N, int T, int S) {
+    if (!xb) return launch_tile(c, nullptr, x, W, relay, y, K, N, T, S);
     const size_t n = (size_t)T * K;
     cudaError_t e;
     {
@@ -764,9 +841,47 @@ cudaError_t launch_tiles(const LaunchCtx &c, const float *x, __nv_bfloat16 *xb, 
     }
     for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += kTcMaxTokens) {
         const int tt = min(kTcMaxTokens, T - t0);
-        e = launch_tile(c, xb + (size_t)t0 * K, nullptr, W, y + (size_t)t0 * N, K, N, tt, S);
+        e = launch_tile(c, xb + (size_t)t0 * K, nullptr, W, relay, y + (size_t)t0 * N, K, N, tt, S);
     }
     return e;
+}
+
+// One-time relayout, canonical Q4_K → tile-major tensor-core chunks: one
+// thread per (tile row, chunk) of the padded layout, 16-byte loads and
+// stores (both buffers 16-byte aligned).  Thread i writes the 48 bytes at
+// 48·i: chunk c = (i / 256) mod nc of tile (i / 256) / nc, row i mod 256 of
+// the tile; rows past N are zero.  The products d·sc and dmin·m are exact in
+// fp32, so the relayouted weight dequantizes to the same fp32 matrix.
+__global__ void q4k_relayout_tc_kernel(const uint8_t *__restrict__ W, uint8_t *__restrict__ R, int K, int N) {
+    const int nc = K / kTcKc, nb = K / kQ4kValues;
+    const size_t tiles = ((size_t)N + kTcRows - 1) / kTcRows;
+    const size_t total = tiles * nc * kTcRows;
+    pdl_launch_dependents();
+    pdl_wait();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t run = i / kTcRows;
+        const int r = (int)(i % kTcRows), ca = (int)(run % nc);
+        const size_t o = (run / nc) * kTcRows + r;
+        uint4 *dst = reinterpret_cast<uint4 *>(R + i * kTcChunkBytes);
+        if (o >= (size_t)N) {
+            dst[0] = dst[1] = dst[2] = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const int b = ca >> 2, j = ca & 3;
+        const uint8_t *blk = W + (o * nb + b) * kQ4kBytes;
+        const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+        const float2 dm = q4k_d_dmin(hdr.x);
+        float2 sl, sh;
+        switch (j) {
+            case 0: sl = sub_scale(0, hdr, dm); sh = sub_scale(1, hdr, dm); break;
+            case 1: sl = sub_scale(2, hdr, dm); sh = sub_scale(3, hdr, dm); break;
+            case 2: sl = sub_scale(4, hdr, dm); sh = sub_scale(5, hdr, dm); break;
+            default: sl = sub_scale(6, hdr, dm); sh = sub_scale(7, hdr, dm); break;
+        }
+        dst[0] = make_uint4(__float_as_uint(sl.x), __float_as_uint(sl.y), __float_as_uint(sh.x), __float_as_uint(sh.y));
+        dst[1] = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
+        dst[2] = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
+    }
 }
 
 // Split of K over the cluster: at least 3 CTAs per row tile, and at most
@@ -785,8 +900,10 @@ size_t q4k_mm_tc_scratch_bytes(int K, int N, int T) {
     return ((size_t)T * K * sizeof(__nv_bfloat16) + 255) / 256 * 256;
 }
 
-cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K,
-                             int N, int T) {
+namespace {
+
+cudaError_t launch_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, bool relay, float *y, int K, int N,
+                         int T) {
     const int S = tc_split(K);
     if (S == 0) return cudaErrorNotSupported;
     // Up to 128 tokens: one launch that rounds x itself, nothing allocated.
@@ -794,13 +911,34 @@ cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *
     // the same stream after the last tile) and the weights are re-read once
     // per tile of 128 tokens.
     const size_t bytes = q4k_mm_tc_scratch_bytes(K, N, T);
-    if (bytes == 0) return launch_tiles(c, x, nullptr, W, y, K, N, T, S);
+    if (bytes == 0) return launch_tiles(c, x, nullptr, W, relay, y, K, N, T, S);
     void *scratch = nullptr;
     cudaError_t e = cudaMallocAsync(&scratch, bytes, c.stream);
     if (e != cudaSuccess) return e;
-    e = launch_tiles(c, x, static_cast<__nv_bfloat16 *>(scratch), W, y, K, N, T, S);
+    e = launch_tiles(c, x, static_cast<__nv_bfloat16 *>(scratch), W, relay, y, K, N, T, S);
     const cudaError_t ef = cudaFreeAsync(scratch, c.stream);
     return e != cudaSuccess ? e : ef;
+}
+
+}  // namespace
+
+cudaError_t launch_q4k_mm_tc(const LaunchCtx &c, const float *x, const uint8_t *W, float *y, int K, int N, int T) {
+    return launch_mm_tc(c, x, W, false, y, K, N, T);
+}
+
+cudaError_t launch_q4k_mm_tc_relayouted(const LaunchCtx &c, const float *x, const uint8_t *R, float *y, int K, int N,
+                                        int T) {
+    return launch_mm_tc(c, x, R, true, y, K, N, T);
+}
+
+size_t q4k_relayout_tc_bytes(int K, int N) {
+    return ((size_t)N + kTcRows - 1) / kTcRows * kTcRows * (size_t)(K / kTcKc) * kTcChunkBytes;
+}
+
+cudaError_t launch_q4k_relayout_tc(const LaunchCtx &c, const uint8_t *W, uint8_t *R, int K, int N) {
+    const size_t total = ((size_t)N + kTcRows - 1) / kTcRows * kTcRows * (K / kTcKc);
+    const int grid = (int)min((size_t)8 * c.num_sms, (total + 255) / 256);
+    return launch_kernel(c, q4k_relayout_tc_kernel, dim3(grid), dim3(256), 0, W, R, K, N);
 }
 
 // ----------------------------------------------------------------------------
@@ -858,7 +996,7 @@ cudaError_t launch_q4k_mm_tc_fixed_scratch(const LaunchCtx &c, const float *x, c
     if (e != cudaSuccess) return e;
     // As in launch_q4k_mm_tc, the scratch (above 128 tokens) holds x rounded
     // to bf16.  Nothing needs clearing: the pre-pass writes all of it.
-    return launch_tiles(c, x, bytes ? reinterpret_cast<__nv_bfloat16 *>(scratch) : nullptr, W, y, K, N, T, S);
+    return launch_tiles(c, x, bytes ? reinterpret_cast<__nv_bfloat16 *>(scratch) : nullptr, W, false, y, K, N, T, S);
 }
 
 }  // namespace q4mm

@@ -93,6 +93,32 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t pari
     }
 }
 
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_wait_abortable, by spinning on non-blocking tests: for a single
+// thread whose next instructions must follow the phase's completion at
+// once (a tensor-core issuer, whose idle time is idle tensor pipe).
+__device__ __forceinline__ bool mbar_spin_abortable(uint64_t *bar, uint32_t parity, long long limit_cycles,
+                                                    const volatile int *abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort || clock64() - t0 > limit_cycles) return false;
+    }
+}
+
 // 1-D bulk copy global → shared, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,

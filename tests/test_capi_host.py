@@ -157,3 +157,37 @@ def test_q6k_rejects_bad_input_dim(q4mm, K):
     with pytest.raises(q4mm.Q4mmError) as e:
         q4mm.q6k_gemv_ptr(X, W, Y, K, 16, 1, 0)
     assert e.value.code == DIM and "inputDim" in q4mm.last_error()
+
+
+@pytest.mark.parametrize("K", [0, -256, 100, 255, 257, 65536 + 256])
+def test_relayout_rejects_bad_input_dim(q4mm, K):
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_relayout_tc_ptr(W, Y, K, 16, 0)
+    assert e.value.code == DIM and "inputDim" in q4mm.last_error()
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_relayouted_ptr(X, W, Y, K, 16, 1, 0)
+    assert e.value.code == DIM
+
+
+def test_relayout_validation(q4mm):
+    for args in ((0, Y), (W, 0)):
+        with pytest.raises(q4mm.Q4mmError) as e:
+            q4mm.q4k_relayout_tc_ptr(*args, 256, 4, 0)
+        assert e.value.code == NULL
+    for args in ((W + 8, Y), (W, Y + 4)):
+        with pytest.raises(q4mm.Q4mmError) as e:
+            q4mm.q4k_relayout_tc_ptr(*args, 256, 4, 0)
+        assert e.value.code == ALIGN
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_relayout_tc_ptr(W, W + 256, 256, 4, 0)   # 4 rows of 144 bytes reach past W + 256
+    assert e.value.code == ALIAS
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_relayout_tc_ptr(W, 16, 0, 4, 0)
+    assert e.value.code == DIM
+    # The relayouted product checks its weight (K/64·48 bytes per row) against x and y.
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_relayouted_ptr(X, Y - 4 * 192 + 16, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIAS
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_relayouted_ptr(X, W + 4, Y, 256, 4, 1, 0)
+    assert e.value.code == ALIGN
