@@ -115,12 +115,14 @@ struct TcLayout {
     static constexpr uint32_t off_x = 0;
     static constexpr uint32_t off_w = off_x + kTcXRegion;
     static constexpr uint32_t off_bar = off_w + kTcWStages * kTcWStageBytes;
-    static constexpr uint32_t n_bars = 2 * kTcWStages + 3 * kTcStagesMax + 1;
+    static constexpr uint32_t n_bars = 2 * kTcWStages + 3 * kTcStagesMax + 2;
     static constexpr uint32_t off_misc = off_bar + 8 * n_bars;
     static constexpr uint32_t total = off_misc + 16;
     static_assert(off_w % 1024 == 0, "activation tiles must be 1024-byte aligned");
-    // The epilogue's [128][260] fp32 tile reuses the rings.
-    static_assert(kTcTok * (kTcRows + 4) * 4 <= off_bar, "epilogue tile must fit the rings");
+    // The epilogue's tiles (own: 256 rows x 72 token slots; receive: S - 1
+    // slots of at most 86 rows, S = 3, or 64 rows, S = 4, x 68) reuse the rings.
+    static_assert((kTcRows * 72 + 2 * 86 * 68) * 4 <= off_bar && (kTcRows * 72 + 3 * 64 * 68) * 4 <= off_bar,
+                  "epilogue tiles must fit the rings");
 };
 
 // Tokens per launch tile: the token rows of one MMA.
@@ -151,6 +153,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to another CTA's of the cluster
+// (cluster addresses dst and bar), completing on that CTA's barrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 
@@ -324,6 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *full_w = bars, *empty_w = full_w + kTcWStages;
     uint64_t *full_x = empty_w + kTcWStages, *full_a = full_x + kTcStagesMax, *empty_a = full_a + kTcStagesMax;
     uint64_t *done = empty_a + kTcStagesMax;
+    uint64_t *recv_bar = done + 1;  // epilogue: slices received from the other ranks
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_misc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -353,6 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&empty_a[s], 2);  // one commit per MMA issuer
         }
         mbar_init(done, 2);
+        mbar_init(recv_bar, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -642,95 +655,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool have_acc = __syncthreads_and(mbar_wait_bounded(done, 0, wait_limit) ? 1 : 0) != 0;
     tc_fence_after();
 
-    // Epilogue.  Warp w reads lane quarter w mod 4 of row half (w / 4) mod 2:
-    // token blocks of 16 alternate between w < 8 and w >= 8.  Each value
-    // goes to a shared tile [T][260] (consecutive lanes: consecutive rows);
-    // the rings are idle by now.  After a cluster barrier every rank takes one
-    // S-th of the tile's outputs, adds the S ranks' values in rank order, read
-    // straight from their shared memory (distributed shared memory, 16 bytes
-    // per load), and writes them to y with consecutive threads on consecutive
-    // columns.  A second barrier keeps each tile in place until every rank
-    // has read it.
-    // Row pitch of the shared tile: 260 floats keeps every row on a 16-byte
-    // boundary for the 16-byte reads of the reduction.
-    constexpr int kPitch = kTcRows + 4;
-    float *ysm = reinterpret_cast<float *>(smem);
-    if (warp < kTcDqWarps) {
-        const int q = warp & 3, mh = (warp >> 2) & 1;
-        const int o = kTcM * mh + 32 * q + lane;
+    // Epilogue: the split-K sum over the cluster, in passes of up to 64
+    // tokens.  Rank s owns the tile's rows [lo(s), lo(s+1)), lo(s) =
+    // floor(256·s/S).  In a pass every rank writes its accumulators to a
+    // local tile own[row][token] (token pitch tp = the pass's tokens rounded
+    // up to 4, plus 4, which keeps 16-byte rows and spreads consecutive rows
+    // over the banks); after a cluster barrier (which also marks every rank
+    // done with its rings, which the tiles reuse) one thread sends the rows
+    // each other rank owns, one contiguous slice per rank, with a bulk copy
+    // into that rank's receive slot (recv[slot][row - lo][token], one slot per
+    // sender), completing on the receiver's barrier.  Bulk copies move the
+    // data far faster than per-thread loads or stores to distributed shared
+    // memory, measured on GB300.  Each rank then adds the S partial sums of
+    // its rows in rank order, all from local shared memory, and writes its
+    // rows of y.  A second cluster barrier keeps every sender's tile until
+    // its copies have landed.  The result does not depend on scheduling.
+    const int rows_cap = (kTcRows + S - 1) / S;
+    auto lo_of = [&](int s_) { return s_ * kTcRows / S; };
+    float *own = reinterpret_cast<float *>(smem);
+    float *recv = own + kTcRows * (64 + 8);  // after the largest own tile
+    const int lo = lo_of(rank), rows = lo_of(rank + 1) - lo;
+    const int ncols = min(kTcRows, N - row0);
+    for (int p0 = 0, pass = 0; p0 < T; p0 += 64, ++pass) {
+        const int tpass = min(64, T - p0);
+        const int tp = ((tpass + 3) & ~3) + 4;
+        if (warp < kTcDqWarps) {
+            const int q = warp & 3, mh = (warp >> 2) & 1;
+            const int o = kTcM * mh + 32 * q + lane;
 #pragma unroll 1
-        for (int tb = warp >> 3; 16 * tb < T; tb += 2) {  // warp-uniform
-            float v[16];
-            if (have_acc && nchunks > 0) {
-                tc_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(dcols * mh + 16 * tb), v);
-            } else {
+            for (int tb = (p0 >> 4) + (warp >> 3); 16 * tb < p0 + tpass; tb += 2) {  // warp-uniform
+                float v[16];
+                if (have_acc && nchunks > 0) {
+                    tc_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(dcols * mh + 16 * tb), v);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                }
+                const int tl = 16 * tb - p0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (tl + 4 * k < tpass)
+                        *reinterpret_cast<float4 *>(own + (size_t)o * tp + tl + 4 * k) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (16 * tb + i < T) ysm[(16 * tb + i) * kPitch + o] = v[i];
         }
-    }
-    tc_fence_before();
-    cluster_sync_all();
-    {
-        // Outputs in groups of four columns; rank r takes groups
-        // [r·G/S, (r+1)·G/S) of the tile's G = T·64.
-        constexpr int kGroupsPerRow = kTcRows / 4;
-        const int n_g = T * kGroupsPerRow;
-        const int g0 = rank * n_g / S, g1 = (rank + 1) * n_g / S;
-        const int ncols = min(kTcRows, N - row0);
-        const bool vec_y = (reinterpret_cast<uintptr_t>(y) & 15) == 0 && (N & 3) == 0;
-        const uint32_t local = smem_addr(ysm);
-        uint32_t tile_of[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) tile_of[s] = map_to_rank(local, (uint32_t)min(s, S - 1));
+        // The tile is read next by bulk copies (the async proxy).
+        fence_async_smem();
+        tc_fence_before();
+        cluster_sync_all();
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(recv_bar, (uint32_t)((S - 1) * rows * tp * 4));
+            for (int s_ = 0; s_ < S; ++s_) {
+                if (s_ == rank) continue;
+                const int slo = lo_of(s_), srows = lo_of(s_ + 1) - slo;
+                const int slot = rank < s_ ? rank : rank - 1;
+                const uint32_t dst = map_to_rank(smem_addr(recv + (size_t)slot * rows_cap * tp), (uint32_t)s_);
+                const uint32_t bar = map_to_rank(smem_addr(recv_bar), (uint32_t)s_);
+                bulk_s2cluster(dst, smem_addr(own + (size_t)slo * tp), (uint32_t)(srows * tp * 4), bar);
+            }
+        }
+        const bool got = mbar_wait_bounded(recv_bar, pass & 1, wait_limit);
+        if (!got && threadIdx.x == 0) flag_timeout(status);
         // The output may be read by the previous kernel on the stream.
-        pdl_wait();
-        // kU groups per thread step, every remote load issued before the
-        // adds so that their latencies overlap.
-        constexpr int kU = 4;
-        for (int i0 = g0 + (int)threadIdx.x; i0 < g1; i0 += kU * kTcThreads) {
-            float4 v[4][kU];
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = min(i0 + u * kTcThreads, g1 - 1);
-                    const uint32_t off = 4u * (uint32_t)((i / kGroupsPerRow) * kPitch + 4 * (i % kGroupsPerRow));
-                    v[s][u] = s < S ? ld_cluster_v4(tile_of[s] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (pass == 0) pdl_wait();
+        const int ngroups = (tpass + 3) / 4;
+        for (int i = threadIdx.x; got && i < rows * ngroups; i += kTcThreads) {
+            const int ol = i % rows, t0 = 4 * (i / rows);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s_ = 0; s_ < S; ++s_) {
+                const float *src = s_ == rank ? own + (size_t)(lo + ol) * tp
+                                              : recv + ((size_t)(s_ < rank ? s_ : s_ - 1) * rows_cap + ol) * tp;
+                const float4 v = *reinterpret_cast<const float4 *>(src + t0);
+                if (s_ == 0) {
+                    acc = v;
+                } else {
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
                 }
             }
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = i0 + u * kTcThreads;
-                if (i < g1) {
-                    const int t = i / kGroupsPerRow, col = 4 * (i % kGroupsPerRow);
-                    float4 acc = v[0][u];
-#pragma unroll
-                    for (int s = 1; s < 4; ++s) {
-                        if (s < S) {
-                            acc.x += v[s][u].x;
-                            acc.y += v[s][u].y;
-                            acc.z += v[s][u].z;
-                            acc.w += v[s][u].w;
-                        }
-                    }
-                    float *dst = y + (size_t)t * N + row0 + col;
-                    if (vec_y && col + 3 < ncols) {
-                        *reinterpret_cast<float4 *>(dst) = acc;
-                    } else {
-                        if (col < ncols) dst[0] = acc.x;
-                        if (col + 1 < ncols) dst[1] = acc.y;
-                        if (col + 2 < ncols) dst[2] = acc.z;
-                        if (col + 3 < ncols) dst[3] = acc.w;
-                    }
-                }
+            const int col = lo + ol;
+            if (col < ncols) {
+                float *dst = y + (size_t)(p0 + t0) * N + row0 + col;
+                dst[0] = acc.x;
+                if (t0 + 1 < tpass) dst[N] = acc.y;
+                if (t0 + 2 < tpass) dst[2 * (size_t)N] = acc.z;
+                if (t0 + 3 < tpass) dst[3 * (size_t)N] = acc.w;
             }
         }
+        // Every rank has received its slices, so every sender's tile has
+        // been read: the next pass (or exit) may proceed.
+        __syncthreads();
+        cluster_sync_all();
     }
-    cluster_sync_all();
     if (warp == kTcWarpMma) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
