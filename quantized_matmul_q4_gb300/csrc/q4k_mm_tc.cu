@@ -369,15 +369,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         abort_flag = 0;
         fence_mbar_init();
     }
-    if constexpr (kXRows > 0) {
-        // Token rows T..n_mma-1 of every activation stage read as zero.
-        const int pad16 = (n_mma - T) * 128 / 16;
-        for (int s = 0; s < nst; ++s) {
-            uint4 *p = reinterpret_cast<uint4 *>(smem + L::off_x + s * xt_bytes + T * 128);
-            for (int i = threadIdx.x; i < pad16; i += kTcThreads) p[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_async_smem();
-    }
     if (warp == kTcWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
@@ -530,14 +521,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the L2 latency hides behind it.
         const int gi = threadIdx.x & (32 * kTcGroupWarps - 1);
         const int aseg = gi & 7, arow = gi >> 3;
-        const float *xrow = x + (size_t)arow * K + (size_t)c_base * kTcKc + 8 * aseg;
+        // Token rows past T are read as a copy of row T - 1: they fill only
+        // accumulator columns that are never stored, and every access stays
+        // inside x and inside the activation tile.
         constexpr int kXR = kXRows > 0 ? kXRows : 1;
+        const float *xp = x + (size_t)c_base * kTcKc + 8 * aseg;
+        int xro[kXR];
+#pragma unroll
+        for (int i = 0; i < kXR; ++i) xro[i] = min(arow + 32 * i, T - 1) * K;
         float4 xr[2 * kXR];
         auto load_x = [&](int cc) {
 #pragma unroll
             for (int i = 0; i < kXR; ++i) {
-                if (kXRows > 0 && arow + 32 * i < T) {
-                    const float4 *src = reinterpret_cast<const float4 *>(xrow + (size_t)(32 * i) * K + (size_t)cc * kTcKc);
+                if (kXRows > 0) {
+                    const float4 *src = reinterpret_cast<const float4 *>(xp + xro[i] + cc * kTcKc);
                     xr[2 * i] = __ldg(src);
                     xr[2 * i + 1] = __ldg(src + 1);
                 }
@@ -553,13 +550,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int st = grp, round = 0;
         for (int c = grp; c < nchunks; c += 2) {
             const int ws = c % kTcWStages;
-            if (__any_sync(0xffffffffu, abort_flag != 0)) {
-                good = false;
-                break;
-            }
-            bool ok = mbar_wait_bounded(&full_w[ws], (c / kTcWStages) & 1, wait_limit);
+            bool ok = mbar_wait_abortable(&full_w[ws], (c / kTcWStages) & 1, wait_limit, &abort_flag);
             // Operand stage st is free once the MMAs of chunk c - nst are done.
-            if (ok && round > 0) ok = mbar_wait_bounded(&empty_a[st], (round - 1) & 1, wait_limit);
+            if (ok && round > 0) ok = mbar_wait_abortable(&empty_a[st], (round - 1) & 1, wait_limit, &abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 good = false;
                 break;
@@ -568,15 +561,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if constexpr (kXRows > 0) {
                 uint8_t *ap = smem + L::off_x + st * xt_bytes + arow * 128 + ((aseg ^ (arow & 7)) << 4);
 #pragma unroll
-                for (int i = 0; i < kXRows; ++i) {
-                    if (arow + 32 * i < T)
-                        *reinterpret_cast<uint4 *>(ap + 32 * 128 * i) = make_uint4(
-                            pack_bf16x2(make_float2(xr[2 * i].x, xr[2 * i].y)),
-                            pack_bf16x2(make_float2(xr[2 * i].z, xr[2 * i].w)),
-                            pack_bf16x2(make_float2(xr[2 * i + 1].x, xr[2 * i + 1].y)),
-                            pack_bf16x2(make_float2(xr[2 * i + 1].z, xr[2 * i + 1].w)));
-                }
-                fence_async_smem();
+                for (int i = 0; i < kXRows; ++i)
+                    *reinterpret_cast<uint4 *>(ap + 32 * 128 * i) =
+                        make_uint4(pack_bf16x2(make_float2(xr[2 * i].x, xr[2 * i].y)),
+                                   pack_bf16x2(make_float2(xr[2 * i].z, xr[2 * i].w)),
+                                   pack_bf16x2(make_float2(xr[2 * i + 1].x, xr[2 * i + 1].y)),
+                                   pack_bf16x2(make_float2(xr[2 * i + 1].z, xr[2 * i + 1].w)));
                 if (c + 2 < nchunks) load_x(c + 2);
             }
             const uint8_t *wst = smem + L::off_w + ws * kTcWStageBytes;
@@ -629,16 +619,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 dequant_hi(q1.w, hi, o[14], o[15]);
                 tc_st16(ta + 16, o);
             }
-            // The weight stage has been read (its words are consumed above):
-            // release it to the next copy.
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_w[ws]);
-            // Publish the chunk's A (and activation tile) to the MMA thread.
+            // Publish the chunk's A (and activation tile) to the MMA issuers,
+            // and release the weight stage (its words are consumed above) to
+            // the next copy.
             tc_wait_st();
             tc_fence_before();
+            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_a[st]);
+            if (lane == 0) {
+                mbar_arrive(&full_a[st]);
+                mbar_arrive(&empty_w[ws]);
+            }
             st += 2;
             if (st >= nst) {
                 st -= nst;
