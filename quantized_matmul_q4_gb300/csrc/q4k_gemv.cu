@@ -32,21 +32,26 @@ namespace {
 // One token: bulk-copied rows, slab lanes, byte planes of the activations
 // ----------------------------------------------------------------------------
 //
-// Roles in a CTA (a contiguous range of output rows):
-//  * warp 0, lane 0 streams the rows into a shared-memory ring with 1-D bulk
-//    copies of whole stages.  Weights are never written by an earlier kernel
-//    on the stream, so in the paired form (every stage of the CTA fits the
-//    ring) all stages go out before the wait on the previous kernel, while
-//    that kernel still computes on the same SM; then x is copied in with one
-//    bulk copy.  In the solo form x is copied first and the stages follow
-//    (an activation fetch queued behind the CTA's own weight stream arrives
-//    late, and everything after it waits for it).  Above 64 KB of x the
-//    compute threads load x themselves and the ring's stages go out first;
-//  * the other warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j
-//    of block b of every row it visits (32 low nibbles of sub-block 2j, 32
-//    high nibbles of 2j+1) and decodes the two 6-bit scale/min pairs it needs
-//    from the block header.  Passes of two rows are numbered across the whole
-//    CTA, so different warps work on different stages at once.
+// Roles in a CTA (a contiguous range of output rows, 16 warps, all of them
+// computing: an SM sub-partition then runs 4 warps of up to 128 registers):
+//  * thread 0 issues the first ring stages: 1-D bulk copies of whole stages
+//    of rows.  Weights are never written by an earlier kernel on the stream,
+//    so stages may go out before the wait on the previous kernel; with x
+//    staged in shared memory (up to 64 KB of it) x is copied first, right
+//    after that wait, and the first stages follow (an activation fetch
+//    queued behind the CTA's own weight stream arrives late, and everything
+//    after it waits for it).  Above 64 KB of x the compute threads load x
+//    themselves and the stages go out first;
+//  * every warp splits its share of x into byte planes; then the first ncw
+//    warps are "slab lanes": lane (b, j) owns the 32-byte qs slab j of block
+//    b of every row it visits (32 low nibbles of sub-block 2j, 32 high
+//    nibbles of 2j+1) and decodes the two 6-bit scale/min pairs it needs
+//    from the block header.  A row group takes passes r, r + rg, ... of the
+//    CTA's rows, kRP rows per row slot and pass;
+//  * the warp that finishes the last pass of a ring slot's stage issues the
+//    stage that next uses the slot (a per-slot pass counter with
+//    release/acquire ordering and an async-proxy fence before the copy), so
+//    no thread is set aside for copying.
 //
 // The code-dot Σ x·q of a sub-block runs on integer dot-product instructions
 // (four byte products per instruction).  Each 32-value group g of x is split,
@@ -540,6 +545,19 @@ __device__ __forceinline__ void split_x(const float *xsrc, int TK, int ct, int n
     }
 }
 
+// Wait until *tag == want (a ring slot's stage tag), bounded; false on
+// time-out or when another thread of the CTA has given up.
+__device__ __forceinline__ bool wait_tag(const int *tag, int want, long long limit, const volatile int *abort) {
+    const volatile int *t = tag;
+    if (*t == want) return true;
+    const long long t0 = clock64();
+    while (*t != want) {
+        if (*abort || clock64() - t0 > limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // Sum of kRP (2 or 4) row partials v[] over a slot of G lanes (G a power of
 // two, at least kRP; slots are aligned lane groups): exchange levels leave
 // each lane with one row, the rest is a butterfly.  Lane l of the slot ends
@@ -649,7 +667,7 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
         // (A test may ask for one stage never to arrive, to see a wait run
         // out; nothing then writes into the slot.)
         if (st == p.withhold) return;
-        holds[slot] = st;
+        *reinterpret_cast<volatile int *>(&holds[slot]) = st;
         // Gate (or only) rows [v0, min(v1, nrows)), then up rows.
         const int g1 = kSwiGLU ? min(v1, nrows) : v1;
         if (g1 > v0) {
@@ -758,7 +776,12 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
         uint32_t phase = (st / p.nslots) & 1;
         for (int pass = rgi; pass < npasses;) {
             if (abort_flag) break;
-            if (!mbar_wait_abortable(&full_bar[slot], phase, p.wait_limit, &abort_flag)) {
+            // The slot's tag names the stage last issued into it; a stage is
+            // issued only once the slot's previous stage has been consumed,
+            // so once the tag names this stage the parity wait below refers
+            // to it, whichever group consumed the previous one.
+            if (!wait_tag(&holds[slot], st, p.wait_limit, &abort_flag) ||
+                !mbar_wait_abortable(&full_bar[slot], phase, p.wait_limit, &abort_flag)) {
                 abort_flag = 1;
                 flag_timeout(p.status);
                 break;

@@ -6,7 +6,6 @@
 
 #include <cstddef>
 #include <cstdint>
-#include <vector>
 
 namespace q4mm {
 
@@ -30,6 +29,7 @@ constexpr int kT1Planes = 4;            // byte planes of the activation split
 constexpr int kT1PlaneSlabBytes = 64 * kT1Planes + 16;  // the planes of 64 activations + 16 B padding
 constexpr int kT1SlotRows = 4;          // rows a row slot (a warp's lanes of one row) takes per pass
 constexpr int kT1SlotRowsWide = 2;      // the same where 4-row stages do not fit shared memory
+constexpr int kT1MaxSlots = 16;         // ring depth at most
 
 struct T1Geometry {
     int ok = 0;            // 0: the kernel cannot take this shape
@@ -45,6 +45,7 @@ struct T1Geometry {
     int grid = 0;
     int x_staged = 0;      // x arrives by one bulk copy
     int nslots = 0;        // ring depth
+    int nstages = 0;       // stages of the CTA's rows
     int pre_stages = 0;    // stages issued before the wait on the previous kernel
     size_t xs_bytes = 0;   // planes, group steps and sums, and (staged) x
     size_t part_bytes = 0; // per-row partial sums of wide rows / SwiGLU
@@ -56,30 +57,6 @@ inline int t1_next_pow2(int v) {
     int p = 1;
     while (p < v) p <<= 1;
     return p;
-}
-
-// Row group r takes passes r, r + rg, r + 2·rg, … (pps passes per stage) and
-// waits on the full barrier of each stage it has a pass in, by phase parity.
-// A wait on a reused slot is sound when the group itself consumed the slot's
-// previous stage: that phase has then completed and the parity names the
-// stage awaited.  Otherwise a previous stage that has not landed yet has the
-// other parity, the wait returns at once and the group would read the old
-// contents.  True when every wait of every group is sound that way.
-inline bool t1_ring_covered(int npasses, int pps, int rg, int nslots) {
-    const int nstages = (npasses + pps - 1) / pps;
-    if (nslots >= nstages) return true;          // no slot is reused
-    if (pps % rg == 0) return true;              // every group has a pass in every stage
-    if (rg % pps == 0) return nslots % (rg / pps) == 0;  // group r: stages r/pps + i·rg/pps
-    std::vector<char> seen(nstages);
-    for (int r = 0; r < rg; ++r) {
-        for (int s = 0; s < nstages; ++s) seen[s] = 0;
-        for (int p = r; p < npasses; p += rg) {
-            const int st = p / pps;
-            if (st >= nslots && !seen[st - nslots]) return false;
-            seen[st] = 1;
-        }
-    }
-    return true;
 }
 
 // Shared memory of the activation side: the byte planes of every 64 values,
@@ -110,14 +87,16 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
     g.rg = (warps / T) / g.wc;
     g.ncw = T * g.wc * g.rg;
     // Stage: whole passes, at least stage_bytes of weights (bulk copies of
-    // 16 KB and more run at full HBM bandwidth).  When the ring must be
-    // reused, a stage holds a pass of every row group (or several): all
-    // groups then work on the same stage and the rest of the ring is
-    // prefetch, and a group that waits on a reused slot has always consumed
-    // the slot's previous stage itself.  A row size off the 16-byte grid
-    // (Q6_K) lets a stage start anywhere: its slot holds the bytes from the
-    // 16-byte boundary below the stage's first byte, so it is 16 bytes
-    // longer.
+    // 16 KB and more run at full HBM bandwidth).  A ring slot is refilled by
+    // the warp that finishes its stage, and every consumer first waits for
+    // the slot's stage tag to name the stage it wants before its parity wait,
+    // so a ring of any depth is sound, whichever row group consumed a slot's
+    // previous stage (without the tag, a ring whose depth is not a multiple
+    // of the groups' stage stride measured up to 10% slower on 4096 → 11008:
+    // its rings had to be cut to a depth where every wait followed the
+    // waiting group's own consumption of the slot).  A row size off the 16-byte grid (Q6_K) lets a stage
+    // start anywhere: its slot holds the bytes from the 16-byte boundary
+    // below the stage's first byte, so it is 16 bytes longer.
     const size_t slot_pad = row_bytes % 16 ? 16 : 0;
 
     // Grid.  A CTA of the next launch on the stream can only start where a
@@ -138,7 +117,6 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
 
     const size_t TK = (size_t)T * K;
     const int vrows = vrow_mult * rows;
-    const int npasses = (vrows + g.pass_rows - 1) / g.pass_rows;
     g.x_staged = TK * sizeof(float) <= (size_t)tun.x_stage_max ? 1 : 0;
     g.part_bytes = (g.wide || vrow_mult > 1) ? (size_t)T * vrows * g.wc * sizeof(float) : 0;
     int nstages = 0, nslots = 0;
@@ -166,21 +144,23 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
         const size_t budget = (size_t)tun.ring_bytes;
         nslots = (int)((budget > fixed ? budget - fixed : 0) / (g.slot_bytes + 16));
         nslots = nslots < nstages ? nslots : nstages;
-        nslots = nslots < 8 ? nslots : 8;
+        nslots = nslots < kT1MaxSlots ? nslots : kT1MaxSlots;
     };
     plan_ring(g.pass_rows);
-    if (nslots < nstages) {
-        // The ring is reused: a pass of every row group per stage.
+    if (nslots < nstages && nslots < 4) {
+        // A ring of fewer than 4 pass-sized slots leaves each row group one
+        // stage in flight at a time, idle while its next stage streams in:
+        // then a stage holds a pass of every row group, all groups work on
+        // the same stage and the other slot is prefetch (measured at 16384²:
+        // 4587 GB/s against 3940 with 2-row passes and six slots).
         plan_ring(g.pass_rows * g.rg);
-        if (nslots < 2) nslots = nstages == 1 ? 1 : 2;
-        // Last resort for very large stages: one slot, its stages in turn.
-        if (smem_for(nslots) > (size_t)max_smem_optin) nslots = 1;
     }
-    // Every wait on a reused slot follows the waiting group's own pass in
-    // the slot's previous stage.
-    if (!t1_ring_covered(npasses, g.stage_rows / g.pass_rows, g.rg, nslots)) return g;
+    if (nslots < 2) nslots = nstages == 1 ? 1 : 2;
+    // Last resort for very large stages: one slot, its stages in turn.
+    if (smem_for(nslots) > (size_t)max_smem_optin) nslots = 1;
     g.ncw = T * g.wc * g.rg;
     g.nslots = nslots;
+    g.nstages = nstages;
     // With plain activation loads nothing needs to go out ahead of the rest.
     g.pre_stages = g.x_staged ? 0 : nslots;
     g.smem = smem_for(nslots);

@@ -8,9 +8,10 @@ The wait is made to run out through the library's test hook
 weight stage and bounds its waits by about a millisecond.  Nothing is left
 in flight, nothing traps or waits without a bound.  Covered: the one-token
 kernel (a ring that holds every stage, and one that is reused), a Q6_K
-row format whose stages start off the 16-byte grid, the 2-8 token kernel and
-the tensor-core prefill (a cluster of CTAs that still meet at their cluster
-barriers and release tensor memory).
+row format whose stages start off the 16-byte grid, the fused gate+up FFN,
+the 2-8 token kernel and the tensor-core prefill on canonical and relayouted
+weights and above 128 tokens (clusters of CTAs that still meet at their
+cluster barriers and release tensor memory).
 """
 import time
 
@@ -88,3 +89,41 @@ def test_tensor_core_wait_runs_out_then_next_call_is_right():
     y = q.q4k_matmul_tc(xd, wd, N=N).cpu().numpy()
     q.device_status()
     assert_rows_close(y, oracle.q4k_matmul_bf16(x, W, K, N), REL, "after a time-out")
+
+
+def test_tensor_core_relayouted_and_wide_tile_waits_run_out():
+    # The relayouted weight (one bulk copy per chunk), and a 200-token call
+    # (the bf16 pre-pass, then tiles whose activations come by TMA).
+    import torch
+    import quantized_matmul_q4_gb300 as q
+    for K, N, T, relay in ((4096, 512, 64, True), (2048, 300, 200, False)):
+        W, x = _q4k_case(K, N, T, seed=K + T)
+        wd, xd = dev(W.reshape(-1)), dev(x)
+        wr = q.q4k_relayout_tc(wd, K, N=N) if relay else None
+        junk = torch.empty((T, N), dtype=torch.float32, device="cuda")
+        if relay:
+            _fail_once(lambda: q.q4k_matmul_tc_relayouted(xd, wr, N=N, out=junk))
+            y = q.q4k_matmul_tc_relayouted(xd, wr, N=N).cpu().numpy()
+        else:
+            _fail_once(lambda: q.q4k_matmul_tc(xd, wd, N=N, out=junk))
+            y = q.q4k_matmul_tc(xd, wd, N=N).cpu().numpy()
+        q.device_status()
+        assert_rows_close(y, oracle.q4k_matmul_bf16(x, W, K, N), REL, f"after a time-out, relay={relay}")
+
+
+def test_fused_ffn_wait_runs_out_then_next_call_is_right():
+    import torch
+    import quantized_matmul_q4_gb300 as q
+    K, N = 4096, 11008
+    g = synth.rng(41)
+    Wg, Wu, x = synth.q4k_weights(g, N, K), synth.q4k_weights(g, N, K), synth.activations(g, 1, K)
+    gd, ud, xd = dev(Wg.reshape(-1)), dev(Wu.reshape(-1)), dev(x)
+    junk = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    _fail_once(lambda: q.q4k_ffn_swiglu(xd, gd, ud, N=N, out=junk))
+    h = q.q4k_ffn_swiglu(xd, gd, ud, N=N).cpu().numpy()
+    q.device_status()
+    g_ref, u_ref, h_ref = oracle.q4k_ffn_swiglu(x, Wg, Wu, K, N)
+    silu = g_ref / (1.0 + np.exp(-g_ref))
+    # The fused FFN's bound (1e-4 on g and u, silu 1.1-Lipschitz), per token.
+    bound = 1e-4 * np.abs(u_ref).max() * (1.1 * np.abs(g_ref).max() + np.abs(silu).max()) + 1e-6 * np.abs(h_ref).max()
+    assert np.abs(h - h_ref).max() <= bound, "after a time-out"
