@@ -112,8 +112,10 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
     return a0 < b0 + nb && b0 < a0 + na;
 }
 
+// w_bytes_per_row: the weight's bytes per output row; w_total_bytes, when
+// nonzero, its whole size instead (a layout padded past N rows).
 int check_common(const float *x, const void *w, const float *y, int K, int N, int T, int k_multiple,
-                 size_t w_bytes_per_row, size_t w_align) {
+                 size_t w_bytes_per_row, size_t w_align, size_t w_total_bytes = 0) {
     if (!x || !w || !y) return fail(Q4MM_ERR_NULL, "x, weight and y must be non-NULL");
     if (K <= 0 || N <= 0 || T <= 0)
         return fail(Q4MM_ERR_DIM, "inputDim (%d), outputDim (%d) and tokens (%d) must be positive", K, N, T);
@@ -126,7 +128,7 @@ int check_common(const float *x, const void *w, const float *y, int K, int N, in
     if (reinterpret_cast<uintptr_t>(w) % w_align)
         return fail(Q4MM_ERR_ALIGN, "weight must be %zu-byte aligned", w_align);
     const size_t xb = (size_t)T * K * sizeof(float), yb = (size_t)T * N * sizeof(float);
-    const size_t wb = (size_t)N * w_bytes_per_row;
+    const size_t wb = w_total_bytes ? w_total_bytes : (size_t)N * w_bytes_per_row;
     if (overlap(x, xb, y, yb) || overlap(x, xb, w, wb) || overlap(w, wb, y, yb))
         return fail(Q4MM_ERR_ALIAS, "x, weight and y must not overlap");
     return Q4MM_OK;
@@ -255,13 +257,9 @@ int q4k_relayout_tc(const void *w_q4k, void *w_tc, int inputDim, int outputDim, 
 
 int q4k_matmul_tc_relayouted(const float *x, const void *w_tc, float *y, int inputDim, int outputDim, int tokens,
                              q4mm_stream_t stream) {
-    // The weight-overlap check takes the padded size: a per-row figure
-    // rounded up so that N rows cover Q4MM_TC_RELAYOUT_BYTES.
-    int rc = check_common(x, w_tc, y, inputDim, outputDim, tokens, 256,
-                          outputDim > 0 && inputDim > 0
-                              ? (Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim) + outputDim - 1) / (size_t)outputDim
-                              : 0,
-                          16);
+    // The weight-overlap check takes the padded layout's exact size.
+    int rc = check_common(x, w_tc, y, inputDim, outputDim, tokens, 256, 0, 16,
+                          inputDim > 0 && outputDim > 0 ? Q4MM_TC_RELAYOUT_BYTES(inputDim, outputDim) : 0);
     if (rc) return rc;
     q4mm::LaunchCtx ctx;
     if ((rc = device_ctx(stream, &ctx))) return rc;

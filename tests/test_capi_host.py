@@ -191,3 +191,23 @@ def test_relayout_validation(q4mm):
     with pytest.raises(q4mm.Q4mmError) as e:
         q4mm.q4k_matmul_tc_relayouted_ptr(X, W + 4, Y, 256, 4, 1, 0)
     assert e.value.code == ALIGN
+
+
+def test_relayouted_weight_adjacent_to_y_is_not_an_overlap(q4mm):
+    # The relayouted weight is padded to whole 256-row tiles: the overlap
+    # check must use that exact size, so a y placed right after it is
+    # accepted (here validation then stops at the device query: this test
+    # runs only where no GPU is present, so nothing is launched on these
+    # fake addresses).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses are only safe without a GPU")
+    K, N = 1024, 300
+    nbytes = q4mm.tc_relayout_bytes(K, N)
+    assert nbytes == 512 * (K // 64) * 48
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_relayouted_ptr(X, W, W + nbytes, K, N, 1, 0)
+    assert e.value.code != ALIAS, q4mm.last_error()
+    with pytest.raises(q4mm.Q4mmError) as e:
+        q4mm.q4k_matmul_tc_relayouted_ptr(X, W, W + nbytes - 16, K, N, 1, 0)
+    assert e.value.code == ALIAS
