@@ -19,12 +19,15 @@ struct MultiGeometry {
     int rows_per_cta = 0;  // multiple of kMultiRows
     int nslots = 0;        // ring depth (groups in flight)
     int consumers = 0;     // compute warps that take groups: min(kMultiCw, nslots)
+    int x_staged = 0;      // x copied into shared memory (T·K fp32 beside the ring)
     size_t smem = 0;       // dynamic shared memory per CTA
 };
 
 // ring_bytes: byte budget of the ring (the library passes kMultiRingBytes; the
-// CPU tests also check smaller budgets).
-inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes) {
+// CPU tests also check smaller budgets).  T: tokens (x is staged in shared
+// memory when its T·K fp32 values fit beside a ring of one slot per
+// consumer warp; T = 0 never stages).
+inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes, int T = 0) {
     MultiGeometry g;
     const size_t row_bytes = (size_t)(K / 256) * 144;
     const size_t slot_bytes = kMultiRows * row_bytes;
@@ -33,19 +36,32 @@ inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_opt
     g.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);
     g.grid = (N + g.rows_per_cta - 1) / g.rows_per_cta;
     const int cta_groups = g.rows_per_cta / kMultiRows;
-    // Ring: up to ring_bytes, at least two slots, never more slots than groups.
-    size_t fit = (size_t)ring_bytes / slot_bytes;
-    if (fit < 2) fit = 2;
-    int n = cta_groups < 16 ? cta_groups : 16;
-    if ((size_t)n > fit) n = (int)fit;
-    const int least = cta_groups < 2 ? cta_groups : 2;
-    if (n < least) n = least;
-    // Every slot has one consumer warp (see the kernel): from kMultiCw slots
-    // on, a multiple of kMultiCw; below that, one warp per slot.
-    if (n >= kMultiCw) n = n / kMultiCw * kMultiCw;
-    g.nslots = n;
-    g.consumers = n < kMultiCw ? n : kMultiCw;
-    g.smem = (size_t)n * slot_bytes + 2 * (size_t)n * sizeof(uint64_t);
+    const size_t bars = 2 * sizeof(uint64_t);  // x barrier (+ padding)
+    const size_t x_bytes = (size_t)T * K * sizeof(float);
+    auto plan = [&](size_t budget) {
+        // Ring: up to budget, at least two slots, never more slots than groups.
+        size_t fit = budget / slot_bytes;
+        if (fit < 2) fit = 2;
+        int n = cta_groups < 16 ? cta_groups : 16;
+        if ((size_t)n > fit) n = (int)fit;
+        const int least = cta_groups < 2 ? cta_groups : 2;
+        if (n < least) n = least;
+        // Every slot has one consumer warp (see the kernel): from kMultiCw slots
+        // on, a multiple of kMultiCw; below that, one warp per slot.
+        if (n >= kMultiCw) n = n / kMultiCw * kMultiCw;
+        g.nslots = n;
+        g.consumers = n < kMultiCw ? n : kMultiCw;
+        g.smem = (size_t)n * slot_bytes + 2 * (size_t)n * sizeof(uint64_t) + bars;
+    };
+    const int want_slots = cta_groups < kMultiCw ? cta_groups : kMultiCw;
+    if (T > 0 && x_bytes + (size_t)want_slots * slot_bytes + 2 * (size_t)want_slots * sizeof(uint64_t) + bars + 1024 <=
+                     (size_t)max_smem_optin) {
+        plan((size_t)max_smem_optin - 1024 - x_bytes - bars - 2 * 16 * sizeof(uint64_t));
+        g.x_staged = 1;
+        g.smem += x_bytes;
+    } else {
+        plan((size_t)ring_bytes);
+    }
     g.ok = g.smem <= (size_t)max_smem_optin ? 1 : 0;
     return g;
 }

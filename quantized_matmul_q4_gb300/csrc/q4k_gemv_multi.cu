@@ -79,7 +79,11 @@ struct MultiParams {
     int withhold;          // test only: a group whose copy is never issued (-1: none)
 };
 
-template <int TT>
+// kXs: x is staged in shared memory by one bulk copy (its T·K fp32 values
+// fit beside the ring), so the per-block activation loads are shared-memory
+// loads instead of L2 round trips.
+
+template <int TT, bool kXs>
 __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(MultiParams p) {
     extern __shared__ __align__(128) uint8_t msmem[];
     __shared__ volatile int abort_flag;  // set by the first warp whose wait runs out
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     uint8_t *ring = msmem;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty = full + p.nslots;
+    uint64_t *x_bar = empty + p.nslots;
+    float *xs = reinterpret_cast<float *>(x_bar + 2);  // [T][K] when staged
     const int row0 = blockIdx.x * p.rows_per_cta;
     const int nrows = min(p.rows_per_cta, p.N - row0);
     const int ngroups = (nrows + kMultiRows - 1) / kMultiRows;
@@ -98,6 +104,7 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(x_bar, 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -106,9 +113,21 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 
     if (warp == 0) {
         if (lane == 0) {
+            // Weights first (no earlier kernel writes them): the ring's first
+            // groups, then (staged) x, which the previous kernel may write,
+            // then the rest of the groups as slots free up.
+            const int first = min(ngroups, p.nslots);
+            bool x_out = !kXs;
+            auto issue_x = [&]() {
+                pdl_wait();
+                mbar_arrive_expect_tx(x_bar, (uint32_t)(p.T * p.K) * sizeof(float));
+                bulk_g2s(xs, p.x, (uint32_t)(p.T * p.K) * sizeof(float), x_bar);
+                x_out = true;
+            };
             int issued = 0;
             for (int g = 0; g < ngroups; ++g, ++issued) {
                 const int slot = g % p.nslots;
+                if (!x_out && g == first) issue_x();
                 if (g >= p.nslots &&
                     !mbar_wait_abortable(&empty[slot], ((g / p.nslots) - 1) & 1, p.wait_limit, &abort_flag)) {
                     abort_flag = 1;
@@ -123,11 +142,13 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
                 bulk_g2s(ring + (size_t)slot * slot_bytes,
                          p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes, &full[slot]);
             }
+            if (!x_out) issue_x();  // every group fitted the ring
             // Never leave a copy writing into an exiting CTA: the last
-            // groups issued (a withheld one has nothing in flight).
+            // groups issued (a withheld one has nothing in flight), and x.
             for (int g = max(0, issued - p.nslots); g < issued; ++g)
                 if (g != p.withhold)
                     (void)mbar_wait_bounded(&full[g % p.nslots], (g / p.nslots) & 1, p.wait_limit);
+            if (kXs) (void)mbar_wait_bounded(x_bar, 0, p.wait_limit);
         }
         __syncwarp();
         return;
@@ -146,6 +167,12 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     const int j = lane >> 3, wq = lane & 7;   // slab and word within it
     // x may be produced by the previous kernel on the stream.
     pdl_wait();
+    if (kXs && !__all_sync(0xffffffffu, mbar_wait_abortable(x_bar, 0, p.wait_limit, &abort_flag))) {
+        abort_flag = 1;
+        flag_timeout(p.status);
+        return;
+    }
+    const float *xsrc = kXs ? xs : p.x;
     for (int g = cw; g < ngroups; g += ncons) {
         const int slot = g % p.nslots;
         if (!__all_sync(0xffffffffu, mbar_wait_abortable(&full[slot], (g / p.nslots) & 1, p.wait_limit, &abort_flag))) {
@@ -168,9 +195,14 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
                 if (t < p.T) {
-                    const float *xt = p.x + (size_t)t * p.K + k0;
-                    xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
-                    xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                    const float *xt = xsrc + (size_t)t * p.K + k0;
+                    if constexpr (kXs) {
+                        xl[t] = *reinterpret_cast<const float4 *>(xt);
+                        xh[t] = *reinterpret_cast<const float4 *>(xt + 32);
+                    } else {
+                        xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
+                        xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                    }
                 } else {
                     xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
                     xh[t] = xl[t];
@@ -259,19 +291,19 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.nb = K / kQ4kValues;
     p.wait_limit = c.wait_limit;
     p.withhold = c.withhold;
-    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes);
+    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes, T);
     if (!g.ok) return cudaErrorNotSupported;
     p.rows_per_cta = g.rows_per_cta;
     p.nslots = g.nslots;
     const int grid = g.grid;
     const size_t smem = g.smem;
 
-#define Q4MM_MULTI_CASE(TT)                                                                    \
-    {                                                                                          \
-        cudaError_t e = ensure_smem(q4k_gemv_multi_kernel<TT>, smem);                          \
-        if (e != cudaSuccess) return e;                                                        \
-        return launch_kernel(c, q4k_gemv_multi_kernel<TT>, dim3(grid), dim3(32 * kMultiWarps), \
-                             smem, p);                                                         \
+#define Q4MM_MULTI_CASE(TT)                                                                           \
+    {                                                                                                 \
+        auto kernel = g.x_staged ? q4k_gemv_multi_kernel<TT, true> : q4k_gemv_multi_kernel<TT, false>; \
+        cudaError_t e = ensure_smem(kernel, smem);                                                    \
+        if (e != cudaSuccess) return e;                                                               \
+        return launch_kernel(c, kernel, dim3(grid), dim3(32 * kMultiWarps), smem, p);                 \
     }
     if (T <= 2) Q4MM_MULTI_CASE(2)
     if (T <= 4) Q4MM_MULTI_CASE(4)

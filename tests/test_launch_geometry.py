@@ -32,7 +32,7 @@ def _shim(tmp_path_factory):
                         os.path.join(HERE, "launch_geometry_shim.cpp")], check=True)
         lib = ctypes.CDLL(out)
         lib.t1_plan.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
-        lib.multi_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_longlong)]
+        lib.multi_plan.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_longlong)]
         _LIB.append(lib)
     return _LIB[0]
 
@@ -137,16 +137,16 @@ def test_streaming_launches_keep_stages_in_flight(plan):
         assert g["nslots"] >= 4 or g["stage_rows"] % (g["pass_rows"] * g["rg"]) == 0, (K, N, g)
 
 
-MULTI = ["ok", "grid", "rows_per_cta", "nslots", "consumers", "smem"]
+MULTI = ["ok", "grid", "rows_per_cta", "nslots", "consumers", "smem", "x_staged"]
 
 
 @pytest.fixture(scope="module")
 def multi(tmp_path_factory):
     lib = _shim(tmp_path_factory)
 
-    def call(K, N, ring_bytes=200 * 1024):
+    def call(K, N, ring_bytes=200 * 1024, T=0):
         buf = (ctypes.c_longlong * len(MULTI))()
-        lib.multi_plan(K, N, SMS, SMEM, ring_bytes, buf)
+        lib.multi_plan(K, N, SMS, SMEM, ring_bytes, T, buf)
         return dict(zip(MULTI, buf))
     return call
 
@@ -187,3 +187,23 @@ def test_multi_token_known_geometries(multi):
     # 4096 -> 11008: 19 groups per CTA, 16 slots would fit; 14 keep two per warp.
     g = multi(4096, 11008)
     assert (g["nslots"], g["consumers"]) == (14, 7)
+
+
+def test_multi_token_x_staged_where_it_fits(multi):
+    # x (T·K fp32) goes into shared memory when it fits beside one ring slot
+    # per consumer warp; the slot rule (one consumer per slot, slots a
+    # multiple of the consumers) holds either way.
+    for K in range(256, 32768 + 1, 256):
+        for T in (2, 4, 5, 8):
+            for N in (100, 4096, 11008):
+                g = multi(K, N, 200 * 1024, T)
+                if not g["ok"]:
+                    continue
+                n, c = g["nslots"], g["consumers"]
+                assert g["smem"] <= SMEM and c == min(7, n) and n % c == 0
+                row_bytes = (K // 256) * 144
+                if g["x_staged"]:
+                    assert g["smem"] >= T * K * 4 + n * 4 * row_bytes
+    assert multi(4096, 4096, 200 * 1024, 8)["x_staged"] == 1
+    assert multi(4096, 11008, 200 * 1024, 8)["x_staged"] == 1
+    assert multi(11008, 4096, 200 * 1024, 8)["x_staged"] == 0
