@@ -39,11 +39,13 @@
 // that the 43 row tiles of an 11008-row weight spread over 129 SMs.  Each
 // CTA accumulates its K range in tensor memory (at most 16384 values of K,
 // within which the tensor core's fp32 accumulation stays far inside the
-// stated tolerance).  Every rank copies its accumulators into its own shared
-// memory; after a cluster barrier each rank takes one S-th of the tile's
-// outputs, adds the S ranks' values in rank order through distributed shared
-// memory and writes them to y, so the result does not depend on scheduling
-// and no partial sum goes through global memory.
+// stated tolerance).  Rank s of a cluster owns the tile's rows
+// [floor(256·s/S), floor(256·(s+1)/S)): every rank writes its accumulators to
+// a row-major shared tile, one thread sends each other rank the rows it owns
+// with one shared-to-cluster bulk copy, and each rank adds the S partial sums
+// of its rows in rank order from local shared memory and writes y, so the
+// result does not depend on scheduling and no partial sum goes through
+// global memory.
 //
 // Tensor memory (512 columns, one CTA per SM): D of row half m at columns
 // c_D·m .. c_D·m + N, with c_D = 64 up to 64 tokens and 128 above; A of
@@ -52,8 +54,7 @@
 // operand ring is as deep as the remaining columns allow: 6 stages up to 64
 // tokens, 4 above.  A stage is released when its MMAs complete, so the ring
 // must cover the MMAs' completion latency as well as the dequantization of
-// the next chunks: measured on GB300, 4 stages held 64-token MMAs to about
-// half of the tensor pipe's rate.
+// the next chunks.
 //
 // Roles in a CTA:
 //  * warp 16 (one thread) issues the weight chunk copies, before the wait on
@@ -69,11 +70,14 @@
 //    activations the same threads also write the chunk's activation tile.
 //  * warp 17 allocates tensor memory; the first threads of warps 17 and 18
 //    issue the chunk's MMAs of row half 0 and 1 (four K steps of 16 each)
-//    and commit them to the chunk's ring stage.
-//  * warps 0–15 then read the accumulators (tcgen05.ld) into shared memory,
-//    and every thread takes part in the cluster-wide reduction.
+//    and commit them to the chunk's ring stage.  An MMA instruction is
+//    accepted only about as fast as the tensor pipe runs it (measured on
+//    GB300), so whatever one issuer does between chunks leaves the pipe idle
+//    unless the other issuer fills that time.
+//  * warps 0–15 then read the accumulators (tcgen05.ld) into the shared
+//    tile, and every thread takes part in the local sum.
 // All mbarrier waits are bounded; a time-out sets the device status word and
-// every thread still reaches the two cluster barriers.
+// every thread still reaches the cluster barriers of every epilogue pass.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
