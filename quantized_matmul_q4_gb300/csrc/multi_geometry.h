@@ -12,6 +12,10 @@ constexpr int kMultiWarps = 8;  // copy warp + 7 compute warps
 constexpr int kMultiCw = kMultiWarps - 1;
 constexpr int kMultiRows = 4;   // rows per group (one ring slot)
 constexpr int kMultiRingBytes = 200 * 1024;  // ring budget the library launches with
+constexpr int kMultiTabBlocks = 16;          // blocks per scale-table chunk
+// Per compute warp: the decoded (scale', offset') of 8 sub-blocks of 4 rows ×
+// kMultiTabBlocks blocks, fp32 pairs.
+constexpr size_t kMultiTabBytes = (size_t)kMultiRows * kMultiTabBlocks * 8 * 2 * sizeof(float);
 
 struct MultiGeometry {
     int ok = 0;            // 0: the ring does not fit shared memory
@@ -23,6 +27,7 @@ struct MultiGeometry {
     size_t smem = 0;       // dynamic shared memory per CTA
 };
 
+// Shared memory: the compute warps' scale tables | ring | barriers | x.
 // ring_bytes: byte budget of the ring (the library passes kMultiRingBytes; the
 // CPU tests also check smaller budgets).  T: tokens (x is staged in shared
 // memory when its T·K fp32 values fit beside a ring of one slot per
@@ -37,6 +42,7 @@ inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_opt
     g.grid = (N + g.rows_per_cta - 1) / g.rows_per_cta;
     const int cta_groups = g.rows_per_cta / kMultiRows;
     const size_t bars = 2 * sizeof(uint64_t);  // x barrier (+ padding)
+    const size_t tab = (size_t)kMultiCw * kMultiTabBytes;  // the compute warps' scale tables
     const size_t x_bytes = (size_t)T * K * sizeof(float);
     auto plan = [&](size_t budget) {
         // Ring: up to budget, at least two slots, never more slots than groups.
@@ -51,16 +57,18 @@ inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_opt
         if (n >= kMultiCw) n = n / kMultiCw * kMultiCw;
         g.nslots = n;
         g.consumers = n < kMultiCw ? n : kMultiCw;
-        g.smem = (size_t)n * slot_bytes + 2 * (size_t)n * sizeof(uint64_t) + bars;
+        g.smem = tab + (size_t)n * slot_bytes + 2 * (size_t)n * sizeof(uint64_t) + bars;
     };
     const int want_slots = cta_groups < kMultiCw ? cta_groups : kMultiCw;
-    if (T > 0 && x_bytes + (size_t)want_slots * slot_bytes + 2 * (size_t)want_slots * sizeof(uint64_t) + bars + 1024 <=
+    if (T > 0 && tab + x_bytes + (size_t)want_slots * slot_bytes + 2 * (size_t)want_slots * sizeof(uint64_t) + bars +
+                         1024 <=
                      (size_t)max_smem_optin) {
-        plan((size_t)max_smem_optin - 1024 - x_bytes - bars - 2 * 16 * sizeof(uint64_t));
+        plan((size_t)max_smem_optin - 1024 - tab - x_bytes - bars - 2 * 16 * sizeof(uint64_t));
         g.x_staged = 1;
         g.smem += x_bytes;
     } else {
-        plan((size_t)ring_bytes);
+        const size_t room = (size_t)max_smem_optin - 1024 - tab - bars - 2 * 16 * sizeof(uint64_t);
+        plan((size_t)ring_bytes < room ? (size_t)ring_bytes : room);
     }
     g.ok = g.smem <= (size_t)max_smem_optin ? 1 : 0;
     return g;

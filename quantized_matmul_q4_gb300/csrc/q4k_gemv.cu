@@ -693,19 +693,25 @@ __global__ void __launch_bounds__(32 * kT1Cw, 1) gemv_t1_kernel(T1Params p) {
         }
     };
 
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
         // The first stages of the ring, before or after x as the geometry
-        // says; x may be written by the previous kernel on the stream.
+        // says (x may be written by the previous kernel on the stream), one
+        // lane each: a bulk copy holds its issuing thread for a few hundred
+        // cycles, so one thread issuing them in turn would delay the last
+        // stage by thousands.
         const int first = min(nstages, p.nslots);
         const int pre = min(first, p.pre_stages);
-        int st = 0;
-        for (; st < pre; ++st) issue(st, st);
-        pdl_wait();
-        if (p.x_staged) {
-            mbar_arrive_expect_tx(&x_bar, (uint32_t)TK * sizeof(float));
-            bulk_g2s(xst, p.x, (uint32_t)TK * sizeof(float), &x_bar);
+        if (lane < pre) issue(lane, lane);
+        __syncwarp();
+        if (lane == 0) {
+            pdl_wait();
+            if (p.x_staged) {
+                mbar_arrive_expect_tx(&x_bar, (uint32_t)TK * sizeof(float));
+                bulk_g2s(xst, p.x, (uint32_t)TK * sizeof(float), &x_bar);
+            }
         }
-        for (; st < first; ++st) issue(st, st);
+        __syncwarp();
+        if (lane >= pre && lane < first) issue(lane, lane);
     }
 
     const bool worker = warp < ncw;  // warps past ncw only help with the split

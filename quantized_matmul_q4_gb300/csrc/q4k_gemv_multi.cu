@@ -54,9 +54,9 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 // 2..8 tokens: bulk-copied row groups, word lanes, register tiles
 // ----------------------------------------------------------------------------
 //
-// A CTA owns a contiguous range of rows in groups of four; one producer
-// thread streams each group (four whole rows) into its own ring slot with a
-// bulk copy, before the wait on the previous kernel.  Compute warp c takes
+// A CTA owns a contiguous range of rows in groups of four; the producer warp
+// streams each group (four whole rows) into its own ring slot with a bulk
+// copy (the first lap's copies one per lane, the refills from lane 0).  Compute warp c takes
 // groups c, c + n, … (n consumer warps, see the kernel), and for each group
 // walks all blocks of the rows:
 // lane l owns qs word l of every block — 4 low-nibble weights of sub-block
@@ -65,6 +65,11 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 // rows.  Each weight is dequantized once (scale'·(0.5 + q/256) − offset') and
 // multiplied into TT token accumulators, two positions per paired FMA.  A
 // butterfly over the 4·TT sums at the end of the group finishes the rows.
+//
+// The eight lanes of a slab share its two sub-blocks' scale' and offset', so
+// the warp decodes the block headers once into its own shared table (4 rows
+// × kMultiTabBlocks blocks × 4 slabs of (s0, o0, s1, o1)) before walking
+// those blocks, and each lane then reads its pair with one 16-byte load.
 
 struct MultiParams {
     const float *x;
@@ -90,7 +95,8 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
     const uint32_t slot_bytes = kMultiRows * row_bytes;
-    uint8_t *ring = msmem;
+    float4 *tabs = reinterpret_cast<float4 *>(msmem);  // kMultiCw tables
+    uint8_t *ring = msmem + kMultiCw * kMultiTabBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty = full + p.nslots;
     uint64_t *x_bar = empty + p.nslots;
@@ -112,37 +118,39 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     pdl_launch_dependents();
 
     if (warp == 0) {
+        // (A test may ask for one group never to arrive, to see a wait run
+        // out; nothing then writes into its slot.)
+        auto issue = [&](int g, int slot) {
+            const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            bulk_g2s(ring + (size_t)slot * slot_bytes, p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes,
+                     &full[slot]);
+        };
+        // Staged x first (the previous kernel on the stream may write it),
+        // then the ring's first groups, one lane each: a bulk copy holds its
+        // issuing thread for a few hundred cycles, so one thread issuing
+        // them in turn would delay the last by thousands.  Then the rest of
+        // the groups as slots free up, from lane 0.
+        const int first = min(ngroups, p.nslots);
+        if (kXs && lane == 0) {
+            pdl_wait();
+            mbar_arrive_expect_tx(x_bar, (uint32_t)(p.T * p.K) * sizeof(float));
+            bulk_g2s(xs, p.x, (uint32_t)(p.T * p.K) * sizeof(float), x_bar);
+        }
+        __syncwarp();
+        if (lane < first && lane != p.withhold) issue(lane, lane);
+        __syncwarp();
         if (lane == 0) {
-            // Weights first (no earlier kernel writes them): the ring's first
-            // groups, then (staged) x, which the previous kernel may write,
-            // then the rest of the groups as slots free up.
-            const int first = min(ngroups, p.nslots);
-            bool x_out = !kXs;
-            auto issue_x = [&]() {
-                pdl_wait();
-                mbar_arrive_expect_tx(x_bar, (uint32_t)(p.T * p.K) * sizeof(float));
-                bulk_g2s(xs, p.x, (uint32_t)(p.T * p.K) * sizeof(float), x_bar);
-                x_out = true;
-            };
-            int issued = 0;
-            for (int g = 0; g < ngroups; ++g, ++issued) {
+            int issued = first;
+            for (int g = first; g < ngroups; ++g, ++issued) {
                 const int slot = g % p.nslots;
-                if (!x_out && g == first) issue_x();
-                if (g >= p.nslots &&
-                    !mbar_wait_abortable(&empty[slot], ((g / p.nslots) - 1) & 1, p.wait_limit, &abort_flag)) {
+                if (!mbar_wait_abortable(&empty[slot], ((g / p.nslots) - 1) & 1, p.wait_limit, &abort_flag)) {
                     abort_flag = 1;
                     flag_timeout(p.status);
                     break;
                 }
-                // (A test may ask for one group never to arrive, to see a
-                // wait run out.)
-                if (g == p.withhold) continue;
-                const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                bulk_g2s(ring + (size_t)slot * slot_bytes,
-                         p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes, &full[slot]);
+                if (g != p.withhold) issue(g, slot);
             }
-            if (!x_out) issue_x();  // every group fitted the ring
             // Never leave a copy writing into an exiting CTA: the last
             // groups issued (a withheld one has nothing in flight), and x.
             for (int g = max(0, issued - p.nslots); g < issued; ++g)
@@ -173,6 +181,8 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
         return;
     }
     const float *xsrc = kXs ? xs : p.x;
+    constexpr int kTabEntries = kMultiRows * kMultiTabBlocks * 4;
+    float4 *tab = tabs + (size_t)cw * kTabEntries;
     for (int g = cw; g < ngroups; g += ncons) {
         const int slot = g % p.nslots;
         if (!__all_sync(0xffffffffu, mbar_wait_abortable(&full[slot], (g / p.nslots) & 1, p.wait_limit, &abort_flag))) {
@@ -188,48 +198,65 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 #pragma unroll
             for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
 
-        for (int b = 0; b < p.nb; ++b) {
-            // Activations of this lane's 8 positions for every token.
-            float4 xl[TT], xh[TT];
-            const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
+        for (int b0 = 0; b0 < p.nb; b0 += kMultiTabBlocks) {
+            const int nbc = min(kMultiTabBlocks, p.nb - b0);
+            // Entry e = (r·kMultiTabBlocks + bb)·4 + slab; every lane keeps its
+            // slab (e mod 4 = lane mod 4), so the table fill is branch-free.
+            __syncwarp();  // the previous chunk's reads are done
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                if (t < p.T) {
-                    const float *xt = xsrc + (size_t)t * p.K + k0;
-                    if constexpr (kXs) {
-                        xl[t] = *reinterpret_cast<const float4 *>(xt);
-                        xh[t] = *reinterpret_cast<const float4 *>(xt + 32);
-                    } else {
-                        xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
-                        xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
-                    }
-                } else {
-                    xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    xh[t] = xl[t];
+            for (int i = 0; i < kTabEntries / 32; ++i) {
+                const int e = lane + 32 * i;
+                const int bb = (e >> 2) % kMultiTabBlocks, r = e / (4 * kMultiTabBlocks);
+                if (bb < nbc) {
+                    const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)(b0 + bb) * kQ4kBytes;
+                    const SlabScales sc = slab_scales(*reinterpret_cast<const uint4 *>(blk), e & 3);
+                    tab[e] = make_float4(sc.s0, sc.o0, sc.s1, sc.o1);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < kMultiRows; ++r) {
-                // Absent rows of a short last group read row 0 of the slot;
-                // their sums are never stored.
-                const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
-                const SlabScales sc = slab_scales(hdr, j);
-                const uint32_t l4 = q & 0x0F0F0F0Fu;
-                const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
-                const float2 s0 = make_float2(sc.s0, sc.s0), n0 = make_float2(-sc.o0, -sc.o0);
-                const float2 s1 = make_float2(sc.s1, sc.s1), n1 = make_float2(-sc.o1, -sc.o1);
-                const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
-                const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
-                const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
-                const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+            __syncwarp();
+            for (int bb = 0; bb < nbc; ++bb) {
+                const int b = b0 + bb;
+                // Activations of this lane's 8 positions for every token.
+                float4 xl[TT], xh[TT];
+                const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
-                    acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
-                    acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
-                    acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
-                    acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                    if (t < p.T) {
+                        const float *xt = xsrc + (size_t)t * p.K + k0;
+                        if constexpr (kXs) {
+                            xl[t] = *reinterpret_cast<const float4 *>(xt);
+                            xh[t] = *reinterpret_cast<const float4 *>(xt + 32);
+                        } else {
+                            xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
+                            xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                        }
+                    } else {
+                        xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        xh[t] = xl[t];
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kMultiRows; ++r) {
+                    // Absent rows of a short last group read row 0 of the slot;
+                    // their sums are never stored.
+                    const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
+                    const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
+                    const float4 sc = tab[(r * kMultiTabBlocks + bb) * 4 + j];  // (s0, o0, s1, o1)
+                    const uint32_t l4 = q & 0x0F0F0F0Fu;
+                    const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
+                    const float2 s0 = make_float2(sc.x, sc.x), n0 = make_float2(-sc.y, -sc.y);
+                    const float2 s1 = make_float2(sc.z, sc.z), n1 = make_float2(-sc.w, -sc.w);
+                    const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
+                    const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
+                    const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
+                    const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) {
+                        acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
+                        acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
+                        acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
+                        acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                    }
                 }
             }
         }
