@@ -150,11 +150,10 @@ WORKLOADS = {w.name: w for w in [
     Workload("llama7b_decode_t1", "q4k", "q4k_matmul", LLAMA, 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers "
              "x q,k,v,o,gate,up,down), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], distinct=1, arithmetic=T1_ARITH),
-    Workload("llama7b_decode_t4", "q4k", "q4k_matmul", LLAMA, 4, 32, "GB/s", "hbm",
-             "gemv_t1_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers x "
-             "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv.cu", "t1_geometry.h", "q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,
-             arithmetic=T1_ARITH + " (one token per compute warp; the 11008-wide down projection on the "
-                                   "fp32 register-tile kernel)"),
+    Workload("llama7b_decode_t4", "q4k", "q4k_matmul", LLAMA, 4, 32, "GB/s", "alu",
+             "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers x "
+             "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,
+             arithmetic="fp32 dequantization and fp32 FMA"),
     Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "alu",
              "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
              "layers x q,k,v,o,gate,up,down), 8 tokens", ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,

@@ -77,7 +77,7 @@ typedef enum {
  * Precision: per token row t, max_o |y − y_exact| <= 1e-4 · max_o |y_exact|
  *         on the pages' test inputs and on rows with a wide dynamic range
  *         (activations of 1e5 next to ones of order 1, including on weights
- *         that are zero).  The bound behind it, up to 4 tokens: each 32-value
+ *         that are zero).  The bound behind it, up to 2 tokens: each 32-value
  *         group g of x is rounded once to a multiple of s_g·2^-23, s_g the
  *         power of two just above max_g|x|/255, i.e. to within
  *         max(2^-23·max_g|x|/255, 2^-127) (about 4.7e-10 of the group's
@@ -86,8 +86,8 @@ typedef enum {
  *         sums; so |y_o − y_exact,o| <= Σ_g 2^-23·max_g|x|/255·Σ_{k∈g}|w_ok|
  *         plus fp32 rounding of the scales, mins and sums (relative 2^-22 or
  *         so of each term).  A large activation changes only its own group's
- *         grid.  Where that kernel's geometry does not fit (2-4 tokens with a
- *         large inputDim), and above 4 tokens: fp32 dequantization and fp32
+ *         grid.  Where that kernel's geometry does not fit (2 tokens with a
+ *         large inputDim), and from 3 tokens on: fp32 dequantization and fp32
  *         fused multiply-add.
  * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
  * 64 tokens above that).

@@ -186,11 +186,13 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
         e = q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, 1);
     } else if (tokens <= 8) {
-        // Up to 4 tokens: the byte-plane kernel with one token per compute
-        // warp where its geometry allows (measured 1.4-1.9x faster at 2 and
-        // 4 tokens; at 8 tokens the FP32 kernel is faster on 4096x4096).
-        // Then the FP32 register-tile kernel, then the prefill kernel.
-        e = tokens > 4
+        // 2 tokens: the byte-plane kernel with one token per compute warp
+        // where its geometry allows (measured on GB300: 7.4 against 7.7 us
+        // at 4096x4096, 13.5 against 17.5 us at 4096 -> 11008).  From 3
+        // tokens on the FP32 register-tile kernel is as fast or faster (4
+        // tokens: 9.3 against 12.6 us and 21.8 against 24.1 us), then the
+        // prefill kernel where neither fits.
+        e = tokens > 2
                 ? cudaErrorNotSupported
                 : q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim, tokens);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);

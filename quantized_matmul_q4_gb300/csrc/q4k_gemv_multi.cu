@@ -263,14 +263,16 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
 
-        // Butterfly over the 4·TT sums: afterwards lane l holds value index
+        // Butterfly over the 4·TP sums (TP: TT rounded up to a power of two,
+        // the padding sums zero): afterwards lane l holds value index
         // idx .. idx + n − 1 (see the halving below), summed over the warp.
-        constexpr int V = kMultiRows * TT;
+        constexpr int TP = TT <= 2 ? 2 : TT <= 4 ? 4 : 8;
+        constexpr int V = kMultiRows * TP;
         float v[V];
 #pragma unroll
         for (int r = 0; r < kMultiRows; ++r)
 #pragma unroll
-            for (int t = 0; t < TT; ++t) v[r * TT + t] = acc[r][t].x + acc[r][t].y;
+            for (int t = 0; t < TP; ++t) v[r * TP + t] = t < TT ? acc[r][t].x + acc[r][t].y : 0.f;
         int idx = 0, n = V;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 #pragma unroll
             for (int i = 0; i < (V >= 32 ? V / 32 : 1); ++i) {
                 const int id = idx + i;
-                const int r = id / TT, t = id % TT;
+                const int r = id / TP, t = id % TP;
                 if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = v[i];
             }
         }
@@ -333,7 +335,9 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
         return launch_kernel(c, kernel, dim3(grid), dim3(32 * kMultiWarps), smem, p);                 \
     }
     if (T <= 2) Q4MM_MULTI_CASE(2)
+    if (T <= 3) Q4MM_MULTI_CASE(3)
     if (T <= 4) Q4MM_MULTI_CASE(4)
+    if (T <= 6) Q4MM_MULTI_CASE(6)
     if (T <= 8) Q4MM_MULTI_CASE(8)
 #undef Q4MM_MULTI_CASE
     return cudaErrorInvalidValue;

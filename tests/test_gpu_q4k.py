@@ -71,8 +71,12 @@ SWEEP = [
     (512, 1000, 1), (768, 5, 3), (1280, 33, 1), (2048, 17, 4), (4096, 33, 63), (4096, 65, 64),
     (4096, 7, 65), (11008, 33, 1), (11008, 3, 8), (11008, 9, 9), (8192, 31, 1), (16384, 5, 1),
     (24576, 3, 1), (24576, 3, 2), (65536, 2, 1), (3072, 1001, 1), (3072, 1001, 2),
-    # 2-4 tokens on the byte-plane kernel (one token per compute warp).
-    (4096, 300, 3), (4096, 1000, 4), (11008, 40, 2), (1024, 77, 4), (256, 9, 3),
+    # 2 tokens on the byte-plane kernel (one token per compute warp).
+    (11008, 40, 2), (4096, 77, 2),
+    # 3-8 tokens on the FP32 register-tile kernel (3, 4, 6 and 8 token
+    # tiles, the 3 and 6 token ones padded in the row butterfly).
+    (4096, 300, 3), (4096, 1000, 4), (1024, 77, 4), (256, 9, 3), (2048, 99, 3),
+    (4096, 301, 5), (768, 13, 6), (11008, 21, 5), (4096, 129, 7),
 ]
 
 
