@@ -1,4 +1,5 @@
-// Q4_K decode GEMV for 2..8 tokens (FP32 register tiles), sm_103a.
+// Q4_K decode GEMV for 3..8 tokens (FP32 register tiles; also 1..2 where the
+// one-token kernel's geometry does not fit), sm_103a.
 //
 // Computes y[t][o] = Σ_k x[t][k]·w[o][k] with w = d·sc_s·q − dmin·m_s decoded
 // on the fly from the 144-byte Q4_K super-blocks (SKaiNET PR #562
@@ -28,8 +29,8 @@ namespace {
 // Block scales of one lane
 // ----------------------------------------------------------------------------
 
-// Per-lane constants for the two sub-blocks 2j and 2j+1 of a block:
-// scale' = 256·d·sc and offset' = 128·d·sc + dmin·m.
+// Constants of slab j (the two sub-blocks 2j and 2j+1) of a block, decoded
+// into a warp's scale table: scale' = 256·d·sc and offset' = 128·d·sc + dmin·m.
 struct SlabScales {
     float s0, s1, o0, o1;
 };
@@ -51,20 +52,22 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 }
 
 // ----------------------------------------------------------------------------
-// 2..8 tokens: bulk-copied row groups, word lanes, register tiles
+// Row groups in a bulk-copy ring, word lanes, register tiles
 // ----------------------------------------------------------------------------
 //
 // A CTA owns a contiguous range of rows in groups of four; the producer warp
 // streams each group (four whole rows) into its own ring slot with a bulk
-// copy (the first lap's copies one per lane, the refills from lane 0).  Compute warp c takes
-// groups c, c + n, … (n consumer warps, see the kernel), and for each group
+// copy (the first lap's copies one per lane, the refills from lane 0).
+// Compute warp c takes groups c, c + n, … (n consumer warps, see the
+// kernel), and for each group
 // walks all blocks of the rows:
 // lane l owns qs word l of every block — 4 low-nibble weights of sub-block
 // 2j and 4 high-nibble weights of 2j+1 (j = l/8) — with the 8 matching
 // activations of all TT tokens loaded once per block and reused by the four
 // rows.  Each weight is dequantized once (scale'·(0.5 + q/256) − offset') and
-// multiplied into TT token accumulators, two positions per paired FMA.  A
-// butterfly over the 4·TT sums at the end of the group finishes the rows.
+// multiplied into TT token accumulators (TT ∈ {2, 3, 4, 6, 8}), two
+// positions per paired FMA.  A butterfly over the 4·TT sums (padded to a
+// power of two) at the end of the group finishes the rows.
 //
 // The eight lanes of a slab share its two sub-blocks' scale' and offset', so
 // the warp decodes the block headers once into its own shared table (4 rows
