@@ -14,8 +14,14 @@ constexpr int kMultiRows = 4;   // rows per group (one ring slot)
 constexpr int kMultiRingBytes = 200 * 1024;  // ring budget the library launches with
 constexpr int kMultiTabBlocks = 16;          // blocks per scale-table chunk
 // Per compute warp: the decoded (scale', offset') of 8 sub-blocks of 4 rows ×
-// kMultiTabBlocks blocks, fp32 pairs.
+// kMultiTabBlocks blocks, fp32 pairs.  (Up to 4 tokens a group is taken by a
+// pair of warps, each over half of the row's blocks, with tables of half
+// that many blocks: the same bytes for twice the warps.)
 constexpr size_t kMultiTabBytes = (size_t)kMultiRows * kMultiTabBlocks * 8 * 2 * sizeof(float);
+constexpr int kMultiSplitWarps = 1 + 2 * kMultiCw;  // copy warp + a pair per consumer (up to 4 tokens)
+// The pairs' exchange of partial sums: per pair two buffers of 16 floats and
+// two barriers, padded to 1 KB.
+constexpr size_t kMultiPairBytes = 1024;
 
 struct MultiGeometry {
     int ok = 0;            // 0: the ring does not fit shared memory
@@ -27,7 +33,8 @@ struct MultiGeometry {
     size_t smem = 0;       // dynamic shared memory per CTA
 };
 
-// Shared memory: the compute warps' scale tables | ring | barriers | x.
+// Shared memory: the compute warps' scale tables | pair exchange | ring |
+// barriers | x.
 // ring_bytes: byte budget of the ring (the library passes kMultiRingBytes; the
 // CPU tests also check smaller budgets).  T: tokens (x is staged in shared
 // memory when its T·K fp32 values fit beside a ring of one slot per
@@ -42,7 +49,7 @@ inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_opt
     g.grid = (N + g.rows_per_cta - 1) / g.rows_per_cta;
     const int cta_groups = g.rows_per_cta / kMultiRows;
     const size_t bars = 2 * sizeof(uint64_t);  // x barrier (+ padding)
-    const size_t tab = (size_t)kMultiCw * kMultiTabBytes;  // the compute warps' scale tables
+    const size_t tab = (size_t)kMultiCw * kMultiTabBytes + kMultiPairBytes;  // scale tables, pair exchange
     const size_t x_bytes = (size_t)T * K * sizeof(float);
     auto plan = [&](size_t budget) {
         // Ring: up to budget, at least two slots, never more slots than groups.

@@ -91,15 +91,24 @@ struct MultiParams {
 // fit beside the ring), so the per-block activation loads are shared-memory
 // loads instead of L2 round trips.
 
-template <int TT, bool kXs>
-__global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(MultiParams p) {
+// kSplit (up to 4 tokens): each group is taken by a pair of compute warps,
+// the first over blocks [0, nb/2) of its rows, the second over the rest; the
+// second hands its partial sums to the first through shared memory, which
+// adds them (first + second, so the result does not depend on timing) and
+// stores the rows.  Twice the warps hide more of each warp's latencies.
+
+template <int TT, bool kXs, bool kSplit>
+__global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps), 1)
+    q4k_gemv_multi_kernel(MultiParams p) {
     extern __shared__ __align__(128) uint8_t msmem[];
     __shared__ volatile int abort_flag;  // set by the first warp whose wait runs out
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
     const uint32_t slot_bytes = kMultiRows * row_bytes;
-    float4 *tabs = reinterpret_cast<float4 *>(msmem);  // kMultiCw tables
-    uint8_t *ring = msmem + kMultiCw * kMultiTabBytes;
+    float4 *tabs = reinterpret_cast<float4 *>(msmem);  // the compute warps' tables
+    float *pair_buf = reinterpret_cast<float *>(msmem + kMultiCw * kMultiTabBytes);  // [pair][2][16]
+    uint64_t *pair_bar = reinterpret_cast<uint64_t *>(pair_buf + kMultiCw * 2 * 16);  // [pair][2]
+    uint8_t *ring = msmem + kMultiCw * kMultiTabBytes + kMultiPairBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty = full + p.nslots;
     uint64_t *x_bar = empty + p.nslots;
@@ -111,8 +120,10 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nslots; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kSplit ? 2 : 1);  // both warps of a pair
         }
+        if (kSplit)
+            for (int i = 0; i < 2 * kMultiCw; ++i) mbar_init(&pair_bar[i], 1);
         mbar_init(x_bar, 1);
         abort_flag = 0;
         fence_mbar_init();
@@ -172,9 +183,18 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
     // slot's previous phase itself, so its parity wait can never match an
     // older phase (a warp reaching group g before group g − nslots, held by
     // another warp, has landed would read the slot's previous contents).
+    //
+    // With kSplit the consumers are pairs of warps (the slot rule holds per
+    // pair), and the first warp of a pair releases its slot only after it
+    // has read the second's partial sums of the group: the second can then
+    // be at most one group ahead, so each of the pair's two buffers (group
+    // parity) and barriers is reused only after its previous use is done.
     const int ncons = min(kMultiCw, p.nslots);
     const int cw = warp - 1;
-    if (cw >= ncons) return;
+    const int unit = kSplit ? cw >> 1 : cw;  // the pair (kSplit) or the warp
+    const bool second = kSplit && (cw & 1);  // the pair's second warp
+    if (unit >= ncons) return;
+    const int kb0 = second ? p.nb / 2 : 0, kb1 = (kSplit && !second) ? p.nb / 2 : p.nb;  // this warp's blocks
     const int j = lane >> 3, wq = lane & 7;   // slab and word within it
     // x may be produced by the previous kernel on the stream.
     pdl_wait();
@@ -184,9 +204,13 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
         return;
     }
     const float *xsrc = kXs ? xs : p.x;
-    constexpr int kTabEntries = kMultiRows * kMultiTabBlocks * 4;
+    constexpr int kTB = kSplit ? kMultiTabBlocks / 2 : kMultiTabBlocks;  // blocks per table chunk
+    constexpr int kTabEntries = kMultiRows * kTB * 4;
     float4 *tab = tabs + (size_t)cw * kTabEntries;
-    for (int g = cw; g < ngroups; g += ncons) {
+    float *pbuf = pair_buf + unit * 2 * 16;
+    uint64_t *pbar = pair_bar + unit * 2;
+    int lg = 0;  // this pair's (warp's) group count so far
+    for (int g = unit; g < ngroups; g += ncons, ++lg) {
         const int slot = g % p.nslots;
         if (!__all_sync(0xffffffffu, mbar_wait_abortable(&full[slot], (g / p.nslots) & 1, p.wait_limit, &abort_flag))) {
             abort_flag = 1;
@@ -201,15 +225,15 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
 #pragma unroll
             for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
 
-        for (int b0 = 0; b0 < p.nb; b0 += kMultiTabBlocks) {
-            const int nbc = min(kMultiTabBlocks, p.nb - b0);
-            // Entry e = (r·kMultiTabBlocks + bb)·4 + slab; every lane keeps its
+        for (int b0 = kb0; b0 < kb1; b0 += kTB) {
+            const int nbc = min(kTB, kb1 - b0);
+            // Entry e = (r·kTB + bb)·4 + slab; every lane keeps its
             // slab (e mod 4 = lane mod 4), so the table fill is branch-free.
             __syncwarp();  // the previous chunk's reads are done
 #pragma unroll
             for (int i = 0; i < kTabEntries / 32; ++i) {
                 const int e = lane + 32 * i;
-                const int bb = (e >> 2) % kMultiTabBlocks, r = e / (4 * kMultiTabBlocks);
+                const int bb = (e >> 2) % kTB, r = e / (4 * kTB);
                 if (bb < nbc) {
                     const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)(b0 + bb) * kQ4kBytes;
                     const SlabScales sc = slab_scales(*reinterpret_cast<const uint4 *>(blk), e & 3);
@@ -244,7 +268,7 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
                     // their sums are never stored.
                     const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
                     const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
-                    const float4 sc = tab[(r * kMultiTabBlocks + bb) * 4 + j];  // (s0, o0, s1, o1)
+                    const float4 sc = tab[(r * kTB + bb) * 4 + j];  // (s0, o0, s1, o1)
                     const uint32_t l4 = q & 0x0F0F0F0Fu;
                     const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
                     const float2 s0 = make_float2(sc.x, sc.x), n0 = make_float2(-sc.y, -sc.y);
@@ -264,7 +288,7 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0 && (!kSplit || second)) mbar_arrive(&empty[slot]);
 
         // Butterfly over the 4·TP sums (TP: TT rounded up to a power of two,
         // the padding sums zero): afterwards lane l holds value index
@@ -297,9 +321,32 @@ __global__ void __launch_bounds__(32 * kMultiWarps, 1) q4k_gemv_multi_kernel(Mul
             }
         }
         const bool writer = V >= 32 || (lane & (32 / V - 1)) == 0;
+        constexpr int NV = V >= 32 ? V / 32 : 1;  // values per writer lane
+        if constexpr (kSplit) {
+            static_assert(V <= 16, "a pair buffer holds 16 sums");
+            float *pb = pbuf + (lg & 1) * 16;
+            if (second) {
+                if (writer)
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) pb[idx + i] = v[i];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pbar[lg & 1]);
+                continue;
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&pbar[lg & 1], (lg >> 1) & 1, p.wait_limit, &abort_flag))) {
+                abort_flag = 1;
+                flag_timeout(p.status);
+                break;
+            }
+            if (writer)
+#pragma unroll
+                for (int i = 0; i < NV; ++i) v[i] += pb[idx + i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
         if (writer) {
 #pragma unroll
-            for (int i = 0; i < (V >= 32 ? V / 32 : 1); ++i) {
+            for (int i = 0; i < NV; ++i) {
                 const int id = idx + i;
                 const int r = id / TP, t = id % TP;
                 if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = v[i];
@@ -330,18 +377,20 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     const int grid = g.grid;
     const size_t smem = g.smem;
 
-#define Q4MM_MULTI_CASE(TT)                                                                           \
+#define Q4MM_MULTI_CASE(TT, SPLIT)                                                                    \
     {                                                                                                 \
-        auto kernel = g.x_staged ? q4k_gemv_multi_kernel<TT, true> : q4k_gemv_multi_kernel<TT, false>; \
+        auto kernel = g.x_staged ? q4k_gemv_multi_kernel<TT, true, SPLIT>                             \
+                                 : q4k_gemv_multi_kernel<TT, false, SPLIT>;                           \
         cudaError_t e = ensure_smem(kernel, smem);                                                    \
         if (e != cudaSuccess) return e;                                                               \
-        return launch_kernel(c, kernel, dim3(grid), dim3(32 * kMultiWarps), smem, p);                 \
+        return launch_kernel(c, kernel, dim3(grid), dim3(32 * (SPLIT ? kMultiSplitWarps : kMultiWarps)), \
+                             smem, p);                                                                \
     }
-    if (T <= 2) Q4MM_MULTI_CASE(2)
-    if (T <= 3) Q4MM_MULTI_CASE(3)
-    if (T <= 4) Q4MM_MULTI_CASE(4)
-    if (T <= 6) Q4MM_MULTI_CASE(6)
-    if (T <= 8) Q4MM_MULTI_CASE(8)
+    if (T <= 2) Q4MM_MULTI_CASE(2, true)
+    if (T <= 3) Q4MM_MULTI_CASE(3, true)
+    if (T <= 4) Q4MM_MULTI_CASE(4, true)
+    if (T <= 6) Q4MM_MULTI_CASE(6, false)
+    if (T <= 8) Q4MM_MULTI_CASE(8, false)
 #undef Q4MM_MULTI_CASE
     return cudaErrorInvalidValue;
 }
