@@ -52,8 +52,10 @@ def _q4k_case(K, N, T, seed):
     return synth.q4k_weights(g, N, K), synth.activations(g, T, K)
 
 
-@pytest.mark.parametrize("K,N,T", [(4096, 4096, 1), (4096, 11008, 1), (4096, 512, 6)],
-                         ids=["one_token_whole_ring", "one_token_reused_ring", "multi_token"])
+@pytest.mark.parametrize("K,N,T", [(4096, 4096, 1), (4096, 11008, 1), (4096, 512, 6), (4096, 4096, 4),
+                                   (11008, 4096, 3)],
+                         ids=["one_token_whole_ring", "one_token_reused_ring", "multi_token", "multi_token_pairs",
+                              "multi_token_pairs_wide_rows"])
 def test_q4k_wait_runs_out_then_next_call_is_right(K, N, T):
     import torch
     import quantized_matmul_q4_gb300 as q
