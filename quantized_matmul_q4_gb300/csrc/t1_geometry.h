@@ -17,7 +17,7 @@ namespace q4mm {
 struct T1Tuning {
     int warps = 16;
     int stage_bytes = 16384;           // weight bytes per ring stage, at least
-    int ring_bytes = 200 * 1024;       // shared-memory budget of a CTA
+    int ring_bytes = 231424;           // shared-memory budget of a CTA (all but 1 KB)
     int x_stage_max = 65536;           // bytes of x staged by one bulk copy (0: plain loads)
     int l2_evict_first = 1;            // weight copies with the L2 evict_first policy
     int spare_sms = 4;                 // SMs left without a CTA of a short launch
@@ -147,6 +147,18 @@ inline T1Geometry plan_gemv_t1_form(int group_bytes, int sums, int K, int N, int
         nslots = nslots < kT1MaxSlots ? nslots : kT1MaxSlots;
     };
     plan_ring(g.pass_rows);
+    if (nslots < nstages && nslots < 4 && g.x_staged) {
+        // Staged x can cost the ring its fourth pass-sized slot (16384-wide
+        // rows: 64 KB of x): the threads then load x themselves if that
+        // gives four (16384²: 4658 against 4567 GB/s with two stages of a
+        // pass of both row groups and x staged).
+        g.x_staged = 0;
+        plan_ring(g.pass_rows);
+        if (nslots < nstages && nslots < 4) {
+            g.x_staged = 1;
+            plan_ring(g.pass_rows);
+        }
+    }
     if (nslots < nstages && nslots < 4) {
         // A ring of fewer than 4 pass-sized slots leaves each row group one
         // stage in flight at a time, idle while its next stage streams in:

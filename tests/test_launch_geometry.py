@@ -106,14 +106,20 @@ def test_known_geometries(plan):
     g = plan(144, 4096, 4096, 1)
     assert (g["grid"], g["rows_per_cta"], g["rg"], g["stage_rows"], g["nslots"]) == (147, 28, 8, 8, 4)
     # 16384²: a long launch keeps every SM; two row groups of eight warps;
-    # 4-row stages would leave two slots, so a stage holds a pass of both
-    # groups (73.7 KB) and the other slot streams in meanwhile; x is loaded
-    # by the threads (staged, it would leave no room for two such stages).
+    # staged x (64 KB) would leave room for only two 4-row stages, so the
+    # threads load x themselves and four 4-row stages (36.9 KB) are in
+    # flight.
     g = plan(144, 16384, 16384, 1)
-    assert (g["grid"], g["rg"], g["stage_rows"], g["nslots"], g["x_staged"]) == (152, 2, 8, 2, 0)
-    # 8192²: x staged, seven 4-row stages of 18.4 KB in flight.
+    assert (g["grid"], g["rg"], g["stage_rows"], g["nslots"], g["x_staged"]) == (152, 2, 4, 4, 0)
+    # 14336²: the same trade (x would leave three slots).
+    g = plan(144, 14336, 14336, 1)
+    assert (g["stage_rows"], g["nslots"], g["x_staged"]) == (4, 5, 0)
+    # 12288²: x staged still leaves four 4-row slots, so it stays staged.
+    g = plan(144, 12288, 12288, 1)
+    assert (g["stage_rows"], g["nslots"], g["x_staged"]) == (4, 4, 1)
+    # 8192²: x staged, eight 4-row stages of 18.4 KB in flight.
     g = plan(144, 8192, 8192, 1)
-    assert (g["stage_rows"], g["nslots"], g["x_staged"]) == (4, 7, 1)
+    assert (g["stage_rows"], g["nslots"], g["x_staged"]) == (4, 8, 1)
     # 32768-wide rows take all 16 warps; odd-width Q6_K rows that wide fall
     # back to 2-row passes.
     g = plan(144, 32768, 1024, 1)
@@ -129,9 +135,10 @@ def test_streaming_launches_keep_stages_in_flight(plan):
     # A CTA whose rows all fit the ring holds them all; a streaming CTA keeps
     # at least four pass-sized stages in flight, or two stages of a pass of
     # every row group.
-    g = plan(144, 4096, 4096, 1)
-    assert g["nslots"] * g["stage_rows"] >= g["rows_per_cta"]
-    for K, N in ((4096, 11008), (8192, 8192), (11008, 4096), (16384, 16384)):
+    for K, N in ((4096, 4096), (4096, 11008)):
+        g = plan(144, K, N, 1)
+        assert g["nslots"] * g["stage_rows"] >= g["rows_per_cta"], (K, N, g)
+    for K, N in ((8192, 8192), (11008, 4096), (16384, 16384)):
         g = plan(144, K, N, 1)
         assert g["nslots"] * g["stage_rows"] < g["rows_per_cta"], (K, N, g)
         assert g["nslots"] >= 4 or g["stage_rows"] % (g["pass_rows"] * g["rg"]) == 0, (K, N, g)
