@@ -70,6 +70,7 @@ class Workload:
     sources: list             # kernel sources (under csrc/) hashed for the traffic record
     profile: str | None = None  # ncu summary with dram_bytes_per_launch, under profiles/
     distinct: int = 4         # distinct host-generated weights per matrix (the rest are copies)
+    kernels_per_call: int = 1  # kernel launches one C-ABI call makes
     arithmetic: str = ""
 
 
@@ -154,6 +155,11 @@ WORKLOADS = {w.name: w for w in [
              "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 layers x "
              "q,k,v,o,gate,up,down), 4 tokens", ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,
              arithmetic="fp32 dequantization and fp32 FMA"),
+    Workload("llama7b_decode_t16", "q4k", "q4k_matmul", LLAMA, 16, 32, "GB/s", "alu",
+             "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
+             "layers x q,k,v,o,gate,up,down), 16 tokens (two 8-token passes per matrix)",
+             ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1, arithmetic="fp32 dequantization and fp32 FMA",
+             kernels_per_call=2),
     Workload("llama7b_decode_t8", "q4k", "q4k_matmul", LLAMA, 8, 32, "GB/s", "alu",
              "q4k_gemv_multi_kernel", "Q4_K decode sweep weight-stream GB/s, Llama-2-7B shapes (32 "
              "layers x q,k,v,o,gate,up,down), 8 tokens", ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,
@@ -656,7 +662,7 @@ def run_ours(a) -> None:
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
                 "arithmetic": w.arithmetic, "data": "synthetic", "config": workload_config(w, plan),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": a.steps * len(plan.launches), "clocks": clocks,
+                "gpu_launches": a.steps * len(plan.launches) * w.kernels_per_call, "clocks": clocks,
                 "gpu": props.name}
         if w.unit == "GB/s":
             line["pct_of_hbm_peak"] = 100.0 * value / n_ranks / peaks["hbm_gbs"]

@@ -89,8 +89,9 @@ typedef enum {
  *         grid.  Where that kernel's geometry does not fit (2 tokens with a
  *         large inputDim), and from 3 tokens on: fp32 dequantization and fp32
  *         fused multiply-add.
- * Weights are streamed from HBM once per call for up to 64 tokens (tiles of
- * 64 tokens above that).
+ * Weights are streamed from HBM once per call for up to 8 tokens; above
+ * that once per 8 tokens (up to 32 tokens, or whenever outputDim is below
+ * about 6,500 rows) or once per 64 tokens (the FP32 tile kernel).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.
  */
 int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int outputDim,

@@ -198,7 +198,28 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
         if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
     } else {
-        e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
+        // More tokens: the 64-token FP32 tile kernel (clusters of 3 CTAs per
+        // 128 rows) computes a whole tile whatever the tokens, and with fewer
+        // CTAs than SMs (outputDim below about 6,500) leaves SMs idle.  Up to
+        // 32 tokens, or with that few CTAs, the register-tile kernel in
+        // chunks of 8 tokens is faster (measured on GB300: 4096x4096 at 16
+        // tokens 27 against 163 us, at 64 tokens 107 against 183 us;
+        // 4096 -> 11008 at 32 tokens 131 against 178 us, at 64 tokens 262
+        // against 198 us, where the tile kernel keeps 258 CTAs busy).
+        const long long tile_ctas = 3LL * ((outputDim + 127) / 128);
+        e = cudaErrorNotSupported;
+        if (tokens <= 32 || tile_ctas < ctx.num_sms) {
+            e = cudaSuccess;
+            for (int t0 = 0; t0 < tokens && e == cudaSuccess; t0 += 8) {
+                const int tt = tokens - t0 < 8 ? tokens - t0 : 8;
+                e = q4mm::launch_q4k_gemv_multi(ctx, x + (size_t)t0 * inputDim, W, y + (size_t)t0 * outputDim, inputDim,
+                                                outputDim, tt);
+                // A geometry the register-tile kernel cannot hold fails on
+                // the first chunk, before anything is launched.
+                if (e == cudaErrorNotSupported && t0 > 0) return fail_cuda(e, "q4k_matmul launch");
+            }
+        }
+        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
     }
     if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul launch");
     return Q4MM_OK;

@@ -102,6 +102,18 @@ def test_prefill_workload_sampled():
     _sampled(4096, 11008, 64, seed=0)
 
 
+@pytest.mark.parametrize("K,N,T", [(4096, 4096, 16), (11008, 4096, 24), (4096, 11008, 32), (4096, 4096, 70),
+                                   (4096, 11008, 40), (4096, 8192, 33)],
+                         ids=["chunks_4096_t16", "chunks_11008_t24", "chunks_11008rows_t32", "chunks_4096_t70",
+                              "tiles_11008rows_t40", "tiles_8192rows_t33"])
+def test_many_tokens_sampled(K, N, T):
+    # More than 8 tokens: 8-token chunks of the register-tile kernel (up to
+    # 32 tokens, or an output too narrow to fill the SMs with 64-token
+    # tiles; the last chunk ragged) and the 64-token FP32 tile kernel
+    # (ragged token tiles), sampled output rows.
+    _sampled(K, N, T, seed=K + N + T)
+
+
 @pytest.mark.parametrize("K,N", [(8192, 8192), (16384, 16384), (14336, 4096)])
 def test_large_one_token_sampled(K, N):
     # One-token GEMVs above 4096²: the 8192² and 16384² bench matrices and a
