@@ -92,8 +92,9 @@ def weight_bytes(kind, K, N):
     return N * (K // 4)
 
 
-T1_ARITH = ("fp32 activations rounded once to about 2^-22 of each 256-value block's maximum and split into three "
-            "byte planes; 4-bit codes x planes in int32 dp4a; scales, mins and combination in fp32")
+T1_ARITH = ("fp32 activations rounded once per 32-value group to a multiple of 2^-23 of the power of two above "
+            "the group's maximum / 255 and split into four byte planes; 4-bit codes x planes in int32 dp4a; scales, "
+            "mins and combination in fp32")
 LLAMA = [(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
 WORKLOADS = {w.name: w for w in [
     Workload("q4k_gemv_4096x4096_t1", "q4k", "q4k_matmul", [(4096, 4096)], 1, 64, "GB/s", "hbm",
@@ -142,9 +143,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("ternary_gemv_2560x6912_t1", "ternary", "ternary_gemv", [(2560, 6912)], 1, 64, "GB/s",
              "hbm", "gemv_t1_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "batch 1", ["ternary_gemv.cu", "q4k_gemv.cu", "t1_geometry.h"], "ternary_t1_2560x6912.md",
-             arithmetic="fp32 activations rounded once to about 2^-22 of each 256-value block's maximum and split "
-                        "into three byte planes; 2-bit fields x planes in int32 dp4a; fp32 combination, scale "
-                        "applied once"),
+             arithmetic="fp32 activations rounded once per 32-value group to a multiple of 2^-23 of the power of "
+                        "two above the group's maximum / 255 and split into four byte planes; 2-bit fields x planes "
+                        "in int32 dp4a; fp32 combination, scale applied once"),
     Workload("ternary_gemv_2560x6912_t16", "ternary", "ternary_gemv", [(2560, 6912)], 16, 64, "GB/s",
              "alu", "ternary_tile_kernel", "BitNet b1.58 ternary GEMV weight-stream GB/s at 2560->6912, "
              "16 tokens", ["ternary_gemv.cu"], "ternary_tile_2560x6912_t16.md", arithmetic="fp32"),
