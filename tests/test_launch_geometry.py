@@ -187,6 +187,64 @@ def test_multi_token_ring_slots_have_one_consumer(multi):
     assert checked > 1000
 
 
+def _pair_order_safe(groups, L):
+    """The pair protocol's happens-before order for one pair's groups
+    0..groups-1, L = the pair's groups between two uses of one ring slot.
+    Events: S2(k) the second warp starts group k, W2(k) it writes buffer
+    k mod 2 and arrives on that buffer's barrier, R1(k) the first warp reads
+    it, E1(k) / E2(k) the warps release the slot (E2 before W2, E1 after
+    R1).  S2(k) needs the slot refilled: E1(k - L) and E2(k - L).  True if
+    every W2(k) comes after R1(k - 2) (the buffer and barrier are free)."""
+    import functools
+
+    @functools.lru_cache(maxsize=None)
+    def before(a, b):  # is event a ordered before event b?
+        if a == b:
+            return True
+        kind, k = b
+        preds = []
+        if kind == "S2" and k >= L:
+            preds += [("E1", k - L), ("E2", k - L)]
+        if kind in ("S2",) and k >= 1:
+            preds.append(("W2", k - 1))  # the second warp's program order
+        if kind == "E2":
+            preds.append(("S2", k))
+        if kind == "W2":
+            preds.append(("E2", k))
+        if kind == "R1":
+            preds.append(("W2", k))
+            if k >= 1:
+                preds.append(("E1", k - 1))  # the first warp's program order
+        if kind == "E1":
+            preds.append(("R1", k))
+        return any(before(a, p) for p in preds)
+
+    return all(before(("R1", k - 2), ("W2", k)) for k in range(2, groups))
+
+
+def test_multi_token_pairs_reuse_buffers_in_order(multi):
+    # Up to 4 tokens a pair of warps takes each group (the first over half of
+    # the blocks, the second over the rest), the second handing its sums to
+    # the first through one of two buffers chosen by the group's parity, and
+    # the first releasing the ring slot only after reading them.  That keeps
+    # the second at most one group ahead only while a slot comes back to the
+    # pair every one or two of its groups (nslots <= 2 pairs): checked for
+    # every geometry, with the order derived from the barriers.
+    assert _pair_order_safe(8, 1) and _pair_order_safe(8, 2) and not _pair_order_safe(8, 3)
+    checked = 0
+    for T in (1, 2, 3, 4):
+        for K in range(256, 32768 + 1, 512):
+            for N in (1, 5, 100, 4096, 11008, 32000):
+                g = multi(K, N, 200 * 1024, T)
+                if not g["ok"]:
+                    continue
+                checked += 1
+                n, c = g["nslots"], g["consumers"]
+                groups = -(-(g["rows_per_cta"] // 4) // c)  # a pair's groups, at most
+                assert n % c == 0 and _pair_order_safe(groups, n // c), (K, N, T, n, c)
+    assert checked > 500
+
+
 def test_multi_token_known_geometries(multi):
     # 14336-wide rows: six 32 KB slots fit, so six consumer warps, one each.
     g = multi(14336, 4096)
