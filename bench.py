@@ -137,6 +137,10 @@ WORKLOADS = {w.name: w for w in [
              "gemv_t1_kernel", "Q4_K fused gate+up SwiGLU weight-stream GB/s, Llama-2-7B FFN (32 layers x "
              "4096 -> 2 x 11008), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], "q4k_ffn_swiglu_llama7b_t1.md", distinct=1,
              arithmetic=T1_ARITH + "; h = silu(g)*u in fp32"),
+    Workload("llama7b_ffn_swiglu_t8", "q4k_ffn", "q4k_ffn_swiglu", [(4096, 11008)], 8, 32, "GB/s", "alu",
+             "q4k_gemv_multi_kernel", "Q4_K fused gate+up SwiGLU weight-stream GB/s, Llama-2-7B FFN (32 layers x "
+             "4096 -> 2 x 11008), 8 tokens", ["q4k_gemv_multi.cu", "multi_geometry.h"], distinct=1,
+             arithmetic="fp32 dequantization and fp32 FMA; h = silu(g)*u in fp32"),
     Workload("llama7b_gate_up_t1", "q4k", "q4k_matmul", [(4096, 11008)] * 2, 1, 32, "GB/s", "hbm",
              "gemv_t1_kernel", "Q4_K gate and up projections as two GEMVs, weight-stream GB/s, Llama-2-7B "
              "FFN (32 layers x 2 x 4096 -> 11008), batch 1", ["q4k_gemv.cu", "t1_geometry.h"], distinct=1, arithmetic=T1_ARITH),

@@ -190,20 +190,22 @@ int q6k_gemv(const float *x, const void *w_q6k, float *y, int inputDim, int outp
 /*
  * q4k_ffn_swiglu — the input side of a Llama feed-forward block in one call:
  *   h = silu(x·W_gateᵀ) ⊙ (x·W_upᵀ),  silu(z) = z / (1 + e^(−z)),
- * both weights Q4_K (layout, values and precision as q4k_matmul's one-token
- * path).  The pages name this fused operation only as the llama.cpp
- * benchmark "ffn_swiglu" (PR #37 "ggml-cpu: cache-aware tiling in
- * ggml_compute_forward_mul_mat", section "Measured impact"); the formula is
- * the standard Llama FFN.  One launch per token reads x once for both
- * weights and writes only h.
+ * both weights Q4_K (layout, values and precision as q4k_matmul's: the
+ * byte-plane path for 1-2 tokens, fp32 FMA from 3 tokens on).  The pages
+ * name this fused operation only as the llama.cpp benchmark "ffn_swiglu"
+ * (PR #37 "ggml-cpu: cache-aware tiling in ggml_compute_forward_mul_mat",
+ * section "Measured impact"); the formula is the standard Llama FFN.  For
+ * 1-2 tokens one launch per token, from 3 tokens on one launch per 8 tokens,
+ * each reading x once for both weights and writing only h.
  *
  * w_gate, w_up : hiddenDim rows of inputDim/256 Q4_K blocks each, 16-byte
  *                aligned; they may be the same buffer.  x: 16-byte aligned.
  *                h: [tokens][hiddenDim], 4-byte aligned, overwritten; h must
  *                not overlap x or either weight.
  * Limits: inputDim a positive multiple of 256 and <= Q4MM_FFN_MAX_INPUT_DIM;
- *         hiddenDim >= 1; tokens >= 1 (each token one pass over both weights).
- * Precision: g and u each within the one-token path's bound; h = silu(g)·u
+ *         hiddenDim >= 1; tokens >= 1 (one pass over both weights per token
+ *         up to 2 tokens, per 8 tokens above).
+ * Precision: g and u each within q4k_matmul's bound; h = silu(g)·u
  *         in fp32 (expf), so max_o |h − h_exact| <= 1e-4 · max_o |u| ·
  *         (1.1 · max_o |g| + max_o |silu(g)|) per token (1.1 bounds |silu'|).
  * Returns Q4MM_OK or Q4MM_ERR_{DIM,NULL,ALIGN,ALIAS,CUDA}.

@@ -340,6 +340,20 @@ int q4k_ffn_swiglu(const float *x, const void *w_gate, const void *w_up, float *
     q4mm::LaunchCtx ctx;
     if ((rc = device_ctx(stream, &ctx))) return rc;
     const uint8_t *Wg = static_cast<const uint8_t *>(w_gate), *Wu = static_cast<const uint8_t *>(w_up);
+    // From 3 tokens on: the FP32 register-tile kernel over both weights, up
+    // to 8 tokens per pass; 1-2 tokens (or a geometry it cannot hold): the
+    // one-token kernel, one launch per token.
+    if (tokens >= 3) {
+        cudaError_t e = cudaSuccess;
+        for (int t0 = 0; t0 < tokens && e == cudaSuccess; t0 += 8) {
+            const int tt = tokens - t0 < 8 ? tokens - t0 : 8;
+            e = q4mm::launch_q4k_ffn_swiglu_multi(ctx, x + (size_t)t0 * inputDim, Wg, Wu, h + (size_t)t0 * hiddenDim,
+                                                  inputDim, hiddenDim, tt);
+            if (e == cudaErrorNotSupported && t0 == 0) break;  // nothing launched yet
+        }
+        if (e == cudaSuccess) return Q4MM_OK;
+        if (e != cudaErrorNotSupported) return fail_cuda(e, "q4k_ffn_swiglu launch");
+    }
     for (int t = 0; t < tokens; ++t) {
         const cudaError_t e = q4mm::launch_q4k_ffn_swiglu_t1(ctx, x + (size_t)t * inputDim, Wg, Wu,
                                                              h + (size_t)t * hiddenDim, inputDim, hiddenDim);

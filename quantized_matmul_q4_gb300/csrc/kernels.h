@@ -47,6 +47,10 @@ cudaError_t launch_q4k_ffn_swiglu_t1(const LaunchCtx &c, const float *x, const u
 // Q4_K decode GEMV for 1..8 tokens with x staged in shared memory.
 cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
                                   int K, int N, int T);
+// The fused gate+up SwiGLU (h = silu(x·Wgᵀ) ⊙ (x·Wuᵀ)) for up to 8 tokens on
+// the same kernel: one pass over both weights for all tokens.
+cudaError_t launch_q4k_ffn_swiglu_multi(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,
+                                        float *h, int K, int N, int T);
 
 // Q4_K prefill, FP32 FMA (any token count, tiles of 64 tokens).
 cudaError_t launch_q4k_mm_fp32(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,

@@ -19,9 +19,9 @@ constexpr int kMultiTabBlocks = 16;          // blocks per scale-table chunk
 // that many blocks: the same bytes for twice the warps.)
 constexpr size_t kMultiTabBytes = (size_t)kMultiRows * kMultiTabBlocks * 8 * 2 * sizeof(float);
 constexpr int kMultiSplitWarps = 1 + 2 * kMultiCw;  // copy warp + a pair per consumer (up to 4 tokens)
-// The pairs' exchange of partial sums: per pair two buffers of 16 floats and
-// two barriers, padded to 1 KB.
-constexpr size_t kMultiPairBytes = 1024;
+// The pairs' exchange of partial sums: per pair two buffers of 32 floats
+// (16 sums of each of up to two weights) and two barriers, padded to 2 KB.
+constexpr size_t kMultiPairBytes = 2048;
 
 struct MultiGeometry {
     int ok = 0;            // 0: the ring does not fit shared memory
@@ -38,11 +38,13 @@ struct MultiGeometry {
 // ring_bytes: byte budget of the ring (the library passes kMultiRingBytes; the
 // CPU tests also check smaller budgets).  T: tokens (x is staged in shared
 // memory when its T·K fp32 values fit beside a ring of one slot per
-// consumer warp; T = 0 never stages).
-inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes, int T = 0) {
+// consumer warp; T = 0 never stages).  vrow_mult: 2 for the fused gate+up
+// (a slot holds the group's rows of both weights).
+inline MultiGeometry plan_gemv_multi(int K, int N, int num_sms, int max_smem_optin, int ring_bytes, int T = 0,
+                                     int vrow_mult = 1) {
     MultiGeometry g;
     const size_t row_bytes = (size_t)(K / 256) * 144;
-    const size_t slot_bytes = kMultiRows * row_bytes;
+    const size_t slot_bytes = (size_t)vrow_mult * kMultiRows * row_bytes;  // a group's rows of each weight
     const int groups = (N + kMultiRows - 1) / kMultiRows;
     const int grid = num_sms < groups ? num_sms : groups;
     g.rows_per_cta = kMultiRows * ((groups + grid - 1) / grid);

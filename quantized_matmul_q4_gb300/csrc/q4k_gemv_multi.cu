@@ -77,6 +77,7 @@ __device__ __forceinline__ SlabScales slab_scales(uint4 hdr, int j) {
 struct MultiParams {
     const float *x;
     const uint8_t *W;
+    const uint8_t *W2;  // kSwiGLU: the up weight (W is the gate weight)
     float *y;
     int *status;
     int K, N, T;       // T: tokens of this launch (<= TT)
@@ -97,17 +98,23 @@ struct MultiParams {
 // adds them (first + second, so the result does not depend on timing) and
 // stores the rows.  Twice the warps hide more of each warp's latencies.
 
-template <int TT, bool kXs, bool kSplit>
+// kSwiGLU: the fused Llama FFN input side, y = silu(x·Wᵀ) ⊙ (x·W2ᵀ): a
+// ring slot holds a group's four gate rows and then the same four rows of
+// the up weight; a warp takes the gate part and then the up part of its
+// group and combines the two sums of each row.
+
+template <int TT, bool kXs, bool kSplit, bool kSwiGLU>
 __global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps), 1)
     q4k_gemv_multi_kernel(MultiParams p) {
+    constexpr int kParts = kSwiGLU ? 2 : 1;
     extern __shared__ __align__(128) uint8_t msmem[];
     __shared__ volatile int abort_flag;  // set by the first warp whose wait runs out
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t row_bytes = (uint32_t)p.nb * kQ4kBytes;
-    const uint32_t slot_bytes = kMultiRows * row_bytes;
+    const uint32_t slot_bytes = kParts * kMultiRows * row_bytes;
     float4 *tabs = reinterpret_cast<float4 *>(msmem);  // the compute warps' tables
-    float *pair_buf = reinterpret_cast<float *>(msmem + kMultiCw * kMultiTabBytes);  // [pair][2][16]
-    uint64_t *pair_bar = reinterpret_cast<uint64_t *>(pair_buf + kMultiCw * 2 * 16);  // [pair][2]
+    float *pair_buf = reinterpret_cast<float *>(msmem + kMultiCw * kMultiTabBytes);  // [pair][2][32]
+    uint64_t *pair_bar = reinterpret_cast<uint64_t *>(pair_buf + kMultiCw * 2 * 32);  // [pair][2]
     uint8_t *ring = msmem + kMultiCw * kMultiTabBytes + kMultiPairBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.nslots * slot_bytes);
     uint64_t *empty = full + p.nslots;
@@ -136,9 +143,11 @@ __global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps)
         // out; nothing then writes into its slot.)
         auto issue = [&](int g, int slot) {
             const uint32_t bytes = (uint32_t)min(kMultiRows, nrows - g * kMultiRows) * row_bytes;
-            mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_g2s(ring + (size_t)slot * slot_bytes, p.W + (size_t)(row0 + g * kMultiRows) * row_bytes, bytes,
-                     &full[slot]);
+            const size_t off = (size_t)(row0 + g * kMultiRows) * row_bytes;
+            uint8_t *dst = ring + (size_t)slot * slot_bytes;
+            mbar_arrive_expect_tx(&full[slot], kParts * bytes);
+            bulk_g2s(dst, p.W + off, bytes, &full[slot]);
+            if (kSwiGLU) bulk_g2s(dst + kMultiRows * row_bytes, p.W2 + off, bytes, &full[slot]);
         };
         // Staged x first (the previous kernel on the stream may write it),
         // then the ring's first groups, one lane each: a bulk copy holds its
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps)
     constexpr int kTB = kSplit ? kMultiTabBlocks / 2 : kMultiTabBlocks;  // blocks per table chunk
     constexpr int kTabEntries = kMultiRows * kTB * 4;
     float4 *tab = tabs + (size_t)cw * kTabEntries;
-    float *pbuf = pair_buf + unit * 2 * 16;
+    float *pbuf = pair_buf + unit * 2 * 32;
     uint64_t *pbar = pair_bar + unit * 2;
     int lg = 0;  // this pair's (warp's) group count so far
     for (int g = unit; g < ngroups; g += ncons, ++lg) {
@@ -219,116 +228,127 @@ __global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps)
         }
         const uint8_t *grp = ring + (size_t)slot * slot_bytes;
         const int rows = min(kMultiRows, nrows - g * kMultiRows);
-        float2 acc[kMultiRows][TT];
+        constexpr int TP = TT <= 2 ? 2 : TT <= 4 ? 4 : 8;
+        constexpr int V = kMultiRows * TP;
+        static_assert(V <= 32, "one value per writer lane");
+        float res0 = 0.f, res1 = 0.f;  // this lane's row sum of the gate (or only) part and of the up part
+        int idx = 0;                   // the value index it belongs to
+#pragma unroll 1
+        for (int part = 0; part < kParts; ++part) {
+            const uint8_t *base = grp + (size_t)part * kMultiRows * row_bytes;
+            float2 acc[kMultiRows][TT];
 #pragma unroll
-        for (int r = 0; r < kMultiRows; ++r)
+            for (int r = 0; r < kMultiRows; ++r)
 #pragma unroll
-            for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
+                for (int t = 0; t < TT; ++t) acc[r][t] = make_float2(0.f, 0.f);
 
-        for (int b0 = kb0; b0 < kb1; b0 += kTB) {
-            const int nbc = min(kTB, kb1 - b0);
-            // Entry e = (r·kTB + bb)·4 + slab; every lane keeps its
-            // slab (e mod 4 = lane mod 4), so the table fill is branch-free.
-            __syncwarp();  // the previous chunk's reads are done
+            for (int b0 = kb0; b0 < kb1; b0 += kTB) {
+                const int nbc = min(kTB, kb1 - b0);
+                // Entry e = (r·kTB + bb)·4 + slab; every lane keeps its
+                // slab (e mod 4 = lane mod 4), so the table fill is branch-free.
+                __syncwarp();  // the previous chunk's reads are done
 #pragma unroll
-            for (int i = 0; i < kTabEntries / 32; ++i) {
-                const int e = lane + 32 * i;
-                const int bb = (e >> 2) % kTB, r = e / (4 * kTB);
-                if (bb < nbc) {
-                    const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)(b0 + bb) * kQ4kBytes;
-                    const SlabScales sc = slab_scales(*reinterpret_cast<const uint4 *>(blk), e & 3);
-                    tab[e] = make_float4(sc.s0, sc.o0, sc.s1, sc.o1);
-                }
-            }
-            __syncwarp();
-            for (int bb = 0; bb < nbc; ++bb) {
-                const int b = b0 + bb;
-                // Activations of this lane's 8 positions for every token.
-                float4 xl[TT], xh[TT];
-                const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
-#pragma unroll
-                for (int t = 0; t < TT; ++t) {
-                    if (t < p.T) {
-                        const float *xt = xsrc + (size_t)t * p.K + k0;
-                        if constexpr (kXs) {
-                            xl[t] = *reinterpret_cast<const float4 *>(xt);
-                            xh[t] = *reinterpret_cast<const float4 *>(xt + 32);
-                        } else {
-                            xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
-                            xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
-                        }
-                    } else {
-                        xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        xh[t] = xl[t];
+                for (int i = 0; i < kTabEntries / 32; ++i) {
+                    const int e = lane + 32 * i;
+                    const int bb = (e >> 2) % kTB, r = e / (4 * kTB);
+                    if (bb < nbc) {
+                        const uint8_t *blk = base + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)(b0 + bb) * kQ4kBytes;
+                        const SlabScales sc = slab_scales(*reinterpret_cast<const uint4 *>(blk), e & 3);
+                        tab[e] = make_float4(sc.s0, sc.o0, sc.s1, sc.o1);
                     }
                 }
-#pragma unroll
-                for (int r = 0; r < kMultiRows; ++r) {
-                    // Absent rows of a short last group read row 0 of the slot;
-                    // their sums are never stored.
-                    const uint8_t *blk = grp + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
-                    const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
-                    const float4 sc = tab[(r * kTB + bb) * 4 + j];  // (s0, o0, s1, o1)
-                    const uint32_t l4 = q & 0x0F0F0F0Fu;
-                    const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
-                    const float2 s0 = make_float2(sc.x, sc.x), n0 = make_float2(-sc.y, -sc.y);
-                    const float2 s1 = make_float2(sc.z, sc.z), n1 = make_float2(-sc.w, -sc.w);
-                    const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
-                    const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
-                    const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
-                    const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+                __syncwarp();
+                for (int bb = 0; bb < nbc; ++bb) {
+                    const int b = b0 + bb;
+                    // Activations of this lane's 8 positions for every token.
+                    float4 xl[TT], xh[TT];
+                    const int k0 = b * kQ4kValues + 64 * j + 4 * wq;
 #pragma unroll
                     for (int t = 0; t < TT; ++t) {
-                        acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
-                        acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
-                        acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
-                        acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                        if (t < p.T) {
+                            const float *xt = xsrc + (size_t)t * p.K + k0;
+                            if constexpr (kXs) {
+                                xl[t] = *reinterpret_cast<const float4 *>(xt);
+                                xh[t] = *reinterpret_cast<const float4 *>(xt + 32);
+                            } else {
+                                xl[t] = __ldg(reinterpret_cast<const float4 *>(xt));
+                                xh[t] = __ldg(reinterpret_cast<const float4 *>(xt + 32));
+                            }
+                        } else {
+                            xl[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            xh[t] = xl[t];
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kMultiRows; ++r) {
+                        // Absent rows of a short last group read row 0 of the slot;
+                        // their sums are never stored.
+                        const uint8_t *blk = base + (size_t)(r < rows ? r : 0) * row_bytes + (size_t)b * kQ4kBytes;
+                        const uint32_t q = *reinterpret_cast<const uint32_t *>(blk + 16 + 32 * j + 4 * wq);
+                        const float4 sc = tab[(r * kTB + bb) * 4 + j];  // (s0, o0, s1, o1)
+                        const uint32_t l4 = q & 0x0F0F0F0Fu;
+                        const uint32_t h4 = (q >> 4) & 0x0F0F0F0Fu;
+                        const float2 s0 = make_float2(sc.x, sc.x), n0 = make_float2(-sc.y, -sc.y);
+                        const float2 s1 = make_float2(sc.z, sc.z), n1 = make_float2(-sc.w, -sc.w);
+                        const float2 wl01 = ffma2(make_float2(nib_biased<0>(l4), nib_biased<1>(l4)), s0, n0);
+                        const float2 wl23 = ffma2(make_float2(nib_biased<2>(l4), nib_biased<3>(l4)), s0, n0);
+                        const float2 wh01 = ffma2(make_float2(nib_biased<0>(h4), nib_biased<1>(h4)), s1, n1);
+                        const float2 wh23 = ffma2(make_float2(nib_biased<2>(h4), nib_biased<3>(h4)), s1, n1);
+#pragma unroll
+                        for (int t = 0; t < TT; ++t) {
+                            acc[r][t] = ffma2(make_float2(xl[t].x, xl[t].y), wl01, acc[r][t]);
+                            acc[r][t] = ffma2(make_float2(xl[t].z, xl[t].w), wl23, acc[r][t]);
+                            acc[r][t] = ffma2(make_float2(xh[t].x, xh[t].y), wh01, acc[r][t]);
+                            acc[r][t] = ffma2(make_float2(xh[t].z, xh[t].w), wh23, acc[r][t]);
+                        }
                     }
                 }
             }
+            // Butterfly over the 4·TP sums (TP: TT rounded up to a power of two,
+            // the padding sums zero): afterwards lane l holds value index
+            // idx .. idx + n − 1 (see the halving below), summed over the warp.
+            float v[V];
+#pragma unroll
+            for (int r = 0; r < kMultiRows; ++r)
+#pragma unroll
+                for (int t = 0; t < TP; ++t) v[r * TP + t] = t < TT ? acc[r][t].x + acc[r][t].y : 0.f;
+            idx = 0;
+            int n = V;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                if (n > 1) {
+                    const int half = n >> 1;
+                    const bool up = lane & o;
+#pragma unroll
+                    for (int i = 0; i < V / 2; ++i) {
+                        if (i < half) {
+                            const float send = up ? v[i] : v[i + half];
+                            const float keep = up ? v[i + half] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                    }
+                    if (up) idx += half;
+                    n = half;
+                } else {
+                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+                }
+            }
+            if (part == 0)
+                res0 = v[0];
+            else
+                res1 = v[0];
         }
         __syncwarp();
         if (lane == 0 && (!kSplit || second)) mbar_arrive(&empty[slot]);
-
-        // Butterfly over the 4·TP sums (TP: TT rounded up to a power of two,
-        // the padding sums zero): afterwards lane l holds value index
-        // idx .. idx + n − 1 (see the halving below), summed over the warp.
-        constexpr int TP = TT <= 2 ? 2 : TT <= 4 ? 4 : 8;
-        constexpr int V = kMultiRows * TP;
-        float v[V];
-#pragma unroll
-        for (int r = 0; r < kMultiRows; ++r)
-#pragma unroll
-            for (int t = 0; t < TP; ++t) v[r * TP + t] = t < TT ? acc[r][t].x + acc[r][t].y : 0.f;
-        int idx = 0, n = V;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            if (n > 1) {
-                const int half = n >> 1;
-                const bool up = lane & o;
-#pragma unroll
-                for (int i = 0; i < V / 2; ++i) {
-                    if (i < half) {
-                        const float send = up ? v[i] : v[i + half];
-                        const float keep = up ? v[i + half] : v[i];
-                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
-                }
-                if (up) idx += half;
-                n = half;
-            } else {
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-            }
-        }
         const bool writer = V >= 32 || (lane & (32 / V - 1)) == 0;
-        constexpr int NV = V >= 32 ? V / 32 : 1;  // values per writer lane
         if constexpr (kSplit) {
-            static_assert(V <= 16, "a pair buffer holds 16 sums");
-            float *pb = pbuf + (lg & 1) * 16;
+            static_assert(V <= 16, "a pair buffer part holds 16 sums");
+            float *pb = pbuf + (lg & 1) * 32;
             if (second) {
-                if (writer)
-#pragma unroll
-                    for (int i = 0; i < NV; ++i) pb[idx + i] = v[i];
+                if (writer) {
+                    pb[idx] = res0;
+                    if (kSwiGLU) pb[16 + idx] = res1;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pbar[lg & 1]);
                 continue;
@@ -338,30 +358,33 @@ __global__ void __launch_bounds__(32 * (kSplit ? kMultiSplitWarps : kMultiWarps)
                 flag_timeout(p.status);
                 break;
             }
-            if (writer)
-#pragma unroll
-                for (int i = 0; i < NV; ++i) v[i] += pb[idx + i];
+            if (writer) {
+                res0 += pb[idx];
+                if (kSwiGLU) res1 += pb[16 + idx];
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
         if (writer) {
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int id = idx + i;
-                const int r = id / TP, t = id % TP;
-                if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = v[i];
-            }
+            const int r = idx / TP, t = idx % TP;
+            float out = res0;
+            if constexpr (kSwiGLU) out = out / (1.0f + expf(-out)) * res1;  // silu(g)·u
+            if (r < rows && t < p.T) p.y[(size_t)t * p.N + row0 + g * kMultiRows + r] = out;
         }
     }
 }
 
 }  // namespace
 
-cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
-                                  int K, int N, int T) {
+namespace {
+
+template <bool kSwiGLU>
+cudaError_t launch_multi(const LaunchCtx &c, const float *x, const uint8_t *W, const uint8_t *W2, float *y, int K,
+                         int N, int T) {
     MultiParams p;
     p.x = x;
     p.W = W;
+    p.W2 = W2;
     p.y = y;
     p.status = c.status;
     p.K = K;
@@ -370,7 +393,8 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
     p.nb = K / kQ4kValues;
     p.wait_limit = c.wait_limit;
     p.withhold = c.withhold;
-    const MultiGeometry g = plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes, T);
+    const MultiGeometry g =
+        plan_gemv_multi(K, N, c.num_sms, c.max_smem_optin, kMultiRingBytes, T, kSwiGLU ? 2 : 1);
     if (!g.ok) return cudaErrorNotSupported;
     p.rows_per_cta = g.rows_per_cta;
     p.nslots = g.nslots;
@@ -379,20 +403,37 @@ cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint
 
 #define Q4MM_MULTI_CASE(TT, SPLIT)                                                                    \
     {                                                                                                 \
-        auto kernel = g.x_staged ? q4k_gemv_multi_kernel<TT, true, SPLIT>                             \
-                                 : q4k_gemv_multi_kernel<TT, false, SPLIT>;                           \
+        auto kernel = g.x_staged ? q4k_gemv_multi_kernel<TT, true, SPLIT, kSwiGLU>                    \
+                                 : q4k_gemv_multi_kernel<TT, false, SPLIT, kSwiGLU>;                  \
         cudaError_t e = ensure_smem(kernel, smem);                                                    \
         if (e != cudaSuccess) return e;                                                               \
         return launch_kernel(c, kernel, dim3(grid), dim3(32 * (SPLIT ? kMultiSplitWarps : kMultiWarps)), \
                              smem, p);                                                                \
     }
-    if (T <= 2) Q4MM_MULTI_CASE(2, true)
-    if (T <= 3) Q4MM_MULTI_CASE(3, true)
-    if (T <= 4) Q4MM_MULTI_CASE(4, true)
-    if (T <= 6) Q4MM_MULTI_CASE(6, false)
-    if (T <= 8) Q4MM_MULTI_CASE(8, false)
+    if constexpr (!kSwiGLU) {
+        if (T <= 2) Q4MM_MULTI_CASE(2, true)
+        if (T <= 3) Q4MM_MULTI_CASE(3, true)
+        if (T <= 4) Q4MM_MULTI_CASE(4, true)
+        if (T <= 6) Q4MM_MULTI_CASE(6, false)
+        if (T <= 8) Q4MM_MULTI_CASE(8, false)
+    } else {
+        if (T <= 4) Q4MM_MULTI_CASE(4, true)
+        if (T <= 8) Q4MM_MULTI_CASE(8, false)
+    }
 #undef Q4MM_MULTI_CASE
     return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_q4k_gemv_multi(const LaunchCtx &c, const float *x, const uint8_t *W, float *y,
+                                  int K, int N, int T) {
+    return launch_multi<false>(c, x, W, nullptr, y, K, N, T);
+}
+
+cudaError_t launch_q4k_ffn_swiglu_multi(const LaunchCtx &c, const float *x, const uint8_t *Wg, const uint8_t *Wu,
+                                        float *h, int K, int N, int T) {
+    return launch_multi<true>(c, x, Wg, Wu, h, K, N, T);
 }
 
 }  // namespace q4mm

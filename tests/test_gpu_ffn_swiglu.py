@@ -38,7 +38,7 @@ def check(h, x, Wg, Wu, K, N, what):
     g, u, ref = oracle.q4k_ffn_swiglu(x, Wg, Wu, K, N)
     assert np.all(np.isfinite(h)), what
     for t in range(ref.shape[0]):
-        silu = g[t] / (1.0 + np.exp(-g[t]))
+        silu = 0.5 * g[t] * (1.0 + np.tanh(0.5 * g[t]))  # g·sigmoid(g), no overflow
         bound = 1e-4 * np.abs(u[t]).max() * (1.1 * np.abs(g[t]).max() + np.abs(silu).max())
         bound += 1e-6 * np.abs(ref[t]).max()
         err = np.abs(h[t].astype(np.float64) - ref[t]).max()
@@ -62,9 +62,16 @@ def test_shapes(K, N):
     check(ffn(x, Wg, Wu, K, N), x, Wg, Wu, K, N, f"K{K} N{N}")
 
 
-def test_several_tokens():
-    x, Wg, Wu = case(1024, 513, 3, seed=9)
-    check(ffn(x, Wg, Wu, 1024, 513), x, Wg, Wu, 1024, 513, "T3")
+TOKENS = [(1024, 513, 2), (1024, 513, 3), (256, 37, 6), (1024, 300, 5), (4096, 11008, 4), (4096, 11008, 8),
+          (4096, 1000, 12), (11008, 4096, 7)]
+
+
+@pytest.mark.parametrize("K,N,T", TOKENS, ids=[f"K{k}_N{n}_T{t}" for k, n, t in TOKENS])
+def test_several_tokens(K, N, T):
+    # 2 tokens: one-token launches; 3 and more: the register-tile kernel over
+    # both weights, 8 tokens per pass (pairs over K up to 4 tokens).
+    x, Wg, Wu = case(K, N, T, seed=9 + K + N + T)
+    check(ffn(x, Wg, Wu, K, N), x, Wg, Wu, K, N, f"K{K} N{N} T{T}")
 
 
 def test_same_buffer_for_gate_and_up():
