@@ -18,8 +18,9 @@ extern "C" int t1_plan(int group_bytes, int sums, int K, int N, int T, int vrow_
     return g.ok;
 }
 
-extern "C" int multi_plan(int K, int N, int num_sms, int max_smem, int ring_bytes, int T, long long *out) {
-    const q4mm::MultiGeometry g = q4mm::plan_gemv_multi(K, N, num_sms, max_smem, ring_bytes, T);
+extern "C" int multi_plan(int K, int N, int num_sms, int max_smem, int ring_bytes, int T, int vrow_mult,
+                          long long *out) {
+    const q4mm::MultiGeometry g = q4mm::plan_gemv_multi(K, N, num_sms, max_smem, ring_bytes, T, vrow_mult);
     const long long v[] = {g.ok, g.grid, g.rows_per_cta, g.nslots, g.consumers, (long long)g.smem, g.x_staged};
     for (int i = 0; i < (int)(sizeof(v) / sizeof(v[0])); ++i) out[i] = v[i];
     return g.ok;

@@ -32,7 +32,7 @@ def _shim(tmp_path_factory):
                         os.path.join(HERE, "launch_geometry_shim.cpp")], check=True)
         lib = ctypes.CDLL(out)
         lib.t1_plan.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
-        lib.multi_plan.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_longlong)]
+        lib.multi_plan.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong)]
         _LIB.append(lib)
     return _LIB[0]
 
@@ -151,9 +151,9 @@ MULTI = ["ok", "grid", "rows_per_cta", "nslots", "consumers", "smem", "x_staged"
 def multi(tmp_path_factory):
     lib = _shim(tmp_path_factory)
 
-    def call(K, N, ring_bytes=200 * 1024, T=0):
+    def call(K, N, ring_bytes=200 * 1024, T=0, vrow_mult=1):
         buf = (ctypes.c_longlong * len(MULTI))()
-        lib.multi_plan(K, N, SMS, SMEM, ring_bytes, T, buf)
+        lib.multi_plan(K, N, SMS, SMEM, ring_bytes, T, vrow_mult, buf)
         return dict(zip(MULTI, buf))
     return call
 
@@ -164,10 +164,10 @@ def test_multi_token_ring_slots_have_one_consumer(multi):
     # exactly one ring lap later, so it has consumed the slot's previous
     # group itself before it waits on the next.
     checked = 0
-    for ring in (200 * 1024, 128 * 1024, 64 * 1024, 8192):
+    for ring, vm in ((200 * 1024, 1), (128 * 1024, 1), (64 * 1024, 1), (8192, 1), (200 * 1024, 2)):
         for K in range(256, 32768 + 1, 256):
             for N in (1, 5, 100, 4096, 11008, 32000):
-                g = multi(K, N, ring)
+                g = multi(K, N, ring, 0, vm)
                 if not g["ok"]:
                     continue
                 checked += 1
@@ -232,10 +232,10 @@ def test_multi_token_pairs_reuse_buffers_in_order(multi):
     # every geometry, with the order derived from the barriers.
     assert _pair_order_safe(8, 1) and _pair_order_safe(8, 2) and not _pair_order_safe(8, 3)
     checked = 0
-    for T in (1, 2, 3, 4):
+    for T, vm in ((1, 1), (2, 1), (3, 1), (4, 1), (3, 2), (4, 2)):
         for K in range(256, 32768 + 1, 512):
             for N in (1, 5, 100, 4096, 11008, 32000):
-                g = multi(K, N, 200 * 1024, T)
+                g = multi(K, N, 200 * 1024, T, vm)
                 if not g["ok"]:
                     continue
                 checked += 1
@@ -272,3 +272,8 @@ def test_multi_token_x_staged_where_it_fits(multi):
     assert multi(4096, 4096, 200 * 1024, 8)["x_staged"] == 1
     assert multi(4096, 11008, 200 * 1024, 8)["x_staged"] == 1
     assert multi(11008, 4096, 200 * 1024, 8)["x_staged"] == 0
+    # The fused gate+up at 8 tokens on 4096 -> 11008: slots of both weights'
+    # rows (18.4 KB) leave no room for 128 KB of staged x beside seven of
+    # them, so x is loaded by the threads and every consumer warp has a slot.
+    g = multi(4096, 11008, 200 * 1024, 8, 2)
+    assert (g["nslots"], g["consumers"], g["x_staged"]) == (7, 7, 0) and g["smem"] <= SMEM
