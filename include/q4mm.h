@@ -349,7 +349,7 @@ int q4mm_device_status(q4mm_stream_t stream, int clear);
 /*
  * q4mm_test_fail_next_wait — a test hook for the library's failure
  * detection; the pages have no counterpart.  The calling thread's next call
- * of q4k_matmul (one-token and 2-8 token kernels), q4_0_gemv, q6k_gemv,
+ * of q4k_matmul (one-token and 3-8 token kernels), q4_0_gemv, q6k_gemv,
  * q4k_ffn_swiglu or q4k_matmul_tc never issues the copy of weight stage
  * `stage` of each CTA (its ring stage, or its 256-row weight tile on the
  * tensor cores) and bounds every in-kernel wait by `limit_cycles` SM cycles

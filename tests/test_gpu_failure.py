@@ -8,10 +8,11 @@ The wait is made to run out through the library's test hook
 weight stage and bounds its waits by about a millisecond.  Nothing is left
 in flight, nothing traps or waits without a bound.  Covered: the one-token
 kernel (a ring that holds every stage, and one that is reused), a Q6_K
-row format whose stages start off the 16-byte grid, the fused gate+up FFN,
-the 2-8 token kernel and the tensor-core prefill on canonical and relayouted
-weights and above 128 tokens (clusters of CTAs that still meet at their
-cluster barriers and release tensor memory).
+row format whose stages start off the 16-byte grid, the fused gate+up FFN
+(1, 4 and 8 tokens), the 3-8 token kernel (single warps and pairs) and the
+tensor-core prefill on canonical and relayouted weights and above 128
+tokens (clusters of CTAs that still meet at their cluster barriers and
+release tensor memory).
 """
 import time
 

@@ -5,7 +5,7 @@ gold dequantize-then-matmul reference), read per token row t as
 max_o |gpu − oracle| <= 1e-4 · max_o |oracle|.  Cases: the hand-worked block
 (exact), one-hot activations (element order), the workloads' shapes (full
 outputs where the oracle is quick, sampled rows at the largest sizes), an
-odd-shape sweep over the three kernels (1 token, 2–8 tokens, >8 tokens),
+odd-shape sweep over the kernels (1–2 tokens, 3–8 tokens, 8-token chunks and 64-token tiles above),
 ragged row counts, and run-to-run bit identity.
 """
 import numpy as np
@@ -123,7 +123,7 @@ def test_large_one_token_sampled(K, N):
 
 @pytest.mark.parametrize("K,N,T", [(14336, 4096, 8), (16384, 4096, 5), (13056, 4096, 3)])
 def test_multi_token_wide_rows_full(K, N, T):
-    # 2-8 token kernel with rows so wide that fewer ring slots than compute
+    # 3-8 token kernel with rows so wide that fewer ring slots than compute
     # warps fit in shared memory (13056 values and up), and more row groups
     # per CTA than slots, so every slot is reused: all outputs checked.
     x, W, K, N, T = synth.q4k_case((K, N, T), seed=K + T)

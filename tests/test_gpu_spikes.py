@@ -13,7 +13,7 @@ or the single element (q = 0 with m = 0) — at inputDim 4096 and 11008, and
 runs it through every route of the one-token kernel: Q4_K at 1 to 4 tokens
 (the spike in one token), Q4_0 (q = 8, or d = 0 for the block), Q6_K
 (q = 32, or a zero 16-value sub-block scale), the fused gate+up SwiGLU, and
-the ternary payload (code 0 at the spike), plus the FP32 2-8 token kernel.
+the ternary payload (code 0 at the spike), plus the FP32 3-8 token kernel.
 """
 import numpy as np
 import pytest

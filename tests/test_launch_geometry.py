@@ -1,4 +1,4 @@
-"""Launch geometry of the one-token and the 2-8 token GEMV kernels, checked
+"""Launch geometry of the one-token and the 3-8 token GEMV kernels, checked
 on the CPU.
 
 The library's own host headers (csrc/t1_geometry.h, csrc/multi_geometry.h)
