@@ -1,4 +1,4 @@
-"""CPU checks of two arithmetic recipes the CUDA kernels rely on, restated in
+"""CPU checks of three arithmetic recipes the CUDA kernels rely on, restated in
 numpy and compared with the oracle (no GPU; nothing here is shared with the
 kernels or the oracle).
 
@@ -24,6 +24,9 @@ kernels or the oracle).
    leaves every other group's representation unchanged.  Together with exact
    integer code-dots this keeps a row within 1e-4 of the oracle even when an
    activation of 1e5 sits on weights that are zero.
+
+3. FP32 register-tile GEMV (3-8 tokens), dequantized weight: one rounding of
+   the offset and one of the weight (see below), zero sub-blocks exactly zero.
 """
 import numpy as np
 
@@ -228,3 +231,89 @@ def test_one_token_split_spike_on_zero_weights_stays_within_1e_4():
             for kind in ("subblock", "element"):
                 err = _row_error_with_spike(K, spike, kind, seed=21)
                 assert err < 1e-5, (K, spike, kind, err)
+
+
+# 3. The FP32 register-tile kernel (3-8 tokens, the 8-token chunks above),
+#    dequantized weight.  Per sub-block s' = 256·d·sc (exact: an 11-bit
+#    mantissa times a 6-bit integer, scaled by a power of two) and
+#    o' = fma(dmin, m, s'/2) (one rounding); a code q becomes the float
+#    0.5 + q/256 (exact, built by one byte permute) and the weight is
+#    w' = fma(0.5 + q/256, s', −o') (one rounding).  So w' − w, with
+#    w = d·sc·q − dmin·m exact, is the rounding of o' plus the rounding of
+#    w', at most 2^-24·(|o'| + |w'|), and a sub-block whose scale and min are
+#    zero gives weights that are exactly zero.
+
+def _multi_recipe(d: F32, dmin: F32, sc: int, m: int, q: np.ndarray) -> np.ndarray:
+    s = F32(F32(256.0) * d) * F32(sc)                                       # exact
+    o = F32(np.float64(dmin) * np.float64(m) + 0.5 * np.float64(s))          # fma, one rounding
+    nib = (0.5 + q.astype(np.float64) / 256.0).astype(F32)                  # exact
+    return (nib.astype(np.float64) * np.float64(s) - np.float64(o)).astype(F32), o  # fma, one rounding
+
+
+def _multi_weights(W: np.ndarray, K: int, N: int):
+    """The recipe's weights and the per-weight bound 2^-24·(|o'| + |w'|)."""
+    blocks = W.reshape(N, K // 256, 144)
+    w = np.empty((N, K), F32)
+    bound = np.empty((N, K), np.float64)
+    for r in range(N):
+        for b in range(K // 256):
+            blk = blocks[r, b]
+            d, dmin, sc, m = _header_scales(blk)
+            qs = blk[16:144].astype(np.uint32)
+            for sub in range(8):
+                slab = qs[32 * (sub // 2):32 * (sub // 2) + 32]
+                q = slab & 15 if sub % 2 == 0 else slab >> 4
+                ws, o = _multi_recipe(d, dmin, int(sc[sub]), int(m[sub]), q)
+                k0 = 256 * b + 32 * sub
+                w[r, k0:k0 + 32] = ws
+                bound[r, k0:k0 + 32] = 2.0 ** -24 * (abs(np.float64(o)) + np.abs(ws.astype(np.float64)))
+    return w, bound
+
+
+def _exact_weights(W: np.ndarray, K: int, N: int) -> np.ndarray:
+    blocks = W.reshape(N, K // 256, 144)
+    w = np.empty((N, K), np.float64)
+    for r in range(N):
+        for b in range(K // 256):
+            d, dmin, sc, m = _header_scales(blocks[r, b])
+            qs = blocks[r, b, 16:144].astype(np.uint32)
+            for sub in range(8):
+                slab = qs[32 * (sub // 2):32 * (sub // 2) + 32]
+                q = (slab & 15 if sub % 2 == 0 else slab >> 4).astype(np.float64)
+                k0 = 256 * b + 32 * sub
+                w[r, k0:k0 + 32] = np.float64(d) * sc[sub] * q - np.float64(dmin) * m[sub]
+    return w
+
+
+def test_multi_dequant_recipe_within_two_roundings():
+    g = synth.rng(12)
+    K, N = 1024, 48
+    W = synth.q4k_weights(g, N, K)
+    w, bound = _multi_weights(W, K, N)
+    exact = _exact_weights(W, K, N)
+    # 2^-24·|w'| of slack for the double rounding of the fp64 emulation.
+    assert np.all(np.abs(w.astype(np.float64) - exact) <= bound + 2.0 ** -24 * np.abs(w.astype(np.float64)))
+    # The exact weight is also the oracle's (before its one fp32 rounding).
+    assert np.array_equal(exact.astype(F32), oracle.q4k_dequant(W, K, N))
+
+
+def test_multi_dequant_recipe_zero_sub_blocks_are_exactly_zero_and_rows_meet_1e_4():
+    # Sub-blocks with scale and min 0 (valid Q4_K) dequantize to exact zeros,
+    # so an activation of 1e5 there adds nothing; the recipe's rows stay
+    # within the 1e-4 contract of the oracle with such spikes.
+    g = synth.rng(13)
+    K, N = 1024, 32
+    W = synth.q4k_weights(g, N, K).reshape(N, K // 256, 144).copy()
+    q = [e % 16 for e in range(256)]
+    zero = oracle.q4k_pack_block(0x2E66, 0x2E66, [0] * 8, [0] * 8, q)
+    W[:, 1] = np.frombuffer(zero.tobytes(), np.uint8)
+    W = W.reshape(-1)
+    w, _ = _multi_weights(W, K, N)
+    assert np.all(w[:, 256:512] == 0)
+    x = synth.activations(g, 2, K).astype(np.float64)
+    x[:, 300] = 1e5
+    x[1, 511] = -1e5
+    y = x @ w.astype(np.float64).T
+    ref = oracle.q4k_matmul(x.astype(F32), W, K, N)
+    for t in range(2):
+        assert np.abs(y[t] - ref[t]).max() <= 1e-4 * np.abs(ref[t]).max()
