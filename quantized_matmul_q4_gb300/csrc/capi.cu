@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "q4mm.h"
+#include "dispatch.h"
 #include "kernels.h"
 #include "sync.cuh"
 
@@ -181,46 +182,25 @@ int q4k_matmul(const float *x, const void *w_q4k, float *y, int inputDim, int ou
     q4mm::LaunchCtx ctx;
     if ((rc = device_ctx(stream, &ctx))) return rc;
     const uint8_t *W = static_cast<const uint8_t *>(w_q4k);
-    cudaError_t e;
-    if (tokens == 1) {
-        e = q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim);
-        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, 1);
-    } else if (tokens <= 8) {
-        // 2 tokens: the byte-plane kernel with one token per compute warp
-        // where its geometry allows (measured on GB300: 7.4 against 7.7 us
-        // at 4096x4096, 13.5 against 17.5 us at 4096 -> 11008).  From 3
-        // tokens on the FP32 register-tile kernel is as fast or faster (4
-        // tokens: 9.3 against 12.6 us and 21.8 against 24.1 us), then the
-        // prefill kernel where neither fits.
-        e = tokens > 2
-                ? cudaErrorNotSupported
-                : q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim, tokens);
-        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
-        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
-    } else {
-        // More tokens: the 64-token FP32 tile kernel (clusters of 3 CTAs per
-        // 128 rows) computes a whole tile whatever the tokens, and with fewer
-        // CTAs than SMs (outputDim below about 6,500) leaves SMs idle.  Up to
-        // 32 tokens, or with that few CTAs, the register-tile kernel in
-        // chunks of 8 tokens is faster (measured on GB300: 4096x4096 at 16
-        // tokens 27 against 163 us, at 64 tokens 107 against 183 us;
-        // 4096 -> 11008 at 32 tokens 131 against 178 us, at 64 tokens 262
-        // against 198 us, where the tile kernel keeps 258 CTAs busy).
-        const long long tile_ctas = 3LL * ((outputDim + 127) / 128);
-        e = cudaErrorNotSupported;
-        if (tokens <= 32 || tile_ctas < ctx.num_sms) {
-            e = cudaSuccess;
-            for (int t0 = 0; t0 < tokens && e == cudaSuccess; t0 += 8) {
-                const int tt = tokens - t0 < 8 ? tokens - t0 : 8;
-                e = q4mm::launch_q4k_gemv_multi(ctx, x + (size_t)t0 * inputDim, W, y + (size_t)t0 * outputDim, inputDim,
-                                                outputDim, tt);
-                // A geometry the register-tile kernel cannot hold fails on
-                // the first chunk, before anything is launched.
-                if (e == cudaErrorNotSupported && t0 > 0) return fail_cuda(e, "q4k_matmul launch");
-            }
+    // The kernel for this token count (dispatch.h), each falling back to the
+    // next where its geometry does not fit the shape.
+    const q4mm::Q4kPath path = q4mm::q4k_matmul_path(tokens, outputDim, ctx.num_sms);
+    cudaError_t e = cudaErrorNotSupported;
+    if (path == q4mm::Q4kPath::kOneToken) e = q4mm::launch_q4k_gemv_t1(ctx, x, W, y, inputDim, outputDim, tokens);
+    if (e == cudaErrorNotSupported && tokens <= 8)
+        e = q4mm::launch_q4k_gemv_multi(ctx, x, W, y, inputDim, outputDim, tokens);
+    if (e == cudaErrorNotSupported && path == q4mm::Q4kPath::kTileChunks) {
+        e = cudaSuccess;
+        for (int t0 = 0; t0 < tokens && e == cudaSuccess; t0 += 8) {
+            const int tt = tokens - t0 < 8 ? tokens - t0 : 8;
+            e = q4mm::launch_q4k_gemv_multi(ctx, x + (size_t)t0 * inputDim, W, y + (size_t)t0 * outputDim, inputDim,
+                                            outputDim, tt);
+            // A geometry the register-tile kernel cannot hold fails on the
+            // first chunk, before anything is launched.
+            if (e == cudaErrorNotSupported && t0 > 0) return fail_cuda(e, "q4k_matmul launch");
         }
-        if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
     }
+    if (e == cudaErrorNotSupported) e = q4mm::launch_q4k_mm_fp32(ctx, x, W, y, inputDim, outputDim, tokens);
     if (e != cudaSuccess) return fail_cuda(e, "q4k_matmul launch");
     return Q4MM_OK;
 }

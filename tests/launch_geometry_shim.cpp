@@ -2,6 +2,7 @@
 // and the 2-8 token GEMV kernels (the library's own headers, default tuning)
 // through a C ABI.
 #include "../quantized_matmul_q4_gb300/csrc/multi_geometry.h"
+#include "../quantized_matmul_q4_gb300/csrc/dispatch.h"
 #include "../quantized_matmul_q4_gb300/csrc/t1_geometry.h"
 
 extern "C" int t1_plan(int group_bytes, int sums, int K, int N, int T, int vrow_mult, int num_sms, int max_smem,
@@ -24,4 +25,8 @@ extern "C" int multi_plan(int K, int N, int num_sms, int max_smem, int ring_byte
     const long long v[] = {g.ok, g.grid, g.rows_per_cta, g.nslots, g.consumers, (long long)g.smem, g.x_staged};
     for (int i = 0; i < (int)(sizeof(v) / sizeof(v[0])); ++i) out[i] = v[i];
     return g.ok;
+}
+
+extern "C" int q4k_path(int tokens, int outputDim, int num_sms) {
+    return (int)q4mm::q4k_matmul_path(tokens, outputDim, num_sms);
 }

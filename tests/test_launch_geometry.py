@@ -277,3 +277,18 @@ def test_multi_token_x_staged_where_it_fits(multi):
     # them, so x is loaded by the threads and every consumer warp has a slot.
     g = multi(4096, 11008, 200 * 1024, 8, 2)
     assert (g["nslots"], g["consumers"], g["x_staged"]) == (7, 7, 0) and g["smem"] <= SMEM
+
+
+def test_q4k_matmul_kernel_choice(tmp_path_factory):
+    # q4k_matmul's kernel per token count (csrc/dispatch.h): the byte-plane
+    # kernel for 1-2 tokens, the register-tile kernel for 3-8, its 8-token
+    # chunks up to 32 tokens or when 64-token tiles (3 CTAs per 128 rows)
+    # would leave SMs without a CTA, else the FP32 tile kernel.
+    lib = _shim(tmp_path_factory)
+    lib.q4k_path.argtypes = [ctypes.c_int] * 3
+    ONE, TILE, CHUNKS, FP32 = 0, 1, 2, 3
+    cases = [((1, 4096), ONE), ((2, 11008), ONE), ((3, 4096), TILE), ((8, 11008), TILE), ((9, 4096), CHUNKS),
+             ((32, 11008), CHUNKS), ((33, 11008), FP32), ((64, 11008), FP32), ((64, 4096), CHUNKS),
+             ((500, 4096), CHUNKS), ((64, 6400), CHUNKS), ((64, 6528), FP32), ((1000, 32000), FP32)]
+    for (T, N), want in cases:
+        assert lib.q4k_path(T, N, SMS) == want, (T, N)
