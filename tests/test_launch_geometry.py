@@ -277,6 +277,9 @@ def test_multi_token_x_staged_where_it_fits(multi):
     # them, so x is loaded by the threads and every consumer warp has a slot.
     g = multi(4096, 11008, 200 * 1024, 8, 2)
     assert (g["nslots"], g["consumers"], g["x_staged"]) == (7, 7, 0) and g["smem"] <= SMEM
+    # 32768-wide rows: two slots of both weights' rows (147 KB each) do not
+    # fit, so the fused FFN falls back to one-token launches.
+    assert multi(32768, 4096, 200 * 1024, 4, 2)["ok"] == 0 and multi(32768, 4096, 200 * 1024, 4, 1)["ok"] == 1
 
 
 def test_q4k_matmul_kernel_choice(tmp_path_factory):
