@@ -106,6 +106,15 @@ def test_workload_plans():
     assert t.weight_bytes == 6912 * 640 and t.flops == 2.0 * 2560 * 6912 * 16
     llama = bench.Plan(bench.WORKLOADS["llama7b_decode_t1"], 32)
     assert llama.weight_bytes == 32 * 113836032
+    # 16 tokens: two 8-token kernels per call, the weights counted once.
+    w16 = bench.WORKLOADS["llama7b_decode_t16"]
+    assert w16.kernels_per_call == 2 and bench.Plan(w16, 32).weight_bytes == llama.weight_bytes
+    assert bench.Plan(w16, 1).flops == 16 * bench.Plan(bench.WORKLOADS["llama7b_decode_t1"], 1).flops
+    # The fused gate+up at 8 tokens: both weights per call, one kernel.
+    ffn8 = bench.Plan(bench.WORKLOADS["llama7b_ffn_swiglu_t8"], 1)
+    assert ffn8.weight_bytes == 2 * 11008 * 16 * 144 and bench.WORKLOADS["llama7b_ffn_swiglu_t8"].kernels_per_call == 1
+    # Every other workload launches one kernel per call.
+    assert all(w.kernels_per_call == 1 for n, w in bench.WORKLOADS.items() if n != "llama7b_decode_t16")
 
 
 @pytest.mark.parametrize("workload", ["ternary_gemv_2560x6912_t16", "q4k_prefill_tc_4096x11008_t64"])
